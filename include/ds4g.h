@@ -1,0 +1,244 @@
+/*
+ * ds4g.h -- C ABI of libds4g: the routed mixture-of-experts expert layer over
+ * 2-bit quantized expert weights, as hand-written CUDA kernels for the
+ * NVIDIA B300 (sm_103a).
+ *
+ * What the layer is.  The ds4 README (codehub.bot mirror, section "Model
+ * Weights") states that only the routed MoE experts are quantized -- up/gate
+ * and down -- at 2 bits (IQ2_XXS for up/gate, Q2_K for down in the shipping
+ * mix), that these experts are the majority of the model's bytes, and that
+ * the GGUF quant layouts are those of llama.cpp (same page, section
+ * "Acknowledgements to llama.cpp and GGML").  The same page ("So, what can I
+ * do with this software?") names micro-batched decode and prefill on CUDA.
+ * For one layer call over T tokens this library computes:
+ *
+ *   1. top-k routing over the router logits (ds4g_route_topk);
+ *   2. per-expert token counts, segment offsets and the token-by-expert
+ *      permutation;
+ *   3. for every (token t, slot i), expert e = ids[t,i]:
+ *        g = W_gate[e] x_t,  u = W_up[e] x_t,  h = SiLU(g) * u,
+ *        o = W_down[e] h;
+ *   4. y_t = sum_{i<k} w[t,i] * o_{t,i}, summed in slot order.
+ *
+ * Formats (256-weight super-blocks, little-endian fp16 scalars):
+ *   Q2_K, 84 bytes:  scales[16] (low nibble = scale sc_s, high nibble = min
+ *     m_s of 16-weight sub-block s), qs[64] (2-bit quants), d, dmin.
+ *     Weight j: h = j/128, g = (j%128)/32, l = j%32,
+ *     q = (qs[32h + l] >> 2g) & 3, s = j/16,
+ *     w_j = d * (sc_s & 15) * q - dmin * (sc_s >> 4).
+ *   Codebook-2-bit ("CB2", IQ2_XXS-style), 70 bytes: idx[32] (codebook row
+ *     of weights 8o..8o+7), sgn[32] (bit b set: weight 8o+b negated), sc[4]
+ *     (4-bit scale of 32-weight group G in nibble G&1 of byte G>>1, low
+ *     nibble first), d.  w_j = d * s_{j/32} * cb[idx[j/8]][j%8] * (+-1);
+ *     cb is a 256 x 8 int8 codebook.
+ *   A matrix [N rows x K] is N rows of ceil(K/256) blocks; row n starts at
+ *   n * row_bytes; weights at columns >= K are ignored.
+ *
+ * Conventions for every entry point.
+ *   - Memory: every array argument is a DEVICE pointer owned by the caller,
+ *     except where an entry point says "host".  The library allocates no
+ *     device memory; scratch lives in the caller's workspace.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *     default stream).  Work is enqueued on it; no entry point synchronizes
+ *     except ds4g_moe_forward_host, which says so.
+ *   - Errors: a status is returned synchronously.  Arguments are validated on
+ *     the host before any launch; a rejected call launches nothing and leaves
+ *     every output untouched.  Launch failures map to DS4G_ERR_CUDA.
+ *     Faults inside a kernel surface at the caller's next synchronization.
+ *   - Threads: calls on distinct streams with distinct workspaces may run
+ *     concurrently.  The only library state is a per-device property cache.
+ *   - Determinism: identical inputs give bit-identical outputs; no result
+ *     depends on floating-point atomics or on launch timing.
+ */
+#ifndef DS4G_H
+#define DS4G_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DS4G_ABI_VERSION 1
+
+typedef enum ds4g_status {
+    DS4G_OK = 0,
+    DS4G_ERR_INVALID = 1,      /* null pointer, negative size, bad enum, k > E ... */
+    DS4G_ERR_SHAPE = 2,        /* a dimension outside the supported range         */
+    DS4G_ERR_LAYOUT = 3,       /* misaligned pointer or unusable row/expert stride */
+    DS4G_ERR_WORKSPACE = 4,    /* workspace pointer misaligned or too small        */
+    DS4G_ERR_UNSUPPORTED = 5,  /* a forced path that cannot run on these inputs    */
+    DS4G_ERR_CUDA = 6,         /* a CUDA runtime call or kernel launch failed      */
+    DS4G_ERR_TIMEOUT = 7       /* reserved: a bounded device-side wait expired     */
+} ds4g_status;
+
+typedef enum ds4g_score {
+    DS4G_SCORE_SOFTMAX = 0,    /* w_i = exp(l_i - l_max) / sum_j exp(l_j - l_max)  */
+    DS4G_SCORE_SIGMOID = 1     /* w_i = sigma(l_i) / sum_j sigma(l_j)              */
+} ds4g_score;
+
+typedef enum ds4g_format {
+    DS4G_FMT_Q2K = 0,          /* 84-byte Q2_K super-blocks                         */
+    DS4G_FMT_CB2 = 1           /* 70-byte codebook-2-bit super-blocks               */
+} ds4g_format;
+
+typedef enum ds4g_dtype {
+    DS4G_F32 = 0,
+    DS4G_F16 = 1,
+    DS4G_BF16 = 2
+} ds4g_dtype;
+
+/* ds4g_moe_desc.flags */
+enum {
+    DS4G_FORCE_GEMV = 1,       /* every expert segment on the decode (GEMV) kernels   */
+    DS4G_FORCE_TC = 2          /* every expert segment on the tensor-core kernels     */
+};
+
+/* Limits checked by the entry points. */
+#define DS4G_MAX_EXPERTS 256
+#define DS4G_MAX_TOPK 8
+#define DS4G_MAX_TOKENS 65536
+#define DS4G_MAX_HIDDEN 32768
+#define DS4G_MAX_INTER 32768
+
+/*
+ * One routed-MoE layer.  Weight tensors are expert-major: expert e of W_gate
+ * starts at w_gate + e * gate_up_expert_stride (bytes), and so on.
+ *   W_gate[e], W_up[e]: [inter rows x hidden], quantized along hidden.
+ *   W_down[e]:          [hidden rows x inter], quantized along inter
+ *                       (ceil(inter/256) blocks per row; columns >= inter
+ *                       are padding and are ignored).
+ * Requirements (else DS4G_ERR_SHAPE / DS4G_ERR_LAYOUT):
+ *   hidden % 256 == 0, 256 <= hidden <= DS4G_MAX_HIDDEN;
+ *   1 <= inter <= DS4G_MAX_INTER; 1 <= n_experts <= 256;
+ *   1 <= top_k <= min(8, n_experts);
+ *   row_bytes >= ceil(K/256) * block_bytes and a multiple of 2;
+ *   expert strides >= rows * row_bytes and multiples of 16;
+ *   w_gate, w_up, w_down 16-byte aligned;
+ *   DS4G_FORCE_TC additionally needs row_bytes % 16 == 0.
+ * tc_min_tokens: expert segments with at least this many tokens run on the
+ * tensor-core kernels, the others on the GEMV kernels (0 = library default).
+ */
+typedef struct ds4g_moe_desc {
+    int32_t hidden;
+    int32_t inter;
+    int32_t n_experts;
+    int32_t top_k;
+    int32_t score;             /* ds4g_score  */
+    int32_t format;            /* ds4g_format */
+    int32_t flags;
+    int32_t tc_min_tokens;
+    const void *w_gate;
+    const void *w_up;
+    const void *w_down;
+    int64_t gate_up_row_bytes;
+    int64_t down_row_bytes;
+    int64_t gate_up_expert_stride;
+    int64_t down_expert_stride;
+    const int8_t *codebook;    /* [256 x 8] int8, device; DS4G_FMT_CB2 only     */
+} ds4g_moe_desc;
+
+/*
+ * ds4g_route_topk -- steps 1 and 2 alone.
+ *   logits  [T x E] fp32, row-major.
+ *   ids     [T x k] int32 out: per token the k largest logits' expert ids in
+ *           rank order: larger logit first, equal logits -> lower id first,
+ *           a NaN logit ranks as -infinity.
+ *   weights [T x k] fp32 out: softmax over the k selected logits, or sigmoid
+ *           of each selected logit divided by their sum (`score`).
+ *   counts  [E] int32 out (nullable): assignments per expert.
+ *   offsets [E+1] int32 out (nullable): exclusive prefix sum of counts.
+ *   perm    [T*k] int32 out (nullable): assignment indices a = t*k + i grouped
+ *           by expert (segment e = perm[offsets[e] .. offsets[e+1]-1]),
+ *           ascending t inside each segment.
+ * Errors: DS4G_ERR_INVALID (null ids/weights/logits, T < 0, E < 1, E > 256,
+ * k < 1, k > min(8, E), bad score); DS4G_ERR_SHAPE (T > DS4G_MAX_TOKENS);
+ * DS4G_ERR_CUDA.  T == 0 is a no-op (counts/offsets still written as zero).
+ */
+ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, int32_t k,
+                            int32_t score, int32_t *ids, float *weights,
+                            int32_t *counts, int32_t *offsets, int32_t *perm,
+                            void *stream);
+
+/*
+ * ds4g_q2k_dequant -- n_blocks consecutive Q2_K super-blocks (84 bytes each,
+ * `blocks` 4-byte aligned) to n_blocks * 256 values of out_dtype in `out`
+ * (16-byte aligned).  fp32 output is exactly the block definition above
+ * (both products are exact; one rounding in the subtraction); fp16 / bf16
+ * output is that fp32 value rounded to nearest even.
+ * Errors: DS4G_ERR_INVALID (null pointer, n_blocks < 0, bad dtype);
+ * DS4G_ERR_LAYOUT (alignment); DS4G_ERR_CUDA.  n_blocks == 0 is a no-op.
+ */
+ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out,
+                             int32_t out_dtype, void *stream);
+
+/*
+ * ds4g_cb2_dequant -- n_blocks consecutive codebook-2-bit super-blocks (70
+ * bytes each, `blocks` 2-byte aligned) with a [256 x 8] int8 device codebook
+ * to n_blocks * 256 values of out_dtype (16-byte aligned).  fp32 output is
+ * exact; fp16 / bf16 output is the fp32 value rounded to nearest even.
+ * Errors as ds4g_q2k_dequant, plus DS4G_ERR_INVALID for a null codebook.
+ */
+ds4g_status ds4g_cb2_dequant(const void *blocks, int64_t n_blocks, const int8_t *codebook,
+                             void *out, int32_t out_dtype, void *stream);
+
+/*
+ * ds4g_moe_workspace_bytes -- bytes of device workspace ds4g_moe_forward
+ * (and ds4g_moe_forward_host) need for this layer and T tokens; 0 when the
+ * descriptor or T is invalid.  The workspace must be 256-byte aligned.
+ */
+size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
+
+/*
+ * ds4g_moe_forward -- the whole layer, steps 1-4.
+ *   x       [T x hidden] bf16 (uint16 bits), 16-byte aligned.
+ *   logits  [T x n_experts] fp32, 4-byte aligned.
+ *   y       [T x hidden] fp32 out, 16-byte aligned; overwritten.
+ *   workspace / ws_bytes: device scratch of at least
+ *           ds4g_moe_workspace_bytes(desc, T) bytes, 256-byte aligned.  After
+ *           the call it holds the routing of this call (see
+ *           ds4g_moe_routing_view).
+ * Errors: DS4G_ERR_INVALID, DS4G_ERR_SHAPE, DS4G_ERR_LAYOUT,
+ * DS4G_ERR_WORKSPACE, DS4G_ERR_UNSUPPORTED (a forced path that cannot run),
+ * DS4G_ERR_CUDA.  T == 0 is a no-op.
+ */
+ds4g_status ds4g_moe_forward(const ds4g_moe_desc *desc, const uint16_t *x,
+                             const float *logits, int32_t T, float *y,
+                             void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * ds4g_moe_forward_host -- ds4g_moe_forward with HOST activations, logits
+ * and output (weights stay on the device, in desc).  Copies x and logits to
+ * the workspace, runs the layer, copies y back and synchronizes `stream`
+ * before returning.  Host buffers should be pinned (cudaHostAlloc) for full
+ * copy bandwidth; pageable memory works but is slower.
+ * Errors: as ds4g_moe_forward.
+ */
+ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint16_t *x_host,
+                                  const float *logits_host, int32_t T, float *y_host,
+                                  void *workspace, size_t ws_bytes, void *stream);
+
+/*
+ * ds4g_moe_routing_view -- device pointers, inside a workspace last used by
+ * ds4g_moe_forward(desc, ..., T, ...), to that call's routing results:
+ * ids [T x k] int32, weights [T x k] fp32, counts [E] int32,
+ * offsets [E+1] int32, perm [T*k] int32 (same meaning as ds4g_route_topk).
+ * Any output pointer may be NULL.  Pure host arithmetic; launches nothing.
+ * Errors: DS4G_ERR_INVALID, DS4G_ERR_WORKSPACE.
+ */
+ds4g_status ds4g_moe_routing_view(const ds4g_moe_desc *desc, int32_t T, void *workspace,
+                                  size_t ws_bytes, int32_t **ids, float **weights,
+                                  int32_t **counts, int32_t **offsets, int32_t **perm);
+
+/* Static text for a status code ("ok", "invalid argument", ...). */
+const char *ds4g_status_string(ds4g_status status);
+
+/* DS4G_ABI_VERSION of the loaded library. */
+int32_t ds4g_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4G_H */

@@ -1,0 +1,87 @@
+"""Planted mistakes: each mutant is a copy of the oracle source with one
+plausible error (a dropped term, a wrong shift, index or sign, a swapped
+operand, a wrong tie-break ...), compiled on the CPU into a temporary
+library.  Every mutant must fail at least one pin; otherwise the pins would
+not notice that mistake in the real oracle."""
+import os
+import shutil
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+MUTANTS = {
+    "drop_min_term": [("w[j] = value - min_part;", "w[j] = value;")],
+    "swap_scale_min_nibbles": [("int sc = scales[j / 16];",
+                                "int sc = ((scales[j / 16] & 15) << 4) | (scales[j / 16] >> 4);")],
+    "shift_g_not_2g": [("(qs[32 * h + l] >> (2 * g)) & 3", "(qs[32 * h + l] >> g) & 3")],
+    "qs_half_stride_16": [("(qs[32 * h + l] >> (2 * g)) & 3", "(qs[16 * h + l] >> (2 * g)) & 3")],
+    "subblock_of_32": [("int sc = scales[j / 16];", "int sc = scales[j / 32];")],
+    "half_exponent_bias": [("v = ldexp((double)(1024 + frac), expo - 25);",
+                            "v = ldexp((double)(1024 + frac), expo - 24);")],
+    "bf16_shift": [("uint32_t u = (uint32_t)b << 16;", "uint32_t u = (uint32_t)b << 15;")],
+    "cb2_nibble_order": [("(sc[group / 2] >> (4 * (group % 2))) & 15",
+                          "(sc[group / 2] >> (4 * (1 - group % 2))) & 15")],
+    "cb2_ignore_sign": [("w[j] = negate ? -value : value;", "w[j] = value;")],
+    "cb2_reversed_entry": [("codebook[8 * idx[o] + b]", "codebook[8 * idx[o] + (7 - b)]")],
+    "cb2_group_of_64": [("int group = j / 32;", "int group = j / 64;")],
+    "tie_break_higher_id": [("return ia < ib;", "return ia > ib;")],
+    "nan_ranks_first": [("(l != l) ? -INFINITY", "(l != l) ? INFINITY")],
+    "softmax_no_shift": [("w[i] = exp(rank_value(lg[ids[i]]) - lmax);",
+                          "w[i] = exp(rank_value(lg[ids[i]]) - lmax + 0.5 * (i > 0));")],
+    "sigmoid_sign": [("w[i] = 1.0 / (1.0 + exp(-rank_value(lg[ids[i]])));",
+                      "w[i] = 1.0 / (1.0 + exp(rank_value(lg[ids[i]])));")],
+    "offsets_inclusive": [("offsets[e] = run;\n            run += c;",
+                           "run += c;\n            offsets[e] = run;")],
+    "perm_slot_major": [("for (int t = 0; t < T; ++t)\n                for (int i = 0; i < k; ++i)\n"
+                         "                    if (ids[(int64_t)t * k + i] == e) perm[pos++] = t * k + i;",
+                         "for (int i = 0; i < k; ++i)\n                for (int t = 0; t < T; ++t)\n"
+                         "                    if (ids[(int64_t)t * k + i] == e) perm[pos++] = t * k + i;")],
+    "silu_sign": [("h[n] = g / (1.0 + exp(-g)) * u;", "h[n] = g / (1.0 + exp(g)) * u;")],
+    "gate_up_swapped": [("h[n] = g / (1.0 + exp(-g)) * u;", "h[n] = u / (1.0 + exp(-u)) * g;")],
+    "down_reversed_h": [("acc += (double)rowbuf[n] * h[n];", "acc += (double)rowbuf[n] * h[I - 1 - n];")],
+    "combine_wrong_slot_weight": [("yt[m] += w[i] * o[m];", "yt[m] += w[k - 1 - i] * o[m];")],
+    "row_blocks_not_advanced": [("orc_q2k_dequant_block(row + (int64_t)b * ORC_Q2K_BYTES, out + b * ORC_QK);",
+                                 "orc_q2k_dequant_block(row, out + b * ORC_QK);")],
+    "up_reads_gate": [("dequant_row(L, wu + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);",
+                       "dequant_row(L, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);")],
+}
+
+
+@pytest.fixture(scope="module")
+def mutant_dir():
+    d = tempfile.mkdtemp(prefix="ds4g_mutants_")
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
+def test_mutant_patterns_exist():
+    src = open(oracle.SOURCE).read()
+    for name, edits in MUTANTS.items():
+        for old, _ in edits:
+            assert src.count(old) >= 1, (name, old)
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, mutant_dir):
+    src = open(oracle.SOURCE).read()
+    for old, new in MUTANTS[name]:
+        src = src.replace(old, new, 1)
+    path = os.path.join(mutant_dir, name + ".c")
+    with open(path, "w") as f:
+        f.write(src)
+    lib = oracle.build(path, os.path.join(mutant_dir, name + ".so"))
+    orc = oracle.Oracle(lib)
+    failures = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(orc)
+        except AssertionError:
+            failures.append(pin.__name__)
+        except (ValueError, FloatingPointError, IndexError):
+            failures.append(pin.__name__)
+        if failures:
+            break
+    assert failures, f"planted mistake {name!r} passed every pin"
