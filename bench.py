@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed-MoE expert layer over 2-bit quantized experts.
+
+One step = one call of the whole layer (routing, counts/offsets/permutation,
+fused dequant gate/up + SiLU, down projection, weighted combine) over one
+batch of synthetic tokens.  The default workload is single-token decode:
+hidden 4096, expert intermediate 1536, 64 Q2_K experts, top-6, 1 token per
+step (the bandwidth-bound GEMV path).  Other workloads: --config NAME.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
+  python bench.py --impl reference ...     # the CPU oracle, timed as it stands
+
+Timing: W eager warm-up steps, then K steps replayed from CUDA graphs,
+bracketed by a barrier and torch.cuda.synchronize() on both sides, timed
+with CUDA events on the launching stream; max over ranks.  Each step uses
+another batch of tokens and another of R copies of the expert weights, with
+R * (bytes touched per step) >= 4 x L2, so that weights stream from HBM.
+Per-kernel durations come from CUDA events recorded between the layer's
+kernels inside the same graphs.  Under torchrun every rank runs its own
+replica of the workload (the layer does not shard here): scaling "weak".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import ds4g_synth as S  # noqa: E402
+
+METRIC = "routed-MoE layer tokens/s; effective HBM GB/s (decode) & tensor util (prefill)"
+L2_BYTES = 126 * 1024 * 1024
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6400.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="ds4g", choices=["ds4g", "reference"])
+    ap.add_argument("--config", default="decode_1tok", choices=list(S.CONFIGS))
+    ap.add_argument("--copies", type=int, default=0, help="weight copies (0 = auto)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def default_steps(cfg: S.Config):
+    # ~1-2 s of device time at the expected step times
+    return {"tiny": 20000, "decode_1tok": 100000, "decode_32tok": 4000,
+            "prefill_2048": 200, "codebook_512": 1000}[cfg.name]
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing
+# ---------------------------------------------------------------------------
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join("/tmp", f"ds4g_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------
+
+def peaks():
+    try:
+        p = json.load(open(PEAKS_FILE))
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "bit_quantized_routed_route_b300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def measured_traffic(kernel: str, workload: str):
+    """dram bytes per launch from the committed ncu summary, when it was taken
+    on the current kernel sources; else None."""
+    try:
+        t = json.load(open(TRAFFIC_FILE))
+        e = t[workload][kernel]
+        if e.get("source_hash") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        pass
+    return None
+
+
+def layer_bytes(cfg: S.Config):
+    """Logical quantized bytes of one expert's matrices."""
+    bb = cfg.block_bytes
+    gu = cfg.inter * (cfg.hidden // 256) * bb                 # one of gate / up
+    dn = cfg.hidden * (-(-cfg.inter // 256)) * bb
+    return gu, dn
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_tokens_per_s(layer, budget_s: float, max_tokens: int):
+    """Times the oracle, single-threaded as it stands, on consecutive tokens of
+    the workload until `budget_s` of CPU time or `max_tokens` tokens."""
+    import oracle
+    orc = oracle.get()
+    T = layer["x"].shape[0]
+    done, t0 = 0, time.perf_counter()
+    while done < max_tokens and (time.perf_counter() - t0) < budget_s:
+        tok = np.array([done % T], dtype=np.int32)
+        orc.moe_forward(layer, layer["x"], layer["logits"], tok)
+        done += 1
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+def reference_arm(args, cfg, rank, world):
+    if rank != 0:
+        return 0
+    K = args.steps if args.steps is not None else 20
+    W = args.warmup if args.warmup is not None else 3
+    layer = S.make_layer(cfg, tokens=min(cfg.tokens, 64))
+    import oracle
+    orc = oracle.get()
+    T = layer["x"].shape[0]
+    for i in range(W):
+        orc.moe_forward(layer, layer["x"], layer["logits"], np.array([i % T], dtype=np.int32))
+    # one step = one token of the workload; bounded to ~150 s of CPU work
+    t0 = time.perf_counter()
+    done = 0
+    while done < K and (done == 0 or (time.perf_counter() - t0) / done * (done + 1) < 150.0):
+        orc.moe_forward(layer, layer["x"], layer["logits"], np.array([done % T], dtype=np.int32))
+        done += 1
+    dt = time.perf_counter() - t0
+    val = done / dt
+    sample = (f"{done} of {K} requested steps, one token of {cfg.name} each "
+              f"(steps capped at ~150 s of CPU work)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s",
+        "n_gpus": world, "steps": done, "warmup": W, "ms_per_step": 1000.0 * dt / done,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(cfg, 0, "oracle"),
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(cfg: S.Config, copies: int, l2_note: str):
+    fmt = "Q2_K" if cfg.format == S.FMT_Q2K else "codebook-2bit"
+    return {"workload": f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.n_experts} "
+                        f"top-{cfg.top_k} T={cfg.tokens} {fmt}",
+            "hidden": cfg.hidden, "inter": cfg.inter, "experts": cfg.n_experts,
+            "top_k": cfg.top_k, "tokens_per_step": cfg.tokens, "weights": fmt,
+            "weight_copies": copies, "l2": l2_note, "parallelism": "replicas"}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    cfg = S.CONFIGS[args.config]
+    rank, world, local = dist_setup(args)
+    if args.impl == "reference":
+        return reference_arm(args, cfg, rank, world)
+
+    import bit_quantized_routed_route_b300 as D
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    dev = torch.device("cuda")
+    K = args.steps if args.steps is not None else default_steps(cfg)
+    W = max(3, args.warmup if args.warmup is not None else 10)
+
+    # --- inputs ------------------------------------------------------------
+    layer = S.make_layer(cfg)
+    gu_b, dn_b = layer_bytes(cfg)
+    T, H, E, k = cfg.tokens, cfg.hidden, cfg.n_experts, cfg.top_k
+    x_b, l_b, y_b = T * H * 2, T * E * 4, T * H * 4
+    batch_bytes = x_b + l_b
+    P = int(max(1, min(256, (64 << 20) // batch_bytes)))
+    xs, ls = [layer["x"]], [layer["logits"]]
+    for b in range(1, P):
+        tk = S.make_tokens(cfg, T, seed=cfg.seed * 100003 + b)
+        xs.append(tk["x"])
+        ls.append(tk["logits"])
+    x_all = np.stack(xs)
+    l_all = np.stack(ls)
+
+    # routing of every batch, computed by the library (untimed), for the
+    # algorithmic byte counts
+    ids_all = []
+    for b in range(P):
+        lg = torch.from_numpy(l_all[b]).to(dev)
+        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+        w = torch.empty((T, k), dtype=torch.float32, device=dev)
+        D.check(D.route_topk(lg, T, E, k, cfg.score, ids, w))
+        ids_all.append(ids.cpu().numpy())
+    active = np.array([len(np.unique(i)) for i in ids_all], dtype=np.float64)
+    touched = active * (2 * gu_b + dn_b)
+    copies = args.copies or int(max(2, min(64, -(-4 * L2_BYTES // max(1, int(touched.min()))))))
+    per_copy = (gu_b * 2 + dn_b) * E
+    if copies * per_copy > 0.5 * torch.cuda.get_device_properties(dev).total_memory:
+        copies = max(1, int(0.5 * torch.cuda.get_device_properties(dev).total_memory // per_copy))
+
+    w_dev = []
+    base = {n: torch.from_numpy(layer[n]).to(dev) for n in ("w_gate", "w_up", "w_down")}
+    cb = None if layer["codebook"] is None else torch.from_numpy(layer["codebook"]).to(dev)
+    for c in range(copies):
+        t = base if c == 0 else {n: v.clone() for n, v in base.items()}
+        w_dev.append(D.Layer(H, cfg.inter, E, k, cfg.score, cfg.format, t["w_gate"], t["w_up"],
+                             t["w_down"], cb))
+    x_dev = torch.from_numpy(x_all.view(np.int16)).to(dev)
+    l_dev = torch.from_numpy(l_all).to(dev)
+    y_dev = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws_bytes = w_dev[0].workspace_bytes(T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    launches_per_step = D.moe_forward_launches(w_dev[0].desc, T)
+
+    stream = torch.cuda.Stream()
+    torch.cuda.synchronize()
+
+    def step(s, st, events=None):
+        L = w_dev[s % copies]
+        b = s % P
+        if events is None:
+            D.check(D.moe_forward(L.desc, x_dev[b], l_dev[b], T, y_dev, ws, ws_bytes, stream=st))
+        else:
+            D.check(D.moe_forward_phased(L.desc, x_dev[b], l_dev[b], T, y_dev, ws, events,
+                                         ws_bytes, stream=st))
+
+    # --- warm-up (eager) -----------------------------------------------------
+    with torch.cuda.stream(stream):
+        for s in range(W):
+            step(s, stream)
+    stream.synchronize()
+
+    # --- graphs: G steps each, with phase events -----------------------------
+    G = min(K, 500 if T <= 64 else 20)
+    n_full, rem = divmod(K, G)
+
+    def capture(n_steps, first):
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_steps)]
+        for row in evs:
+            for e in row:
+                e.record(stream)          # materialise the cudaEvent_t handles
+        stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(n_steps):
+                step(first + j, stream, [e.cuda_event for e in evs[j]])
+        return g, evs
+
+    g_main, ev_main = capture(G, 0)
+    g_rem, ev_rem = capture(rem, 0) if rem else (None, None)
+    # one untimed replay of each graph
+    g_main.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.25)
+    start.record(stream)
+    for _ in range(n_full):
+        g_main.replay()
+    if g_rem is not None:
+        g_rem.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop()
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world)
+
+    tokens = K * T * world
+    value = tokens / (elapsed_ms / 1000.0)
+    ms_per_step = elapsed_ms / K
+
+    # per-phase durations over the last replay of the main graph
+    ph = np.array([[ev_main[j][i].elapsed_time(ev_main[j][i + 1]) for i in range(4)]
+                   for j in range(G)])
+    ph_ms = ph.mean(axis=0)                        # route, gateup, down, combine
+    # algorithmic bytes per launch of the dominant (gate/up) kernel, averaged
+    # over the steps of the graph: gate + up bytes of the active experts,
+    # x read, h written (fp32, padded rows)
+    steps_b = np.arange(G) % P
+    act = active[steps_b]
+    i_pad = -(-cfg.inter // 256) * 256
+    gate_up_bytes = float(np.mean(act * 2 * gu_b)) + x_b + T * k * i_pad * 4
+    down_bytes = float(np.mean(act * dn_b)) + T * k * i_pad * 4 + T * k * H * 4
+    step_bytes = float(np.mean(touched[steps_b])) + x_b + l_b + y_b
+    hbm_peak, peak_kind = peaks()
+    achieved = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9
+    traffic = measured_traffic("gateup", cfg.name)
+
+    # --- end to end through the host entry point ------------------------------
+    e2e = None
+    if not args.no_e2e:
+        xh = torch.from_numpy(x_all.view(np.int16)).pin_memory()
+        lh = torch.from_numpy(l_all).pin_memory()
+        yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
+        ws2 = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+        K2 = min(K, max(50, int(2000 * 64 / max(1, T))))
+        for s in range(W):
+            D.check(D.moe_forward_host(w_dev[s % copies].desc, xh[s % P], lh[s % P], T, yh, ws2,
+                                       ws_bytes, stream=stream))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for s in range(K2):
+            D.check(D.moe_forward_host(w_dev[s % copies].desc, xh[s % P], lh[s % P], T, yh, ws2,
+                                       ws_bytes, stream=stream))
+        torch.cuda.synchronize()
+        barrier(world)
+        dt = max_over_ranks(time.perf_counter() - t0, world)
+        e2e = {"value": K2 * T * world / dt, "unit": "tokens/s", "h2d_bytes_per_step": x_b + l_b,
+               "d2h_bytes_per_step": y_b, "steps": K2}
+
+    # --- CPU baseline (rank 0, one GPU) --------------------------------------
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        small = S.make_layer(cfg, tokens=min(T, 64)) if T > 64 else layer
+        v, n, dt = oracle_tokens_per_s(small, budget_s=15.0, max_tokens=10_000)
+        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"{n} tokens of {cfg.name} through the single-threaded fp64 oracle "
+                         f"in {dt:.1f} s"}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": workload_config(cfg, copies,
+                                  f"inputs larger than L2: {copies} rotating weight copies, "
+                                  f"{touched.mean() / 1e6:.1f} MB touched per step"),
+        "roofline": {"bound": "hbm", "kernel": "gateup", "achieved": achieved, "peak": hbm_peak,
+                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": traffic, "algorithmic_bytes": gate_up_bytes,
+                     "duration_us": ph_ms[1] * 1000.0},
+        "effective_hbm": {"step_bytes": step_bytes,
+                          "gbs": step_bytes / (ms_per_step / 1000.0) / 1e9,
+                          "frac_of_measured": step_bytes / (ms_per_step / 1000.0) / 1e9 / hbm_peak,
+                          "frac_of_8tbs": step_bytes / (ms_per_step / 1000.0) / 1e9 / NOMINAL_HBM_GBS},
+        "phases_us": {"route": ph_ms[0] * 1e3, "gateup": ph_ms[1] * 1e3, "down": ph_ms[2] * 1e3,
+                      "combine": ph_ms[3] * 1e3},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,350 @@
+// ds4g_api.cu -- the C ABI of libds4g: argument validation, the workspace
+// plan and the launch sequence of one routed-MoE layer call.  Every entry
+// point validates on the host before launching anything and returns a
+// ds4g_status; no entry point allocates device memory.
+#include <mutex>
+
+#include "ds4g_common.cuh"
+
+namespace ds4g {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+ds4g_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DS4G_OK : DS4G_ERR_CUDA; }
+
+std::mutex g_dev_mu;
+DeviceInfo g_dev[64];
+bool g_dev_ok[64];
+
+}  // namespace
+
+ds4g_status device_info(DeviceInfo *out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DS4G_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!g_dev_ok[dev]) {
+        DeviceInfo info{};
+        if (cudaDeviceGetAttribute(&info.sm_count, cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess ||
+            cudaDeviceGetAttribute(&info.max_smem_optin,
+                                   cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return DS4G_ERR_CUDA;
+        g_dev[dev] = info;
+        g_dev_ok[dev] = true;
+    }
+    *out = g_dev[dev];
+    return DS4G_OK;
+}
+
+ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
+{
+    if (!d || !p) return DS4G_ERR_INVALID;
+    if (T < 0) return DS4G_ERR_INVALID;
+    if (d->n_experts < 1 || d->n_experts > DS4G_MAX_EXPERTS) return DS4G_ERR_INVALID;
+    if (d->top_k < 1 || d->top_k > DS4G_MAX_TOPK || d->top_k > d->n_experts)
+        return DS4G_ERR_INVALID;
+    if (d->score != DS4G_SCORE_SOFTMAX && d->score != DS4G_SCORE_SIGMOID) return DS4G_ERR_INVALID;
+    if (d->format != DS4G_FMT_Q2K && d->format != DS4G_FMT_CB2) return DS4G_ERR_INVALID;
+    if ((d->flags & ~(DS4G_FORCE_GEMV | DS4G_FORCE_TC)) != 0) return DS4G_ERR_INVALID;
+    if ((d->flags & DS4G_FORCE_GEMV) && (d->flags & DS4G_FORCE_TC)) return DS4G_ERR_INVALID;
+    if (d->tc_min_tokens < 0) return DS4G_ERR_INVALID;
+    if (!d->w_gate || !d->w_up || !d->w_down) return DS4G_ERR_INVALID;
+    if (d->format == DS4G_FMT_CB2 && !d->codebook) return DS4G_ERR_INVALID;
+    if (T > DS4G_MAX_TOKENS) return DS4G_ERR_SHAPE;
+    if (d->hidden < kQK || d->hidden > DS4G_MAX_HIDDEN || d->hidden % kQK != 0)
+        return DS4G_ERR_SHAPE;
+    if (d->inter < 1 || d->inter > DS4G_MAX_INTER) return DS4G_ERR_SHAPE;
+
+    Plan q{};
+    q.T = T;
+    q.H = d->hidden;
+    q.I = d->inter;
+    q.E = d->n_experts;
+    q.k = d->top_k;
+    q.A = T * d->top_k;
+    q.I_pad = (d->inter + kQK - 1) / kQK * kQK;
+    q.H_blocks = d->hidden / kQK;
+    q.I_blocks = q.I_pad / kQK;
+    q.block_bytes = d->format == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+
+    const int64_t gu_logical = (int64_t)q.H_blocks * q.block_bytes;
+    const int64_t dn_logical = (int64_t)q.I_blocks * q.block_bytes;
+    const int64_t row_mult = d->format == DS4G_FMT_Q2K ? 4 : 2;
+    if (d->gate_up_row_bytes < gu_logical || d->down_row_bytes < dn_logical)
+        return DS4G_ERR_LAYOUT;
+    if (d->gate_up_row_bytes % row_mult || d->down_row_bytes % row_mult) return DS4G_ERR_LAYOUT;
+    if (d->gate_up_expert_stride < (int64_t)q.I * d->gate_up_row_bytes ||
+        d->down_expert_stride < (int64_t)q.H * d->down_row_bytes)
+        return DS4G_ERR_LAYOUT;
+    if (d->gate_up_expert_stride % 16 || d->down_expert_stride % 16) return DS4G_ERR_LAYOUT;
+    if (!aligned(d->w_gate, 16) || !aligned(d->w_up, 16) || !aligned(d->w_down, 16))
+        return DS4G_ERR_LAYOUT;
+    if ((d->flags & DS4G_FORCE_TC) &&
+        (d->gate_up_row_bytes % 16 != 0 || d->down_row_bytes % 16 != 0))
+        return DS4G_ERR_LAYOUT;
+
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t at = off;
+        off = align_up(off + bytes);
+        return at;
+    };
+    const size_t A = (size_t)q.A;
+    q.ids = take(A * 4);
+    q.wts = take(A * 4);
+    q.counts = take((size_t)q.E * 4);
+    q.offsets = take((size_t)(q.E + 1) * 4);
+    q.perm = take(A * 4);
+    q.slot_pos = take(A * 4);
+    q.active = take((size_t)q.E * 4);
+    q.meta = take(kMetaWords * 4);
+    q.hbuf = take(A * q.I_pad * 4);
+    q.yslot = take(A * q.H * 4);
+    q.x_stage = take((size_t)T * q.H * 2);
+    q.l_stage = take((size_t)T * q.E * 4);
+    q.y_stage = take((size_t)T * q.H * 4);
+    q.total = off;
+    *p = q;
+    return DS4G_OK;
+}
+
+namespace {
+
+// Records events[i] (when given) at the phase boundaries of one forward.
+struct PhaseEvents {
+    cudaEvent_t ev[5];
+    bool on;
+    cudaError_t mark(int i, cudaStream_t s) const
+    {
+        return on ? record_phase(ev[i], s) : cudaSuccess;
+    }
+};
+
+ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *x,
+                         const float *logits, float *y, uint8_t *ws, cudaStream_t s,
+                         const PhaseEvents &pe)
+{
+    DeviceInfo dev;
+    ds4g_status st = device_info(&dev);
+    if (st != DS4G_OK) return st;
+    int32_t *ids = reinterpret_cast<int32_t *>(ws + p.ids);
+    float *wts = reinterpret_cast<float *>(ws + p.wts);
+    int32_t *counts = reinterpret_cast<int32_t *>(ws + p.counts);
+    int32_t *offsets = reinterpret_cast<int32_t *>(ws + p.offsets);
+    int32_t *perm = reinterpret_cast<int32_t *>(ws + p.perm);
+    int32_t *slot_pos = reinterpret_cast<int32_t *>(ws + p.slot_pos);
+    int32_t *active = reinterpret_cast<int32_t *>(ws + p.active);
+    int32_t *meta = reinterpret_cast<int32_t *>(ws + p.meta);
+    if (pe.mark(0, s) != cudaSuccess) return DS4G_ERR_CUDA;
+    cudaError_t e = launch_route(logits, p.T, p.E, p.k, d->score, ids, wts, counts, offsets, perm,
+                                 slot_pos, active, meta + kMetaActive, s);
+    if (e != cudaSuccess) return DS4G_ERR_CUDA;
+    if (pe.mark(1, s) != cudaSuccess) return DS4G_ERR_CUDA;
+    LayerArgs a{};
+    a.H = p.H;
+    a.I = p.I;
+    a.I_pad = p.I_pad;
+    a.E = p.E;
+    a.k = p.k;
+    a.A = p.A;
+    a.T = p.T;
+    a.format = d->format;
+    a.w_gate = static_cast<const uint8_t *>(d->w_gate);
+    a.w_up = static_cast<const uint8_t *>(d->w_up);
+    a.w_down = static_cast<const uint8_t *>(d->w_down);
+    a.gu_row = d->gate_up_row_bytes;
+    a.dn_row = d->down_row_bytes;
+    a.gu_stride = d->gate_up_expert_stride;
+    a.dn_stride = d->down_expert_stride;
+    a.codebook = d->codebook;
+    a.x = x;
+    a.wts = wts;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.perm = perm;
+    a.slot_pos = slot_pos;
+    a.active = active;
+    a.n_active = meta + kMetaActive;
+    a.hbuf = reinterpret_cast<float *>(ws + p.hbuf);
+    a.yslot = reinterpret_cast<float *>(ws + p.yslot);
+    a.y = y;
+    return from_cuda(launch_gemv_path(a, dev, s, pe.on ? pe.ev : nullptr));
+}
+
+int32_t route_launches(int32_t T) { return T <= kRouteSmallT ? 1 : 2; }
+
+ds4g_status check_forward_args(const ds4g_moe_desc *d, const void *x, const void *logits,
+                               const void *y, void *ws, size_t ws_bytes, int32_t T, Plan *p)
+{
+    ds4g_status st = make_plan(d, T, p);
+    if (st != DS4G_OK) return st;
+    if (T == 0) return DS4G_OK;
+    if (!x || !logits || !y || !ws) return DS4G_ERR_INVALID;
+    if (!aligned(ws, kAlign)) return DS4G_ERR_WORKSPACE;
+    if (ws_bytes < p->total) return DS4G_ERR_WORKSPACE;
+    return DS4G_OK;
+}
+
+}  // namespace
+}  // namespace ds4g
+
+using namespace ds4g;
+
+extern "C" {
+
+ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, int32_t k, int32_t score,
+                            int32_t *ids, float *weights, int32_t *counts, int32_t *offsets,
+                            int32_t *perm, void *stream)
+{
+    if (!logits || !ids || !weights) return DS4G_ERR_INVALID;
+    if (T < 0 || E < 1 || E > DS4G_MAX_EXPERTS || k < 1 || k > DS4G_MAX_TOPK || k > E)
+        return DS4G_ERR_INVALID;
+    if (score != DS4G_SCORE_SOFTMAX && score != DS4G_SCORE_SIGMOID) return DS4G_ERR_INVALID;
+    if (T > DS4G_MAX_TOKENS) return DS4G_ERR_SHAPE;
+    if (!aligned(logits, 4) || !aligned(ids, 4) || !aligned(weights, 4) ||
+        !aligned(counts, 4) || !aligned(offsets, 4) || !aligned(perm, 4))
+        return DS4G_ERR_LAYOUT;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return from_cuda(launch_route(logits, T, E, k, score, ids, weights, counts, offsets, perm,
+                                  nullptr, nullptr, nullptr, s));
+}
+
+ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out, int32_t out_dtype,
+                             void *stream)
+{
+    if (n_blocks < 0) return DS4G_ERR_INVALID;
+    if (out_dtype != DS4G_F32 && out_dtype != DS4G_F16 && out_dtype != DS4G_BF16)
+        return DS4G_ERR_INVALID;
+    if (n_blocks == 0) return DS4G_OK;
+    if (!blocks || !out) return DS4G_ERR_INVALID;
+    if (!aligned(blocks, 4) || !aligned(out, 16)) return DS4G_ERR_LAYOUT;
+    return from_cuda(launch_q2k_dequant(static_cast<const uint8_t *>(blocks), n_blocks, out,
+                                        out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+ds4g_status ds4g_cb2_dequant(const void *blocks, int64_t n_blocks, const int8_t *codebook,
+                             void *out, int32_t out_dtype, void *stream)
+{
+    if (n_blocks < 0) return DS4G_ERR_INVALID;
+    if (out_dtype != DS4G_F32 && out_dtype != DS4G_F16 && out_dtype != DS4G_BF16)
+        return DS4G_ERR_INVALID;
+    if (n_blocks == 0) return DS4G_OK;
+    if (!blocks || !out || !codebook) return DS4G_ERR_INVALID;
+    if (!aligned(blocks, 2) || !aligned(out, 16)) return DS4G_ERR_LAYOUT;
+    return from_cuda(launch_cb2_dequant(static_cast<const uint8_t *>(blocks), n_blocks, codebook,
+                                        out, out_dtype, static_cast<cudaStream_t>(stream)));
+}
+
+size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T)
+{
+    Plan p;
+    if (make_plan(desc, T, &p) != DS4G_OK) return 0;
+    return p.total;
+}
+
+ds4g_status ds4g_moe_forward(const ds4g_moe_desc *desc, const uint16_t *x, const float *logits,
+                             int32_t T, float *y, void *workspace, size_t ws_bytes, void *stream)
+{
+    Plan p;
+    ds4g_status st = check_forward_args(desc, x, logits, y, workspace, ws_bytes, T, &p);
+    if (st != DS4G_OK || T == 0) return st;
+    if (!aligned(x, 16) || !aligned(logits, 4) || !aligned(y, 16)) return DS4G_ERR_LAYOUT;
+    return forward_impl(desc, p, x, logits, y, static_cast<uint8_t *>(workspace),
+                        static_cast<cudaStream_t>(stream), PhaseEvents{{}, false});
+}
+
+ds4g_status ds4g_moe_forward_phased(const ds4g_moe_desc *desc, const uint16_t *x,
+                                    const float *logits, int32_t T, float *y, void *workspace,
+                                    size_t ws_bytes, void *stream, void *const *events,
+                                    int32_t n_events)
+{
+    Plan p;
+    ds4g_status st = check_forward_args(desc, x, logits, y, workspace, ws_bytes, T, &p);
+    if (st != DS4G_OK || T == 0) return st;
+    if (!events || n_events != 5) return DS4G_ERR_INVALID;
+    PhaseEvents pe{};
+    pe.on = true;
+    for (int i = 0; i < 5; ++i) {
+        if (!events[i]) return DS4G_ERR_INVALID;
+        pe.ev[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    if (!aligned(x, 16) || !aligned(logits, 4) || !aligned(y, 16)) return DS4G_ERR_LAYOUT;
+    return forward_impl(desc, p, x, logits, y, static_cast<uint8_t *>(workspace),
+                        static_cast<cudaStream_t>(stream), pe);
+}
+
+int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T)
+{
+    Plan p;
+    if (T <= 0 || make_plan(desc, T, &p) != DS4G_OK) return 0;
+    return route_launches(T) + gemv_path_launches(p);
+}
+
+ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint16_t *x_host,
+                                  const float *logits_host, int32_t T, float *y_host,
+                                  void *workspace, size_t ws_bytes, void *stream)
+{
+    Plan p;
+    ds4g_status st = check_forward_args(desc, x_host, logits_host, y_host, workspace, ws_bytes, T,
+                                        &p);
+    if (st != DS4G_OK || T == 0) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint16_t *x = reinterpret_cast<uint16_t *>(ws + p.x_stage);
+    float *lg = reinterpret_cast<float *>(ws + p.l_stage);
+    float *y = reinterpret_cast<float *>(ws + p.y_stage);
+    const size_t xb = (size_t)T * p.H * 2, lb = (size_t)T * p.E * 4, yb = (size_t)T * p.H * 4;
+    if (cudaMemcpyAsync(x, x_host, xb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DS4G_ERR_CUDA;
+    if (cudaMemcpyAsync(lg, logits_host, lb, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return DS4G_ERR_CUDA;
+    st = forward_impl(desc, p, x, lg, y, ws, s, PhaseEvents{{}, false});
+    if (st != DS4G_OK) return st;
+    if (cudaMemcpyAsync(y_host, y, yb, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return DS4G_ERR_CUDA;
+    return from_cuda(cudaStreamSynchronize(s));
+}
+
+ds4g_status ds4g_moe_routing_view(const ds4g_moe_desc *desc, int32_t T, void *workspace,
+                                  size_t ws_bytes, int32_t **ids, float **weights,
+                                  int32_t **counts, int32_t **offsets, int32_t **perm)
+{
+    Plan p;
+    ds4g_status st = make_plan(desc, T, &p);
+    if (st != DS4G_OK) return st;
+    if (!workspace) return DS4G_ERR_INVALID;
+    if (!aligned(workspace, kAlign) || ws_bytes < p.total) return DS4G_ERR_WORKSPACE;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    if (ids) *ids = reinterpret_cast<int32_t *>(ws + p.ids);
+    if (weights) *weights = reinterpret_cast<float *>(ws + p.wts);
+    if (counts) *counts = reinterpret_cast<int32_t *>(ws + p.counts);
+    if (offsets) *offsets = reinterpret_cast<int32_t *>(ws + p.offsets);
+    if (perm) *perm = reinterpret_cast<int32_t *>(ws + p.perm);
+    return DS4G_OK;
+}
+
+const char *ds4g_status_string(ds4g_status status)
+{
+    switch (status) {
+    case DS4G_OK: return "ok";
+    case DS4G_ERR_INVALID: return "invalid argument";
+    case DS4G_ERR_SHAPE: return "unsupported shape";
+    case DS4G_ERR_LAYOUT: return "misaligned pointer or unusable stride";
+    case DS4G_ERR_WORKSPACE: return "workspace misaligned or too small";
+    case DS4G_ERR_UNSUPPORTED: return "forced path not possible for these inputs";
+    case DS4G_ERR_CUDA: return "CUDA error";
+    case DS4G_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+int32_t ds4g_abi_version(void) { return DS4G_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// ds4g_common.cuh -- internal declarations shared by the libds4g translation
+// units (device helpers, workspace plan, kernel launchers).  Not installed.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/ds4g.h"
+
+namespace ds4g {
+
+constexpr int kQK = 256;         // weights per super-block
+constexpr int kQ2KBytes = 84;    // Q2_K super-block
+constexpr int kCB2Bytes = 70;    // codebook-2-bit super-block
+
+// ---------------------------------------------------------------------------
+// Workspace plan: byte offsets of every scratch array inside the caller's
+// workspace (each 256-byte aligned).  A = T * k assignments.
+// ---------------------------------------------------------------------------
+struct Plan {
+    int32_t T, H, I, E, k, A;
+    int32_t I_pad;          // inter rounded up to a multiple of 256 (down K)
+    int32_t H_blocks;       // hidden / 256
+    int32_t I_blocks;       // I_pad / 256
+    int32_t block_bytes;    // 84 or 70
+    size_t ids, wts, counts, offsets, perm, slot_pos, active, meta;
+    size_t hbuf;            // [A x I_pad] fp32: SiLU(g)*u per assignment (segment order)
+    size_t yslot;           // [A x H] fp32: w * o per assignment (segment order)
+    size_t x_stage;         // [T x H] bf16 (host entry point)
+    size_t l_stage;         // [T x E] fp32 (host entry point)
+    size_t y_stage;         // [T x H] fp32 (host entry point)
+    size_t total;
+};
+
+// meta words (int32) at Plan::meta
+enum { kMetaActive = 0, kMetaWords = 64 };
+
+// Validation + plan.  Returns DS4G_OK or the first error found.
+ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p);
+
+// Per-device cached properties.
+struct DeviceInfo {
+    int sm_count;
+    int max_smem_optin;
+};
+ds4g_status device_info(DeviceInfo *out);
+
+// ---------------------------------------------------------------------------
+// Kernel launchers (all asynchronous on `s`; return cudaGetLastError()).
+// ---------------------------------------------------------------------------
+cudaError_t launch_route(const float *logits, int T, int E, int k, int score,
+                         int32_t *ids, float *wts, int32_t *counts, int32_t *offsets,
+                         int32_t *perm, int32_t *slot_pos, int32_t *active,
+                         int32_t *n_active, cudaStream_t s);
+
+cudaError_t launch_q2k_dequant(const uint8_t *blocks, int64_t n_blocks, void *out, int dtype,
+                               cudaStream_t s);
+cudaError_t launch_cb2_dequant(const uint8_t *blocks, int64_t n_blocks, const int8_t *cb,
+                               void *out, int dtype, cudaStream_t s);
+
+struct LayerArgs {
+    int H, I, I_pad, E, k, A, T, format;
+    const uint8_t *w_gate, *w_up, *w_down;
+    int64_t gu_row, dn_row, gu_stride, dn_stride;
+    const int8_t *codebook;
+    const uint16_t *x;         // [T x H] bf16
+    const float *wts;          // [A] routing weights (assignment order)
+    const int32_t *counts, *offsets, *perm, *slot_pos, *active, *n_active;
+    float *hbuf;               // [A x I_pad]
+    float *yslot;              // [A x H]
+    float *y;                  // [T x H]
+};
+
+// Launches gate/up, down and combine.  `events` (nullable): events[2..4]
+// are recorded after each of the three kernels.
+cudaError_t launch_gemv_path(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
+                             const cudaEvent_t *events);
+int32_t gemv_path_launches(const Plan &p);
+
+// Records `ev` on `s`; inside a stream capture the record becomes an
+// external event node, so that it is recorded again at every replay.
+inline cudaError_t record_phase(cudaEvent_t ev, cudaStream_t s)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    return cudaEventRecordWithFlags(
+        ev, s, cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault);
+}
+
+// T at or below which routing runs as one single-CTA launch.
+constexpr int kRouteSmallT = 64;
+
+// ---------------------------------------------------------------------------
+// Device helpers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float half_bits(uint32_t bits16)
+{
+    return __half2float(__ushort_as_half((unsigned short)bits16));
+}
+
+__device__ __forceinline__ float bf16_bits(uint32_t bits16)
+{
+    return __uint_as_float(bits16 << 16);
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u)
+{
+    return g / (1.0f + expf(-g)) * u;
+}
+
+}  // namespace ds4g

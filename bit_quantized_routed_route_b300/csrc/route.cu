@@ -1,0 +1,243 @@
+// route.cu -- top-k routing, routing weights, per-expert counts, segment
+// offsets and the token-by-expert permutation.
+//
+// Routing is what makes the experts "routed" (ds4 README mirror, "Model
+// Weights": only the routed MoE experts are quantized).  Rule used here and
+// in the reference: rank by fp32 logit, larger first, equal logits -> lower
+// expert id first, a NaN logit counts as -infinity; weights over the k picks
+// are a softmax, or each pick's sigmoid divided by their sum.
+//
+// Kernels:
+//   topk_kernel   one warp per token; each lane holds E/32 logits in
+//                 registers; k rounds of a butterfly arg-max over the
+//                 (logit desc, id asc) order.
+//   scan_kernel   one CTA: histogram, exclusive scan, then a stable counting
+//                 sort of the assignments a = t*k + i by expert (warp
+//                 match-any ranks + per-warp bases), ascending t inside each
+//                 segment.  Integer atomics only; no float atomics.
+//   route_small   both phases in one CTA for small T (decode), one launch.
+#include "ds4g_common.cuh"
+
+namespace ds4g {
+namespace {
+
+constexpr int kMaxPerLane = 8;   // 256 experts / 32 lanes
+
+__device__ __forceinline__ float canon(float v) { return v != v ? -INFINITY : v; }
+
+// a ranks before b
+__device__ __forceinline__ bool before(float va, int ia, float vb, int ib)
+{
+    return ib < 0 || (ia >= 0 && (va > vb || (va == vb && ia < ib)));
+}
+
+// One token, one warp.  Writes ids[k], wts[k] (lane 0).
+__device__ __forceinline__ void topk_warp(const float *__restrict__ row, int E, int k, int score,
+                                          int32_t *__restrict__ ids, float *__restrict__ wts)
+{
+    const int lane = threadIdx.x & 31;
+    float v[kMaxPerLane];
+    uint32_t avail = 0;
+#pragma unroll
+    for (int j = 0; j < kMaxPerLane; ++j) {
+        int e = lane + 32 * j;
+        v[j] = -INFINITY;
+        if (e < E) {
+            v[j] = canon(__ldg(row + e));
+            avail |= 1u << j;
+        }
+    }
+    float sel_v[DS4G_MAX_TOPK];
+    int sel_i[DS4G_MAX_TOPK];
+#pragma unroll
+    for (int i = 0; i < DS4G_MAX_TOPK; ++i) {
+        if (i >= k) break;
+        float bv = -INFINITY;
+        int bi = -1;
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) {
+            if ((avail >> j) & 1u) {
+                int e = lane + 32 * j;
+                if (before(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
+        sel_v[i] = bv;
+        sel_i[i] = bi;
+    }
+    if (lane == 0) {
+        float p[DS4G_MAX_TOPK];
+        float sum = 0.0f;
+        if (score == DS4G_SCORE_SOFTMAX) {
+            float m = sel_v[0];
+#pragma unroll
+            for (int i = 0; i < DS4G_MAX_TOPK; ++i)
+                if (i < k) { p[i] = expf(sel_v[i] - m); sum += p[i]; }
+        } else {
+#pragma unroll
+            for (int i = 0; i < DS4G_MAX_TOPK; ++i)
+                if (i < k) { p[i] = 1.0f / (1.0f + expf(-sel_v[i])); sum += p[i]; }
+        }
+#pragma unroll
+        for (int i = 0; i < DS4G_MAX_TOPK; ++i)
+            if (i < k) { ids[i] = sel_i[i]; wts[i] = p[i] / sum; }
+    }
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E,
+                                                   int k, int score, int32_t *__restrict__ ids,
+                                                   float *__restrict__ wts)
+{
+    int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    topk_warp(logits + (size_t)t * E, E, k, score, ids + (size_t)t * k, wts + (size_t)t * k);
+}
+
+// Shared state of the counting sort (one CTA of 1024 threads = 32 warps).
+struct ScanSmem {
+    int count[DS4G_MAX_EXPERTS];
+    int offset[DS4G_MAX_EXPERTS + 1];
+    int running[DS4G_MAX_EXPERTS];
+    int warp_base[32][DS4G_MAX_EXPERTS];
+    int warp_sum[8];
+    int act_sum[8];
+};
+
+// counts / offsets / perm / slot_pos / active from ids[A].  Called by all
+// 1024 threads of the CTA.  `ids` may have been written earlier in the same
+// kernel, so it is read through the coherent path (no __restrict__).
+__device__ void scan_body(ScanSmem &sm, const int32_t *ids, int A, int E,
+                          int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
+                          int32_t *active, int32_t *n_active)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid < DS4G_MAX_EXPERTS) { sm.count[tid] = 0; sm.running[tid] = 0; }
+    __syncthreads();
+    for (int a = tid; a < A; a += blockDim.x) {
+        int e = ids[a];
+        if (e >= 0 && e < E) atomicAdd(&sm.count[e], 1);
+    }
+    __syncthreads();
+    // exclusive scan over E <= 256 experts: 8 warps x 32
+    int c = (tid < E) ? sm.count[tid] : 0;
+    int incl = c;
+    if (warp < 8) {
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) sm.warp_sum[warp] = incl;
+    }
+    __syncthreads();
+    if (warp < 8) {
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += sm.warp_sum[w];
+        if (tid < E) sm.offset[tid] = base + incl - c;
+        if (tid == E - 1) sm.offset[E] = base + incl;
+    }
+    // active experts (count > 0) in id order
+    if (warp < 8) {
+        bool act = (tid < E) && c > 0;
+        unsigned b = __ballot_sync(0xffffffffu, act);
+        if (lane == 0) sm.act_sum[warp] = __popc(b);
+    }
+    __syncthreads();
+    if (warp < 8) {
+        bool act = (tid < E) && c > 0;
+        unsigned b = __ballot_sync(0xffffffffu, act);
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += sm.act_sum[w];
+        if (act && active) active[base + __popc(b & ((1u << lane) - 1u))] = tid;
+        if (tid == 255 && n_active) {
+            int tot = 0;
+            for (int w = 0; w < 8; ++w) tot += sm.act_sum[w];
+            *n_active = tot;
+        }
+    }
+    if (tid < E) {
+        if (counts) counts[tid] = c;
+        if (offsets) offsets[tid] = sm.offset[tid];
+    }
+    if (tid == 0 && offsets) offsets[E] = sm.offset[E];
+    __syncthreads();
+    // stable placement, 1024 assignments per round
+    for (int base = 0; base < A; base += blockDim.x) {
+        for (int i = tid; i < 32 * DS4G_MAX_EXPERTS; i += blockDim.x)
+            (&sm.warp_base[0][0])[i] = 0;
+        __syncthreads();
+        int a = base + tid;
+        int e = (a < A) ? ids[a] : -1;
+        if (e < 0 || e >= E) e = -1;
+        unsigned same = __match_any_sync(0xffffffffu, e);
+        int rank = __popc(same & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) sm.warp_base[warp][e] = __popc(same);
+        __syncthreads();
+        if (tid < E) {
+            int run = sm.running[tid];
+            for (int w = 0; w < 32; ++w) {
+                int cnt = sm.warp_base[w][tid];
+                sm.warp_base[w][tid] = run;
+                run += cnt;
+            }
+            sm.running[tid] = run;
+        }
+        __syncthreads();
+        if (e >= 0) {
+            int pos = sm.offset[e] + sm.warp_base[warp][e] + rank;
+            if (perm) perm[pos] = a;
+            if (slot_pos) slot_pos[a] = pos;
+        }
+        __syncthreads();
+    }
+}
+
+__global__ void __launch_bounds__(1024) scan_kernel(const int32_t *ids, int A, int E,
+                                                    int32_t *counts, int32_t *offsets,
+                                                    int32_t *perm, int32_t *slot_pos,
+                                                    int32_t *active, int32_t *n_active)
+{
+    __shared__ ScanSmem sm;
+    scan_body(sm, ids, A, E, counts, offsets, perm, slot_pos, active, n_active);
+}
+
+// Small T: top-k by the 32 warps of the CTA, then the scan, one launch.
+__global__ void __launch_bounds__(1024) route_small_kernel(
+    const float *__restrict__ logits, int T, int E, int k, int score, int32_t *ids, float *wts,
+    int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos, int32_t *active,
+    int32_t *n_active)
+{
+    __shared__ ScanSmem sm;
+    for (int t = threadIdx.x >> 5; t < T; t += 32)
+        topk_warp(logits + (size_t)t * E, E, k, score, ids + (size_t)t * k, wts + (size_t)t * k);
+    __threadfence_block();
+    __syncthreads();
+    scan_body(sm, ids, T * k, E, counts, offsets, perm, slot_pos, active, n_active);
+}
+
+}  // namespace
+
+cudaError_t launch_route(const float *logits, int T, int E, int k, int score, int32_t *ids,
+                         float *wts, int32_t *counts, int32_t *offsets, int32_t *perm,
+                         int32_t *slot_pos, int32_t *active, int32_t *n_active, cudaStream_t s)
+{
+    if (T <= kRouteSmallT) {
+        route_small_kernel<<<1, 1024, 0, s>>>(logits, T, E, k, score, ids, wts, counts, offsets,
+                                             perm, slot_pos, active, n_active);
+    } else {
+        int warps = 8;
+        topk_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(logits, T, E, k, score, ids,
+                                                                  wts);
+        scan_kernel<<<1, 1024, 0, s>>>(ids, T * k, E, counts, offsets, perm, slot_pos, active,
+                                       n_active);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ds4g

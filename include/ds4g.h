@@ -62,6 +62,13 @@ extern "C" {
 
 #define DS4G_ABI_VERSION 1
 
+/* Symbols of the shared library (built with hidden default visibility). */
+#if defined(__GNUC__)
+#define DS4G_API __attribute__((visibility("default")))
+#else
+#define DS4G_API
+#endif
+
 typedef enum ds4g_status {
     DS4G_OK = 0,
     DS4G_ERR_INVALID = 1,      /* null pointer, negative size, bad enum, k > E ... */
@@ -156,7 +163,7 @@ typedef struct ds4g_moe_desc {
  * k < 1, k > min(8, E), bad score); DS4G_ERR_SHAPE (T > DS4G_MAX_TOKENS);
  * DS4G_ERR_CUDA.  T == 0 is a no-op (counts/offsets still written as zero).
  */
-ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, int32_t k,
+DS4G_API ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, int32_t k,
                             int32_t score, int32_t *ids, float *weights,
                             int32_t *counts, int32_t *offsets, int32_t *perm,
                             void *stream);
@@ -170,7 +177,7 @@ ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, int32_t k
  * Errors: DS4G_ERR_INVALID (null pointer, n_blocks < 0, bad dtype);
  * DS4G_ERR_LAYOUT (alignment); DS4G_ERR_CUDA.  n_blocks == 0 is a no-op.
  */
-ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out,
+DS4G_API ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out,
                              int32_t out_dtype, void *stream);
 
 /*
@@ -180,7 +187,7 @@ ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out,
  * exact; fp16 / bf16 output is the fp32 value rounded to nearest even.
  * Errors as ds4g_q2k_dequant, plus DS4G_ERR_INVALID for a null codebook.
  */
-ds4g_status ds4g_cb2_dequant(const void *blocks, int64_t n_blocks, const int8_t *codebook,
+DS4G_API ds4g_status ds4g_cb2_dequant(const void *blocks, int64_t n_blocks, const int8_t *codebook,
                              void *out, int32_t out_dtype, void *stream);
 
 /*
@@ -188,7 +195,7 @@ ds4g_status ds4g_cb2_dequant(const void *blocks, int64_t n_blocks, const int8_t 
  * (and ds4g_moe_forward_host) need for this layer and T tokens; 0 when the
  * descriptor or T is invalid.  The workspace must be 256-byte aligned.
  */
-size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
+DS4G_API size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
 
 /*
  * ds4g_moe_forward -- the whole layer, steps 1-4.
@@ -203,7 +210,7 @@ size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
  * DS4G_ERR_WORKSPACE, DS4G_ERR_UNSUPPORTED (a forced path that cannot run),
  * DS4G_ERR_CUDA.  T == 0 is a no-op.
  */
-ds4g_status ds4g_moe_forward(const ds4g_moe_desc *desc, const uint16_t *x,
+DS4G_API ds4g_status ds4g_moe_forward(const ds4g_moe_desc *desc, const uint16_t *x,
                              const float *logits, int32_t T, float *y,
                              void *workspace, size_t ws_bytes, void *stream);
 
@@ -215,7 +222,7 @@ ds4g_status ds4g_moe_forward(const ds4g_moe_desc *desc, const uint16_t *x,
  * copy bandwidth; pageable memory works but is slower.
  * Errors: as ds4g_moe_forward.
  */
-ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint16_t *x_host,
+DS4G_API ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint16_t *x_host,
                                   const float *logits_host, int32_t T, float *y_host,
                                   void *workspace, size_t ws_bytes, void *stream);
 
@@ -227,15 +234,37 @@ ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint16_t *x_h
  * Any output pointer may be NULL.  Pure host arithmetic; launches nothing.
  * Errors: DS4G_ERR_INVALID, DS4G_ERR_WORKSPACE.
  */
-ds4g_status ds4g_moe_routing_view(const ds4g_moe_desc *desc, int32_t T, void *workspace,
+DS4G_API ds4g_status ds4g_moe_routing_view(const ds4g_moe_desc *desc, int32_t T, void *workspace,
                                   size_t ws_bytes, int32_t **ids, float **weights,
                                   int32_t **counts, int32_t **offsets, int32_t **perm);
 
+/*
+ * ds4g_moe_forward_phased -- ds4g_moe_forward that also records caller-created
+ * CUDA events (cudaEvent_t, passed as void*) on `stream` at the phase
+ * boundaries, for per-kernel timing:
+ *   events[0] before routing,          events[1] after routing,
+ *   events[2] after gate/up + SiLU,    events[3] after the down projection,
+ *   events[4] after the weighted combine.
+ * n_events must be 5.  Errors: as ds4g_moe_forward, plus DS4G_ERR_INVALID
+ * for a null or short event array.
+ */
+DS4G_API ds4g_status ds4g_moe_forward_phased(const ds4g_moe_desc *desc, const uint16_t *x,
+                                             const float *logits, int32_t T, float *y,
+                                             void *workspace, size_t ws_bytes, void *stream,
+                                             void *const *events, int32_t n_events);
+
+/*
+ * ds4g_moe_forward_launches -- number of kernel launches one
+ * ds4g_moe_forward(desc, ..., T, ...) call enqueues (0 for an invalid
+ * descriptor or T == 0).  Pure host arithmetic.
+ */
+DS4G_API int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T);
+
 /* Static text for a status code ("ok", "invalid argument", ...). */
-const char *ds4g_status_string(ds4g_status status);
+DS4G_API const char *ds4g_status_string(ds4g_status status);
 
 /* DS4G_ABI_VERSION of the loaded library. */
-int32_t ds4g_abi_version(void);
+DS4G_API int32_t ds4g_abi_version(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,152 @@
+"""The C-ABI library on the CPU (no GPU calls): it loads, exports every symbol
+that include/ds4g.h declares, and rejects bad arguments on the host before
+any launch."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_quantized_routed_route_b300 as D
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "ds4g.h")
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"DS4G_API\s+[\w\s\*]+?\b(ds4g_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    assert set(D.EXPORTED) <= set(names), names
+    assert len(names) >= 9
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ctypes.CDLL(D.LIBRARY)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_abi_version_and_status_strings():
+    assert D.abi_version() == 1
+    assert D.status_string(D.OK) == "ok"
+    for s in range(1, 8):
+        assert D.status_string(s) not in ("ok", "unknown status")
+    assert D.status_string(99) == "unknown status"
+
+
+FAKE = 1 << 20   # a 256-byte aligned address that is never dereferenced
+
+
+def desc(**kw):
+    d = D.MoeDesc()
+    d.hidden, d.inter, d.n_experts, d.top_k = 256, 128, 8, 2
+    d.score, d.format, d.flags, d.tc_min_tokens = D.SCORE_SOFTMAX, D.FMT_Q2K, 0, 0
+    d.w_gate = d.w_up = d.w_down = FAKE
+    d.gate_up_row_bytes, d.down_row_bytes = 84, 84
+    d.gate_up_expert_stride, d.down_expert_stride = 128 * 84, 256 * 84
+    d.codebook = None
+    for k, v in kw.items():
+        setattr(d, k, v)
+    return d
+
+
+def fwd(d, T=4, ws_bytes=None, ws=FAKE, x=FAKE, logits=FAKE, y=FAKE):
+    if ws_bytes is None:
+        ws_bytes = max(D.moe_workspace_bytes(d, T), 1)
+    return D.lib().ds4g_moe_forward(ctypes.byref(d), x, logits, T, y, ws, ws_bytes, None)
+
+
+def test_workspace_size_is_positive_and_grows_with_T():
+    d = desc()
+    a, b = D.moe_workspace_bytes(d, 4), D.moe_workspace_bytes(d, 400)
+    assert 0 < a < b and a % 256 == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(hidden=300), D.ERR_SHAPE),
+    (dict(hidden=0), D.ERR_SHAPE),
+    (dict(inter=0), D.ERR_SHAPE),
+    (dict(n_experts=0), D.ERR_INVALID),
+    (dict(n_experts=257), D.ERR_INVALID),
+    (dict(top_k=9, n_experts=16), D.ERR_INVALID),
+    (dict(top_k=3, n_experts=2), D.ERR_INVALID),
+    (dict(score=2), D.ERR_INVALID),
+    (dict(format=5), D.ERR_INVALID),
+    (dict(flags=D.FORCE_GEMV | D.FORCE_TC), D.ERR_INVALID),
+    (dict(flags=64), D.ERR_INVALID),
+    (dict(tc_min_tokens=-1), D.ERR_INVALID),
+    (dict(w_up=None), D.ERR_INVALID),
+    (dict(format=D.FMT_CB2, gate_up_row_bytes=70, down_row_bytes=70,
+          gate_up_expert_stride=128 * 80, down_expert_stride=256 * 80), D.ERR_INVALID),
+    (dict(gate_up_row_bytes=80), D.ERR_LAYOUT),
+    (dict(gate_up_row_bytes=86), D.ERR_LAYOUT),
+    (dict(gate_up_expert_stride=100 * 84), D.ERR_LAYOUT),
+    (dict(down_expert_stride=256 * 84 + 4), D.ERR_LAYOUT),
+    (dict(w_gate=FAKE + 8), D.ERR_LAYOUT),
+    (dict(flags=D.FORCE_TC), D.ERR_LAYOUT),
+])
+def test_forward_rejects_bad_descriptors(kw, code):
+    d = desc(**kw)
+    assert fwd(d, ws_bytes=1 << 30) == code
+    assert D.moe_workspace_bytes(d, 4) == 0
+
+
+def test_forward_rejects_bad_calls():
+    d = desc()
+    need = D.moe_workspace_bytes(d, 4)
+    assert fwd(d, T=-1, ws_bytes=need) == D.ERR_INVALID
+    assert fwd(d, T=D.lib().ds4g_abi_version() * 70000, ws_bytes=1 << 40) == D.ERR_SHAPE
+    assert fwd(d, ws_bytes=need - 1) == D.ERR_WORKSPACE
+    assert fwd(d, ws=FAKE + 16, ws_bytes=need) == D.ERR_WORKSPACE
+    assert fwd(d, x=None, ws_bytes=need) == D.ERR_INVALID
+    assert fwd(d, x=FAKE + 2, ws_bytes=need) == D.ERR_LAYOUT
+    assert fwd(d, y=FAKE + 4, ws_bytes=need) == D.ERR_LAYOUT
+    # T == 0 is a no-op that touches nothing
+    assert fwd(d, T=0, ws=None, x=None, logits=None, y=None, ws_bytes=0) == D.OK
+    assert D.lib().ds4g_moe_forward(None, FAKE, FAKE, 4, FAKE, FAKE, 1 << 30, None) == D.ERR_INVALID
+
+
+def test_host_entry_point_validates_first():
+    d = desc()
+    L = D.lib()
+    assert L.ds4g_moe_forward_host(ctypes.byref(d), FAKE, FAKE, 4, FAKE, FAKE, 10, None) == D.ERR_WORKSPACE
+    assert L.ds4g_moe_forward_host(ctypes.byref(desc(hidden=100)), FAKE, FAKE, 4, FAKE, FAKE, 1 << 30,
+                                   None) == D.ERR_SHAPE
+
+
+def test_route_topk_validation():
+    L = D.lib()
+    assert L.ds4g_route_topk(None, 4, 8, 2, 0, FAKE, FAKE, None, None, None, None) == D.ERR_INVALID
+    assert L.ds4g_route_topk(FAKE, 4, 8, 9, 0, FAKE, FAKE, None, None, None, None) == D.ERR_INVALID
+    assert L.ds4g_route_topk(FAKE, 4, 8, 4, 3, FAKE, FAKE, None, None, None, None) == D.ERR_INVALID
+    assert L.ds4g_route_topk(FAKE, 4, 300, 4, 0, FAKE, FAKE, None, None, None, None) == D.ERR_INVALID
+    assert L.ds4g_route_topk(FAKE, -1, 8, 2, 0, FAKE, FAKE, None, None, None, None) == D.ERR_INVALID
+    assert L.ds4g_route_topk(FAKE, 70000, 8, 2, 0, FAKE, FAKE, None, None, None, None) == D.ERR_SHAPE
+    assert L.ds4g_route_topk(FAKE + 2, 4, 8, 2, 0, FAKE, FAKE, None, None, None, None) == D.ERR_LAYOUT
+
+
+def test_dequant_validation():
+    L = D.lib()
+    assert L.ds4g_q2k_dequant(FAKE, 0, FAKE, D.F32, None) == D.OK          # no-op
+    assert L.ds4g_q2k_dequant(FAKE, -1, FAKE, D.F32, None) == D.ERR_INVALID
+    assert L.ds4g_q2k_dequant(FAKE, 4, FAKE, 7, None) == D.ERR_INVALID
+    assert L.ds4g_q2k_dequant(None, 4, FAKE, D.F32, None) == D.ERR_INVALID
+    assert L.ds4g_q2k_dequant(FAKE + 2, 4, FAKE, D.F32, None) == D.ERR_LAYOUT
+    assert L.ds4g_q2k_dequant(FAKE, 4, FAKE + 4, D.F16, None) == D.ERR_LAYOUT
+    assert L.ds4g_cb2_dequant(FAKE, 4, None, FAKE, D.F32, None) == D.ERR_INVALID
+    assert L.ds4g_cb2_dequant(FAKE + 1, 4, FAKE, FAKE, D.F32, None) == D.ERR_LAYOUT
+
+
+def test_routing_view_points_inside_the_workspace():
+    d = desc()
+    need = D.moe_workspace_bytes(d, 4)
+    st, v = D.moe_routing_view(d, 4, FAKE, need)
+    assert st == D.OK
+    for name in ("ids", "weights", "counts", "offsets", "perm"):
+        assert FAKE <= v[name] < FAKE + need and (v[name] - FAKE) % 256 == 0
+    assert len({v[n] for n in v}) == 5
+    st, _ = D.moe_routing_view(d, 4, FAKE, need - 1)
+    assert st == D.ERR_WORKSPACE

@@ -1,0 +1,90 @@
+"""ds4g_moe_forward against the oracle on the five synthetic workloads and on
+small edge-case layers: routing bit-exact, per-token relative L2 <= 1e-3 and
+max-abs <= 5e-3 * max|ref| on the output.
+
+Full-size workloads run at their full token counts (the launch configuration
+the benchmark times); the oracle computes a seeded sample of tokens one by
+one (its result for a token does not depend on the other tokens)."""
+import numpy as np
+import pytest
+import torch
+
+import bit_quantized_routed_route_b300 as D
+import ds4g_synth as S
+import oracle_pins as P
+from gpu_helpers import (cached_layer, check_output, check_routing, run_forward, to_device)
+
+pytestmark = pytest.mark.gpu
+
+SAMPLE = {"tiny": None, "decode_1tok": None, "decode_32tok": 6, "prefill_2048": 4,
+          "codebook_512": 4}
+
+
+def sample_tokens(T, n, seed):
+    if n is None or n >= T:
+        return None
+    rng = np.random.default_rng(seed)
+    return np.sort(rng.choice(T, size=n, replace=False)).astype(np.int32)
+
+
+@pytest.mark.parametrize("name", list(S.CONFIGS))
+def test_forward_workloads(orc, name):
+    layer = cached_layer(name)
+    L = to_device(layer)
+    y, routing = run_forward(L, layer["x"], layer["logits"])
+    k, score = layer["top_k"], layer["score"]
+    rref = orc.route(layer["logits"], k, score)
+    check_routing(routing, rref)
+    tok = sample_tokens(layer["tokens"], SAMPLE[name], 1234)
+    yref, ids, _ = orc.moe_forward(layer, layer["x"], layer["logits"], tok)
+    yy = y if tok is None else y[tok]
+    check_output(yy, yref)
+    assert np.array_equal(ids, rref["ids"] if tok is None else rref["ids"][tok])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=256, I=128, E=8, k=2, T=4),                     # tiny shape, I < 256
+    dict(H=512, I=320, E=6, k=3, T=5),                     # ragged I (padded down K)
+    dict(H=768, I=256, E=33, k=5, T=70),                   # E not a multiple of 32; T > 64
+    dict(H=256, I=256, E=1, k=1, T=3),                     # one expert
+    dict(H=512, I=512, E=4, k=4, T=40),                    # k = E, every expert busy
+    dict(H=1024, I=384, E=16, k=2, T=1, score=S.SCORE_SIGMOID, logits_kind=S.LOGITS_UNIFORM),
+    dict(H=512, I=256, E=5, k=2, T=9, fmt=S.FMT_CB2, align=16),
+    dict(H=512, I=200, E=7, k=3, T=17, fmt=S.FMT_CB2, align=2),
+])
+def test_forward_edge_layers(orc, kw):
+    layer = P.small_layer(seed=sum(kw.get(x, 0) for x in ("H", "I", "E", "T")), **kw)
+    L = to_device(layer)
+    y, routing = run_forward(L, layer["x"], layer["logits"])
+    check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    check_output(y, yref)
+
+
+def test_forward_zero_scale_expert_gives_exact_zero(orc):
+    layer = P.small_layer(seed=21, E=4, k=1, T=6)
+    layer["w_down"][:, :, :] = 0
+    y, _ = run_forward(to_device(layer), layer["x"], layer["logits"])
+    assert np.all(y == 0.0)
+
+
+def test_forward_is_deterministic():
+    layer = cached_layer("tiny")
+    L = to_device(layer)
+    y1, _ = run_forward(L, layer["x"], layer["logits"])
+    y2, _ = run_forward(L, layer["x"], layer["logits"])
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def test_host_entry_point_matches_device_entry_point():
+    layer = cached_layer("decode_1tok")
+    L = to_device(layer)
+    y_dev, _ = run_forward(L, layer["x"], layer["logits"])
+    T, H = layer["x"].shape
+    x_h = torch.from_numpy(layer["x"].view(np.int16)).pin_memory()
+    l_h = torch.from_numpy(layer["logits"]).pin_memory()
+    y_h = torch.empty((T, H), dtype=torch.float32).pin_memory()
+    ws_bytes = L.workspace_bytes(T)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+    D.check(D.moe_forward_host(L.desc, x_h, l_h, T, y_h, ws, ws_bytes))
+    assert np.array_equal(y_h.numpy().view(np.uint32), y_dev.view(np.uint32))
