@@ -54,6 +54,7 @@ def parse():
     ap.add_argument("--impl", default="ds4g", choices=["ds4g", "reference"])
     ap.add_argument("--config", default="decode_1tok", choices=list(S.CONFIGS))
     ap.add_argument("--copies", type=int, default=0, help="weight copies (0 = auto)")
+    ap.add_argument("--pool", type=int, default=0, help="distinct token batches (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     return ap.parse_args()
@@ -281,7 +282,7 @@ def main():
     T, H, E, k = cfg.tokens, cfg.hidden, cfg.n_experts, cfg.top_k
     x_b, l_b, y_b = T * H * 2, T * E * 4, T * H * 4
     batch_bytes = x_b + l_b
-    P = int(max(1, min(256, (64 << 20) // batch_bytes)))
+    P = args.pool or int(max(1, min(256, (64 << 20) // batch_bytes)))
     xs, ls = [layer["x"]], [layer["logits"]]
     for b in range(1, P):
         tk = S.make_tokens(cfg, T, seed=cfg.seed * 100003 + b)
@@ -338,28 +339,34 @@ def main():
             step(s, stream)
     stream.synchronize()
 
-    # --- graphs: G steps each, with phase events -----------------------------
+    # --- graphs: G steps each ------------------------------------------------
+    # `value` comes from graphs of plain layer calls; per-kernel durations from
+    # one replay of a graph of phased calls (events between the kernels),
+    # inside the same timed bracket.
     G = min(K, 500 if T <= 64 else 20)
     n_full, rem = divmod(K, G)
 
-    def capture(n_steps, first):
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_steps)]
-        for row in evs:
-            for e in row:
-                e.record(stream)          # materialise the cudaEvent_t handles
-        stream.synchronize()
+    def capture(n_steps, phased):
+        evs = None
+        if phased:
+            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_steps)]
+            for row in evs:
+                for e in row:
+                    e.record(stream)      # materialise the cudaEvent_t handles
+            stream.synchronize()
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             for j in range(n_steps):
-                step(first + j, stream, [e.cuda_event for e in evs[j]])
+                step(j, stream, [e.cuda_event for e in evs[j]] if phased else None)
         return g, evs
 
-    g_main, ev_main = capture(G, 0)
-    g_rem, ev_rem = capture(rem, 0) if rem else (None, None)
-    # one untimed replay of each graph
-    g_main.replay()
-    if g_rem is not None:
-        g_rem.replay()
+    g_main, _ = capture(G, False)
+    g_rem = capture(rem, False)[0] if rem else None
+    g_phase, ev_phase = capture(G, True)
+    with torch.cuda.stream(stream):        # graphs replay on the current stream
+        for g in (g_main, g_rem, g_phase):     # one untimed replay of each graph
+            if g is not None:
+                g.replay()
     stream.synchronize()
 
     sampler = ClockSampler(local)
@@ -368,12 +375,14 @@ def main():
     torch.cuda.synchronize()
     sampler.start()
     time.sleep(0.25)
-    start.record(stream)
-    for _ in range(n_full):
-        g_main.replay()
-    if g_rem is not None:
-        g_rem.replay()
-    end.record(stream)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(n_full):
+            g_main.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        end.record(stream)
+        g_phase.replay()
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop()
@@ -383,18 +392,17 @@ def main():
     value = tokens / (elapsed_ms / 1000.0)
     ms_per_step = elapsed_ms / K
 
-    # per-phase durations over the last replay of the main graph
-    ph = np.array([[ev_main[j][i].elapsed_time(ev_main[j][i + 1]) for i in range(4)]
+    # per-phase durations over the phased replay
+    ph = np.array([[ev_phase[j][i].elapsed_time(ev_phase[j][i + 1]) for i in range(4)]
                    for j in range(G)])
     ph_ms = ph.mean(axis=0)                        # route, gateup, down, combine
     # algorithmic bytes per launch of the dominant (gate/up) kernel, averaged
-    # over the steps of the graph: gate + up bytes of the active experts,
-    # x read, h written (fp32, padded rows)
+    # over the steps of the graph: the logical quantized bytes of W_gate and
+    # W_up of the active experts, the activations read (bf16) and h written
+    # (2 bytes per value)
     steps_b = np.arange(G) % P
     act = active[steps_b]
-    i_pad = -(-cfg.inter // 256) * 256
-    gate_up_bytes = float(np.mean(act * 2 * gu_b)) + x_b + T * k * i_pad * 4
-    down_bytes = float(np.mean(act * dn_b)) + T * k * i_pad * 4 + T * k * H * 4
+    gate_up_bytes = float(np.mean(act * 2 * gu_b)) + x_b + T * k * cfg.inter * 2
     step_bytes = float(np.mean(touched[steps_b])) + x_b + l_b + y_b
     hbm_peak, peak_kind = peaks()
     achieved = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9

@@ -26,19 +26,22 @@ OK, ERR_INVALID, ERR_SHAPE, ERR_LAYOUT, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 FMT_Q2K, FMT_CB2 = 0, 1
 F32, F16, BF16 = 0, 1, 2
-FORCE_GEMV, FORCE_TC = 1, 2
+FORCE_GEMV, FORCE_TC, DEBUG_STALL = 1, 2, 256
 
 EXPORTED = (
     "ds4g_route_topk", "ds4g_q2k_dequant", "ds4g_cb2_dequant", "ds4g_moe_workspace_bytes",
     "ds4g_moe_forward", "ds4g_moe_forward_host", "ds4g_moe_routing_view",
-    "ds4g_moe_forward_phased", "ds4g_moe_forward_launches",
-    "ds4g_status_string", "ds4g_abi_version",
+    "ds4g_moe_forward_phased", "ds4g_moe_forward_launches", "ds4g_moe_device_status",
+    "ds4g_status_string", "ds4g_abi_version", "ds4g_last_cuda_error",
 )
 
 
 class DS4GError(RuntimeError):
     def __init__(self, status: int):
-        super().__init__(f"ds4g status {status}: {status_string(status)}")
+        msg = f"ds4g status {status}: {status_string(status)}"
+        if status == ERR_CUDA:
+            msg += f" (cudaError {_lib.ds4g_last_cuda_error()})"
+        super().__init__(msg)
         self.status = status
 
 
@@ -75,8 +78,10 @@ def _load() -> ctypes.CDLL:
         "ds4g_moe_forward_phased": (i32, [pdesc, vp, vp, i32, vp, vp, sz, vp,
                                           ctypes.POINTER(ctypes.c_void_p), i32]),
         "ds4g_moe_forward_launches": (i32, [pdesc, i32]),
+        "ds4g_moe_device_status": (i32, [pdesc, i32, vp, sz, ctypes.POINTER(i32), vp]),
         "ds4g_status_string": (ctypes.c_char_p, [i32]),
         "ds4g_abi_version": (i32, []),
+        "ds4g_last_cuda_error": (i32, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -176,6 +181,16 @@ def moe_forward_phased(desc: MoeDesc, x, logits, T, y, workspace, events, ws_byt
 
 def moe_forward_launches(desc: MoeDesc, T: int) -> int:
     return _lib.ds4g_moe_forward_launches(ctypes.byref(desc), T)
+
+
+def moe_device_status(desc: MoeDesc, T: int, workspace, ws_bytes=None, stream=None):
+    """(status of the call, device status word of the last forward)."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    v = ctypes.c_int32(-1)
+    st = _lib.ds4g_moe_device_status(ctypes.byref(desc), T, _ptr(workspace), ws_bytes,
+                                     ctypes.byref(v), _stream(stream))
+    return st, v.value
 
 
 def moe_routing_view(desc: MoeDesc, T: int, workspace, ws_bytes=None):

@@ -16,7 +16,14 @@ size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-ds4g_status from_cuda(cudaError_t e) { return e == cudaSuccess ? DS4G_OK : DS4G_ERR_CUDA; }
+thread_local int g_last_cuda_error = 0;
+
+ds4g_status from_cuda(cudaError_t e)
+{
+    if (e == cudaSuccess) return DS4G_OK;
+    g_last_cuda_error = (int)e;
+    return DS4G_ERR_CUDA;
+}
 
 std::mutex g_dev_mu;
 DeviceInfo g_dev[64];
@@ -52,7 +59,8 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
         return DS4G_ERR_INVALID;
     if (d->score != DS4G_SCORE_SOFTMAX && d->score != DS4G_SCORE_SIGMOID) return DS4G_ERR_INVALID;
     if (d->format != DS4G_FMT_Q2K && d->format != DS4G_FMT_CB2) return DS4G_ERR_INVALID;
-    if ((d->flags & ~(DS4G_FORCE_GEMV | DS4G_FORCE_TC)) != 0) return DS4G_ERR_INVALID;
+    if ((d->flags & ~(DS4G_FORCE_GEMV | DS4G_FORCE_TC | DS4G_DEBUG_STALL)) != 0)
+        return DS4G_ERR_INVALID;
     if ((d->flags & DS4G_FORCE_GEMV) && (d->flags & DS4G_FORCE_TC)) return DS4G_ERR_INVALID;
     if (d->tc_min_tokens < 0) return DS4G_ERR_INVALID;
     if (!d->w_gate || !d->w_up || !d->w_down) return DS4G_ERR_INVALID;
@@ -105,6 +113,11 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     q.slot_pos = take(A * 4);
     q.active = take((size_t)q.E * 4);
     q.meta = take(kMetaWords * 4);
+    q.status = take(4);
+    q.xp = take((size_t)T * q.H * 2);
+    q.xs = take((size_t)T * (q.H / 16) * 4);
+    q.hp = take(A * q.I_pad * 2);
+    q.hs = take(A * (q.I_pad / 16) * 4);
     q.hbuf = take(A * q.I_pad * 4);
     q.yslot = take(A * q.H * 4);
     q.x_stage = take((size_t)T * q.H * 2);
@@ -116,6 +129,12 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
 }
 
 namespace {
+
+bool use_decode_path(const ds4g_moe_desc *d, const Plan &p)
+{
+    if (d->flags & DS4G_FORCE_TC) return false;
+    return decode_path_supported(p, d);
+}
 
 // Records events[i] (when given) at the phase boundaries of one forward.
 struct PhaseEvents {
@@ -142,10 +161,15 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     int32_t *slot_pos = reinterpret_cast<int32_t *>(ws + p.slot_pos);
     int32_t *active = reinterpret_cast<int32_t *>(ws + p.active);
     int32_t *meta = reinterpret_cast<int32_t *>(ws + p.meta);
+    int32_t *status = reinterpret_cast<int32_t *>(ws + p.status);
+    __half *xp = reinterpret_cast<__half *>(ws + p.xp);
+    float *xs = reinterpret_cast<float *>(ws + p.xs);
+    const bool decode = use_decode_path(d, p);
     if (pe.mark(0, s) != cudaSuccess) return DS4G_ERR_CUDA;
     cudaError_t e = launch_route(logits, p.T, p.E, p.k, d->score, ids, wts, counts, offsets, perm,
-                                 slot_pos, active, meta + kMetaActive, s);
-    if (e != cudaSuccess) return DS4G_ERR_CUDA;
+                                 slot_pos, active, meta + kMetaActive, decode ? x : nullptr, p.H,
+                                 xp, xs, status, s);
+    if (e != cudaSuccess) return from_cuda(e);
     if (pe.mark(1, s) != cudaSuccess) return DS4G_ERR_CUDA;
     LayerArgs a{};
     a.H = p.H;
@@ -175,6 +199,13 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     a.hbuf = reinterpret_cast<float *>(ws + p.hbuf);
     a.yslot = reinterpret_cast<float *>(ws + p.yslot);
     a.y = y;
+    if (decode) {
+        DecodeBufs b{xp, xs, reinterpret_cast<__half *>(ws + p.hp),
+                     reinterpret_cast<float *>(ws + p.hs), status};
+        const bool stall = (d->flags & DS4G_DEBUG_STALL) != 0;
+        return from_cuda(launch_decode_path(a, b, dev, s, pe.on ? pe.ev : nullptr,
+                                            stall ? kStallWaitNs : kWaitNs, stall));
+    }
     return from_cuda(launch_gemv_path(a, dev, s, pe.on ? pe.ev : nullptr));
 }
 
@@ -213,7 +244,8 @@ ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, int32_t k
         return DS4G_ERR_LAYOUT;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return from_cuda(launch_route(logits, T, E, k, score, ids, weights, counts, offsets, perm,
-                                  nullptr, nullptr, nullptr, s));
+                                  nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr, nullptr,
+                                  s));
 }
 
 ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out, int32_t out_dtype,
@@ -284,7 +316,7 @@ int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T)
 {
     Plan p;
     if (T <= 0 || make_plan(desc, T, &p) != DS4G_OK) return 0;
-    return route_launches(T) + gemv_path_launches(p);
+    return route_launches(T) + (use_decode_path(desc, p) ? 2 : gemv_path_launches(p));
 }
 
 ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint16_t *x_host,
@@ -330,6 +362,24 @@ ds4g_status ds4g_moe_routing_view(const ds4g_moe_desc *desc, int32_t T, void *wo
     return DS4G_OK;
 }
 
+ds4g_status ds4g_moe_device_status(const ds4g_moe_desc *desc, int32_t T, const void *workspace,
+                                   size_t ws_bytes, int32_t *status_out, void *stream)
+{
+    Plan p;
+    ds4g_status st = make_plan(desc, T, &p);
+    if (st != DS4G_OK) return st;
+    if (!workspace || !status_out) return DS4G_ERR_INVALID;
+    if (!aligned(workspace, kAlign) || ws_bytes < p.total) return DS4G_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    if (cudaMemcpyAsync(&v, static_cast<const uint8_t *>(workspace) + p.status, 4,
+                        cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return DS4G_ERR_CUDA;
+    *status_out = v;
+    return DS4G_OK;
+}
+
 const char *ds4g_status_string(ds4g_status status)
 {
     switch (status) {
@@ -346,5 +396,7 @@ const char *ds4g_status_string(ds4g_status status)
 }
 
 int32_t ds4g_abi_version(void) { return DS4G_ABI_VERSION; }
+
+int32_t ds4g_last_cuda_error(void) { return g_last_cuda_error; }
 
 }  // extern "C"

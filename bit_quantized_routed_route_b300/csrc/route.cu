@@ -16,7 +16,12 @@
 //                 match-any ranks + per-warp bases), ascending t inside each
 //                 segment.  Integer atomics only; no float atomics.
 //   route_small   both phases in one CTA for small T (decode), one launch.
+//
+// With an activation pointer the kernels also write the decode path's
+// activation operand: xp = fp16(x) with every aligned group of 4 stored in the
+// order (0, 2, 1, 3), and xs = fp32 sums of each 16 consecutive fp16 values.
 #include "ds4g_common.cuh"
+#include "ptx.cuh"
 
 namespace ds4g {
 namespace {
@@ -90,13 +95,47 @@ __device__ __forceinline__ void topk_warp(const float *__restrict__ row, int E, 
     }
 }
 
+// Four activations x[4g..4g+3] -> fp16, stored permuted (0,2,1,3); returns
+// their fp32 sum.
+__device__ __forceinline__ float prep4(const uint16_t *__restrict__ x, __half *__restrict__ xp,
+                                       size_t g)
+{
+    const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(x) + g);
+    const __half h0 = __float2half_rn(bf16_bits(raw.x & 0xFFFFu));
+    const __half h1 = __float2half_rn(bf16_bits(raw.x >> 16));
+    const __half h2 = __float2half_rn(bf16_bits(raw.y & 0xFFFFu));
+    const __half h3 = __float2half_rn(bf16_bits(raw.y >> 16));
+    __half2 *o = reinterpret_cast<__half2 *>(xp + 4 * g);
+    o[0] = __halves2half2(h0, h2);
+    o[1] = __halves2half2(h1, h3);
+    return __half2float(h0) + __half2float(h1) + __half2float(h2) + __half2float(h3);
+}
+
+// One group of 4 per lane; lanes 4j..4j+3 of a warp cover one sub-block of
+// 16 and reduce its sum.  n_groups must be a multiple of 32 per warp pass.
+__device__ __forceinline__ void prep_groups(const uint16_t *x, __half *xp, float *xs, size_t g)
+{
+    float v = prep4(x, xp, g);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    if ((g & 3) == 0) xs[g >> 2] = v;
+}
+
 __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ logits, int T, int E,
                                                    int k, int score, int32_t *__restrict__ ids,
-                                                   float *__restrict__ wts)
+                                                   float *__restrict__ wts,
+                                                   const uint16_t *__restrict__ x, int H,
+                                                   __half *__restrict__ xp, float *__restrict__ xs,
+                                                   int32_t *status)
 {
+    if (status && blockIdx.x == 0 && threadIdx.x == 0) *status = DS4G_OK;
     int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     topk_warp(logits + (size_t)t * E, E, k, score, ids + (size_t)t * k, wts + (size_t)t * k);
+    if (x) {
+        const size_t g0 = (size_t)t * (H / 4);
+        for (int g = threadIdx.x & 31; g < H / 4; g += 32) prep_groups(x, xp, xs, g0 + g);
+    }
 }
 
 // Shared state of the counting sort (one CTA of 1024 threads = 32 warps).
@@ -211,11 +250,18 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t *ids, int A, i
 __global__ void __launch_bounds__(1024) route_small_kernel(
     const float *__restrict__ logits, int T, int E, int k, int score, int32_t *ids, float *wts,
     int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos, int32_t *active,
-    int32_t *n_active)
+    int32_t *n_active, const uint16_t *__restrict__ x, int H, __half *__restrict__ xp,
+    float *__restrict__ xs, int32_t *status)
 {
     __shared__ ScanSmem sm;
+    ptx::grid_dep_launch();    // the consumer kernels may become resident and wait
+    if (status && threadIdx.x == 0) *status = DS4G_OK;
     for (int t = threadIdx.x >> 5; t < T; t += 32)
         topk_warp(logits + (size_t)t * E, E, k, score, ids + (size_t)t * k, wts + (size_t)t * k);
+    if (x) {
+        const size_t groups = (size_t)T * (H / 4);
+        for (size_t g = threadIdx.x; g < groups; g += blockDim.x) prep_groups(x, xp, xs, g);
+    }
     __threadfence_block();
     __syncthreads();
     scan_body(sm, ids, T * k, E, counts, offsets, perm, slot_pos, active, n_active);
@@ -225,15 +271,18 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
 
 cudaError_t launch_route(const float *logits, int T, int E, int k, int score, int32_t *ids,
                          float *wts, int32_t *counts, int32_t *offsets, int32_t *perm,
-                         int32_t *slot_pos, int32_t *active, int32_t *n_active, cudaStream_t s)
+                         int32_t *slot_pos, int32_t *active, int32_t *n_active,
+                         const uint16_t *x, int H, __half *xp, float *xs, int32_t *status,
+                         cudaStream_t s)
 {
     if (T <= kRouteSmallT) {
         route_small_kernel<<<1, 1024, 0, s>>>(logits, T, E, k, score, ids, wts, counts, offsets,
-                                             perm, slot_pos, active, n_active);
+                                             perm, slot_pos, active, n_active, x, H, xp, xs,
+                                             status);
     } else {
         int warps = 8;
         topk_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(logits, T, E, k, score, ids,
-                                                                  wts);
+                                                                  wts, x, H, xp, xs, status);
         scan_kernel<<<1, 1024, 0, s>>>(ids, T * k, E, counts, offsets, perm, slot_pos, active,
                                        n_active);
     }

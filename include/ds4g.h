@@ -77,7 +77,7 @@ typedef enum ds4g_status {
     DS4G_ERR_WORKSPACE = 4,    /* workspace pointer misaligned or too small        */
     DS4G_ERR_UNSUPPORTED = 5,  /* a forced path that cannot run on these inputs    */
     DS4G_ERR_CUDA = 6,         /* a CUDA runtime call or kernel launch failed      */
-    DS4G_ERR_TIMEOUT = 7       /* reserved: a bounded device-side wait expired     */
+    DS4G_ERR_TIMEOUT = 7       /* a bounded device-side wait expired (device status) */
 } ds4g_status;
 
 typedef enum ds4g_score {
@@ -99,7 +99,11 @@ typedef enum ds4g_dtype {
 /* ds4g_moe_desc.flags */
 enum {
     DS4G_FORCE_GEMV = 1,       /* every expert segment on the decode (GEMV) kernels   */
-    DS4G_FORCE_TC = 2          /* every expert segment on the tensor-core kernels     */
+    DS4G_FORCE_TC = 2,         /* every expert segment on the tensor-core kernels     */
+    DS4G_DEBUG_STALL = 256     /* test hook: the decode kernels' copy producers issue
+                                  nothing, so their consumers' bounded waits (2 ms in
+                                  this mode) expire and the workspace status word
+                                  reads DS4G_ERR_TIMEOUT; y is garbage              */
 };
 
 /* Limits checked by the entry points. */
@@ -260,11 +264,26 @@ DS4G_API ds4g_status ds4g_moe_forward_phased(const ds4g_moe_desc *desc, const ui
  */
 DS4G_API int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T);
 
+/*
+ * ds4g_moe_device_status -- the device status word of the last
+ * ds4g_moe_forward on this workspace: DS4G_OK, or DS4G_ERR_TIMEOUT when a
+ * bounded wait inside a kernel expired (the kernel then returned early and y
+ * is not valid).  Synchronizes `stream`.  Errors: DS4G_ERR_INVALID,
+ * DS4G_ERR_WORKSPACE, DS4G_ERR_CUDA.
+ */
+DS4G_API ds4g_status ds4g_moe_device_status(const ds4g_moe_desc *desc, int32_t T,
+                                            const void *workspace, size_t ws_bytes,
+                                            int32_t *status_out, void *stream);
+
 /* Static text for a status code ("ok", "invalid argument", ...). */
 DS4G_API const char *ds4g_status_string(ds4g_status status);
 
 /* DS4G_ABI_VERSION of the loaded library. */
 DS4G_API int32_t ds4g_abi_version(void);
+
+/* The cudaError_t behind the calling thread's most recent DS4G_ERR_CUDA
+ * (0 when none occurred yet).  Pure host call. */
+DS4G_API int32_t ds4g_last_cuda_error(void);
 
 #ifdef __cplusplus
 }
