@@ -28,6 +28,13 @@ def pytest_sessionstart(session):
         oracle.build()
     if _stale(ds4g_synth.LIBRARY, ds4g_synth.SOURCE):
         ds4g_synth.build()
+    import importlib.util
+    path = os.path.join(ROOT, "bit_quantized_routed_route_b300", "build.py")
+    spec = importlib.util.spec_from_file_location("ds4g_build", path)
+    b = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(b)
+    if b.stale():
+        b.build()
 
 
 @pytest.fixture(scope="session")
