@@ -33,6 +33,7 @@ EXPORTED = (
     "ds4g_moe_forward", "ds4g_moe_forward_host", "ds4g_moe_routing_view",
     "ds4g_moe_forward_phased", "ds4g_moe_forward_launches", "ds4g_moe_device_status",
     "ds4g_status_string", "ds4g_abi_version", "ds4g_last_cuda_error",
+    "ds4g_moe_forward_noalloc",
 )
 
 
@@ -82,6 +83,7 @@ def _load() -> ctypes.CDLL:
         "ds4g_status_string": (ctypes.c_char_p, [i32]),
         "ds4g_abi_version": (i32, []),
         "ds4g_last_cuda_error": (i32, []),
+        "ds4g_moe_forward_noalloc": (i32, [pdesc, vp, vp, i32, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -181,6 +183,16 @@ def moe_forward_phased(desc: MoeDesc, x, logits, T, y, workspace, events, ws_byt
 
 def moe_forward_launches(desc: MoeDesc, T: int) -> int:
     return _lib.ds4g_moe_forward_launches(ctypes.byref(desc), T)
+
+
+def moe_forward_noalloc(desc: MoeDesc, x, logits, T, y, stream=None) -> int:
+    """The layer without a caller workspace (a static device array of
+    NOALLOC_SCRATCH_BYTES per GPU); for callers that cannot allocate."""
+    return _lib.ds4g_moe_forward_noalloc(ctypes.byref(desc), _ptr(x), _ptr(logits), T, _ptr(y),
+                                         _stream(stream))
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def moe_device_status(desc: MoeDesc, T: int, workspace, ws_bytes=None, stream=None):

@@ -400,3 +400,55 @@ int32_t ds4g_abi_version(void) { return DS4G_ABI_VERSION; }
 int32_t ds4g_last_cuda_error(void) { return g_last_cuda_error; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Forward without a caller-provided workspace (ds4g_moe_forward_noalloc).
+// The scratch is one file-scope device array per GPU.  Host code must not use
+// the array's name as a device address; it asks the runtime for the address
+// once per device and hands that pointer to the kernels.
+// ---------------------------------------------------------------------------
+namespace ds4g {
+namespace {
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[DS4G_NOALLOC_SCRATCH_BYTES];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[64];
+
+// Device address of the scratch array on the current device, looked up on
+// the first call for that device.
+ds4g_status noalloc_scratch(void **out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return DS4G_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return from_cuda(e);
+        if (!p) return DS4G_ERR_CUDA;
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return DS4G_OK;
+}
+
+}  // namespace
+}  // namespace ds4g
+
+extern "C" ds4g_status ds4g_moe_forward_noalloc(const ds4g_moe_desc *desc, const uint16_t *x,
+                                                const float *logits, int32_t T, float *y,
+                                                void *stream)
+{
+    Plan p;
+    ds4g_status st = make_plan(desc, T, &p);
+    if (st != DS4G_OK || T == 0) return st;
+    if (!x || !logits || !y) return DS4G_ERR_INVALID;
+    if (!aligned(x, 16) || !aligned(logits, 4) || !aligned(y, 16)) return DS4G_ERR_LAYOUT;
+    if (p.total > (size_t)DS4G_NOALLOC_SCRATCH_BYTES) return DS4G_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != DS4G_OK) return st;
+    return forward_impl(desc, p, x, logits, y, static_cast<uint8_t *>(scratch),
+                        static_cast<cudaStream_t>(stream), PhaseEvents{{}, false});
+}

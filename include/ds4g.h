@@ -275,6 +275,37 @@ DS4G_API ds4g_status ds4g_moe_device_status(const ds4g_moe_desc *desc, int32_t T
                                             const void *workspace, size_t ws_bytes,
                                             int32_t *status_out, void *stream);
 
+/*
+ * ds4g_moe_forward_noalloc -- ds4g_moe_forward for callers that cannot
+ * allocate device memory, so cannot hand the library a workspace: a plugin
+ * inside a host runtime that owns every device allocation and gives its
+ * plugins no allocator, or a serving loop that must not call cudaMalloc
+ * (which can synchronize the device) once it is running.  This entry point
+ * has no counterpart on the pages; it is a convenience of this library.
+ *
+ * Scratch comes from one static device array of DS4G_NOALLOC_SCRATCH_BYTES
+ * per GPU, held by every GPU that loads the library until the process exits.
+ * Calls whose workspace (ds4g_moe_workspace_bytes(desc, T)) would exceed it
+ * return DS4G_ERR_WORKSPACE before launching anything; 16 MiB covers decode
+ * up to T = 32 tokens at hidden 7168 / inter 2048 / 256 experts / top-8.
+ * x, logits, y: as ds4g_moe_forward (device pointers owned by the caller).
+ *
+ * The first call on a device looks up the array's device address (a CUDA
+ * runtime query, no allocation); make that first call before any stream
+ * capture.  No call allocates or frees device memory.  Every call on a GPU
+ * shares the one array and leaves its contents behind; the kernels write
+ * every scratch value they later read (the status word is reset by the first
+ * kernel of each call), so nothing needs clearing between calls.  Calls that
+ * overlap on the same GPU (other streams, other host threads) race on the
+ * array: serialize them.  ds4g_moe_routing_view and ds4g_moe_device_status do
+ * not apply to this entry point.
+ * Errors: as ds4g_moe_forward.
+ */
+#define DS4G_NOALLOC_SCRATCH_BYTES (16u << 20)
+DS4G_API ds4g_status ds4g_moe_forward_noalloc(const ds4g_moe_desc *desc, const uint16_t *x,
+                                              const float *logits, int32_t T, float *y,
+                                              void *stream);
+
 /* Static text for a status code ("ok", "invalid argument", ...). */
 DS4G_API const char *ds4g_status_string(ds4g_status status);
 
