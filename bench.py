@@ -43,6 +43,8 @@ L2_BYTES = 126 * 1024 * 1024
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 FALLBACK_HBM_GBS = 6400.0
+FALLBACK_BF16_TFLOPS = 1800.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1400.0
 NOMINAL_HBM_GBS = 8000.0
 
 
@@ -164,6 +166,27 @@ def peaks():
         return float(p["hbm_gbs"]), "measured"
     except (OSError, KeyError, ValueError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peaks():
+    """(burst, sustained) dense bf16 TFLOP/s; fp16 kind::f16 runs at the same rate."""
+    try:
+        p = json.load(open(PEAKS_FILE))
+        return float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+def layer_path(cfg: S.Config) -> str:
+    """Which kernels the library runs for this workload (mirrors its choice:
+    decode kernels up to 32 tokens for Q2_K, tensor-core kernels above that
+    for Q2_K with 16-byte rows, the general kernels otherwise)."""
+    if cfg.format == S.FMT_Q2K and cfg.tokens <= 32 and cfg.inter % 16 == 0:
+        return "decode"
+    if (cfg.format == S.FMT_Q2K and cfg.row_bytes(cfg.hidden) % 16 == 0
+            and cfg.row_bytes(cfg.inter) % 16 == 0):
+        return "tc"
+    return "general"
 
 
 def kernel_source_hash() -> str:
@@ -405,8 +428,26 @@ def main():
     gate_up_bytes = float(np.mean(act * 2 * gu_b)) + x_b + T * k * cfg.inter * 2
     step_bytes = float(np.mean(touched[steps_b])) + x_b + l_b + y_b
     hbm_peak, peak_kind = peaks()
-    achieved = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9
-    traffic = measured_traffic("gateup", cfg.name)
+    path = layer_path(cfg)
+    if path == "tc":
+        # the tensor-core gate/up kernel: 2 * A * 2 * H * I flops per launch
+        burst, sustained, tkind = tensor_peaks()
+        flops = 2.0 * T * k * 2 * H * cfg.inter
+        achieved = flops / (ph_ms[1] / 1000.0) / 1e12
+        roofline = {"bound": "tensor", "kernel": "tc_kernel<0> (gate/up)", "achieved": achieved,
+                    "peak": sustained, "peak_kind": f"{tkind} bf16 sustained (fp16 same rate)",
+                    "unit": "TFLOP/s", "frac": achieved / sustained,
+                    "frac_of_burst": achieved / burst,
+                    "traffic": measured_traffic("tc_gateup", cfg.name),
+                    "algorithmic_flops": flops, "duration_us": ph_ms[1] * 1000.0}
+    else:
+        achieved = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9
+        roofline = {"bound": "hbm",
+                    "kernel": "gateup_q2k_kernel" if path == "decode" else "gateup_kernel",
+                    "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind,
+                    "unit": "GB/s", "frac": achieved / hbm_peak,
+                    "traffic": measured_traffic("gateup", cfg.name),
+                    "algorithmic_bytes": gate_up_bytes, "duration_us": ph_ms[1] * 1000.0}
 
     # --- end to end through the host entry point ------------------------------
     e2e = None
@@ -449,10 +490,8 @@ def main():
         "config": workload_config(cfg, copies,
                                   f"inputs larger than L2: {copies} rotating weight copies, "
                                   f"{touched.mean() / 1e6:.1f} MB touched per step"),
-        "roofline": {"bound": "hbm", "kernel": "gateup", "achieved": achieved, "peak": hbm_peak,
-                     "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / hbm_peak,
-                     "traffic": traffic, "algorithmic_bytes": gate_up_bytes,
-                     "duration_us": ph_ms[1] * 1000.0},
+        "roofline": roofline,
+        "path": path,
         "effective_hbm": {"step_bytes": step_bytes,
                           "gbs": step_bytes / (ms_per_step / 1000.0) / 1e9,
                           "frac_of_measured": step_bytes / (ms_per_step / 1000.0) / 1e9 / hbm_peak,

@@ -120,6 +120,8 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     q.hs = take(A * (q.I_pad / 16) * 4);
     q.hbuf = take(A * q.I_pad * 4);
     q.yslot = take(A * q.H * 4);
+    q.xseg = take(A * q.H * 2);
+    q.tiles = take((size_t)tc_max_tiles(q.E, q.A) * 16);
     q.x_stage = take((size_t)T * q.H * 2);
     q.l_stage = take((size_t)T * q.E * 4);
     q.y_stage = take((size_t)T * q.H * 4);
@@ -130,10 +132,19 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
 
 namespace {
 
-bool use_decode_path(const ds4g_moe_desc *d, const Plan &p)
+enum class Path { kDecode, kTensorCore, kGeneral };
+
+// Decode kernels for small token counts, the tensor-core kernels for larger
+// ones, the general kernels where neither applies (codebook format, rows
+// that are not a multiple of 16 bytes, ragged inter on the decode side).
+Path choose_path(const ds4g_moe_desc *d, const Plan &p)
 {
-    if (d->flags & DS4G_FORCE_TC) return false;
-    return decode_path_supported(p, d);
+    if (d->flags & DS4G_FORCE_TC) return Path::kTensorCore;
+    const bool decode = decode_path_supported(p, d);
+    if (d->flags & DS4G_FORCE_GEMV) return decode ? Path::kDecode : Path::kGeneral;
+    if (decode) return Path::kDecode;
+    if (tc_path_supported(p, d)) return Path::kTensorCore;
+    return Path::kGeneral;
 }
 
 // Records events[i] (when given) at the phase boundaries of one forward.
@@ -164,13 +175,14 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     int32_t *status = reinterpret_cast<int32_t *>(ws + p.status);
     __half *xp = reinterpret_cast<__half *>(ws + p.xp);
     float *xs = reinterpret_cast<float *>(ws + p.xs);
-    const bool decode = use_decode_path(d, p);
+    const Path path = choose_path(d, p);
+    if (path == Path::kTensorCore && !tc_path_supported(p, d)) return DS4G_ERR_UNSUPPORTED;
+    const bool decode = path == Path::kDecode;
     if (pe.mark(0, s) != cudaSuccess) return DS4G_ERR_CUDA;
     cudaError_t e = launch_route(logits, p.T, p.E, p.k, d->score, ids, wts, counts, offsets, perm,
                                  slot_pos, active, meta + kMetaActive, decode ? x : nullptr, p.H,
                                  xp, xs, status, s);
     if (e != cudaSuccess) return from_cuda(e);
-    if (pe.mark(1, s) != cudaSuccess) return DS4G_ERR_CUDA;
     LayerArgs a{};
     a.H = p.H;
     a.I = p.I;
@@ -199,6 +211,12 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     a.hbuf = reinterpret_cast<float *>(ws + p.hbuf);
     a.yslot = reinterpret_cast<float *>(ws + p.yslot);
     a.y = y;
+    TcBufs tb{reinterpret_cast<__half *>(ws + p.xseg), reinterpret_cast<__half *>(ws + p.hp),
+              reinterpret_cast<int32_t *>(ws + p.tiles), meta + kMetaTiles, status};
+    // the activation gather of the tensor-core path belongs to the routing phase
+    if (path == Path::kTensorCore && (e = launch_tc_prep(a, tb, dev, s)) != cudaSuccess)
+        return from_cuda(e);
+    if (pe.mark(1, s) != cudaSuccess) return DS4G_ERR_CUDA;
     if (decode) {
         DecodeBufs b{xp, xs, reinterpret_cast<__half *>(ws + p.hp),
                      reinterpret_cast<float *>(ws + p.hs), status};
@@ -206,6 +224,8 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
         return from_cuda(launch_decode_path(a, b, dev, s, pe.on ? pe.ev : nullptr,
                                             stall ? kStallWaitNs : kWaitNs, stall));
     }
+    if (path == Path::kTensorCore)
+        return from_cuda(launch_tc_path(a, tb, dev, s, pe.on ? pe.ev : nullptr, kWaitNs));
     return from_cuda(launch_gemv_path(a, dev, s, pe.on ? pe.ev : nullptr));
 }
 
@@ -316,7 +336,10 @@ int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T)
 {
     Plan p;
     if (T <= 0 || make_plan(desc, T, &p) != DS4G_OK) return 0;
-    return route_launches(T) + (use_decode_path(desc, p) ? 2 : gemv_path_launches(p));
+    const Path path = choose_path(desc, p);
+    return route_launches(T) + (path == Path::kDecode       ? 2
+                                : path == Path::kTensorCore ? kTcPathLaunches
+                                                            : gemv_path_launches(p));
 }
 
 ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint16_t *x_host,

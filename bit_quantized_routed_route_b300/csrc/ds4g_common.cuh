@@ -31,6 +31,8 @@ struct Plan {
     size_t hp, hs;          // [A x I_pad] fp16 h (4-group permuted), [A x I_pad/16] sums
     size_t hbuf;            // [A x I_pad] fp32: SiLU(g)*u per assignment (segment order)
     size_t yslot;           // [A x H] fp32: w * o per assignment (segment order)
+    size_t xseg;            // [A x H] fp16: activations in segment order (tensor-core path)
+    size_t tiles;           // [tc_max_tiles x 4] int32 token tiles (tensor-core path)
     size_t x_stage;         // [T x H] bf16 (host entry point)
     size_t l_stage;         // [T x E] fp32 (host entry point)
     size_t y_stage;         // [T x H] fp32 (host entry point)
@@ -38,7 +40,7 @@ struct Plan {
 };
 
 // meta words (int32) at Plan::meta
-enum { kMetaActive = 0, kMetaWords = 64 };
+enum { kMetaActive = 0, kMetaTiles = 1, kMetaWords = 64 };
 
 // Validation + plan.  Returns DS4G_OK or the first error found.
 ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p);
@@ -85,6 +87,8 @@ struct LayerArgs {
 cudaError_t launch_gemv_path(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
                              const cudaEvent_t *events);
 int32_t gemv_path_launches(const Plan &p);
+// y[t] = sum_i yslot[slot_pos[t*k+i]] in slot order (one launch).
+cudaError_t launch_combine(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s);
 
 // Records `ev` on `s`; inside a stream capture the record becomes an
 // external event node, so that it is recorded again at every replay.
@@ -113,6 +117,25 @@ bool decode_path_supported(const Plan &p, const ds4g_moe_desc *d);
 cudaError_t launch_decode_path(const LayerArgs &a, const DecodeBufs &b, const DeviceInfo &dev,
                                cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns,
                                bool stall);
+
+// Tensor-core path (tc.cu): Q2_K, rows a multiple of 16 bytes.
+constexpr int kTcTileTokens = 128;      // tokens per tensor-core work item at most
+struct TcBufs {
+    __half *xseg;          // [A x H] fp16
+    __half *hp;            // [A x I_pad] fp16
+    int32_t *tiles;        // [tc_max_tiles x 4]
+    int32_t *n_tiles;
+    int32_t *status;
+};
+bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d);
+int32_t tc_max_tiles(int32_t E, int32_t A);
+// Token tiles and the activation gather (one launch), then gate/up, down and
+// the combine (events[2..4] recorded after each, when given).
+cudaError_t launch_tc_prep(const LayerArgs &a, const TcBufs &b, const DeviceInfo &dev,
+                           cudaStream_t s);
+cudaError_t launch_tc_path(const LayerArgs &a, const TcBufs &b, const DeviceInfo &dev,
+                           cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns);
+constexpr int32_t kTcPathLaunches = 4;  // prep, gate/up, down, combine
 
 // Bounded device waits: default limit, and the short limit used with
 // DS4G_DEBUG_STALL.

@@ -235,15 +235,22 @@ cudaError_t launch_fmt(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s
     if (ev && record_phase(ev[2], s) != cudaSuccess) return cudaGetLastError();
     down_kernel<FMT><<<min(dn_items, persistent), kWarps * 32, 0, s>>>(a);
     if (ev && record_phase(ev[3], s) != cudaSuccess) return cudaGetLastError();
-    int64_t quads = (int64_t)a.T * (a.H / 4);
-    int64_t want = (quads + 255) / 256, cap = (int64_t)dev.sm_count * 8;
-    int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
-    combine_kernel<<<grid, 256, 0, s>>>(a);
+    cudaError_t e = launch_combine(a, dev, s);
+    if (e != cudaSuccess) return e;
     if (ev && record_phase(ev[4], s) != cudaSuccess) return cudaGetLastError();
     return cudaGetLastError();
 }
 
 }  // namespace
+
+cudaError_t launch_combine(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s)
+{
+    int64_t quads = (int64_t)a.T * (a.H / 4);
+    int64_t want = (quads + 255) / 256, cap = (int64_t)dev.sm_count * 8;
+    int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+    combine_kernel<<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemv_path(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
                              const cudaEvent_t *events)

@@ -1,0 +1,71 @@
+"""The tensor-core (tcgen05) path of ds4g_moe_forward against the oracle:
+routing bit-exact, per-token relative L2 <= 1e-3 and max-abs <= 5e-3 *
+max|ref| on the output.
+
+The path runs by itself for Q2_K layers above the decode token counts whose
+rows are multiples of 16 bytes; DS4G_FORCE_TC sends smaller layers to it.
+Cases span several 128-row weight tiles and several 128-token tiles, with
+ragged tails on both (inter not a multiple of 128, segments longer than one
+token tile), a single expert, k = E, and the full-size decode layer."""
+import numpy as np
+import pytest
+
+import bit_quantized_routed_route_b300 as D
+import oracle_pins as P
+from gpu_helpers import cached_layer, check_output, check_routing, run_forward, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=256, I=128, E=8, k=2, T=4),                     # one tile of each; I < 256
+    dict(H=512, I=320, E=6, k=3, T=40),                    # ragged inter (rows >= inter read as zero)
+    dict(H=1024, I=256, E=5, k=2, T=200),                  # segments of > 128 tokens
+    dict(H=1024, I=512, E=1, k=1, T=300),                  # one expert, three token tiles
+    dict(H=2048, I=384, E=33, k=5, T=70),                  # E not a multiple of 32
+    dict(H=768, I=1024, E=4, k=4, T=33),                   # k = E, every expert busy
+])
+def test_tc_forward_small_layers(orc, kw):
+    layer = P.small_layer(seed=1000 + kw["H"] + kw["T"], align=16, **kw)
+    L = to_device(layer, flags=D.FORCE_TC)
+    y, routing = run_forward(L, layer["x"], layer["logits"])
+    check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    check_output(y, yref)
+
+
+def test_tc_forward_decode_layer_forced(orc):
+    """The 7168/2048/256/top-8 layer at 32 tokens, forced onto the
+    tensor-core kernels, on a sample of tokens."""
+    layer = cached_layer("decode_32tok")
+    L = to_device(layer, flags=D.FORCE_TC)
+    y, routing = run_forward(L, layer["x"], layer["logits"])
+    check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
+    tok = np.array([0, 13, 31], dtype=np.int32)
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"], tok)
+    check_output(y[tok], yref)
+
+
+def test_tc_matches_general_path():
+    """Both device paths on the same layer agree within the output tolerance."""
+    layer = P.small_layer(seed=5, H=1024, I=512, E=7, k=3, T=150, align=16)
+    L = to_device(layer, flags=D.FORCE_TC)
+    y_tc, _ = run_forward(L, layer["x"], layer["logits"])
+    y_gv, _ = run_forward(L.with_flags(D.FORCE_GEMV), layer["x"], layer["logits"])
+    check_output(y_tc, y_gv.astype(np.float64))
+
+
+def test_tc_is_deterministic():
+    layer = P.small_layer(seed=9, H=1024, I=256, E=4, k=2, T=130, align=16)
+    L = to_device(layer, flags=D.FORCE_TC)
+    y1, _ = run_forward(L, layer["x"], layer["logits"])
+    y2, _ = run_forward(L, layer["x"], layer["logits"])
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def test_tc_forced_on_unaligned_rows_is_rejected():
+    layer = P.small_layer(seed=3, H=512, I=256, E=4, k=2, T=8)      # 168-byte rows
+    L = to_device(layer, flags=D.FORCE_TC)
+    assert L.workspace_bytes(8) == 0
+    with pytest.raises(D.DS4GError):
+        run_forward(L, layer["x"], layer["logits"])
