@@ -440,10 +440,18 @@ def main():
                     "frac_of_burst": achieved / burst,
                     "traffic": measured_traffic("tc_gateup", cfg.name),
                     "algorithmic_flops": flops, "duration_us": ph_ms[1] * 1000.0}
+    elif path == "decode":
+        # one fused kernel streams W_gate, W_up and W_down of the active experts
+        dec_bytes = float(np.mean(touched[steps_b])) + x_b + y_b
+        achieved = dec_bytes / (ph_ms[1] / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "kernel": "decode_q2k_kernel", "achieved": achieved,
+                    "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+                    "traffic": measured_traffic("decode", cfg.name),
+                    "algorithmic_bytes": dec_bytes, "duration_us": ph_ms[1] * 1000.0}
     else:
         achieved = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9
-        roofline = {"bound": "hbm",
-                    "kernel": "gateup_q2k_kernel" if path == "decode" else "gateup_kernel",
+        roofline = {"bound": "hbm", "kernel": "gateup_kernel",
                     "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind,
                     "unit": "GB/s", "frac": achieved / hbm_peak,
                     "traffic": measured_traffic("gateup", cfg.name),

@@ -2,14 +2,32 @@
 // (micro-batched decode, ds4 README mirror, "So, what can I do with this
 // software?"), bound by the HBM bytes of the quantized weights.
 //
-//   gateup kernel: h[p, n] = SiLU(W_gate[e][n,:] . x_t) * (W_up[e][n,:] . x_t)
-//   down kernel:   y[t, m] = sum_{i<k} w[t,i] * (W_down[e_i][m,:] . h[p(t,i), :])
+//   gate/up: h[p, n] = SiLU(W_gate[e][n,:] . x_t) * (W_up[e][n,:] . x_t)
+//   down:    y[t, m] = sum_{i<k} w[t,i] * (W_down[e_i][m,:] . h[p(t,i), :])
 //
-// Both kernels are persistent (one CTA per SM).  A producer warp streams
-// 16-row (gate/up) or 32-row (down) weight tiles -- contiguous runs of
-// 84-byte blocks -- into a shared-memory ring with cp.async.bulk (TMA, no
-// tensor map) completing on mbarriers; eight consumer warps dequantize in
-// registers straight into mma.sync m16n8k16 fragments.
+// One persistent kernel runs the whole layer (decode_q2k_kernel), one CTA per
+// SM.  Every CTA first routes all T tokens itself (top-k, counts, offsets,
+// the stable token-by-expert order) into shared memory, so no work item
+// waits on global metadata; CTA 0 also writes the routing to the workspace.
+// A tiny kernel ahead of it (decode_pre_kernel) resets the claim counters
+// and, when the activations do not fit in shared memory, converts them;
+// programmatic dependent launch overlaps the two.  A producer warp then
+// claims work from two global counters -- first 16-row gate/up tiles
+// (expert, rows), then 32-row down items -- and streams each claimed tile
+// (contiguous runs of 84-byte blocks) into a shared-memory ring with
+// cp.async.bulk (TMA, no tensor map) completing on mbarriers; a down stage
+// also carries the h rows of its experts.  The ring keeps streaming W_down
+// right after W_gate/W_up, so HBM does not idle at the phase boundary.
+// Sixteen consumer warps dequantize in registers straight into mma.sync
+// m16n8k16 fragments; each warp owns one (matrix, half) pair and every
+// fourth K block of a tile, and the warps' partial sums meet in shared
+// memory.
+//
+// Phase order without a grid barrier: a gate/up tile bumps its expert's
+// completion counter after its h rows are written (fence, then atomic); the
+// producer issues a down tile of expert e only once that counter shows all
+// of e's tiles.  Work is claimed dynamically, so a tile that is waited on has
+// always been claimed by a CTA that is running; every wait is bounded.
 //
 // Block-diagonal activation operand.  A Q2_K weight is
 // w = d*sc_s*q - dmin*m_s with per-row, per-16-weight-sub-block scales.  One
@@ -28,43 +46,33 @@
 //
 // Activations enter as fp16 (bf16 -> fp16 is exact for 6.1e-5 <= |x| <=
 // 65504; smaller magnitudes become fp16 subnormals).  h leaves the gate/up
-// kernel as fp16 (one rounding, relative 2^-11) with fp32 sub-block sums of
-// those fp16 values for the down kernel's correction and min terms.
+// phase as fp16 (one rounding, relative 2^-11) with fp32 sub-block sums of
+// those fp16 values for the down phase's correction and min terms.  When the
+// layer's activations fit, every CTA converts them into its shared memory.
 //
-// Kernel chaining: routing -> gateup -> down by programmatic dependent launch.
-// The down kernel's producer starts streaming W_down (which does not depend
-// on h) before griddepcontrol.wait; its consumers wait.
-//
-// Every mbarrier wait is bounded (globaltimer); on expiry the kernel records
-// DS4G_ERR_TIMEOUT in the workspace status word, drains its own copies (also
-// bounded) and returns.
+// Every mbarrier and counter wait is bounded (globaltimer); on expiry the
+// kernel records DS4G_ERR_TIMEOUT in the workspace status word, drains its
+// own copies (also bounded) and returns.
 #include "ds4g_common.cuh"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace ds4g {
 namespace {
 
 constexpr int kTileM = 16;
-constexpr int kConsumers = 8;
-constexpr int kThreads = (kConsumers + 1) * 32;
 
 // 4-group permutation of activations: element i of an aligned group of 4 is
 // stored at position perm4(i), so that elements (i, i+2) are adjacent.
 __device__ __forceinline__ int perm4(int n) { return (n & ~3) | ((n & 1) << 1) | ((n >> 1) & 1); }
 
-__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-__device__ __forceinline__ float nib_lo(uint32_t b) { return (float)(b & 15u); }
-__device__ __forceinline__ float nib_hi(uint32_t b) { return (float)((b >> 4) & 15u); }
-
-struct Ring {
-    uint64_t *full;
-    uint64_t *empty;
-    uint8_t *data;
-    int stages;
-    uint32_t stage_bytes;
-    __device__ uint8_t *stage(int s) const { return data + (size_t)s * stage_bytes; }
-};
+// 4-bit fields as floats without the integer-conversion pipe: OR into the
+// mantissa of 2^23, subtract 2^23 (exact).
+__device__ __forceinline__ float nib_lo(uint32_t b)
+{
+    return __uint_as_float(ptx::lop3_and_or(b, 15u, 0x4B000000u)) - 8388608.0f;
+}
+__device__ __forceinline__ float nib_hi(uint32_t b) { return nib_lo(b >> 4); }
 
 __device__ __forceinline__ void set_status(int32_t *status, int code)
 {
@@ -102,87 +110,333 @@ __device__ __forceinline__ void build_half_a(HalfA &ha, const uint8_t *blk0, con
     }
 }
 
-// The 8 MMAs of one half for one activation vector.  `xh`: the half's 128
-// activations (fp16, 4-group permuted) in global memory; `xs`: the 8
-// sub-block sums.  Returns D (rows grp, grp+8 x columns 2c, 2c+1) =
-// 4^c * sum_{sub-block} q*x.
-__device__ __forceinline__ void half_mma(const HalfA &ha, const __half *xh, const float *xs,
-                                         int grp, int c, float (&d)[4], float &x0, float &x1)
+constexpr int kConsumers = 16;
+constexpr int kProducerWarp = kConsumers;
+constexpr int kThreads = (kConsumers + 2) * 32;
+// named barriers: 1 = consumers only; 2, 3 = reduction buffer 0/1 filled
+// (consumers arrive, epilogue warp waits); 4, 5 = buffer 0/1 released
+// (epilogue warp arrives, consumers wait)
+constexpr int kBarConsumers = 1, kBarJobFull = 2, kBarJobEmpty = 4;
+constexpr int kJobThreads = (kConsumers + 1) * 32;
+constexpr int kDownRows = 32;            // rows of H per down item (two MMA tiles)
+constexpr int kMaxDownPerStage = 8;
+constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kXStageMax = 48 * 1024;
+constexpr int kMaxAssign = kDecodeMaxT * DS4G_MAX_TOPK;     // 256
+
+// Stage tag written by the producer before it arms the stage's barrier:
+// [0] kind, [1] item, [2] first active-expert index, [3] experts in the stage,
+// [4 + 2j] byte offset of expert j's W_down tile, [5 + 2j] byte offset of its
+// h rows (h sums follow them), or -1 when h is read from global memory.
+enum { kTagEnd = -1, kTagGateUp = 0, kTagDown = 1 };
+constexpr int kTagWords = 4 + 2 * kMaxDownPerStage;
+
+struct DecArgs {
+    int H, I, I_pad, E, k, T, A, score;
+    int H_blocks, I_blocks;
+    const uint8_t *w_gate, *w_up, *w_down;
+    int64_t gu_row, dn_row, gu_stride, dn_stride;
+    int gu_pitch, dn_pitch;   // row pitch of the tiles in shared memory (padded against bank conflicts)
+    const float *logits;   // [T][E]
+    const uint16_t *x;     // [T][H] bf16
+    const __half *xp;      // [T][H] converted by decode_pre_kernel (x_smem == 0)
+    const float *xs;       // [T][H/16]
+    __half *hp;            // [A][I_pad]
+    float *hs;             // [A][I_pad/16]
+    float *y;              // [T][H]
+    int32_t *ids, *counts, *offsets, *perm;   // routing outputs (CTA 0)
+    float *wts;
+    int32_t *status;
+    int32_t *sync;         // [0] gate/up claim, [1] down claim, [4 + e] h values done of expert e
+    uint64_t wait_ns;
+    int stages;
+    uint32_t stage_bytes;
+    int x_smem;            // activations converted into shared memory
+    int stall;             // debug: the producer issues nothing (tests the bounded waits)
+};
+
+// Routing of the call in shared memory.
+struct RouteSmem {
+    int32_t ids[kMaxAssign];
+    float wts[kMaxAssign];
+    int32_t perm[kMaxAssign];      // segment position -> assignment
+    int32_t slot[kMaxAssign];      // assignment -> segment position
+    int32_t cnt[DS4G_MAX_EXPERTS];
+    int32_t off[DS4G_MAX_EXPERTS + 1];
+    int32_t act[DS4G_MAX_EXPERTS];
+    int32_t n_act;
+};
+
+__device__ __forceinline__ void named_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void named_arrive(int id, int n) { asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void consumer_sync() { named_sync(kBarConsumers, kConsumers * 32); }
+
+// One epilogue job: the consumers' partial sums of one token chunk of one
+// tile sit in reduction buffer `rb`; the epilogue warp finishes it.
+enum { kJobStop = 0, kJobGateUp = 1, kJobDown = 2 };
+struct Job {
+    int kind, e, mt, seg0, c0, nt, item, last;
+};
+
+// Bounded wait for a global counter to reach `target` (acquire, gpu scope).
+__device__ __forceinline__ bool wait_counter(const int32_t *p, int target, uint64_t limit_ns)
 {
-    const float2 xx = *reinterpret_cast<const float2 *>(xs + 2 * c);
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    if (v >= target) return true;
+    const uint64_t t0 = ptx::globaltimer_ns();
+    while (true) {
+        __nanosleep(64);
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+        if (v >= target) return true;
+        if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// h of the gate/up phase is written by other CTAs of this kernel: read it at
+// L2 (ld.global.cg), never through a possibly stale L1 line.
+__device__ __forceinline__ uint4 ld_cg4(const void *p) { return __ldcg(reinterpret_cast<const uint4 *>(p)); }
+__device__ __forceinline__ float2 ld_cg2f(const float *p) { return __ldcg(reinterpret_cast<const float2 *>(p)); }
+
+// The 8 MMAs of one half for one activation vector.  `xh`: the half's 128
+// activations (fp16, 4-group permuted); `xs`: its 8 sub-block sums.
+// SHARED: both in shared memory; lanes whose B registers are zero read the
+// 32-byte zero buffer `zero` instead, so no selects are needed.  Otherwise
+// global memory written by other CTAs of this kernel.  Returns D (rows grp,
+// grp+8 x columns 2c, 2c+1) = 4^c * sum_{sub-block} q*x.
+template <bool SHARED>
+__device__ __forceinline__ void half_mma_v(const HalfA &ha, const __half *xh, const float *xs,
+                                           const __half *zero, int grp, int c, float (&d)[4],
+                                           float &x0, float &x1)
+{
+    const float2 xx = SHARED ? *reinterpret_cast<const float2 *>(xs + 2 * c) : ld_cg2f(xs + 2 * c);
     x0 = xx.x;
     x1 = xx.y;
     d[0] = -1024.0f * x0;
     d[1] = -1024.0f * x1;
     d[2] = d[0];
     d[3] = d[1];
-    uint32_t bv[8];
-    const bool act = (grp & 3) == c;
-    if (act) {
-        // coherent loads: h is written by the previous grid of the chain
-        const uint4 *p = reinterpret_cast<const uint4 *>(xh + 16 * grp);
-        uint4 u0 = p[0], u1 = p[1];
-        bv[0] = u0.x; bv[1] = u0.y; bv[2] = u0.z; bv[3] = u0.w;
-        bv[4] = u1.x; bv[5] = u1.y; bv[6] = u1.z; bv[7] = u1.w;
+    const bool act = (grp & 3) == c, lo = grp < 4;
+    uint32_t b0[8], b1[8];
+    if (SHARED) {
+        const uint4 *p0 = reinterpret_cast<const uint4 *>(act && lo ? xh + 16 * grp : zero);
+        const uint4 *p1 = reinterpret_cast<const uint4 *>(act && !lo ? xh + 16 * grp : zero);
+        const uint4 u0 = p0[0], u1 = p0[1], v0 = p1[0], v1 = p1[1];
+        b0[0] = u0.x; b0[1] = u0.y; b0[2] = u0.z; b0[3] = u0.w;
+        b0[4] = u1.x; b0[5] = u1.y; b0[6] = u1.z; b0[7] = u1.w;
+        b1[0] = v0.x; b1[1] = v0.y; b1[2] = v0.z; b1[3] = v0.w;
+        b1[4] = v1.x; b1[5] = v1.y; b1[6] = v1.z; b1[7] = v1.w;
     } else {
+        uint32_t bv[8];
+        if (act) {
+            const uint4 u0 = ld_cg4(xh + 16 * grp), u1 = ld_cg4(xh + 16 * grp + 8);
+            bv[0] = u0.x; bv[1] = u0.y; bv[2] = u0.z; bv[3] = u0.w;
+            bv[4] = u1.x; bv[5] = u1.y; bv[6] = u1.z; bv[7] = u1.w;
+        } else {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) bv[t] = 0u;
+            for (int t = 0; t < 8; ++t) bv[t] = 0u;
+        }
+#pragma unroll
+        for (int t = 0; t < 8; ++t) {
+            b0[t] = lo ? bv[t] : 0u;
+            b1[t] = lo ? 0u : bv[t];
+        }
     }
-    const bool lo = grp < 4;
 #pragma unroll
-    for (int t = 0; t < 8; ++t) {
-        const uint32_t b0 = lo ? bv[t] : 0u;
-        const uint32_t b1 = lo ? 0u : bv[t];
-        ptx::mma_16816(d, ha.a[t], b0, b1, d);
+    for (int t = 0; t < 8; ++t) ptx::mma_16816(d, ha.a[t], b0[t], b1[t], d);
+}
+
+// One (K block, half) unit of one 16-row tile for up to NT activation
+// vectors: accumulates d * (scale terms) - dmin * (min terms) into part.
+// `blk0`: block kb of row grp of the tile in shared memory; `xk`/`sk`: the
+// K block's activations / sub-block sums; `off[j]`: element offset of
+// vector j's activations (its sums start at off[j] / 16).
+template <int NT, bool SHARED>
+__device__ __forceinline__ void tile_unit(const uint8_t *blk0, int64_t row_bytes, int h, int grp,
+                                          int c, float inv4c, const __half *xk, const float *sk,
+                                          const __half *zero, const uint32_t (&off)[NT], int nt,
+                                          float (&part)[NT][2])
+{
+    const uint8_t *blk1 = blk0 + 8 * row_bytes;
+    const uint32_t dd0 = ptx::lds32(blk0 + 80), dd1 = ptx::lds32(blk1 + 80);
+    HalfA ha;
+    build_half_a(ha, blk0, blk1, h, c);
+    const uint32_t sb0 = *reinterpret_cast<const uint16_t *>(blk0 + 8 * h + 2 * c);
+    const uint32_t sb1 = *reinterpret_cast<const uint16_t *>(blk1 + 8 * h + 2 * c);
+    // d*sc and dmin*m per sub-block (columns 2c, 2c+1), rows grp and grp+8
+    const float d0 = half_bits(dd0 & 0xFFFFu) * inv4c, dm0 = half_bits(dd0 >> 16);
+    const float d1 = half_bits(dd1 & 0xFFFFu) * inv4c, dm1 = half_bits(dd1 >> 16);
+    const float s00 = d0 * nib_lo(sb0), s01 = d0 * nib_lo(sb0 >> 8);
+    const float s10 = d1 * nib_lo(sb1), s11 = d1 * nib_lo(sb1 >> 8);
+    const float m00 = dm0 * nib_hi(sb0), m01 = dm0 * nib_hi(sb0 >> 8);
+    const float m10 = dm1 * nib_hi(sb1), m11 = dm1 * nib_hi(sb1 >> 8);
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        if (j < nt) {
+            float d[4], x0, x1;
+            half_mma_v<SHARED>(ha, xk + off[j] + 128 * h, sk + (off[j] >> 4) + 8 * h, zero, grp, c,
+                               d, x0, x1);
+            part[j][0] += s00 * d[0] + s01 * d[1] - (m00 * x0 + m01 * x1);
+            part[j][1] += s10 * d[2] + s11 * d[3] - (m10 * x0 + m11 * x1);
+        }
     }
 }
 
-struct DecArgs {
-    int H, I, I_pad, E, k, T, A;
-    int H_blocks, I_blocks;
-    const uint8_t *w_gate, *w_up, *w_down;
-    int64_t gu_row, dn_row, gu_stride, dn_stride;
-    const float *wts;
-    const int32_t *offsets, *perm, *slot_pos, *active, *n_active;
-    const __half *xp;   // [T][H]
-    const float *xs;    // [T][H/16]
-    __half *hp;         // [A][I_pad]
-    float *hs;          // [A][I_pad/16]
-    float *y;           // [T][H]
-    int32_t *status;
-    uint64_t wait_ns;
-    int stages;
-    int stall;          // debug: the producer issues nothing (tests the bounded waits)
-};
-
-// ---------------------------------------------------------------------------
-// gate/up
-// ---------------------------------------------------------------------------
+// Quad-reduces this warp's partial sums into red[warp][j][16] (the caller
+// reads red after consumer_sync).
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) gateup_q2k_kernel(DecArgs a)
+__device__ __forceinline__ void store_partials(float *red, int warp, int grp, int c,
+                                               float (&part)[NT][2])
+{
+    float *rw = red + (size_t)warp * NT * kTileM;
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            float v = part[j][r];
+            v += __shfl_xor_sync(0xffffffffu, v, 1);
+            v += __shfl_xor_sync(0xffffffffu, v, 2);
+            if (c == 0) rw[j * kTileM + grp + 8 * r] = v;
+        }
+}
+
+// Routing of all T tokens by the whole CTA into shared memory (every CTA
+// computes the same result); CTA 0 writes it to the workspace.
+__device__ void route_into_smem(const DecArgs &a, RouteSmem &r)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nw = blockDim.x >> 5;
+    const int A = a.A;
+    for (int t = warp; t < a.T; t += nw)
+        topk_warp(a.logits + (size_t)t * a.E, a.E, a.k, a.score, r.ids + t * a.k, r.wts + t * a.k);
+    for (int e = tid; e < DS4G_MAX_EXPERTS; e += blockDim.x) r.cnt[e] = 0;
+    __syncthreads();
+    for (int i = tid; i < A; i += blockDim.x) atomicAdd(&r.cnt[r.ids[i]], 1);
+    __syncthreads();
+    if (warp == 0) {
+        // exclusive scan of the counts (8 experts per lane) and the active list
+        int c[kMaxPerLane], sum = 0;
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) {
+            const int e = lane * kMaxPerLane + j;
+            c[j] = e < a.E ? r.cnt[e] : 0;
+            sum += c[j];
+        }
+        int incl = sum, nact = 0;
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) nact += c[j] > 0;
+        int nincl = nact;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            const int w = __shfl_up_sync(0xffffffffu, nincl, o);
+            if (lane >= o) { incl += v; nincl += w; }
+        }
+        int run = incl - sum, arun = nincl - nact;
+#pragma unroll
+        for (int j = 0; j < kMaxPerLane; ++j) {
+            const int e = lane * kMaxPerLane + j;
+            if (e < a.E) {
+                r.off[e] = run;
+                if (c[j] > 0) r.act[arun++] = e;
+            }
+            run += c[j];
+        }
+        if (lane == 31) {
+            r.off[a.E] = incl;
+            r.n_act = nincl;
+        }
+    }
+    __syncthreads();
+    // stable placement: rank of assignment i among the earlier ones of its expert
+    for (int i = tid; i < A; i += blockDim.x) {
+        const int e = r.ids[i];
+        int rank = 0;
+        for (int q = 0; q < i; ++q) rank += r.ids[q] == e;
+        const int pos = r.off[e] + rank;
+        r.perm[pos] = i;
+        r.slot[i] = pos;
+    }
+    __syncthreads();
+    if (blockIdx.x == 0) {
+        for (int i = tid; i < A; i += blockDim.x) {
+            a.ids[i] = r.ids[i];
+            a.wts[i] = r.wts[i];
+            a.perm[i] = r.perm[i];
+        }
+        for (int e = tid; e < a.E; e += blockDim.x) a.counts[e] = r.cnt[e];
+        if (tid == 0) a.offsets[a.E] = r.off[a.E];
+        for (int e = tid; e < a.E; e += blockDim.x) a.offsets[e] = r.off[e];
+    }
+}
+
+// x (bf16) -> fp16 in the (0, 2, 1, 3) order per 4, plus fp32 sums of 16,
+// for `n_groups` groups of 4 starting at group g0 (all threads of the CTA or
+// grid stride by `stride`).
+__device__ __forceinline__ void convert_x(const uint16_t *x, __half *xp, float *xs, size_t g0,
+                                          size_t n_groups, size_t stride)
+{
+    // one group of 4 per lane; lanes 4j..4j+3 of a warp form a sub-block
+    for (size_t g = g0; g < n_groups; g += stride) {
+        const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(x) + g);
+        const __half h0 = __float2half_rn(bf16_bits(raw.x & 0xFFFFu));
+        const __half h1 = __float2half_rn(bf16_bits(raw.x >> 16));
+        const __half h2 = __float2half_rn(bf16_bits(raw.y & 0xFFFFu));
+        const __half h3 = __float2half_rn(bf16_bits(raw.y >> 16));
+        __half2 *o = reinterpret_cast<__half2 *>(xp + 4 * g);
+        o[0] = __halves2half2(h0, h2);
+        o[1] = __halves2half2(h1, h3);
+        float v = __half2float(h0) + __half2float(h1) + __half2float(h2) + __half2float(h3);
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        if ((g & 3) == 0) xs[g >> 2] = v;
+    }
+}
+
+// Resets the status word and the decode kernel's counters; converts the
+// activations when they do not fit in the decode kernel's shared memory.
+__global__ void __launch_bounds__(256) decode_pre_kernel(int32_t *status, int32_t *sync, int n_sync,
+                                                         const uint16_t *x, __half *xp, float *xs,
+                                                         size_t n_groups)
+{
+    ptx::grid_dep_launch();
+    if (blockIdx.x == 0) {
+        if (threadIdx.x == 0) *status = DS4G_OK;
+        for (int i = threadIdx.x; i < n_sync; i += blockDim.x) sync[i] = 0;
+    }
+    if (x) convert_x(x, xp, xs, (size_t)blockIdx.x * blockDim.x + threadIdx.x, n_groups,
+                     (size_t)gridDim.x * blockDim.x);
+}
+
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ RouteSmem rs;
+    __shared__ __align__(16) __half zero[16];
+    __shared__ int s_pabort, s_cabort, s_consumed, s_issued;
+    __shared__ Job jobs[2];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = lane >> 2, c = lane & 3;
-    const uint32_t tile_bytes = (uint32_t)(kTileM * a.gu_row);
-    Ring ring;
-    ring.stages = a.stages;
-    ring.stage_bytes = (2 * tile_bytes + 127) / 128 * 128;
-    ring.data = smem;
-    float *red = reinterpret_cast<float *>(smem + (size_t)ring.stages * ring.stage_bytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(red + kConsumers * 2 * NT * kTileM);
-    ring.full = bars;
-    ring.empty = bars + ring.stages;
-    // s_pabort: set by the producer; s_cabort: set by consumers only between
-    // their wait and the consumer barrier that follows it, and read by all
-    // consumers right after that barrier, so every consumer warp takes the
-    // same branch (a bar.sync cannot time out).
-    __shared__ int s_pabort, s_cabort, s_consumed, s_issued;
+    const uint32_t gu_tile = (uint32_t)(kTileM * a.gu_row);
+    const uint32_t dn_tile = (uint32_t)(kDownRows * a.dn_row);
+    const uint32_t h_row = (uint32_t)a.I_pad * 2, hs_row = (uint32_t)(a.I_pad / 16) * 4;
+    uint8_t *ring = smem;
+    uint8_t *p = smem + (size_t)a.stages * a.stage_bytes;
+    const size_t x_bytes = a.x_smem ? (size_t)a.T * a.H * 2 : 0;
+    const size_t xs_bytes = a.x_smem ? (size_t)a.T * (a.H / 16) * 4 : 0;
+    __half *x_s = reinterpret_cast<__half *>(p);
+    float *xs_s = reinterpret_cast<float *>(p + x_bytes);
+    float *red = reinterpret_cast<float *>(p + x_bytes + xs_bytes);       // [2][16][NT][16]
+    float *obuf = red + 2 * kConsumers * NT * kTileM;                     // [A][32]
+    int *tags = reinterpret_cast<int *>(obuf + (size_t)a.A * kDownRows);  // [stages][kTagWords]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tags + kTagWords * a.stages);
+    uint64_t *full = bars, *empty = bars + a.stages;
 
     if (tid == 0) {
-        for (int s = 0; s < ring.stages; ++s) {
-            ptx::mbar_init(&ring.full[s], 1);
-            ptx::mbar_init(&ring.empty[s], kConsumers);
+        for (int s = 0; s < a.stages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], kConsumers);
         }
         ptx::fence_mbar_init();
         s_pabort = 0;
@@ -190,366 +444,350 @@ __global__ void __launch_bounds__(kThreads, 1) gateup_q2k_kernel(DecArgs a)
         s_consumed = 0;
         s_issued = 0;
     }
-    __syncthreads();
+    if (tid < 16) zero[tid] = __float2half_rn(0.0f);
+    if (a.x_smem)
+        convert_x(a.x, x_s, xs_s, tid, (size_t)a.T * (a.H / 4), blockDim.x);
+    route_into_smem(a, rs);       // ends with __syncthreads
 
-    ptx::grid_dep_wait();          // routing and the activation prep are complete
-    ptx::grid_dep_launch();        // let the down kernel start streaming W_down
+    // the counters are reset (and, without x_smem, the activations converted)
+    // by the kernel ahead of this one
+    ptx::grid_dep_wait();
 
+    const int n_act = rs.n_act;
     const int tiles = a.I / kTileM;
-    const int n_items = *a.n_active * tiles;
-    const int first = (int)((int64_t)blockIdx.x * n_items / gridDim.x);
-    const int last = (int)((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
-    const int mine = last - first;
+    const int gu_items = n_act * tiles;
+    const int dn_items = a.H / kDownRows;
+    int32_t *const claim_gu = a.sync, *const claim_dn = a.sync + 1, *const done = a.sync + 4;
 
-    if (warp == kConsumers) {
+    if (warp == kProducerWarp) {
         // ---------------- producer ----------------
         if (lane == 0 && !a.stall) {
-            for (int li = 0; li < mine; ++li) {
-                const int s = li % ring.stages;
-                if (li >= ring.stages &&
-                    !ptx::mbar_wait(&ring.empty[s], ((li / ring.stages) - 1) & 1, a.wait_ns)) {
+            int q = 0;
+            bool ok = true;
+            // claims a ring slot: waits for it to be empty; false on abort
+            auto slot = [&](int &s) -> bool {
+                s = q % a.stages;
+                if (q >= a.stages &&
+                    !ptx::mbar_wait(&empty[s], ((q / a.stages) - 1) & 1, a.wait_ns)) {
                     set_status(a.status, DS4G_ERR_TIMEOUT);
                     s_pabort = 1;
-                    break;
+                    return false;
                 }
-                if (*(volatile int *)&s_cabort) break;
-                const int item = first + li;
-                const int e = a.active[item / tiles];
-                const int mt = item % tiles;
-                const uint8_t *g = a.w_gate + (size_t)e * a.gu_stride + (size_t)mt * tile_bytes;
-                const uint8_t *u = a.w_up + (size_t)e * a.gu_stride + (size_t)mt * tile_bytes;
-                ptx::mbar_arrive_expect_tx(&ring.full[s], 2 * tile_bytes);
-                ptx::bulk_g2s(ring.stage(s), g, tile_bytes, &ring.full[s]);
-                ptx::bulk_g2s(ring.stage(s) + tile_bytes, u, tile_bytes, &ring.full[s]);
-                s_issued = li + 1;
+                return !*(volatile int *)&s_cabort;
+            };
+            while (ok) {
+                const int it = atomicAdd(claim_gu, 1);
+                if (it >= gu_items) break;
+                int s;
+                if (!(ok = slot(s))) break;
+                const int e = rs.act[it / tiles], mt = it % tiles;
+                int *tg = tags + kTagWords * s;
+                tg[0] = kTagGateUp;
+                tg[1] = it;
+                uint8_t *st = ring + (size_t)s * a.stage_bytes;
+                const uint8_t *g = a.w_gate + (size_t)e * a.gu_stride + (size_t)mt * gu_tile;
+                const uint8_t *u = a.w_up + (size_t)e * a.gu_stride + (size_t)mt * gu_tile;
+                ptx::mbar_arrive_expect_tx(&full[s], 2 * gu_tile);
+                if (a.gu_pitch == a.gu_row) {
+                    ptx::bulk_g2s(st, g, gu_tile, &full[s]);
+                    ptx::bulk_g2s(st + gu_tile, u, gu_tile, &full[s]);
+                } else {
+                    for (int r = 0; r < kTileM; ++r) {
+                        ptx::bulk_g2s(st + (size_t)r * a.gu_pitch, g + (size_t)r * a.gu_row,
+                                      (uint32_t)a.gu_row, &full[s]);
+                        ptx::bulk_g2s(st + (size_t)(kTileM + r) * a.gu_pitch, u + (size_t)r * a.gu_row,
+                                      (uint32_t)a.gu_row, &full[s]);
+                    }
+                }
+                s_issued = ++q;
+            }
+            while (ok) {
+                const int it = atomicAdd(claim_dn, 1);
+                if (it >= dn_items) break;
+                int j = 0;
+                while (ok && j < n_act) {
+                    int s;
+                    if (!(ok = slot(s))) break;
+                    int *tg = tags + kTagWords * s;
+                    uint8_t *st = ring + (size_t)s * a.stage_bytes;
+                    // pack experts j, j+1, ... with their h rows while they fit
+                    const uint32_t dn_smem = (uint32_t)(kDownRows * a.dn_pitch);
+                    uint32_t used = 0, bytes = 0;
+                    int cnt = 0;
+                    const int j0 = j;
+                    while (j < n_act && cnt < kMaxDownPerStage) {
+                        const int e = rs.act[j];
+                        const int n_e = rs.cnt[e];
+                        const uint32_t hb = (uint32_t)n_e * (h_row + hs_row);
+                        const bool h_in = used + dn_smem + hb <= a.stage_bytes;
+                        const uint32_t need = dn_smem + (h_in ? hb : 0);
+                        if (cnt > 0 && used + need > a.stage_bytes) break;
+                        if (!wait_counter(done + e, a.I * n_e, a.wait_ns)) {
+                            set_status(a.status, DS4G_ERR_TIMEOUT);
+                            s_pabort = 1;
+                            ok = false;
+                            break;
+                        }
+                        tg[4 + 2 * cnt] = (int)used;
+                        tg[5 + 2 * cnt] = h_in ? (int)(used + dn_smem) : -1;
+                        used += need;
+                        ++cnt;
+                        ++j;
+                    }
+                    if (!ok) break;
+                    tg[0] = kTagDown;
+                    tg[1] = it;
+                    tg[2] = j0;
+                    tg[3] = cnt;
+                    // h was written by other CTAs (generic proxy); the copies
+                    // below read it through the async proxy
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    for (int i = 0; i < cnt; ++i)
+                        bytes += dn_tile + (tg[5 + 2 * i] >= 0 ? (uint32_t)rs.cnt[rs.act[j0 + i]] * (h_row + hs_row) : 0u);
+                    ptx::mbar_arrive_expect_tx(&full[s], bytes);
+                    for (int i = 0; i < cnt; ++i) {
+                        const int e = rs.act[j0 + i];
+                        const uint8_t *src = a.w_down + (size_t)e * a.dn_stride + (size_t)it * dn_tile;
+                        if (a.dn_pitch == a.dn_row)
+                            ptx::bulk_g2s(st + tg[4 + 2 * i], src, dn_tile, &full[s]);
+                        else
+                            for (int r = 0; r < kDownRows; ++r)
+                                ptx::bulk_g2s(st + tg[4 + 2 * i] + (size_t)r * a.dn_pitch,
+                                              src + (size_t)r * a.dn_row, (uint32_t)a.dn_row, &full[s]);
+                        if (tg[5 + 2 * i] >= 0) {
+                            const int n_e = rs.cnt[e], seg0 = rs.off[e];
+                            uint8_t *hd = st + tg[5 + 2 * i];
+                            ptx::bulk_g2s(hd, a.hp + (size_t)seg0 * a.I_pad, n_e * h_row, &full[s]);
+                            ptx::bulk_g2s(hd + (size_t)n_e * h_row,
+                                          a.hs + (size_t)seg0 * (a.I_pad / 16), n_e * hs_row,
+                                          &full[s]);
+                        }
+                    }
+                    s_issued = ++q;
+                }
+            }
+            if (ok) {
+                int s;
+                if (slot(s)) {
+                    tags[kTagWords * s] = kTagEnd;
+                    ptx::mbar_arrive(&full[s]);
+                }
             }
         }
-    } else {
+    } else if (warp < kConsumers) {
         // ---------------- consumers ----------------
         const float inv4c = 1.0f / (float)(1 << (2 * c));
-        for (int li = 0; li < mine; ++li) {
-            const int s = li % ring.stages;
-            if (!ptx::mbar_wait(&ring.full[s], (li / ring.stages) & 1, a.wait_ns)) {
+        // each consumer warp owns one (matrix or m-tile, half) pair and every
+        // fourth K block: units u = 4*kb + 2*wm + wh with u = warp (mod 16)
+        const int wm = (warp >> 1) & 1, wh = warp & 1, wk = warp >> 2;
+        int rb = 0, uses0 = 0, uses1 = 0;
+        // hands the partial sums in `part` to the epilogue warp as job `jb`
+        auto emit = [&](const Job &jb, float (&part)[NT][2]) {
+            int &uses = rb ? uses1 : uses0;
+            if (uses > 0) named_sync(kBarJobEmpty + rb, kJobThreads);
+            store_partials<NT>(red + rb * kConsumers * NT * kTileM, warp, grp, c, part);
+            if (tid == 0) jobs[rb] = jb;
+            named_arrive(kBarJobFull + rb, kJobThreads);
+            ++uses;
+            rb ^= 1;
+        };
+        for (int q = 0; !*(volatile int *)&s_cabort; ++q) {
+            const int s = q % a.stages;
+            if (!ptx::mbar_wait(&full[s], (q / a.stages) & 1, a.wait_ns)) {
                 set_status(a.status, DS4G_ERR_TIMEOUT);
                 s_cabort = 1;
             }
             consumer_sync();
             if (*(volatile int *)&s_cabort) break;
-            const int item = first + li;
-            const int e = a.active[item / tiles];
-            const int mt = item % tiles;
-            const int seg0 = a.offsets[e], seg_n = a.offsets[e + 1] - seg0;
-            const uint8_t *st = ring.stage(s);
-            for (int c0 = 0; c0 < seg_n; c0 += NT) {
-                const int nt = min(NT, seg_n - c0);
-                int tok[NT];
-#pragma unroll
-                for (int j = 0; j < NT; ++j) tok[j] = a.perm[seg0 + c0 + (j < nt ? j : 0)] / a.k;
-                float part[2][NT][2];
-#pragma unroll
-                for (int m = 0; m < 2; ++m)
-#pragma unroll
-                    for (int j = 0; j < NT; ++j) part[m][j][0] = part[m][j][1] = 0.0f;
-                for (int kb = warp; kb < a.H_blocks; kb += kConsumers) {
-#pragma unroll
-                    for (int m = 0; m < 2; ++m) {
-                        const uint8_t *b0 = st + m * tile_bytes + (size_t)grp * a.gu_row + kb * kQ2KBytes;
-                        const uint8_t *b1 = b0 + 8 * a.gu_row;
-                        const uint32_t dd0 = ptx::lds32(b0 + 80), dd1 = ptx::lds32(b1 + 80);
-                        float S[NT][2], M[NT][2];
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) S[j][0] = S[j][1] = M[j][0] = M[j][1] = 0.0f;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            HalfA ha;
-                            build_half_a(ha, b0, b1, h, c);
-                            const uint32_t sb0 = *reinterpret_cast<const uint16_t *>(b0 + 8 * h + 2 * c);
-                            const uint32_t sb1 = *reinterpret_cast<const uint16_t *>(b1 + 8 * h + 2 * c);
-                            const float sc00 = nib_lo(sb0), sc01 = nib_lo(sb0 >> 8);
-                            const float mn00 = nib_hi(sb0), mn01 = nib_hi(sb0 >> 8);
-                            const float sc10 = nib_lo(sb1), sc11 = nib_lo(sb1 >> 8);
-                            const float mn10 = nib_hi(sb1), mn11 = nib_hi(sb1 >> 8);
-#pragma unroll
-                            for (int j = 0; j < NT; ++j) {
-                                if (j < nt) {
-                                    const __half *xh = a.xp + (size_t)tok[j] * a.H + kb * kQK + 128 * h;
-                                    const float *xsh = a.xs + (size_t)tok[j] * (a.H / 16) + kb * 16 + 8 * h;
-                                    float d[4], x0, x1;
-                                    half_mma(ha, xh, xsh, grp, c, d, x0, x1);
-                                    S[j][0] += sc00 * d[0] + sc01 * d[1];
-                                    S[j][1] += sc10 * d[2] + sc11 * d[3];
-                                    M[j][0] += mn00 * x0 + mn01 * x1;
-                                    M[j][1] += mn10 * x0 + mn11 * x1;
-                                }
-                            }
-                        }
-                        const float d0 = half_bits(dd0 & 0xFFFFu) * inv4c, dm0 = half_bits(dd0 >> 16);
-                        const float d1 = half_bits(dd1 & 0xFFFFu) * inv4c, dm1 = half_bits(dd1 >> 16);
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            part[m][j][0] += d0 * S[j][0] - dm0 * M[j][0];
-                            part[m][j][1] += d1 * S[j][1] - dm1 * M[j][1];
-                        }
-                    }
-                }
-                // reduce over the quad (sub-block owners), then over warps
-                float *rw = red + (size_t)warp * 2 * NT * kTileM;
-#pragma unroll
-                for (int m = 0; m < 2; ++m)
+            const int *tg = tags + kTagWords * s;
+            const int kind = tg[0];
+            if (kind == kTagEnd) break;
+            const uint8_t *st = ring + (size_t)s * a.stage_bytes;
+            if (kind == kTagGateUp) {
+                const int it = tg[1];
+                const int e = rs.act[it / tiles], mt = it % tiles;
+                const int seg0 = rs.off[e], seg_n = rs.cnt[e];
+                const uint8_t *mat = st + (size_t)wm * kTileM * a.gu_pitch + (size_t)grp * a.gu_pitch;
+                for (int c0 = 0; c0 < seg_n; c0 += NT) {
+                    const int nt = min(NT, seg_n - c0);
+                    uint32_t off[NT];
 #pragma unroll
                     for (int j = 0; j < NT; ++j)
+                        off[j] = (uint32_t)(rs.perm[seg0 + c0 + (j < nt ? j : 0)] / a.k) * a.H;
+                    float part[NT][2];
 #pragma unroll
-                        for (int r = 0; r < 2; ++r) {
-                            float v = part[m][j][r];
-                            v += __shfl_xor_sync(0xffffffffu, v, 1);
-                            v += __shfl_xor_sync(0xffffffffu, v, 2);
-                            if (c == 0) rw[(m * NT + j) * kTileM + grp + 8 * r] = v;
-                        }
-                consumer_sync();
-                if (tid < nt * kTileM) {
-                    const int row = tid & 15, j = tid >> 4;
-                    float g = 0.0f, u = 0.0f;
-                    for (int w = 0; w < kConsumers; ++w) {
-                        g += red[((size_t)w * 2 * NT + j) * kTileM + row];
-                        u += red[((size_t)w * 2 * NT + NT + j) * kTileM + row];
+                    for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
+                    if (a.x_smem) {
+                        for (int kb = wk; kb < a.H_blocks; kb += kConsumers / 4)
+                            tile_unit<NT, true>(mat + kb * kQ2KBytes, a.gu_pitch, wh, grp, c, inv4c,
+                                                x_s + kb * kQK, xs_s + kb * 16, zero, off, nt, part);
+                    } else {
+                        for (int kb = wk; kb < a.H_blocks; kb += kConsumers / 4)
+                            tile_unit<NT, false>(mat + kb * kQ2KBytes, a.gu_pitch, wh, grp, c, inv4c,
+                                                 a.xp + kb * kQK, a.xs + kb * 16, zero, off, nt, part);
                     }
-                    const __half hv = __float2half_rn(silu_mul(g, u));
-                    const int pos = seg0 + c0 + j;
-                    const int n = mt * kTileM + row;
-                    a.hp[(size_t)pos * a.I_pad + perm4(n)] = hv;
-                    float hsum = __half2float(hv);
-#pragma unroll
-                    for (int off = 8; off > 0; off >>= 1) hsum += __shfl_xor_sync(0x0000ffffu << (16 * ((tid >> 4) & 1)), hsum, off);
-                    if (row == 0) a.hs[(size_t)pos * (a.I_pad / 16) + mt] = hsum;
+                    emit(Job{kJobGateUp, e, mt, seg0, c0, nt, it, 0}, part);
                 }
-                consumer_sync();
+            } else {
+                const int it = tg[1], j0 = tg[2], cnt = tg[3];
+                for (int jj = 0; jj < cnt; ++jj) {
+                    const int e = rs.act[j0 + jj];
+                    const int seg0 = rs.off[e], seg_n = rs.cnt[e];
+                    const uint8_t *mat = st + tg[4 + 2 * jj] + (size_t)(wm * kTileM + grp) * a.dn_pitch;
+                    const int hoff = tg[5 + 2 * jj];
+                    const __half *h_s = reinterpret_cast<const __half *>(st + (hoff >= 0 ? hoff : 0));
+                    const float *hs_s = reinterpret_cast<const float *>(st + (hoff >= 0 ? hoff : 0) +
+                                                                        (size_t)seg_n * h_row);
+                    for (int c0 = 0; c0 < seg_n; c0 += NT) {
+                        const int nt = min(NT, seg_n - c0);
+                        float part[NT][2];
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
+                        if (hoff >= 0) {
+                            uint32_t off[NT];
+#pragma unroll
+                            for (int j = 0; j < NT; ++j) off[j] = (uint32_t)(c0 + (j < nt ? j : 0)) * a.I_pad;
+                            for (int kb = wk; kb < a.I_blocks; kb += kConsumers / 4)
+                                tile_unit<NT, true>(mat + kb * kQ2KBytes, a.dn_pitch, wh, grp, c, inv4c,
+                                                    h_s + kb * kQK, hs_s + kb * 16, zero, off, nt, part);
+                        } else {
+                            uint32_t off[NT];
+#pragma unroll
+                            for (int j = 0; j < NT; ++j)
+                                off[j] = (uint32_t)(seg0 + c0 + (j < nt ? j : 0)) * a.I_pad;
+                            for (int kb = wk; kb < a.I_blocks; kb += kConsumers / 4)
+                                tile_unit<NT, false>(mat + kb * kQ2KBytes, a.dn_pitch, wh, grp, c, inv4c,
+                                                     a.hp + kb * kQK, a.hs + kb * 16, zero, off, nt, part);
+                        }
+                        const int last = (j0 + cnt == n_act) && (jj == cnt - 1) && (c0 + NT >= seg_n);
+                        emit(Job{kJobDown, e, 0, seg0, c0, nt, it, last}, part);
+                    }
+                }
             }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&ring.empty[s]);
-            if (tid == 0) s_consumed = li + 1;
+            if (lane == 0) ptx::mbar_arrive(&empty[s]);
+            if (tid == 0) s_consumed = q + 1;
         }
-    }
-    __syncthreads();
-    const bool aborted = s_pabort || s_cabort;
-    // drain copies that were issued but not consumed (only after an abort)
-    if (tid == kConsumers * 32 && aborted) {
-        for (int li = s_consumed; li < s_issued; ++li) {
-            const int s = li % ring.stages;
-            if (!ptx::mbar_wait(&ring.full[s], (li / ring.stages) & 1, a.wait_ns)) break;
-        }
-    }
-    // zero h rows inter..I_pad-1 (padding of the down projection's K)
-    const int pad_tiles = (a.I_pad - a.I) / kTileM;
-    if (pad_tiles > 0 && !aborted) {
-        const int n_act = *a.n_active;
-        for (int j = blockIdx.x; j < n_act; j += gridDim.x) {
-            const int e = a.active[j];
-            const int seg0 = a.offsets[e], seg_n = a.offsets[e + 1] - seg0;
-            for (int i = tid; i < seg_n * (a.I_pad - a.I); i += blockDim.x) {
-                const int pos = seg0 + i / (a.I_pad - a.I), n = a.I + i % (a.I_pad - a.I);
-                a.hp[(size_t)pos * a.I_pad + n] = __float2half_rn(0.0f);
-                if ((n & 15) == 0) a.hs[(size_t)pos * (a.I_pad / 16) + n / 16] = 0.0f;
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// down + weighted combine
-// ---------------------------------------------------------------------------
-constexpr int kDownRows = 32;   // two MMA tiles per work item
-
-template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) down_q2k_kernel(DecArgs a)
-{
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int grp = lane >> 2, c = lane & 3;
-    const uint32_t tile_bytes = (uint32_t)(kDownRows * a.dn_row);
-    Ring ring;
-    ring.stages = a.stages;
-    ring.stage_bytes = (tile_bytes + 127) / 128 * 128;
-    ring.data = smem;
-    float *red = reinterpret_cast<float *>(smem + (size_t)ring.stages * ring.stage_bytes);
-    float *obuf = red + kConsumers * NT * kTileM;                   // [A][32]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(obuf + (size_t)a.A * kDownRows);
-    ring.full = bars;
-    ring.empty = bars + ring.stages;
-    __shared__ int s_pabort, s_cabort, s_consumed, s_issued;   // as in the gate/up kernel
-
-    if (tid == 0) {
-        for (int s = 0; s < ring.stages; ++s) {
-            ptx::mbar_init(&ring.full[s], 1);
-            ptx::mbar_init(&ring.empty[s], kConsumers);
-        }
-        ptx::fence_mbar_init();
-        s_pabort = 0;
-        s_cabort = 0;
-        s_consumed = 0;
-        s_issued = 0;
-    }
-    __syncthreads();
-
-    // Routing finished before the gate/up kernel let this grid launch, so the
-    // expert list is final; h is not (consumers wait for it below).
-    const int n_act = *a.n_active;
-    const int n_items = a.H / kDownRows;
-    const int first = (int)((int64_t)blockIdx.x * n_items / gridDim.x);
-    const int last = (int)((int64_t)(blockIdx.x + 1) * n_items / gridDim.x);
-    const int total = (last - first) * n_act;     // (item, expert) stages
-
-    if (warp == kConsumers) {
-        if (lane == 0 && !a.stall) {
-            for (int q = 0; q < total; ++q) {
-                const int s = q % ring.stages;
-                if (q >= ring.stages &&
-                    !ptx::mbar_wait(&ring.empty[s], ((q / ring.stages) - 1) & 1, a.wait_ns)) {
-                    set_status(a.status, DS4G_ERR_TIMEOUT);
-                    s_pabort = 1;
-                    break;
-                }
-                if (*(volatile int *)&s_cabort) break;
-                const int item = first + q / n_act;
-                const int e = a.active[q % n_act];
-                const uint8_t *src = a.w_down + (size_t)e * a.dn_stride + (size_t)item * tile_bytes;
-                ptx::mbar_arrive_expect_tx(&ring.full[s], tile_bytes);
-                ptx::bulk_g2s(ring.stage(s), src, tile_bytes, &ring.full[s]);
-                s_issued = q + 1;
-            }
+        // tell the epilogue warp to stop
+        {
+            int &uses = rb ? uses1 : uses0;
+            if (uses > 0) named_sync(kBarJobEmpty + rb, kJobThreads);
+            if (tid == 0) jobs[rb].kind = kJobStop;
+            named_arrive(kBarJobFull + rb, kJobThreads);
         }
     } else {
-        ptx::grid_dep_wait();      // h from the gate/up kernel
-        const int mtile = warp >> 2, kw = warp & 3;
-        const float inv4c = 1.0f / (float)(1 << (2 * c));
-        for (int q = 0; q < total; ++q) {
-            const int s = q % ring.stages;
-            if (!ptx::mbar_wait(&ring.full[s], (q / ring.stages) & 1, a.wait_ns)) {
-                set_status(a.status, DS4G_ERR_TIMEOUT);
-                s_cabort = 1;
-            }
-            consumer_sync();
-            if (*(volatile int *)&s_cabort) break;
-            const int item = first + q / n_act;
-            const int jx = q % n_act;
-            const int e = a.active[jx];
-            const int seg0 = a.offsets[e], seg_n = a.offsets[e + 1] - seg0;
-            const uint8_t *st = ring.stage(s) + (size_t)mtile * kTileM * a.dn_row;
-            for (int c0 = 0; c0 < seg_n; c0 += NT) {
-                const int nt = min(NT, seg_n - c0);
-                float part[NT][2];
+        // ---------------- epilogue warp ----------------
+        for (int rb = 0;; rb ^= 1) {
+            named_sync(kBarJobFull + rb, kJobThreads);
+            const Job jb = jobs[rb];
+            if (jb.kind == kJobStop) break;
+            const float *rbuf = red + rb * kConsumers * NT * kTileM;
+            if (jb.kind == kJobGateUp) {
+                const int tiles_e = tiles;
+                for (int base = 0; base < jb.nt * kTileM; base += 32) {
+                    const int i = base + lane;
+                    const bool valid = i < jb.nt * kTileM;
+                    const int row = i & 15, j = valid ? i >> 4 : 0;
+                    float g = 0.0f, uu = 0.0f;
+                    // warps with (warp >> 1) & 1 == 0 hold gate, the others up
 #pragma unroll
-                for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
-                for (int kb = kw; kb < a.I_blocks; kb += 4) {
-                    const uint8_t *b0 = st + (size_t)grp * a.dn_row + kb * kQ2KBytes;
-                    const uint8_t *b1 = b0 + 8 * a.dn_row;
-                    const uint32_t dd0 = ptx::lds32(b0 + 80), dd1 = ptx::lds32(b1 + 80);
-                    float S[NT][2], M[NT][2];
+                    for (int w = 0; w < kConsumers; ++w) {
+                        const float v = rbuf[((size_t)w * NT + j) * kTileM + row];
+                        if ((w >> 1) & 1) uu += v; else g += v;
+                    }
+                    const __half hv = __float2half_rn(silu_mul(g, uu));
+                    const int pos = jb.seg0 + jb.c0 + j;
+                    const int n = jb.mt * kTileM + row;
+                    float hsum = valid ? __half2float(hv) : 0.0f;
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) S[j][0] = S[j][1] = M[j][0] = M[j][1] = 0.0f;
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        HalfA ha;
-                        build_half_a(ha, b0, b1, h, c);
-                        const uint32_t sb0 = *reinterpret_cast<const uint16_t *>(b0 + 8 * h + 2 * c);
-                        const uint32_t sb1 = *reinterpret_cast<const uint16_t *>(b1 + 8 * h + 2 * c);
-                        const float sc00 = nib_lo(sb0), sc01 = nib_lo(sb0 >> 8);
-                        const float mn00 = nib_hi(sb0), mn01 = nib_hi(sb0 >> 8);
-                        const float sc10 = nib_lo(sb1), sc11 = nib_lo(sb1 >> 8);
-                        const float mn10 = nib_hi(sb1), mn11 = nib_hi(sb1 >> 8);
-#pragma unroll
-                        for (int j = 0; j < NT; ++j) {
-                            if (j < nt) {
-                                const int pos = seg0 + c0 + j;
-                                const __half *hh = a.hp + (size_t)pos * a.I_pad + kb * kQK + 128 * h;
-                                const float *hsh = a.hs + (size_t)pos * (a.I_pad / 16) + kb * 16 + 8 * h;
-                                float d[4], x0, x1;
-                                half_mma(ha, hh, hsh, grp, c, d, x0, x1);
-                                S[j][0] += sc00 * d[0] + sc01 * d[1];
-                                S[j][1] += sc10 * d[2] + sc11 * d[3];
-                                M[j][0] += mn00 * x0 + mn01 * x1;
-                                M[j][1] += mn10 * x0 + mn11 * x1;
+                    for (int o = 8; o > 0; o >>= 1) hsum += __shfl_xor_sync(0xffffffffu, hsum, o);
+                    if (valid) {
+                        a.hp[(size_t)pos * a.I_pad + perm4(n)] = hv;
+                        if (row == 0) a.hs[(size_t)pos * (a.I_pad / 16) + jb.mt] = hsum;
+                        // rows inter .. I_pad-1 of h (the down projection's padded K) are 0
+                        if (jb.mt == tiles_e - 1)
+                            for (int n2 = a.I + row; n2 < a.I_pad; n2 += kTileM) {
+                                a.hp[(size_t)pos * a.I_pad + n2] = __float2half_rn(0.0f);
+                                if ((n2 & 15) == 0) a.hs[(size_t)pos * (a.I_pad / 16) + n2 / 16] = 0.0f;
                             }
-                        }
-                    }
-                    const float d0 = half_bits(dd0 & 0xFFFFu) * inv4c, dm0 = half_bits(dd0 >> 16);
-                    const float d1 = half_bits(dd1 & 0xFFFFu) * inv4c, dm1 = half_bits(dd1 >> 16);
-#pragma unroll
-                    for (int j = 0; j < NT; ++j) {
-                        part[j][0] += d0 * S[j][0] - dm0 * M[j][0];
-                        part[j][1] += d1 * S[j][1] - dm1 * M[j][1];
                     }
                 }
-                float *rw = red + (size_t)warp * NT * kTileM;
-#pragma unroll
-                for (int j = 0; j < NT; ++j)
-#pragma unroll
-                    for (int r = 0; r < 2; ++r) {
-                        float v = part[j][r];
-                        v += __shfl_xor_sync(0xffffffffu, v, 1);
-                        v += __shfl_xor_sync(0xffffffffu, v, 2);
-                        if (c == 0) rw[j * kTileM + grp + 8 * r] = v;
-                    }
-                consumer_sync();
-                if (tid < nt * kDownRows) {
-                    const int row = tid & 31, j = tid >> 5;
-                    const int mt = row >> 4, r16 = row & 15;
+                // publish: every value of h counts once toward its expert's total
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) atomicAdd(done + jb.e, jb.nt * kTileM);
+            } else {
+                for (int j = 0; j < jb.nt; ++j) {
+                    const int row = lane, mtl = row >> 4, r16 = row & 15;
+                    // warps with (warp >> 1) & 1 == mtl hold rows mtl*16 .. +15
                     float o = 0.0f;
-                    for (int w = 0; w < 4; ++w) o += red[((size_t)(4 * mt + w) * NT + j) * kTileM + r16];
-                    obuf[(size_t)(seg0 + c0 + j) * kDownRows + row] = o;
+#pragma unroll
+                    for (int w = 0; w < kConsumers; ++w)
+                        if (((w >> 1) & 1) == mtl) o += rbuf[((size_t)w * NT + j) * kTileM + r16];
+                    obuf[(size_t)(jb.seg0 + jb.c0 + j) * kDownRows + row] = o;
                 }
-                consumer_sync();
-            }
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&ring.empty[s]);
-            if (tid == 0) s_consumed = q + 1;
-            // after the item's last expert: weighted combine in slot order
-            if (jx == n_act - 1) {
-                consumer_sync();
-                for (int i = tid; i < a.T * kDownRows; i += kConsumers * 32) {
-                    const int t = i / kDownRows, row = i % kDownRows;
-                    float acc = 0.0f;
-                    for (int sl = 0; sl < a.k; ++sl) {
-                        const int asg = t * a.k + sl;
-                        acc += a.wts[asg] * obuf[(size_t)a.slot_pos[asg] * kDownRows + row];
+                if (jb.last) {
+                    // every expert of this item is in obuf: weighted combine in slot order
+                    __syncwarp();
+                    for (int i = lane; i < a.T * kDownRows; i += 32) {
+                        const int t = i / kDownRows, row = i % kDownRows;
+                        float acc = 0.0f;
+                        for (int sl = 0; sl < a.k; ++sl) {
+                            const int asg = t * a.k + sl;
+                            acc += rs.wts[asg] * obuf[(size_t)rs.slot[asg] * kDownRows + row];
+                        }
+                        a.y[(size_t)t * a.H + (size_t)jb.item * kDownRows + row] = acc;
                     }
-                    a.y[(size_t)t * a.H + (size_t)item * kDownRows + row] = acc;
+                    __syncwarp();
                 }
-                consumer_sync();
             }
+            named_arrive(kBarJobEmpty + rb, kJobThreads);
         }
     }
     __syncthreads();
-    if (tid == kConsumers * 32 && (s_pabort || s_cabort)) {
+    // after an abort: the copies this CTA issued land before it exits
+    if (tid == kProducerWarp * 32 && (s_pabort || s_cabort)) {
         for (int q = s_consumed; q < s_issued; ++q) {
-            const int s = q % ring.stages;
-            if (!ptx::mbar_wait(&ring.full[s], (q / ring.stages) & 1, a.wait_ns)) break;
+            const int s = q % a.stages;
+            if (!ptx::mbar_wait(&full[s], (q / a.stages) & 1, a.wait_ns)) break;
         }
     }
 }
 
-size_t gateup_smem(const DecArgs &a, int nt)
+// Row pitch of a weight tile in shared memory.  Lane groups read rows grp
+// and grp+8 (grp = 0..7) at the same column: a pitch of a multiple of 32
+// bytes would put several groups on one bank, so such rows get 16 bytes of
+// padding (copied row by row; only possible for rows of a multiple of 16
+// bytes, the others are copied whole).
+int64_t smem_pitch(int64_t row_bytes)
 {
-    const size_t stage = ((size_t)2 * kTileM * a.gu_row + 127) / 128 * 128;
-    return stage * a.stages + (size_t)kConsumers * 2 * nt * kTileM * 4 + 2 * a.stages * 8;
+    if (row_bytes % 16 == 0 && (row_bytes / 4) % 8 == 0) return row_bytes + 16;
+    return row_bytes;
 }
 
-size_t down_smem(const DecArgs &a, int nt)
+size_t fixed_smem(const DecArgs &a, int nt)
 {
-    const size_t stage = ((size_t)kDownRows * a.dn_row + 127) / 128 * 128;
-    return stage * a.stages + (size_t)kConsumers * nt * kTileM * 4 + (size_t)a.A * kDownRows * 4 +
-           2 * a.stages * 8;
+    const size_t x = a.x_smem ? (size_t)a.T * a.H * 2 + (size_t)a.T * (a.H / 16) * 4 : 0;
+    return x + (size_t)2 * kConsumers * nt * kTileM * 4 + (size_t)a.A * kDownRows * 4 +
+           4 * (size_t)kTagWords * a.stages + 8 * (2 * (size_t)a.stages);
 }
 
-template <typename K>
-cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t s, const DecArgs &a)
+template <int NT>
+cudaError_t launch_nt(DecArgs a, const DeviceInfo &dev, cudaStream_t s, const cudaEvent_t *ev)
 {
-    // the opt-in limit covers static + dynamic shared memory, so ask for the
-    // dynamic bytes this launch needs
-    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
+    const size_t gu = (size_t)2 * kTileM * a.gu_pitch, dn = (size_t)kDownRows * a.dn_pitch;
+    a.stage_bytes = (uint32_t)((std::max(gu, dn) + 127) / 128 * 128);
+    const size_t budget = std::min(kSmemBudget, (size_t)dev.max_smem_optin - 1024) -
+                          sizeof(RouteSmem) - 256;
+    a.stages = 8;
+    while (a.stages > 2 && (size_t)a.stages * a.stage_bytes + fixed_smem(a, NT) > budget) --a.stages;
+    if ((size_t)a.stages * a.stage_bytes + fixed_smem(a, NT) > budget) return cudaErrorInvalidValue;
+    const size_t smem = (size_t)a.stages * a.stage_bytes + fixed_smem(a, NT);
+    cudaError_t e = cudaFuncSetAttribute(decode_q2k_kernel<NT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(grid);
+    cfg.gridDim = dim3(dev.sm_count);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -558,37 +796,12 @@ cudaError_t launch_pdl(K kernel, int grid, size_t smem, cudaStream_t s, const De
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, a);
-}
-
-// Shared memory per SM is split so that a gate/up CTA and a down CTA can be
-// resident together (the down CTA streams W_down while gate/up computes).
-constexpr size_t kGateUpBudget = 132 * 1024;
-constexpr size_t kDownBudget = 90 * 1024;
-
-
-template <int NT>
-cudaError_t launch_nt(DecArgs a, const DeviceInfo &dev, cudaStream_t s, const cudaEvent_t *ev)
-{
-    const size_t budget = (size_t)dev.max_smem_optin - 1024;   // static shared memory
-    a.stages = 4;
-    while (a.stages > 2 && gateup_smem(a, NT) > kGateUpBudget) --a.stages;
-    if (gateup_smem(a, NT) > budget) return cudaErrorInvalidValue;
-    const int gu_items = min(a.E, a.A) * (a.I / kTileM);
-    int grid = min(dev.sm_count, gu_items);
-    cudaError_t e = launch_pdl(gateup_q2k_kernel<NT>, grid, gateup_smem(a, NT), s, a);
+    e = cudaLaunchKernelEx(&cfg, decode_q2k_kernel<NT>, a);
     if (e != cudaSuccess) return e;
-    if (ev && (e = record_phase(ev[2], s)) != cudaSuccess) return e;
-    DecArgs b = a;
-    b.stages = 6;
-    while (b.stages > 2 && down_smem(b, NT) > kDownBudget) --b.stages;
-    if (down_smem(b, NT) > budget) return cudaErrorInvalidValue;
-    grid = min(dev.sm_count, a.H / kDownRows);
-    e = launch_pdl(down_q2k_kernel<NT>, grid, down_smem(b, NT), s, b);
-    if (e != cudaSuccess) return e;
+    // one kernel covers the whole layer: the gate/up, down and combine marks coincide
     if (ev) {
-        if ((e = record_phase(ev[3], s)) != cudaSuccess) return e;
-        if ((e = record_phase(ev[4], s)) != cudaSuccess) return e;
+        for (int i = 2; i <= 4; ++i)
+            if ((e = record_phase(ev[i], s)) != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }
@@ -600,11 +813,13 @@ bool decode_path_supported(const Plan &p, const ds4g_moe_desc *d)
     if (d->format != DS4G_FMT_Q2K || p.T > kDecodeMaxT || p.I % kTileM != 0 ||
         p.H % kDownRows != 0)
         return false;
-    // two ring stages of each kernel must fit in shared memory
-    const size_t gu = 2 * (((size_t)2 * kTileM * d->gate_up_row_bytes + 127) / 128 * 128);
-    const size_t dn = 2 * (((size_t)kDownRows * d->down_row_bytes + 127) / 128 * 128) +
-                      (size_t)p.A * kDownRows * 4;
-    return gu + 16 * 1024 <= 200 * 1024 && dn + 16 * 1024 <= 200 * 1024;
+    // two ring stages and the fixed buffers must fit in shared memory
+    const size_t gu = (size_t)2 * kTileM * smem_pitch(d->gate_up_row_bytes);
+    const size_t dn = (size_t)kDownRows * smem_pitch(d->down_row_bytes);
+    const size_t stage = (std::max(gu, dn) + 127) / 128 * 128;
+    const size_t fixed = (size_t)2 * kConsumers * 4 * kTileM * 4 + (size_t)p.A * kDownRows * 4 +
+                         sizeof(RouteSmem) + 1024;
+    return 2 * stage + fixed <= kSmemBudget;
 }
 
 cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const DeviceInfo &dev,
@@ -619,6 +834,7 @@ cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const 
     a.k = la.k;
     a.T = la.T;
     a.A = la.A;
+    a.score = db.score;
     a.H_blocks = la.H / kQK;
     a.I_blocks = la.I_pad / kQK;
     a.w_gate = la.w_gate;
@@ -628,24 +844,42 @@ cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const 
     a.dn_row = la.dn_row;
     a.gu_stride = la.gu_stride;
     a.dn_stride = la.dn_stride;
-    a.wts = la.wts;
-    a.offsets = la.offsets;
-    a.perm = la.perm;
-    a.slot_pos = la.slot_pos;
-    a.active = la.active;
-    a.n_active = la.n_active;
+    a.gu_pitch = (int)smem_pitch(la.gu_row);
+    a.dn_pitch = (int)smem_pitch(la.dn_row);
+    a.logits = db.logits;
+    a.x = la.x;
     a.xp = db.xp;
     a.xs = db.xs;
     a.hp = db.hp;
     a.hs = db.hs;
     a.y = la.y;
+    a.ids = db.ids;
+    a.wts = const_cast<float *>(la.wts);
+    a.counts = const_cast<int32_t *>(la.counts);
+    a.offsets = const_cast<int32_t *>(la.offsets);
+    a.perm = const_cast<int32_t *>(la.perm);
     a.status = db.status;
+    a.sync = db.sync;
     a.wait_ns = wait_ns;
     a.stall = stall ? 1 : 0;
+    const size_t xb = (size_t)a.T * a.H * 2 + (size_t)a.T * (a.H / 16) * 4;
+    a.x_smem = xb <= kXStageMax ? 1 : 0;
+
+    // counters and status reset; activation conversion when it does not fit
+    const size_t groups = (size_t)a.T * (a.H / 4);
+    const int pre_grid = a.x_smem ? 1 : (int)std::min<size_t>((groups + 255) / 256, (size_t)dev.sm_count * 4);
+    decode_pre_kernel<<<pre_grid, 256, 0, s>>>(db.status, db.sync, kSyncWords + a.E,
+                                               a.x_smem ? nullptr : la.x,
+                                               const_cast<__half *>(db.xp),
+                                               const_cast<float *>(db.xs), groups);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (events && (e = record_phase(events[1], s)) != cudaSuccess) return e;
+
+    // token chunk per pass: segments longer than 4 run in several chunks
     if (la.T <= 1) return launch_nt<1>(a, dev, s, events);
     if (la.T <= 2) return launch_nt<2>(a, dev, s, events);
-    if (la.T <= 4) return launch_nt<4>(a, dev, s, events);
-    return launch_nt<8>(a, dev, s, events);
+    return launch_nt<4>(a, dev, s, events);
 }
 
 }  // namespace ds4g

@@ -114,6 +114,7 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     q.active = take((size_t)q.E * 4);
     q.meta = take(kMetaWords * 4);
     q.status = take(4);
+    q.sync = take((size_t)(kSyncWords + q.E) * 4);
     q.xp = take((size_t)T * q.H * 2);
     q.xs = take((size_t)T * (q.H / 16) * 4);
     q.hp = take(A * q.I_pad * 2);
@@ -173,15 +174,18 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     int32_t *active = reinterpret_cast<int32_t *>(ws + p.active);
     int32_t *meta = reinterpret_cast<int32_t *>(ws + p.meta);
     int32_t *status = reinterpret_cast<int32_t *>(ws + p.status);
+    int32_t *sync = reinterpret_cast<int32_t *>(ws + p.sync);
     __half *xp = reinterpret_cast<__half *>(ws + p.xp);
     float *xs = reinterpret_cast<float *>(ws + p.xs);
     const Path path = choose_path(d, p);
     if (path == Path::kTensorCore && !tc_path_supported(p, d)) return DS4G_ERR_UNSUPPORTED;
     const bool decode = path == Path::kDecode;
     if (pe.mark(0, s) != cudaSuccess) return DS4G_ERR_CUDA;
-    cudaError_t e = launch_route(logits, p.T, p.E, p.k, d->score, ids, wts, counts, offsets, perm,
-                                 slot_pos, active, meta + kMetaActive, decode ? x : nullptr, p.H,
-                                 xp, xs, status, s);
+    cudaError_t e = cudaSuccess;
+    if (!decode)
+        e = launch_route(logits, p.T, p.E, p.k, d->score, ids, wts, counts, offsets, perm,
+                         slot_pos, active, meta + kMetaActive, nullptr, p.H,
+                         xp, xs, status, nullptr, 0, s);
     if (e != cudaSuccess) return from_cuda(e);
     LayerArgs a{};
     a.H = p.H;
@@ -216,10 +220,10 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     // the activation gather of the tensor-core path belongs to the routing phase
     if (path == Path::kTensorCore && (e = launch_tc_prep(a, tb, dev, s)) != cudaSuccess)
         return from_cuda(e);
-    if (pe.mark(1, s) != cudaSuccess) return DS4G_ERR_CUDA;
+    if (!decode && pe.mark(1, s) != cudaSuccess) return DS4G_ERR_CUDA;
     if (decode) {
-        DecodeBufs b{xp, xs, reinterpret_cast<__half *>(ws + p.hp),
-                     reinterpret_cast<float *>(ws + p.hs), status};
+        DecodeBufs b{logits, ids, d->score, xp, xs, reinterpret_cast<__half *>(ws + p.hp),
+                     reinterpret_cast<float *>(ws + p.hs), status, sync};
         const bool stall = (d->flags & DS4G_DEBUG_STALL) != 0;
         return from_cuda(launch_decode_path(a, b, dev, s, pe.on ? pe.ev : nullptr,
                                             stall ? kStallWaitNs : kWaitNs, stall));
@@ -265,7 +269,7 @@ ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, int32_t k
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return from_cuda(launch_route(logits, T, E, k, score, ids, weights, counts, offsets, perm,
                                   nullptr, nullptr, nullptr, nullptr, 0, nullptr, nullptr, nullptr,
-                                  s));
+                                  nullptr, 0, s));
 }
 
 ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out, int32_t out_dtype,
@@ -337,7 +341,8 @@ int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T)
     Plan p;
     if (T <= 0 || make_plan(desc, T, &p) != DS4G_OK) return 0;
     const Path path = choose_path(desc, p);
-    return route_launches(T) + (path == Path::kDecode       ? 2
+    if (path == Path::kDecode) return 2;     // reset/convert, fused layer kernel
+    return route_launches(T) + (path == Path::kDecode       ? 0
                                 : path == Path::kTensorCore ? kTcPathLaunches
                                                             : gemv_path_launches(p));
 }

@@ -27,6 +27,7 @@ struct Plan {
     int32_t block_bytes;    // 84 or 70
     size_t ids, wts, counts, offsets, perm, slot_pos, active, meta;
     size_t status;          // int32 device status word (DS4G_OK or DS4G_ERR_TIMEOUT)
+    size_t sync;            // [kSyncWords + E] int32 counters of the decode kernel
     size_t xp, xs;          // [T x H] fp16 activations (4-group permuted), [T x H/16] sums
     size_t hp, hs;          // [A x I_pad] fp16 h (4-group permuted), [A x I_pad/16] sums
     size_t hbuf;            // [A x I_pad] fp32: SiLU(g)*u per assignment (segment order)
@@ -57,12 +58,12 @@ ds4g_status device_info(DeviceInfo *out);
 // ---------------------------------------------------------------------------
 // Routing; optionally (x != nullptr) also the activation prep of the decode
 // path: xp = fp16(x) in 4-group permuted order, xs = fp32 sums of 16.
-// Writes *status = DS4G_OK first (status nullable).
+// Writes *status = DS4G_OK first (status nullable) and zeroes sync[0 .. n_sync).
 cudaError_t launch_route(const float *logits, int T, int E, int k, int score,
                          int32_t *ids, float *wts, int32_t *counts, int32_t *offsets,
                          int32_t *perm, int32_t *slot_pos, int32_t *active,
                          int32_t *n_active, const uint16_t *x, int H, __half *xp, float *xs,
-                         int32_t *status, cudaStream_t s);
+                         int32_t *status, int32_t *sync, int n_sync, cudaStream_t s);
 
 cudaError_t launch_q2k_dequant(const uint8_t *blocks, int64_t n_blocks, void *out, int dtype,
                                cudaStream_t s);
@@ -104,15 +105,22 @@ inline cudaError_t record_phase(cudaEvent_t ev, cudaStream_t s)
 // T at or below which routing runs as one single-CTA launch.
 constexpr int kRouteSmallT = 64;
 
-// Decode path (decode.cu): T <= kDecodeMaxT, Q2_K, inter % 16 == 0.
+// Decode path (decode.cu): T <= kDecodeMaxT, Q2_K, inter % 16 == 0.  Two
+// launches: a reset/conversion kernel and the fused layer kernel, which
+// routes by itself (events[1] after the first, events[2..4] after the second).
 constexpr int kDecodeMaxT = 32;
 struct DecodeBufs {
-    const __half *xp;
+    const float *logits;    // [T x E]
+    int32_t *ids;           // routing outputs of the call (the kernel routes by itself)
+    int score;
+    const __half *xp;       // [T x H] fp16 activations when they do not fit on chip
     const float *xs;
     __half *hp;
     float *hs;
     int32_t *status;
+    int32_t *sync;          // [kSyncWords + E] claim and completion counters
 };
+constexpr int kSyncWords = 4;
 bool decode_path_supported(const Plan &p, const ds4g_moe_desc *d);
 cudaError_t launch_decode_path(const LayerArgs &a, const DecodeBufs &b, const DeviceInfo &dev,
                                cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns,

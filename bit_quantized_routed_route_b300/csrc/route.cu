@@ -22,78 +22,10 @@
 // order (0, 2, 1, 3), and xs = fp32 sums of each 16 consecutive fp16 values.
 #include "ds4g_common.cuh"
 #include "ptx.cuh"
+#include "topk.cuh"
 
 namespace ds4g {
 namespace {
-
-constexpr int kMaxPerLane = 8;   // 256 experts / 32 lanes
-
-__device__ __forceinline__ float canon(float v) { return v != v ? -INFINITY : v; }
-
-// a ranks before b
-__device__ __forceinline__ bool before(float va, int ia, float vb, int ib)
-{
-    return ib < 0 || (ia >= 0 && (va > vb || (va == vb && ia < ib)));
-}
-
-// One token, one warp.  Writes ids[k], wts[k] (lane 0).
-__device__ __forceinline__ void topk_warp(const float *__restrict__ row, int E, int k, int score,
-                                          int32_t *__restrict__ ids, float *__restrict__ wts)
-{
-    const int lane = threadIdx.x & 31;
-    float v[kMaxPerLane];
-    uint32_t avail = 0;
-#pragma unroll
-    for (int j = 0; j < kMaxPerLane; ++j) {
-        int e = lane + 32 * j;
-        v[j] = -INFINITY;
-        if (e < E) {
-            v[j] = canon(__ldg(row + e));
-            avail |= 1u << j;
-        }
-    }
-    float sel_v[DS4G_MAX_TOPK];
-    int sel_i[DS4G_MAX_TOPK];
-#pragma unroll
-    for (int i = 0; i < DS4G_MAX_TOPK; ++i) {
-        if (i >= k) break;
-        float bv = -INFINITY;
-        int bi = -1;
-#pragma unroll
-        for (int j = 0; j < kMaxPerLane; ++j) {
-            if ((avail >> j) & 1u) {
-                int e = lane + 32 * j;
-                if (before(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-        sel_v[i] = bv;
-        sel_i[i] = bi;
-    }
-    if (lane == 0) {
-        float p[DS4G_MAX_TOPK];
-        float sum = 0.0f;
-        if (score == DS4G_SCORE_SOFTMAX) {
-            float m = sel_v[0];
-#pragma unroll
-            for (int i = 0; i < DS4G_MAX_TOPK; ++i)
-                if (i < k) { p[i] = expf(sel_v[i] - m); sum += p[i]; }
-        } else {
-#pragma unroll
-            for (int i = 0; i < DS4G_MAX_TOPK; ++i)
-                if (i < k) { p[i] = 1.0f / (1.0f + expf(-sel_v[i])); sum += p[i]; }
-        }
-#pragma unroll
-        for (int i = 0; i < DS4G_MAX_TOPK; ++i)
-            if (i < k) { ids[i] = sel_i[i]; wts[i] = p[i] / sum; }
-    }
-}
 
 // Four activations x[4g..4g+3] -> fp16, stored permuted (0,2,1,3); returns
 // their fp32 sum.
@@ -126,9 +58,11 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
                                                    float *__restrict__ wts,
                                                    const uint16_t *__restrict__ x, int H,
                                                    __half *__restrict__ xp, float *__restrict__ xs,
-                                                   int32_t *status)
+                                                   int32_t *status, int32_t *sync, int n_sync)
 {
     if (status && blockIdx.x == 0 && threadIdx.x == 0) *status = DS4G_OK;
+    if (blockIdx.x == 0)
+        for (int i = threadIdx.x; i < n_sync; i += blockDim.x) sync[i] = 0;
     int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (t >= T) return;
     topk_warp(logits + (size_t)t * E, E, k, score, ids + (size_t)t * k, wts + (size_t)t * k);
@@ -138,20 +72,22 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
     }
 }
 
-// Shared state of the counting sort (one CTA of 1024 threads = 32 warps).
+// Shared state of the counting sort (one CTA of NW >= 8 warps).
+template <int NW>
 struct ScanSmem {
     int count[DS4G_MAX_EXPERTS];
     int offset[DS4G_MAX_EXPERTS + 1];
     int running[DS4G_MAX_EXPERTS];
-    int warp_base[32][DS4G_MAX_EXPERTS];
+    int warp_base[NW][DS4G_MAX_EXPERTS];
     int warp_sum[8];
     int act_sum[8];
 };
 
 // counts / offsets / perm / slot_pos / active from ids[A].  Called by all
-// 1024 threads of the CTA.  `ids` may have been written earlier in the same
+// NW * 32 threads of the CTA.  `ids` may have been written earlier in the same
 // kernel, so it is read through the coherent path (no __restrict__).
-__device__ void scan_body(ScanSmem &sm, const int32_t *ids, int A, int E,
+template <int NW>
+__device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
                           int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
                           int32_t *active, int32_t *n_active)
 {
@@ -208,7 +144,7 @@ __device__ void scan_body(ScanSmem &sm, const int32_t *ids, int A, int E,
     __syncthreads();
     // stable placement, 1024 assignments per round
     for (int base = 0; base < A; base += blockDim.x) {
-        for (int i = tid; i < 32 * DS4G_MAX_EXPERTS; i += blockDim.x)
+        for (int i = tid; i < NW * DS4G_MAX_EXPERTS; i += blockDim.x)
             (&sm.warp_base[0][0])[i] = 0;
         __syncthreads();
         int a = base + tid;
@@ -220,7 +156,7 @@ __device__ void scan_body(ScanSmem &sm, const int32_t *ids, int A, int E,
         __syncthreads();
         if (tid < E) {
             int run = sm.running[tid];
-            for (int w = 0; w < 32; ++w) {
+            for (int w = 0; w < NW; ++w) {
                 int cnt = sm.warp_base[w][tid];
                 sm.warp_base[w][tid] = run;
                 run += cnt;
@@ -242,21 +178,23 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t *ids, int A, i
                                                     int32_t *perm, int32_t *slot_pos,
                                                     int32_t *active, int32_t *n_active)
 {
-    __shared__ ScanSmem sm;
-    scan_body(sm, ids, A, E, counts, offsets, perm, slot_pos, active, n_active);
+    __shared__ ScanSmem<32> sm;
+    scan_body<32>(sm, ids, A, E, counts, offsets, perm, slot_pos, active, n_active);
 }
 
-// Small T: top-k by the 32 warps of the CTA, then the scan, one launch.
-__global__ void __launch_bounds__(1024) route_small_kernel(
+// Small T: top-k by the 8 warps of the CTA, then the scan, one launch.
+constexpr int kSmallWarps = 8;
+__global__ void __launch_bounds__(kSmallWarps * 32) route_small_kernel(
     const float *__restrict__ logits, int T, int E, int k, int score, int32_t *ids, float *wts,
     int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos, int32_t *active,
     int32_t *n_active, const uint16_t *__restrict__ x, int H, __half *__restrict__ xp,
-    float *__restrict__ xs, int32_t *status)
+    float *__restrict__ xs, int32_t *status, int32_t *sync, int n_sync)
 {
-    __shared__ ScanSmem sm;
+    __shared__ ScanSmem<kSmallWarps> sm;
     ptx::grid_dep_launch();    // the consumer kernels may become resident and wait
     if (status && threadIdx.x == 0) *status = DS4G_OK;
-    for (int t = threadIdx.x >> 5; t < T; t += 32)
+    for (int i = threadIdx.x; i < n_sync; i += blockDim.x) sync[i] = 0;
+    for (int t = threadIdx.x >> 5; t < T; t += kSmallWarps)
         topk_warp(logits + (size_t)t * E, E, k, score, ids + (size_t)t * k, wts + (size_t)t * k);
     if (x) {
         const size_t groups = (size_t)T * (H / 4);
@@ -264,7 +202,7 @@ __global__ void __launch_bounds__(1024) route_small_kernel(
     }
     __threadfence_block();
     __syncthreads();
-    scan_body(sm, ids, T * k, E, counts, offsets, perm, slot_pos, active, n_active);
+    scan_body<kSmallWarps>(sm, ids, T * k, E, counts, offsets, perm, slot_pos, active, n_active);
 }
 
 }  // namespace
@@ -273,16 +211,16 @@ cudaError_t launch_route(const float *logits, int T, int E, int k, int score, in
                          float *wts, int32_t *counts, int32_t *offsets, int32_t *perm,
                          int32_t *slot_pos, int32_t *active, int32_t *n_active,
                          const uint16_t *x, int H, __half *xp, float *xs, int32_t *status,
-                         cudaStream_t s)
+                         int32_t *sync, int n_sync, cudaStream_t s)
 {
     if (T <= kRouteSmallT) {
-        route_small_kernel<<<1, 1024, 0, s>>>(logits, T, E, k, score, ids, wts, counts, offsets,
+        route_small_kernel<<<1, kSmallWarps * 32, 0, s>>>(logits, T, E, k, score, ids, wts, counts, offsets,
                                              perm, slot_pos, active, n_active, x, H, xp, xs,
-                                             status);
+                                             status, sync, n_sync);
     } else {
         int warps = 8;
         topk_kernel<<<(T + warps - 1) / warps, 32 * warps, 0, s>>>(logits, T, E, k, score, ids,
-                                                                  wts, x, H, xp, xs, status);
+                                                                  wts, x, H, xp, xs, status, sync, n_sync);
         scan_kernel<<<1, 1024, 0, s>>>(ids, T * k, E, counts, offsets, perm, slot_pos, active,
                                        n_active);
     }

@@ -30,7 +30,7 @@ CASES = [
 def test_decode_path(orc, kw):
     layer = P.small_layer(seed=kw["H"] + kw["I"] + kw["T"], **kw)
     L = to_device(layer)
-    assert D.moe_forward_launches(L.desc, kw["T"]) == 3        # routing, gate/up, down
+    assert D.moe_forward_launches(L.desc, kw["T"]) == 2        # routing, fused decode kernel
     y, routing = run_forward(L, layer["x"], layer["logits"])
     check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
     yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
@@ -45,9 +45,9 @@ def test_decode_is_deterministic():
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
 
 
-def test_decode_matches_general_path_closely(orc):
-    """The CUDA-core general path (fp32 weights) and the tensor-core decode
-    path agree with each other to the same tolerance."""
+def test_decode_matches_tensor_core_path_closely(orc):
+    """The tcgen05 path (forced) and the mma.sync decode path agree with each
+    other to the same tolerance."""
     layer = P.small_layer(seed=9, H=2048, I=768, E=12, k=3, T=4, align=16)
     y_dec, _ = run_forward(to_device(layer), layer["x"], layer["logits"])
     y_gen, _ = run_forward(to_device(layer, flags=D.FORCE_TC), layer["x"], layer["logits"])
