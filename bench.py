@@ -179,14 +179,15 @@ def tensor_peaks():
 
 def layer_path(cfg: S.Config) -> str:
     """Which kernels the library runs for this workload (mirrors its choice:
-    decode kernels up to 32 tokens for Q2_K, tensor-core kernels above that
-    for Q2_K with 16-byte rows, the general kernels otherwise)."""
-    if cfg.format == S.FMT_Q2K and cfg.tokens <= 32 and cfg.inter % 16 == 0:
+    decode kernels up to 8 tokens for Q2_K (up to 32 when the rows are not a
+    multiple of 16 bytes), tensor-core kernels for Q2_K with 16-byte rows
+    above that, the general kernels otherwise)."""
+    tc = (cfg.format == S.FMT_Q2K and cfg.row_bytes(cfg.hidden) % 16 == 0
+          and cfg.row_bytes(cfg.inter) % 16 == 0)
+    if (cfg.format == S.FMT_Q2K and cfg.inter % 16 == 0
+            and (cfg.tokens <= 8 or (cfg.tokens <= 32 and not tc))):
         return "decode"
-    if (cfg.format == S.FMT_Q2K and cfg.row_bytes(cfg.hidden) % 16 == 0
-            and cfg.row_bytes(cfg.inter) % 16 == 0):
-        return "tc"
-    return "general"
+    return "tc" if tc else "general"
 
 
 def kernel_source_hash() -> str:

@@ -86,13 +86,28 @@ struct HalfA {
     uint32_t a[8][4];
 };
 
-__device__ __forceinline__ void build_half_a(HalfA &ha, const uint8_t *blk0, const uint8_t *blk1,
-                                             int h, int c)
+// Lane constants of build_half_a: the two bit-field masks and the qs byte
+// offset of this lane's 16 weights.
+struct LaneA {
+    uint32_t m1, m2;
+    int off;
+};
+
+__device__ __forceinline__ LaneA lane_a(int h, int c)
 {
     const uint32_t g1 = (uint32_t)(c >> 1);
-    const uint32_t m1 = 0x00030003u << (2 * g1);          // field g1   -> sub-block c
-    const uint32_t m2 = 0x00030003u << (2 * (g1 + 2));    // field g1+2 -> sub-block c+4
-    const int off = 16 + 32 * h + 16 * (c & 1);
+    LaneA l;
+    l.m1 = 0x00030003u << (2 * g1);          // field g1   -> sub-block c
+    l.m2 = 0x00030003u << (2 * (g1 + 2));    // field g1+2 -> sub-block c+4
+    l.off = 16 + 32 * h + 16 * (c & 1);
+    return l;
+}
+
+__device__ __forceinline__ void build_half_a(HalfA &ha, const uint8_t *blk0, const uint8_t *blk1,
+                                             const LaneA &la)
+{
+    const uint32_t m1 = la.m1, m2 = la.m2;
+    const int off = la.off;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
         const uint32_t r0 = ptx::lds32(blk0 + off + 4 * w);
@@ -120,7 +135,7 @@ constexpr int kBarConsumers = 1, kBarJobFull = 2, kBarJobEmpty = 4;
 constexpr int kJobThreads = (kConsumers + 1) * 32;
 constexpr int kDownRows = 32;            // rows of H per down item (two MMA tiles)
 constexpr int kMaxDownPerStage = 8;
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kSmemBudget = 216 * 1024;     // dynamic shared memory of the decode kernel
 constexpr size_t kXStageMax = 48 * 1024;
 constexpr int kMaxAssign = kDecodeMaxT * DS4G_MAX_TOPK;     // 256
 
@@ -172,8 +187,9 @@ __device__ __forceinline__ void named_arrive(int id, int n) { asm volatile("bar.
 __device__ __forceinline__ void consumer_sync() { named_sync(kBarConsumers, kConsumers * 32); }
 
 // One epilogue job: the consumers' partial sums of one token chunk of one
-// tile sit in reduction buffer `rb`; the epilogue warp finishes it.
-enum { kJobStop = 0, kJobGateUp = 1, kJobDown = 2 };
+// gate/up tile sit in reduction buffer `rb`; the epilogue warp finishes it
+// (SiLU * up, the h stores, and publishing them to the down phase).
+enum { kJobStop = 0, kJobGateUp = 1 };
 struct Job {
     int kind, e, mt, seg0, c0, nt, item, last;
 };
@@ -253,14 +269,14 @@ __device__ __forceinline__ void half_mma_v(const HalfA &ha, const __half *xh, co
 // vector j's activations (its sums start at off[j] / 16).
 template <int NT, bool SHARED>
 __device__ __forceinline__ void tile_unit(const uint8_t *blk0, int64_t row_bytes, int h, int grp,
-                                          int c, float inv4c, const __half *xk, const float *sk,
-                                          const __half *zero, const uint32_t (&off)[NT], int nt,
-                                          float (&part)[NT][2])
+                                          int c, const LaneA &la, float inv4c, const __half *xk,
+                                          const float *sk, const __half *zero,
+                                          const uint32_t (&off)[NT], int nt, float (&part)[NT][2])
 {
     const uint8_t *blk1 = blk0 + 8 * row_bytes;
     const uint32_t dd0 = ptx::lds32(blk0 + 80), dd1 = ptx::lds32(blk1 + 80);
     HalfA ha;
-    build_half_a(ha, blk0, blk1, h, c);
+    build_half_a(ha, blk0, blk1, la);
     const uint32_t sb0 = *reinterpret_cast<const uint16_t *>(blk0 + 8 * h + 2 * c);
     const uint32_t sb1 = *reinterpret_cast<const uint16_t *>(blk1 + 8 * h + 2 * c);
     // d*sc and dmin*m per sub-block (columns 2c, 2c+1), rows grp and grp+8
@@ -278,6 +294,67 @@ __device__ __forceinline__ void tile_unit(const uint8_t *blk0, int64_t row_bytes
                                d, x0, x1);
             part[j][0] += s00 * d[0] + s01 * d[1] - (m00 * x0 + m01 * x1);
             part[j][1] += s10 * d[2] + s11 * d[3] - (m10 * x0 + m11 * x1);
+        }
+    }
+}
+
+// tile_unit with every operand in shared memory, addressed by 32-bit
+// shared-window addresses: `blk0` (block kb of row grp), `xk`/`sk` (the K
+// block's activations / sums), `zero` (32 zero bytes), `lut` (the
+// 256-entry {sc, m} table of scale bytes).  off[j]: element offset of vector
+// j's activations (its sums start at off[j] / 16).
+template <int NT>
+__device__ __forceinline__ void tile_unit_s(uint32_t blk0, uint32_t pitch, int h, int grp, int c,
+                                            const LaneA &la, float inv4c, uint32_t xk, uint32_t sk,
+                                            uint32_t zero, uint32_t lut, const uint32_t (&off)[NT],
+                                            int nt, float (&part)[NT][2])
+{
+    const uint32_t blk1 = blk0 + 8 * pitch;
+    const uint32_t dd0 = ptx::ld_s32(blk0 + 80), dd1 = ptx::ld_s32(blk1 + 80);
+    HalfA ha;
+    {
+        const uint32_t m1 = la.m1, m2 = la.m2;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const uint32_t r0 = ptx::ld_s32(blk0 + la.off + 4 * w);
+            const uint32_t r1 = ptx::ld_s32(blk1 + la.off + 4 * w);
+            const uint32_t r0h = r0 >> 8, r1h = r1 >> 8;
+            ha.a[2 * w][0] = ptx::lop3_and_or(r0, m1, 0x64006400u);
+            ha.a[2 * w][1] = ptx::lop3_and_or(r1, m1, 0x64006400u);
+            ha.a[2 * w][2] = ptx::lop3_and_or(r0, m2, 0x64006400u);
+            ha.a[2 * w][3] = ptx::lop3_and_or(r1, m2, 0x64006400u);
+            ha.a[2 * w + 1][0] = ptx::lop3_and_or(r0h, m1, 0x64006400u);
+            ha.a[2 * w + 1][1] = ptx::lop3_and_or(r1h, m1, 0x64006400u);
+            ha.a[2 * w + 1][2] = ptx::lop3_and_or(r0h, m2, 0x64006400u);
+            ha.a[2 * w + 1][3] = ptx::lop3_and_or(r1h, m2, 0x64006400u);
+        }
+    }
+    const uint32_t sb0 = ptx::ld_s16(blk0 + 8 * h + 2 * c), sb1 = ptx::ld_s16(blk1 + 8 * h + 2 * c);
+    const float2 q00 = ptx::ld_s64f(lut + 8 * (sb0 & 0xFFu)), q01 = ptx::ld_s64f(lut + 8 * (sb0 >> 8));
+    const float2 q10 = ptx::ld_s64f(lut + 8 * (sb1 & 0xFFu)), q11 = ptx::ld_s64f(lut + 8 * (sb1 >> 8));
+    const float d0 = half_bits(dd0 & 0xFFFFu) * inv4c, dm0 = half_bits(dd0 >> 16);
+    const float d1 = half_bits(dd1 & 0xFFFFu) * inv4c, dm1 = half_bits(dd1 >> 16);
+    const float s00 = d0 * q00.x, s01 = d0 * q01.x, m00 = dm0 * q00.y, m01 = dm0 * q01.y;
+    const float s10 = d1 * q10.x, s11 = d1 * q11.x, m10 = dm1 * q10.y, m11 = dm1 * q11.y;
+    const bool act = (grp & 3) == c, lo = grp < 4;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+        if (j < nt) {
+            const uint32_t xa = xk + 2 * (off[j] + 128 * h + 16 * grp);
+            const uint32_t p0 = act && lo ? xa : zero, p1 = act && !lo ? xa : zero;
+            const float2 xx = ptx::ld_s64f(sk + 4 * ((off[j] >> 4) + 8 * h + 2 * c));
+            const uint4 u0 = ptx::ld_s128(p0), u1 = ptx::ld_s128(p0 + 16);
+            const uint4 v0 = ptx::ld_s128(p1), v1 = ptx::ld_s128(p1 + 16);
+            const uint32_t b0[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            const uint32_t b1[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+            float d[4] = {-1024.0f * xx.x, -1024.0f * xx.y, -1024.0f * xx.x, -1024.0f * xx.y};
+#pragma unroll
+            for (int t = 0; t < 8; ++t) ptx::mma_16816(d, ha.a[t], b0[t], b1[t], d);
+            float p = part[j][0], r = part[j][1];
+            p = fmaf(s00, d[0], p); p = fmaf(s01, d[1], p); p = fmaf(-m00, xx.x, p); p = fmaf(-m01, xx.y, p);
+            r = fmaf(s10, d[2], r); r = fmaf(s11, d[3], r); r = fmaf(-m10, xx.x, r); r = fmaf(-m11, xx.y, r);
+            part[j][0] = p;
+            part[j][1] = r;
         }
     }
 }
@@ -370,6 +447,73 @@ __device__ void route_into_smem(const DecArgs &a, RouteSmem &r)
     }
 }
 
+constexpr int kWarpRouteT = 4;   // T at or below which one warp routes (T*k <= 32)
+
+// Routing of up to 32 assignments by one warp (the producer warp) into
+// shared memory: top-k per token, then counts, offsets, the stable
+// token-by-expert order and the active list from warp votes.  Only the
+// entries of active experts are written.  In CTA 0 the warp also writes the
+// routing to the workspace.
+__device__ void route_warp(const DecArgs &a, RouteSmem &r)
+{
+    const int lane = threadIdx.x & 31;
+    for (int t = 0; t < a.T; ++t)
+        topk_warp(a.logits + (size_t)t * a.E, a.E, a.k, a.score, r.ids + t * a.k, r.wts + t * a.k);
+    __syncwarp();
+    const bool valid = lane < a.A;
+    const int e = valid ? r.ids[lane] : (1 << 20);           // invalid lanes sort last
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    const bool leader = valid && rank == 0;
+    int off = 0, aidx = 0;
+    for (int L = 0; L < 32; ++L) {
+        const int thr = __shfl_sync(0xffffffffu, e, L);
+        const unsigned lt = __ballot_sync(0xffffffffu, valid && e < thr);
+        const unsigned llt = __ballot_sync(0xffffffffu, leader && e < thr);
+        if (lane == L) {
+            off = __popc(lt);
+            aidx = __popc(llt);
+        }
+    }
+    const unsigned lm = __ballot_sync(0xffffffffu, leader);
+    if (valid) {
+        r.perm[off + rank] = lane;
+        r.slot[lane] = off + rank;
+    }
+    if (leader) {
+        r.cnt[e] = __popc(peers);
+        r.off[e] = off;
+        r.act[aidx] = e;
+    }
+    if (lane == 0) r.n_act = __popc(lm);
+    __syncwarp();
+    if (blockIdx.x == 0) {
+        if (valid) {
+            a.ids[lane] = r.ids[lane];
+            a.wts[lane] = r.wts[lane];
+            a.perm[lane] = r.perm[lane];
+        }
+        int run = 0;
+        for (int e0 = 0; e0 < a.E; e0 += 32) {
+            const int me = e0 + lane;
+            int cnt = 0;
+            for (int i = 0; i < 32; ++i) cnt += __shfl_sync(0xffffffffu, e, i) == me;
+            int incl = cnt;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            if (me < a.E) {
+                a.counts[me] = cnt;
+                a.offsets[me] = run + incl - cnt;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) a.offsets[a.E] = run;
+    }
+}
+
 // x (bf16) -> fp16 in the (0, 2, 1, 3) order per 4, plus fp32 sums of 16,
 // for `n_groups` groups of 4 starting at group g0 (all threads of the CTA or
 // grid stride by `stride`).
@@ -414,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ RouteSmem rs;
     __shared__ __align__(16) __half zero[16];
+    __shared__ __align__(8) float2 sc_lut[256];   // scale byte -> {low nibble, high nibble}
     __shared__ int s_pabort, s_cabort, s_consumed, s_issued;
     __shared__ Job jobs[2];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -427,8 +572,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
     const size_t xs_bytes = a.x_smem ? (size_t)a.T * (a.H / 16) * 4 : 0;
     __half *x_s = reinterpret_cast<__half *>(p);
     float *xs_s = reinterpret_cast<float *>(p + x_bytes);
-    float *red = reinterpret_cast<float *>(p + x_bytes + xs_bytes);       // [2][16][NT][16]
-    float *obuf = red + 2 * kConsumers * NT * kTileM;                     // [A][32]
+    float *red = reinterpret_cast<float *>(p + x_bytes + xs_bytes);       // [2][16][NT][16] gate/up
+    float *redd = red + 2 * kConsumers * NT * kTileM;                     // [2][16][NT][16] down
+    float *obuf = redd + 2 * kConsumers * NT * kTileM;                    // [A][32]
     int *tags = reinterpret_cast<int *>(obuf + (size_t)a.A * kDownRows);  // [stages][kTagWords]
     uint64_t *bars = reinterpret_cast<uint64_t *>(tags + kTagWords * a.stages);
     uint64_t *full = bars, *empty = bars + a.stages;
@@ -445,9 +591,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
         s_issued = 0;
     }
     if (tid < 16) zero[tid] = __float2half_rn(0.0f);
-    if (a.x_smem)
-        convert_x(a.x, x_s, xs_s, tid, (size_t)a.T * (a.H / 4), blockDim.x);
-    route_into_smem(a, rs);       // ends with __syncthreads
+    if (tid < 256) sc_lut[tid] = make_float2((float)(tid & 15), (float)(tid >> 4));
+    if (a.T <= kWarpRouteT && a.A <= 32) {
+        // the producer warp routes while the other warps convert x
+        __syncthreads();
+        if (warp == kProducerWarp) {
+            route_warp(a, rs);
+        } else if (a.x_smem) {
+            const int t2 = tid < kProducerWarp * 32 ? tid : tid - 32;
+            convert_x(a.x, x_s, xs_s, t2, (size_t)a.T * (a.H / 4), blockDim.x - 32);
+        }
+        __syncthreads();
+    } else {
+        if (a.x_smem) convert_x(a.x, x_s, xs_s, tid, (size_t)a.T * (a.H / 4), blockDim.x);
+        route_into_smem(a, rs);   // ends with __syncthreads
+    }
 
     // the counters are reset (and, without x_smem, the activations converted)
     // by the kernel ahead of this one
@@ -580,7 +738,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
         // each consumer warp owns one (matrix or m-tile, half) pair and every
         // fourth K block: units u = 4*kb + 2*wm + wh with u = warp (mod 16)
         const int wm = (warp >> 1) & 1, wh = warp & 1, wk = warp >> 2;
-        int rb = 0, uses0 = 0, uses1 = 0;
+        const LaneA la_ = lane_a(wh, c);
+        const uint32_t x_s_a = ptx::smem_addr(x_s), xs_s_a = ptx::smem_addr(xs_s);
+        const uint32_t zero_a = ptx::smem_addr(zero), lut_a = ptx::smem_addr(sc_lut);
+        int rb = 0, uses0 = 0, uses1 = 0, rbd = 0;
         // hands the partial sums in `part` to the epilogue warp as job `jb`
         auto emit = [&](const Job &jb, float (&part)[NT][2]) {
             int &uses = rb ? uses1 : uses0;
@@ -618,12 +779,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
 #pragma unroll
                     for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
                     if (a.x_smem) {
+                        const uint32_t mat_s = ptx::smem_addr(mat);
                         for (int kb = wk; kb < a.H_blocks; kb += kConsumers / 4)
-                            tile_unit<NT, true>(mat + kb * kQ2KBytes, a.gu_pitch, wh, grp, c, inv4c,
-                                                x_s + kb * kQK, xs_s + kb * 16, zero, off, nt, part);
+                            tile_unit_s<NT>(mat_s + kb * kQ2KBytes, (uint32_t)a.gu_pitch, wh, grp, c, la_,
+                                            inv4c, x_s_a + kb * kQK * 2, xs_s_a + kb * 64, zero_a,
+                                            lut_a, off, nt, part);
                     } else {
                         for (int kb = wk; kb < a.H_blocks; kb += kConsumers / 4)
-                            tile_unit<NT, false>(mat + kb * kQ2KBytes, a.gu_pitch, wh, grp, c, inv4c,
+                            tile_unit<NT, false>(mat + kb * kQ2KBytes, a.gu_pitch, wh, grp, c, la_, inv4c,
                                                  a.xp + kb * kQK, a.xs + kb * 16, zero, off, nt, part);
                     }
                     emit(Job{kJobGateUp, e, mt, seg0, c0, nt, it, 0}, part);
@@ -647,20 +810,49 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
                             uint32_t off[NT];
 #pragma unroll
                             for (int j = 0; j < NT; ++j) off[j] = (uint32_t)(c0 + (j < nt ? j : 0)) * a.I_pad;
+                            const uint32_t mat_s = ptx::smem_addr(mat);
+                            const uint32_t h_a = ptx::smem_addr(h_s), hs_a = ptx::smem_addr(hs_s);
                             for (int kb = wk; kb < a.I_blocks; kb += kConsumers / 4)
-                                tile_unit<NT, true>(mat + kb * kQ2KBytes, a.dn_pitch, wh, grp, c, inv4c,
-                                                    h_s + kb * kQK, hs_s + kb * 16, zero, off, nt, part);
+                                tile_unit_s<NT>(mat_s + kb * kQ2KBytes, (uint32_t)a.dn_pitch, wh, grp, c,
+                                                la_, inv4c, h_a + kb * kQK * 2, hs_a + kb * 64, zero_a,
+                                                lut_a, off, nt, part);
                         } else {
                             uint32_t off[NT];
 #pragma unroll
                             for (int j = 0; j < NT; ++j)
                                 off[j] = (uint32_t)(seg0 + c0 + (j < nt ? j : 0)) * a.I_pad;
                             for (int kb = wk; kb < a.I_blocks; kb += kConsumers / 4)
-                                tile_unit<NT, false>(mat + kb * kQ2KBytes, a.dn_pitch, wh, grp, c, inv4c,
+                                tile_unit<NT, false>(mat + kb * kQ2KBytes, a.dn_pitch, wh, grp, c, la_, inv4c,
                                                      a.hp + kb * kQK, a.hs + kb * 16, zero, off, nt, part);
                         }
-                        const int last = (j0 + cnt == n_act) && (jj == cnt - 1) && (c0 + NT >= seg_n);
-                        emit(Job{kJobDown, e, 0, seg0, c0, nt, it, last}, part);
+                        // the down partial sums are finished here, by the consumers
+                        float *rbuf = redd + rbd * kConsumers * NT * kTileM;
+                        store_partials<NT>(rbuf, warp, grp, c, part);
+                        consumer_sync();
+                        if (tid < nt * kDownRows) {
+                            const int row = tid & 31, j = tid >> 5;
+                            const int mtl = row >> 4, r16 = row & 15;
+                            // warps with (warp >> 1) & 1 == mtl hold rows mtl*16 .. +15
+                            float o = 0.0f;
+#pragma unroll
+                            for (int w = 0; w < kConsumers; ++w)
+                                if (((w >> 1) & 1) == mtl) o += rbuf[((size_t)w * NT + j) * kTileM + r16];
+                            obuf[(size_t)(seg0 + c0 + j) * kDownRows + row] = o;
+                        }
+                        rbd ^= 1;
+                    }
+                }
+                if (j0 + cnt == n_act) {
+                    // every expert of this item is in obuf: weighted combine in slot order
+                    consumer_sync();
+                    for (int i = tid; i < a.T * kDownRows; i += kConsumers * 32) {
+                        const int t = i / kDownRows, row = i % kDownRows;
+                        float acc = 0.0f;
+                        for (int sl = 0; sl < a.k; ++sl) {
+                            const int asg = t * a.k + sl;
+                            acc += rs.wts[asg] * obuf[(size_t)rs.slot[asg] * kDownRows + row];
+                        }
+                        a.y[(size_t)t * a.H + (size_t)it * kDownRows + row] = acc;
                     }
                 }
             }
@@ -716,30 +908,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
                 __threadfence();
                 __syncwarp();
                 if (lane == 0) atomicAdd(done + jb.e, jb.nt * kTileM);
-            } else {
-                for (int j = 0; j < jb.nt; ++j) {
-                    const int row = lane, mtl = row >> 4, r16 = row & 15;
-                    // warps with (warp >> 1) & 1 == mtl hold rows mtl*16 .. +15
-                    float o = 0.0f;
-#pragma unroll
-                    for (int w = 0; w < kConsumers; ++w)
-                        if (((w >> 1) & 1) == mtl) o += rbuf[((size_t)w * NT + j) * kTileM + r16];
-                    obuf[(size_t)(jb.seg0 + jb.c0 + j) * kDownRows + row] = o;
-                }
-                if (jb.last) {
-                    // every expert of this item is in obuf: weighted combine in slot order
-                    __syncwarp();
-                    for (int i = lane; i < a.T * kDownRows; i += 32) {
-                        const int t = i / kDownRows, row = i % kDownRows;
-                        float acc = 0.0f;
-                        for (int sl = 0; sl < a.k; ++sl) {
-                            const int asg = t * a.k + sl;
-                            acc += rs.wts[asg] * obuf[(size_t)rs.slot[asg] * kDownRows + row];
-                        }
-                        a.y[(size_t)t * a.H + (size_t)jb.item * kDownRows + row] = acc;
-                    }
-                    __syncwarp();
-                }
             }
             named_arrive(kBarJobEmpty + rb, kJobThreads);
         }
@@ -768,7 +936,7 @@ int64_t smem_pitch(int64_t row_bytes)
 size_t fixed_smem(const DecArgs &a, int nt)
 {
     const size_t x = a.x_smem ? (size_t)a.T * a.H * 2 + (size_t)a.T * (a.H / 16) * 4 : 0;
-    return x + (size_t)2 * kConsumers * nt * kTileM * 4 + (size_t)a.A * kDownRows * 4 +
+    return x + (size_t)4 * kConsumers * nt * kTileM * 4 + (size_t)a.A * kDownRows * 4 +
            4 * (size_t)kTagWords * a.stages + 8 * (2 * (size_t)a.stages);
 }
 
@@ -777,14 +945,16 @@ cudaError_t launch_nt(DecArgs a, const DeviceInfo &dev, cudaStream_t s, const cu
 {
     const size_t gu = (size_t)2 * kTileM * a.gu_pitch, dn = (size_t)kDownRows * a.dn_pitch;
     a.stage_bytes = (uint32_t)((std::max(gu, dn) + 127) / 128 * 128);
-    const size_t budget = std::min(kSmemBudget, (size_t)dev.max_smem_optin - 1024) -
-                          sizeof(RouteSmem) - 256;
+    cudaFuncAttributes fa{};
+    cudaError_t e = cudaFuncGetAttributes(&fa, decode_q2k_kernel<NT>);
+    if (e != cudaSuccess) return e;
+    const size_t budget = std::min(kSmemBudget, (size_t)dev.max_smem_optin - fa.sharedSizeBytes - 256);
     a.stages = 8;
     while (a.stages > 2 && (size_t)a.stages * a.stage_bytes + fixed_smem(a, NT) > budget) --a.stages;
     if ((size_t)a.stages * a.stage_bytes + fixed_smem(a, NT) > budget) return cudaErrorInvalidValue;
     const size_t smem = (size_t)a.stages * a.stage_bytes + fixed_smem(a, NT);
-    cudaError_t e = cudaFuncSetAttribute(decode_q2k_kernel<NT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(decode_q2k_kernel<NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(dev.sm_count);
@@ -817,8 +987,7 @@ bool decode_path_supported(const Plan &p, const ds4g_moe_desc *d)
     const size_t gu = (size_t)2 * kTileM * smem_pitch(d->gate_up_row_bytes);
     const size_t dn = (size_t)kDownRows * smem_pitch(d->down_row_bytes);
     const size_t stage = (std::max(gu, dn) + 127) / 128 * 128;
-    const size_t fixed = (size_t)2 * kConsumers * 4 * kTileM * 4 + (size_t)p.A * kDownRows * 4 +
-                         sizeof(RouteSmem) + 1024;
+    const size_t fixed = (size_t)4 * kConsumers * 4 * kTileM * 4 + (size_t)p.A * kDownRows * 4 + 1024;
     return 2 * stage + fixed <= kSmemBudget;
 }
 

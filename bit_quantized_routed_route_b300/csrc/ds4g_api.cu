@@ -135,16 +135,18 @@ namespace {
 
 enum class Path { kDecode, kTensorCore, kGeneral };
 
-// Decode kernels for small token counts, the tensor-core kernels for larger
-// ones, the general kernels where neither applies (codebook format, rows
-// that are not a multiple of 16 bytes, ragged inter on the decode side).
+// Decode kernels for small token counts (up to kDecodePreferT, or up to
+// kDecodeMaxT when the tensor-core kernels cannot run), the tensor-core
+// kernels for larger ones, the general kernels where neither applies
+// (codebook format, rows that are not a multiple of 16 bytes).
 Path choose_path(const ds4g_moe_desc *d, const Plan &p)
 {
     if (d->flags & DS4G_FORCE_TC) return Path::kTensorCore;
     const bool decode = decode_path_supported(p, d);
     if (d->flags & DS4G_FORCE_GEMV) return decode ? Path::kDecode : Path::kGeneral;
-    if (decode) return Path::kDecode;
-    if (tc_path_supported(p, d)) return Path::kTensorCore;
+    const bool tc = tc_path_supported(p, d);
+    if (decode && (p.T <= kDecodePreferT || !tc)) return Path::kDecode;
+    if (tc) return Path::kTensorCore;
     return Path::kGeneral;
 }
 

@@ -109,6 +109,7 @@ constexpr int kRouteSmallT = 64;
 // launches: a reset/conversion kernel and the fused layer kernel, which
 // routes by itself (events[1] after the first, events[2..4] after the second).
 constexpr int kDecodeMaxT = 32;
+constexpr int kDecodePreferT = 8;       // above this the tensor-core kernels are faster
 struct DecodeBufs {
     const float *logits;    // [T x E]
     int32_t *ids;           // routing outputs of the call (the kernel routes by itself)

@@ -66,12 +66,15 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
 }
 
 // Waits for phase `parity` of `bar` to complete, for at most `limit_ns`
-// nanoseconds.  Returns false when the limit expired.
+// nanoseconds.  Returns false when the limit expired.  Between polls the
+// thread sleeps briefly, so waiting warps leave the issue slots to the
+// warps that have work.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
+        __nanosleep(32);
         if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
@@ -97,6 +100,35 @@ __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes
 // Programmatic dependent launch.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// Shared-memory loads at 32-bit shared-window addresses.
+__device__ __forceinline__ uint32_t ld_s32(uint32_t a)
+{
+    uint32_t v;
+    asm volatile("ld.shared.b32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_s16(uint32_t a)
+{
+    uint16_t v;
+    asm volatile("ld.shared.b16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+    return v;
+}
+__device__ __forceinline__ uint4 ld_s128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(a)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ float2 ld_s64f(uint32_t a)
+{
+    float2 v;
+    asm volatile("ld.shared.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(a) : "memory");
+    return v;
+}
 
 __device__ __forceinline__ uint32_t lds32(const uint8_t *p)
 {

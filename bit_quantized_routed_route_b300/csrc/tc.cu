@@ -94,6 +94,7 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
+        __nanosleep(32);
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
