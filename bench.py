@@ -59,6 +59,8 @@ def parse():
     ap.add_argument("--pool", type=int, default=0, help="distinct token batches (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--force", default="auto", choices=["auto", "decode", "tc"],
+                    help="run the layer on one path (default: the library's choice)")
     return ap.parse_args()
 
 
@@ -179,13 +181,12 @@ def tensor_peaks():
 
 def layer_path(cfg: S.Config) -> str:
     """Which kernels the library runs for this workload (mirrors its choice:
-    decode kernels up to 8 tokens for Q2_K (up to 32 when the rows are not a
-    multiple of 16 bytes), tensor-core kernels for Q2_K with 16-byte rows
-    above that, the general kernels otherwise)."""
+    the decode kernels up to 32 tokens for Q2_K, the tensor-core prefill
+    kernels for Q2_K with 16-byte rows above that, the general kernels
+    otherwise)."""
     tc = (cfg.format == S.FMT_Q2K and cfg.row_bytes(cfg.hidden) % 16 == 0
           and cfg.row_bytes(cfg.inter) % 16 == 0)
-    if (cfg.format == S.FMT_Q2K and cfg.inter % 16 == 0
-            and (cfg.tokens <= 8 or (cfg.tokens <= 32 and not tc))):
+    if cfg.format == S.FMT_Q2K and cfg.inter % 16 == 0 and cfg.tokens <= 32:
         return "decode"
     return "tc" if tc else "general"
 
@@ -334,10 +335,11 @@ def main():
     w_dev = []
     base = {n: torch.from_numpy(layer[n]).to(dev) for n in ("w_gate", "w_up", "w_down")}
     cb = None if layer["codebook"] is None else torch.from_numpy(layer["codebook"]).to(dev)
+    flags = {"auto": 0, "decode": D.FORCE_GEMV, "tc": D.FORCE_TC}[args.force]
     for c in range(copies):
         t = base if c == 0 else {n: v.clone() for n, v in base.items()}
         w_dev.append(D.Layer(H, cfg.inter, E, k, cfg.score, cfg.format, t["w_gate"], t["w_up"],
-                             t["w_down"], cb))
+                             t["w_down"], cb, flags=flags))
     x_dev = torch.from_numpy(x_all.view(np.int16)).to(dev)
     l_dev = torch.from_numpy(l_all).to(dev)
     y_dev = torch.empty((T, H), dtype=torch.float32, device=dev)
@@ -429,7 +431,7 @@ def main():
     gate_up_bytes = float(np.mean(act * 2 * gu_b)) + x_b + T * k * cfg.inter * 2
     step_bytes = float(np.mean(touched[steps_b])) + x_b + l_b + y_b
     hbm_peak, peak_kind = peaks()
-    path = layer_path(cfg)
+    path = layer_path(cfg) if args.force == "auto" else args.force
     if path == "tc":
         # the tensor-core gate/up kernel: 2 * A * 2 * H * I flops per launch
         burst, sustained, tkind = tensor_peaks()
@@ -445,7 +447,9 @@ def main():
         # one fused kernel streams W_gate, W_up and W_down of the active experts
         dec_bytes = float(np.mean(touched[steps_b])) + x_b + y_b
         achieved = dec_bytes / (ph_ms[1] / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "kernel": "decode_q2k_kernel", "achieved": achieved,
+        roofline = {"bound": "hbm",
+                    "kernel": "decode_q2k_kernel" if T <= 8 else "decode_tc_kernel",
+                    "achieved": achieved,
                     "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
                     "traffic": measured_traffic("decode", cfg.name),

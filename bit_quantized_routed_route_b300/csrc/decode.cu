@@ -55,6 +55,7 @@
 // own copies (also bounded) and returns.
 #include "ds4g_common.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 #include "topk.cuh"
 
 namespace ds4g {
@@ -922,6 +923,650 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
     }
 }
 
+// ===========================================================================
+// tcgen05 decode kernel (decode_tc_kernel)
+//
+// The block-diagonal trick of the mma.sync kernel above, on the 5th
+// generation tensor core.  Per 16-row... rather, per 128-row tile and
+// 256-wide K block: the dequantizing warps store the raw fields
+// (1024 + q * 4^g, exact fp16, lop3 only) of their row to tensor memory as
+// the MMA's A operand; B, in shared memory, is block-diagonal over the 16
+// sub-blocks: row (t, s) of B holds activation vector t only in the 16
+// k-slots of sub-block s.  D (tensor memory, fp32) then holds per row one
+// value per (vector, sub-block), and the same warps apply
+//   w . x = sum_s d*sc_s*4^-g (D_s - 1024*X_s) - dmin*m_s*X_s
+// in a short per-block epilogue.  The tensor core does the 16-term sums, so
+// the CUDA cores spend about one instruction per weight.
+//
+// Work items, claimed from global counters by the producer warp:
+//   gate/up  (token chunk of <= 4 vectors of one expert, 128 rows of I,
+//             K half when the layer is small): both matrices, h = SiLU(g)*u;
+//             the CTA that finishes the second K half of a tile combines the
+//             halves;
+//   down     (token chunk, 128 rows of H): y_slot[p, m] = w_p * o; the CTA
+//             that completes the last chunk of an m-tile combines y in slot
+//             order.
+// A down item waits (bounded) until its expert's h is complete.
+// ===========================================================================
+namespace tcd {
+
+constexpr int kBM = 128;
+constexpr int kNtMax = 4;                 // activation vectors per item
+constexpr int kWinBytes = 112;            // 16-byte aligned window of one block row
+constexpr int kAq = kWinBytes * kBM;      // one matrix's windows of 128 rows
+constexpr int kChunk = 16 * kNtMax * 128; // one 64-wide K chunk of the diagonal operand
+constexpr int kBDiag = 4 * kChunk;
+constexpr int kOffB = 2 * kAq;            // 28672, 1024-aligned
+constexpr int kOffXc = kOffB + kBDiag;    // compact fp16 activations of the block
+constexpr int kOffXs = kOffXc + kNtMax * 512;   // their sub-block sums
+constexpr uint32_t kStage = 64 * 1024;
+constexpr int kStages = 3;
+constexpr int kDq = 8;                    // dequantizing warps (two warpgroups)
+constexpr int kThreads = (2 + kDq) * 32;
+constexpr uint32_t kTmemCols = 512, kDCol = 256;
+constexpr int kMaxPairs = 1024;           // K-split tile pairs
+constexpr int kBarWG = 1, kBarWG0 = 2;    // named barriers: both warpgroups / warpgroup 0
+
+enum { kItemGateUp = 0, kItemDown = 1, kItemEnd = 2 };
+
+struct Args {
+    int H, I, I_pad, E, k, T, A, score;
+    int H_blocks, I_blocks;
+    int P_gu, P_dn;                 // row phases of the weight windows
+    int64_t gu_row, dn_row;
+    int ks;                         // K split of gate/up tiles (1 or 2)
+    const float *logits;
+    const uint16_t *x;
+    const __half *xp;               // [T][H] fp16 (4-group permuted)
+    const float *xs;                // [T][H/16]
+    __half *hp;                     // [A][I_pad]
+    float *hs;                      // [A][I_pad/16]
+    float *yslot;                   // [A][H]
+    float *gpart;                   // [pairs][2 halves][2 matrices][kNtMax][128]
+    float *y;
+    int32_t *ids, *counts, *offsets, *perm;
+    float *wts;
+    int32_t *status;
+    int32_t *sync;                  // [0] gate/up claim, [1] down claim, [4 + e] h done,
+                                    // [4 + E + mt] y tiles done, [4 + E + H/128 + i] pair halves
+    uint64_t wait_ns;
+    int stall;
+};
+
+struct Chunk {
+    int e, pos0, nt;
+};
+
+// Raw fields of half HALF of the block at word SH of `win`: 64 packed fp16
+// pairs (1024 + q * 4^g), stored to tensor memory at taddr.
+template <int SH, int HALF>
+__device__ __forceinline__ void raw_store(const uint32_t (&win)[24], uint32_t taddr)
+{
+    const uint32_t *w = win + SH;
+    uint32_t out[64];
+#pragma unroll
+    for (int wd = 0; wd < 8; ++wd) {
+        const uint32_t qw = w[4 + 8 * HALF + wd], qh = qw >> 8;
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const uint32_t mask = 0x00030003u << (2 * g);
+            out[16 * g + 2 * wd] = ptx::lop3_and_or(qw, mask, 0x64006400u);
+            out[16 * g + 2 * wd + 1] = ptx::lop3_and_or(qh, mask, 0x64006400u);
+        }
+    }
+    ptx::tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&out[0]));
+    ptx::tmem_st32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&out[32]));
+}
+
+__device__ __forceinline__ void raw_store_sh(const uint32_t (&win)[24], int sh, int half,
+                                             uint32_t taddr)
+{
+    switch (sh * 2 + half) {
+    case 0: raw_store<0, 0>(win, taddr); break;
+    case 1: raw_store<0, 1>(win, taddr); break;
+    case 2: raw_store<1, 0>(win, taddr); break;
+    case 3: raw_store<1, 1>(win, taddr); break;
+    case 4: raw_store<2, 0>(win, taddr); break;
+    case 5: raw_store<2, 1>(win, taddr); break;
+    case 6: raw_store<3, 0>(win, taddr); break;
+    default: raw_store<3, 1>(win, taddr); break;
+    }
+}
+
+// The 5 words of the block that the epilogue needs (scales 0..3, d|dmin).
+__device__ __forceinline__ void keep_scales(const uint32_t (&win)[24], int sh, uint32_t (&sc)[5])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t v = win[i];
+        v = sh == 1 ? win[i + 1] : v;
+        v = sh == 2 ? win[i + 2] : v;
+        v = sh == 3 ? win[i + 3] : v;
+        sc[i] = v;
+    }
+    uint32_t v = win[20];
+    v = sh == 1 ? win[21] : v;
+    v = sh == 2 ? win[22] : v;
+    v = sh == 3 ? win[23] : v;
+    sc[4] = v;
+}
+
+// Adds sub-blocks s0 .. s0+NS-1 of one 256-wide block to acc[t], t < nt:
+// D from tensor memory (columns 16t + s), sums X from shared memory.
+template <int NS>
+__device__ __forceinline__ void block_epilogue(uint32_t dcol, int s0, const uint32_t (&sc)[5],
+                                               const float2 *lut, const float *xsum, int nt,
+                                               float (&acc)[kNtMax])
+{
+    const float d = half_bits(sc[4] & 0xFFFFu), dmin = half_bits(sc[4] >> 16);
+    float cA[NS], cX[NS];
+#pragma unroll
+    for (int i = 0; i < NS; ++i) {
+        const int s = s0 + i;
+        const uint32_t b = (sc[s >> 2] >> (8 * (s & 3))) & 0xFFu;
+        const float2 f = lut[b];
+        const int g = (s & 7) >> 1;
+        cA[i] = d * f.x * (g == 0 ? 1.0f : g == 1 ? 0.25f : g == 2 ? 0.0625f : 0.015625f);
+        cX[i] = -fmaf(1024.0f, cA[i], dmin * f.y);
+    }
+#pragma unroll
+    for (int t = 0; t < kNtMax; ++t) {
+        if (t < nt) {
+            float v[16];
+            if (NS == 16) {
+                ptx::tmem_ld16(dcol + 16 * t, v);
+            } else {
+                float v8[8];
+                ptx::tmem_ld8(dcol + 16 * t + s0, v8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = v8[i];
+            }
+            ptx::tmem_ld_wait();
+            float a = acc[t];
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                a = fmaf(cA[i], v[i], a);
+                a = fmaf(cX[i], xsum[16 * t + s0 + i], a);
+            }
+            acc[t] = a;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_gate,
+                     const __grid_constant__ CUtensorMap tm_up,
+                     const __grid_constant__ CUtensorMap tm_down, const Args a)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    __shared__ RouteSmem rs;
+    __shared__ Chunk chunks[kMaxAssign];
+    __shared__ int s_nchunks;
+    __shared__ __align__(8) float2 sc_lut[256];
+    __shared__ float xch[kNtMax][kBM];        // warpgroup 1 -> warpgroup 0 hand-off
+    __shared__ float hsm[kNtMax][kBM];        // h of the tile (for the sub-block sums)
+    __shared__ int tags[kStages][2];
+    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], afull[2], aempty[2];
+    __shared__ __align__(8) uint64_t dfull[2], dempty[2], drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort, s_issued, s_flag;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int *abort_flag = &s_abort;
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&empty[s], kDq);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&afull[b], kDq);
+            ptx::mbar_init(&aempty[b], 1);
+            ptx::mbar_init(&dfull[b], 1);
+            ptx::mbar_init(&dempty[b], kDq);
+        }
+        ptx::mbar_init(&drain, 1);
+        ptx::fence_mbar_init();
+        s_abort = 0;
+        s_issued = 0;
+    }
+    if (tid < 256) sc_lut[tid] = make_float2((float)(tid & 15), (float)(tid >> 4));
+    // zero the diagonal operand of every stage once; items only rewrite the
+    // diagonal entries
+    for (int i = tid; i < kStages * kBDiag / 16; i += blockDim.x) {
+        const int s = i / (kBDiag / 16), o = i % (kBDiag / 16);
+        reinterpret_cast<uint4 *>(smem + (size_t)s * kStage + kOffB)[o] = make_uint4(0, 0, 0, 0);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&s_tmem, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    // routing: one warp for small batches, the whole CTA otherwise
+    DecArgs ra{};
+    ra.E = a.E; ra.k = a.k; ra.T = a.T; ra.A = a.A; ra.score = a.score; ra.logits = a.logits;
+    ra.ids = a.ids; ra.wts = a.wts; ra.counts = a.counts; ra.offsets = a.offsets; ra.perm = a.perm;
+    __syncthreads();
+    if (a.T <= kWarpRouteT && a.A <= 32) {
+        if (warp == 0) route_warp(ra, rs);
+        __syncthreads();
+    } else {
+        route_into_smem(ra, rs);
+    }
+    if (warp == 0) {
+        // token chunks of <= kNtMax vectors per active expert
+        int run = 0;
+        for (int j0 = 0; j0 < rs.n_act; j0 += 32) {
+            const int j = j0 + lane;
+            const int e = j < rs.n_act ? rs.act[j] : 0;
+            const int n = j < rs.n_act ? (rs.cnt[e] + kNtMax - 1) / kNtMax : 0;
+            int incl = n;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += v;
+            }
+            for (int c = 0; c < n; ++c) {
+                Chunk ch;
+                ch.e = e;
+                ch.pos0 = rs.off[e] + c * kNtMax;
+                ch.nt = min(kNtMax, rs.cnt[e] - c * kNtMax);
+                chunks[run + incl - n + c] = ch;
+            }
+            run += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) s_nchunks = run;
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    ptx::grid_dep_wait();        // counters reset, activations converted
+    const uint32_t tmem = s_tmem;
+
+    const int n_chunks = s_nchunks;
+    const int mt_gu = a.I_pad / kBM, mt_dn = a.H / kBM;
+    const int n_gu = n_chunks * mt_gu * a.ks, n_dn = n_chunks * mt_dn;
+    const int kb_gu = a.H_blocks / a.ks, kb_dn = a.I_blocks;
+    int32_t *const claim_gu = a.sync, *const claim_dn = a.sync + 1, *const done = a.sync + 4;
+    int32_t *const tiles_done = a.sync + 4 + a.E, *const pairs = tiles_done + mt_dn;
+
+    if (warp == 0) {
+        // ---------------- producer ----------------
+        if (lane == 0 && !a.stall) {
+            ptx::prefetch_tmap(&tm_gate);
+            ptx::prefetch_tmap(&tm_up);
+            ptx::prefetch_tmap(&tm_down);
+            int sc = 0;
+            bool ok = true;
+            auto slot = [&](int &s) -> bool {
+                s = sc % kStages;
+                if (sc >= kStages &&
+                    !ptx::mbar_wait_or_abort(&empty[s], ((sc / kStages) - 1) & 1, a.wait_ns,
+                                             abort_flag)) {
+                    set_status(a.status, DS4G_ERR_TIMEOUT);
+                    *abort_flag = 1;
+                    return false;
+                }
+                return true;
+            };
+            for (int phase = 0; ok && phase < 2; ++phase) {
+                while (ok) {
+                    const int it = atomicAdd(phase == 0 ? claim_gu : claim_dn, 1);
+                    if (it >= (phase == 0 ? n_gu : n_dn)) break;
+                    int ch, mt, kh = 0;
+                    if (phase == 0) {
+                        ch = it / (mt_gu * a.ks);
+                        const int rem = it % (mt_gu * a.ks);
+                        mt = rem / a.ks;
+                        kh = rem % a.ks;
+                    } else {
+                        ch = it / mt_dn;
+                        mt = it % mt_dn;
+                    }
+                    const Chunk c = chunks[ch];
+                    if (phase == 1) {
+                        if (!wait_counter(done + c.e, a.I_pad * rs.cnt[c.e], a.wait_ns)) {
+                            set_status(a.status, DS4G_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        // h was written by other CTAs (generic proxy); the
+                        // copies below read it through the async proxy
+                        asm volatile("fence.proxy.async.global;" ::: "memory");
+                    }
+                    const int P = phase == 0 ? a.P_gu : a.P_dn;
+                    const int64_t row = phase == 0 ? a.gu_row : a.dn_row;
+                    const int nkb = phase == 0 ? kb_gu : kb_dn;
+                    const int nmat = phase == 0 ? 2 : 1;
+                    const uint32_t bytes = (uint32_t)(nmat * kAq + c.nt * (512 + 64));
+                    for (int j = 0; ok && j < nkb; ++j, ++sc) {
+                        const int kb = kh * nkb + j;
+                        int s;
+                        if (!(ok = slot(s))) break;
+                        tags[s][0] = phase;
+                        tags[s][1] = it;
+                        uint8_t *st = smem + (size_t)s * kStage;
+                        ptx::mbar_arrive_expect_tx(&full[s], bytes);
+                        for (int p = 0; p < P; ++p) {
+                            const int xw = (int)(((p * row + kQ2KBytes * kb) & ~15ll) / 4);
+                            uint8_t *dst = st + p * (kBM / P) * kWinBytes;
+                            if (phase == 0) {
+                                ptx::tma_load_3d(dst, &tm_gate, xw, mt * (kBM / P), c.e, &full[s]);
+                                ptx::tma_load_3d(dst + kAq, &tm_up, xw, mt * (kBM / P), c.e, &full[s]);
+                            } else {
+                                ptx::tma_load_3d(dst, &tm_down, xw, mt * (kBM / P), c.e, &full[s]);
+                            }
+                        }
+                        for (int t = 0; t < c.nt; ++t) {
+                            const __half *src;
+                            const float *ssrc;
+                            if (phase == 0) {
+                                const int tok = rs.perm[c.pos0 + t] / a.k;
+                                src = a.xp + (size_t)tok * a.H + (size_t)kb * kQK;
+                                ssrc = a.xs + (size_t)tok * (a.H / 16) + (size_t)kb * 16;
+                            } else {
+                                const int pos = c.pos0 + t;
+                                src = a.hp + (size_t)pos * a.I_pad + (size_t)kb * kQK;
+                                ssrc = a.hs + (size_t)pos * (a.I_pad / 16) + (size_t)kb * 16;
+                            }
+                            ptx::bulk_g2s(st + kOffXc + t * 512, src, 512, &full[s]);
+                            ptx::bulk_g2s(st + kOffXs + t * 64, ssrc, 64, &full[s]);
+                        }
+                        s_issued = sc + 1;
+                    }
+                }
+            }
+            int s;
+            if (ok && slot(s)) {
+                tags[s][0] = kItemEnd;
+                ptx::mbar_arrive(&full[s]);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            int sc = 0, fc = 0, dc = 0;
+            bool ok = true;
+            while (ok) {
+                const int s = sc % kStages;
+                if (!ptx::mbar_wait_or_abort(&full[s], (sc / kStages) & 1, a.wait_ns, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const int kind = tags[s][0];
+                if (kind == kItemEnd) break;
+                const int it = tags[s][1];
+                const Chunk c = chunks[kind == kItemGateUp ? it / (mt_gu * a.ks) : it / mt_dn];
+                const uint32_t idesc = ptx::idesc_f16(kBM, 16 * c.nt);
+                const int db = dc & 1;
+                if (dc >= 2 && !ptx::mbar_wait_or_abort(&dempty[db], ((dc >> 1) - 1) & 1, a.wait_ns,
+                                                        abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t b_base = ptx::smem_addr(smem + (size_t)s * kStage + kOffB);
+                const uint32_t dcol = tmem + kDCol + 128u * db;
+                const int fills = kind == kItemGateUp ? 2 : 1;
+                for (int h = 0; ok && h < fills; ++h, ++fc) {
+                    const int fb = fc & 1;
+                    if (!ptx::mbar_wait_or_abort(&afull[fb], (fc >> 1) & 1, a.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t abuf = tmem + 128u * fb;
+                    if (kind == kItemGateUp) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const int kk = 128 * h + 16 * i;
+                            const uint64_t bd =
+                                ptx::sw128_desc(b_base + (kk >> 6) * kChunk + (kk & 63) * 2);
+                            const bool acc = !(h == 0 && i == 0);
+                            ptx::mma_f16_ts(dcol, abuf + 8 * i, bd, idesc, acc);
+                            ptx::mma_f16_ts(dcol + 64, abuf + 64 + 8 * i, bd, idesc, acc);
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const int kk = 16 * i;
+                            const uint64_t bd =
+                                ptx::sw128_desc(b_base + (kk >> 6) * kChunk + (kk & 63) * 2);
+                            ptx::mma_f16_ts(dcol, abuf + 8 * i, bd, idesc, i > 0);
+                        }
+                    }
+                    ptx::mma_commit(&aempty[fb]);
+                }
+                if (!ok) break;
+                ptx::mma_commit(&dfull[db]);
+                ++dc;
+                ++sc;
+            }
+            if (!ok) {
+                set_status(a.status, DS4G_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            ptx::mma_commit(&drain);
+            ptx::mbar_wait(&drain, 0, a.wait_ns);
+        }
+    } else {
+        // ---------------- dequantizers / epilogue ----------------
+        const int wg = (warp - 2) >> 2;                 // 0: gate (or K half 0), 1: up (half 1)
+        const int ell = 32 * (warp & 3) + lane;         // tensor-memory lane = A row
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const int wtid = tid - 64 - 128 * wg;            // 0..127 inside the warpgroup
+        uint32_t dfull_phase[2] = {0, 0};
+        int sc = 0, fc = 0, dc = 0;
+        float acc[kNtMax];
+        // the epilogue of one block: its D buffer, scales and stage (the
+        // stage still holds the block's activation sums)
+        uint32_t pscw[5] = {0, 0, 0, 0, 0};
+        int pss = 0, pdb = 0;
+        auto block_done = [&](bool gu_, const uint32_t (&sc5)[5], int stg, int db, int nt,
+                              float (&ac)[kNtMax]) {
+            if (!ptx::mbar_wait_or_abort(&dfull[db], dfull_phase[db], a.wait_ns, abort_flag)) {
+                set_status(a.status, DS4G_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            dfull_phase[db] ^= 1;
+            ptx::tc_fence_after();
+            const float *xsum = reinterpret_cast<const float *>(smem + (size_t)stg * kStage + kOffXs);
+            const uint32_t dcol = tmem + lane_base + kDCol + 128u * db;
+            if (gu_)
+                block_epilogue<16>(dcol + 64u * wg, 0, sc5, sc_lut, xsum, nt, ac);
+            else
+                block_epilogue<8>(dcol, 8 * wg, sc5, sc_lut, xsum, nt, ac);
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                ptx::mbar_arrive(&dempty[db]);
+                ptx::mbar_arrive(&empty[stg]);
+            }
+        };
+        while (true) {
+            const int s = sc % kStages;
+            if (!ptx::mbar_wait_or_abort(&full[s], (sc / kStages) & 1, a.wait_ns, abort_flag)) {
+                set_status(a.status, DS4G_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every abort decision is taken here, by both warpgroups alike
+            named_sync(kBarWG, kDq * 32);
+            if (*abort_flag) break;
+            const int kind = tags[s][0];
+            if (kind == kItemEnd) break;
+            const int it = tags[s][1];
+            const bool gu = kind == kItemGateUp;
+            int ch, mt, kh = 0;
+            if (gu) {
+                ch = it / (mt_gu * a.ks);
+                const int rem = it % (mt_gu * a.ks);
+                mt = rem / a.ks;
+                kh = rem % a.ks;
+            } else {
+                ch = it / mt_dn;
+                mt = it % mt_dn;
+            }
+            const Chunk c = chunks[ch];
+            const int P = gu ? a.P_gu : a.P_dn;
+            const int64_t row = gu ? a.gu_row : a.dn_row;
+            const int nkb = gu ? kb_gu : kb_dn;
+            const int p = ell / (kBM / P);                 // row phase of this lane
+            const int wrow = (ell % (kBM / P)) * P + p;    // weight row inside the tile
+#pragma unroll
+            for (int t = 0; t < kNtMax; ++t) acc[t] = 0.0f;
+            for (int j = 0; j < nkb; ++j, ++sc) {
+                const int ss = sc % kStages;
+                if (j > 0) {
+                    if (!ptx::mbar_wait_or_abort(&full[ss], (sc / kStages) & 1, a.wait_ns, abort_flag)) {
+                        set_status(a.status, DS4G_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                }
+                const int kb = kh * nkb + j;
+                uint8_t *st = smem + (size_t)ss * kStage;
+                // warpgroup 0 scatters the block's activations onto the diagonal
+                if (wg == 0) {
+                    const uint32_t bb = ptx::smem_addr(st + kOffB), xc = ptx::smem_addr(st + kOffXc);
+                    const int kk = 2 * wtid, sb = kk >> 4, ck = kk >> 6, u = (kk & 63) >> 3;
+                    for (int t = 0; t < c.nt; ++t) {
+                        const int r = 16 * t + sb;
+                        const uint32_t v = ptx::ld_s32(xc + t * 512 + 4 * wtid);
+                        ptx::sts32(bb + ck * kChunk + r * 128 + ((u ^ (r & 7)) << 4) + (kk & 7) * 2, v);
+                    }
+                    ptx::fence_proxy_async_smem();
+                }
+                // this lane's 112-byte window of its matrix
+                const uint8_t *wn = st + (gu ? wg * kAq : 0) + ell * kWinBytes;
+                uint32_t win[24];
+#pragma unroll
+                for (int v = 0; v < 6; ++v) {
+                    const uint4 q = reinterpret_cast<const uint4 *>(wn)[v];
+                    win[4 * v] = q.x; win[4 * v + 1] = q.y; win[4 * v + 2] = q.z; win[4 * v + 3] = q.w;
+                }
+                const int sh = (int)(((p * row + kQ2KBytes * kb) & 15) >> 2);
+                uint32_t scw[5];
+                keep_scales(win, sh, scw);
+                const int fills = gu ? 2 : 1;
+                for (int h = 0; h < fills; ++h, ++fc) {
+                    const int fb = fc & 1;
+                    if (fc >= 2 &&
+                        !ptx::mbar_wait_or_abort(&aempty[fb], ((fc >> 1) - 1) & 1, a.wait_ns, abort_flag)) {
+                        set_status(a.status, DS4G_ERR_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    ptx::tc_fence_after();
+                    const int half = gu ? h : wg;
+                    raw_store_sh(win, sh, half, tmem + lane_base + 128u * fb + 64u * wg);
+                    ptx::tmem_st_wait();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&afull[fb]);
+                }
+                // epilogue of the previous block, while the tensor core works on this one
+                if (j > 0) block_done(gu, pscw, pss, pdb, c.nt, acc);
+#pragma unroll
+                for (int i = 0; i < 5; ++i) pscw[i] = scw[i];
+                pss = ss;
+                pdb = dc & 1;
+                ++dc;
+            }
+            block_done(gu, pscw, pss, pdb, c.nt, acc);
+            // ---- item epilogue ----
+            if (gu) {
+                const int pair = ch * mt_gu + mt;
+                bool have = true;
+                if (a.ks == 2) {
+                    // both warpgroups park their half-K partial sums; the
+                    // second half to finish combines them (fixed order)
+                    float *gp = a.gpart + ((size_t)(pair * 2 + kh) * 2 + wg) * kNtMax * kBM;
+                    for (int t = 0; t < c.nt; ++t) gp[t * kBM + wrow] = acc[t];
+                    __threadfence();
+                    named_sync(kBarWG, kDq * 32);
+                    if (wtid == 0 && wg == 0) s_flag = atomicAdd(pairs + pair, 1);
+                    named_sync(kBarWG, kDq * 32);
+                    have = s_flag == 1;
+                    if (have) {
+                        __threadfence();
+                        const float *g0 = a.gpart + ((size_t)(pair * 2 + 0) * 2 + wg) * kNtMax * kBM;
+                        const float *g1 = a.gpart + ((size_t)(pair * 2 + 1) * 2 + wg) * kNtMax * kBM;
+                        for (int t = 0; t < c.nt; ++t)
+                            acc[t] = __ldcg(g0 + t * kBM + wrow) + __ldcg(g1 + t * kBM + wrow);
+                    }
+                }
+                if (have) {
+                    if (wg == 1)
+                        for (int t = 0; t < c.nt; ++t) xch[t][wrow] = acc[t];
+                    named_sync(kBarWG, kDq * 32);
+                    if (wg == 0) {
+                        const int n = mt * kBM + wrow;
+                        for (int t = 0; t < c.nt; ++t) {
+                            const __half hv = __float2half_rn(silu_mul(acc[t], xch[t][wrow]));
+                            a.hp[(size_t)(c.pos0 + t) * a.I_pad + perm4(n)] = hv;
+                            hsm[t][wrow] = __half2float(hv);
+                        }
+                        named_sync(kBarWG0, 128);
+                        if (wtid < 8 * c.nt) {
+                            const int t = wtid >> 3, sb = wtid & 7;
+                            float sum = 0.0f;
+                            for (int r = 0; r < 16; ++r) sum += hsm[t][16 * sb + r];
+                            a.hs[(size_t)(c.pos0 + t) * (a.I_pad / 16) + mt * 8 + sb] = sum;
+                        }
+                        // publish: h and its sums of this tile are visible
+                        __threadfence();
+                        named_sync(kBarWG0, 128);
+                        if (wtid == 0) atomicAdd(done + c.e, kBM * c.nt);
+                    }
+                }
+            } else {
+                if (wg == 1)
+                    for (int t = 0; t < c.nt; ++t) xch[t][wrow] = acc[t];
+                named_sync(kBarWG, kDq * 32);
+                if (wg == 0) {
+                    const int m = mt * kBM + wrow;
+                    for (int t = 0; t < c.nt; ++t) {
+                        const int pos = c.pos0 + t;
+                        a.yslot[(size_t)pos * a.H + m] = rs.wts[rs.perm[pos]] * (acc[t] + xch[t][wrow]);
+                    }
+                    __threadfence();
+                    named_sync(kBarWG0, 128);
+                    if (wtid == 0) s_flag = atomicAdd(tiles_done + mt, c.nt) + c.nt == a.A;
+                }
+                named_sync(kBarWG, kDq * 32);
+                if (s_flag) {
+                    // every assignment of these rows is in y_slot: combine in slot order
+                    __threadfence();
+                    const int i0 = wg * 128 + wtid;
+                    for (int i = i0; i < a.T * kBM; i += 256) {
+                        const int t = i / kBM, m = mt * kBM + i % kBM;
+                        float yv = 0.0f;
+                        for (int sl = 0; sl < a.k; ++sl)
+                            yv += __ldcg(a.yslot + (size_t)rs.slot[t * a.k + sl] * a.H + m);
+                        a.y[(size_t)t * a.H + m] = yv;
+                    }
+                }
+                named_sync(kBarWG, kDq * 32);
+            }
+        }
+    }
+
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        const int issued = s_issued;
+        for (int q = issued - kStages; q < issued; ++q) {
+            if (q < 0) continue;
+            if (!ptx::mbar_wait(&full[q % kStages], (q / kStages) & 1, a.wait_ns)) break;
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace tcd
+
+
 // Row pitch of a weight tile in shared memory.  Lane groups read rows grp
 // and grp+8 (grp = 0..7) at the same column: a pitch of a multiple of 32
 // bytes would put several groups on one bank, so such rows get 16 bytes of
@@ -978,11 +1623,104 @@ cudaError_t launch_nt(DecArgs a, const DeviceInfo &dev, cudaStream_t s, const cu
 
 }  // namespace
 
+// Row phases that make a super-row a multiple of 16 bytes.
+int row_phases(int64_t row_bytes)
+{
+    int64_t g = 16;
+    while (row_bytes % g) g >>= 1;
+    return (int)(16 / g);
+}
+
+cudaError_t launch_decode_tc(const LayerArgs &la, const DecodeBufs &db, const DeviceInfo &dev,
+                             cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns, bool stall)
+{
+    tcd::Args a{};
+    a.H = la.H;
+    a.I = la.I;
+    a.I_pad = la.I_pad;
+    a.E = la.E;
+    a.k = la.k;
+    a.T = la.T;
+    a.A = la.A;
+    a.score = db.score;
+    a.H_blocks = la.H / kQK;
+    a.I_blocks = la.I_pad / kQK;
+    a.P_gu = row_phases(la.gu_row);
+    a.P_dn = row_phases(la.dn_row);
+    a.gu_row = la.gu_row;
+    a.dn_row = la.dn_row;
+    // split the gate/up tiles over K when there are too few of them to
+    // occupy every SM (single-token decode)
+    const int mt_gu = la.I_pad / tcd::kBM;
+    const int est_chunks = std::min(la.A, la.E);
+    a.ks = (est_chunks * mt_gu < 2 * dev.sm_count && a.H_blocks % 2 == 0 &&
+            la.A * mt_gu <= tcd::kMaxPairs)
+               ? 2
+               : 1;
+    a.logits = db.logits;
+    a.x = la.x;
+    a.xp = db.xp;
+    a.xs = db.xs;
+    a.hp = db.hp;
+    a.hs = db.hs;
+    a.yslot = la.yslot;
+    a.gpart = db.gpart;
+    a.y = la.y;
+    a.ids = db.ids;
+    a.wts = const_cast<float *>(la.wts);
+    a.counts = const_cast<int32_t *>(la.counts);
+    a.offsets = const_cast<int32_t *>(la.offsets);
+    a.perm = const_cast<int32_t *>(la.perm);
+    a.status = db.status;
+    a.sync = db.sync;
+    a.wait_ns = wait_ns;
+    a.stall = stall ? 1 : 0;
+
+    CUtensorMap m_gate, m_up, m_down;
+    cudaError_t e;
+    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, la.E, a.P_gu)) != cudaSuccess ||
+        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, la.E, a.P_gu)) != cudaSuccess ||
+        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, la.E, a.P_dn)) != cudaSuccess)
+        return e;
+
+    // counters and status reset, activations to fp16 (the kernel copies them
+    // into its pipeline by TMA)
+    const size_t groups = (size_t)a.T * (a.H / 4);
+    const int pre_grid = (int)std::min<size_t>((groups + 255) / 256, (size_t)dev.sm_count * 4);
+    decode_pre_kernel<<<pre_grid, 256, 0, s>>>(db.status, db.sync, decode_sync_words(la.E, la.H),
+                                               la.x, const_cast<__half *>(db.xp),
+                                               const_cast<float *>(db.xs), groups);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (events && (e = record_phase(events[1], s)) != cudaSuccess) return e;
+
+    const size_t smem = (size_t)tcd::kStages * tcd::kStage + 1024;
+    if ((e = cudaFuncSetAttribute(tcd::decode_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)smem)) != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(dev.sm_count);
+    cfg.blockDim = dim3(tcd::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, tcd::decode_tc_kernel, m_gate, m_up, m_down, a)) != cudaSuccess)
+        return e;
+    if (events)
+        for (int i = 2; i <= 4; ++i)
+            if ((e = record_phase(events[i], s)) != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 bool decode_path_supported(const Plan &p, const ds4g_moe_desc *d)
 {
     if (d->format != DS4G_FMT_Q2K || p.T > kDecodeMaxT || p.I % kTileM != 0 ||
         p.H % kDownRows != 0)
         return false;
+    if (p.T > kDecodePreferT) return p.H % tcd::kBM == 0;      // tcgen05 decode kernel
     // two ring stages and the fixed buffers must fit in shared memory
     const size_t gu = (size_t)2 * kTileM * smem_pitch(d->gate_up_row_bytes);
     const size_t dn = (size_t)kDownRows * smem_pitch(d->down_row_bytes);
@@ -995,6 +1733,10 @@ cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const 
                                cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns,
                                bool stall)
 {
+    // up to kDecodePreferT vectors the mma.sync kernel has the shorter
+    // dependency chain; above that the tcgen05 kernel's lower instruction
+    // count per weight wins
+    if (la.T > kDecodePreferT) return launch_decode_tc(la, db, dev, s, events, wait_ns, stall);
     DecArgs a{};
     a.H = la.H;
     a.I = la.I;
@@ -1037,7 +1779,7 @@ cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const 
     // counters and status reset; activation conversion when it does not fit
     const size_t groups = (size_t)a.T * (a.H / 4);
     const int pre_grid = a.x_smem ? 1 : (int)std::min<size_t>((groups + 255) / 256, (size_t)dev.sm_count * 4);
-    decode_pre_kernel<<<pre_grid, 256, 0, s>>>(db.status, db.sync, kSyncWords + a.E,
+    decode_pre_kernel<<<pre_grid, 256, 0, s>>>(db.status, db.sync, decode_sync_words(a.E, a.H),
                                                a.x_smem ? nullptr : la.x,
                                                const_cast<__half *>(db.xp),
                                                const_cast<float *>(db.xs), groups);

@@ -114,7 +114,8 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     q.active = take((size_t)q.E * 4);
     q.meta = take(kMetaWords * 4);
     q.status = take(4);
-    q.sync = take((size_t)(kSyncWords + q.E) * 4);
+    q.sync = take((size_t)decode_sync_words(q.E, q.H) * 4);
+    q.gpart = take(decode_gpart_bytes(q.A, q.I_pad));
     q.xp = take((size_t)T * q.H * 2);
     q.xs = take((size_t)T * (q.H / 16) * 4);
     q.hp = take(A * q.I_pad * 2);
@@ -135,18 +136,17 @@ namespace {
 
 enum class Path { kDecode, kTensorCore, kGeneral };
 
-// Decode kernels for small token counts (up to kDecodePreferT, or up to
-// kDecodeMaxT when the tensor-core kernels cannot run), the tensor-core
-// kernels for larger ones, the general kernels where neither applies
-// (codebook format, rows that are not a multiple of 16 bytes).
+// Decode kernels up to kDecodeMaxT tokens (mma.sync up to kDecodePreferT,
+// tcgen05 above), the tensor-core prefill kernels for larger token counts,
+// the general kernels where neither applies (codebook format, or prefill
+// rows that are not a multiple of 16 bytes).
 Path choose_path(const ds4g_moe_desc *d, const Plan &p)
 {
     if (d->flags & DS4G_FORCE_TC) return Path::kTensorCore;
     const bool decode = decode_path_supported(p, d);
     if (d->flags & DS4G_FORCE_GEMV) return decode ? Path::kDecode : Path::kGeneral;
-    const bool tc = tc_path_supported(p, d);
-    if (decode && (p.T <= kDecodePreferT || !tc)) return Path::kDecode;
-    if (tc) return Path::kTensorCore;
+    if (decode) return Path::kDecode;
+    if (tc_path_supported(p, d)) return Path::kTensorCore;
     return Path::kGeneral;
 }
 
@@ -225,7 +225,8 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     if (!decode && pe.mark(1, s) != cudaSuccess) return DS4G_ERR_CUDA;
     if (decode) {
         DecodeBufs b{logits, ids, d->score, xp, xs, reinterpret_cast<__half *>(ws + p.hp),
-                     reinterpret_cast<float *>(ws + p.hs), status, sync};
+                     reinterpret_cast<float *>(ws + p.hs), status, sync,
+                     reinterpret_cast<float *>(ws + p.gpart)};
         const bool stall = (d->flags & DS4G_DEBUG_STALL) != 0;
         return from_cuda(launch_decode_path(a, b, dev, s, pe.on ? pe.ev : nullptr,
                                             stall ? kStallWaitNs : kWaitNs, stall));

@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "../../include/ds4g.h"
 
 namespace ds4g {
@@ -27,7 +29,8 @@ struct Plan {
     int32_t block_bytes;    // 84 or 70
     size_t ids, wts, counts, offsets, perm, slot_pos, active, meta;
     size_t status;          // int32 device status word (DS4G_OK or DS4G_ERR_TIMEOUT)
-    size_t sync;            // [kSyncWords + E] int32 counters of the decode kernel
+    size_t sync;            // [decode_sync_words] int32 counters of the decode kernels
+    size_t gpart;           // K-split partial sums (decode)
     size_t xp, xs;          // [T x H] fp16 activations (4-group permuted), [T x H/16] sums
     size_t hp, hs;          // [A x I_pad] fp16 h (4-group permuted), [A x I_pad/16] sums
     size_t hbuf;            // [A x I_pad] fp32: SiLU(g)*u per assignment (segment order)
@@ -106,10 +109,12 @@ inline cudaError_t record_phase(cudaEvent_t ev, cudaStream_t s)
 constexpr int kRouteSmallT = 64;
 
 // Decode path (decode.cu): T <= kDecodeMaxT, Q2_K, inter % 16 == 0.  Two
-// launches: a reset/conversion kernel and the fused layer kernel, which
-// routes by itself (events[1] after the first, events[2..4] after the second).
+// launches: a reset/conversion kernel and one persistent layer kernel that
+// routes by itself -- the mma.sync kernel up to kDecodePreferT tokens, the
+// tcgen05 kernel above (events[1] after the first, events[2..4] after the
+// second).
 constexpr int kDecodeMaxT = 32;
-constexpr int kDecodePreferT = 8;       // above this the tensor-core kernels are faster
+constexpr int kDecodePreferT = 8;       // mma.sync decode kernel up to here, tcgen05 above
 struct DecodeBufs {
     const float *logits;    // [T x E]
     int32_t *ids;           // routing outputs of the call (the kernel routes by itself)
@@ -119,9 +124,21 @@ struct DecodeBufs {
     __half *hp;
     float *hs;
     int32_t *status;
-    int32_t *sync;          // [kSyncWords + E] claim and completion counters
+    int32_t *sync;          // [decode_sync_words] claim and completion counters
+    float *gpart;           // K-split partial sums of the tensor-core decode kernel
 };
 constexpr int kSyncWords = 4;
+constexpr int kDecodeMaxPairs = 1024;
+// Counter words of the decode kernels: claims, per-expert h completion,
+// per-128-row y tiles, K-split tile pairs.
+inline int decode_sync_words(int E, int H) { return kSyncWords + E + H / 128 + kDecodeMaxPairs; }
+// Bytes of K-split partial sums: per (token chunk, 128-row tile) pair, two
+// K halves x two matrices x 4 vectors x 128 rows of fp32.
+inline size_t decode_gpart_bytes(int A, int I_pad)
+{
+    const size_t pairs = (size_t)std::min(A * (I_pad / 128), kDecodeMaxPairs);
+    return pairs * 2 * 2 * 4 * 128 * 4;
+}
 bool decode_path_supported(const Plan &p, const ds4g_moe_desc *d);
 cudaError_t launch_decode_path(const LayerArgs &a, const DecodeBufs &b, const DeviceInfo &dev,
                                cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns,

@@ -49,6 +49,7 @@
 
 #include "ds4g_common.cuh"
 #include "ptx.cuh"
+#include "tmap.cuh"
 
 namespace ds4g {
 namespace {
@@ -94,7 +95,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
     while (true) {
-        __nanosleep(32);
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if (ptx::globaltimer_ns() - t0 > limit_ns) return false;
@@ -505,43 +505,6 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
 // host side
 // ---------------------------------------------------------------------------
 
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::mutex g_encode_mu;
-
-cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000 *out)
-{
-    std::lock_guard<std::mutex> lock(g_encode_mu);
-    if (!g_encode) {
-        void *fn = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                                         cudaEnableDefault, &q);
-        if (e != cudaSuccess) return e;
-        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
-        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-    *out = g_encode;
-    return cudaSuccess;
-}
-
-// 3-D map over [experts][rows][row words] of one quantized weight tensor:
-// box = 28 words (112 bytes) x 128 rows x 1 expert, no swizzle, zero fill.
-cudaError_t weight_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows,
-                       int64_t expert_stride, int64_t experts)
-{
-    PFN_cuTensorMapEncodeTiled_v12000 enc;
-    cudaError_t e = get_encode(&enc);
-    if (e != cudaSuccess) return e;
-    cuuint64_t dims[3] = {(cuuint64_t)(row_bytes / 4), (cuuint64_t)rows, (cuuint64_t)experts};
-    cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)expert_stride};
-    cuuint32_t box[3] = {(cuuint32_t)kWinWords, (cuuint32_t)kBM, 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
-                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
-
 // 2-D map over [rows][K] fp16 activations: box = 64 (128 bytes) x 16 rows,
 // 128-byte swizzle, zero fill beyond the last row.
 cudaError_t act_map(CUtensorMap *m, const void *base, int64_t K, int64_t rows)
@@ -574,6 +537,46 @@ cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtens
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::mutex g_encode_mu;
+
+cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000 *out)
+{
+    std::lock_guard<std::mutex> lock(g_encode_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess) return e;
+        if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = g_encode;
+    return cudaSuccess;
+}
+
+// 3-D map over [experts][rows][row words] of one quantized weight tensor:
+// box = 28 words (112 bytes) x 128 rows x 1 expert, no swizzle, zero fill.
+cudaError_t weight_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows,
+                       int64_t expert_stride, int64_t experts, int phases)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    cudaError_t e = get_encode(&enc);
+    if (e != cudaSuccess) return e;
+    // `phases` consecutive rows form one super-row (phases * row_bytes is a
+    // multiple of 16); the box covers 128 / phases super-rows
+    cuuint64_t dims[3] = {(cuuint64_t)(phases * row_bytes / 4), (cuuint64_t)(rows / phases),
+                          (cuuint64_t)experts};
+    cuuint64_t strides[2] = {(cuuint64_t)(phases * row_bytes), (cuuint64_t)expert_stride};
+    cuuint32_t box[3] = {(cuuint32_t)kWinWords, (cuuint32_t)(kBM / phases), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d)
 {
     return d->format == DS4G_FMT_Q2K && p.A > 0 && d->gate_up_row_bytes % 16 == 0 &&
@@ -596,9 +599,9 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
 {
     CUtensorMap m_gate, m_up, m_down, m_x, m_h;
     cudaError_t e;
-    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, la.E)) != cudaSuccess ||
-        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, la.E)) != cudaSuccess ||
-        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, la.E)) != cudaSuccess ||
+    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, la.E, 1)) != cudaSuccess ||
+        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, la.E, 1)) != cudaSuccess ||
+        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, la.E, 1)) != cudaSuccess ||
         (e = act_map(&m_x, tb.xseg, la.H, la.A)) != cudaSuccess ||
         (e = act_map(&m_h, tb.hp, la.I_pad, la.A)) != cudaSuccess)
         return e;
