@@ -182,10 +182,9 @@ def tensor_peaks():
 def layer_path(cfg: S.Config) -> str:
     """Which kernels the library runs for this workload (mirrors its choice:
     the decode kernels up to 32 tokens for Q2_K, the tensor-core prefill
-    kernels for Q2_K with 16-byte rows above that, the general kernels
-    otherwise)."""
-    tc = (cfg.format == S.FMT_Q2K and cfg.row_bytes(cfg.hidden) % 16 == 0
-          and cfg.row_bytes(cfg.inter) % 16 == 0)
+    kernels (both formats) for rows of a multiple of 16 bytes otherwise, the
+    general kernels for the rest)."""
+    tc = cfg.row_bytes(cfg.hidden) % 16 == 0 and cfg.row_bytes(cfg.inter) % 16 == 0
     if cfg.format == S.FMT_Q2K and cfg.inter % 16 == 0 and cfg.tokens <= 32:
         return "decode"
     return "tc" if tc else "general"

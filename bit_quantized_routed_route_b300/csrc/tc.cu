@@ -77,6 +77,7 @@ struct TcArgs {
     const int32_t *perm;        // segment row -> assignment
     __half *hp;                 // gate/up output [A][I_pad] (permuted order)
     float *yslot;               // down output [A][H]
+    const int8_t *codebook;     // [256 x 8] int8 (codebook format)
     int32_t *status;
     uint64_t wait_ns;
 };
@@ -182,7 +183,78 @@ __device__ __forceinline__ void dequant_store_sh(const uint32_t (&win)[24], int 
     }
 }
 
-template <int MODE>
+// ---------------------------------------------------------------------------
+// Codebook-2-bit blocks (70 bytes: idx[32], sgn[32], 4-bit scales sc[4], d).
+// Per group of 8 weights one 8-byte codebook row is read from a shared-memory
+// copy replicated 16 times, so the 16 lanes of a half-warp never share a bank
+// whatever their indices.  Per pair of weights:
+//   v = 1024 + (c + 128)          byte-biased int8 OR-ed into fp16 1024 (prmt)
+//   n = v * s - 1152 * s = c * s  exact (|c * s| <= 645)
+//   n ^= sign bits                the weight's sign from the sign byte
+//   w = fp16(n * d)               one rounding, relative to w
+// Weights stay in natural order; the activation operand is stored likewise.
+// ---------------------------------------------------------------------------
+constexpr int kCbCopies = 16;
+constexpr int kCbRepBytes = 256 * kCbCopies * 8;
+
+template <int WO, int HALF>
+__device__ __forceinline__ void cb2_store(const uint32_t (&win)[24], uint32_t fs, uint32_t cb_lane,
+                                          uint32_t taddr)
+{
+    // the block's words (it starts fs/8 bytes into word WO of the window)
+    auto word = [&](int i) -> uint32_t { return __funnelshift_r(win[WO + i], win[WO + i + 1], fs); };
+    const uint32_t d2 = __byte_perm(word(17), 0, 0x1010);
+    const uint32_t scw = word(16);
+    uint32_t s2[4], ns2[4], idxw[4], sgnw[4];
+#pragma unroll
+    for (int G = 0; G < 4; ++G) {
+        const float sf = (float)((scw >> (4 * (4 * HALF + G))) & 15u);
+        s2[G] = ptx::pack_half2(sf, sf);
+        ns2[G] = ptx::pack_half2(-1152.0f * sf, -1152.0f * sf);
+        idxw[G] = word(4 * HALF + G);
+        sgnw[G] = word(8 + 4 * HALF + G);
+    }
+    uint32_t out[64];
+#pragma unroll
+    for (int o = 0; o < 16; ++o) {
+        const uint32_t idx = (idxw[o >> 2] >> (8 * (o & 3))) & 0xFFu;
+        const uint32_t sg = (sgnw[o >> 2] >> (8 * (o & 3))) & 0xFFu;
+        const int G = o >> 2;
+        uint32_t cw[2];
+        asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(cw[0]), "=r"(cw[1]) : "r"(cb_lane + idx * (kCbCopies * 8)));
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint32_t wb = cw[q] ^ 0x80808080u;
+            const uint32_t v0 = __byte_perm(wb, 0x64646464u, 0x4140);
+            const uint32_t v1 = __byte_perm(wb, 0x64646464u, 0x4342);
+            const uint32_t x = sg >> (4 * q);
+            const uint32_t m0 = ((x & 1u) << 15) | ((x & 2u) << 30);
+            const uint32_t m1 = ((x & 4u) << 13) | ((x & 8u) << 28);
+            out[4 * o + 2 * q] = ptx::hmul2_u(ptx::hfma2_u(v0, s2[G], ns2[G]) ^ m0, d2);
+            out[4 * o + 2 * q + 1] = ptx::hmul2_u(ptx::hfma2_u(v1, s2[G], ns2[G]) ^ m1, d2);
+        }
+    }
+    ptx::tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&out[0]));
+    ptx::tmem_st32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&out[32]));
+}
+
+__device__ __forceinline__ void cb2_store_off(const uint32_t (&win)[24], int byteoff, int half,
+                                              uint32_t cb_lane, uint32_t taddr)
+{
+    const uint32_t fs = (uint32_t)(byteoff & 3) * 8;
+    switch ((byteoff >> 2) * 2 + half) {
+    case 0: cb2_store<0, 0>(win, fs, cb_lane, taddr); break;
+    case 1: cb2_store<0, 1>(win, fs, cb_lane, taddr); break;
+    case 2: cb2_store<1, 0>(win, fs, cb_lane, taddr); break;
+    case 3: cb2_store<1, 1>(win, fs, cb_lane, taddr); break;
+    case 4: cb2_store<2, 0>(win, fs, cb_lane, taddr); break;
+    case 5: cb2_store<2, 1>(win, fs, cb_lane, taddr); break;
+    case 6: cb2_store<3, 0>(win, fs, cb_lane, taddr); break;
+    default: cb2_store<3, 1>(win, fs, cb_lane, taddr); break;
+    }
+}
+
+template <int MODE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
               const __grid_constant__ CUtensorMap tm_b, const TcArgs a)
@@ -190,6 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int NMAT = MODE == 0 ? 2 : 1;
     constexpr uint32_t kStageBytes = kBBytes + NMAT * kAqBytes;
     constexpr int kFills = MODE == 0 ? 2 : 1;     // A buffers per K step
+    constexpr int kBlockBytes = FMT == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -218,6 +291,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 1) {
         ptx::tmem_alloc(&s_tmem, kTmemCols);
         ptx::tmem_relinquish();
+    }
+    uint8_t *cbrep = smem + (size_t)kStages * kStageBytes;    // codebook format only
+    if (FMT == DS4G_FMT_CB2) {
+        for (int i = threadIdx.x; i < 256 * kCbCopies; i += blockDim.x) {
+            const int r = i / kCbCopies, cpy = i % kCbCopies;
+            uint8_t *dst = cbrep + r * (kCbCopies * 8) + cpy * 8;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) dst[b] = (uint8_t)a.codebook[8 * r + b];
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -256,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int r = 0; r < nb; ++r)
                             ptx::tma_load_2d(st + kc * kChunkBytes + r * kBoxRows * 128, &tm_b,
                                              kb * kQK + 64 * kc, row0 + kBoxRows * r, &full[s]);
-                    const int x = ((kQ2KBytes * kb) & ~15) / 4;
+                    const int x = ((kBlockBytes * kb) & ~15) / 4;
                     ptx::tma_load_3d(st + kBBytes, &tm_a0, x, mt * kBM, e, &full[s]);
                     if (NMAT == 2)
                         ptx::tma_load_3d(st + kBBytes + kAqBytes, &tm_a1, x, mt * kBM, e, &full[s]);
@@ -359,7 +441,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     win[4 * v + 2] = q.z;
                     win[4 * v + 3] = q.w;
                 }
-                const int sh = kb & 3;       // (84 * kb) mod 16, in words
+                const int sh = kb & 3;       // (84 * kb) mod 16, in words (Q2_K)
+                const int boff = (kBlockBytes * kb) & 15;   // block start in the window, bytes
                 for (int h = 0; h < kFills; ++h, ++fc) {
                     const int buf = fc & 1;
                     if (fc >= 2) {
@@ -369,7 +452,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ptx::tc_fence_after();
                     }
                     const uint32_t taddr = tmem + lane_base + (uint32_t)buf * 128u + 64u * wg;
-                    dequant_store_sh(win, sh, MODE == 0 ? h : wg, taddr);
+                    if (FMT == DS4G_FMT_Q2K)
+                        dequant_store_sh(win, sh, MODE == 0 ? h : wg, taddr);
+                    else
+                        cb2_store_off(win, boff, MODE == 0 ? h : wg,
+                                      ptx::smem_addr(cbrep) + (uint32_t)(lane & 15) * 8, taddr);
                     ptx::tmem_st_wait();
                     ptx::tc_fence_before();
                     __syncwarp();
@@ -394,7 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int j = 0; j < 8; ++j) {
                         const int t = 8 * c + j;
                         if (t < nlen)
-                            a.hp[(size_t)(row0 + t) * a.I_pad + perm4(n)] =
+                            a.hp[(size_t)(row0 + t) * a.I_pad + (FMT == DS4G_FMT_Q2K ? perm4(n) : n)] =
                                 __float2half_rn(silu_mul(g[j], u[j]));
                     }
                 } else {
@@ -440,13 +527,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Token tiles of every active segment and the activation gather:
 //   tiles[j] = (expert, first segment row, rows <= kNT, 0), heaviest expert
 //   segments are not reordered; *n_tiles = count;
-//   xseg[p, :] = fp16(x[perm[p] / k, :]) in the (0, 2, 1, 3) order per 4.
+//   xseg[p, :] = fp16(x[perm[p] / k, :]), in the (0, 2, 1, 3) order per 4
+//   for Q2_K (permute4), in natural order for the codebook format.
 __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict__ x, int H, int k,
                                                       int A, const int32_t *__restrict__ perm,
                                                       const int32_t *counts,
                                                       const int32_t *offsets, int E,
                                                       __half *__restrict__ xseg, int32_t *tiles,
-                                                      int32_t *n_tiles)
+                                                      int32_t *n_tiles, int permute4)
 {
     if (blockIdx.x == 0) {
         __shared__ int s_nt[DS4G_MAX_EXPERTS];
@@ -489,9 +577,11 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
             hv[2 * j] = __float2half_rn(bf16_bits(wv[j] & 0xFFFFu));
             hv[2 * j + 1] = __float2half_rn(bf16_bits(wv[j] >> 16));
         }
-        // (0, 2, 1, 3) inside each group of 4
-        const __half2 o0 = __halves2half2(hv[0], hv[2]), o1 = __halves2half2(hv[1], hv[3]);
-        const __half2 o2 = __halves2half2(hv[4], hv[6]), o3 = __halves2half2(hv[5], hv[7]);
+        // Q2_K: (0, 2, 1, 3) inside each group of 4; codebook format: natural
+        const __half2 o0 = permute4 ? __halves2half2(hv[0], hv[2]) : __halves2half2(hv[0], hv[1]);
+        const __half2 o1 = permute4 ? __halves2half2(hv[1], hv[3]) : __halves2half2(hv[2], hv[3]);
+        const __half2 o2 = permute4 ? __halves2half2(hv[4], hv[6]) : __halves2half2(hv[4], hv[5]);
+        const __half2 o3 = permute4 ? __halves2half2(hv[5], hv[7]) : __halves2half2(hv[6], hv[7]);
         uint4 out;
         out.x = *reinterpret_cast<const uint32_t *>(&o0);
         out.y = *reinterpret_cast<const uint32_t *>(&o1);
@@ -522,16 +612,17 @@ cudaError_t act_map(CUtensorMap *m, const void *base, int64_t K, int64_t rows)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int MODE>
+template <int MODE, int FMT>
 cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                       const TcArgs &args, int grid, cudaStream_t s)
 {
     constexpr int NMAT = MODE == 0 ? 2 : 1;
-    const size_t smem = (size_t)kStages * (kBBytes + NMAT * kAqBytes) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(tc_kernel<MODE>,
+    const size_t smem = (size_t)kStages * (kBBytes + NMAT * kAqBytes) + 1024 +
+                        (FMT == DS4G_FMT_CB2 ? kCbRepBytes : 0);
+    cudaError_t e = cudaFuncSetAttribute(tc_kernel<MODE, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    tc_kernel<MODE><<<grid, kThreads, smem, s>>>(a0, a1, b, args);
+    tc_kernel<MODE, FMT><<<grid, kThreads, smem, s>>>(a0, a1, b, args);
     return cudaGetLastError();
 }
 
@@ -579,8 +670,8 @@ cudaError_t weight_map(CUtensorMap *m, const void *base, int64_t row_bytes, int6
 
 bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d)
 {
-    return d->format == DS4G_FMT_Q2K && p.A > 0 && d->gate_up_row_bytes % 16 == 0 &&
-           d->down_row_bytes % 16 == 0 && p.H % kBM == 0;
+    return p.A > 0 && d->gate_up_row_bytes % 16 == 0 && d->down_row_bytes % 16 == 0 &&
+           p.H % kBM == 0;
 }
 
 int32_t tc_max_tiles(int32_t E, int32_t A) { return E + A / kNT + 1; }
@@ -590,7 +681,8 @@ cudaError_t launch_tc_prep(const LayerArgs &la, const TcBufs &tb, const DeviceIn
 {
     const int prep_grid = dev.sm_count * 4;
     tc_prep_kernel<<<prep_grid, 256, 0, s>>>(la.x, la.H, la.k, la.A, la.perm, la.counts,
-                                             la.offsets, la.E, tb.xseg, tb.tiles, tb.n_tiles);
+                                             la.offsets, la.E, tb.xseg, tb.tiles, tb.n_tiles,
+                                             la.format == DS4G_FMT_Q2K ? 1 : 0);
     return cudaGetLastError();
 }
 
@@ -620,12 +712,18 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
 
     a.K = la.H;
     a.m_tiles = la.I_pad / kBM;
-    if ((e = launch_tc<0>(m_gate, m_up, m_x, a, dev.sm_count, s)) != cudaSuccess) return e;
+    a.codebook = la.codebook;
+    const bool cb2 = la.format == DS4G_FMT_CB2;
+    if ((e = cb2 ? launch_tc<0, DS4G_FMT_CB2>(m_gate, m_up, m_x, a, dev.sm_count, s)
+                 : launch_tc<0, DS4G_FMT_Q2K>(m_gate, m_up, m_x, a, dev.sm_count, s)) != cudaSuccess)
+        return e;
     if (ev && (e = record_phase(ev[2], s)) != cudaSuccess) return e;
 
     a.K = la.I_pad;
     a.m_tiles = la.H / kBM;
-    if ((e = launch_tc<1>(m_down, m_down, m_h, a, dev.sm_count, s)) != cudaSuccess) return e;
+    if ((e = cb2 ? launch_tc<1, DS4G_FMT_CB2>(m_down, m_down, m_h, a, dev.sm_count, s)
+                 : launch_tc<1, DS4G_FMT_Q2K>(m_down, m_down, m_h, a, dev.sm_count, s)) != cudaSuccess)
+        return e;
     if (ev && (e = record_phase(ev[3], s)) != cudaSuccess) return e;
 
     if ((e = launch_combine(la, dev, s)) != cudaSuccess) return e;

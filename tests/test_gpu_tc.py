@@ -2,8 +2,9 @@
 routing bit-exact, per-token relative L2 <= 1e-3 and max-abs <= 5e-3 *
 max|ref| on the output.
 
-The path runs by itself for Q2_K layers above the decode token counts whose
-rows are multiples of 16 bytes; DS4G_FORCE_TC sends smaller layers to it.
+The path runs by itself for layers above the decode token counts whose rows
+are multiples of 16 bytes (both formats); DS4G_FORCE_TC sends smaller layers
+to it.
 Cases span several 128-row weight tiles and several 128-token tiles, with
 ragged tails on both (inter not a multiple of 128, segments longer than one
 token tile), a single expert, k = E, and the full-size decode layer."""
@@ -11,6 +12,7 @@ import numpy as np
 import pytest
 
 import bit_quantized_routed_route_b300 as D
+import ds4g_synth as S
 import oracle_pins as P
 from gpu_helpers import cached_layer, check_output, check_routing, run_forward, to_device
 
@@ -27,6 +29,24 @@ pytestmark = pytest.mark.gpu
 ])
 def test_tc_forward_small_layers(orc, kw):
     layer = P.small_layer(seed=1000 + kw["H"] + kw["T"], align=16, **kw)
+    L = to_device(layer, flags=D.FORCE_TC)
+    y, routing = run_forward(L, layer["x"], layer["logits"])
+    check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    check_output(y, yref)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=256, I=128, E=8, k=2, T=12),                    # one block per row; I < 256
+    dict(H=512, I=256, E=5, k=2, T=40),                    # 70-byte blocks at every 2-byte offset
+    dict(H=1024, I=384, E=7, k=3, T=150),                  # ragged inter; segments over 128 tokens
+    dict(H=2048, I=512, E=33, k=5, T=70),
+])
+def test_tc_forward_codebook_layers(orc, kw):
+    """The codebook-2-bit format on the tensor-core kernels (rows padded to
+    16 bytes)."""
+    layer = P.small_layer(seed=2000 + kw["H"] + kw["T"], fmt=S.FMT_CB2, align=16,
+                          score=S.SCORE_SIGMOID, **kw)
     L = to_device(layer, flags=D.FORCE_TC)
     y, routing = run_forward(L, layer["x"], layer["logits"])
     check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
