@@ -37,6 +37,7 @@ struct Plan {
     size_t yslot;           // [A x H] fp32: w * o per assignment (segment order)
     size_t xseg;            // [A x H] fp16: activations in segment order (tensor-core path)
     size_t tiles;           // [tc_max_tiles x 4] int32 token tiles (tensor-core path)
+    size_t wseg;            // [A] fp32 routing weight per segment row (tensor-core path)
     size_t x_stage;         // [T x H] bf16 (host entry point)
     size_t l_stage;         // [T x E] fp32 (host entry point)
     size_t y_stage;         // [T x H] fp32 (host entry point)
@@ -152,6 +153,7 @@ struct TcBufs {
     int32_t *tiles;        // [tc_max_tiles x 4]
     int32_t *n_tiles;
     int32_t *status;
+    float *wseg;           // [A] routing weight of each segment row
 };
 bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d);
 int32_t tc_max_tiles(int32_t E, int32_t A);

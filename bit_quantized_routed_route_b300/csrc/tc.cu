@@ -63,7 +63,11 @@ constexpr int kAqBytes = kWinWords * 4 * kBM;
 constexpr int kChunkBytes = kNT * 128;    // one 64-wide K chunk of the activation tile
 constexpr int kBBytes = 4 * kChunkBytes;
 constexpr int kDequantWarps = 8;
-constexpr int kThreads = (2 + kDequantWarps) * 32;
+constexpr int kEpilogueWarps = 4;          // down kernel: dedicated epilogue warps
+__host__ __device__ constexpr int tc_threads(int mode)
+{
+    return (2 + kDequantWarps + (mode == 1 ? kEpilogueWarps : 0)) * 32;
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 256;
 
@@ -73,8 +77,7 @@ struct TcArgs {
     int H, I_pad;
     const int32_t *tiles;       // [n][4]: expert, first segment row, rows, 0
     const int32_t *n_tiles;
-    const float *wts;           // routing weights (assignment order)
-    const int32_t *perm;        // segment row -> assignment
+    const float *wseg;          // routing weight of each segment row
     __half *hp;                 // gate/up output [A][I_pad] (permuted order)
     float *yslot;               // down output [A][H]
     const int8_t *codebook;     // [256 x 8] int8 (codebook format)
@@ -255,7 +258,7 @@ __device__ __forceinline__ void cb2_store_off(const uint32_t (&win)[24], int byt
 }
 
 template <int MODE, int FMT>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(tc_threads(MODE), 1)
     tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
               const __grid_constant__ CUtensorMap tm_b, const TcArgs a)
 {
@@ -267,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], afull[2], aempty[2];
-    __shared__ __align__(8) uint64_t accfull, accempty, drain;
+    __shared__ __align__(8) uint64_t accfull[2], accempty[2], drain;
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort, s_issued;
 
@@ -281,8 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mbar_init(&afull[b], kDequantWarps);
             ptx::mbar_init(&aempty[b], 1);
         }
-        ptx::mbar_init(&accfull, 1);
-        ptx::mbar_init(&accempty, kDequantWarps);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&accfull[b], 1);
+            ptx::mbar_init(&accempty[b], MODE == 0 ? kDequantWarps : kEpilogueWarps);
+        }
         ptx::mbar_init(&drain, 1);
         ptx::fence_mbar_init();
         s_abort = 0;
@@ -355,11 +360,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tile = it / a.m_tiles;
                 const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
                 const uint32_t idesc = ptx::idesc_f16(kBM, nb * kBoxRows);
-                if (ic > 0 && !wait_bar(&accempty, (ic - 1) & 1, a.wait_ns, abort_flag)) {
+                // gate/up: one accumulator pair; down: two accumulators, so the
+                // epilogue warps drain one while the next item accumulates
+                const int ab = MODE == 1 ? (ic & 1) : 0;
+                const int uses = MODE == 1 ? (ic >> 1) : ic;
+                if (uses > 0 && !wait_bar(&accempty[ab], (uses - 1) & 1, a.wait_ns, abort_flag)) {
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
+                const uint32_t acc_col = kAccCol + 128u * ab;
                 for (int kb = 0; ok && kb < KB; ++kb, ++sc) {
                     const int s = sc % kStages;
                     if (!wait_bar(&full[s], (sc / kStages) & 1, a.wait_ns, abort_flag)) {
@@ -392,7 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const int kk = 16 * i;
                                 const uint64_t bd = ptx::sw128_desc(
                                     b_base + (kk >> 6) * kChunkBytes + (kk & 63) * 2);
-                                ptx::mma_f16_ts(tmem + kAccCol, a_buf + 8 * i, bd, idesc,
+                                ptx::mma_f16_ts(tmem + acc_col, a_buf + 8 * i, bd, idesc,
                                                 !(kb == 0 && i == 0));
                             }
                         }
@@ -402,7 +412,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_commit(&empty[s]);
                 }
                 if (!ok) break;
-                ptx::mma_commit(&accfull);
+                ptx::mma_commit(&accfull[ab]);
             }
             if (!ok) {
                 set_status(a.status, DS4G_ERR_TIMEOUT);
@@ -413,8 +423,45 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::mma_commit(&drain);
             ptx::mbar_wait(&drain, 0, a.wait_ns);
         }
+    } else if (warp >= 2 + kDequantWarps) {
+        // ---------------- down epilogue warps (MODE 1) ----------------
+        const int row = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        int ic = 0;
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
+            const int tile = it / a.m_tiles, mt = it % a.m_tiles;
+            const int row0 = a.tiles[4 * tile + 1], nlen = a.tiles[4 * tile + 2];
+            const int ab = ic & 1;
+            ok = wait_bar(&accfull[ab], (ic >> 1) & 1, a.wait_ns, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int m = mt * kBM + row;
+            const uint32_t acc = tmem + lane_base + kAccCol + 128u * ab;
+            for (int c = 0; 8 * c < nlen; ++c) {
+                float o[8];
+                ptx::tmem_ld8(acc + 8 * c, o);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = 8 * c + j;
+                    if (t < nlen) {
+                        const int pos = row0 + t;
+                        a.yslot[(size_t)pos * a.H + m] = __ldg(a.wseg + pos) * o[j];
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&accempty[ab]);
+        }
+        if (!ok) {
+            if (lane == 0) set_status(a.status, DS4G_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
     } else {
-        // ---------------- dequantizers / epilogue ----------------
+        // ---------------- dequantizers / gate-up epilogue ----------------
         const int dw = warp - 2;                 // 0..7
         const int wg = dw >> 2;                  // warpgroup: matrix (gate/up) or half
         const int quarter = warp & 3;            // tensor-memory lane quarter
@@ -464,8 +511,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (!ok) break;
+            if (MODE == 1) continue;                 // the epilogue warps finish down items
             // epilogue of the item
-            ok = wait_bar(&accfull, ic & 1, a.wait_ns, abort_flag);
+            ok = wait_bar(&accfull[0], ic & 1, a.wait_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
@@ -484,24 +532,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                             a.hp[(size_t)(row0 + t) * a.I_pad + (FMT == DS4G_FMT_Q2K ? perm4(n) : n)] =
                                 __float2half_rn(silu_mul(g[j], u[j]));
                     }
-                } else {
-                    float o[8];
-                    ptx::tmem_ld8(tmem + lane_base + kAccCol + 8 * c, o);
-                    ptx::tmem_ld_wait();
-                    const int m = mt * kBM + row;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int t = 8 * c + j;
-                        if (t < nlen) {
-                            const int pos = row0 + t;
-                            a.yslot[(size_t)pos * a.H + m] = a.wts[a.perm[pos]] * o[j];
-                        }
-                    }
                 }
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&accempty);
+            if (lane == 0) ptx::mbar_arrive(&accempty[0]);
         }
         if (!ok) {
             if (lane == 0) set_status(a.status, DS4G_ERR_TIMEOUT);
@@ -526,7 +561,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Token tiles of every active segment and the activation gather:
 //   tiles[j] = (expert, first segment row, rows <= kNT, 0), heaviest expert
-//   segments are not reordered; *n_tiles = count;
+//   segments are not reordered; *n_tiles = count; wseg[p] = wts[perm[p]];
 //   xseg[p, :] = fp16(x[perm[p] / k, :]), in the (0, 2, 1, 3) order per 4
 //   for Q2_K (permute4), in natural order for the codebook format.
 __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict__ x, int H, int k,
@@ -534,8 +569,12 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
                                                       const int32_t *counts,
                                                       const int32_t *offsets, int E,
                                                       __half *__restrict__ xseg, int32_t *tiles,
-                                                      int32_t *n_tiles, int permute4)
+                                                      int32_t *n_tiles, int permute4,
+                                                      const float *__restrict__ wts,
+                                                      float *__restrict__ wseg)
 {
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < A; p += gridDim.x * blockDim.x)
+        wseg[p] = wts[perm[p]];
     if (blockIdx.x == 0) {
         __shared__ int s_nt[DS4G_MAX_EXPERTS];
         __shared__ int s_base[DS4G_MAX_EXPERTS + 1];
@@ -622,7 +661,7 @@ cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtens
     cudaError_t e = cudaFuncSetAttribute(tc_kernel<MODE, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    tc_kernel<MODE, FMT><<<grid, kThreads, smem, s>>>(a0, a1, b, args);
+    tc_kernel<MODE, FMT><<<grid, tc_threads(MODE), smem, s>>>(a0, a1, b, args);
     return cudaGetLastError();
 }
 
@@ -682,7 +721,7 @@ cudaError_t launch_tc_prep(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     const int prep_grid = dev.sm_count * 4;
     tc_prep_kernel<<<prep_grid, 256, 0, s>>>(la.x, la.H, la.k, la.A, la.perm, la.counts,
                                              la.offsets, la.E, tb.xseg, tb.tiles, tb.n_tiles,
-                                             la.format == DS4G_FMT_Q2K ? 1 : 0);
+                                             la.format == DS4G_FMT_Q2K ? 1 : 0, la.wts, tb.wseg);
     return cudaGetLastError();
 }
 
@@ -703,8 +742,7 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     a.I_pad = la.I_pad;
     a.tiles = tb.tiles;
     a.n_tiles = tb.n_tiles;
-    a.wts = la.wts;
-    a.perm = la.perm;
+    a.wseg = tb.wseg;
     a.hp = tb.hp;
     a.yslot = la.yslot;
     a.status = tb.status;
