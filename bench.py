@@ -24,6 +24,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import subprocess
 import sys
@@ -191,11 +192,16 @@ def layer_path(cfg: S.Config) -> str:
 
 
 def kernel_source_hash() -> str:
+    """Hash of the kernel sources with comments and blank lines removed, so a
+    comment edit keeps recorded counters valid and a code edit drops them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_quantized_routed_route_b300", "csrc")
     for name in sorted(os.listdir(csrc)):
         if name.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, name), "rb").read())
+            text = open(os.path.join(csrc, name), encoding="utf-8").read()
+            lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+            h.update(name.encode())
+            h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 
