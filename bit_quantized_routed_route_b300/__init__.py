@@ -192,7 +192,7 @@ def moe_forward_noalloc(desc: MoeDesc, x, logits, T, y, stream=None) -> int:
                                          _stream(stream))
 
 
-NOALLOC_SCRATCH_BYTES = 16 << 20
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 def moe_device_status(desc: MoeDesc, T: int, workspace, ws_bytes=None, stream=None):

@@ -5,8 +5,10 @@
 //   gate/up: h[p, n] = SiLU(W_gate[e][n,:] . x_t) * (W_up[e][n,:] . x_t)
 //   down:    y[t, m] = sum_{i<k} w[t,i] * (W_down[e_i][m,:] . h[p(t,i), :])
 //
-// One persistent kernel runs the whole layer (decode_q2k_kernel), one CTA per
-// SM.  Every CTA first routes all T tokens itself (top-k, counts, offsets,
+// Up to 8 tokens, one persistent kernel runs the whole layer
+// (decode_q2k_kernel, below), one CTA per SM; from 9 to 32 tokens the
+// tcgen05 kernel further down (decode_tc_kernel) does, with the same routing
+// and work claiming.  Every CTA first routes all T tokens itself (top-k, counts, offsets,
 // the stable token-by-expert order) into shared memory, so no work item
 // waits on global metadata; CTA 0 also writes the routing to the workspace.
 // A tiny kernel ahead of it (decode_pre_kernel) resets the claim counters
@@ -948,6 +950,22 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
 //             order.
 // A down item waits (bounded) until its expert's h is complete.
 // ===========================================================================
+// decode_tc_kernel: the same layer on the 5th-generation tensor cores, for
+// 9..32 tokens, where the mma.sync kernel's fixed 8-column operand would be
+// re-streamed per token chunk.  One work item is 128 weight rows of one
+// expert and up to kNtMax of its segment's tokens (a K split of 2 when there
+// are fewer items than SMs).  The block-diagonal idea carries over with a
+// wider N: for each token the 16 sub-blocks of a 256-wide block are 16 MMA
+// columns, so a 64-column B operand in shared memory (zero off the diagonal)
+// serves 4 tokens, and D column 16t+s is token t's dot over sub-block s.
+// The dequantizing warps store only the raw fields 1024 + q*4^g to tensor
+// memory (no scale arithmetic per weight); the scales, the mins and the
+// -1024*X correction are applied per sub-block in an fp32 epilogue that
+// lags the MMAs by one K block.  Warps: 0 TMA producer (3-D tensor maps
+// over 112-byte block windows, row phases for rows that are not a multiple
+// of 16 bytes), 1 MMA issuer, 2..9 two dequantizing warpgroups that are
+// also the epilogue.  Down items write yslot rows; the last CTA to finish a
+// 128-row y tile sums its slots in slot order (deterministic).
 namespace tcd {
 
 constexpr int kBM = 128;

@@ -225,16 +225,17 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     if (path == Path::kTensorCore && (e = launch_tc_prep(a, tb, dev, s)) != cudaSuccess)
         return from_cuda(e);
     if (!decode && pe.mark(1, s) != cudaSuccess) return DS4G_ERR_CUDA;
+    const bool stall = (d->flags & DS4G_DEBUG_STALL) != 0;
+    const uint64_t wait_ns = stall ? kStallWaitNs : kWaitNs;
     if (decode) {
         DecodeBufs b{logits, ids, d->score, xp, xs, reinterpret_cast<__half *>(ws + p.hp),
                      reinterpret_cast<float *>(ws + p.hs), status, sync,
                      reinterpret_cast<float *>(ws + p.gpart)};
-        const bool stall = (d->flags & DS4G_DEBUG_STALL) != 0;
-        return from_cuda(launch_decode_path(a, b, dev, s, pe.on ? pe.ev : nullptr,
-                                            stall ? kStallWaitNs : kWaitNs, stall));
+        return from_cuda(launch_decode_path(a, b, dev, s, pe.on ? pe.ev : nullptr, wait_ns,
+                                            stall));
     }
     if (path == Path::kTensorCore)
-        return from_cuda(launch_tc_path(a, tb, dev, s, pe.on ? pe.ev : nullptr, kWaitNs));
+        return from_cuda(launch_tc_path(a, tb, dev, s, pe.on ? pe.ev : nullptr, wait_ns, stall));
     return from_cuda(launch_gemv_path(a, dev, s, pe.on ? pe.ev : nullptr));
 }
 

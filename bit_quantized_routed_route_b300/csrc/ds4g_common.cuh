@@ -162,7 +162,8 @@ int32_t tc_max_tiles(int32_t E, int32_t A);
 cudaError_t launch_tc_prep(const LayerArgs &a, const TcBufs &b, const DeviceInfo &dev,
                            cudaStream_t s);
 cudaError_t launch_tc_path(const LayerArgs &a, const TcBufs &b, const DeviceInfo &dev,
-                           cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns);
+                           cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns,
+                           bool stall);
 constexpr int32_t kTcPathLaunches = 4;  // prep, gate/up, down, combine
 
 // Bounded device waits: default limit, and the short limit used with

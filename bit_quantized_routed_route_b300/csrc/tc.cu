@@ -1,7 +1,7 @@
-// tc.cu -- the tensor-core path for Q2_K experts: expert segments long
-// enough that the layer is a dense contraction (prefill; ds4 README mirror,
-// "So, what can I do with this software?" names micro-batched prefill on
-// CUDA).
+// tc.cu -- the tensor-core path for Q2_K and codebook-2-bit experts: expert
+// segments long enough that the layer is a dense contraction (prefill; ds4
+// README mirror, "So, what can I do with this software?" names micro-batched
+// prefill on CUDA).
 //
 // Per active expert e with segment rows P = offsets[e] .. offsets[e+1]-1
 // (assignments in segment order):
@@ -25,21 +25,27 @@
 //   warps 2-9  dequantizers, two warpgroups: each thread owns one weight row,
 //              reads its block from shared memory, forms fp16 weights in
 //              registers and stores them to tensor memory (tcgen05.st) as
-//              the next A buffer; after an item they are the epilogue
-//              (tcgen05.ld of the accumulators, SiLU*up or the routing
-//              weight, global stores).
+//              the next A buffer.  In the gate/up kernel they are also the
+//              epilogue after each item (tcgen05.ld of the accumulators,
+//              SiLU*up, fp16 stores of h);
+//   warps 10-13  down kernel only: the epilogue (tcgen05.ld, routing weight,
+//              fp32 stores of yslot), on double-buffered accumulators so
+//              the next item's MMAs overlap it.
 //
 // Weight values.  w = d*(sc&15)*q - dmin*(sc>>4) is formed on half2 pairs
 // with two roundings, each relative to w (q2k_half below); the per-token
 // relative L2 error of the layer stays near 5e-4.  The pair order inside
 // each aligned group of 4 weights is (0, 2, 1, 3), the order the lop3
 // extraction yields; the activation operand is stored in the same permuted
-// order, so the contraction is unchanged.
+// order, so the contraction is unchanged.  Codebook-2-bit weights keep the
+// natural order: each 8-weight codebook row comes from a 16-way replicated
+// copy of the codebook in shared memory, c*s is formed exactly in fp16 and
+// the single rounding is the multiply by d.
 //
 // Tensor memory (512 columns): columns 0..255 are two A buffers of 128
 // columns (K = 128 fp16 per matrix-half pair, or K = 256 of one matrix);
 // columns 256..383 and 384..511 are the fp32 accumulators (gate and up, or
-// down).  Every mbarrier wait is bounded; on expiry the kernel records
+// the down kernel's two alternating accumulators).  Every mbarrier wait is bounded; on expiry the kernel records
 // DS4G_ERR_TIMEOUT in the status word, lets every role leave its loop,
 // drains its own copies and MMAs (bounded) and frees its tensor memory.
 #include <cuda.h>
@@ -83,6 +89,7 @@ struct TcArgs {
     const int8_t *codebook;     // [256 x 8] int8 (codebook format)
     int32_t *status;
     uint64_t wait_ns;
+    int stall;                  // debug: the producer issues nothing (tests the bounded waits)
 };
 
 __device__ __forceinline__ int perm4(int n) { return (n & ~3) | ((n & 1) << 1) | ((n >> 1) & 1); }
@@ -317,7 +324,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
-        if (lane == 0) {
+        if (lane == 0 && !a.stall) {
             ptx::prefetch_tmap(&tm_a0);
             if (NMAT == 2) ptx::prefetch_tmap(&tm_a1);
             ptx::prefetch_tmap(&tm_b);
@@ -726,7 +733,8 @@ cudaError_t launch_tc_prep(const LayerArgs &la, const TcBufs &tb, const DeviceIn
 }
 
 cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceInfo &dev,
-                           cudaStream_t s, const cudaEvent_t *ev, uint64_t wait_ns)
+                           cudaStream_t s, const cudaEvent_t *ev, uint64_t wait_ns,
+                           bool stall)
 {
     CUtensorMap m_gate, m_up, m_down, m_x, m_h;
     cudaError_t e;
@@ -747,6 +755,7 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     a.yslot = la.yslot;
     a.status = tb.status;
     a.wait_ns = wait_ns;
+    a.stall = stall ? 1 : 0;
 
     a.K = la.H;
     a.m_tiles = la.I_pad / kBM;

@@ -100,10 +100,11 @@ typedef enum ds4g_dtype {
 enum {
     DS4G_FORCE_GEMV = 1,       /* every expert segment on the decode (GEMV) kernels   */
     DS4G_FORCE_TC = 2,         /* every expert segment on the tensor-core kernels     */
-    DS4G_DEBUG_STALL = 256     /* test hook: the decode kernels' copy producers issue
-                                  nothing, so their consumers' bounded waits (2 ms in
-                                  this mode) expire and the workspace status word
-                                  reads DS4G_ERR_TIMEOUT; y is garbage              */
+    DS4G_DEBUG_STALL = 256     /* test hook: the copy producers of the decode and
+                                  tensor-core kernels issue nothing, so their
+                                  consumers' bounded waits (2 ms in this mode)
+                                  expire and the workspace status word reads
+                                  DS4G_ERR_TIMEOUT; y is garbage                    */
 };
 
 /* Limits checked by the entry points. */
@@ -286,8 +287,9 @@ DS4G_API ds4g_status ds4g_moe_device_status(const ds4g_moe_desc *desc, int32_t T
  * Scratch comes from one static device array of DS4G_NOALLOC_SCRATCH_BYTES
  * per GPU, held by every GPU that loads the library until the process exits.
  * Calls whose workspace (ds4g_moe_workspace_bytes(desc, T)) would exceed it
- * return DS4G_ERR_WORKSPACE before launching anything; 16 MiB covers decode
- * up to T = 32 tokens at hidden 7168 / inter 2048 / 256 experts / top-8.
+ * return DS4G_ERR_WORKSPACE before launching anything; 32 MiB covers decode
+ * up to T = 32 tokens at hidden 7168 / inter 2048 / 256 experts / top-8
+ * (a 23.5 MiB workspace).
  * x, logits, y: as ds4g_moe_forward (device pointers owned by the caller).
  *
  * The first call on a device looks up the array's device address (a CUDA
@@ -301,7 +303,7 @@ DS4G_API ds4g_status ds4g_moe_device_status(const ds4g_moe_desc *desc, int32_t T
  * not apply to this entry point.
  * Errors: as ds4g_moe_forward.
  */
-#define DS4G_NOALLOC_SCRATCH_BYTES (16u << 20)
+#define DS4G_NOALLOC_SCRATCH_BYTES (32u << 20)
 DS4G_API ds4g_status ds4g_moe_forward_noalloc(const ds4g_moe_desc *desc, const uint16_t *x,
                                               const float *logits, int32_t T, float *y,
                                               void *stream);

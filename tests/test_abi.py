@@ -65,6 +65,20 @@ def test_workspace_size_is_positive_and_grows_with_T():
     assert 0 < a < b and a % 256 == 0
 
 
+def test_noalloc_scratch_covers_a_32_token_decode_of_the_7168_layer():
+    # the static scratch size is stated in the header and mirrored in Python
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "ds4g.h")).read()
+    m = re.search(r"#define DS4G_NOALLOC_SCRATCH_BYTES \((\d+)u << (\d+)\)", hdr)
+    assert m and int(m.group(1)) << int(m.group(2)) == D.NOALLOC_SCRATCH_BYTES
+    H, I, E, k = 7168, 2048, 256, 8
+    row = H // 256 * 84
+    d = desc(hidden=H, inter=I, n_experts=E, top_k=k, score=D.SCORE_SIGMOID,
+             gate_up_row_bytes=row, down_row_bytes=I // 256 * 84,
+             gate_up_expert_stride=I * row, down_expert_stride=H * (I // 256 * 84))
+    assert 0 < D.moe_workspace_bytes(d, 32) <= D.NOALLOC_SCRATCH_BYTES
+    assert D.moe_workspace_bytes(d, 2048) > D.NOALLOC_SCRATCH_BYTES
+
+
 @pytest.mark.parametrize("kw,code", [
     (dict(hidden=300), D.ERR_SHAPE),
     (dict(hidden=0), D.ERR_SHAPE),
