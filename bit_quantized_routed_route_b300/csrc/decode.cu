@@ -76,6 +76,11 @@ __device__ __forceinline__ float nib_lo(uint32_t b)
     return __uint_as_float(ptx::lop3_and_or(b, 15u, 0x4B000000u)) - 8388608.0f;
 }
 __device__ __forceinline__ float nib_hi(uint32_t b) { return nib_lo(b >> 4); }
+// The low 4 bits of b as the float 2^23 + v (exact).
+__device__ __forceinline__ float nib23(uint32_t b)
+{
+    return __uint_as_float(ptx::lop3_and_or(b, 15u, 0x4B000000u));
+}
 
 __device__ __forceinline__ void set_status(int32_t *status, int code)
 {
@@ -138,6 +143,7 @@ constexpr int kBarConsumers = 1, kBarJobFull = 2, kBarJobEmpty = 4;
 constexpr int kJobThreads = (kConsumers + 1) * 32;
 constexpr int kDownRows = 32;            // rows of H per down item (two MMA tiles)
 constexpr int kMaxDownPerStage = 8;
+constexpr int kDownPairs = 4;             // (expert, token chunk) pairs per down reduction round
 constexpr size_t kSmemBudget = 216 * 1024;     // dynamic shared memory of the decode kernel
 constexpr size_t kXStageMax = 48 * 1024;
 constexpr int kMaxAssign = kDecodeMaxT * DS4G_MAX_TOPK;     // 256
@@ -303,24 +309,37 @@ __device__ __forceinline__ void tile_unit(const uint8_t *blk0, int64_t row_bytes
 
 // tile_unit with every operand in shared memory, addressed by 32-bit
 // shared-window addresses: `blk0` (block kb of row grp), `xk`/`sk` (the K
-// block's activations / sums), `zero` (32 zero bytes), `lut` (the
-// 256-entry {sc, m} table of scale bytes).  off[j]: element offset of vector
-// j's activations (its sums start at off[j] / 16).
+// block's activations / sums).  off[j]: element offset of vector j's
+// activations (its sums start at off[j] / 16).
+//
+// Shared-memory traffic is kept to about 17 wavefronts per unit:
+//  * lanes with odd c read their qs words rotated by two words, so the two
+//    16-byte halves of a row's 32-byte qs chunk land in different banks; the
+//    activation operand of those sub-blocks is loaded with the same rotation,
+//    so every MMA still pairs each weight with its activation;
+//  * b0/b1 are the caller's registers, zero in every lane that holds no
+//    diagonal entry: only the 8 lanes on the diagonal load (predicated), the
+//    others keep their zeros across units;
+//  * the 4-bit scales and mins are read from the scale bytes with ALU
+//    operations instead of a table: (2^23 + v) as a float, times s, minus
+//    2^23 * s, is v * s exactly in one fma.
 template <int NT>
 __device__ __forceinline__ void tile_unit_s(uint32_t blk0, uint32_t pitch, int h, int grp, int c,
                                             const LaneA &la, float inv4c, uint32_t xk, uint32_t sk,
-                                            uint32_t zero, uint32_t lut, const uint32_t (&off)[NT],
-                                            int nt, float (&part)[NT][2])
+                                            const uint32_t (&off)[NT], int nt, uint32_t (&b0)[8],
+                                            uint32_t (&b1)[8], float (&part)[NT][2])
 {
     const uint32_t blk1 = blk0 + 8 * pitch;
     const uint32_t dd0 = ptx::ld_s32(blk0 + 80), dd1 = ptx::ld_s32(blk1 + 80);
+    const uint32_t rot = (uint32_t)(c & 1) * 8u;
     HalfA ha;
     {
         const uint32_t m1 = la.m1, m2 = la.m2;
+        const uint32_t q0 = blk0 + la.off, q1 = blk1 + la.off;
 #pragma unroll
         for (int w = 0; w < 4; ++w) {
-            const uint32_t r0 = ptx::ld_s32(blk0 + la.off + 4 * w);
-            const uint32_t r1 = ptx::ld_s32(blk1 + la.off + 4 * w);
+            const uint32_t o = (4u * w + rot) & 15u;
+            const uint32_t r0 = ptx::ld_s32(q0 + o), r1 = ptx::ld_s32(q1 + o);
             const uint32_t r0h = r0 >> 8, r1h = r1 >> 8;
             ha.a[2 * w][0] = ptx::lop3_and_or(r0, m1, 0x64006400u);
             ha.a[2 * w][1] = ptx::lop3_and_or(r1, m1, 0x64006400u);
@@ -333,29 +352,38 @@ __device__ __forceinline__ void tile_unit_s(uint32_t blk0, uint32_t pitch, int h
         }
     }
     const uint32_t sb0 = ptx::ld_s16(blk0 + 8 * h + 2 * c), sb1 = ptx::ld_s16(blk1 + 8 * h + 2 * c);
-    const float2 q00 = ptx::ld_s64f(lut + 8 * (sb0 & 0xFFu)), q01 = ptx::ld_s64f(lut + 8 * (sb0 >> 8));
-    const float2 q10 = ptx::ld_s64f(lut + 8 * (sb1 & 0xFFu)), q11 = ptx::ld_s64f(lut + 8 * (sb1 >> 8));
     const float d0 = half_bits(dd0 & 0xFFFFu) * inv4c, dm0 = half_bits(dd0 >> 16);
     const float d1 = half_bits(dd1 & 0xFFFFu) * inv4c, dm1 = half_bits(dd1 >> 16);
-    const float s00 = d0 * q00.x, s01 = d0 * q01.x, m00 = dm0 * q00.y, m01 = dm0 * q01.y;
-    const float s10 = d1 * q10.x, s11 = d1 * q11.x, m10 = dm1 * q10.y, m11 = dm1 * q11.y;
-    const bool act = (grp & 3) == c, lo = grp < 4;
+    const float nd0 = -8388608.0f * d0, ndm0 = -8388608.0f * dm0;
+    const float nd1 = -8388608.0f * d1, ndm1 = -8388608.0f * dm1;
+    const float s00 = fmaf(nib23(sb0), d0, nd0), s01 = fmaf(nib23(sb0 >> 8), d0, nd0);
+    const float m00 = fmaf(nib23(sb0 >> 4), dm0, ndm0), m01 = fmaf(nib23(sb0 >> 12), dm0, ndm0);
+    const float s10 = fmaf(nib23(sb1), d1, nd1), s11 = fmaf(nib23(sb1 >> 8), d1, nd1);
+    const float m10 = fmaf(nib23(sb1 >> 4), dm1, ndm1), m11 = fmaf(nib23(sb1 >> 12), dm1, ndm1);
+    const uint32_t ld_lo = (grp & 3) == c && grp < 4, ld_hi = (grp & 3) == c && grp >= 4;
+    const uint32_t sw = (uint32_t)(c & 1) * 16u;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
         if (j < nt) {
             const uint32_t xa = xk + 2 * (off[j] + 128 * h + 16 * grp);
-            const uint32_t p0 = act && lo ? xa : zero, p1 = act && !lo ? xa : zero;
             const float2 xx = ptx::ld_s64f(sk + 4 * ((off[j] >> 4) + 8 * h + 2 * c));
-            const uint4 u0 = ptx::ld_s128(p0), u1 = ptx::ld_s128(p0 + 16);
-            const uint4 v0 = ptx::ld_s128(p1), v1 = ptx::ld_s128(p1 + 16);
-            const uint32_t b0[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-            const uint32_t b1[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-            float d[4] = {-1024.0f * xx.x, -1024.0f * xx.y, -1024.0f * xx.x, -1024.0f * xx.y};
+            ptx::ld_s128_if(ld_lo, xa + sw, b0);
+            ptx::ld_s128_if(ld_lo, xa + (sw ^ 16u), b0 + 4);
+            ptx::ld_s128_if(ld_hi, xa + sw, b1);
+            ptx::ld_s128_if(ld_hi, xa + (sw ^ 16u), b1 + 4);
+            // two accumulator chains (even and odd MMAs) halve the dependent latency
+            float de[4] = {-1024.0f * xx.x, -1024.0f * xx.y, -1024.0f * xx.x, -1024.0f * xx.y};
+            float dq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-            for (int t = 0; t < 8; ++t) ptx::mma_16816(d, ha.a[t], b0[t], b1[t], d);
+            for (int t = 0; t < 8; t += 2) {
+                ptx::mma_16816(de, ha.a[t], b0[t], b1[t], de);
+                ptx::mma_16816(dq, ha.a[t + 1], b0[t + 1], b1[t + 1], dq);
+            }
             float p = part[j][0], r = part[j][1];
-            p = fmaf(s00, d[0], p); p = fmaf(s01, d[1], p); p = fmaf(-m00, xx.x, p); p = fmaf(-m01, xx.y, p);
-            r = fmaf(s10, d[2], r); r = fmaf(s11, d[3], r); r = fmaf(-m10, xx.x, r); r = fmaf(-m11, xx.y, r);
+            p = fmaf(s00, de[0] + dq[0], p); p = fmaf(s01, de[1] + dq[1], p);
+            p = fmaf(-m00, xx.x, p); p = fmaf(-m01, xx.y, p);
+            r = fmaf(s10, de[2] + dq[2], r); r = fmaf(s11, de[3] + dq[3], r);
+            r = fmaf(-m10, xx.x, r); r = fmaf(-m11, xx.y, r);
             part[j][0] = p;
             part[j][1] = r;
         }
@@ -464,21 +492,22 @@ __device__ void route_warp(const DecArgs &a, RouteSmem &r)
         topk_warp(a.logits + (size_t)t * a.E, a.E, a.k, a.score, r.ids + t * a.k, r.wts + t * a.k);
     __syncwarp();
     const bool valid = lane < a.A;
-    const int e = valid ? r.ids[lane] : (1 << 20);           // invalid lanes sort last
-    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int e = valid ? r.ids[lane] : 0x1FF;               // invalid lanes sort last
+    // lanes whose expert id is smaller than this lane's (`less`) or equal
+    // (`peers`), one ballot per bit of the 9-bit key, most significant first
+    unsigned less = 0u, peers = 0xffffffffu;
+#pragma unroll
+    for (int b = 8; b >= 0; --b) {
+        const unsigned bit = (unsigned)(e >> b) & 1u;
+        const unsigned ones = __ballot_sync(0xffffffffu, bit);
+        if (bit) less |= peers & ~ones;
+        peers &= bit ? ones : ~ones;
+    }
     const int rank = __popc(peers & ((1u << lane) - 1u));
     const bool leader = valid && rank == 0;
-    int off = 0, aidx = 0;
-    for (int L = 0; L < 32; ++L) {
-        const int thr = __shfl_sync(0xffffffffu, e, L);
-        const unsigned lt = __ballot_sync(0xffffffffu, valid && e < thr);
-        const unsigned llt = __ballot_sync(0xffffffffu, leader && e < thr);
-        if (lane == L) {
-            off = __popc(lt);
-            aidx = __popc(llt);
-        }
-    }
     const unsigned lm = __ballot_sync(0xffffffffu, leader);
+    const int off = __popc(less);              // invalid keys are larger than every valid one
+    const int aidx = __popc(less & lm);
     if (valid) {
         r.perm[off + rank] = lane;
         r.slot[lane] = off + rank;
@@ -561,7 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ RouteSmem rs;
     __shared__ __align__(16) __half zero[16];
-    __shared__ __align__(8) float2 sc_lut[256];   // scale byte -> {low nibble, high nibble}
     __shared__ int s_pabort, s_cabort, s_consumed, s_issued;
     __shared__ Job jobs[2];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -576,8 +604,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
     __half *x_s = reinterpret_cast<__half *>(p);
     float *xs_s = reinterpret_cast<float *>(p + x_bytes);
     float *red = reinterpret_cast<float *>(p + x_bytes + xs_bytes);       // [2][16][NT][16] gate/up
-    float *redd = red + 2 * kConsumers * NT * kTileM;                     // [2][16][NT][16] down
-    float *obuf = redd + 2 * kConsumers * NT * kTileM;                    // [A][32]
+    float *redd = red + 2 * kConsumers * NT * kTileM;                     // [kDownPairs][16][NT][16] down
+    float *obuf = redd + kDownPairs * kConsumers * NT * kTileM;           // [A][32]
     int *tags = reinterpret_cast<int *>(obuf + (size_t)a.A * kDownRows);  // [stages][kTagWords]
     uint64_t *bars = reinterpret_cast<uint64_t *>(tags + kTagWords * a.stages);
     uint64_t *full = bars, *empty = bars + a.stages;
@@ -594,10 +622,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
         s_issued = 0;
     }
     if (tid < 16) zero[tid] = __float2half_rn(0.0f);
-    if (tid < 256) sc_lut[tid] = make_float2((float)(tid & 15), (float)(tid >> 4));
     if (a.T <= kWarpRouteT && a.A <= 32) {
-        // the producer warp routes while the other warps convert x
-        __syncthreads();
+        // the producer warp routes while the other warps convert x (neither
+        // needs the barriers or tables set up above until the barrier below)
         if (warp == kProducerWarp) {
             route_warp(a, rs);
         } else if (a.x_smem) {
@@ -636,8 +663,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
                 }
                 return !*(volatile int *)&s_cabort;
             };
-            while (ok) {
-                const int it = atomicAdd(claim_gu, 1);
+            // the first item of each CTA is its index; later ones come from the
+            // counter, offset by the grid (no atomic round trip at start-up)
+            for (bool first = true; ok; first = false) {
+                const int it = first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(claim_gu, 1);
                 if (it >= gu_items) break;
                 int s;
                 if (!(ok = slot(s))) break;
@@ -743,8 +772,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
         const int wm = (warp >> 1) & 1, wh = warp & 1, wk = warp >> 2;
         const LaneA la_ = lane_a(wh, c);
         const uint32_t x_s_a = ptx::smem_addr(x_s), xs_s_a = ptx::smem_addr(xs_s);
-        const uint32_t zero_a = ptx::smem_addr(zero), lut_a = ptx::smem_addr(sc_lut);
-        int rb = 0, uses0 = 0, uses1 = 0, rbd = 0;
+        // activation operand registers: zero except in the lanes on the block
+        // diagonal, which reload them per unit (see tile_unit_s)
+        uint32_t bz0[8], bz1[8];
+#pragma unroll
+        for (int t = 0; t < 8; ++t) bz0[t] = bz1[t] = 0u;
+        int rb = 0, uses0 = 0, uses1 = 0;
         // hands the partial sums in `part` to the epilogue warp as job `jb`
         auto emit = [&](const Job &jb, float (&part)[NT][2]) {
             int &uses = rb ? uses1 : uses0;
@@ -785,8 +818,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
                         const uint32_t mat_s = ptx::smem_addr(mat);
                         for (int kb = wk; kb < a.H_blocks; kb += kConsumers / 4)
                             tile_unit_s<NT>(mat_s + kb * kQ2KBytes, (uint32_t)a.gu_pitch, wh, grp, c, la_,
-                                            inv4c, x_s_a + kb * kQK * 2, xs_s_a + kb * 64, zero_a,
-                                            lut_a, off, nt, part);
+                                            inv4c, x_s_a + kb * kQK * 2, xs_s_a + kb * 64, off, nt,
+                                            bz0, bz1, part);
                     } else {
                         for (int kb = wk; kb < a.H_blocks; kb += kConsumers / 4)
                             tile_unit<NT, false>(mat + kb * kQ2KBytes, a.gu_pitch, wh, grp, c, la_, inv4c,
@@ -796,54 +829,75 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
                 }
             } else {
                 const int it = tg[1], j0 = tg[2], cnt = tg[3];
-                for (int jj = 0; jj < cnt; ++jj) {
-                    const int e = rs.act[j0 + jj];
-                    const int seg0 = rs.off[e], seg_n = rs.cnt[e];
-                    const uint8_t *mat = st + tg[4 + 2 * jj] + (size_t)(wm * kTileM + grp) * a.dn_pitch;
-                    const int hoff = tg[5 + 2 * jj];
-                    const __half *h_s = reinterpret_cast<const __half *>(st + (hoff >= 0 ? hoff : 0));
-                    const float *hs_s = reinterpret_cast<const float *>(st + (hoff >= 0 ? hoff : 0) +
-                                                                        (size_t)seg_n * h_row);
-                    for (int c0 = 0; c0 < seg_n; c0 += NT) {
-                        const int nt = min(NT, seg_n - c0);
+                // The stage's (expert, token chunk) pairs, in rounds of up to
+                // kDownPairs.  Inside a round the (pair, K block) units are
+                // dealt to the four K-phase warps of each (m-tile, half) in
+                // turn, so every warp gets the same number of units; each warp
+                // leaves one partial sum per pair, and one barrier per round
+                // precedes the reduction into obuf.
+                int rj = 0, rc = 0;                  // first pair of the round
+                while (rj < cnt) {
+                    int np = 0, qj = rj, qc = rc;
+                    for (; np < kDownPairs && qj < cnt; ++np) {
+                        const int e = rs.act[j0 + qj];
+                        const int seg0 = rs.off[e], seg_n = rs.cnt[e];
+                        const int nt = min(NT, seg_n - qc);
+                        const uint8_t *mat = st + tg[4 + 2 * qj] + (size_t)(wm * kTileM + grp) * a.dn_pitch;
+                        const int hoff = tg[5 + 2 * qj];
                         float part[NT][2];
 #pragma unroll
                         for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
+                        const int kb0 = ((wk - np * a.I_blocks) % 4 + 4) % 4;
                         if (hoff >= 0) {
                             uint32_t off[NT];
 #pragma unroll
-                            for (int j = 0; j < NT; ++j) off[j] = (uint32_t)(c0 + (j < nt ? j : 0)) * a.I_pad;
+                            for (int j = 0; j < NT; ++j) off[j] = (uint32_t)(qc + (j < nt ? j : 0)) * a.I_pad;
                             const uint32_t mat_s = ptx::smem_addr(mat);
-                            const uint32_t h_a = ptx::smem_addr(h_s), hs_a = ptx::smem_addr(hs_s);
-                            for (int kb = wk; kb < a.I_blocks; kb += kConsumers / 4)
+                            const uint32_t h_a = ptx::smem_addr(st + hoff);
+                            const uint32_t hs_a = h_a + (uint32_t)seg_n * h_row;
+                            for (int kb = kb0; kb < a.I_blocks; kb += kConsumers / 4)
                                 tile_unit_s<NT>(mat_s + kb * kQ2KBytes, (uint32_t)a.dn_pitch, wh, grp, c,
-                                                la_, inv4c, h_a + kb * kQK * 2, hs_a + kb * 64, zero_a,
-                                                lut_a, off, nt, part);
+                                                la_, inv4c, h_a + kb * kQK * 2, hs_a + kb * 64, off, nt,
+                                                bz0, bz1, part);
                         } else {
                             uint32_t off[NT];
 #pragma unroll
                             for (int j = 0; j < NT; ++j)
-                                off[j] = (uint32_t)(seg0 + c0 + (j < nt ? j : 0)) * a.I_pad;
-                            for (int kb = wk; kb < a.I_blocks; kb += kConsumers / 4)
+                                off[j] = (uint32_t)(seg0 + qc + (j < nt ? j : 0)) * a.I_pad;
+                            for (int kb = kb0; kb < a.I_blocks; kb += kConsumers / 4)
                                 tile_unit<NT, false>(mat + kb * kQ2KBytes, a.dn_pitch, wh, grp, c, la_, inv4c,
                                                      a.hp + kb * kQK, a.hs + kb * 16, zero, off, nt, part);
                         }
-                        // the down partial sums are finished here, by the consumers
-                        float *rbuf = redd + rbd * kConsumers * NT * kTileM;
-                        store_partials<NT>(rbuf, warp, grp, c, part);
-                        consumer_sync();
-                        if (tid < nt * kDownRows) {
-                            const int row = tid & 31, j = tid >> 5;
+                        store_partials<NT>(redd + (size_t)np * kConsumers * NT * kTileM, warp, grp, c, part);
+                        qc += NT;
+                        if (qc >= seg_n) { ++qj; qc = 0; }
+                    }
+                    consumer_sync();
+                    // the down partial sums are finished here, by the consumers:
+                    // thread i -> pair i / (NT * 32), vector, row
+                    for (int i = tid; i < np * NT * kDownRows; i += kConsumers * 32) {
+                        const int pq = i / (NT * kDownRows), rem = i % (NT * kDownRows);
+                        const int j = rem / kDownRows, row = rem % kDownRows;
+                        int pj = rj, pc = rc;                  // walk to pair pq
+                        for (int w = 0; w < pq; ++w) {
+                            pc += NT;
+                            if (pc >= rs.cnt[rs.act[j0 + pj]]) { ++pj; pc = 0; }
+                        }
+                        const int e = rs.act[j0 + pj];
+                        if (pc + j < rs.cnt[e]) {
                             const int mtl = row >> 4, r16 = row & 15;
+                            const float *rbuf = redd + (size_t)pq * kConsumers * NT * kTileM;
                             // warps with (warp >> 1) & 1 == mtl hold rows mtl*16 .. +15
                             float o = 0.0f;
 #pragma unroll
                             for (int w = 0; w < kConsumers; ++w)
                                 if (((w >> 1) & 1) == mtl) o += rbuf[((size_t)w * NT + j) * kTileM + r16];
-                            obuf[(size_t)(seg0 + c0 + j) * kDownRows + row] = o;
+                            obuf[(size_t)(rs.off[e] + pc + j) * kDownRows + row] = o;
                         }
-                        rbd ^= 1;
                     }
+                    rj = qj;
+                    rc = qc;
+                    if (rj < cnt) consumer_sync();       // redd is reused by the next round
                 }
                 if (j0 + cnt == n_act) {
                     // every expert of this item is in obuf: weighted combine in slot order
@@ -929,8 +983,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
 // tcgen05 decode kernel (decode_tc_kernel)
 //
 // The block-diagonal trick of the mma.sync kernel above, on the 5th
-// generation tensor core.  Per 16-row... rather, per 128-row tile and
-// 256-wide K block: the dequantizing warps store the raw fields
+// generation tensor core, for 9..32 tokens (where the mma.sync kernel's
+// 8-column operand would be re-run per chunk of tokens).  Per 128-row tile
+// and 256-wide K block: the dequantizing warps store the raw fields
 // (1024 + q * 4^g, exact fp16, lop3 only) of their row to tensor memory as
 // the MMA's A operand; B, in shared memory, is block-diagonal over the 16
 // sub-blocks: row (t, s) of B holds activation vector t only in the 16
@@ -948,24 +1003,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
 //   down     (token chunk, 128 rows of H): y_slot[p, m] = w_p * o; the CTA
 //             that completes the last chunk of an m-tile combines y in slot
 //             order.
-// A down item waits (bounded) until its expert's h is complete.
+// A down item waits (bounded) until its expert's h is complete.  Warps: 0 TMA
+// producer (3-D tensor maps over 112-byte block windows; rows that are not a
+// multiple of 16 bytes use several row phases), 1 MMA issuer, 2..9 two
+// dequantizing warpgroups that are also the epilogue, which lags the MMAs by
+// one K block.
 // ===========================================================================
-// decode_tc_kernel: the same layer on the 5th-generation tensor cores, for
-// 9..32 tokens, where the mma.sync kernel's fixed 8-column operand would be
-// re-streamed per token chunk.  One work item is 128 weight rows of one
-// expert and up to kNtMax of its segment's tokens (a K split of 2 when there
-// are fewer items than SMs).  The block-diagonal idea carries over with a
-// wider N: for each token the 16 sub-blocks of a 256-wide block are 16 MMA
-// columns, so a 64-column B operand in shared memory (zero off the diagonal)
-// serves 4 tokens, and D column 16t+s is token t's dot over sub-block s.
-// The dequantizing warps store only the raw fields 1024 + q*4^g to tensor
-// memory (no scale arithmetic per weight); the scales, the mins and the
-// -1024*X correction are applied per sub-block in an fp32 epilogue that
-// lags the MMAs by one K block.  Warps: 0 TMA producer (3-D tensor maps
-// over 112-byte block windows, row phases for rows that are not a multiple
-// of 16 bytes), 1 MMA issuer, 2..9 two dequantizing warpgroups that are
-// also the epilogue.  Down items write yslot rows; the last CTA to finish a
-// 128-row y tile sums its slots in slot order (deterministic).
 namespace tcd {
 
 constexpr int kBM = 128;
@@ -1599,7 +1642,7 @@ int64_t smem_pitch(int64_t row_bytes)
 size_t fixed_smem(const DecArgs &a, int nt)
 {
     const size_t x = a.x_smem ? (size_t)a.T * a.H * 2 + (size_t)a.T * (a.H / 16) * 4 : 0;
-    return x + (size_t)4 * kConsumers * nt * kTileM * 4 + (size_t)a.A * kDownRows * 4 +
+    return x + (size_t)(2 + kDownPairs) * kConsumers * nt * kTileM * 4 + (size_t)a.A * kDownRows * 4 +
            4 * (size_t)kTagWords * a.stages + 8 * (2 * (size_t)a.stages);
 }
 
@@ -1743,7 +1786,8 @@ bool decode_path_supported(const Plan &p, const ds4g_moe_desc *d)
     const size_t gu = (size_t)2 * kTileM * smem_pitch(d->gate_up_row_bytes);
     const size_t dn = (size_t)kDownRows * smem_pitch(d->down_row_bytes);
     const size_t stage = (std::max(gu, dn) + 127) / 128 * 128;
-    const size_t fixed = (size_t)4 * kConsumers * 4 * kTileM * 4 + (size_t)p.A * kDownRows * 4 + 1024;
+    const size_t fixed = (size_t)(2 + kDownPairs) * kConsumers * 4 * kTileM * 4 +
+                         (size_t)p.A * kDownRows * 4 + 1024;
     return 2 * stage + fixed <= kSmemBudget;
 }
 

@@ -162,6 +162,15 @@ __device__ __forceinline__ uint4 ld_s128(uint32_t a)
                  : "memory");
     return v;
 }
+// 16 bytes into v[0..3] when p != 0 (per lane); otherwise v keeps its value.
+__device__ __forceinline__ void ld_s128_if(uint32_t p, uint32_t a, uint32_t *v)
+{
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %4, 0;\n\t"
+                 "@q ld.shared.v4.b32 {%0, %1, %2, %3}, [%5];\n\t}"
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3])
+                 : "r"(p), "r"(a)
+                 : "memory");
+}
 __device__ __forceinline__ float2 ld_s64f(uint32_t a)
 {
     float2 v;
