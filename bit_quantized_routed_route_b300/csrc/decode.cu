@@ -133,9 +133,14 @@ __device__ __forceinline__ void build_half_a(HalfA &ha, const uint8_t *blk0, con
     }
 }
 
-constexpr int kConsumers = 16;
+constexpr int kConsumers = 12;
+constexpr int kKPhases = kConsumers / 4;   // warps per (matrix or m-tile, half) pair
 constexpr int kProducerWarp = kConsumers;
 constexpr int kThreads = (kConsumers + 2) * 32;
+// Register budget: with 14 warps at most 4 share an SM sub-partition (16K
+// registers), so 128 registers per thread fit; bounds of 512 threads let the
+// compiler use them.
+constexpr int kLaunchBound = 512;
 // named barriers: 1 = consumers only; 2, 3 = reduction buffer 0/1 filled
 // (consumers arrive, epilogue warp waits); 4, 5 = buffer 0/1 released
 // (epilogue warp arrives, consumers wait)
@@ -585,7 +590,7 @@ __global__ void __launch_bounds__(256) decode_pre_kernel(int32_t *status, int32_
 }
 
 template <int NT>
-__global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
+__global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ RouteSmem rs;
@@ -768,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
         // ---------------- consumers ----------------
         const float inv4c = 1.0f / (float)(1 << (2 * c));
         // each consumer warp owns one (matrix or m-tile, half) pair and every
-        // fourth K block: units u = 4*kb + 2*wm + wh with u = warp (mod 16)
+        // kKPhases-th K block: warp = 4 * wk + 2 * wm + wh, K blocks kb = wk (mod kKPhases)
         const int wm = (warp >> 1) & 1, wh = warp & 1, wk = warp >> 2;
         const LaneA la_ = lane_a(wh, c);
         const uint32_t x_s_a = ptx::smem_addr(x_s), xs_s_a = ptx::smem_addr(xs_s);
@@ -816,12 +821,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
                     for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
                     if (a.x_smem) {
                         const uint32_t mat_s = ptx::smem_addr(mat);
-                        for (int kb = wk; kb < a.H_blocks; kb += kConsumers / 4)
+                        for (int kb = wk; kb < a.H_blocks; kb += kKPhases)
                             tile_unit_s<NT>(mat_s + kb * kQ2KBytes, (uint32_t)a.gu_pitch, wh, grp, c, la_,
                                             inv4c, x_s_a + kb * kQK * 2, xs_s_a + kb * 64, off, nt,
                                             bz0, bz1, part);
                     } else {
-                        for (int kb = wk; kb < a.H_blocks; kb += kConsumers / 4)
+                        for (int kb = wk; kb < a.H_blocks; kb += kKPhases)
                             tile_unit<NT, false>(mat + kb * kQ2KBytes, a.gu_pitch, wh, grp, c, la_, inv4c,
                                                  a.xp + kb * kQK, a.xs + kb * 16, zero, off, nt, part);
                     }
@@ -847,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
                         float part[NT][2];
 #pragma unroll
                         for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
-                        const int kb0 = ((wk - np * a.I_blocks) % 4 + 4) % 4;
+                        const int kb0 = ((wk - np * a.I_blocks) % kKPhases + kKPhases) % kKPhases;
                         if (hoff >= 0) {
                             uint32_t off[NT];
 #pragma unroll
@@ -855,7 +860,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
                             const uint32_t mat_s = ptx::smem_addr(mat);
                             const uint32_t h_a = ptx::smem_addr(st + hoff);
                             const uint32_t hs_a = h_a + (uint32_t)seg_n * h_row;
-                            for (int kb = kb0; kb < a.I_blocks; kb += kConsumers / 4)
+                            for (int kb = kb0; kb < a.I_blocks; kb += kKPhases)
                                 tile_unit_s<NT>(mat_s + kb * kQ2KBytes, (uint32_t)a.dn_pitch, wh, grp, c,
                                                 la_, inv4c, h_a + kb * kQK * 2, hs_a + kb * 64, off, nt,
                                                 bz0, bz1, part);
@@ -864,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_q2k_kernel(DecArgs a)
 #pragma unroll
                             for (int j = 0; j < NT; ++j)
                                 off[j] = (uint32_t)(seg0 + qc + (j < nt ? j : 0)) * a.I_pad;
-                            for (int kb = kb0; kb < a.I_blocks; kb += kConsumers / 4)
+                            for (int kb = kb0; kb < a.I_blocks; kb += kKPhases)
                                 tile_unit<NT, false>(mat + kb * kQ2KBytes, a.dn_pitch, wh, grp, c, la_, inv4c,
                                                      a.hp + kb * kQK, a.hs + kb * 16, zero, off, nt, part);
                         }
