@@ -592,6 +592,9 @@ __global__ void __launch_bounds__(256) decode_pre_kernel(int32_t *status, int32_
 template <int NT>
 __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
 {
+    // one vector: the launcher guarantees that x and every expert's h rows
+    // sit in shared memory, so the global-memory unit paths are compiled out
+    constexpr bool kSmemOnly = NT == 1;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ RouteSmem rs;
     __shared__ __align__(16) __half zero[16];
@@ -819,7 +822,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                     float part[NT][2];
 #pragma unroll
                     for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
-                    if (a.x_smem) {
+                    if (kSmemOnly || a.x_smem) {
                         const uint32_t mat_s = ptx::smem_addr(mat);
                         for (int kb = wk; kb < a.H_blocks; kb += kKPhases)
                             tile_unit_s<NT>(mat_s + kb * kQ2KBytes, (uint32_t)a.gu_pitch, wh, grp, c, la_,
@@ -853,7 +856,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
 #pragma unroll
                         for (int j = 0; j < NT; ++j) part[j][0] = part[j][1] = 0.0f;
                         const int kb0 = ((wk - np * a.I_blocks) % kKPhases + kKPhases) % kKPhases;
-                        if (hoff >= 0) {
+                        if (kSmemOnly || hoff >= 0) {
                             uint32_t off[NT];
 #pragma unroll
                             for (int j = 0; j < NT; ++j) off[j] = (uint32_t)(qc + (j < nt ? j : 0)) * a.I_pad;
@@ -1855,8 +1858,12 @@ cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const 
     if (events && (e = record_phase(events[1], s)) != cudaSuccess) return e;
 
     // token chunk per pass: segments longer than 4 run in several chunks
-    if (la.T <= 1) return launch_nt<1>(a, dev, s, events);
-    if (la.T <= 2) return launch_nt<2>(a, dev, s, events);
+    // the one-vector kernel reads x and h from shared memory only
+    const size_t dn_stage = (size_t)kDownRows * a.dn_pitch + (size_t)a.I_pad * 2 + (size_t)(a.I_pad / 16) * 4;
+    const size_t gu_stage = (size_t)2 * kTileM * a.gu_pitch;
+    if (la.T <= 1 && a.x_smem && dn_stage <= std::max(gu_stage, (size_t)kDownRows * a.dn_pitch))
+        return launch_nt<1>(a, dev, s, events);
+    if (la.T <= 2) return launch_nt<2>(a, dev, s, events);   // also T = 1 otherwise
     return launch_nt<4>(a, dev, s, events);
 }
 
