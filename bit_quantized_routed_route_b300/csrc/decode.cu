@@ -20,10 +20,10 @@
 // cp.async.bulk (TMA, no tensor map) completing on mbarriers; a down stage
 // also carries the h rows of its experts.  The ring keeps streaming W_down
 // right after W_gate/W_up, so HBM does not idle at the phase boundary.
-// Sixteen consumer warps dequantize in registers straight into mma.sync
+// Twelve consumer warps dequantize in registers straight into mma.sync
 // m16n8k16 fragments; each warp owns one (matrix, half) pair and every
-// fourth K block of a tile, and the warps' partial sums meet in shared
-// memory.
+// third K block of a tile, and the warps' partial sums meet in shared
+// memory.  (Fourteen warps in all, so each thread may use 128 registers.)
 //
 // Phase order without a grid barrier: a gate/up tile bumps its expert's
 // completion counter after its h rows are written (fence, then atomic); the
