@@ -14,68 +14,63 @@ constexpr int kMaxPerLane = 8;   // 256 experts / 32 lanes
 
 __device__ __forceinline__ float canon(float v) { return v != v ? -INFINITY : v; }
 
-// a ranks before b
-__device__ __forceinline__ bool before(float va, int ia, float vb, int ib)
+// Order-preserving map of a non-NaN float to an unsigned key (larger float,
+// larger key; -0 is mapped as +0 so that the two zeros tie as they compare
+// equal), and back.  Every key of a real logit, -inf included, is above 0.
+__device__ __forceinline__ uint32_t order_key(float v)
 {
-    return ib < 0 || (ia >= 0 && (va > vb || (va == vb && ia < ib)));
+    const uint32_t u = __float_as_uint(v == 0.0f ? 0.0f : v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t o)
+{
+    return __uint_as_float((o & 0x80000000u) ? (o & 0x7FFFFFFFu) : ~o);
 }
 
-// One token, one warp.  Writes ids[k], wts[k] (lane 0).
+// One token, one warp.  Writes ids[k], wts[k] (lanes 0..k-1).  Each round the
+// warp takes the largest remaining key with two warp reductions (the largest
+// key, then the smallest expert id holding it), so the order is: larger
+// logit first, equal logits -> lower id first.  Lane i keeps pick i; the
+// weights are formed with the picks' fp32 values and summed in pick order.
 __device__ __forceinline__ void topk_warp(const float *__restrict__ row, int E, int k, int score,
                                           int32_t *__restrict__ ids, float *__restrict__ wts)
 {
     const int lane = threadIdx.x & 31;
-    float v[kMaxPerLane];
+    uint32_t key[kMaxPerLane];
     uint32_t avail = 0;
 #pragma unroll
     for (int j = 0; j < kMaxPerLane; ++j) {
-        int e = lane + 32 * j;
-        v[j] = -INFINITY;
+        const int e = lane + 32 * j;
+        key[j] = 0u;
         if (e < E) {
-            v[j] = canon(__ldg(row + e));
+            key[j] = order_key(canon(__ldg(row + e)));
             avail |= 1u << j;
         }
     }
-    float sel_v[DS4G_MAX_TOPK];
-    int sel_i[DS4G_MAX_TOPK];
+    float my_v = 0.0f;
+    int my_id = 0;
 #pragma unroll
     for (int i = 0; i < DS4G_MAX_TOPK; ++i) {
         if (i >= k) break;
-        float bv = -INFINITY;
-        int bi = -1;
+        // this lane's best remaining key; equal keys keep the lower j (lower id)
+        uint32_t bk = 0u;
+        int bj = 0;
 #pragma unroll
-        for (int j = 0; j < kMaxPerLane; ++j) {
-            if ((avail >> j) & 1u) {
-                int e = lane + 32 * j;
-                if (before(v[j], e, bv, bi)) { bv = v[j]; bi = e; }
-            }
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-        }
-        if ((bi & 31) == lane) avail &= ~(1u << (bi >> 5));
-        sel_v[i] = bv;
-        sel_i[i] = bi;
+        for (int j = 0; j < kMaxPerLane; ++j)
+            if (((avail >> j) & 1u) && key[j] > bk) { bk = key[j]; bj = j; }
+        const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bj) : 0xFFFFFFFFu);
+        if ((int)(win & 31u) == lane) avail &= ~(1u << (win >> 5));
+        if (lane == i) { my_v = key_value(m); my_id = (int)win; }
     }
-    if (lane == 0) {
-        float p[DS4G_MAX_TOPK];
-        float sum = 0.0f;
-        if (score == DS4G_SCORE_SOFTMAX) {
-            float m = sel_v[0];
-#pragma unroll
-            for (int i = 0; i < DS4G_MAX_TOPK; ++i)
-                if (i < k) { p[i] = expf(sel_v[i] - m); sum += p[i]; }
-        } else {
-#pragma unroll
-            for (int i = 0; i < DS4G_MAX_TOPK; ++i)
-                if (i < k) { p[i] = 1.0f / (1.0f + expf(-sel_v[i])); sum += p[i]; }
-        }
-#pragma unroll
-        for (int i = 0; i < DS4G_MAX_TOPK; ++i)
-            if (i < k) { ids[i] = sel_i[i]; wts[i] = p[i] / sum; }
+    const float top = __shfl_sync(0xffffffffu, my_v, 0);
+    float p = 0.0f;
+    if (lane < k) p = score == DS4G_SCORE_SOFTMAX ? expf(my_v - top) : 1.0f / (1.0f + expf(-my_v));
+    float sum = 0.0f;
+    for (int i = 0; i < k; ++i) sum += __shfl_sync(0xffffffffu, p, i);
+    if (lane < k) {
+        ids[lane] = my_id;
+        wts[lane] = p / sum;
     }
 }
 
