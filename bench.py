@@ -191,17 +191,25 @@ def layer_path(cfg: S.Config) -> str:
     return "tc" if tc else "general"
 
 
-def kernel_source_hash() -> str:
-    """Hash of the kernel sources with comments and blank lines removed, so a
+# The sources each profiled kernel is built from: a recorded DRAM traffic
+# stays valid while these (comments and blank lines aside) are unchanged.
+KERNEL_SOURCES = {
+    "decode": ("decode.cu", "topk.cuh", "ptx.cuh", "tmap.cuh", "ds4g_common.cuh"),
+    "tc_gateup": ("tc.cu", "ptx.cuh", "tmap.cuh", "ds4g_common.cuh"),
+    "gateup": ("gemv.cu", "ptx.cuh", "ds4g_common.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    """Hash of a kernel's sources with comments and blank lines removed, so a
     comment edit keeps recorded counters valid and a code edit drops them."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "bit_quantized_routed_route_b300", "csrc")
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh")):
-            text = open(os.path.join(csrc, name), encoding="utf-8").read()
-            lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
-            h.update(name.encode())
-            h.update("\n".join(ln for ln in lines if ln).encode())
+    for name in sorted(KERNEL_SOURCES[kernel]):
+        text = open(os.path.join(csrc, name), encoding="utf-8").read()
+        lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+        h.update(name.encode())
+        h.update("\n".join(ln for ln in lines if ln).encode())
     return h.hexdigest()[:16]
 
 
@@ -211,7 +219,7 @@ def measured_traffic(kernel: str, workload: str):
     try:
         t = json.load(open(TRAFFIC_FILE))
         e = t[workload][kernel]
-        if e.get("source_hash") == kernel_source_hash():
+        if e.get("source_hash") == kernel_source_hash(kernel):
             return float(e["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
         pass
