@@ -9,8 +9,8 @@
 //
 // Kernels:
 //   topk_kernel   one warp per token; each lane holds E/32 logits in
-//                 registers; k rounds of a butterfly arg-max over the
-//                 (logit desc, id asc) order.
+//                 registers; k rounds of two warp reductions (largest
+//                 order key, then lowest expert id holding it).
 //   scan_kernel   one CTA: histogram, exclusive scan, then a stable counting
 //                 sort of the assignments a = t*k + i by expert (warp
 //                 match-any ranks + per-warp bases), ascending t inside each
