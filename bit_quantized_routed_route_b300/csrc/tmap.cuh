@@ -8,7 +8,7 @@
 
 namespace ds4g {
 
-// cuTensorMapEncodeTiled from the driver, looked up once.
+// cuTensorMapEncodeTiled from the CUDA driver API, looked up once.
 cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000 *out);
 
 // 3-D map over [experts][rows / phases][phases * row_bytes / 4 words] of
