@@ -129,8 +129,10 @@ enum {
  *   expert strides >= rows * row_bytes and multiples of 16;
  *   w_gate, w_up, w_down 16-byte aligned;
  *   DS4G_FORCE_TC additionally needs row_bytes % 16 == 0.
- * tc_min_tokens: expert segments with at least this many tokens run on the
- * tensor-core kernels, the others on the GEMV kernels (0 = library default).
+ * tc_min_tokens: reserved for a per-segment split between the tensor-core
+ * and the GEMV kernels; validated (>= 0) and otherwise ignored: every
+ * segment of a call takes the path chosen for the call (see "Path" under
+ * ds4g_moe_forward).
  */
 typedef struct ds4g_moe_desc {
     int32_t hidden;
@@ -211,6 +213,12 @@ DS4G_API size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
  *           ds4g_moe_workspace_bytes(desc, T) bytes, 256-byte aligned.  After
  *           the call it holds the routing of this call (see
  *           ds4g_moe_routing_view).
+ * Path (one per call): Q2_K layers with inter % 16 == 0 and T <= 32 run
+ * the decode kernels (mma.sync up to 8 vectors, tcgen05 from 9 to 32, the
+ * latter with hidden % 128 == 0); otherwise layers whose row_bytes are
+ * multiples of 16 and hidden % 128 == 0 run the tensor-core kernels; all
+ * others run the GEMV kernels.  DS4G_FORCE_TC forces the tensor-core kernels
+ * and DS4G_FORCE_GEMV rules them out.
  * Errors: DS4G_ERR_INVALID, DS4G_ERR_SHAPE, DS4G_ERR_LAYOUT,
  * DS4G_ERR_WORKSPACE, DS4G_ERR_UNSUPPORTED (a forced path that cannot run),
  * DS4G_ERR_CUDA.  T == 0 is a no-op.
