@@ -512,7 +512,10 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "arithmetic": ("fp16 tensor-core operands (decode: exact 2-bit fields and fp16 "
+                       "activations; prefill: weights dequantized to fp16), fp32 accumulation "
+                       "and fp32 output"),
         "config": workload_config(cfg, copies,
                                   f"inputs larger than L2: {copies} rotating weight copies, "
                                   f"{touched.mean() / 1e6:.1f} MB touched per step"),
