@@ -690,11 +690,13 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                     ptx::bulk_g2s(st, g, gu_tile, &full[s]);
                     ptx::bulk_g2s(st + gu_tile, u, gu_tile, &full[s]);
                 } else {
-                    for (int r = 0; r < kTileM; ++r) {
-                        ptx::bulk_g2s(st + (size_t)r * a.gu_pitch, g + (size_t)r * a.gu_row,
-                                      (uint32_t)a.gu_row, &full[s]);
-                        ptx::bulk_g2s(st + (size_t)(kTileM + r) * a.gu_pitch, u + (size_t)r * a.gu_row,
-                                      (uint32_t)a.gu_row, &full[s]);
+                    // padded layout: pairs of rows, each pair one copy (see gu_pair)
+                    const size_t pp = 2 * (size_t)a.gu_pitch - 16;
+                    for (int r = 0; r < kTileM; r += 2) {
+                        ptx::bulk_g2s(st + (size_t)(r >> 1) * pp, g + (size_t)r * a.gu_row,
+                                      2 * (uint32_t)a.gu_row, &full[s]);
+                        ptx::bulk_g2s(st + (size_t)(kTileM / 2 + (r >> 1)) * pp, u + (size_t)r * a.gu_row,
+                                      2 * (uint32_t)a.gu_row, &full[s]);
                     }
                 }
                 s_issued = ++q;
@@ -812,7 +814,15 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                 const int it = tg[1];
                 const int e = rs.act[it / tiles], mt = it % tiles;
                 const int seg0 = rs.off[e], seg_n = rs.cnt[e];
-                const uint8_t *mat = st + (size_t)wm * kTileM * a.gu_pitch + (size_t)grp * a.gu_pitch;
+                // padded tiles hold row pairs back to back with 16 bytes after each
+                // pair: row r at (r / 2) * pp + (r % 2) * row_bytes, so row r + 8 is
+                // 4 pairs on, i.e. an effective pitch of pp / 2 for the unit
+                const bool paired = a.gu_pitch != a.gu_row;
+                const size_t pp = 2 * (size_t)a.gu_pitch - 16;
+                const uint32_t gu_step = paired ? (uint32_t)(pp / 2) : (uint32_t)a.gu_pitch;
+                const uint8_t *mat = paired ? st + (size_t)wm * (kTileM / 2) * pp + (size_t)(grp >> 1) * pp +
+                                                  (size_t)(grp & 1) * a.gu_row
+                                            : st + (size_t)wm * kTileM * a.gu_pitch + (size_t)grp * a.gu_pitch;
                 for (int c0 = 0; c0 < seg_n; c0 += NT) {
                     const int nt = min(NT, seg_n - c0);
                     uint32_t off[NT];
@@ -825,12 +835,12 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                     if (kSmemOnly || a.x_smem) {
                         const uint32_t mat_s = ptx::smem_addr(mat);
                         for (int kb = wk; kb < a.H_blocks; kb += kKPhases)
-                            tile_unit_s<NT>(mat_s + kb * kQ2KBytes, (uint32_t)a.gu_pitch, wh, grp, c, la_,
+                            tile_unit_s<NT>(mat_s + kb * kQ2KBytes, gu_step, wh, grp, c, la_,
                                             inv4c, x_s_a + kb * kQK * 2, xs_s_a + kb * 64, off, nt,
                                             bz0, bz1, part);
                     } else {
                         for (int kb = wk; kb < a.H_blocks; kb += kKPhases)
-                            tile_unit<NT, false>(mat + kb * kQ2KBytes, a.gu_pitch, wh, grp, c, la_, inv4c,
+                            tile_unit<NT, false>(mat + kb * kQ2KBytes, gu_step, wh, grp, c, la_, inv4c,
                                                  a.xp + kb * kQK, a.xs + kb * 16, zero, off, nt, part);
                     }
                     emit(Job{kJobGateUp, e, mt, seg0, c0, nt, it, 0}, part);
