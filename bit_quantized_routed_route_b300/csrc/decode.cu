@@ -671,10 +671,10 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                 }
                 return !*(volatile int *)&s_cabort;
             };
-            // the first item of each CTA is its index; later ones come from the
-            // counter, offset by the grid (no atomic round trip at start-up)
-            for (bool first = true; ok; first = false) {
-                const int it = first ? (int)blockIdx.x : (int)gridDim.x + atomicAdd(claim_gu, 1);
+            // every item comes from the counter, so an item that a down item
+            // waits for has always been claimed by a CTA that is running
+            while (ok) {
+                const int it = atomicAdd(claim_gu, 1);
                 if (it >= gu_items) break;
                 int s;
                 if (!(ok = slot(s))) break;
