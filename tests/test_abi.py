@@ -164,3 +164,39 @@ def test_routing_view_points_inside_the_workspace():
     assert len({v[n] for n in v}) == 5
     st, _ = D.moe_routing_view(d, 4, FAKE, need - 1)
     assert st == D.ERR_WORKSPACE
+
+def layer_desc(H, I, E, k, fmt=None, flags=0, align=1):
+    """A descriptor with packed (or `align`-padded) rows at a fake address."""
+    fmt = D.FMT_Q2K if fmt is None else fmt
+    bb = 84 if fmt == D.FMT_Q2K else 70
+    gr, dr = H // 256 * bb, -(-I // 256) * bb
+    gr, dr = -(-gr // align) * align, -(-dr // align) * align
+    return desc(hidden=H, inter=I, n_experts=E, top_k=k, format=fmt, flags=flags,
+                gate_up_row_bytes=gr, down_row_bytes=dr,
+                gate_up_expert_stride=-(-I * gr // 16) * 16,
+                down_expert_stride=-(-H * dr // 16) * 16,
+                codebook=FAKE if fmt == D.FMT_CB2 else None)
+
+
+@pytest.mark.parametrize("shape,T,kw,launches", [
+    # decode kernels (reset + fused layer): Q2_K, inter % 16 == 0, up to 32 vectors
+    ((4096, 1536, 64, 6), 1, {}, 2),
+    ((7168, 2048, 256, 8), 32, {}, 2),
+    # tensor-core path above 32 vectors: routing (1 launch up to 64 tokens, else 2) + 4
+    ((7168, 2048, 256, 8), 33, {}, 1 + 4),
+    ((7168, 2048, 256, 8), 65, {}, 2 + 4),
+    # rows that are not multiples of 16 bytes: GEMV kernels (routing + 3)
+    ((512, 320, 8, 2), 100, {}, 2 + 3),
+    # the codebook format never takes the decode kernels
+    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_CB2, align=16), 1 + 4),
+    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_CB2), 1 + 3),
+    # FORCE_GEMV keeps the decode kernels where they apply and rules out the
+    # tensor-core kernels elsewhere; FORCE_TC needs 16-byte rows (504-byte down rows here)
+    ((4096, 1536, 64, 6), 1, dict(flags=D.FORCE_GEMV), 2),
+    ((7168, 2048, 256, 8), 100, dict(flags=D.FORCE_GEMV), 2 + 3),
+    ((4096, 1536, 64, 6), 1, dict(flags=D.FORCE_TC), 0),
+])
+def test_path_choice_by_launch_count(shape, T, kw, launches):
+    """The per-call path choice documented under ds4g_moe_forward ("Path"),
+    read through ds4g_moe_forward_launches (pure host arithmetic)."""
+    assert D.moe_forward_launches(layer_desc(*shape, **kw), T) == launches
