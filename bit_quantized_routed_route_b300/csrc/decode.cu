@@ -16,7 +16,8 @@
 // programmatic dependent launch overlaps the two.  A producer warp then
 // claims work from two global counters -- first 16-row gate/up tiles
 // (expert, rows), then 32-row down items -- and streams each claimed tile
-// (contiguous runs of 84-byte blocks) into a shared-memory ring with
+// (runs of 84-byte blocks: the whole tile, pairs of padded gate/up rows, or
+// single padded down rows) into a shared-memory ring with
 // cp.async.bulk (TMA, no tensor map) completing on mbarriers; a down stage
 // also carries the h rows of its experts.  The ring keeps streaming W_down
 // right after W_gate/W_up, so HBM does not idle at the phase boundary.
