@@ -47,6 +47,17 @@ MUTANTS = {
                                  "orc_q2k_dequant_block(row, out + b * ORC_QK);")],
     "up_reads_gate": [("dequant_row(L, wu + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);",
                        "dequant_row(L, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);")],
+    "min_term_uses_d": [("float min_part = dmin * (float)(sc >> 4);",
+                         "float min_part = d * (float)(sc >> 4);")],
+    "sigmoid_weights_not_normalised": [
+        ("            w[i] = 1.0 / (1.0 + exp(-rank_value(lg[ids[i]])));\n            sum += w[i];\n"
+         "        }\n        for (int i = 0; i < k; ++i) w[i] /= sum;",
+         "            w[i] = 1.0 / (1.0 + exp(-rank_value(lg[ids[i]])));\n            sum += w[i];\n"
+         "        }")],
+    "down_expert_stride_of_gate": [("L->w_down + (int64_t)e * L->down_expert_stride",
+                                    "L->w_down + (int64_t)e * L->gate_up_expert_stride")],
+    "down_row_bytes_of_gate": [("dequant_row(L, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);",
+                                "dequant_row(L, wd + (int64_t)m * L->gate_up_row_bytes, I, rowbuf);")],
 }
 
 
