@@ -58,6 +58,13 @@ MUTANTS = {
                                     "L->w_down + (int64_t)e * L->gate_up_expert_stride")],
     "down_row_bytes_of_gate": [("dequant_row(L, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);",
                                 "dequant_row(L, wd + (int64_t)m * L->gate_up_row_bytes, I, rowbuf);")],
+    "q2k_three_bit_field": [("(qs[32 * h + l] >> (2 * g)) & 3", "(qs[32 * h + l] >> (2 * g)) & 7")],
+    "q2k_halves_swapped": [("(qs[32 * h + l] >> (2 * g)) & 3", "(qs[32 * (1 - h) + l] >> (2 * g)) & 3")],
+    "cb2_drops_d": [("float value = d * (float)scale;", "float value = (float)scale;")],
+    "cb2_sign_bits_reversed": [("int negate = (sgn[o] >> b) & 1;", "int negate = (sgn[o] >> (7 - b)) & 1;")],
+    "cb2_index_per_4": [("int o = j / 8;\n        int b = j % 8;", "int o = j / 4;\n        int b = j % 8;")],
+    "route_picks_repeat": [("        ids[i] = best;\n        used[best] = 1;", "        ids[i] = best;")],
+    "combine_averages_slots": [("yt[m] += w[i] * o[m];", "yt[m] += w[i] * o[m] / k;")],
 }
 
 
