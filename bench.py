@@ -5,7 +5,8 @@ One step = one call of the whole layer (routing, counts/offsets/permutation,
 fused dequant gate/up + SiLU, down projection, weighted combine) over one
 batch of synthetic tokens.  The default workload is single-token decode:
 hidden 4096, expert intermediate 1536, 64 Q2_K experts, top-6, 1 token per
-step (the bandwidth-bound GEMV path).  Other workloads: --config NAME.
+step (the bandwidth-bound mma.sync decode kernel).  Other workloads:
+--config NAME.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...     # the CPU oracle, timed as it stands
@@ -16,7 +17,8 @@ with CUDA events on the launching stream; max over ranks.  Each step uses
 another batch of tokens and another of R copies of the expert weights, with
 R * (bytes touched per step) >= 4 x L2, so that weights stream from HBM.
 Per-kernel durations come from CUDA events recorded between the layer's
-kernels inside the same graphs.  Under torchrun every rank runs its own
+kernels in a second graph of the same steps, replayed once inside the timed
+bracket after the measured replays.  Under torchrun every rank runs its own
 replica of the workload (the layer does not shard here): scaling "weak".
 """
 from __future__ import annotations
