@@ -3,10 +3,12 @@
 
 One step = one call of the whole layer (routing, counts/offsets/permutation,
 fused dequant gate/up + SiLU, down projection, weighted combine) over one
-batch of synthetic tokens.  The default workload is single-token decode:
-hidden 4096, expert intermediate 1536, 64 Q2_K experts, top-6, 1 token per
-step (the bandwidth-bound mma.sync decode kernel).  Other workloads:
---config NAME.
+batch of synthetic tokens.  The headline workload is prefill: hidden 7168,
+expert intermediate 2048, 256 Q2_K experts, top-8, 2048 tokens per step
+(the largest single-GPU workload; the tcgen05 tensor-core kernels).  The
+same JSON line carries a `per_config` object with the other workloads
+(single-token decode, 32-token decode, 512-token codebook layer, the tiny
+layer), each timed in the same run the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...     # the CPU oracle, timed as it stands
@@ -18,16 +20,24 @@ another batch of tokens and another of R copies of the expert weights, with
 R * (bytes touched per step) >= 4 x L2, so that weights stream from HBM.
 Per-kernel durations come from CUDA events recorded between the layer's
 kernels in a second graph of the same steps, replayed once inside the timed
-bracket after the measured replays.  Under torchrun every rank runs its own
-replica of the workload (the layer does not shard here): scaling "weak".
+bracket after the measured replays.  The per-config workloads run at least
+max(K, a floor of about 0.2 s) steps each, reported in their `steps`.
+Under torchrun every rank runs its own replica of the workload (the layer
+does not shard here): scaling "weak".
+
+e2e: the same metric through ds4g_moe_forward_host (pinned host x and
+logits copied in, y copied out, one synchronization per call), at least
+2000 calls or about 6 s of calls, whichever is fewer, and never fewer than
+K -- independent of K otherwise.
 """
 from __future__ import annotations
 
 import argparse
 import hashlib
 import json
-import re
 import os
+import platform
+import re
 import subprocess
 import sys
 import time
@@ -42,6 +52,7 @@ if ROOT not in sys.path:
 import ds4g_synth as S  # noqa: E402
 
 METRIC = "routed-MoE layer tokens/s; effective HBM GB/s (decode) & tensor util (prefill)"
+HEADLINE = "prefill_2048"
 L2_BYTES = 126 * 1024 * 1024
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
@@ -49,28 +60,38 @@ FALLBACK_HBM_GBS = 6400.0
 FALLBACK_BF16_TFLOPS = 1800.0
 FALLBACK_BF16_TFLOPS_SUSTAINED = 1400.0
 NOMINAL_HBM_GBS = 8000.0
+E2E_MIN_CALLS = 2000
+E2E_MAX_SECONDS = 6.0
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="ds4g", choices=["ds4g", "reference"])
-    ap.add_argument("--config", default="decode_1tok", choices=list(S.CONFIGS))
+    ap.add_argument("--config", default=HEADLINE, choices=list(S.CONFIGS))
     ap.add_argument("--copies", type=int, default=0, help="weight copies (0 = auto)")
     ap.add_argument("--pool", type=int, default=0, help="distinct token batches (0 = auto)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only --config (no per_config object)")
     ap.add_argument("--force", default="auto", choices=["auto", "decode", "tc"],
                     help="run the layer on one path (default: the library's choice)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def default_steps(cfg: S.Config):
     # ~1-2 s of device time at the expected step times
     return {"tiny": 20000, "decode_1tok": 100000, "decode_32tok": 4000,
             "prefill_2048": 200, "codebook_512": 1000}[cfg.name]
+
+
+def floor_steps(cfg: S.Config):
+    # about 0.2 s of device time: the least a per-config line is timed over
+    return {"tiny": 5000, "decode_1tok": 5000, "decode_32tok": 150,
+            "prefill_2048": 60, "codebook_512": 80}[cfg.name]
 
 
 # ---------------------------------------------------------------------------
@@ -236,6 +257,61 @@ def layer_bytes(cfg: S.Config):
     return gu, dn
 
 
+def host_info():
+    """Logical cores of this host and its CPU model (for the CPU baseline)."""
+    model = platform.processor() or ""
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except OSError:
+        pass
+    return os.cpu_count() or 1, model
+
+
+def roofline_for(cfg: S.Config, path: str, ph_ms, active, steps_b, T, k):
+    """Roofline of the dominant kernel over the phased replay: its algorithmic
+    bytes or flops per launch (averaged over the graph's steps) / its mean
+    duration.  Decode: the fused layer kernel against HBM.  Tensor-core path:
+    the gate/up kernel; prefill against the tensor peak, the codebook layer
+    (HBM-bound by its bytes) against HBM with its tensor fraction beside it."""
+    gu_b, dn_b = layer_bytes(cfg)
+    H, I = cfg.hidden, cfg.inter
+    x_b, y_b = T * H * 2, T * H * 4
+    act = active[steps_b]
+    hbm_peak, peak_kind = peaks()
+    burst, sustained, tkind = tensor_peaks()
+    if path == "decode":
+        dec_bytes = float(np.mean(act * (2 * gu_b + dn_b))) + x_b + y_b
+        achieved = dec_bytes / (ph_ms[1] / 1000.0) / 1e9
+        return {"bound": "hbm", "kernel": "decode_q2k_kernel" if T <= 8 else "decode_tc_kernel",
+                "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
+                "traffic": measured_traffic("decode", cfg.name),
+                "algorithmic_bytes": dec_bytes, "duration_us": ph_ms[1] * 1000.0}
+    # gate/up kernel: W_gate and W_up of the active experts, the gathered
+    # fp16 activations (2 bytes per assignment and column) and h written
+    gate_up_bytes = float(np.mean(act * 2 * gu_b)) + T * k * H * 2 + T * k * I * 2
+    flops = 2.0 * T * k * 2 * H * I
+    tflops = flops / (ph_ms[1] / 1000.0) / 1e12
+    gbs = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9
+    if path == "tc" and cfg.format == S.FMT_Q2K:
+        return {"bound": "tensor", "kernel": "tc_kernel<0> (gate/up)", "achieved": tflops,
+                "peak": sustained, "peak_kind": f"{tkind} bf16 sustained (fp16 same rate)",
+                "unit": "TFLOP/s", "frac": tflops / sustained, "frac_of_burst": tflops / burst,
+                "traffic": measured_traffic("tc_gateup", cfg.name),
+                "algorithmic_flops": flops, "duration_us": ph_ms[1] * 1000.0}
+    kern = "tc_kernel<0> (gate/up)" if path == "tc" else "gateup_kernel"
+    return {"bound": "hbm", "kernel": kern, "achieved": gbs, "peak": hbm_peak,
+            "peak_kind": peak_kind, "unit": "GB/s", "frac": gbs / hbm_peak,
+            "frac_of_8tbs": gbs / NOMINAL_HBM_GBS,
+            "tensor": {"achieved": tflops, "unit": "TFLOP/s", "peak": sustained,
+                       "frac": tflops / sustained},
+            "traffic": measured_traffic("tc_gateup" if path == "tc" else "gateup", cfg.name),
+            "algorithmic_bytes": gate_up_bytes, "duration_us": ph_ms[1] * 1000.0}
+
+
 # ---------------------------------------------------------------------------
 # the CPU oracle (baseline and reference arm)
 # ---------------------------------------------------------------------------
@@ -274,6 +350,7 @@ def reference_arm(args, cfg, rank, world):
         done += 1
     dt = time.perf_counter() - t0
     val = done / dt
+    nproc, model = host_info()
     sample = (f"{done} of {K} requested steps, one token of {cfg.name} each "
               f"(steps capped at ~150 s of CPU work)")
     line = {
@@ -282,7 +359,7 @@ def reference_arm(args, cfg, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_config(cfg, 0, "oracle"),
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": sample},
+                         "host_cores": nproc, "cpu_model": model, "sample": sample},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -303,236 +380,275 @@ def workload_config(cfg: S.Config, copies: int, l2_note: str):
 # the GPU arm
 # ---------------------------------------------------------------------------
 
-def main():
-    args = parse()
+class Workload:
+    """One configuration resident on the device: R weight copies, a pool of
+    token batches, the output and the workspace."""
+
+    def __init__(self, cfg: S.Config, args, dev):
+        import bit_quantized_routed_route_b300 as D
+        self.D, self.cfg, self.dev = D, cfg, dev
+        layer = S.make_layer(cfg)
+        self.layer = layer
+        gu_b, dn_b = layer_bytes(cfg)
+        T, H, E, k = cfg.tokens, cfg.hidden, cfg.n_experts, cfg.top_k
+        self.T, self.H, self.E, self.k = T, H, E, k
+        self.x_b, self.l_b, self.y_b = T * H * 2, T * E * 4, T * H * 4
+        P = args.pool or int(max(1, min(256, (64 << 20) // (self.x_b + self.l_b))))
+        xs, ls = [layer["x"]], [layer["logits"]]
+        for b in range(1, P):
+            tk = S.make_tokens(cfg, T, seed=cfg.seed * 100003 + b)
+            xs.append(tk["x"])
+            ls.append(tk["logits"])
+        self.P = P
+        self.x_all = np.stack(xs)
+        self.l_all = np.stack(ls)
+
+        # routing of every batch, computed by the library (untimed), for the
+        # algorithmic byte counts
+        ids_all = []
+        for b in range(P):
+            lg = torch.from_numpy(self.l_all[b]).to(dev)
+            ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+            w = torch.empty((T, k), dtype=torch.float32, device=dev)
+            D.check(D.route_topk(lg, T, E, k, cfg.score, ids, w))
+            ids_all.append(ids.cpu().numpy())
+        self.active = np.array([len(np.unique(i)) for i in ids_all], dtype=np.float64)
+        self.touched = self.active * (2 * gu_b + dn_b)
+        copies = args.copies or int(max(2, min(64, -(-4 * L2_BYTES //
+                                                     max(1, int(self.touched.min()))))))
+        per_copy = (gu_b * 2 + dn_b) * E
+        total_mem = torch.cuda.get_device_properties(dev).total_memory
+        if copies * per_copy > 0.4 * total_mem:
+            copies = max(1, int(0.4 * total_mem // per_copy))
+        self.copies = copies
+
+        base = {n: torch.from_numpy(layer[n]).to(dev) for n in ("w_gate", "w_up", "w_down")}
+        cb = None if layer["codebook"] is None else torch.from_numpy(layer["codebook"]).to(dev)
+        flags = {"auto": 0, "decode": D.FORCE_GEMV, "tc": D.FORCE_TC}[args.force]
+        self.w_dev = []
+        for c in range(copies):
+            t = base if c == 0 else {n: v.clone() for n, v in base.items()}
+            self.w_dev.append(D.Layer(H, cfg.inter, E, k, cfg.score, cfg.format, t["w_gate"],
+                                      t["w_up"], t["w_down"], cb, flags=flags))
+        self.x_dev = torch.from_numpy(self.x_all.view(np.int16)).to(dev)
+        self.l_dev = torch.from_numpy(self.l_all).to(dev)
+        self.y_dev = torch.empty((T, H), dtype=torch.float32, device=dev)
+        self.ws_bytes = self.w_dev[0].workspace_bytes(T)
+        self.ws = torch.empty(self.ws_bytes, dtype=torch.uint8, device=dev)
+        self.launches_per_step = D.moe_forward_launches(self.w_dev[0].desc, T)
+        self.path = layer_path(cfg) if args.force == "auto" else args.force
+        self.stream = torch.cuda.Stream()
+        torch.cuda.synchronize()
+
+    def step(self, s, events=None):
+        D, L, b = self.D, self.w_dev[s % self.copies], s % self.P
+        if events is None:
+            D.check(D.moe_forward(L.desc, self.x_dev[b], self.l_dev[b], self.T, self.y_dev,
+                                  self.ws, self.ws_bytes, stream=self.stream))
+        else:
+            D.check(D.moe_forward_phased(L.desc, self.x_dev[b], self.l_dev[b], self.T,
+                                         self.y_dev, self.ws, events, self.ws_bytes,
+                                         stream=self.stream))
+
+    def time_device(self, K: int, W: int, world: int, sampler=None):
+        """W eager steps, then K steps from CUDA graphs timed with events on
+        the launching stream (barrier + synchronize on both sides), then one
+        replay of a phased graph for per-kernel durations.  `sampler` (a
+        ClockSampler) runs around the timed region only.  Returns (elapsed ms
+        over the K steps, max over ranks; phase ms [4]; G; clocks)."""
+        stream = self.stream
+        with torch.cuda.stream(stream):
+            for s in range(W):
+                self.step(s)
+        stream.synchronize()
+        G = min(K, 500 if self.T <= 64 else 20)
+        n_full, rem = divmod(K, G)
+
+        def capture(n_steps, phased):
+            evs = None
+            if phased:
+                evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)]
+                       for _ in range(n_steps)]
+                for row in evs:
+                    for e in row:
+                        e.record(stream)      # materialise the cudaEvent_t handles
+                stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(n_steps):
+                    self.step(j, [e.cuda_event for e in evs[j]] if phased else None)
+            return g, evs
+
+        g_main, _ = capture(G, False)
+        g_rem = capture(rem, False)[0] if rem else None
+        g_phase, ev_phase = capture(G, True)
+        with torch.cuda.stream(stream):        # graphs replay on the current stream
+            for g in (g_main, g_rem, g_phase):     # one untimed replay of each graph
+                if g is not None:
+                    g.replay()
+        stream.synchronize()
+
+        start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if sampler is not None:
+            sampler.start()
+            time.sleep(0.25)
+        barrier(world)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            start.record(stream)
+            for _ in range(n_full):
+                g_main.replay()
+            if g_rem is not None:
+                g_rem.replay()
+            end.record(stream)
+            g_phase.replay()
+        torch.cuda.synchronize()
+        barrier(world)
+        clocks = sampler.stop() if sampler is not None else None
+        elapsed_ms = max_over_ranks(start.elapsed_time(end), world)
+        ph = np.array([[ev_phase[j][i].elapsed_time(ev_phase[j][i + 1]) for i in range(4)]
+                       for j in range(G)])
+        return elapsed_ms, ph.mean(axis=0), G, clocks
+
+    def time_e2e(self, K: int, W: int, world: int, ms_per_step: float):
+        """The layer through the host entry point with pinned host buffers."""
+        D, T = self.D, self.T
+        xh = torch.from_numpy(self.x_all.view(np.int16)).pin_memory()
+        lh = torch.from_numpy(self.l_all).pin_memory()
+        yh = torch.empty((T, self.H), dtype=torch.float32).pin_memory()
+        # a rough per-call estimate (device time + copies at ~20 GB/s + ~60 us
+        # of host overhead) sizes the loop to at most E2E_MAX_SECONDS
+        est_s = ms_per_step / 1000.0 + (self.x_b + self.l_b + self.y_b) / 20e9 + 60e-6
+        calls = max(K, min(E2E_MIN_CALLS, int(E2E_MAX_SECONDS / est_s)))
+        calls = max(calls, 20)
+        for s in range(max(W, 3)):
+            D.check(D.moe_forward_host(self.w_dev[s % self.copies].desc, xh[s % self.P],
+                                       lh[s % self.P], T, yh, self.ws, self.ws_bytes,
+                                       stream=self.stream))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for s in range(calls):
+            D.check(D.moe_forward_host(self.w_dev[s % self.copies].desc, xh[s % self.P],
+                                       lh[s % self.P], T, yh, self.ws, self.ws_bytes,
+                                       stream=self.stream))
+        torch.cuda.synchronize()
+        barrier(world)
+        dt = max_over_ranks(time.perf_counter() - t0, world)
+        return {"value": calls * T * world / dt, "unit": "tokens/s",
+                "h2d_bytes_per_step": self.x_b + self.l_b, "d2h_bytes_per_step": self.y_b,
+                "steps": calls, "ms_per_call": 1000.0 * dt / calls,
+                "api": "ds4g_moe_forward_host (pinned host buffers)"}
+
+    def measure(self, K: int, W: int, world: int, e2e: bool, gpu_index: int):
+        """Everything the JSON line reports for this workload."""
+        cfg, T, k = self.cfg, self.T, self.k
+        elapsed_ms, ph_ms, G, clocks = self.time_device(K, W, world, ClockSampler(gpu_index))
+        value = K * T * world / (elapsed_ms / 1000.0)
+        ms_per_step = elapsed_ms / K
+        steps_b = np.arange(G) % self.P
+        step_bytes = float(np.mean(self.touched[steps_b])) + self.x_b + self.l_b + self.y_b
+        hbm_peak, _ = peaks()
+        gbs = step_bytes / (ms_per_step / 1000.0) / 1e9
+        if self.path == "decode":
+            # one reset/convert launch, then one kernel that routes, runs gate/up
+            # + SiLU, the down projection and the combine
+            phases = {"reset_convert": ph_ms[0] * 1e3, "fused_layer": ph_ms[1] * 1e3,
+                      "route": None, "gateup": None, "down": None, "combine": None}
+        else:
+            phases = {"route": ph_ms[0] * 1e3, "gateup": ph_ms[1] * 1e3,
+                      "down": ph_ms[2] * 1e3, "combine": ph_ms[3] * 1e3}
+        out = {
+            "value": value, "unit": "tokens/s", "steps": K, "warmup": W,
+            "ms_per_step": ms_per_step, "path": self.path,
+            "config": workload_config(cfg, self.copies,
+                                      f"inputs larger than L2: {self.copies} rotating weight "
+                                      f"copies, {self.touched.mean() / 1e6:.1f} MB touched per "
+                                      f"step"),
+            "roofline": roofline_for(cfg, self.path, ph_ms, self.active, steps_b, T, k),
+            "effective_hbm": {"step_bytes": step_bytes, "gbs": gbs,
+                              "frac_of_measured": gbs / hbm_peak,
+                              "frac_of_8tbs": gbs / NOMINAL_HBM_GBS},
+            "phases_us": phases,
+            "gpu_launches": self.launches_per_step * K,
+            "clocks": clocks,
+        }
+        if e2e:
+            out["e2e"] = self.time_e2e(K, W, world, ms_per_step)
+        return out
+
+    def free(self):
+        del self.w_dev, self.x_dev, self.l_dev, self.y_dev, self.ws
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def cpu_baseline(cfg: S.Config, layer: dict):
+    """The oracle as it stands, single-threaded, on consecutive tokens of the
+    workload for about 15 s."""
+    small = S.make_layer(cfg, tokens=min(cfg.tokens, 64)) if cfg.tokens > 64 else layer
+    v, n, dt = oracle_tokens_per_s(small, budget_s=15.0, max_tokens=10_000)
+    nproc, model = host_info()
+    return {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "host_cores": nproc, "cpu_model": model,
+            "sample": f"{n} tokens of {cfg.name} through the single-threaded fp64 oracle "
+                      f"in {dt:.1f} s"}
+
+
+def main(argv=None):
+    args = parse(argv)
     cfg = S.CONFIGS[args.config]
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
         return reference_arm(args, cfg, rank, world)
 
-    import bit_quantized_routed_route_b300 as D
+    import bit_quantized_routed_route_b300  # noqa: F401  (fails loudly without the library)
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
     dev = torch.device("cuda")
     K = args.steps if args.steps is not None else default_steps(cfg)
     W = max(3, args.warmup if args.warmup is not None else 10)
 
-    # --- inputs ------------------------------------------------------------
-    layer = S.make_layer(cfg)
-    gu_b, dn_b = layer_bytes(cfg)
-    T, H, E, k = cfg.tokens, cfg.hidden, cfg.n_experts, cfg.top_k
-    x_b, l_b, y_b = T * H * 2, T * E * 4, T * H * 4
-    batch_bytes = x_b + l_b
-    P = args.pool or int(max(1, min(256, (64 << 20) // batch_bytes)))
-    xs, ls = [layer["x"]], [layer["logits"]]
-    for b in range(1, P):
-        tk = S.make_tokens(cfg, T, seed=cfg.seed * 100003 + b)
-        xs.append(tk["x"])
-        ls.append(tk["logits"])
-    x_all = np.stack(xs)
-    l_all = np.stack(ls)
+    wl = Workload(cfg, args, dev)
+    head = wl.measure(K, W, world, e2e=not args.no_e2e, gpu_index=local)
+    headline_layer = wl.layer
+    wl.free()
+    del wl
 
-    # routing of every batch, computed by the library (untimed), for the
-    # algorithmic byte counts
-    ids_all = []
-    for b in range(P):
-        lg = torch.from_numpy(l_all[b]).to(dev)
-        ids = torch.empty((T, k), dtype=torch.int32, device=dev)
-        w = torch.empty((T, k), dtype=torch.float32, device=dev)
-        D.check(D.route_topk(lg, T, E, k, cfg.score, ids, w))
-        ids_all.append(ids.cpu().numpy())
-    active = np.array([len(np.unique(i)) for i in ids_all], dtype=np.float64)
-    touched = active * (2 * gu_b + dn_b)
-    copies = args.copies or int(max(2, min(64, -(-4 * L2_BYTES // max(1, int(touched.min()))))))
-    per_copy = (gu_b * 2 + dn_b) * E
-    if copies * per_copy > 0.5 * torch.cuda.get_device_properties(dev).total_memory:
-        copies = max(1, int(0.5 * torch.cuda.get_device_properties(dev).total_memory // per_copy))
+    per_config = {}
+    if not args.no_per_config:
+        for name, c in S.CONFIGS.items():
+            if name == cfg.name:
+                continue
+            w = Workload(c, args, dev)
+            per_config[name] = w.measure(max(K, floor_steps(c)), W, world, e2e=not args.no_e2e,
+                                         gpu_index=local)
+            w.free()
+            del w
 
-    w_dev = []
-    base = {n: torch.from_numpy(layer[n]).to(dev) for n in ("w_gate", "w_up", "w_down")}
-    cb = None if layer["codebook"] is None else torch.from_numpy(layer["codebook"]).to(dev)
-    flags = {"auto": 0, "decode": D.FORCE_GEMV, "tc": D.FORCE_TC}[args.force]
-    for c in range(copies):
-        t = base if c == 0 else {n: v.clone() for n, v in base.items()}
-        w_dev.append(D.Layer(H, cfg.inter, E, k, cfg.score, cfg.format, t["w_gate"], t["w_up"],
-                             t["w_down"], cb, flags=flags))
-    x_dev = torch.from_numpy(x_all.view(np.int16)).to(dev)
-    l_dev = torch.from_numpy(l_all).to(dev)
-    y_dev = torch.empty((T, H), dtype=torch.float32, device=dev)
-    ws_bytes = w_dev[0].workspace_bytes(T)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    launches_per_step = D.moe_forward_launches(w_dev[0].desc, T)
-
-    stream = torch.cuda.Stream()
-    torch.cuda.synchronize()
-
-    def step(s, st, events=None):
-        L = w_dev[s % copies]
-        b = s % P
-        if events is None:
-            D.check(D.moe_forward(L.desc, x_dev[b], l_dev[b], T, y_dev, ws, ws_bytes, stream=st))
-        else:
-            D.check(D.moe_forward_phased(L.desc, x_dev[b], l_dev[b], T, y_dev, ws, events,
-                                         ws_bytes, stream=st))
-
-    # --- warm-up (eager) -----------------------------------------------------
-    with torch.cuda.stream(stream):
-        for s in range(W):
-            step(s, stream)
-    stream.synchronize()
-
-    # --- graphs: G steps each ------------------------------------------------
-    # `value` comes from graphs of plain layer calls; per-kernel durations from
-    # one replay of a graph of phased calls (events between the kernels),
-    # inside the same timed bracket.
-    G = min(K, 500 if T <= 64 else 20)
-    n_full, rem = divmod(K, G)
-
-    def capture(n_steps, phased):
-        evs = None
-        if phased:
-            evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_steps)]
-            for row in evs:
-                for e in row:
-                    e.record(stream)      # materialise the cudaEvent_t handles
-            stream.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=stream):
-            for j in range(n_steps):
-                step(j, stream, [e.cuda_event for e in evs[j]] if phased else None)
-        return g, evs
-
-    g_main, _ = capture(G, False)
-    g_rem = capture(rem, False)[0] if rem else None
-    g_phase, ev_phase = capture(G, True)
-    with torch.cuda.stream(stream):        # graphs replay on the current stream
-        for g in (g_main, g_rem, g_phase):     # one untimed replay of each graph
-            if g is not None:
-                g.replay()
-    stream.synchronize()
-
-    sampler = ClockSampler(local)
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.25)
-    with torch.cuda.stream(stream):
-        start.record(stream)
-        for _ in range(n_full):
-            g_main.replay()
-        if g_rem is not None:
-            g_rem.replay()
-        end.record(stream)
-        g_phase.replay()
-    torch.cuda.synchronize()
-    barrier(world)
-    clocks = sampler.stop()
-    elapsed_ms = max_over_ranks(start.elapsed_time(end), world)
-
-    tokens = K * T * world
-    value = tokens / (elapsed_ms / 1000.0)
-    ms_per_step = elapsed_ms / K
-
-    # per-phase durations over the phased replay
-    ph = np.array([[ev_phase[j][i].elapsed_time(ev_phase[j][i + 1]) for i in range(4)]
-                   for j in range(G)])
-    ph_ms = ph.mean(axis=0)                        # route, gateup, down, combine
-    # algorithmic bytes per launch of the dominant (gate/up) kernel, averaged
-    # over the steps of the graph: the logical quantized bytes of W_gate and
-    # W_up of the active experts, the activations read (bf16) and h written
-    # (2 bytes per value)
-    steps_b = np.arange(G) % P
-    act = active[steps_b]
-    gate_up_bytes = float(np.mean(act * 2 * gu_b)) + x_b + T * k * cfg.inter * 2
-    step_bytes = float(np.mean(touched[steps_b])) + x_b + l_b + y_b
-    hbm_peak, peak_kind = peaks()
-    path = layer_path(cfg) if args.force == "auto" else args.force
-    if path == "tc":
-        # the tensor-core gate/up kernel: 2 * A * 2 * H * I flops per launch
-        burst, sustained, tkind = tensor_peaks()
-        flops = 2.0 * T * k * 2 * H * cfg.inter
-        achieved = flops / (ph_ms[1] / 1000.0) / 1e12
-        roofline = {"bound": "tensor", "kernel": "tc_kernel<0> (gate/up)", "achieved": achieved,
-                    "peak": sustained, "peak_kind": f"{tkind} bf16 sustained (fp16 same rate)",
-                    "unit": "TFLOP/s", "frac": achieved / sustained,
-                    "frac_of_burst": achieved / burst,
-                    "traffic": measured_traffic("tc_gateup", cfg.name),
-                    "algorithmic_flops": flops, "duration_us": ph_ms[1] * 1000.0}
-    elif path == "decode":
-        # one fused kernel streams W_gate, W_up and W_down of the active experts
-        dec_bytes = float(np.mean(touched[steps_b])) + x_b + y_b
-        achieved = dec_bytes / (ph_ms[1] / 1000.0) / 1e9
-        roofline = {"bound": "hbm",
-                    "kernel": "decode_q2k_kernel" if T <= 8 else "decode_tc_kernel",
-                    "achieved": achieved,
-                    "peak": hbm_peak, "peak_kind": peak_kind, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "frac_of_8tbs": achieved / NOMINAL_HBM_GBS,
-                    "traffic": measured_traffic("decode", cfg.name),
-                    "algorithmic_bytes": dec_bytes, "duration_us": ph_ms[1] * 1000.0}
-    else:
-        achieved = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9
-        roofline = {"bound": "hbm", "kernel": "gateup_kernel",
-                    "achieved": achieved, "peak": hbm_peak, "peak_kind": peak_kind,
-                    "unit": "GB/s", "frac": achieved / hbm_peak,
-                    "traffic": measured_traffic("gateup", cfg.name),
-                    "algorithmic_bytes": gate_up_bytes, "duration_us": ph_ms[1] * 1000.0}
-
-    # --- end to end through the host entry point ------------------------------
-    e2e = None
-    if not args.no_e2e:
-        xh = torch.from_numpy(x_all.view(np.int16)).pin_memory()
-        lh = torch.from_numpy(l_all).pin_memory()
-        yh = torch.empty((T, H), dtype=torch.float32).pin_memory()
-        ws2 = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-        K2 = min(K, max(50, int(2000 * 64 / max(1, T))))
-        for s in range(W):
-            D.check(D.moe_forward_host(w_dev[s % copies].desc, xh[s % P], lh[s % P], T, yh, ws2,
-                                       ws_bytes, stream=stream))
-        barrier(world)
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for s in range(K2):
-            D.check(D.moe_forward_host(w_dev[s % copies].desc, xh[s % P], lh[s % P], T, yh, ws2,
-                                       ws_bytes, stream=stream))
-        torch.cuda.synchronize()
-        barrier(world)
-        dt = max_over_ranks(time.perf_counter() - t0, world)
-        e2e = {"value": K2 * T * world / dt, "unit": "tokens/s", "h2d_bytes_per_step": x_b + l_b,
-               "d2h_bytes_per_step": y_b, "steps": K2}
-
-    # --- CPU baseline (rank 0, one GPU) --------------------------------------
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        small = S.make_layer(cfg, tokens=min(T, 64)) if T > 64 else layer
-        v, n, dt = oracle_tokens_per_s(small, budget_s=15.0, max_tokens=10_000)
-        cpu = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-               "sample": f"{n} tokens of {cfg.name} through the single-threaded fp64 oracle "
-                         f"in {dt:.1f} s"}
+        cpu = cpu_baseline(cfg, headline_layer)
 
     if rank != 0:
         return 0
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": W, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
         "arithmetic": ("fp16 tensor-core operands (decode: exact 2-bit fields and fp16 "
                        "activations; prefill: weights dequantized to fp16), fp32 accumulation "
                        "and fp32 output"),
-        "config": workload_config(cfg, copies,
-                                  f"inputs larger than L2: {copies} rotating weight copies, "
-                                  f"{touched.mean() / 1e6:.1f} MB touched per step"),
-        "roofline": roofline,
-        "path": path,
-        "effective_hbm": {"step_bytes": step_bytes,
-                          "gbs": step_bytes / (ms_per_step / 1000.0) / 1e9,
-                          "frac_of_measured": step_bytes / (ms_per_step / 1000.0) / 1e9 / hbm_peak,
-                          "frac_of_8tbs": step_bytes / (ms_per_step / 1000.0) / 1e9 / NOMINAL_HBM_GBS},
-        "phases_us": {"route": ph_ms[0] * 1e3, "gateup": ph_ms[1] * 1e3, "down": ph_ms[2] * 1e3,
-                      "combine": ph_ms[3] * 1e3},
+        "config": head["config"],
+        "roofline": head["roofline"],
+        "path": head["path"],
+        "effective_hbm": head["effective_hbm"],
+        "phases_us": head["phases_us"],
         "cpu_baseline": cpu,
-        "e2e": e2e,
-        "gpu_launches": launches_per_step * K,
-        "clocks": clocks,
+        "e2e": head.get("e2e"),
+        "gpu_launches": head["gpu_launches"],
+        "clocks": head["clocks"],
+        "per_config": per_config,
     }
     print(json.dumps(line), flush=True)
     if world > 1:

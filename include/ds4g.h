@@ -154,7 +154,9 @@ typedef struct ds4g_moe_desc {
 } ds4g_moe_desc;
 
 /*
- * ds4g_route_topk -- steps 1 and 2 alone.
+ * ds4g_route_topk -- steps 1 and 2 alone.  Passage: the routed experts of
+ * the layer (ds4 README mirror, "Model Weights"); the selection order and
+ * tie rule are this library's definition (the pages state none).
  *   logits  [T x E] fp32, row-major.
  *   ids     [T x k] int32 out: per token the k largest logits' expert ids in
  *           rank order: larger logit first, equal logits -> lower id first,
@@ -176,7 +178,10 @@ DS4G_API ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, 
                             void *stream);
 
 /*
- * ds4g_q2k_dequant -- n_blocks consecutive Q2_K super-blocks (84 bytes each,
+ * ds4g_q2k_dequant -- passage: Q2_K routed experts (ds4 README mirror,
+ * "Model Weights") in the GGUF layout kept from llama.cpp (same page,
+ * "Acknowledgements to llama.cpp and GGML").
+ * n_blocks consecutive Q2_K super-blocks (84 bytes each,
  * `blocks` 4-byte aligned) to n_blocks * 256 values of out_dtype in `out`
  * (16-byte aligned).  fp32 output is exactly the block definition above
  * (both products are exact; one rounding in the subtraction); fp16 / bf16
@@ -188,7 +193,10 @@ DS4G_API ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void
                              int32_t out_dtype, void *stream);
 
 /*
- * ds4g_cb2_dequant -- n_blocks consecutive codebook-2-bit super-blocks (70
+ * ds4g_cb2_dequant -- passage: the IQ2_XXS half of the IQ2_XXS / Q2_K expert
+ * mix (DwarfStar 4 on aiany.app, "What Sets It Apart"; ds4 README mirror,
+ * "Model Weights"), as the codebook-2-bit stand-in described at the top.
+ * n_blocks consecutive codebook-2-bit super-blocks (70
  * bytes each, `blocks` 2-byte aligned) with a [256 x 8] int8 device codebook
  * to n_blocks * 256 values of out_dtype (16-byte aligned).  fp32 output is
  * exact; fp16 / bf16 output is the fp32 value rounded to nearest even.
@@ -198,14 +206,17 @@ DS4G_API ds4g_status ds4g_cb2_dequant(const void *blocks, int64_t n_blocks, cons
                              void *out, int32_t out_dtype, void *stream);
 
 /*
- * ds4g_moe_workspace_bytes -- bytes of device workspace ds4g_moe_forward
+ * ds4g_moe_workspace_bytes -- no counterpart on the pages (sizing helper of
+ * ds4g_moe_forward).  Bytes of device workspace ds4g_moe_forward
  * (and ds4g_moe_forward_host) need for this layer and T tokens; 0 when the
  * descriptor or T is invalid.  The workspace must be 256-byte aligned.
  */
 DS4G_API size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
 
 /*
- * ds4g_moe_forward -- the whole layer, steps 1-4.
+ * ds4g_moe_forward -- the whole layer, steps 1-4.  Passage: the routed-MoE
+ * experts run micro-batched in decode and prefill on CUDA (ds4 README mirror,
+ * "So, what can I do with this software?" and "Model Weights").
  *   x       [T x hidden] bf16 (uint16 bits), 16-byte aligned.
  *   logits  [T x n_experts] fp32, 4-byte aligned.
  *   y       [T x hidden] fp32 out, 16-byte aligned; overwritten.
@@ -228,7 +239,9 @@ DS4G_API ds4g_status ds4g_moe_forward(const ds4g_moe_desc *desc, const uint16_t 
                              void *workspace, size_t ws_bytes, void *stream);
 
 /*
- * ds4g_moe_forward_host -- ds4g_moe_forward with HOST activations, logits
+ * ds4g_moe_forward_host -- no counterpart on the pages (a convenience for
+ * callers whose activations live in host memory).
+ * ds4g_moe_forward with HOST activations, logits
  * and output (weights stay on the device, in desc).  Copies x and logits to
  * the workspace, runs the layer, copies y back and synchronizes `stream`
  * before returning.  Host buffers should be pinned (cudaHostAlloc) for full
@@ -240,7 +253,8 @@ DS4G_API ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint
                                   void *workspace, size_t ws_bytes, void *stream);
 
 /*
- * ds4g_moe_routing_view -- device pointers, inside a workspace last used by
+ * ds4g_moe_routing_view -- no counterpart on the pages (exposes steps 1-2 of
+ * the last ds4g_moe_forward for checking).  Device pointers, inside a workspace last used by
  * ds4g_moe_forward(desc, ..., T, ...), to that call's routing results:
  * ids [T x k] int32, weights [T x k] fp32, counts [E] int32,
  * offsets [E+1] int32, perm [T*k] int32 (same meaning as ds4g_route_topk).
@@ -252,7 +266,8 @@ DS4G_API ds4g_status ds4g_moe_routing_view(const ds4g_moe_desc *desc, int32_t T,
                                   int32_t **counts, int32_t **offsets, int32_t **perm);
 
 /*
- * ds4g_moe_forward_phased -- ds4g_moe_forward that also records caller-created
+ * ds4g_moe_forward_phased -- no counterpart on the pages (measurement aid).
+ * ds4g_moe_forward that also records caller-created
  * CUDA events (cudaEvent_t, passed as void*) on `stream` at the phase
  * boundaries, for per-kernel timing:
  *   events[0] before routing,          events[1] after routing,
@@ -267,14 +282,16 @@ DS4G_API ds4g_status ds4g_moe_forward_phased(const ds4g_moe_desc *desc, const ui
                                              void *const *events, int32_t n_events);
 
 /*
- * ds4g_moe_forward_launches -- number of kernel launches one
+ * ds4g_moe_forward_launches -- no counterpart on the pages (measurement
+ * aid).  Number of kernel launches one
  * ds4g_moe_forward(desc, ..., T, ...) call enqueues (0 for an invalid
  * descriptor or T == 0).  Pure host arithmetic.
  */
 DS4G_API int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T);
 
 /*
- * ds4g_moe_device_status -- the device status word of the last
+ * ds4g_moe_device_status -- no counterpart on the pages (failure detection
+ * of this library).  The device status word of the last
  * ds4g_moe_forward on this workspace: DS4G_OK, or DS4G_ERR_TIMEOUT when a
  * bounded wait inside a kernel expired (the kernel then returned early and y
  * is not valid).  Synchronizes `stream`.  Errors: DS4G_ERR_INVALID,

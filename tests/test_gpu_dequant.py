@@ -12,7 +12,10 @@ pytestmark = pytest.mark.gpu
 
 
 def _rne_f16(f):
-    return f.astype(np.float16).view(np.uint16)
+    # random d up to 65504 times a scale of 15 overflows fp16 on purpose: the
+    # library's fp16 output must then be the same infinity as RNE gives
+    with np.errstate(over="ignore"):
+        return f.astype(np.float16).view(np.uint16)
 
 
 def _random_q2k(n, seed):

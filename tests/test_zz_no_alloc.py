@@ -2,14 +2,18 @@
 memory (a plugin whose host runtime owns every allocation, or a serving loop
 that must not call cudaMalloc once running).  Its scratch is a static device
 array inside the library.  Checked against the workspace entry point,
-ds4g_moe_forward, with the layer tolerance, on two calls in a row (the second
-call reuses the array the first one left behind).  Collected last so that a
+ds4g_moe_forward, on two calls in a row (the second call reuses the array
+the first one left behind): both run the same deterministic kernels, so the
+outputs must be bit-identical, which also shows that nothing a call leaves
+in the array leaks into the next one.  One case is forced onto the
+tensor-core kernels, one is the codebook format.  Collected last so that a
 stop-at-first-failure run has already run every other test."""
 import numpy as np
 import pytest
 import torch
 
 import bit_quantized_routed_route_b300 as D
+import ds4g_synth as S
 import oracle_pins as P
 from gpu_helpers import cached_layer, check_output, run_forward, to_device
 
@@ -23,19 +27,33 @@ def _dev_inputs(layer):
     return x, lg
 
 
-@pytest.mark.parametrize("which", ["decode_1tok", "small"])
+def _small(which):
+    if which == "small":
+        return P.small_layer(seed=77, H=1024, I=320, E=12, k=3, T=5), 0
+    if which == "small_tc":            # segments over one 128-token tile
+        return P.small_layer(seed=78, H=1024, I=256, E=4, k=2, T=200, align=16), D.FORCE_TC
+    if which == "small_codebook":
+        return P.small_layer(seed=79, H=512, I=256, E=5, k=2, T=40, fmt=S.FMT_CB2, align=16,
+                             score=S.SCORE_SIGMOID), 0
+    return cached_layer(which), 0
+
+
+@pytest.mark.parametrize("which", ["decode_1tok", "small", "small_tc", "small_codebook"])
 def test_noalloc_matches_workspace_entry_point_twice(which):
-    layer = cached_layer(which) if which != "small" else P.small_layer(
-        seed=77, H=1024, I=320, E=12, k=3, T=5)
-    L = to_device(layer)
+    layer, flags = _small(which)
+    L = to_device(layer, flags=flags)
     y_ws, _ = run_forward(L, layer["x"], layer["logits"])      # ds4g_moe_forward
     x, lg = _dev_inputs(layer)
     T, H = layer["x"].shape
+    assert L.workspace_bytes(T) <= D.NOALLOC_SCRATCH_BYTES
     for _ in range(2):
         y = torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda")
         D.check(D.moe_forward_noalloc(L.desc, x, lg, T, y))
         torch.cuda.synchronize()
-        check_output(y.cpu().numpy(), y_ws.astype(np.float64))
+        got = y.cpu().numpy()
+        check_output(got, y_ws.astype(np.float64))
+        assert np.array_equal(got.view(np.uint32), y_ws.view(np.uint32)), \
+            "no-alloc output differs from the workspace entry point's"
 
 
 def test_noalloc_rejects_plans_beyond_the_static_scratch():
