@@ -15,39 +15,46 @@
 //
 // Roles inside a CTA (one CTA per SM, persistent over the items):
 //   warp 0     TMA producer: per 256-wide K step, the 16-byte aligned window
-//              of each weight row's 84-byte super-block (a 3-D tensor map
-//              over [experts][rows][row words]) and the activation tile (a
-//              2-D tensor map over [segment rows][K], fp16, 128-byte swizzle)
+//              of each weight row's super-block (a 3-D tensor map over
+//              [experts][rows][row words]) and the activation tile (a 2-D
+//              tensor map over [segment rows][K], fp16, 128-byte swizzle)
 //              land in a two-stage shared-memory ring;
 //   warp 1     MMA issuer: tcgen05.mma kind::f16, A (dequantized weights)
 //              from tensor memory, B (activations) from shared memory, fp32
 //              accumulators in tensor memory;
-//   warps 2-9  dequantizers, two warpgroups: each thread owns one weight row,
-//              reads its block from shared memory, forms fp16 weights in
-//              registers and stores them to tensor memory (tcgen05.st) as
-//              the next A buffer.  In the gate/up kernel they are also the
-//              epilogue after each item (tcgen05.ld of the accumulators,
-//              SiLU*up, fp16 stores of h);
-//   warps 10-13  down kernel only: the epilogue (tcgen05.ld, routing weight,
+//   warps 2-17 dequantizers, four warpgroups of four warps: each thread owns
+//              one weight row and, per fill of an A buffer, one quarter of
+//              it (32 columns = 64 weights): gate/up kernel warpgroup w is
+//              (matrix w/2, field pair w%2) of the fill's half super-block,
+//              down kernel warpgroup w is (half w/2, field pair w%2) of the
+//              K step's block.  It forms fp16 weights in registers and
+//              stores them to tensor memory (tcgen05.st).  In the gate/up
+//              kernel the sixteen warps are also the epilogue after each
+//              item (tcgen05.ld of the accumulators, SiLU*up, fp16 stores
+//              of h);
+//   warps 18-21  down kernel only: the epilogue (tcgen05.ld, routing weight,
 //              fp32 stores of yslot), on double-buffered accumulators so
 //              the next item's MMAs overlap it.
 //
 // Weight values.  w = d*(sc&15)*q - dmin*(sc>>4) is formed on half2 pairs
-// with two roundings, each relative to w (q2k_half below); the per-token
-// relative L2 error of the layer stays near 5e-4.  The pair order inside
-// each aligned group of 4 weights is (0, 2, 1, 3), the order the lop3
-// extraction yields; the activation operand is stored in the same permuted
-// order, so the contraction is unchanged.  Codebook-2-bit weights keep the
-// natural order: each 8-weight codebook row comes from a 16-way replicated
-// copy of the codebook in shared memory, c*s is formed exactly in fp16 and
-// the single rounding is the multiply by d.
+// with two roundings, each relative to w (q2k_quarter below); the per-token
+// relative L2 error of the layer stays near 5e-4.  A pair holds weights l
+// and l+16 of one 32-weight field group: they lie in the two sub-blocks of
+// the group, so one half2 of scales serves both lanes without replication.
+// Inside every aligned group of 32, weight 16b + l is stored at K position
+// 2l + b (the activation operand and h use the same order, so the
+// contraction is unchanged).  Codebook-2-bit weights keep the natural order:
+// each 8-weight codebook row comes from a 16-way replicated copy of the
+// codebook in shared memory, c*s is formed exactly in fp16 and the single
+// rounding is the multiply by d.
 //
 // Tensor memory (512 columns): columns 0..255 are two A buffers of 128
 // columns (K = 128 fp16 per matrix-half pair, or K = 256 of one matrix);
 // columns 256..383 and 384..511 are the fp32 accumulators (gate and up, or
-// the down kernel's two alternating accumulators).  Every mbarrier wait is bounded; on expiry the kernel records
-// DS4G_ERR_TIMEOUT in the status word, lets every role leave its loop,
-// drains its own copies and MMAs (bounded) and frees its tensor memory.
+// the down kernel's two alternating accumulators).  Every mbarrier wait is
+// bounded; on expiry the kernel records DS4G_ERR_TIMEOUT in the status word,
+// lets every role leave its loop, drains its own copies and MMAs (bounded)
+// and frees its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -68,11 +75,11 @@ constexpr int kWinWords = 28;             // 112-byte window per weight row
 constexpr int kAqBytes = kWinWords * 4 * kBM;
 constexpr int kChunkBytes = kNT * 128;    // one 64-wide K chunk of the activation tile
 constexpr int kBBytes = 4 * kChunkBytes;
-constexpr int kDequantWarps = 8;
+constexpr int kDequantWarps = 16;          // four warpgroups
 constexpr int kEpilogueWarps = 4;          // down kernel: dedicated epilogue warps
 __host__ __device__ constexpr int tc_threads(int mode)
 {
-    return (2 + kDequantWarps + (mode == 1 ? kEpilogueWarps : 0)) * 32;
+    return (3 + kDequantWarps + (mode == 1 ? kEpilogueWarps : 0)) * 32;   // producer, 2 issuers
 }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 256;
@@ -92,7 +99,12 @@ struct TcArgs {
     int stall;                  // debug: the producer issues nothing (tests the bounded waits)
 };
 
-__device__ __forceinline__ int perm4(int n) { return (n & ~3) | ((n & 1) << 1) | ((n >> 1) & 1); }
+// K position of element n inside its aligned group of 32 (Q2_K operands):
+// element 16b + l goes to 2l + b.
+__host__ __device__ __forceinline__ int perm32(int n)
+{
+    return (n & ~31) | ((n & 15) << 1) | ((n >> 4) & 1);
+}
 
 __device__ __forceinline__ void set_status(int32_t *status, int code)
 {
@@ -112,84 +124,83 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_
     }
 }
 
-// The 64 packed fp16 pairs (128 weights) of half `h` of one Q2_K block for
-// this thread's row.  `w`: the block's 21 words (scales 0..3, qs 4..19,
-// d|dmin 20).
+// Per-warp constants of the dequantizing role: this warp's quarter of every
+// fill is half HH, field pair GH (Q2_K) / 64-weight half GH (codebook) of
+// the block, columns 32 * (2*HH + GH) .. +31 of the A buffer.
+struct QuarterConst {
+    int hh, gh;
+    uint32_t mask[2];           // Q2_K: 2-bit field masks of g = 2*gh, 2*gh+1 (both lanes)
+    uint32_t p4[2], c4[2];      // Q2_K: 4^-g and -1024 * 4^-g, replicated fp16
+};
+
+__device__ __forceinline__ QuarterConst quarter_const(int hh, int gh)
+{
+    QuarterConst q;
+    q.hh = hh;
+    q.gh = gh;
+#pragma unroll
+    for (int gi = 0; gi < 2; ++gi) {
+        const int g = 2 * gh + gi;
+        q.mask[gi] = 0x00030003u << (2 * g);
+        // fp16 4^-g: exponent 15 - 2g; -1024 * 4^-g: sign, exponent 25 - 2g
+        q.p4[gi] = 0x3C003C00u - (uint32_t)g * 0x08000800u;
+        q.c4[gi] = 0xE400E400u - (uint32_t)g * 0x08000800u;
+    }
+    return q;
+}
+
+// One quarter of a fill for this thread's row of a Q2_K block: the field
+// pair g = 2*gh, 2*gh+1 of half hh, 64 weights as 32 fp16 pairs.  `qw`: the
+// three 16-byte units of the window from word 4 + 8*hh (the half's qs bytes
+// start SH words into it); `sw`: the scale word of sub-blocks 8*hh + 4*gh
+// .. +3; `dd`: the d | dmin word.
 //
-// Per weight, with exact fp16 operands throughout:
+// Pair (l, l+16) of field g (l = 0..15) holds weights 32g + l and 32g + l + 16
+// of the half: sub-blocks 2g and 2g+1, so each lane of the half2 has its own
+// sub-block scale.  Per weight, with exact fp16 operands throughout:
 //   v  = 1024 + q*4^g           lop3 of the 2-bit field in place (no shift)
 //   n  = v*S + C = q*sc         S = sc*4^-g, C = -1024*S; exact (integer <= 45)
 //   w1 = fp16(n*d + c_hi)       one rounding, relative to w itself
 //   w  = fp16(w1 + c_lo)        c_hi + c_lo = -dmin*m exactly (c_lo from an fma)
 // Rounding d*sc or dmin*m to fp16 before the subtraction instead would be
 // amplified by the cancellation between the two terms of a Q2_K weight.
-__device__ __forceinline__ void q2k_half(const uint32_t *w, int h, uint32_t (&out)[64])
+// out[16*gi + l] = the pair of field 2*gh + gi (column 16g + l of the half).
+template <int SH>
+__device__ __forceinline__ void q2k_quarter(const uint32_t (&qw)[12], uint32_t sw, uint32_t dd,
+                                            const QuarterConst &k, uint32_t (&out)[32])
 {
-    const uint32_t dd = w[20];
     const uint32_t d2 = __byte_perm(dd, 0, 0x1010);                    // (d, d)
     const uint32_t ndmin2 = __byte_perm(dd, 0, 0x3232) ^ 0x80008000u;  // (-dmin, -dmin)
     const uint32_t k1024 = 0x64006400u, kn1024 = 0xE400E400u;
-    // 4^-g and -1024 * 4^-g, g = 0..3, replicated fp16
-    const uint32_t p4[4] = {0x3C003C00u, 0x34003400u, 0x2C002C00u, 0x24002400u};
-    const uint32_t c4[4] = {0xE400E400u, 0xDC00DC00u, 0xD400D400u, 0xCC00CC00u};
-    uint32_t S2[8], C2[8], HI2[8], LO2[8];
+    uint32_t S2[2], C2[2], HI2[2], LO2[2];
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-        const uint32_t sw = w[2 * h + (s >> 2)];
-        const uint32_t j = (uint32_t)(s & 3);
-        const uint32_t rep = __byte_perm(sw, 0, 0x4040u | j | (j << 8));   // byte j twice
+    for (int gi = 0; gi < 2; ++gi) {
+        // scale bytes 2gi and 2gi+1 of the word (sub-blocks 2g, 2g+1) -> the two halves
+        const uint32_t rep = __byte_perm(sw, 0, gi == 0 ? 0x4140u : 0x4342u);
         const uint32_t sc2 = ptx::lop3_and_or(rep, 0x000F000Fu, k1024);       // 1024 + sc
         const uint32_t mn2 = ptx::lop3_and_or(rep >> 4, 0x000F000Fu, k1024);  // 1024 + m
-        S2[s] = ptx::hfma2_u(sc2, p4[s >> 1], c4[s >> 1]);                   // sc * 4^-g
-        C2[s] = ptx::hmul2_u(S2[s], kn1024);
-        const uint32_t mnf = ptx::hsub2_u(mn2, k1024);                       // m
-        HI2[s] = ptx::hmul2_u(mnf, ndmin2);
-        LO2[s] = ptx::hfma2_u(mnf, ndmin2, HI2[s] ^ 0x80008000u);
+        S2[gi] = ptx::hfma2_u(sc2, k.p4[gi], k.c4[gi]);                      // sc * 4^-g
+        C2[gi] = ptx::hmul2_u(S2[gi], kn1024);
+        const uint32_t mnf = ptx::hsub2_u(mn2, k1024);                      // m
+        HI2[gi] = ptx::hmul2_u(mnf, ndmin2);
+        LO2[gi] = ptx::hfma2_u(mnf, ndmin2, HI2[gi] ^ 0x80008000u);
     }
 #pragma unroll
-    for (int wd = 0; wd < 8; ++wd) {
-        const uint32_t qw = w[4 + 8 * h + wd];
-        const uint32_t qh = qw >> 8;
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t A = qw[SH + i];                      // qs bytes 4i .. 4i+3 of the half
+        const uint32_t B = qw[SH + 4 + i];                  // qs bytes 16+4i .. 16+4i+3
+        const uint32_t W1 = __byte_perm(A, B, 0x5410);      // A0 A1 B0 B1
+        const uint32_t W2 = __byte_perm(A, B, 0x7632);      // A2 A3 B2 B3
+        const uint32_t Wu[4] = {W1, W1 >> 8, W2, W2 >> 8};  // pairs (4i+u, 4i+u+16)
 #pragma unroll
-        for (int g = 0; g < 4; ++g) {
-            const int s = 2 * g + (wd >> 2);
-            const uint32_t mask = 0x00030003u << (2 * g);
-            const uint32_t v0 = ptx::lop3_and_or(qw, mask, k1024);
-            const uint32_t v1 = ptx::lop3_and_or(qh, mask, k1024);
-            const uint32_t n0 = ptx::hfma2_u(v0, S2[s], C2[s]);
-            const uint32_t n1 = ptx::hfma2_u(v1, S2[s], C2[s]);
-            out[16 * g + 2 * wd] = ptx::hadd2_u(ptx::hfma2_u(n0, d2, HI2[s]), LO2[s]);
-            out[16 * g + 2 * wd + 1] = ptx::hadd2_u(ptx::hfma2_u(n1, d2, HI2[s]), LO2[s]);
+        for (int u = 0; u < 4; ++u) {
+#pragma unroll
+            for (int gi = 0; gi < 2; ++gi) {
+                const uint32_t v = ptx::lop3_and_or(Wu[u], k.mask[gi], k1024);
+                const uint32_t n = ptx::hfma2_u(v, S2[gi], C2[gi]);
+                out[16 * gi + 4 * i + u] = ptx::hadd2_u(ptx::hfma2_u(n, d2, HI2[gi]), LO2[gi]);
+            }
         }
-    }
-}
-
-// Dequantizes half HALF of this thread's row block (the block starts at word
-// SH of the 112-byte window `win`) and stores it to tensor-memory columns
-// taddr.col .. +63 of this warp's 32 lanes.
-template <int SH, int HALF>
-__device__ __forceinline__ void dequant_store(const uint32_t (&win)[24], uint32_t taddr)
-{
-    uint32_t out[64];
-    q2k_half(win + SH, HALF, out);
-    ptx::tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&out[0]));
-    ptx::tmem_st32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&out[32]));
-}
-
-// Register arrays are only indexed with constants: dispatch on the
-// (warp-uniform) word offset and half.
-__device__ __forceinline__ void dequant_store_sh(const uint32_t (&win)[24], int sh, int half,
-                                                 uint32_t taddr)
-{
-    switch (sh * 2 + half) {
-    case 0: dequant_store<0, 0>(win, taddr); break;
-    case 1: dequant_store<0, 1>(win, taddr); break;
-    case 2: dequant_store<1, 0>(win, taddr); break;
-    case 3: dequant_store<1, 1>(win, taddr); break;
-    case 4: dequant_store<2, 0>(win, taddr); break;
-    case 5: dequant_store<2, 1>(win, taddr); break;
-    case 6: dequant_store<3, 0>(win, taddr); break;
-    default: dequant_store<3, 1>(win, taddr); break;
     }
 }
 
@@ -203,33 +214,36 @@ __device__ __forceinline__ void dequant_store_sh(const uint32_t (&win)[24], int 
 //   n ^= sign bits                the weight's sign from the sign byte
 //   w = fp16(n * d)               one rounding, relative to w
 // Weights stay in natural order; the activation operand is stored likewise.
+// One quarter of a fill: weights 128*hh + 64*gh .. +63 of the block (groups
+// of 8 o = 16hh + 8gh .. +7, 32-weight scale groups 4hh + 2gh, +1).  `iw`,
+// `gw`: the window words holding idx / sgn bytes of those groups (three each,
+// for the funnel shift), `tw`: the words holding sc and d; `fs`: the block's
+// bit offset inside its first word.
 // ---------------------------------------------------------------------------
 constexpr int kCbCopies = 16;
 constexpr int kCbRepBytes = 256 * kCbCopies * 8;
 
-template <int WO, int HALF>
-__device__ __forceinline__ void cb2_store(const uint32_t (&win)[24], uint32_t fs, uint32_t cb_lane,
-                                          uint32_t taddr)
+__device__ __forceinline__ void cb2_quarter(const uint32_t (&iw)[3], const uint32_t (&gw)[3],
+                                            const uint32_t (&tw)[3], uint32_t fs, int hh, int gh,
+                                            uint32_t cb_lane, uint32_t (&out)[32])
 {
-    // the block's words (it starts fs/8 bytes into word WO of the window)
-    auto word = [&](int i) -> uint32_t { return __funnelshift_r(win[WO + i], win[WO + i + 1], fs); };
-    const uint32_t d2 = __byte_perm(word(17), 0, 0x1010);
-    const uint32_t scw = word(16);
-    uint32_t s2[4], ns2[4], idxw[4], sgnw[4];
+    const uint32_t d2 = __byte_perm(__funnelshift_r(tw[1], tw[2], fs), 0, 0x1010);
+    const uint32_t scw = __funnelshift_r(tw[0], tw[1], fs);
+    uint32_t s2[2], ns2[2];
 #pragma unroll
-    for (int G = 0; G < 4; ++G) {
-        const float sf = (float)((scw >> (4 * (4 * HALF + G))) & 15u);
-        s2[G] = ptx::pack_half2(sf, sf);
-        ns2[G] = ptx::pack_half2(-1152.0f * sf, -1152.0f * sf);
-        idxw[G] = word(4 * HALF + G);
-        sgnw[G] = word(8 + 4 * HALF + G);
+    for (int Gi = 0; Gi < 2; ++Gi) {
+        const int G = 4 * hh + 2 * gh + Gi;
+        const float sf = (float)((scw >> (4 * G)) & 15u);
+        s2[Gi] = ptx::pack_half2(sf, sf);
+        ns2[Gi] = ptx::pack_half2(-1152.0f * sf, -1152.0f * sf);
     }
-    uint32_t out[64];
+    const uint32_t idxw[2] = {__funnelshift_r(iw[0], iw[1], fs), __funnelshift_r(iw[1], iw[2], fs)};
+    const uint32_t sgnw[2] = {__funnelshift_r(gw[0], gw[1], fs), __funnelshift_r(gw[1], gw[2], fs)};
 #pragma unroll
-    for (int o = 0; o < 16; ++o) {
-        const uint32_t idx = (idxw[o >> 2] >> (8 * (o & 3))) & 0xFFu;
-        const uint32_t sg = (sgnw[o >> 2] >> (8 * (o & 3))) & 0xFFu;
-        const int G = o >> 2;
+    for (int oi = 0; oi < 8; ++oi) {
+        const uint32_t idx = (idxw[oi >> 2] >> (8 * (oi & 3))) & 0xFFu;
+        const uint32_t sg = (sgnw[oi >> 2] >> (8 * (oi & 3))) & 0xFFu;
+        const int Gi = oi >> 2;
         uint32_t cw[2];
         asm volatile("ld.shared.v2.b32 {%0, %1}, [%2];" : "=r"(cw[0]), "=r"(cw[1]) : "r"(cb_lane + idx * (kCbCopies * 8)));
 #pragma unroll
@@ -240,29 +254,173 @@ __device__ __forceinline__ void cb2_store(const uint32_t (&win)[24], uint32_t fs
             const uint32_t x = sg >> (4 * q);
             const uint32_t m0 = ((x & 1u) << 15) | ((x & 2u) << 30);
             const uint32_t m1 = ((x & 4u) << 13) | ((x & 8u) << 28);
-            out[4 * o + 2 * q] = ptx::hmul2_u(ptx::hfma2_u(v0, s2[G], ns2[G]) ^ m0, d2);
-            out[4 * o + 2 * q + 1] = ptx::hmul2_u(ptx::hfma2_u(v1, s2[G], ns2[G]) ^ m1, d2);
+            out[4 * oi + 2 * q] = ptx::hmul2_u(ptx::hfma2_u(v0, s2[Gi], ns2[Gi]) ^ m0, d2);
+            out[4 * oi + 2 * q + 1] = ptx::hmul2_u(ptx::hfma2_u(v1, s2[Gi], ns2[Gi]) ^ m1, d2);
         }
     }
-    ptx::tmem_st32(taddr, *reinterpret_cast<const uint32_t(*)[32]>(&out[0]));
-    ptx::tmem_st32(taddr + 32, *reinterpret_cast<const uint32_t(*)[32]>(&out[32]));
 }
 
-__device__ __forceinline__ void cb2_store_off(const uint32_t (&win)[24], int byteoff, int half,
-                                              uint32_t cb_lane, uint32_t taddr)
-{
-    const uint32_t fs = (uint32_t)(byteoff & 3) * 8;
-    switch ((byteoff >> 2) * 2 + half) {
-    case 0: cb2_store<0, 0>(win, fs, cb_lane, taddr); break;
-    case 1: cb2_store<0, 1>(win, fs, cb_lane, taddr); break;
-    case 2: cb2_store<1, 0>(win, fs, cb_lane, taddr); break;
-    case 3: cb2_store<1, 1>(win, fs, cb_lane, taddr); break;
-    case 4: cb2_store<2, 0>(win, fs, cb_lane, taddr); break;
-    case 5: cb2_store<2, 1>(win, fs, cb_lane, taddr); break;
-    case 6: cb2_store<3, 0>(win, fs, cb_lane, taddr); break;
-    default: cb2_store<3, 1>(win, fs, cb_lane, taddr); break;
+// Shared state of one CTA of tc_kernel (barriers, tensor memory, abort flag).
+struct TcCta {
+    uint8_t *smem;
+    uint64_t *full, *empty, *afull, *aempty, *accfull, *accempty;
+    uint32_t tmem;
+    uint32_t cbrep;             // shared address of the replicated codebook
+    volatile int *abort_flag;
+    int n_items, KB;
+};
+
+// The dequantizing role of one warp (both kernels).  Every fill of an A
+// buffer is one matrix's whole block (K = 256, 128 columns): the gate/up
+// kernel fills W_gate then W_up per K step, the down kernel W_down.  This
+// warp's quarter is fixed (QuarterConst); the block's offset inside its
+// 16-byte aligned window (repeating every 4 K steps for Q2_K, 8 for the
+// codebook format) is dispatched once per fill to a body where it is a
+// compile-time constant, so all warps share the same few bodies.
+template <int MODE, int FMT>
+struct DequantRole {
+    static constexpr int NMAT = MODE == 0 ? 2 : 1;
+    static constexpr uint32_t kStageBytes = kBBytes + NMAT * kAqBytes;
+
+    const TcArgs &a;
+    const TcCta &c;
+    QuarterConst k;
+    int lane, row, wg;
+    uint32_t lane_base;
+    int sc = 0, fc = 0;
+    bool ok = true;
+
+    __device__ __forceinline__ DequantRole(const TcArgs &a_, const TcCta &c_, int warp, int lane_,
+                                           int wg_)
+        : a(a_), c(c_), lane(lane_), wg(wg_)
+    {
+        k = quarter_const(wg >> 1, wg & 1);
+        const int quarter = warp & 3;             // tensor-memory lane quarter
+        row = 32 * quarter + lane;
+        lane_base = (uint32_t)(32 * quarter) << 16;
     }
-}
+
+    template <int SH>
+    __device__ __forceinline__ void q2k_fill(const uint8_t *win, uint32_t (&out)[32])
+    {
+        // 16-byte units 1 + 2hh .. 3 + 2hh hold the half's qs words (from word SH)
+        uint32_t qw[12];
+        const uint4 *u = reinterpret_cast<const uint4 *>(win) + 1 + 2 * k.hh;
+#pragma unroll
+        for (int v = 0; v < 3; ++v) {
+            const uint4 q = u[v];
+            qw[4 * v] = q.x;
+            qw[4 * v + 1] = q.y;
+            qw[4 * v + 2] = q.z;
+            qw[4 * v + 3] = q.w;
+        }
+        const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win);
+        const uint32_t sw = w32[SH + 2 * k.hh + k.gh];
+        const uint32_t dd = w32[SH + 20];
+        q2k_quarter<SH>(qw, sw, dd, k, out);
+    }
+
+    __device__ __forceinline__ void cb2_fill(const uint8_t *win, int boff, uint32_t (&out)[32])
+    {
+        const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win) + (boff >> 2);
+        const int o = 4 * k.hh + 2 * k.gh;
+        uint32_t iw[3], gw[3], tw[3];
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+            iw[j] = w32[o + j];
+            gw[j] = w32[8 + o + j];
+            tw[j] = w32[16 + j];
+        }
+        cb2_quarter(iw, gw, tw, (uint32_t)(boff & 3) * 8, k.hh, k.gh,
+                    c.cbrep + (uint32_t)(lane & 15) * 8, out);
+    }
+
+    // One fill: matrix `mat` of K step kb from stage s.
+    __device__ __forceinline__ void fill(int s, int mat, int kb)
+    {
+        const int buf = fc & 1;
+        if (fc >= 2) {
+            ok = wait_bar(&c.aempty[buf], ((fc >> 1) - 1) & 1, a.wait_ns, c.abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) return;
+            ptx::tc_fence_after();
+        }
+        const uint8_t *win = c.smem + (size_t)s * kStageBytes + kBBytes + mat * kAqBytes +
+                             row * (kWinWords * 4);
+        uint32_t out[32];
+        if (FMT == DS4G_FMT_Q2K) {
+            switch (kb & 3) {           // (84 * kb) mod 16, in words
+            case 0: q2k_fill<0>(win, out); break;
+            case 1: q2k_fill<1>(win, out); break;
+            case 2: q2k_fill<2>(win, out); break;
+            default: q2k_fill<3>(win, out); break;
+            }
+        } else {
+            cb2_fill(win, (kCB2Bytes * kb) & 15, out);
+        }
+        ptx::tmem_st32(c.tmem + lane_base + (uint32_t)buf * 128u + 32u * wg, out);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c.afull[buf]);
+        ++fc;
+    }
+
+    __device__ __forceinline__ void run()
+    {
+        int ic = 0;
+        for (int it = blockIdx.x; ok && it < c.n_items; it += gridDim.x, ++ic) {
+            const int tile = it / a.m_tiles, mt = it % a.m_tiles;
+            const int row0 = a.tiles[4 * tile + 1], nlen = a.tiles[4 * tile + 2];
+            for (int kb = 0; ok && kb < c.KB; ++kb, ++sc) {
+                const int s = sc % kStages;
+                ok = wait_bar(&c.full[s], (sc / kStages) & 1, a.wait_ns, c.abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                for (int mat = 0; ok && mat < NMAT; ++mat) fill(s, mat, kb);
+            }
+            if (!ok) break;
+            if (MODE == 1) continue;                 // the epilogue warps finish down items
+            // gate/up epilogue of the item: chunks of 8 tokens, warpgroup w
+            // takes chunks w, w + 4, ...; accumulator 0 = gate, 1 = up
+            ok = wait_bar(&c.accfull[0], ic & 1, a.wait_ns, c.abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int chunks = (nlen + 7) / 8;
+            const int n = mt * kBM + row;
+            const int col = FMT == DS4G_FMT_Q2K ? perm32(n) : n;
+            for (int ch = wg; ch < chunks; ch += 4) {
+                float g[8], u[8];
+                ptx::tmem_ld8(c.tmem + lane_base + kAccCol + 8 * ch, g);
+                ptx::tmem_ld8(c.tmem + lane_base + kAccCol + 128 + 8 * ch, u);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int t = 8 * ch + j;
+                    if (t < nlen)
+                        a.hp[(size_t)(row0 + t) * a.I_pad + col] =
+                            __float2half_rn(silu_mul(g[j], u[j]));
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&c.accempty[0]);
+        }
+        if (!ok) {
+            if (lane == 0) set_status(a.status, DS4G_ERR_TIMEOUT);
+            *c.abort_flag = 1;
+        }
+    }
+};
+
+// Weight-window prefetch distance of the producer, in K steps.
+constexpr int kPrefetchSteps = 6;
+
+// Warps of tc_kernel: 0 TMA producer, 1-2 MMA issuers, then the dequantizers,
+// then (down kernel) the epilogue warps.
+constexpr int kIssuers = 2;
+constexpr int kFirstDequantWarp = 1 + kIssuers;
 
 template <int MODE, int FMT>
 __global__ void __launch_bounds__(tc_threads(MODE), 1)
@@ -271,13 +429,12 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
 {
     constexpr int NMAT = MODE == 0 ? 2 : 1;
     constexpr uint32_t kStageBytes = kBBytes + NMAT * kAqBytes;
-    constexpr int kFills = MODE == 0 ? 2 : 1;     // A buffers per K step
     constexpr int kBlockBytes = FMT == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], afull[2], aempty[2];
-    __shared__ __align__(8) uint64_t accfull[2], accempty[2], drain;
+    __shared__ __align__(8) uint64_t accfull, accempty, drain[kIssuers];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort, s_issued;
 
@@ -285,17 +442,15 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
             ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&empty[s], NMAT);        // one commit per fill of the stage
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&afull[b], kDequantWarps);
             ptx::mbar_init(&aempty[b], 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(&accfull[b], 1);
-            ptx::mbar_init(&accempty[b], MODE == 0 ? kDequantWarps : kEpilogueWarps);
-        }
-        ptx::mbar_init(&drain, 1);
+        ptx::mbar_init(&accfull, kIssuers);
+        ptx::mbar_init(&accempty, MODE == 0 ? kDequantWarps : kEpilogueWarps);
+        for (int i = 0; i < kIssuers; ++i) ptx::mbar_init(&drain[i], 1);
         ptx::fence_mbar_init();
         s_abort = 0;
         s_issued = 0;
@@ -324,10 +479,26 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
+        // The weight windows of the K step kPrefetchSteps ahead are also
+        // prefetched into L2, so the ring's copies of them hit L2.
         if (lane == 0 && !a.stall) {
             ptx::prefetch_tmap(&tm_a0);
             if (NMAT == 2) ptx::prefetch_tmap(&tm_a1);
             ptx::prefetch_tmap(&tm_b);
+            int pf_it = blockIdx.x, pf_kb = 0;       // the prefetch cursor
+            auto prefetch_next = [&]() {
+                if (pf_it >= n_items) return;
+                const int tile = pf_it / a.m_tiles, mt = pf_it % a.m_tiles;
+                const int e = a.tiles[4 * tile];
+                const int x = ((kBlockBytes * pf_kb) & ~15) / 4;
+                ptx::tma_prefetch_3d(&tm_a0, x, mt * kBM, e);
+                if (NMAT == 2) ptx::tma_prefetch_3d(&tm_a1, x, mt * kBM, e);
+                if (++pf_kb == KB) {
+                    pf_kb = 0;
+                    pf_it += gridDim.x;
+                }
+            };
+            for (int i = 0; i < kPrefetchSteps; ++i) prefetch_next();
             int sc = 0;
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
@@ -346,91 +517,87 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                     }
                     uint8_t *st = smem + (size_t)s * kStageBytes;
                     ptx::mbar_arrive_expect_tx(&full[s], bytes);
-                    for (int kc = 0; kc < 4; ++kc)
-                        for (int r = 0; r < nb; ++r)
-                            ptx::tma_load_2d(st + kc * kChunkBytes + r * kBoxRows * 128, &tm_b,
-                                             kb * kQK + 64 * kc, row0 + kBoxRows * r, &full[s]);
                     const int x = ((kBlockBytes * kb) & ~15) / 4;
                     ptx::tma_load_3d(st + kBBytes, &tm_a0, x, mt * kBM, e, &full[s]);
                     if (NMAT == 2)
                         ptx::tma_load_3d(st + kBBytes + kAqBytes, &tm_a1, x, mt * kBM, e, &full[s]);
+                    for (int kc = 0; kc < 4; ++kc)
+                        for (int r = 0; r < nb; ++r)
+                            ptx::tma_load_2d(st + kc * kChunkBytes + r * kBoxRows * 128, &tm_b,
+                                             kb * kQK + 64 * kc, row0 + kBoxRows * r, &full[s]);
                     s_issued = sc + 1;
+                    prefetch_next();
                 }
             }
         }
-    } else if (warp == 1) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            int sc = 0, fc = 0, ic = 0;
-            bool ok = true;
-            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
-                const int tile = it / a.m_tiles;
-                const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
-                const uint32_t idesc = ptx::idesc_f16(kBM, nb * kBoxRows);
-                // gate/up: one accumulator pair; down: two accumulators, so the
-                // epilogue warps drain one while the next item accumulates
-                const int ab = MODE == 1 ? (ic & 1) : 0;
-                const int uses = MODE == 1 ? (ic >> 1) : ic;
-                if (uses > 0 && !wait_bar(&accempty[ab], (uses - 1) & 1, a.wait_ns, abort_flag)) {
-                    ok = false;
-                    break;
-                }
+    } else if (warp < kFirstDequantWarp) {
+        // ---------------- MMA issuers ----------------
+        // Issuer X owns A buffer X and accumulator X and issues every fill
+        // with (global fill index) % 2 == X: in the gate/up kernel the W_gate
+        // (X = 0) or W_up (X = 1) fill of every K step, in the down kernel
+        // every other K step (accumulator X holds the K steps of its parity;
+        // the epilogue adds the two in a fixed order).  One thread cannot
+        // issue tcgen05.mma faster than about one per 55 cycles, which is
+        // slower than the tensor pipe at the token counts of a segment; two
+        // issuers keep it fed.  The whole warp runs the loop; lane 0 issues.
+        const int X = warp - 1;
+        const uint64_t desc0 = ptx::sw128_desc(ptx::smem_addr(smem));
+        const uint32_t acc = tmem + kAccCol + 128u * (uint32_t)X;
+        int sc = 0, nx = 0, ic = 0;                  // stages, fills of this issuer, items
+        bool ok = true;
+        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
+            const int tile = it / a.m_tiles;
+            const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
+            const uint32_t idesc = ptx::idesc_f16(kBM, nb * kBoxRows);
+            if (ic > 0) {
+                ok = wait_bar(&accempty, (ic - 1) & 1, a.wait_ns, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
+            ptx::tc_fence_after();
+            bool first = true;
+            for (int kb = 0; ok && kb < KB; ++kb, ++sc) {
+                // gate/up: every stage has this issuer's fill; down: stages of parity X
+                if (MODE == 1 && (sc & 1) != X) continue;
+                const int s = sc % kStages;
+                ok = wait_bar(&full[s], (sc / kStages) & 1, a.wait_ns, abort_flag);
+                ok = ok && wait_bar(&afull[X], nx & 1, a.wait_ns, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
                 ptx::tc_fence_after();
-                const uint32_t acc_col = kAccCol + 128u * ab;
-                for (int kb = 0; ok && kb < KB; ++kb, ++sc) {
-                    const int s = sc % kStages;
-                    if (!wait_bar(&full[s], (sc / kStages) & 1, a.wait_ns, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
-                    const uint32_t b_base = ptx::smem_addr(smem + (size_t)s * kStageBytes);
-                    for (int h = 0; h < kFills; ++h, ++fc) {
-                        const int buf = fc & 1;
-                        if (!wait_bar(&afull[buf], (fc >> 1) & 1, a.wait_ns, abort_flag)) {
-                            ok = false;
-                            break;
-                        }
-                        ptx::tc_fence_after();
-                        const uint32_t a_buf = tmem + (uint32_t)buf * 128u;
-                        if (MODE == 0) {
+                const uint64_t dst = desc0 + (uint64_t)((s * kStageBytes) >> 4);
+                const uint32_t a_buf = tmem + (uint32_t)X * 128u;
+                if (lane == 0) {
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int kk = 128 * h + 16 * i;
-                                const uint64_t bd = ptx::sw128_desc(
-                                    b_base + (kk >> 6) * kChunkBytes + (kk & 63) * 2);
-                                const bool acc = !(kb == 0 && h == 0 && i == 0);
-                                ptx::mma_f16_ts(tmem + kAccCol, a_buf + 8 * i, bd, idesc, acc);
-                                ptx::mma_f16_ts(tmem + kAccCol + 128, a_buf + 64 + 8 * i, bd, idesc,
-                                                acc);
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i) {
-                                const int kk = 16 * i;
-                                const uint64_t bd = ptx::sw128_desc(
-                                    b_base + (kk >> 6) * kChunkBytes + (kk & 63) * 2);
-                                ptx::mma_f16_ts(tmem + acc_col, a_buf + 8 * i, bd, idesc,
-                                                !(kb == 0 && i == 0));
-                            }
-                        }
-                        ptx::mma_commit(&aempty[buf]);
+                    for (int i = 0; i < 16; ++i) {
+                        const int kk = 16 * i;
+                        const uint64_t bd =
+                            dst + (uint64_t)(((kk >> 6) * kChunkBytes + (kk & 63) * 2) >> 4);
+                        ptx::mma_f16_ts(acc, a_buf + 8 * i, bd, idesc, !(first && i == 0));
                     }
-                    if (!ok) break;
+                    ptx::mma_commit(&aempty[X]);
                     ptx::mma_commit(&empty[s]);
                 }
-                if (!ok) break;
-                ptx::mma_commit(&accfull[ab]);
+                __syncwarp();
+                first = false;
+                ++nx;
             }
-            if (!ok) {
-                set_status(a.status, DS4G_ERR_TIMEOUT);
-                *abort_flag = 1;
-            }
-            // every MMA issued by this thread is complete before the CTA
-            // frees its tensor memory
-            ptx::mma_commit(&drain);
-            ptx::mbar_wait(&drain, 0, a.wait_ns);
+            if (!ok) break;
+            if (lane == 0) ptx::mma_commit(&accfull);
+            __syncwarp();
         }
-    } else if (warp >= 2 + kDequantWarps) {
+        if (!ok && lane == 0) {
+            set_status(a.status, DS4G_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        // every MMA issued by this thread is complete before the CTA frees
+        // its tensor memory
+        if (lane == 0) {
+            ptx::mma_commit(&drain[X]);
+            ptx::mbar_wait(&drain[X], 0, a.wait_ns);
+        }
+        __syncwarp();
+    } else if (warp >= kFirstDequantWarp + kDequantWarps) {
         // ---------------- down epilogue warps (MODE 1) ----------------
         const int row = 32 * (warp & 3) + lane;
         const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
@@ -439,29 +606,34 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
             const int tile = it / a.m_tiles, mt = it % a.m_tiles;
             const int row0 = a.tiles[4 * tile + 1], nlen = a.tiles[4 * tile + 2];
-            const int ab = ic & 1;
-            ok = wait_bar(&accfull[ab], (ic >> 1) & 1, a.wait_ns, abort_flag);
+            ok = wait_bar(&accfull, ic & 1, a.wait_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
+            // accumulator X holds the item's K steps of stage parity X; with a
+            // single K step only one of them was written
+            const int sc0 = ic * KB;
+            const bool use0 = KB > 1 || (sc0 & 1) == 0, use1 = KB > 1 || (sc0 & 1) == 1;
             const int m = mt * kBM + row;
-            const uint32_t acc = tmem + lane_base + kAccCol + 128u * ab;
+            const uint32_t acc = tmem + lane_base + kAccCol;
             for (int c = 0; 8 * c < nlen; ++c) {
-                float o[8];
-                ptx::tmem_ld8(acc + 8 * c, o);
+                float o0[8], o1[8];
+                ptx::tmem_ld8(acc + 8 * c, o0);
+                ptx::tmem_ld8(acc + 128 + 8 * c, o1);
                 ptx::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int t = 8 * c + j;
                     if (t < nlen) {
                         const int pos = row0 + t;
-                        a.yslot[(size_t)pos * a.H + m] = __ldg(a.wseg + pos) * o[j];
+                        const float o = (use0 ? o0[j] : 0.0f) + (use1 ? o1[j] : 0.0f);
+                        a.yslot[(size_t)pos * a.H + m] = __ldg(a.wseg + pos) * o;
                     }
                 }
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&accempty[ab]);
+            if (lane == 0) ptx::mbar_arrive(&accempty);
         }
         if (!ok) {
             if (lane == 0) set_status(a.status, DS4G_ERR_TIMEOUT);
@@ -469,86 +641,9 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         }
     } else {
         // ---------------- dequantizers / gate-up epilogue ----------------
-        const int dw = warp - 2;                 // 0..7
-        const int wg = dw >> 2;                  // warpgroup: matrix (gate/up) or half
-        const int quarter = warp & 3;            // tensor-memory lane quarter
-        const int row = 32 * quarter + lane;
-        const uint32_t lane_base = (uint32_t)(32 * quarter) << 16;
-        int sc = 0, fc = 0, ic = 0;
-        bool ok = true;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
-            const int tile = it / a.m_tiles, mt = it % a.m_tiles;
-            const int row0 = a.tiles[4 * tile + 1], nlen = a.tiles[4 * tile + 2];
-            for (int kb = 0; ok && kb < KB; ++kb, ++sc) {
-                const int s = sc % kStages;
-                ok = wait_bar(&full[s], (sc / kStages) & 1, a.wait_ns, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                const uint8_t *aq = smem + (size_t)s * kStageBytes + kBBytes +
-                                    (MODE == 0 ? wg * kAqBytes : 0) + row * (kWinWords * 4);
-                uint32_t win[24];
-#pragma unroll
-                for (int v = 0; v < 6; ++v) {
-                    const uint4 q = reinterpret_cast<const uint4 *>(aq)[v];
-                    win[4 * v] = q.x;
-                    win[4 * v + 1] = q.y;
-                    win[4 * v + 2] = q.z;
-                    win[4 * v + 3] = q.w;
-                }
-                const int sh = kb & 3;       // (84 * kb) mod 16, in words (Q2_K)
-                const int boff = (kBlockBytes * kb) & 15;   // block start in the window, bytes
-                for (int h = 0; h < kFills; ++h, ++fc) {
-                    const int buf = fc & 1;
-                    if (fc >= 2) {
-                        ok = wait_bar(&aempty[buf], ((fc >> 1) - 1) & 1, a.wait_ns, abort_flag);
-                        ok = __all_sync(0xffffffffu, ok);
-                        if (!ok) break;
-                        ptx::tc_fence_after();
-                    }
-                    const uint32_t taddr = tmem + lane_base + (uint32_t)buf * 128u + 64u * wg;
-                    if (FMT == DS4G_FMT_Q2K)
-                        dequant_store_sh(win, sh, MODE == 0 ? h : wg, taddr);
-                    else
-                        cb2_store_off(win, boff, MODE == 0 ? h : wg,
-                                      ptx::smem_addr(cbrep) + (uint32_t)(lane & 15) * 8, taddr);
-                    ptx::tmem_st_wait();
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&afull[buf]);
-                }
-            }
-            if (!ok) break;
-            if (MODE == 1) continue;                 // the epilogue warps finish down items
-            // epilogue of the item
-            ok = wait_bar(&accfull[0], ic & 1, a.wait_ns, abort_flag);
-            ok = __all_sync(0xffffffffu, ok);
-            if (!ok) break;
-            ptx::tc_fence_after();
-            const int chunks = (nlen + 7) / 8;
-            for (int c = wg; c < chunks; c += 2) {
-                if (MODE == 0) {
-                    float g[8], u[8];
-                    ptx::tmem_ld8(tmem + lane_base + kAccCol + 8 * c, g);
-                    ptx::tmem_ld8(tmem + lane_base + kAccCol + 128 + 8 * c, u);
-                    ptx::tmem_ld_wait();
-                    const int n = mt * kBM + row;
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        const int t = 8 * c + j;
-                        if (t < nlen)
-                            a.hp[(size_t)(row0 + t) * a.I_pad + (FMT == DS4G_FMT_Q2K ? perm4(n) : n)] =
-                                __float2half_rn(silu_mul(g[j], u[j]));
-                    }
-                }
-            }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&accempty[0]);
-        }
-        if (!ok) {
-            if (lane == 0) set_status(a.status, DS4G_ERR_TIMEOUT);
-            *abort_flag = 1;
-        }
+        const TcCta cta{smem, full, empty, afull, aempty, &accfull, &accempty, tmem,
+                        ptx::smem_addr(cbrep), abort_flag, n_items, KB};
+        DequantRole<MODE, FMT>(a, cta, warp, lane, (warp - kFirstDequantWarp) >> 2).run();
     }
 
     __syncthreads();
@@ -569,14 +664,15 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
 // Token tiles of every active segment and the activation gather:
 //   tiles[j] = (expert, first segment row, rows <= kNT, 0), heaviest expert
 //   segments are not reordered; *n_tiles = count; wseg[p] = wts[perm[p]];
-//   xseg[p, :] = fp16(x[perm[p] / k, :]), in the (0, 2, 1, 3) order per 4
-//   for Q2_K (permute4), in natural order for the codebook format.
+//   xseg[p, :] = fp16(x[perm[p] / k, :]), for Q2_K with element 16b + l of
+//   every aligned group of 32 at position 2l + b (perm32), in natural order
+//   for the codebook format.  One thread writes 16 consecutive positions.
 __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict__ x, int H, int k,
                                                       int A, const int32_t *__restrict__ perm,
                                                       const int32_t *counts,
                                                       const int32_t *offsets, int E,
                                                       __half *__restrict__ xseg, int32_t *tiles,
-                                                      int32_t *n_tiles, int permute4,
+                                                      int32_t *n_tiles, int permute32,
                                                       const float *__restrict__ wts,
                                                       float *__restrict__ wseg)
 {
@@ -609,31 +705,46 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
             }
         }
     }
-    const int per_row = H / 8;
+    const int per_row = H / 16;
     const int64_t total = (int64_t)A * per_row;
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
          i += (int64_t)gridDim.x * blockDim.x) {
         const int p = (int)(i / per_row), c = (int)(i % per_row);
         const int t = perm[p] / k;
-        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * H) + c);
-        const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-        __half hv[8];
+        const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+        // Q2_K: positions 16c .. 16c+15 interleave elements 32(c/2) + 8(c%2) + l'
+        // and the same + 16 (l' = 0..7); codebook: elements 16c .. 16c+15
+        const int e0 = permute32 ? 32 * (c >> 1) + 8 * (c & 1) : 16 * c;
+        const int e1 = permute32 ? e0 + 16 : e0 + 8;
+        const uint4 ra = __ldg(src + e0 / 8), rb = __ldg(src + e1 / 8);
+        const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+        __half ha[8], hb[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            hv[2 * j] = __float2half_rn(bf16_bits(wv[j] & 0xFFFFu));
-            hv[2 * j + 1] = __float2half_rn(bf16_bits(wv[j] >> 16));
+            ha[2 * j] = __float2half_rn(bf16_bits(wa[j] & 0xFFFFu));
+            ha[2 * j + 1] = __float2half_rn(bf16_bits(wa[j] >> 16));
+            hb[2 * j] = __float2half_rn(bf16_bits(wb[j] & 0xFFFFu));
+            hb[2 * j + 1] = __float2half_rn(bf16_bits(wb[j] >> 16));
         }
-        // Q2_K: (0, 2, 1, 3) inside each group of 4; codebook format: natural
-        const __half2 o0 = permute4 ? __halves2half2(hv[0], hv[2]) : __halves2half2(hv[0], hv[1]);
-        const __half2 o1 = permute4 ? __halves2half2(hv[1], hv[3]) : __halves2half2(hv[2], hv[3]);
-        const __half2 o2 = permute4 ? __halves2half2(hv[4], hv[6]) : __halves2half2(hv[4], hv[5]);
-        const __half2 o3 = permute4 ? __halves2half2(hv[5], hv[7]) : __halves2half2(hv[6], hv[7]);
-        uint4 out;
-        out.x = *reinterpret_cast<const uint32_t *>(&o0);
-        out.y = *reinterpret_cast<const uint32_t *>(&o1);
-        out.z = *reinterpret_cast<const uint32_t *>(&o2);
-        out.w = *reinterpret_cast<const uint32_t *>(&o3);
-        reinterpret_cast<uint4 *>(xseg + (size_t)p * H)[c] = out;
+        uint32_t o[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            __half2 lo, hi;
+            if (permute32) {
+                lo = __halves2half2(ha[2 * j], hb[2 * j]);
+                hi = __halves2half2(ha[2 * j + 1], hb[2 * j + 1]);
+                o[2 * j] = *reinterpret_cast<const uint32_t *>(&lo);
+                o[2 * j + 1] = *reinterpret_cast<const uint32_t *>(&hi);
+            } else {
+                lo = __halves2half2(ha[2 * j], ha[2 * j + 1]);
+                hi = __halves2half2(hb[2 * j], hb[2 * j + 1]);
+                o[j] = *reinterpret_cast<const uint32_t *>(&lo);
+                o[4 + j] = *reinterpret_cast<const uint32_t *>(&hi);
+            }
+        }
+        uint4 *dst = reinterpret_cast<uint4 *>(xseg + (size_t)p * H + 16 * c);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
     }
 }
 
