@@ -145,7 +145,7 @@ constexpr int kLaunchBound = 512;
 // named barriers: 1 = consumers only; 2, 3 = reduction buffer 0/1 filled
 // (consumers arrive, epilogue warp waits); 4, 5 = buffer 0/1 released
 // (epilogue warp arrives, consumers wait)
-constexpr int kBarConsumers = 1, kBarJobFull = 2, kBarJobEmpty = 4;
+constexpr int kBarConsumers = 1, kBarJobFull = 2, kBarJobEmpty = 4, kBarConvert = 6;
 constexpr int kJobThreads = (kConsumers + 1) * 32;
 constexpr int kDownRows = 32;            // rows of H per down item (two MMA tiles)
 constexpr int kMaxDownPerStage = 8;
@@ -171,6 +171,7 @@ struct DecArgs {
     const uint16_t *x;     // [T][H] bf16
     const __half *xp;      // [T][H] converted by decode_pre_kernel (x_smem == 0)
     const float *xs;       // [T][H/16]
+    const int32_t *texp;   // [T] token exponents written by decode_pre_kernel (x_smem == 0)
     __half *hp;            // [A][I_pad]
     float *hs;             // [A][I_pad/16]
     float *y;              // [T][H]
@@ -552,19 +553,21 @@ __device__ void route_warp(const DecArgs &a, RouteSmem &r)
     }
 }
 
-// x (bf16) -> fp16 in the (0, 2, 1, 3) order per 4, plus fp32 sums of 16,
-// for `n_groups` groups of 4 starting at group g0 (all threads of the CTA or
-// grid stride by `stride`).
+// x (bf16) -> fp16 x * 2^-e_t in the (0, 2, 1, 3) order per 4, plus fp32
+// sums of 16, for groups of 4 g0, g0 + stride, ... below n_groups (all
+// threads of the CTA or a grid stride).  `texp`: e_t of each token (H
+// elements per token).
 __device__ __forceinline__ void convert_x(const uint16_t *x, __half *xp, float *xs, size_t g0,
-                                          size_t n_groups, size_t stride)
+                                          size_t n_groups, size_t stride, int H, const int32_t *texp)
 {
     // one group of 4 per lane; lanes 4j..4j+3 of a warp form a sub-block
     for (size_t g = g0; g < n_groups; g += stride) {
+        const float sx = exp2i(-texp[(4 * g) / H]);
         const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(x) + g);
-        const __half h0 = __float2half_rn(bf16_bits(raw.x & 0xFFFFu));
-        const __half h1 = __float2half_rn(bf16_bits(raw.x >> 16));
-        const __half h2 = __float2half_rn(bf16_bits(raw.y & 0xFFFFu));
-        const __half h3 = __float2half_rn(bf16_bits(raw.y >> 16));
+        const __half h0 = __float2half_rn(bf16_bits(raw.x & 0xFFFFu) * sx);
+        const __half h1 = __float2half_rn(bf16_bits(raw.x >> 16) * sx);
+        const __half h2 = __float2half_rn(bf16_bits(raw.y & 0xFFFFu) * sx);
+        const __half h3 = __float2half_rn(bf16_bits(raw.y >> 16) * sx);
         __half2 *o = reinterpret_cast<__half2 *>(xp + 4 * g);
         o[0] = __halves2half2(h0, h2);
         o[1] = __halves2half2(h1, h3);
@@ -575,19 +578,80 @@ __device__ __forceinline__ void convert_x(const uint16_t *x, __half *xp, float *
     }
 }
 
-// Resets the status word and the decode kernel's counters; converts the
-// activations when they do not fit in the decode kernel's shared memory.
+// Largest finite |x| of token t's H elements over the threads of a block
+// (every thread gets the result; `red` is 32 floats of shared memory).
+__device__ __forceinline__ float token_max_block(const uint16_t *x, int t, int H, float *red)
+{
+    const uint32_t *row = reinterpret_cast<const uint32_t *>(x + (size_t)t * H);
+    float m = 0.0f;
+    for (int i = threadIdx.x; i < H / 2; i += blockDim.x) {
+        const uint32_t w = __ldg(row + i);
+        m = fmaxf(m, fmaxf(bf16_abs_finite(w & 0xFFFFu), bf16_abs_finite(w >> 16)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    float r = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r = fmaxf(r, red[w]);
+    return r;
+}
+
+// Resets the status word and the decode kernel's counters; when the
+// activations do not fit in the decode kernel's shared memory, computes
+// every token's exponent (texp) and converts the activations (one block per
+// token at a time).
 __global__ void __launch_bounds__(256) decode_pre_kernel(int32_t *status, int32_t *sync, int n_sync,
                                                          const uint16_t *x, __half *xp, float *xs,
-                                                         size_t n_groups)
+                                                         int T, int H, int32_t *texp)
 {
+    __shared__ float red[32];
+    __shared__ int32_t s_e[1];
     ptx::grid_dep_launch();
     if (blockIdx.x == 0) {
         if (threadIdx.x == 0) *status = DS4G_OK;
         for (int i = threadIdx.x; i < n_sync; i += blockDim.x) sync[i] = 0;
     }
-    if (x) convert_x(x, xp, xs, (size_t)blockIdx.x * blockDim.x + threadIdx.x, n_groups,
-                     (size_t)gridDim.x * blockDim.x);
+    if (!x) return;
+    for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        const float m = token_max_block(x, t, H, red);
+        if (threadIdx.x == 0) {
+            s_e[0] = token_exponent(m);
+            texp[t] = s_e[0];
+        }
+        __syncthreads();
+        const size_t q = (size_t)H / 4;
+        convert_x(x + (size_t)t * H, xp + (size_t)t * H, xs + (size_t)t * (H / 16), threadIdx.x, q,
+                  blockDim.x, H, s_e);
+        __syncthreads();
+    }
+}
+
+// Exponents of the T tokens (s_e) from x, by `nthr` threads of the CTA with
+// index i (consecutive within each warp); `sync` separates the phases (a
+// named barrier over those threads, or __syncthreads).  s_m: T ints of
+// shared memory for the maxima (float bits, monotone for non-negative values).
+template <typename Sync>
+__device__ __forceinline__ void token_exponents_cta(const uint16_t *x, int T, int H, int i,
+                                                    int nthr, int *s_m, int32_t *s_e, Sync sync)
+{
+    for (int t = i; t < T; t += nthr) s_m[t] = 0;
+    sync();
+    for (int t = 0; t < T; ++t) {
+        const uint32_t *row = reinterpret_cast<const uint32_t *>(x + (size_t)t * H);
+        float m = 0.0f;
+        for (int j = i; j < H / 2; j += nthr) {
+            const uint32_t w = __ldg(row + j);
+            m = fmaxf(m, fmaxf(bf16_abs_finite(w & 0xFFFFu), bf16_abs_finite(w >> 16)));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if ((i & 31) == 0 && m > 0.0f) atomicMax(s_m + t, __float_as_int(m));
+    }
+    sync();
+    for (int t = i; t < T; t += nthr) s_e[t] = token_exponent(__int_as_float(s_m[t]));
+    sync();
 }
 
 template <int NT>
@@ -601,6 +665,8 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
     __shared__ __align__(16) __half zero[16];
     __shared__ int s_pabort, s_cabort, s_consumed, s_issued;
     __shared__ Job jobs[2];
+    __shared__ int32_t s_e[kDecodeMaxT];     // token exponents
+    __shared__ int s_m[kDecodeMaxT];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = lane >> 2, c = lane & 3;
     const uint32_t gu_tile = (uint32_t)(kTileM * a.gu_row);
@@ -638,17 +704,27 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
             route_warp(a, rs);
         } else if (a.x_smem) {
             const int t2 = tid < kProducerWarp * 32 ? tid : tid - 32;
-            convert_x(a.x, x_s, xs_s, t2, (size_t)a.T * (a.H / 4), blockDim.x - 32);
+            const int nthr = blockDim.x - 32;
+            token_exponents_cta(a.x, a.T, a.H, t2, nthr, s_m, s_e,
+                                [&] { named_sync(kBarConvert, nthr); });
+            convert_x(a.x, x_s, xs_s, t2, (size_t)a.T * (a.H / 4), nthr, a.H, s_e);
         }
         __syncthreads();
     } else {
-        if (a.x_smem) convert_x(a.x, x_s, xs_s, tid, (size_t)a.T * (a.H / 4), blockDim.x);
+        if (a.x_smem) {
+            token_exponents_cta(a.x, a.T, a.H, tid, blockDim.x, s_m, s_e, [] { __syncthreads(); });
+            convert_x(a.x, x_s, xs_s, tid, (size_t)a.T * (a.H / 4), blockDim.x, a.H, s_e);
+        }
         route_into_smem(a, rs);   // ends with __syncthreads
     }
 
-    // the counters are reset (and, without x_smem, the activations converted)
-    // by the kernel ahead of this one
+    // the counters are reset (and, without x_smem, the activations converted
+    // and the token exponents written) by the kernel ahead of this one
     ptx::grid_dep_wait();
+    if (!a.x_smem) {
+        if (tid < a.T) s_e[tid] = a.texp[tid];
+        __syncthreads();
+    }
 
     const int n_act = rs.n_act;
     const int tiles = a.I / kTileM;
@@ -928,7 +1004,8 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                             const int asg = t * a.k + sl;
                             acc += rs.wts[asg] * obuf[(size_t)rs.slot[asg] * kDownRows + row];
                         }
-                        a.y[(size_t)t * a.H + (size_t)it * kDownRows + row] = acc;
+                        a.y[(size_t)t * a.H + (size_t)it * kDownRows + row] =
+                            acc * exp2i(2 * s_e[t] + kHExpOffset);
                     }
                 }
             }
@@ -963,8 +1040,12 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                         const float v = rbuf[((size_t)w * NT + j) * kTileM + row];
                         if ((w >> 1) & 1) uu += v; else g += v;
                     }
-                    const __half hv = __float2half_rn(silu_mul(g, uu));
                     const int pos = jb.seg0 + jb.c0 + j;
+                    // undo the token's activation scale; h leaves scaled by 2^-f
+                    const int e = s_e[rs.perm[pos] / a.k];
+                    const float sx = exp2i(e);
+                    const __half hv = __float2half_rn(silu_mul(g * sx, uu * sx) *
+                                                      exp2i(-(2 * e + kHExpOffset)));
                     const int n = jb.mt * kTileM + row;
                     float hsum = valid ? __half2float(hv) : 0.0f;
 #pragma unroll
@@ -1059,6 +1140,7 @@ struct Args {
     const uint16_t *x;
     const __half *xp;               // [T][H] fp16 (4-group permuted)
     const float *xs;                // [T][H/16]
+    const int32_t *texp;            // [T] token exponents (decode_pre_kernel)
     __half *hp;                     // [A][I_pad]
     float *hs;                      // [A][I_pad/16]
     float *yslot;                   // [A][H]
@@ -1182,6 +1264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ RouteSmem rs;
+    __shared__ int32_t s_e[kDecodeMaxT];     // token exponents
     __shared__ Chunk chunks[kMaxAssign];
     __shared__ int s_nchunks;
     __shared__ __align__(8) float2 sc_lut[256];
@@ -1260,7 +1343,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
-    ptx::grid_dep_wait();        // counters reset, activations converted
+    ptx::grid_dep_wait();        // counters reset, activations converted, exponents written
+    if (threadIdx.x < a.T) s_e[threadIdx.x] = a.texp[threadIdx.x];
+    __syncthreads();
     const uint32_t tmem = s_tmem;
 
     const int n_chunks = s_nchunks;
@@ -1581,7 +1666,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (wg == 0) {
                         const int n = mt * kBM + wrow;
                         for (int t = 0; t < c.nt; ++t) {
-                            const __half hv = __float2half_rn(silu_mul(acc[t], xch[t][wrow]));
+                            // undo the token's activation scale; h leaves scaled by 2^-f
+                            const int e = s_e[rs.perm[c.pos0 + t] / a.k];
+                            const float sx = exp2i(e);
+                            const __half hv = __float2half_rn(
+                                silu_mul(acc[t] * sx, xch[t][wrow] * sx) * exp2i(-(2 * e + kHExpOffset)));
                             a.hp[(size_t)(c.pos0 + t) * a.I_pad + perm4(n)] = hv;
                             hsm[t][wrow] = __half2float(hv);
                         }
@@ -1606,7 +1695,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int m = mt * kBM + wrow;
                     for (int t = 0; t < c.nt; ++t) {
                         const int pos = c.pos0 + t;
-                        a.yslot[(size_t)pos * a.H + m] = rs.wts[rs.perm[pos]] * (acc[t] + xch[t][wrow]);
+                        const float sh = exp2i(2 * s_e[rs.perm[pos] / a.k] + kHExpOffset);
+                        a.yslot[(size_t)pos * a.H + m] =
+                            rs.wts[rs.perm[pos]] * ((acc[t] + xch[t][wrow]) * sh);
                     }
                     __threadfence();
                     named_sync(kBarWG0, 128);
@@ -1741,6 +1832,7 @@ cudaError_t launch_decode_tc(const LayerArgs &la, const DecodeBufs &db, const De
     a.x = la.x;
     a.xp = db.xp;
     a.xs = db.xs;
+    a.texp = db.texp;
     a.hp = db.hp;
     a.hs = db.hs;
     a.yslot = la.yslot;
@@ -1765,11 +1857,9 @@ cudaError_t launch_decode_tc(const LayerArgs &la, const DecodeBufs &db, const De
 
     // counters and status reset, activations to fp16 (the kernel copies them
     // into its pipeline by TMA)
-    const size_t groups = (size_t)a.T * (a.H / 4);
-    const int pre_grid = (int)std::min<size_t>((groups + 255) / 256, (size_t)dev.sm_count * 4);
-    decode_pre_kernel<<<pre_grid, 256, 0, s>>>(db.status, db.sync, decode_sync_words(la.E, la.H),
-                                               la.x, const_cast<__half *>(db.xp),
-                                               const_cast<float *>(db.xs), groups);
+    decode_pre_kernel<<<a.T, 256, 0, s>>>(db.status, db.sync, decode_sync_words(la.E, la.H), la.x,
+                                          const_cast<__half *>(db.xp), const_cast<float *>(db.xs),
+                                          a.T, a.H, db.texp);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (events && (e = record_phase(events[1], s)) != cudaSuccess) return e;
 
@@ -1842,6 +1932,7 @@ cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const 
     a.x = la.x;
     a.xp = db.xp;
     a.xs = db.xs;
+    a.texp = db.texp;
     a.hp = db.hp;
     a.hs = db.hs;
     a.y = la.y;
@@ -1858,12 +1949,11 @@ cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const 
     a.x_smem = xb <= kXStageMax ? 1 : 0;
 
     // counters and status reset; activation conversion when it does not fit
-    const size_t groups = (size_t)a.T * (a.H / 4);
-    const int pre_grid = a.x_smem ? 1 : (int)std::min<size_t>((groups + 255) / 256, (size_t)dev.sm_count * 4);
+    const int pre_grid = a.x_smem ? 1 : a.T;
     decode_pre_kernel<<<pre_grid, 256, 0, s>>>(db.status, db.sync, decode_sync_words(a.E, a.H),
                                                a.x_smem ? nullptr : la.x,
                                                const_cast<__half *>(db.xp),
-                                               const_cast<float *>(db.xs), groups);
+                                               const_cast<float *>(db.xs), a.T, a.H, db.texp);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (events && (e = record_phase(events[1], s)) != cudaSuccess) return e;

@@ -125,6 +125,8 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     q.xseg = take(A * q.H * 2);
     q.tiles = take((size_t)tc_max_tiles(q.E, q.A) * 16);
     q.wseg = take(A * 4);
+    q.texp = take((size_t)T * 4);
+    q.eseg = take(A * 4);
     q.x_stage = take((size_t)T * q.H * 2);
     q.l_stage = take((size_t)T * q.E * 4);
     q.y_stage = take((size_t)T * q.H * 4);
@@ -220,7 +222,8 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     a.y = y;
     TcBufs tb{reinterpret_cast<__half *>(ws + p.xseg), reinterpret_cast<__half *>(ws + p.hp),
               reinterpret_cast<int32_t *>(ws + p.tiles), meta + kMetaTiles, status,
-              reinterpret_cast<float *>(ws + p.wseg)};
+              reinterpret_cast<float *>(ws + p.wseg), reinterpret_cast<int32_t *>(ws + p.texp),
+              reinterpret_cast<int32_t *>(ws + p.eseg)};
     // the activation gather of the tensor-core path belongs to the routing phase
     if (path == Path::kTensorCore && (e = launch_tc_prep(a, tb, dev, s)) != cudaSuccess)
         return from_cuda(e);
@@ -230,7 +233,8 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     if (decode) {
         DecodeBufs b{logits, ids, d->score, xp, xs, reinterpret_cast<__half *>(ws + p.hp),
                      reinterpret_cast<float *>(ws + p.hs), status, sync,
-                     reinterpret_cast<float *>(ws + p.gpart)};
+                     reinterpret_cast<float *>(ws + p.gpart),
+                     reinterpret_cast<int32_t *>(ws + p.texp)};
         return from_cuda(launch_decode_path(a, b, dev, s, pe.on ? pe.ev : nullptr, wait_ns,
                                             stall));
     }

@@ -38,6 +38,8 @@ struct Plan {
     size_t xseg;            // [A x H] fp16: activations in segment order (tensor-core path)
     size_t tiles;           // [tc_max_tiles x 4] int32 token tiles (tensor-core path)
     size_t wseg;            // [A] fp32 routing weight per segment row (tensor-core path)
+    size_t texp;            // [T] int32 activation exponent of each token (see token_exponent)
+    size_t eseg;            // [A] int32 activation exponent of each segment row (tensor-core path)
     size_t x_stage;         // [T x H] bf16 (host entry point)
     size_t l_stage;         // [T x E] fp32 (host entry point)
     size_t y_stage;         // [T x H] fp32 (host entry point)
@@ -127,6 +129,7 @@ struct DecodeBufs {
     int32_t *status;
     int32_t *sync;          // [decode_sync_words] claim and completion counters
     float *gpart;           // K-split partial sums of the tensor-core decode kernel
+    int32_t *texp;          // [T] token exponents (written when the activations are converted ahead)
 };
 constexpr int kSyncWords = 4;
 constexpr int kDecodeMaxPairs = 1024;
@@ -154,6 +157,8 @@ struct TcBufs {
     int32_t *n_tiles;
     int32_t *status;
     float *wseg;           // [A] routing weight of each segment row
+    int32_t *texp;         // [T] activation exponent of each token
+    int32_t *eseg;         // [A] activation exponent of each segment row
 };
 bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d);
 int32_t tc_max_tiles(int32_t E, int32_t A);
@@ -164,7 +169,7 @@ cudaError_t launch_tc_prep(const LayerArgs &a, const TcBufs &b, const DeviceInfo
 cudaError_t launch_tc_path(const LayerArgs &a, const TcBufs &b, const DeviceInfo &dev,
                            cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns,
                            bool stall);
-constexpr int32_t kTcPathLaunches = 4;  // prep, gate/up, down, combine
+constexpr int32_t kTcPathLaunches = 5;  // token exponents, prep, gate/up, down, combine
 
 // Bounded device waits: default limit, and the short limit used with
 // DS4G_DEBUG_STALL.
@@ -188,5 +193,42 @@ __device__ __forceinline__ float silu_mul(float g, float u)
 {
     return g / (1.0f + expf(-g)) * u;
 }
+
+// ---------------------------------------------------------------------------
+// Per-token power-of-two scaling of the fp16 operands.  The tensor-core and
+// decode kernels multiply in fp16, whose range (6.1e-5 .. 65504 at full
+// precision) is narrower than bf16's.  Token t's activations enter as
+// x * 2^-e_t with e_t chosen so that the largest finite |x| of the token lands
+// in [2^10, 2^11); the gate and up accumulators are multiplied back by 2^e_t
+// in fp32, SiLU(g)*u is formed in fp32 and stored as h * 2^-f_t with
+// f_t = 2 e_t + 14 (h grows like x^2), and the down projection's result is
+// multiplied back by 2^f_t.  Every scaling is by a power of two, so it is
+// exact wherever no value leaves the normal range.  e_t is clamped to
+// [-40, 40]; a token without a nonzero finite value gets 0.
+// ---------------------------------------------------------------------------
+constexpr int kExpTarget = 10;
+constexpr int kExpMin = -40, kExpMax = 40;
+constexpr int kHExpOffset = 14;
+
+// e_t from the token's largest finite |x| (non-negative, finite).
+__device__ __forceinline__ int token_exponent(float max_abs)
+{
+    if (!(max_abs > 0.0f)) return 0;                 // no nonzero finite value
+    const int e = ((int)((__float_as_uint(max_abs) >> 23) & 0xFF) - 127) - kExpTarget;
+    return e < kExpMin ? kExpMin : (e > kExpMax ? kExpMax : e);
+}
+
+// 2^e as a float for -126 <= e <= 127.
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(e + 127) << 23); }
+
+// |x| of a bf16 value as float when finite, else 0 (for token maxima).
+__device__ __forceinline__ float bf16_abs_finite(uint32_t bits16)
+{
+    const uint32_t a = (bits16 & 0x7FFFu) << 16;
+    return a < 0x7F800000u ? __uint_as_float(a) : 0.0f;
+}
+
+// texp[t] = e_t for t < T (one warp per token; x [T x H] bf16).
+cudaError_t launch_token_exponents(const uint16_t *x, int T, int H, int32_t *texp, cudaStream_t s);
 
 }  // namespace ds4g

@@ -91,6 +91,7 @@ struct TcArgs {
     const int32_t *tiles;       // [n][4]: expert, first segment row, rows, 0
     const int32_t *n_tiles;
     const float *wseg;          // routing weight of each segment row
+    const int32_t *eseg;        // activation exponent of each segment row
     __half *hp;                 // gate/up output [A][I_pad] (permuted order)
     float *yslot;               // down output [A][H]
     const int8_t *codebook;     // [256 x 8] int8 (codebook format)
@@ -398,9 +399,14 @@ struct DequantRole {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int t = 8 * ch + j;
-                    if (t < nlen)
+                    if (t < nlen) {
+                        // undo the row's activation scale, store h scaled by 2^-f
+                        const int e = __ldg(a.eseg + row0 + t);
+                        const float sx = exp2i(e);
+                        const float h = silu_mul(g[j] * sx, u[j] * sx);
                         a.hp[(size_t)(row0 + t) * a.I_pad + col] =
-                            __float2half_rn(silu_mul(g[j], u[j]));
+                            __float2half_rn(h * exp2i(-(2 * e + kHExpOffset)));
+                    }
                 }
             }
             ptx::tc_fence_before();
@@ -627,7 +633,8 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                     if (t < nlen) {
                         const int pos = row0 + t;
                         const float o = (use0 ? o0[j] : 0.0f) + (use1 ? o1[j] : 0.0f);
-                        a.yslot[(size_t)pos * a.H + m] = __ldg(a.wseg + pos) * o;
+                        const float sh = exp2i(2 * __ldg(a.eseg + pos) + kHExpOffset);
+                        a.yslot[(size_t)pos * a.H + m] = __ldg(a.wseg + pos) * (o * sh);
                     }
                 }
             }
@@ -661,12 +668,34 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
     if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
 }
 
+// Token exponents: texp[t] = e_t (see token_exponent), one warp per token.
+__global__ void __launch_bounds__(256) token_exp_kernel(const uint16_t *__restrict__ x, int T, int H,
+                                                        int32_t *__restrict__ texp)
+{
+    const int t = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const uint4 *row = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
+    float m = 0.0f;
+    for (int i = lane; i < H / 8; i += 32) {
+        const uint4 r = __ldg(row + i);
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            m = fmaxf(m, fmaxf(bf16_abs_finite(w[j] & 0xFFFFu), bf16_abs_finite(w[j] >> 16)));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) texp[t] = token_exponent(m);
+}
+
 // Token tiles of every active segment and the activation gather:
 //   tiles[j] = (expert, first segment row, rows <= kNT, 0), heaviest expert
 //   segments are not reordered; *n_tiles = count; wseg[p] = wts[perm[p]];
-//   xseg[p, :] = fp16(x[perm[p] / k, :]), for Q2_K with element 16b + l of
-//   every aligned group of 32 at position 2l + b (perm32), in natural order
-//   for the codebook format.  One thread writes 16 consecutive positions.
+//   eseg[p] = texp[perm[p] / k];
+//   xseg[p, :] = fp16(x[perm[p] / k, :] * 2^-eseg[p]), for Q2_K with element
+//   16b + l of every aligned group of 32 at position 2l + b (perm32), in
+//   natural order for the codebook format.  One thread writes 16 consecutive
+//   positions.
 __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict__ x, int H, int k,
                                                       int A, const int32_t *__restrict__ perm,
                                                       const int32_t *counts,
@@ -674,10 +703,14 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
                                                       __half *__restrict__ xseg, int32_t *tiles,
                                                       int32_t *n_tiles, int permute32,
                                                       const float *__restrict__ wts,
-                                                      float *__restrict__ wseg)
+                                                      float *__restrict__ wseg,
+                                                      const int32_t *__restrict__ texp,
+                                                      int32_t *__restrict__ eseg)
 {
-    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < A; p += gridDim.x * blockDim.x)
+    for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < A; p += gridDim.x * blockDim.x) {
         wseg[p] = wts[perm[p]];
+        eseg[p] = texp[perm[p] / k];
+    }
     if (blockIdx.x == 0) {
         __shared__ int s_nt[DS4G_MAX_EXPERTS];
         __shared__ int s_base[DS4G_MAX_EXPERTS + 1];
@@ -711,6 +744,7 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
          i += (int64_t)gridDim.x * blockDim.x) {
         const int p = (int)(i / per_row), c = (int)(i % per_row);
         const int t = perm[p] / k;
+        const float sx = exp2i(-__ldg(texp + t));
         const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * H);
         // Q2_K: positions 16c .. 16c+15 interleave elements 32(c/2) + 8(c%2) + l'
         // and the same + 16 (l' = 0..7); codebook: elements 16c .. 16c+15
@@ -721,10 +755,10 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
         __half ha[8], hb[8];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            ha[2 * j] = __float2half_rn(bf16_bits(wa[j] & 0xFFFFu));
-            ha[2 * j + 1] = __float2half_rn(bf16_bits(wa[j] >> 16));
-            hb[2 * j] = __float2half_rn(bf16_bits(wb[j] & 0xFFFFu));
-            hb[2 * j + 1] = __float2half_rn(bf16_bits(wb[j] >> 16));
+            ha[2 * j] = __float2half_rn(bf16_bits(wa[j] & 0xFFFFu) * sx);
+            ha[2 * j + 1] = __float2half_rn(bf16_bits(wa[j] >> 16) * sx);
+            hb[2 * j] = __float2half_rn(bf16_bits(wb[j] & 0xFFFFu) * sx);
+            hb[2 * j + 1] = __float2half_rn(bf16_bits(wb[j] >> 16) * sx);
         }
         uint32_t o[8];
 #pragma unroll
@@ -833,13 +867,22 @@ bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d)
 
 int32_t tc_max_tiles(int32_t E, int32_t A) { return E + A / kNT + 1; }
 
+cudaError_t launch_token_exponents(const uint16_t *x, int T, int H, int32_t *texp, cudaStream_t s)
+{
+    token_exp_kernel<<<(T + 7) / 8, 256, 0, s>>>(x, T, H, texp);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_tc_prep(const LayerArgs &la, const TcBufs &tb, const DeviceInfo &dev,
                            cudaStream_t s)
 {
+    cudaError_t e = launch_token_exponents(la.x, la.T, la.H, tb.texp, s);
+    if (e != cudaSuccess) return e;
     const int prep_grid = dev.sm_count * 4;
     tc_prep_kernel<<<prep_grid, 256, 0, s>>>(la.x, la.H, la.k, la.A, la.perm, la.counts,
                                              la.offsets, la.E, tb.xseg, tb.tiles, tb.n_tiles,
-                                             la.format == DS4G_FMT_Q2K ? 1 : 0, la.wts, tb.wseg);
+                                             la.format == DS4G_FMT_Q2K ? 1 : 0, la.wts, tb.wseg,
+                                             tb.texp, tb.eseg);
     return cudaGetLastError();
 }
 
@@ -862,6 +905,7 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     a.tiles = tb.tiles;
     a.n_tiles = tb.n_tiles;
     a.wseg = tb.wseg;
+    a.eseg = tb.eseg;
     a.hp = tb.hp;
     a.yslot = la.yslot;
     a.status = tb.status;

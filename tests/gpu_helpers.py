@@ -75,6 +75,46 @@ def run_forward(L: D.Layer, x: np.ndarray, logits: np.ndarray):
     return y.cpu().numpy(), routing
 
 
+def oracle_tokens(orc, layer: dict, x: np.ndarray, logits: np.ndarray, tokens=None):
+    """The oracle's y for the listed tokens (all when None), computed on all
+    host cores: the oracle is re-entrant and ctypes releases the GIL, so the
+    tokens are split across threads.  Returns fp64 [n x H]."""
+    import concurrent.futures as cf
+    import os
+    T = x.shape[0]
+    tok = np.arange(T, dtype=np.int32) if tokens is None else np.asarray(tokens, dtype=np.int32)
+    n_thr = max(1, min(len(tok), os.cpu_count() or 1))
+    parts = np.array_split(tok, n_thr)
+    with cf.ThreadPoolExecutor(n_thr) as ex:
+        outs = list(ex.map(lambda tk: orc.moe_forward(layer, x, logits, tk)[0], parts))
+    return np.concatenate(outs, axis=0)
+
+
+def boundary_tokens(route: dict, k: int, T: int, n_total: int, seed: int) -> np.ndarray:
+    """Tokens that exercise every code path of a large call: the first and
+    last token of the three heaviest expert segments and the tokens on both
+    sides of each 128-token tile boundary inside them, tokens routed to
+    one-token segments, then seeded random tokens up to n_total."""
+    counts, offsets, perm = route["counts"], route["offsets"], route["perm"]
+    picks = []
+    for e in np.argsort(-counts, kind="stable")[:3]:
+        n = int(counts[e])
+        pos = {0, n - 1}
+        for b in range(128, n, 128):
+            pos.update((b - 1, b))
+        picks += [int(perm[offsets[e] + q]) // k for q in sorted(pos) if 0 <= q < n]
+    for e in np.nonzero(counts == 1)[0][:16]:
+        picks.append(int(perm[offsets[e]]) // k)
+    out = list(dict.fromkeys(picks))
+    rng = np.random.default_rng(seed)
+    for t in rng.permutation(T):
+        if len(out) >= n_total:
+            break
+        if int(t) not in out:
+            out.append(int(t))
+    return np.sort(np.array(out, dtype=np.int32))
+
+
 def check_output(y: np.ndarray, yref: np.ndarray, rel_l2=REL_L2_TOL, max_abs=MAX_ABS_TOL):
     """Per-token relative L2 <= rel_l2 and max-abs <= max_abs * max|ref|; a
     token whose reference is exactly zero must be exactly zero."""

@@ -182,13 +182,14 @@ def layer_desc(H, I, E, k, fmt=None, flags=0, align=1):
     # decode kernels (reset + fused layer): Q2_K, inter % 16 == 0, up to 32 vectors
     ((4096, 1536, 64, 6), 1, {}, 2),
     ((7168, 2048, 256, 8), 32, {}, 2),
-    # tensor-core path above 32 vectors: routing (1 launch up to 64 tokens, else 2) + 4
-    ((7168, 2048, 256, 8), 33, {}, 1 + 4),
-    ((7168, 2048, 256, 8), 65, {}, 2 + 4),
+    # tensor-core path above 32 vectors: routing (1 launch up to 64 tokens, else 2) +
+    # token exponents, prep/gather, gate/up, down, combine
+    ((7168, 2048, 256, 8), 33, {}, 1 + 5),
+    ((7168, 2048, 256, 8), 65, {}, 2 + 5),
     # rows that are not multiples of 16 bytes: GEMV kernels (routing + 3)
     ((512, 320, 8, 2), 100, {}, 2 + 3),
     # the codebook format never takes the decode kernels
-    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_CB2, align=16), 1 + 4),
+    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_CB2, align=16), 1 + 5),
     ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_CB2), 1 + 3),
     # FORCE_GEMV keeps the decode kernels where they apply and rules out the
     # tensor-core kernels elsewhere; FORCE_TC needs 16-byte rows (504-byte down rows here)
