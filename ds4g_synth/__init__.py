@@ -17,7 +17,11 @@ decode_1tok    4096   1536  64   6   1     Q2_K      softmax  1
 decode_32tok   7168   2048  256  8   32    Q2_K      sigmoid  2
 prefill_2048   7168   2048  256  8   2048  Q2_K      sigmoid  3
 codebook_512   7168   2048  256  8   512   codebook  sigmoid  4
+mixed_2048     7168   2048  256  8   2048  mixed     sigmoid  5
 =============  =====  ====  ===  ==  ====  ========  =======  ====
+
+mixed_2048 is the shipping mix of the ds4 weights (codebook-2-bit gate/up,
+Q2_K down) on the prefill layer with the prefill routing recipe.
 
 Rows are stored packed (ceil(K/256) blocks back to back) for Q2_K; the
 codebook rows (70-byte blocks) are padded to a multiple of 16 bytes so that
@@ -60,16 +64,28 @@ class Config:
     logits: int
     seed: int
     row_align: int = 1
+    down_format: Optional[int] = None      # W_down's format when it differs (mixed layers)
+
+    @property
+    def dn_format(self) -> int:
+        return self.format if self.down_format is None else self.down_format
 
     @property
     def block_bytes(self) -> int:
+        """Bytes of one W_gate / W_up super-block."""
         return 84 if self.format == FMT_Q2K else 70
 
-    def row_bytes(self, K: int, align: Optional[int] = None) -> int:
-        """Row stride: ceil(K/256) blocks, padded up to `align` bytes
-        (default: the configuration's own row alignment)."""
+    @property
+    def down_block_bytes(self) -> int:
+        return 84 if self.dn_format == FMT_Q2K else 70
+
+    def row_bytes(self, K: int, align: Optional[int] = None, fmt: Optional[int] = None) -> int:
+        """Row stride: ceil(K/256) blocks of `fmt` (default: the gate/up
+        format), padded up to `align` bytes (default: the configuration's
+        own row alignment)."""
         align = self.row_align if align is None else align
-        logical = -(-K // QK) * self.block_bytes
+        fmt = self.format if fmt is None else fmt
+        logical = -(-K // QK) * (84 if fmt == FMT_Q2K else 70)
         return -(-logical // align) * align
 
 
@@ -81,6 +97,8 @@ CONFIGS: Dict[str, Config] = {
         Config("prefill_2048", 7168, 2048, 256, 8, 2048, FMT_Q2K, SCORE_SIGMOID, LOGITS_BIASED, 3),
         Config("codebook_512", 7168, 2048, 256, 8, 512, FMT_CB2, SCORE_SIGMOID, LOGITS_ZIPF, 4,
                row_align=16),
+        Config("mixed_2048", 7168, 2048, 256, 8, 2048, FMT_CB2, SCORE_SIGMOID, LOGITS_BIASED, 5,
+               row_align=16, down_format=FMT_Q2K),
     ]
 }
 
@@ -215,26 +233,26 @@ def make_layer(cfg: Config, tokens: Optional[int] = None, seed: Optional[int] = 
     """All inputs of one configuration as host numpy arrays.
 
     Returns a dict with the layer description (hidden, inter, n_experts,
-    top_k, score, format, strides) plus w_gate / w_up / w_down (uint8
-    [E x N x row_bytes]), codebook (int8 [256 x 8] or None), x (bf16 bits
-    [T x H]) and logits (fp32 [T x E]).
+    top_k, score, format (W_gate / W_up), down_format, strides) plus w_gate /
+    w_up / w_down (uint8 [E x N x row_bytes]), codebook (int8 [256 x 8] or
+    None), x (bf16 bits [T x H]) and logits (fp32 [T x E]).
     """
     seed = cfg.seed if seed is None else seed
     T = cfg.tokens if tokens is None else tokens
     H, I, E, k = cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k
-    codebook = make_codebook(seed) if cfg.format == FMT_CB2 else None
+    codebook = make_codebook(seed) if FMT_CB2 in (cfg.format, cfg.dn_format) else None
     gu_rb = cfg.row_bytes(H, align)
-    dn_rb = cfg.row_bytes(I, align)
+    dn_rb = cfg.row_bytes(I, align, cfg.dn_format)
     layer = dict(
         name=cfg.name, hidden=H, inter=I, n_experts=E, top_k=k, score=cfg.score,
-        format=cfg.format, tokens=T,
+        format=cfg.format, down_format=cfg.dn_format, tokens=T,
         gate_up_row_bytes=gu_rb, down_row_bytes=dn_rb,
         gate_up_expert_stride=I * gu_rb, down_expert_stride=H * dn_rb,
         codebook=codebook,
     )
     layer["w_gate"] = make_experts(seed, TENSOR_GATE, E, I, H, cfg.format, gu_rb, codebook)
     layer["w_up"] = make_experts(seed, TENSOR_UP, E, I, H, cfg.format, gu_rb, codebook)
-    layer["w_down"] = make_experts(seed, TENSOR_DOWN, E, H, I, cfg.format, dn_rb, codebook)
+    layer["w_down"] = make_experts(seed, TENSOR_DOWN, E, H, I, cfg.dn_format, dn_rb, codebook)
     layer["x"] = make_x(seed, T, H)
     layer["logits"] = make_logits(seed, cfg.logits, T, E, k)
     return layer

@@ -46,6 +46,7 @@ class _Layer(ctypes.Structure):
         ("hidden", ctypes.c_int32), ("inter", ctypes.c_int32),
         ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
         ("score", ctypes.c_int32), ("format", ctypes.c_int32),
+        ("down_format", ctypes.c_int32),
         ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p),
         ("w_down", ctypes.c_void_p),
         ("gate_up_row_bytes", ctypes.c_int64), ("down_row_bytes", ctypes.c_int64),
@@ -136,6 +137,8 @@ class Oracle:
         L.hidden, L.inter = layer["hidden"], layer["inter"]
         L.n_experts, L.top_k = layer["n_experts"], layer["top_k"]
         L.score, L.format = layer["score"], layer["format"]
+        # the down projection may use another format (the shipping mix)
+        L.down_format = layer.get("down_format", layer["format"])
         for name in ("w_gate", "w_up", "w_down"):
             arr = layer[name]
             assert arr.dtype == np.uint8 and arr.flags["C_CONTIGUOUS"]

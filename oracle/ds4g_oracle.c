@@ -255,19 +255,32 @@ int orc_route(const float *logits, int T, int E, int k, int score,
  * kk >= K (padding of the last block) are ignored.
  * --------------------------------------------------------------------- */
 typedef struct {
-    int32_t hidden, inter, n_experts, top_k, score, format;
+    int32_t hidden, inter, n_experts, top_k, score;
+    int32_t format;         /* W_gate and W_up                                  */
+    int32_t down_format;    /* W_down (the shipping mix: codebook up/gate, Q2_K
+                               down -- ds4 README mirror, "Model Weights")      */
     const uint8_t *w_gate, *w_up, *w_down;
     int64_t gate_up_row_bytes, down_row_bytes;
     int64_t gate_up_expert_stride, down_expert_stride;
     const int8_t *codebook;
 } orc_layer;
 
-/* Dequantizes one row of K logical weights (ceil(K/256) blocks) to fp32. */
-static void dequant_row(const orc_layer *L, const uint8_t *row, int K, float *out)
+/* Both formats known; a codebook present when either matrix uses it. */
+static int orc_formats_ok(const orc_layer *L)
+{
+    if (L->format != ORC_FMT_Q2K && L->format != ORC_FMT_CB2) return 0;
+    if (L->down_format != ORC_FMT_Q2K && L->down_format != ORC_FMT_CB2) return 0;
+    if ((L->format == ORC_FMT_CB2 || L->down_format == ORC_FMT_CB2) && !L->codebook) return 0;
+    return 1;
+}
+
+/* Dequantizes one row of K logical weights (ceil(K/256) blocks of format
+ * fmt) to fp32. */
+static void dequant_row(const orc_layer *L, int fmt, const uint8_t *row, int K, float *out)
 {
     int nblk = (K + ORC_QK - 1) / ORC_QK;
     for (int b = 0; b < nblk; ++b) {
-        if (L->format == ORC_FMT_Q2K)
+        if (fmt == ORC_FMT_Q2K)
             orc_q2k_dequant_block(row + (int64_t)b * ORC_Q2K_BYTES, out + b * ORC_QK);
         else
             orc_cb2_dequant_block(row + (int64_t)b * ORC_CB2_BYTES, L->codebook,
@@ -288,15 +301,15 @@ static void expert_ffn(const orc_layer *L, int e, const double *x, double *o,
     const uint8_t *wd = L->w_down + (int64_t)e * L->down_expert_stride;
     for (int n = 0; n < I; ++n) {
         double g = 0.0, u = 0.0;
-        dequant_row(L, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);
+        dequant_row(L, L->format, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);
         for (int kk = 0; kk < H; ++kk) g += (double)rowbuf[kk] * x[kk];
-        dequant_row(L, wu + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);
+        dequant_row(L, L->format, wu + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);
         for (int kk = 0; kk < H; ++kk) u += (double)rowbuf[kk] * x[kk];
         h[n] = g / (1.0 + exp(-g)) * u;
     }
     for (int m = 0; m < H; ++m) {
         double acc = 0.0;
-        dequant_row(L, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);
+        dequant_row(L, L->down_format, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);
         for (int n = 0; n < I; ++n) acc += (double)rowbuf[n] * h[n];
         o[m] = acc;
     }
@@ -314,8 +327,7 @@ int orc_moe_forward(const orc_layer *L, const uint16_t *x, const float *logits,
     if (!L || !x || !logits || !y || T < 0) return ORC_ERR_INVALID;
     const int H = L->hidden, I = L->inter, E = L->n_experts, k = L->top_k;
     if (H < 1 || I < 1 || E < 1 || E > 256 || k < 1 || k > E) return ORC_ERR_INVALID;
-    if (L->format != ORC_FMT_Q2K && L->format != ORC_FMT_CB2) return ORC_ERR_INVALID;
-    if (L->format == ORC_FMT_CB2 && !L->codebook) return ORC_ERR_INVALID;
+    if (!orc_formats_ok(L)) return ORC_ERR_INVALID;
     if (!tokens) n_tokens = T;
     int kmax = H > I ? H : I;
     int kpad = ((kmax + ORC_QK - 1) / ORC_QK) * ORC_QK;
@@ -354,6 +366,7 @@ done:
 int orc_expert_ffn(const orc_layer *L, int e, const uint16_t *x, double *o)
 {
     if (!L || !x || !o || e < 0 || e >= L->n_experts) return ORC_ERR_INVALID;
+    if (!orc_formats_ok(L)) return ORC_ERR_INVALID;
     const int H = L->hidden, I = L->inter;
     int kmax = H > I ? H : I;
     int kpad = ((kmax + ORC_QK - 1) / ORC_QK) * ORC_QK;

@@ -66,10 +66,11 @@ def np_dense_weights(layer, name: str, K: int) -> np.ndarray:
     routines above."""
     W = layer[name]
     E, N, rb = W.shape
-    bb = 84 if layer["format"] == S.FMT_Q2K else 70
+    fmt = layer.get("down_format", layer["format"]) if name == "w_down" else layer["format"]
+    bb = 84 if fmt == S.FMT_Q2K else 70
     nblk = -(-K // 256)
     raw = np.ascontiguousarray(W[:, :, :nblk * bb]).reshape(-1)
-    if layer["format"] == S.FMT_Q2K:
+    if fmt == S.FMT_Q2K:
         w = np_q2k_dequant(raw)
     else:
         w = np_cb2_dequant(raw, layer["codebook"])
@@ -115,8 +116,9 @@ def np_forward(layer, x_bf16, logits) -> np.ndarray:
 
 
 def small_layer(seed=11, H=512, I=320, E=6, k=3, T=5, fmt=S.FMT_Q2K, score=S.SCORE_SOFTMAX,
-                logits_kind=S.LOGITS_NORMAL, align=1):
-    cfg = S.Config("pin", H, I, E, k, T, fmt, score, logits_kind, seed, row_align=align)
+                logits_kind=S.LOGITS_NORMAL, align=1, down_fmt=None):
+    cfg = S.Config("pin", H, I, E, k, T, fmt, score, logits_kind, seed, row_align=align,
+                   down_format=down_fmt)
     return S.make_layer(cfg)
 
 
@@ -279,11 +281,17 @@ def pin_route_full_k(orc):
 
 def pin_forward_dense(orc):
     """Oracle forward against the dense numpy fp64 reference: the tiny
-    workload, a padded-I layer, a sigmoid layer and a codebook layer."""
+    workload, a padded-I layer, a sigmoid layer, a codebook layer, and the
+    two mixed layers (codebook gate/up with Q2_K down -- the shipping mix --
+    and the reverse, so that a format read for the wrong matrix fails)."""
     layers = [S.make_layer(S.CONFIGS["tiny"]),
               small_layer(),
               small_layer(seed=12, I=256 + 40, score=S.SCORE_SIGMOID, logits_kind=S.LOGITS_UNIFORM),
-              small_layer(seed=13, H=512, I=256, E=5, k=2, T=3, fmt=S.FMT_CB2, align=16)]
+              small_layer(seed=13, H=512, I=256, E=5, k=2, T=3, fmt=S.FMT_CB2, align=16),
+              small_layer(seed=15, H=512, I=320, E=5, k=2, T=3, fmt=S.FMT_CB2, align=16,
+                          down_fmt=S.FMT_Q2K),
+              small_layer(seed=16, H=512, I=256, E=4, k=2, T=3, fmt=S.FMT_Q2K, align=16,
+                          down_fmt=S.FMT_CB2)]
     for L in layers:
         y, ids, w = orc.moe_forward(L, L["x"], L["logits"])
         ref = np_forward(L, L["x"], L["logits"])

@@ -45,8 +45,8 @@ MUTANTS = {
     "combine_wrong_slot_weight": [("yt[m] += w[i] * o[m];", "yt[m] += w[k - 1 - i] * o[m];")],
     "row_blocks_not_advanced": [("orc_q2k_dequant_block(row + (int64_t)b * ORC_Q2K_BYTES, out + b * ORC_QK);",
                                  "orc_q2k_dequant_block(row, out + b * ORC_QK);")],
-    "up_reads_gate": [("dequant_row(L, wu + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);",
-                       "dequant_row(L, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);")],
+    "up_reads_gate": [("dequant_row(L, L->format, wu + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);",
+                       "dequant_row(L, L->format, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);")],
     "min_term_uses_d": [("float min_part = dmin * (float)(sc >> 4);",
                          "float min_part = d * (float)(sc >> 4);")],
     "sigmoid_weights_not_normalised": [
@@ -56,8 +56,18 @@ MUTANTS = {
          "        }")],
     "down_expert_stride_of_gate": [("L->w_down + (int64_t)e * L->down_expert_stride",
                                     "L->w_down + (int64_t)e * L->gate_up_expert_stride")],
-    "down_row_bytes_of_gate": [("dequant_row(L, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);",
-                                "dequant_row(L, wd + (int64_t)m * L->gate_up_row_bytes, I, rowbuf);")],
+    "down_row_bytes_of_gate": [("dequant_row(L, L->down_format, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);",
+                                "dequant_row(L, L->down_format, wd + (int64_t)m * L->gate_up_row_bytes, I, rowbuf);")],
+    "down_in_gate_format": [("dequant_row(L, L->down_format, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);",
+                             "dequant_row(L, L->format, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);")],
+    "gate_in_down_format": [("dequant_row(L, L->format, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);",
+                             "dequant_row(L, L->down_format, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);")],
+    "formats_swapped": [("dequant_row(L, L->format, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);",
+                         "dequant_row(L, L->down_format, wg + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);"),
+                        ("dequant_row(L, L->format, wu + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);",
+                         "dequant_row(L, L->down_format, wu + (int64_t)n * L->gate_up_row_bytes, H, rowbuf);"),
+                        ("dequant_row(L, L->down_format, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);",
+                         "dequant_row(L, L->format, wd + (int64_t)m * L->down_row_bytes, I, rowbuf);")],
     "q2k_three_bit_field": [("(qs[32 * h + l] >> (2 * g)) & 3", "(qs[32 * h + l] >> (2 * g)) & 7")],
     "q2k_halves_swapped": [("(qs[32 * h + l] >> (2 * g)) & 3", "(qs[32 * (1 - h) + l] >> (2 * g)) & 3")],
     "cb2_drops_d": [("float value = d * (float)scale;", "float value = (float)scale;")],
