@@ -85,13 +85,13 @@ def parse(argv=None):
 def default_steps(cfg: S.Config):
     # ~1-2 s of device time at the expected step times
     return {"tiny": 20000, "decode_1tok": 100000, "decode_32tok": 4000,
-            "prefill_2048": 200, "codebook_512": 1000}[cfg.name]
+            "prefill_2048": 200, "codebook_512": 1000, "mixed_2048": 200}[cfg.name]
 
 
 def floor_steps(cfg: S.Config):
     # about 0.2 s of device time: the least a per-config line is timed over
     return {"tiny": 5000, "decode_1tok": 5000, "decode_32tok": 150,
-            "prefill_2048": 60, "codebook_512": 80}[cfg.name]
+            "prefill_2048": 60, "codebook_512": 80, "mixed_2048": 60}[cfg.name]
 
 
 # ---------------------------------------------------------------------------
@@ -208,8 +208,10 @@ def layer_path(cfg: S.Config) -> str:
     the decode kernels up to 32 tokens for Q2_K, the tensor-core prefill
     kernels (both formats) for rows of a multiple of 16 bytes otherwise, the
     general kernels for the rest)."""
-    tc = cfg.row_bytes(cfg.hidden) % 16 == 0 and cfg.row_bytes(cfg.inter) % 16 == 0
-    if cfg.format == S.FMT_Q2K and cfg.inter % 16 == 0 and cfg.tokens <= 32:
+    tc = (cfg.row_bytes(cfg.hidden) % 16 == 0 and
+          cfg.row_bytes(cfg.inter, fmt=cfg.dn_format) % 16 == 0)
+    if (cfg.format == S.FMT_Q2K and cfg.dn_format == S.FMT_Q2K and cfg.inter % 16 == 0 and
+            cfg.tokens <= 32):
         return "decode"
     return "tc" if tc else "general"
 
@@ -251,9 +253,8 @@ def measured_traffic(kernel: str, workload: str):
 
 def layer_bytes(cfg: S.Config):
     """Logical quantized bytes of one expert's matrices."""
-    bb = cfg.block_bytes
-    gu = cfg.inter * (cfg.hidden // 256) * bb                 # one of gate / up
-    dn = cfg.hidden * (-(-cfg.inter // 256)) * bb
+    gu = cfg.inter * (cfg.hidden // 256) * cfg.block_bytes          # one of gate / up
+    dn = cfg.hidden * (-(-cfg.inter // 256)) * cfg.down_block_bytes
     return gu, dn
 
 
@@ -296,7 +297,7 @@ def roofline_for(cfg: S.Config, path: str, ph_ms, active, steps_b, T, k):
     flops = 2.0 * T * k * 2 * H * I
     tflops = flops / (ph_ms[1] / 1000.0) / 1e12
     gbs = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9
-    if path == "tc" and cfg.format == S.FMT_Q2K:
+    if path == "tc" and cfg.format == S.FMT_Q2K and cfg.dn_format == S.FMT_Q2K:
         return {"bound": "tensor", "kernel": "tc_kernel<0> (gate/up)", "achieved": tflops,
                 "peak": sustained, "peak_kind": f"{tkind} bf16 sustained (fp16 same rate)",
                 "unit": "TFLOP/s", "frac": tflops / sustained, "frac_of_burst": tflops / burst,
@@ -368,7 +369,9 @@ def reference_arm(args, cfg, rank, world):
 
 
 def workload_config(cfg: S.Config, copies: int, l2_note: str):
-    fmt = "Q2_K" if cfg.format == S.FMT_Q2K else "codebook-2bit"
+    names = {S.FMT_Q2K: "Q2_K", S.FMT_CB2: "codebook-2bit"}
+    fmt = (names[cfg.format] if cfg.format == cfg.dn_format
+           else f"{names[cfg.format]} gate/up + {names[cfg.dn_format]} down")
     return {"workload": f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.n_experts} "
                         f"top-{cfg.top_k} T={cfg.tokens} {fmt}",
             "hidden": cfg.hidden, "inter": cfg.inter, "experts": cfg.n_experts,
@@ -429,7 +432,8 @@ class Workload:
         for c in range(copies):
             t = base if c == 0 else {n: v.clone() for n, v in base.items()}
             self.w_dev.append(D.Layer(H, cfg.inter, E, k, cfg.score, cfg.format, t["w_gate"],
-                                      t["w_up"], t["w_down"], cb, flags=flags))
+                                      t["w_up"], t["w_down"], cb, flags=flags,
+                                      down_fmt=cfg.dn_format))
         self.x_dev = torch.from_numpy(self.x_all.view(np.int16)).to(dev)
         self.l_dev = torch.from_numpy(self.l_all).to(dev)
         self.y_dev = torch.empty((T, H), dtype=torch.float32, device=dev)

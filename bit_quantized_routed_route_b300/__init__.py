@@ -53,6 +53,7 @@ class MoeDesc(ctypes.Structure):
         ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
         ("score", ctypes.c_int32), ("format", ctypes.c_int32),
         ("flags", ctypes.c_int32), ("tc_min_tokens", ctypes.c_int32),
+        ("down_format", ctypes.c_int32), ("reserved", ctypes.c_int32),
         ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
         ("gate_up_row_bytes", ctypes.c_int64), ("down_row_bytes", ctypes.c_int64),
         ("gate_up_expert_stride", ctypes.c_int64), ("down_expert_stride", ctypes.c_int64),
@@ -220,14 +221,17 @@ class Layer:
     """Device-resident expert weights of one layer plus their descriptor.
 
     ``weights`` holds uint8 tensors [E x N x row_bytes] (any device tensors
-    the caller keeps alive); the descriptor points at them."""
+    the caller keeps alive); the descriptor points at them.  ``fmt`` is the
+    format of W_gate and W_up, ``down_fmt`` that of W_down (default: fmt)."""
 
     def __init__(self, hidden, inter, n_experts, top_k, score, fmt, w_gate, w_up, w_down,
-                 codebook=None, flags=0, tc_min_tokens=0):
+                 codebook=None, flags=0, tc_min_tokens=0, down_fmt=None):
         self.tensors = (w_gate, w_up, w_down, codebook)
         d = MoeDesc()
         d.hidden, d.inter, d.n_experts, d.top_k = hidden, inter, n_experts, top_k
         d.score, d.format, d.flags, d.tc_min_tokens = score, fmt, flags, tc_min_tokens
+        d.down_format = fmt if down_fmt is None else down_fmt
+        d.reserved = 0
         d.w_gate, d.w_up, d.w_down = _ptr(w_gate), _ptr(w_up), _ptr(w_down)
         d.gate_up_row_bytes = w_gate.shape[-1]
         d.down_row_bytes = w_down.shape[-1]

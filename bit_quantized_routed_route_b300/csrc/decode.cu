@@ -1887,7 +1887,8 @@ cudaError_t launch_decode_tc(const LayerArgs &la, const DecodeBufs &db, const De
 
 bool decode_path_supported(const Plan &p, const ds4g_moe_desc *d)
 {
-    if (d->format != DS4G_FMT_Q2K || p.T > kDecodeMaxT || p.I % kTileM != 0 ||
+    if (d->format != DS4G_FMT_Q2K || d->down_format != DS4G_FMT_Q2K || p.T > kDecodeMaxT ||
+        p.I % kTileM != 0 ||
         p.H % kDownRows != 0)
         return false;
     if (p.T > kDecodePreferT) return p.H % tcd::kBM == 0;      // tcgen05 decode kernel

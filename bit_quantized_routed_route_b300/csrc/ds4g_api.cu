@@ -59,12 +59,15 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
         return DS4G_ERR_INVALID;
     if (d->score != DS4G_SCORE_SOFTMAX && d->score != DS4G_SCORE_SIGMOID) return DS4G_ERR_INVALID;
     if (d->format != DS4G_FMT_Q2K && d->format != DS4G_FMT_CB2) return DS4G_ERR_INVALID;
+    if (d->down_format != DS4G_FMT_Q2K && d->down_format != DS4G_FMT_CB2) return DS4G_ERR_INVALID;
+    if (d->reserved != 0) return DS4G_ERR_INVALID;
     if ((d->flags & ~(DS4G_FORCE_GEMV | DS4G_FORCE_TC | DS4G_DEBUG_STALL)) != 0)
         return DS4G_ERR_INVALID;
     if ((d->flags & DS4G_FORCE_GEMV) && (d->flags & DS4G_FORCE_TC)) return DS4G_ERR_INVALID;
     if (d->tc_min_tokens < 0) return DS4G_ERR_INVALID;
     if (!d->w_gate || !d->w_up || !d->w_down) return DS4G_ERR_INVALID;
-    if (d->format == DS4G_FMT_CB2 && !d->codebook) return DS4G_ERR_INVALID;
+    if ((d->format == DS4G_FMT_CB2 || d->down_format == DS4G_FMT_CB2) && !d->codebook)
+        return DS4G_ERR_INVALID;
     if (T > DS4G_MAX_TOKENS) return DS4G_ERR_SHAPE;
     if (d->hidden < kQK || d->hidden > DS4G_MAX_HIDDEN || d->hidden % kQK != 0)
         return DS4G_ERR_SHAPE;
@@ -80,14 +83,17 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     q.I_pad = (d->inter + kQK - 1) / kQK * kQK;
     q.H_blocks = d->hidden / kQK;
     q.I_blocks = q.I_pad / kQK;
-    q.block_bytes = d->format == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+    q.gu_block_bytes = d->format == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+    q.dn_block_bytes = d->down_format == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
 
-    const int64_t gu_logical = (int64_t)q.H_blocks * q.block_bytes;
-    const int64_t dn_logical = (int64_t)q.I_blocks * q.block_bytes;
-    const int64_t row_mult = d->format == DS4G_FMT_Q2K ? 4 : 2;
+    const int64_t gu_logical = (int64_t)q.H_blocks * q.gu_block_bytes;
+    const int64_t dn_logical = (int64_t)q.I_blocks * q.dn_block_bytes;
+    // Q2_K rows hold 4-byte aligned blocks, codebook rows 2-byte aligned ones
+    const int64_t gu_mult = d->format == DS4G_FMT_Q2K ? 4 : 2;
+    const int64_t dn_mult = d->down_format == DS4G_FMT_Q2K ? 4 : 2;
     if (d->gate_up_row_bytes < gu_logical || d->down_row_bytes < dn_logical)
         return DS4G_ERR_LAYOUT;
-    if (d->gate_up_row_bytes % row_mult || d->down_row_bytes % row_mult) return DS4G_ERR_LAYOUT;
+    if (d->gate_up_row_bytes % gu_mult || d->down_row_bytes % dn_mult) return DS4G_ERR_LAYOUT;
     if (d->gate_up_expert_stride < (int64_t)q.I * d->gate_up_row_bytes ||
         d->down_expert_stride < (int64_t)q.H * d->down_row_bytes)
         return DS4G_ERR_LAYOUT;
@@ -200,7 +206,8 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     a.k = p.k;
     a.A = p.A;
     a.T = p.T;
-    a.format = d->format;
+    a.gu_format = d->format;
+    a.dn_format = d->down_format;
     a.w_gate = static_cast<const uint8_t *>(d->w_gate);
     a.w_up = static_cast<const uint8_t *>(d->w_up);
     a.w_down = static_cast<const uint8_t *>(d->w_down);

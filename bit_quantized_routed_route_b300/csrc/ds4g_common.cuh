@@ -26,7 +26,8 @@ struct Plan {
     int32_t I_pad;          // inter rounded up to a multiple of 256 (down K)
     int32_t H_blocks;       // hidden / 256
     int32_t I_blocks;       // I_pad / 256
-    int32_t block_bytes;    // 84 or 70
+    int32_t gu_block_bytes; // 84 or 70 (W_gate, W_up)
+    int32_t dn_block_bytes; // 84 or 70 (W_down)
     size_t ids, wts, counts, offsets, perm, slot_pos, active, meta;
     size_t status;          // int32 device status word (DS4G_OK or DS4G_ERR_TIMEOUT)
     size_t sync;            // [decode_sync_words] int32 counters of the decode kernels
@@ -77,7 +78,8 @@ cudaError_t launch_cb2_dequant(const uint8_t *blocks, int64_t n_blocks, const in
                                void *out, int dtype, cudaStream_t s);
 
 struct LayerArgs {
-    int H, I, I_pad, E, k, A, T, format;
+    int H, I, I_pad, E, k, A, T;
+    int gu_format, dn_format;  // block formats of W_gate / W_up and of W_down
     const uint8_t *w_gate, *w_up, *w_down;
     int64_t gu_row, dn_row, gu_stride, dn_stride;
     const int8_t *codebook;

@@ -224,16 +224,23 @@ __global__ void __launch_bounds__(256) combine_kernel(LayerArgs a)
     }
 }
 
-template <int FMT>
-cudaError_t launch_fmt(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
-                       const cudaEvent_t *ev)
+// Gate/up in the W_gate / W_up format, down in the W_down format (they may
+// differ: the shipping mix has codebook gate/up and Q2_K down).
+cudaError_t launch_gemv_kernels(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
+                                const cudaEvent_t *ev)
 {
     const int persistent = dev.sm_count * 8;
     const int gu_items = min(a.E, a.A) * (a.I_pad / kWarps);
     const int dn_items = min(a.E, a.A) * (a.H / kWarps);
-    gateup_kernel<FMT><<<min(gu_items, persistent), kWarps * 32, 0, s>>>(a);
+    if (a.gu_format == DS4G_FMT_Q2K)
+        gateup_kernel<DS4G_FMT_Q2K><<<min(gu_items, persistent), kWarps * 32, 0, s>>>(a);
+    else
+        gateup_kernel<DS4G_FMT_CB2><<<min(gu_items, persistent), kWarps * 32, 0, s>>>(a);
     if (ev && record_phase(ev[2], s) != cudaSuccess) return cudaGetLastError();
-    down_kernel<FMT><<<min(dn_items, persistent), kWarps * 32, 0, s>>>(a);
+    if (a.dn_format == DS4G_FMT_Q2K)
+        down_kernel<DS4G_FMT_Q2K><<<min(dn_items, persistent), kWarps * 32, 0, s>>>(a);
+    else
+        down_kernel<DS4G_FMT_CB2><<<min(dn_items, persistent), kWarps * 32, 0, s>>>(a);
     if (ev && record_phase(ev[3], s) != cudaSuccess) return cudaGetLastError();
     cudaError_t e = launch_combine(a, dev, s);
     if (e != cudaSuccess) return e;
@@ -255,8 +262,7 @@ cudaError_t launch_combine(const LayerArgs &a, const DeviceInfo &dev, cudaStream
 cudaError_t launch_gemv_path(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
                              const cudaEvent_t *events)
 {
-    if (a.format == DS4G_FMT_Q2K) return launch_fmt<DS4G_FMT_Q2K>(a, dev, s, events);
-    return launch_fmt<DS4G_FMT_CB2>(a, dev, s, events);
+    return launch_gemv_kernels(a, dev, s, events);
 }
 
 int32_t gemv_path_launches(const Plan &) { return 3; }

@@ -93,6 +93,7 @@ struct TcArgs {
     const float *wseg;          // routing weight of each segment row
     const int32_t *eseg;        // activation exponent of each segment row
     __half *hp;                 // gate/up output [A][I_pad] (permuted order)
+    int h_perm32;               // h in the perm32 order of a Q2_K W_down (else natural)
     float *yslot;               // down output [A][H]
     const int8_t *codebook;     // [256 x 8] int8 (codebook format)
     int32_t *status;
@@ -390,7 +391,8 @@ struct DequantRole {
             ptx::tc_fence_after();
             const int chunks = (nlen + 7) / 8;
             const int n = mt * kBM + row;
-            const int col = FMT == DS4G_FMT_Q2K ? perm32(n) : n;
+            // h is laid out for the down kernel's format
+            const int col = a.h_perm32 ? perm32(n) : n;
             for (int ch = wg; ch < chunks; ch += 4) {
                 float g[8], u[8];
                 ptx::tmem_ld8(c.tmem + lane_base + kAccCol + 8 * ch, g);
@@ -881,7 +883,7 @@ cudaError_t launch_tc_prep(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     const int prep_grid = dev.sm_count * 4;
     tc_prep_kernel<<<prep_grid, 256, 0, s>>>(la.x, la.H, la.k, la.A, la.perm, la.counts,
                                              la.offsets, la.E, tb.xseg, tb.tiles, tb.n_tiles,
-                                             la.format == DS4G_FMT_Q2K ? 1 : 0, la.wts, tb.wseg,
+                                             la.gu_format == DS4G_FMT_Q2K ? 1 : 0, la.wts, tb.wseg,
                                              tb.texp, tb.eseg);
     return cudaGetLastError();
 }
@@ -915,15 +917,17 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     a.K = la.H;
     a.m_tiles = la.I_pad / kBM;
     a.codebook = la.codebook;
-    const bool cb2 = la.format == DS4G_FMT_CB2;
-    if ((e = cb2 ? launch_tc<0, DS4G_FMT_CB2>(m_gate, m_up, m_x, a, dev.sm_count, s)
+    a.h_perm32 = la.dn_format == DS4G_FMT_Q2K ? 1 : 0;
+    if ((e = la.gu_format == DS4G_FMT_CB2
+                 ? launch_tc<0, DS4G_FMT_CB2>(m_gate, m_up, m_x, a, dev.sm_count, s)
                  : launch_tc<0, DS4G_FMT_Q2K>(m_gate, m_up, m_x, a, dev.sm_count, s)) != cudaSuccess)
         return e;
     if (ev && (e = record_phase(ev[2], s)) != cudaSuccess) return e;
 
     a.K = la.I_pad;
     a.m_tiles = la.H / kBM;
-    if ((e = cb2 ? launch_tc<1, DS4G_FMT_CB2>(m_down, m_down, m_h, a, dev.sm_count, s)
+    if ((e = la.dn_format == DS4G_FMT_CB2
+                 ? launch_tc<1, DS4G_FMT_CB2>(m_down, m_down, m_h, a, dev.sm_count, s)
                  : launch_tc<1, DS4G_FMT_Q2K>(m_down, m_down, m_h, a, dev.sm_count, s)) != cudaSuccess)
         return e;
     if (ev && (e = record_phase(ev[3], s)) != cudaSuccess) return e;

@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define DS4G_ABI_VERSION 1
+#define DS4G_ABI_VERSION 2
 
 /* Symbols of the shared library (built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -133,6 +133,11 @@ enum {
  * and the GEMV kernels; validated (>= 0) and otherwise ignored: every
  * segment of a call takes the path chosen for the call (see "Path" under
  * ds4g_moe_forward).
+ * format / down_format: the block format of W_gate and W_up / of W_down.
+ * The shipping mix of the ds4 weights is DS4G_FMT_CB2 / DS4G_FMT_Q2K
+ * (IQ2_XXS up/gate, Q2_K down: ds4 README mirror, "Model Weights").  Set
+ * both; the codebook is required when either is DS4G_FMT_CB2.
+ * reserved: must be 0.
  */
 typedef struct ds4g_moe_desc {
     int32_t hidden;
@@ -140,9 +145,11 @@ typedef struct ds4g_moe_desc {
     int32_t n_experts;
     int32_t top_k;
     int32_t score;             /* ds4g_score  */
-    int32_t format;            /* ds4g_format */
+    int32_t format;            /* ds4g_format of W_gate and W_up */
     int32_t flags;
     int32_t tc_min_tokens;
+    int32_t down_format;       /* ds4g_format of W_down                          */
+    int32_t reserved;          /* 0                                              */
     const void *w_gate;
     const void *w_up;
     const void *w_down;
@@ -150,7 +157,7 @@ typedef struct ds4g_moe_desc {
     int64_t down_row_bytes;
     int64_t gate_up_expert_stride;
     int64_t down_expert_stride;
-    const int8_t *codebook;    /* [256 x 8] int8, device; DS4G_FMT_CB2 only     */
+    const int8_t *codebook;    /* [256 x 8] int8, device; when a matrix is CB2  */
 } ds4g_moe_desc;
 
 /*

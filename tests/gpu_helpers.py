@@ -38,7 +38,8 @@ def to_device(layer: dict, flags: int = 0, tc_min_tokens: int = 0) -> D.Layer:
     t = layer[key]
     return D.Layer(layer["hidden"], layer["inter"], layer["n_experts"], layer["top_k"],
                    layer["score"], layer["format"], t["w_gate"], t["w_up"], t["w_down"],
-                   t["codebook"], flags=flags, tc_min_tokens=tc_min_tokens)
+                   t["codebook"], flags=flags, tc_min_tokens=tc_min_tokens,
+                   down_fmt=layer.get("down_format"))
 
 
 def run_forward(L: D.Layer, x: np.ndarray, logits: np.ndarray):

@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert D.abi_version() == 1
+    assert D.abi_version() == 2
     assert D.status_string(D.OK) == "ok"
     for s in range(1, 8):
         assert D.status_string(s) not in ("ok", "unknown status")
@@ -44,6 +44,7 @@ def desc(**kw):
     d = D.MoeDesc()
     d.hidden, d.inter, d.n_experts, d.top_k = 256, 128, 8, 2
     d.score, d.format, d.flags, d.tc_min_tokens = D.SCORE_SOFTMAX, D.FMT_Q2K, 0, 0
+    d.down_format, d.reserved = D.FMT_Q2K, 0
     d.w_gate = d.w_up = d.w_down = FAKE
     d.gate_up_row_bytes, d.down_row_bytes = 84, 84
     d.gate_up_expert_stride, d.down_expert_stride = 128 * 84, 256 * 84
@@ -89,6 +90,9 @@ def test_noalloc_scratch_covers_a_32_token_decode_of_the_7168_layer():
     (dict(top_k=3, n_experts=2), D.ERR_INVALID),
     (dict(score=2), D.ERR_INVALID),
     (dict(format=5), D.ERR_INVALID),
+    (dict(down_format=5), D.ERR_INVALID),
+    (dict(reserved=1), D.ERR_INVALID),
+    (dict(down_format=D.FMT_CB2, down_row_bytes=70), D.ERR_INVALID),      # no codebook
     (dict(flags=D.FORCE_GEMV | D.FORCE_TC), D.ERR_INVALID),
     (dict(flags=64), D.ERR_INVALID),
     (dict(tc_min_tokens=-1), D.ERR_INVALID),
@@ -165,17 +169,35 @@ def test_routing_view_points_inside_the_workspace():
     st, _ = D.moe_routing_view(d, 4, FAKE, need - 1)
     assert st == D.ERR_WORKSPACE
 
-def layer_desc(H, I, E, k, fmt=None, flags=0, align=1):
-    """A descriptor with packed (or `align`-padded) rows at a fake address."""
+def layer_desc(H, I, E, k, fmt=None, flags=0, align=1, down_fmt=None):
+    """A descriptor with packed (or `align`-padded) rows at a fake address;
+    W_down in `down_fmt` (default: fmt)."""
     fmt = D.FMT_Q2K if fmt is None else fmt
+    down_fmt = fmt if down_fmt is None else down_fmt
     bb = 84 if fmt == D.FMT_Q2K else 70
-    gr, dr = H // 256 * bb, -(-I // 256) * bb
+    dbb = 84 if down_fmt == D.FMT_Q2K else 70
+    gr, dr = H // 256 * bb, -(-I // 256) * dbb
     gr, dr = -(-gr // align) * align, -(-dr // align) * align
-    return desc(hidden=H, inter=I, n_experts=E, top_k=k, format=fmt, flags=flags,
-                gate_up_row_bytes=gr, down_row_bytes=dr,
+    return desc(hidden=H, inter=I, n_experts=E, top_k=k, format=fmt, down_format=down_fmt,
+                flags=flags, gate_up_row_bytes=gr, down_row_bytes=dr,
                 gate_up_expert_stride=-(-I * gr // 16) * 16,
                 down_expert_stride=-(-H * dr // 16) * 16,
-                codebook=FAKE if fmt == D.FMT_CB2 else None)
+                codebook=FAKE if D.FMT_CB2 in (fmt, down_fmt) else None)
+
+
+def test_mixed_format_descriptor_is_accepted():
+    """Codebook gate/up with Q2_K down (the shipping mix) and the reverse:
+    each matrix's rows are checked against its own block size."""
+    d = layer_desc(7168, 2048, 256, 8, fmt=D.FMT_CB2, down_fmt=D.FMT_Q2K, align=16)
+    assert (d.gate_up_row_bytes, d.down_row_bytes) == (1968, 672)
+    assert D.moe_workspace_bytes(d, 64) > 0
+    d = layer_desc(512, 256, 4, 2, fmt=D.FMT_Q2K, down_fmt=D.FMT_CB2)
+    assert (d.gate_up_row_bytes, d.down_row_bytes) == (168, 70)
+    assert D.moe_workspace_bytes(d, 4) > 0
+    # W_down rows sized for the gate/up format are too short
+    d = layer_desc(512, 512, 4, 2, fmt=D.FMT_CB2, down_fmt=D.FMT_Q2K)
+    d.down_row_bytes = 2 * 70
+    assert D.moe_workspace_bytes(d, 4) == 0
 
 
 @pytest.mark.parametrize("shape,T,kw,launches", [
@@ -191,6 +213,10 @@ def layer_desc(H, I, E, k, fmt=None, flags=0, align=1):
     # the codebook format never takes the decode kernels
     ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_CB2, align=16), 1 + 5),
     ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_CB2), 1 + 3),
+    # mixed formats never take the (Q2_K-only) decode kernels
+    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_CB2, down_fmt=D.FMT_Q2K, align=16), 1 + 5),
+    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_Q2K, down_fmt=D.FMT_CB2), 1 + 5),   # 560-byte rows
+    ((7168, 1024, 256, 8), 1, dict(fmt=D.FMT_Q2K, down_fmt=D.FMT_CB2), 1 + 3),   # 280-byte rows
     # FORCE_GEMV keeps the decode kernels where they apply and rules out the
     # tensor-core kernels elsewhere; FORCE_TC needs 16-byte rows (504-byte down rows here)
     ((4096, 1536, 64, 6), 1, dict(flags=D.FORCE_GEMV), 2),

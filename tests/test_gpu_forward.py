@@ -22,7 +22,7 @@ from gpu_helpers import (boundary_tokens, cached_layer, check_output, check_rout
 pytestmark = pytest.mark.gpu
 
 SAMPLE = {"tiny": None, "decode_1tok": None, "decode_32tok": None, "prefill_2048": 64,
-          "codebook_512": 64}
+          "codebook_512": 64, "mixed_2048": 64}
 
 
 @pytest.mark.parametrize("name", list(S.CONFIGS))

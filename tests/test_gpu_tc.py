@@ -89,3 +89,22 @@ def test_tc_forced_on_unaligned_rows_is_rejected():
     assert L.workspace_bytes(8) == 0
     with pytest.raises(D.DS4GError):
         run_forward(L, layer["x"], layer["logits"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=1024, I=512, E=6, k=2, T=70, fmt=S.FMT_CB2, down_fmt=S.FMT_Q2K, align=16),
+    dict(H=512, I=320, E=5, k=3, T=150, fmt=S.FMT_CB2, down_fmt=S.FMT_Q2K, align=16),
+    dict(H=1024, I=512, E=4, k=2, T=40, fmt=S.FMT_Q2K, down_fmt=S.FMT_CB2, align=16),
+    dict(H=512, I=200, E=5, k=2, T=20, fmt=S.FMT_CB2, down_fmt=S.FMT_Q2K, align=2),   # general
+], ids=["cb2_q2k", "cb2_q2k_ragged_I", "q2k_cb2", "cb2_q2k_general"])
+def test_mixed_format_layers(orc, kw):
+    """W_gate / W_up in one format and W_down in the other (the shipping mix
+    is codebook gate/up with Q2_K down): the tensor-core kernels run each
+    matrix through its own dequantizer, h in the order the down kernel's
+    format needs; 2-byte aligned rows take the general kernels."""
+    layer = P.small_layer(seed=3000 + kw["H"] + kw["T"], score=S.SCORE_SIGMOID, **kw)
+    L = to_device(layer)
+    y, routing = run_forward(L, layer["x"], layer["logits"])
+    check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    check_output(y, yref)
