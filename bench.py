@@ -79,6 +79,9 @@ def parse(argv=None):
                     help="time only --config (no per_config object)")
     ap.add_argument("--force", default="auto", choices=["auto", "decode", "tc"],
                     help="run the layer on one path (default: the library's choice)")
+    ap.add_argument("--tc-min-tokens", type=int, default=0,
+                    help="per-segment split: segments below this many tokens take the GEMV "
+                         "kernels (tensor-core path only; 0 = off)")
     return ap.parse_args(argv)
 
 
@@ -433,7 +436,7 @@ class Workload:
             t = base if c == 0 else {n: v.clone() for n, v in base.items()}
             self.w_dev.append(D.Layer(H, cfg.inter, E, k, cfg.score, cfg.format, t["w_gate"],
                                       t["w_up"], t["w_down"], cb, flags=flags,
-                                      down_fmt=cfg.dn_format))
+                                      tc_min_tokens=args.tc_min_tokens, down_fmt=cfg.dn_format))
         self.x_dev = torch.from_numpy(self.x_all.view(np.int16)).to(dev)
         self.l_dev = torch.from_numpy(self.l_all).to(dev)
         self.y_dev = torch.empty((T, H), dtype=torch.float32, device=dev)

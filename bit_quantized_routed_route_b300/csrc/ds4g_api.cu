@@ -133,6 +133,7 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     q.wseg = take(A * 4);
     q.texp = take((size_t)T * 4);
     q.eseg = take(A * 4);
+    q.light = take((size_t)q.E * 4);
     q.x_stage = take((size_t)T * q.H * 2);
     q.l_stage = take((size_t)T * q.E * 4);
     q.y_stage = take((size_t)T * q.H * 4);
@@ -230,7 +231,8 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     TcBufs tb{reinterpret_cast<__half *>(ws + p.xseg), reinterpret_cast<__half *>(ws + p.hp),
               reinterpret_cast<int32_t *>(ws + p.tiles), meta + kMetaTiles, status,
               reinterpret_cast<float *>(ws + p.wseg), reinterpret_cast<int32_t *>(ws + p.texp),
-              reinterpret_cast<int32_t *>(ws + p.eseg)};
+              reinterpret_cast<int32_t *>(ws + p.eseg), reinterpret_cast<int32_t *>(ws + p.light),
+              meta + kMetaLight, d->tc_min_tokens};
     // the activation gather of the tensor-core path belongs to the routing phase
     if (path == Path::kTensorCore && (e = launch_tc_prep(a, tb, dev, s)) != cudaSuccess)
         return from_cuda(e);
@@ -359,9 +361,10 @@ int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T)
     if (T <= 0 || make_plan(desc, T, &p) != DS4G_OK) return 0;
     const Path path = choose_path(desc, p);
     if (path == Path::kDecode) return 2;     // reset/convert, fused layer kernel
-    return route_launches(T) + (path == Path::kDecode       ? 0
-                                : path == Path::kTensorCore ? kTcPathLaunches
-                                                            : gemv_path_launches(p));
+    return route_launches(T) +
+           (path == Path::kDecode       ? 0
+            : path == Path::kTensorCore ? kTcPathLaunches + (desc->tc_min_tokens > 0 ? kSplitLaunches : 0)
+                                        : gemv_path_launches(p));
 }
 
 ds4g_status ds4g_moe_forward_host(const ds4g_moe_desc *desc, const uint16_t *x_host,

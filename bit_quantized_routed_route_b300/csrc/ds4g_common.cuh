@@ -41,6 +41,7 @@ struct Plan {
     size_t wseg;            // [A] fp32 routing weight per segment row (tensor-core path)
     size_t texp;            // [T] int32 activation exponent of each token (see token_exponent)
     size_t eseg;            // [A] int32 activation exponent of each segment row (tensor-core path)
+    size_t light;           // [E] int32 experts whose segments take the GEMV kernels (split calls)
     size_t x_stage;         // [T x H] bf16 (host entry point)
     size_t l_stage;         // [T x E] fp32 (host entry point)
     size_t y_stage;         // [T x H] fp32 (host entry point)
@@ -48,7 +49,7 @@ struct Plan {
 };
 
 // meta words (int32) at Plan::meta
-enum { kMetaActive = 0, kMetaTiles = 1, kMetaWords = 64 };
+enum { kMetaActive = 0, kMetaTiles = 1, kMetaLight = 2, kMetaWords = 64 };
 
 // Validation + plan.  Returns DS4G_OK or the first error found.
 ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p);
@@ -98,6 +99,10 @@ cudaError_t launch_gemv_path(const LayerArgs &a, const DeviceInfo &dev, cudaStre
 int32_t gemv_path_launches(const Plan &p);
 // y[t] = sum_i yslot[slot_pos[t*k+i]] in slot order (one launch).
 cudaError_t launch_combine(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s);
+// The GEMV gate/up and down kernels alone, over the experts a.active[0 ..
+// *a.n_active) (the per-segment split runs them on the light segments).
+cudaError_t launch_gemv_gateup(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s);
+cudaError_t launch_gemv_down(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s);
 
 // Records `ev` on `s`; inside a stream capture the record becomes an
 // external event node, so that it is recorded again at every replay.
@@ -161,6 +166,9 @@ struct TcBufs {
     float *wseg;           // [A] routing weight of each segment row
     int32_t *texp;         // [T] activation exponent of each token
     int32_t *eseg;         // [A] activation exponent of each segment row
+    int32_t *light;        // [E] experts routed to the GEMV kernels (split calls)
+    int32_t *n_light;
+    int min_tokens;        // segments with fewer tokens take the GEMV kernels (0: none)
 };
 bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d);
 int32_t tc_max_tiles(int32_t E, int32_t A);
@@ -172,6 +180,7 @@ cudaError_t launch_tc_path(const LayerArgs &a, const TcBufs &b, const DeviceInfo
                            cudaStream_t s, const cudaEvent_t *events, uint64_t wait_ns,
                            bool stall);
 constexpr int32_t kTcPathLaunches = 5;  // token exponents, prep, gate/up, down, combine
+constexpr int32_t kSplitLaunches = 2;   // GEMV gate/up and down of a per-segment split
 
 // Bounded device waits: default limit, and the short limit used with
 // DS4G_DEBUG_STALL.

@@ -224,30 +224,6 @@ __global__ void __launch_bounds__(256) combine_kernel(LayerArgs a)
     }
 }
 
-// Gate/up in the W_gate / W_up format, down in the W_down format (they may
-// differ: the shipping mix has codebook gate/up and Q2_K down).
-cudaError_t launch_gemv_kernels(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
-                                const cudaEvent_t *ev)
-{
-    const int persistent = dev.sm_count * 8;
-    const int gu_items = min(a.E, a.A) * (a.I_pad / kWarps);
-    const int dn_items = min(a.E, a.A) * (a.H / kWarps);
-    if (a.gu_format == DS4G_FMT_Q2K)
-        gateup_kernel<DS4G_FMT_Q2K><<<min(gu_items, persistent), kWarps * 32, 0, s>>>(a);
-    else
-        gateup_kernel<DS4G_FMT_CB2><<<min(gu_items, persistent), kWarps * 32, 0, s>>>(a);
-    if (ev && record_phase(ev[2], s) != cudaSuccess) return cudaGetLastError();
-    if (a.dn_format == DS4G_FMT_Q2K)
-        down_kernel<DS4G_FMT_Q2K><<<min(dn_items, persistent), kWarps * 32, 0, s>>>(a);
-    else
-        down_kernel<DS4G_FMT_CB2><<<min(dn_items, persistent), kWarps * 32, 0, s>>>(a);
-    if (ev && record_phase(ev[3], s) != cudaSuccess) return cudaGetLastError();
-    cudaError_t e = launch_combine(a, dev, s);
-    if (e != cudaSuccess) return e;
-    if (ev && record_phase(ev[4], s) != cudaSuccess) return cudaGetLastError();
-    return cudaGetLastError();
-}
-
 }  // namespace
 
 cudaError_t launch_combine(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s)
@@ -259,10 +235,39 @@ cudaError_t launch_combine(const LayerArgs &a, const DeviceInfo &dev, cudaStream
     return cudaGetLastError();
 }
 
-cudaError_t launch_gemv_path(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
-                             const cudaEvent_t *events)
+// Gate/up in the W_gate / W_up format, down in the W_down format (they may
+// differ: the shipping mix has codebook gate/up and Q2_K down).
+cudaError_t launch_gemv_gateup(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s)
 {
-    return launch_gemv_kernels(a, dev, s, events);
+    const int grid = min(min(a.E, a.A) * (a.I_pad / kWarps), dev.sm_count * 8);
+    if (a.gu_format == DS4G_FMT_Q2K)
+        gateup_kernel<DS4G_FMT_Q2K><<<grid, kWarps * 32, 0, s>>>(a);
+    else
+        gateup_kernel<DS4G_FMT_CB2><<<grid, kWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_down(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s)
+{
+    const int grid = min(min(a.E, a.A) * (a.H / kWarps), dev.sm_count * 8);
+    if (a.dn_format == DS4G_FMT_Q2K)
+        down_kernel<DS4G_FMT_Q2K><<<grid, kWarps * 32, 0, s>>>(a);
+    else
+        down_kernel<DS4G_FMT_CB2><<<grid, kWarps * 32, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gemv_path(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s,
+                             const cudaEvent_t *ev)
+{
+    cudaError_t e;
+    if ((e = launch_gemv_gateup(a, dev, s)) != cudaSuccess) return e;
+    if (ev && (e = record_phase(ev[2], s)) != cudaSuccess) return e;
+    if ((e = launch_gemv_down(a, dev, s)) != cudaSuccess) return e;
+    if (ev && (e = record_phase(ev[3], s)) != cudaSuccess) return e;
+    if ((e = launch_combine(a, dev, s)) != cudaSuccess) return e;
+    if (ev && (e = record_phase(ev[4], s)) != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 int32_t gemv_path_launches(const Plan &) { return 3; }

@@ -691,8 +691,11 @@ __global__ void __launch_bounds__(256) token_exp_kernel(const uint16_t *__restri
 }
 
 // Token tiles of every active segment and the activation gather:
-//   tiles[j] = (expert, first segment row, rows <= kNT, 0), heaviest expert
-//   segments are not reordered; *n_tiles = count; wseg[p] = wts[perm[p]];
+//   tiles[j] = (expert, first segment row, rows <= kNT, 0) for the segments
+//   of at least min_tokens rows, in expert order; *n_tiles = count; the
+//   shorter non-empty segments' experts in light[0 .. *n_light) (the GEMV
+//   kernels take those; min_tokens 0 sends every segment to the tiles);
+//   wseg[p] = wts[perm[p]];
 //   eseg[p] = texp[perm[p] / k];
 //   xseg[p, :] = fp16(x[perm[p] / k, :] * 2^-eseg[p]), for Q2_K with element
 //   16b + l of every aligned group of 32 at position 2l + b (perm32), in
@@ -707,7 +710,9 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
                                                       const float *__restrict__ wts,
                                                       float *__restrict__ wseg,
                                                       const int32_t *__restrict__ texp,
-                                                      int32_t *__restrict__ eseg)
+                                                      int32_t *__restrict__ eseg, int min_tokens,
+                                                      int32_t *__restrict__ light,
+                                                      int32_t *__restrict__ n_light)
 {
     for (int p = blockIdx.x * blockDim.x + threadIdx.x; p < A; p += gridDim.x * blockDim.x) {
         wseg[p] = wts[perm[p]];
@@ -717,16 +722,19 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
         __shared__ int s_nt[DS4G_MAX_EXPERTS];
         __shared__ int s_base[DS4G_MAX_EXPERTS + 1];
         const int e = threadIdx.x;
-        if (e < DS4G_MAX_EXPERTS) s_nt[e] = e < E ? (counts[e] + kNT - 1) / kNT : 0;
+        if (e < DS4G_MAX_EXPERTS)
+            s_nt[e] = e < E && counts[e] >= min_tokens ? (counts[e] + kNT - 1) / kNT : 0;
         __syncthreads();
         if (threadIdx.x == 0) {
-            int run = 0;
+            int run = 0, nl = 0;
             for (int i = 0; i < E; ++i) {
                 s_base[i] = run;
                 run += s_nt[i];
+                if (counts[i] > 0 && counts[i] < min_tokens) light[nl++] = i;
             }
             s_base[E] = run;
             *n_tiles = run;
+            *n_light = nl;
         }
         __syncthreads();
         if (e < E) {
@@ -884,7 +892,7 @@ cudaError_t launch_tc_prep(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     tc_prep_kernel<<<prep_grid, 256, 0, s>>>(la.x, la.H, la.k, la.A, la.perm, la.counts,
                                              la.offsets, la.E, tb.xseg, tb.tiles, tb.n_tiles,
                                              la.gu_format == DS4G_FMT_Q2K ? 1 : 0, la.wts, tb.wseg,
-                                             tb.texp, tb.eseg);
+                                             tb.texp, tb.eseg, tb.min_tokens, tb.light, tb.n_light);
     return cudaGetLastError();
 }
 
@@ -918,10 +926,16 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     a.m_tiles = la.I_pad / kBM;
     a.codebook = la.codebook;
     a.h_perm32 = la.dn_format == DS4G_FMT_Q2K ? 1 : 0;
+    // per-segment split: the light segments' experts on the GEMV kernels
+    LayerArgs lg = la;
+    lg.active = tb.light;
+    lg.n_active = tb.n_light;
+    const bool split = tb.min_tokens > 0;
     if ((e = la.gu_format == DS4G_FMT_CB2
                  ? launch_tc<0, DS4G_FMT_CB2>(m_gate, m_up, m_x, a, dev.sm_count, s)
                  : launch_tc<0, DS4G_FMT_Q2K>(m_gate, m_up, m_x, a, dev.sm_count, s)) != cudaSuccess)
         return e;
+    if (split && (e = launch_gemv_gateup(lg, dev, s)) != cudaSuccess) return e;
     if (ev && (e = record_phase(ev[2], s)) != cudaSuccess) return e;
 
     a.K = la.I_pad;
@@ -930,6 +944,7 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
                  ? launch_tc<1, DS4G_FMT_CB2>(m_down, m_down, m_h, a, dev.sm_count, s)
                  : launch_tc<1, DS4G_FMT_Q2K>(m_down, m_down, m_h, a, dev.sm_count, s)) != cudaSuccess)
         return e;
+    if (split && (e = launch_gemv_down(lg, dev, s)) != cudaSuccess) return e;
     if (ev && (e = record_phase(ev[3], s)) != cudaSuccess) return e;
 
     if ((e = launch_combine(la, dev, s)) != cudaSuccess) return e;

@@ -129,9 +129,12 @@ enum {
  *   expert strides >= rows * row_bytes and multiples of 16;
  *   w_gate, w_up, w_down 16-byte aligned;
  *   DS4G_FORCE_TC additionally needs row_bytes % 16 == 0.
- * tc_min_tokens: reserved for a per-segment split between the tensor-core
- * and the GEMV kernels; validated (>= 0) and otherwise ignored: every
- * segment of a call takes the path chosen for the call (see "Path" under
+ * tc_min_tokens: the per-segment split of calls that take the tensor-core
+ * kernels.  0 (the default): every expert segment runs on them.  N > 0:
+ * segments of fewer than N tokens run on the GEMV kernels instead, in the
+ * same call (the tensor-core kernels take the others; both write the same
+ * per-assignment buffer, summed in slot order as usual).  Calls that take
+ * the decode or GEMV kernels as a whole ignore it (see "Path" under
  * ds4g_moe_forward).
  * format / down_format: the block format of W_gate and W_up / of W_down.
  * The shipping mix of the ds4 weights is DS4G_FMT_CB2 / DS4G_FMT_Q2K

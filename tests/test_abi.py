@@ -169,7 +169,7 @@ def test_routing_view_points_inside_the_workspace():
     st, _ = D.moe_routing_view(d, 4, FAKE, need - 1)
     assert st == D.ERR_WORKSPACE
 
-def layer_desc(H, I, E, k, fmt=None, flags=0, align=1, down_fmt=None):
+def layer_desc(H, I, E, k, fmt=None, flags=0, align=1, down_fmt=None, tc_min_tokens=0):
     """A descriptor with packed (or `align`-padded) rows at a fake address;
     W_down in `down_fmt` (default: fmt)."""
     fmt = D.FMT_Q2K if fmt is None else fmt
@@ -179,7 +179,7 @@ def layer_desc(H, I, E, k, fmt=None, flags=0, align=1, down_fmt=None):
     gr, dr = H // 256 * bb, -(-I // 256) * dbb
     gr, dr = -(-gr // align) * align, -(-dr // align) * align
     return desc(hidden=H, inter=I, n_experts=E, top_k=k, format=fmt, down_format=down_fmt,
-                flags=flags, gate_up_row_bytes=gr, down_row_bytes=dr,
+                flags=flags, tc_min_tokens=tc_min_tokens, gate_up_row_bytes=gr, down_row_bytes=dr,
                 gate_up_expert_stride=-(-I * gr // 16) * 16,
                 down_expert_stride=-(-H * dr // 16) * 16,
                 codebook=FAKE if D.FMT_CB2 in (fmt, down_fmt) else None)
@@ -222,6 +222,9 @@ def test_mixed_format_descriptor_is_accepted():
     ((4096, 1536, 64, 6), 1, dict(flags=D.FORCE_GEMV), 2),
     ((7168, 2048, 256, 8), 100, dict(flags=D.FORCE_GEMV), 2 + 3),
     ((4096, 1536, 64, 6), 1, dict(flags=D.FORCE_TC), 0),
+    # per-segment split on the tensor-core path: + GEMV gate/up and down
+    ((7168, 2048, 256, 8), 2048, dict(tc_min_tokens=16), 2 + 5 + 2),
+    ((7168, 2048, 256, 8), 16, dict(tc_min_tokens=16), 2),        # decode kernels: no split
 ])
 def test_path_choice_by_launch_count(shape, T, kw, launches):
     """The per-call path choice documented under ds4g_moe_forward ("Path"),

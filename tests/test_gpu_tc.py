@@ -108,3 +108,26 @@ def test_mixed_format_layers(orc, kw):
     check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
     yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
     check_output(y, yref)
+
+
+@pytest.mark.parametrize("theta,fmt", [(8, S.FMT_Q2K), (8, S.FMT_CB2), (1000, S.FMT_Q2K),
+                                        (1, S.FMT_CB2)],
+                         ids=["q2k_theta8", "cb2_theta8", "all_light", "all_heavy"])
+def test_per_segment_split(orc, theta, fmt):
+    """tc_min_tokens = theta: segments of fewer than theta tokens run on the
+    GEMV kernels, the others on the tensor-core kernels, in one call.  The
+    layer's biased routing gives both kinds (with theta 8); theta 1000 sends
+    every segment to the GEMV kernels, theta 1 none."""
+    layer = P.small_layer(seed=4000 + theta, H=1024, I=384, E=24, k=4, T=96, fmt=fmt, align=16,
+                          score=S.SCORE_SIGMOID, logits_kind=S.LOGITS_BIASED)
+    counts = orc.route(layer["logits"], layer["top_k"], layer["score"])["counts"]
+    if theta == 8:
+        assert (counts >= 8).any() and ((counts > 0) & (counts < 8)).any()
+    L = to_device(layer, tc_min_tokens=theta)
+    y, routing = run_forward(L, layer["x"], layer["logits"])
+    check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    check_output(y, yref)
+    # the split result is deterministic too
+    y2, _ = run_forward(L, layer["x"], layer["logits"])
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
