@@ -442,7 +442,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     __shared__ __align__(8) uint64_t full[kStages], empty[kStages], afull[2], aempty[2];
-    __shared__ __align__(8) uint64_t accfull, accempty, drain[kIssuers];
+    __shared__ __align__(8) uint64_t accfull[2], accempty[2], drain[kIssuers];
     __shared__ uint32_t s_tmem;
     __shared__ int s_abort, s_issued;
 
@@ -456,8 +456,12 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
             ptx::mbar_init(&afull[b], kDequantWarps);
             ptx::mbar_init(&aempty[b], 1);
         }
-        ptx::mbar_init(&accfull, kIssuers);
-        ptx::mbar_init(&accempty, MODE == 0 ? kDequantWarps : kEpilogueWarps);
+        // gate/up: one accumulator pair, both issuers commit; down: two
+        // alternating accumulators, one issuer
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&accfull[b], MODE == 0 ? kIssuers : 1);
+            ptx::mbar_init(&accempty[b], MODE == 0 ? kDequantWarps : kEpilogueWarps);
+        }
         for (int i = 0; i < kIssuers; ++i) ptx::mbar_init(&drain[i], 1);
         ptx::fence_mbar_init();
         s_abort = 0;
@@ -540,41 +544,47 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         }
     } else if (warp < kFirstDequantWarp) {
         // ---------------- MMA issuers ----------------
-        // Issuer X owns A buffer X and accumulator X and issues every fill
-        // with (global fill index) % 2 == X: in the gate/up kernel the W_gate
-        // (X = 0) or W_up (X = 1) fill of every K step, in the down kernel
-        // every other K step (accumulator X holds the K steps of its parity;
-        // the epilogue adds the two in a fixed order).  One thread cannot
-        // issue tcgen05.mma faster than about one per 55 cycles, which is
+        // Gate/up kernel: issuer X owns A buffer X and accumulator X and
+        // issues the W_gate (X = 0) or W_up (X = 1) fill of every K step.  One
+        // thread cannot issue tcgen05.mma faster than about one per 55 cycles,
         // slower than the tensor pipe at the token counts of a segment; two
-        // issuers keep it fed.  The whole warp runs the loop; lane 0 issues.
+        // issuers keep it fed.  Down kernel (one fill per K step, bound by its
+        // dequantizers): issuer 0 alone, with two accumulators that alternate
+        // per item, so the epilogue warps drain one while the next item
+        // accumulates.  The whole warp runs the loop; lane 0 issues.
         const int X = warp - 1;
+        if (MODE == 1 && X == 1) {
+            // no second issuer in the down kernel
+        } else {
         const uint64_t desc0 = ptx::sw128_desc(ptx::smem_addr(smem));
-        const uint32_t acc = tmem + kAccCol + 128u * (uint32_t)X;
         int sc = 0, nx = 0, ic = 0;                  // stages, fills of this issuer, items
         bool ok = true;
         for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
             const int tile = it / a.m_tiles;
             const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
             const uint32_t idesc = ptx::idesc_f16(kBM, nb * kBoxRows);
-            if (ic > 0) {
-                ok = wait_bar(&accempty, (ic - 1) & 1, a.wait_ns, abort_flag);
+            const int ab = MODE == 1 ? (ic & 1) : 0;
+            const int uses = MODE == 1 ? (ic >> 1) : ic;
+            if (uses > 0) {
+                ok = wait_bar(&accempty[ab], (uses - 1) & 1, a.wait_ns, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
             }
             ptx::tc_fence_after();
+            const uint32_t acc = tmem + kAccCol + 128u * (uint32_t)(MODE == 1 ? ab : X);
             bool first = true;
             for (int kb = 0; ok && kb < KB; ++kb, ++sc) {
-                // gate/up: every stage has this issuer's fill; down: stages of parity X
-                if (MODE == 1 && (sc & 1) != X) continue;
                 const int s = sc % kStages;
+                // gate/up: this issuer's fill of the stage; down: the stage's fill
+                const int b = MODE == 1 ? (sc & 1) : X;
                 ok = wait_bar(&full[s], (sc / kStages) & 1, a.wait_ns, abort_flag);
-                ok = ok && wait_bar(&afull[X], nx & 1, a.wait_ns, abort_flag);
+                ok = ok && wait_bar(&afull[b], (MODE == 1 ? (sc >> 1) : nx) & 1, a.wait_ns,
+                                    abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
                 ptx::tc_fence_after();
                 const uint64_t dst = desc0 + (uint64_t)((s * kStageBytes) >> 4);
-                const uint32_t a_buf = tmem + (uint32_t)X * 128u;
+                const uint32_t a_buf = tmem + (uint32_t)b * 128u;
                 if (lane == 0) {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -583,7 +593,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                             dst + (uint64_t)(((kk >> 6) * kChunkBytes + (kk & 63) * 2) >> 4);
                         ptx::mma_f16_ts(acc, a_buf + 8 * i, bd, idesc, !(first && i == 0));
                     }
-                    ptx::mma_commit(&aempty[X]);
+                    ptx::mma_commit(&aempty[b]);
                     ptx::mma_commit(&empty[s]);
                 }
                 __syncwarp();
@@ -591,7 +601,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                 ++nx;
             }
             if (!ok) break;
-            if (lane == 0) ptx::mma_commit(&accfull);
+            if (lane == 0) ptx::mma_commit(&accfull[ab]);
             __syncwarp();
         }
         if (!ok && lane == 0) {
@@ -605,6 +615,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
             ptx::mbar_wait(&drain[X], 0, a.wait_ns);
         }
         __syncwarp();
+        }
     } else if (warp >= kFirstDequantWarp + kDequantWarps) {
         // ---------------- down epilogue warps (MODE 1) ----------------
         const int row = 32 * (warp & 3) + lane;
@@ -614,35 +625,30 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
             const int tile = it / a.m_tiles, mt = it % a.m_tiles;
             const int row0 = a.tiles[4 * tile + 1], nlen = a.tiles[4 * tile + 2];
-            ok = wait_bar(&accfull, ic & 1, a.wait_ns, abort_flag);
+            const int ab = ic & 1;
+            ok = wait_bar(&accfull[ab], (ic >> 1) & 1, a.wait_ns, abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) break;
             ptx::tc_fence_after();
-            // accumulator X holds the item's K steps of stage parity X; with a
-            // single K step only one of them was written
-            const int sc0 = ic * KB;
-            const bool use0 = KB > 1 || (sc0 & 1) == 0, use1 = KB > 1 || (sc0 & 1) == 1;
             const int m = mt * kBM + row;
-            const uint32_t acc = tmem + lane_base + kAccCol;
+            const uint32_t acc = tmem + lane_base + kAccCol + 128u * ab;
             for (int c = 0; 8 * c < nlen; ++c) {
-                float o0[8], o1[8];
-                ptx::tmem_ld8(acc + 8 * c, o0);
-                ptx::tmem_ld8(acc + 128 + 8 * c, o1);
+                float o[8];
+                ptx::tmem_ld8(acc + 8 * c, o);
                 ptx::tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     const int t = 8 * c + j;
                     if (t < nlen) {
                         const int pos = row0 + t;
-                        const float o = (use0 ? o0[j] : 0.0f) + (use1 ? o1[j] : 0.0f);
                         const float sh = exp2i(2 * __ldg(a.eseg + pos) + kHExpOffset);
-                        a.yslot[(size_t)pos * a.H + m] = __ldg(a.wseg + pos) * (o * sh);
+                        a.yslot[(size_t)pos * a.H + m] = __ldg(a.wseg + pos) * (o[j] * sh);
                     }
                 }
             }
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&accempty);
+            if (lane == 0) ptx::mbar_arrive(&accempty[ab]);
         }
         if (!ok) {
             if (lane == 0) set_status(a.status, DS4G_ERR_TIMEOUT);
@@ -650,7 +656,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         }
     } else {
         // ---------------- dequantizers / gate-up epilogue ----------------
-        const TcCta cta{smem, full, empty, afull, aempty, &accfull, &accempty, tmem,
+        const TcCta cta{smem, full, empty, afull, aempty, accfull, accempty, tmem,
                         ptx::smem_addr(cbrep), abort_flag, n_items, KB};
         DequantRole<MODE, FMT>(a, cta, warp, lane, (warp - kFirstDequantWarp) >> 2).run();
     }
