@@ -13,26 +13,40 @@
 // rows).  The weights are the MMA's M side, the tokens its N side, so one
 // dequantized weight serves every token of the tile.
 //
+// The pipeline unit is the half block: 128 weights of every row of the item
+// (one half of a 256-weight super-block), one fill of a 64-column A buffer in
+// tensor memory, eight K = 16 MMAs.  Each half has its own team of
+// dequantizing warps and its own two A buffers, so a buffer is dequantized
+// again only after the team's other fill: the time one thread needs to issue
+// a fill's MMAs (about 100-150 cycles per tcgen05.mma while the dequantizing
+// warps run, whatever the token count) and their completion overlap the
+// dequantization of the next fill, and the two teams' hand-off latencies
+// (tensor-memory stores, barrier arrivals and waits) overlap each other's
+// arithmetic.
+//
 // Roles inside a CTA (one CTA per SM, persistent over the items):
-//   warp 0     TMA producer: per 256-wide K step, the 16-byte aligned window
-//              of each weight row's super-block (a 3-D tensor map over
-//              [experts][rows][row words]) and the activation tile (a 2-D
-//              tensor map over [segment rows][K], fp16, 128-byte swizzle)
-//              land in a two-stage shared-memory ring;
-//   warp 1     MMA issuer: tcgen05.mma kind::f16, A (dequantized weights)
+//   warp 0     weight producer: per 256-wide K step, the 16-byte aligned
+//              window of each weight row's super-block (a 3-D tensor map
+//              over [experts][rows][row words]) into a ring of window stages
+//              that the dequantizers release once they have read them; the
+//              windows a few K steps ahead are prefetched into L2;
+//   warp 1     activation producer: per half K step, the activation tile
+//              (a 2-D tensor map over [segment rows][K], fp16, 128-byte
+//              swizzle) into a ring of half stages that the MMAs release;
+//   warps 2-3  MMA issuers: tcgen05.mma kind::f16, A (dequantized weights)
 //              from tensor memory, B (activations) from shared memory, fp32
-//              accumulators in tensor memory;
-//   warps 2-17 dequantizers, four warpgroups of four warps: each thread owns
-//              one weight row and, per fill of an A buffer, one quarter of
-//              it (32 columns = 64 weights): gate/up kernel warpgroup w is
-//              (matrix w/2, field pair w%2) of the fill's half super-block,
-//              down kernel warpgroup w is (half w/2, field pair w%2) of the
-//              K step's block.  It forms fp16 weights in registers and
-//              stores them to tensor memory (tcgen05.st).  In the gate/up
-//              kernel the sixteen warps are also the epilogue after each
-//              item (tcgen05.ld of the accumulators, SiLU*up, fp16 stores
-//              of h);
-//   warps 18-21  down kernel only: the epilogue (tcgen05.ld, routing weight,
+//              accumulators in tensor memory.  Gate/up kernel: warp 2 issues
+//              every W_gate fill, warp 3 every W_up fill.  Down kernel: warp
+//              2 alone;
+//   warps 4-19 dequantizers, two teams (halves 0 and 1) of two warpgroups:
+//              each thread owns one weight row and, per fill, one quarter of
+//              the block, the field pair 2*gh, 2*gh+1 (Q2_K) or weights 64*gh
+//              .. +63 (codebook) of its team's half: 64 weights, 32 fp16
+//              pairs formed in registers and stored to tensor memory
+//              (tcgen05.st).  In the gate/up kernel the sixteen warps are
+//              also the epilogue after each item (tcgen05.ld of the
+//              accumulators, SiLU*up, fp16 stores of h);
+//   warps 20-23  down kernel only: the epilogue (tcgen05.ld, routing weight,
 //              fp32 stores of yslot), on double-buffered accumulators so
 //              the next item's MMAs overlap it.
 //
@@ -48,13 +62,12 @@
 // codebook in shared memory, c*s is formed exactly in fp16 and the single
 // rounding is the multiply by d.
 //
-// Tensor memory (512 columns): columns 0..255 are two A buffers of 128
-// columns (K = 128 fp16 per matrix-half pair, or K = 256 of one matrix);
-// columns 256..383 and 384..511 are the fp32 accumulators (gate and up, or
-// the down kernel's two alternating accumulators).  Every mbarrier wait is
-// bounded; on expiry the kernel records DS4G_ERR_TIMEOUT in the status word,
-// lets every role leave its loop, drains its own copies and MMAs (bounded)
-// and frees its tensor memory.
+// Tensor memory (512 columns): columns 0..255 are the four A buffers of 64
+// columns (K = 128 fp16), 2hh and 2hh+1 for half hh; columns 256..383 and 384..511 are the fp32
+// accumulators (gate and up, or the down kernel's two alternating
+// accumulators).  Every mbarrier wait is bounded; on expiry the kernel
+// records DS4G_ERR_TIMEOUT in the status word, lets every role leave its
+// loop, drains its own copies and MMAs (bounded) and frees its tensor memory.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -70,19 +83,42 @@ namespace {
 constexpr int kBM = 128;                  // weight rows per item (MMA M)
 constexpr int kNT = kTcTileTokens;        // tokens per item at most (MMA N)
 constexpr int kBoxRows = 16;              // token rows per activation TMA box
-constexpr int kStages = 2;
 constexpr int kWinWords = 28;             // 112-byte window per weight row
 constexpr int kAqBytes = kWinWords * 4 * kBM;
 constexpr int kChunkBytes = kNT * 128;    // one 64-wide K chunk of the activation tile
-constexpr int kBBytes = 4 * kChunkBytes;
-constexpr int kDequantWarps = 16;          // four warpgroups
-constexpr int kEpilogueWarps = 4;          // down kernel: dedicated epilogue warps
+constexpr int kHalfBytes = 2 * kChunkBytes;   // activation half stage: K = 128
+constexpr int kHalfMmas = 8;              // K = 16 MMAs per half block
+constexpr int kABufs = 4;                 // A buffers of 64 columns
+constexpr int kDequantWarps = 16;         // two teams of two warpgroups
+constexpr int kTeamWarps = 8;             // one team fills half hh = team of every block
+constexpr int kEpilogueWarps = 4;         // down kernel: dedicated epilogue warps
+constexpr int kIssuers = 2;
+// warps: 0 weight producer, 1 activation producer, 2-3 MMA issuers, then the
+// dequantizers, then (down kernel) the epilogue warps
+constexpr int kFirstIssuerWarp = 2;
+constexpr int kFirstDequantWarp = kFirstIssuerWarp + kIssuers;
 __host__ __device__ constexpr int tc_threads(int mode)
 {
-    return (3 + kDequantWarps + (mode == 1 ? kEpilogueWarps : 0)) * 32;   // producer, 2 issuers
+    return (kFirstDequantWarp + kDequantWarps + (mode == 1 ? kEpilogueWarps : 0)) * 32;
 }
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol = 256;
+constexpr int kCbCopies = 16;
+constexpr int kCbRepBytes = 256 * kCbCopies * 8;
+
+// Shared-memory rings of one kernel: kW window stages (one K step of every
+// matrix's windows), kB activation half stages; the codebook copy last.
+template <int MODE, int FMT>
+struct Ring {
+    static constexpr int NMAT = MODE == 0 ? 2 : 1;
+    static constexpr int kW = MODE == 0 ? (FMT == DS4G_FMT_Q2K ? 3 : 2) : 4;
+    static constexpr int kB = MODE == 1 && FMT == DS4G_FMT_Q2K ? 5 : 4;
+    static constexpr uint32_t kWStageBytes = NMAT * kAqBytes;
+    static constexpr size_t kWOff = (size_t)kB * kHalfBytes;
+    static constexpr size_t kCbOff = kWOff + (size_t)kW * kWStageBytes;
+    static constexpr size_t kBytes = kCbOff + (FMT == DS4G_FMT_CB2 ? kCbRepBytes : 0);
+    static_assert(kBytes + 1024 <= 225 * 1024, "shared-memory rings exceed the per-CTA limit");
+};
 
 struct TcArgs {
     int K;                      // contraction length: hidden, or I_pad
@@ -98,7 +134,7 @@ struct TcArgs {
     const int8_t *codebook;     // [256 x 8] int8 (codebook format)
     int32_t *status;
     uint64_t wait_ns;
-    int stall;                  // debug: the producer issues nothing (tests the bounded waits)
+    int stall;                  // debug: the producers issue nothing (tests the bounded waits)
 };
 
 // K position of element n inside its aligned group of 32 (Q2_K operands):
@@ -127,8 +163,8 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, uint64_
 }
 
 // Per-warp constants of the dequantizing role: this warp's quarter of every
-// fill is half HH, field pair GH (Q2_K) / 64-weight half GH (codebook) of
-// the block, columns 32 * (2*HH + GH) .. +31 of the A buffer.
+// block is half HH, field pair GH (Q2_K) / 64-weight half GH (codebook),
+// columns 32 * GH .. +31 of the half's A buffer.
 struct QuarterConst {
     int hh, gh;
     uint32_t mask[2];           // Q2_K: 2-bit field masks of g = 2*gh, 2*gh+1 (both lanes)
@@ -222,9 +258,6 @@ __device__ __forceinline__ void q2k_quarter(const uint32_t (&qw)[12], uint32_t s
 // for the funnel shift), `tw`: the words holding sc and d; `fs`: the block's
 // bit offset inside its first word.
 // ---------------------------------------------------------------------------
-constexpr int kCbCopies = 16;
-constexpr int kCbRepBytes = 256 * kCbCopies * 8;
-
 __device__ __forceinline__ void cb2_quarter(const uint32_t (&iw)[3], const uint32_t (&gw)[3],
                                             const uint32_t (&tw)[3], uint32_t fs, int hh, int gh,
                                             uint32_t cb_lane, uint32_t (&out)[32])
@@ -264,32 +297,34 @@ __device__ __forceinline__ void cb2_quarter(const uint32_t (&iw)[3], const uint3
 
 // Shared state of one CTA of tc_kernel (barriers, tensor memory, abort flag).
 struct TcCta {
-    uint8_t *smem;
-    uint64_t *full, *empty, *afull, *aempty, *accfull, *accempty;
+    uint8_t *wring;             // window stages
+    uint64_t *wfull, *wempty, *afull, *aempty, *accfull, *accempty;
     uint32_t tmem;
     uint32_t cbrep;             // shared address of the replicated codebook
     volatile int *abort_flag;
     int n_items, KB;
 };
 
-// The dequantizing role of one warp (both kernels).  Every fill of an A
-// buffer is one matrix's whole block (K = 256, 128 columns): the gate/up
-// kernel fills W_gate then W_up per K step, the down kernel W_down.  This
-// warp's quarter is fixed (QuarterConst); the block's offset inside its
-// 16-byte aligned window (repeating every 4 K steps for Q2_K, 8 for the
-// codebook format) is dispatched once per fill to a body where it is a
-// compile-time constant, so all warps share the same few bodies.
+// The dequantizing role of one warp (both kernels).  Team hh (warpgroups
+// 2hh, 2hh+1) fills half hh of every block: per K step the W_gate and W_up
+// halves into A buffers 2hh and 2hh+1 (gate/up kernel), or the W_down half
+// into A buffer 2hh + (K step & 1) (down kernel).  The two teams run
+// independently, so one team's hand-off latencies overlap the other's
+// arithmetic.  The block's offset inside its 16-byte aligned window
+// (repeating every 4 K steps for Q2_K) is dispatched once per fill to a
+// body where it is a compile-time constant, so all warps share the same few
+// bodies.
 template <int MODE, int FMT>
 struct DequantRole {
-    static constexpr int NMAT = MODE == 0 ? 2 : 1;
-    static constexpr uint32_t kStageBytes = kBBytes + NMAT * kAqBytes;
+    using R = Ring<MODE, FMT>;
+    static constexpr int NMAT = R::NMAT;
 
     const TcArgs &a;
     const TcCta &c;
     QuarterConst k;
     int lane, row, wg;
     uint32_t lane_base;
-    int sc = 0, fc = 0;
+    int kc = 0;                 // K steps done
     bool ok = true;
 
     __device__ __forceinline__ DequantRole(const TcArgs &a_, const TcCta &c_, int warp, int lane_,
@@ -337,17 +372,18 @@ struct DequantRole {
                     c.cbrep + (uint32_t)(lane & 15) * 8, out);
     }
 
-    // One fill: matrix `mat` of K step kb from stage s.
-    __device__ __forceinline__ void fill(int s, int mat, int kb)
+    // One fill: this team's half of matrix `mat`, K step kb, window stage ws.
+    __device__ __forceinline__ void fill(int ws, int mat, int kb)
     {
-        const int buf = fc & 1;
-        if (fc >= 2) {
-            ok = wait_bar(&c.aempty[buf], ((fc >> 1) - 1) & 1, a.wait_ns, c.abort_flag);
+        const int buf = 2 * k.hh + (MODE == 0 ? mat : (kc & 1));
+        const int uses = MODE == 0 ? kc : (kc >> 1);      // earlier fills of the buffer
+        if (uses > 0) {
+            ok = wait_bar(&c.aempty[buf], (uses - 1) & 1, a.wait_ns, c.abort_flag);
             ok = __all_sync(0xffffffffu, ok);
             if (!ok) return;
             ptx::tc_fence_after();
         }
-        const uint8_t *win = c.smem + (size_t)s * kStageBytes + kBBytes + mat * kAqBytes +
+        const uint8_t *win = c.wring + (size_t)ws * R::kWStageBytes + mat * kAqBytes +
                              row * (kWinWords * 4);
         uint32_t out[32];
         if (FMT == DS4G_FMT_Q2K) {
@@ -360,12 +396,11 @@ struct DequantRole {
         } else {
             cb2_fill(win, (kCB2Bytes * kb) & 15, out);
         }
-        ptx::tmem_st32(c.tmem + lane_base + (uint32_t)buf * 128u + 32u * wg, out);
+        ptx::tmem_st32(c.tmem + lane_base + (uint32_t)buf * 64u + 32u * k.gh, out);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&c.afull[buf]);
-        ++fc;
     }
 
     __device__ __forceinline__ void run()
@@ -374,12 +409,16 @@ struct DequantRole {
         for (int it = blockIdx.x; ok && it < c.n_items; it += gridDim.x, ++ic) {
             const int tile = it / a.m_tiles, mt = it % a.m_tiles;
             const int row0 = a.tiles[4 * tile + 1], nlen = a.tiles[4 * tile + 2];
-            for (int kb = 0; ok && kb < c.KB; ++kb, ++sc) {
-                const int s = sc % kStages;
-                ok = wait_bar(&c.full[s], (sc / kStages) & 1, a.wait_ns, c.abort_flag);
+            for (int kb = 0; ok && kb < c.KB; ++kb, ++kc) {
+                const int ws = kc % R::kW;
+                ok = wait_bar(&c.wfull[ws], (kc / R::kW) & 1, a.wait_ns, c.abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                for (int mat = 0; ok && mat < NMAT; ++mat) fill(s, mat, kb);
+                for (int mat = 0; ok && mat < NMAT; ++mat) fill(ws, mat, kb);
+                if (!ok) break;
+                // this warp has read the stage's windows
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&c.wempty[ws]);
             }
             if (!ok) break;
             if (MODE == 1) continue;                 // the epilogue warps finish down items
@@ -422,38 +461,51 @@ struct DequantRole {
     }
 };
 
-// Weight-window prefetch distance of the producer, in K steps.
+// Weight-window prefetch distance of the weight producer, in K steps.
 constexpr int kPrefetchSteps = 6;
 
-// Warps of tc_kernel: 0 TMA producer, 1-2 MMA issuers, then the dequantizers,
-// then (down kernel) the epilogue warps.
-constexpr int kIssuers = 2;
-constexpr int kFirstDequantWarp = 1 + kIssuers;
+// After an abort: wait (bounded) for the copies still in flight on a ring
+// whose `issued` stages were armed in order.
+__device__ __forceinline__ void drain_ring(uint64_t *full, int ring, int issued, uint64_t wait_ns)
+{
+    for (int q = issued - ring; q < issued; ++q) {
+        if (q < 0) continue;
+        if (!ptx::mbar_wait(&full[q % ring], (q / ring) & 1, wait_ns)) break;
+    }
+}
 
 template <int MODE, int FMT>
 __global__ void __launch_bounds__(tc_threads(MODE), 1)
     tc_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
               const __grid_constant__ CUtensorMap tm_b, const TcArgs a)
 {
-    constexpr int NMAT = MODE == 0 ? 2 : 1;
-    constexpr uint32_t kStageBytes = kBBytes + NMAT * kAqBytes;
+    using R = Ring<MODE, FMT>;
+    constexpr int NMAT = R::NMAT;
     constexpr int kBlockBytes = FMT == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    __shared__ __align__(8) uint64_t full[kStages], empty[kStages], afull[2], aempty[2];
+    uint8_t *bring = smem;                      // activation half stages (1024-aligned)
+    uint8_t *wring = smem + R::kWOff;           // window stages
+    uint8_t *cbrep = smem + R::kCbOff;          // codebook format only
+    __shared__ __align__(8) uint64_t wfull[R::kW], wempty[R::kW], bfull[R::kB], bempty[R::kB];
+    __shared__ __align__(8) uint64_t afull[kABufs], aempty[kABufs];
     __shared__ __align__(8) uint64_t accfull[2], accempty[2], drain[kIssuers];
     __shared__ uint32_t s_tmem;
-    __shared__ int s_abort, s_issued;
+    __shared__ int s_abort, s_wissued, s_bissued;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            ptx::mbar_init(&full[s], 1);
-            ptx::mbar_init(&empty[s], NMAT);        // one commit per fill of the stage
+        for (int s = 0; s < R::kW; ++s) {
+            ptx::mbar_init(&wfull[s], 1);
+            ptx::mbar_init(&wempty[s], kDequantWarps);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(&afull[b], kDequantWarps);
+        for (int s = 0; s < R::kB; ++s) {
+            ptx::mbar_init(&bfull[s], 1);
+            ptx::mbar_init(&bempty[s], NMAT);       // one commit per issuer
+        }
+        for (int b = 0; b < kABufs; ++b) {
+            ptx::mbar_init(&afull[b], kTeamWarps);
             ptx::mbar_init(&aempty[b], 1);
         }
         // gate/up: one accumulator pair, both issuers commit; down: two
@@ -465,13 +517,13 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         for (int i = 0; i < kIssuers; ++i) ptx::mbar_init(&drain[i], 1);
         ptx::fence_mbar_init();
         s_abort = 0;
-        s_issued = 0;
+        s_wissued = 0;
+        s_bissued = 0;
     }
     if (warp == 1) {
         ptx::tmem_alloc(&s_tmem, kTmemCols);
         ptx::tmem_relinquish();
     }
-    uint8_t *cbrep = smem + (size_t)kStages * kStageBytes;    // codebook format only
     if (FMT == DS4G_FMT_CB2) {
         for (int i = threadIdx.x; i < 256 * kCbCopies; i += blockDim.x) {
             const int r = i / kCbCopies, cpy = i % kCbCopies;
@@ -490,13 +542,12 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
     const int KB = a.K / kQK;
 
     if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        // The weight windows of the K step kPrefetchSteps ahead are also
-        // prefetched into L2, so the ring's copies of them hit L2.
+        // ---------------- weight producer ----------------
+        // The windows of the K step kPrefetchSteps ahead are also prefetched
+        // into L2, so the ring's copies of them hit L2.
         if (lane == 0 && !a.stall) {
             ptx::prefetch_tmap(&tm_a0);
             if (NMAT == 2) ptx::prefetch_tmap(&tm_a1);
-            ptx::prefetch_tmap(&tm_b);
             int pf_it = blockIdx.x, pf_kb = 0;       // the prefetch cursor
             auto prefetch_next = [&]() {
                 if (pf_it >= n_items) return;
@@ -511,110 +562,136 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                 }
             };
             for (int i = 0; i < kPrefetchSteps; ++i) prefetch_next();
-            int sc = 0;
+            int wc = 0;
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const int tile = it / a.m_tiles, mt = it % a.m_tiles;
-                const int e = a.tiles[4 * tile], row0 = a.tiles[4 * tile + 1];
-                const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
-                const uint32_t bytes = NMAT * kAqBytes + 4u * nb * kBoxRows * 128u;
-                for (int kb = 0; kb < KB; ++kb, ++sc) {
-                    const int s = sc % kStages;
-                    if (sc >= kStages &&
-                        !wait_bar(&empty[s], ((sc / kStages) - 1) & 1, a.wait_ns, abort_flag)) {
-                        set_status(a.status, DS4G_ERR_TIMEOUT);
-                        *abort_flag = 1;
+                const int e = a.tiles[4 * tile];
+                for (int kb = 0; kb < KB; ++kb, ++wc) {
+                    const int s = wc % R::kW;
+                    if (wc >= R::kW &&
+                        !wait_bar(&wempty[s], ((wc / R::kW) - 1) & 1, a.wait_ns, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    uint8_t *st = smem + (size_t)s * kStageBytes;
-                    ptx::mbar_arrive_expect_tx(&full[s], bytes);
+                    uint8_t *st = wring + (size_t)s * R::kWStageBytes;
+                    ptx::mbar_arrive_expect_tx(&wfull[s], R::kWStageBytes);
                     const int x = ((kBlockBytes * kb) & ~15) / 4;
-                    ptx::tma_load_3d(st + kBBytes, &tm_a0, x, mt * kBM, e, &full[s]);
-                    if (NMAT == 2)
-                        ptx::tma_load_3d(st + kBBytes + kAqBytes, &tm_a1, x, mt * kBM, e, &full[s]);
-                    for (int kc = 0; kc < 4; ++kc)
-                        for (int r = 0; r < nb; ++r)
-                            ptx::tma_load_2d(st + kc * kChunkBytes + r * kBoxRows * 128, &tm_b,
-                                             kb * kQK + 64 * kc, row0 + kBoxRows * r, &full[s]);
-                    s_issued = sc + 1;
+                    ptx::tma_load_3d(st, &tm_a0, x, mt * kBM, e, &wfull[s]);
+                    if (NMAT == 2) ptx::tma_load_3d(st + kAqBytes, &tm_a1, x, mt * kBM, e, &wfull[s]);
                     prefetch_next();
                 }
             }
+            if (!ok) {
+                set_status(a.status, DS4G_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            s_wissued = wc;
+        }
+    } else if (warp == 1) {
+        // ---------------- activation producer ----------------
+        if (lane == 0 && !a.stall) {
+            ptx::prefetch_tmap(&tm_b);
+            int bc = 0;
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
+                const int tile = it / a.m_tiles;
+                const int row0 = a.tiles[4 * tile + 1];
+                const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
+                const uint32_t bytes = 2u * nb * kBoxRows * 128u;
+                for (int hs = 0; ok && hs < 2 * KB; ++hs, ++bc) {
+                    const int s = bc % R::kB;
+                    if (bc >= R::kB &&
+                        !wait_bar(&bempty[s], ((bc / R::kB) - 1) & 1, a.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = bring + (size_t)s * kHalfBytes;
+                    ptx::mbar_arrive_expect_tx(&bfull[s], bytes);
+                    for (int kc = 0; kc < 2; ++kc)
+                        for (int r = 0; r < nb; ++r)
+                            ptx::tma_load_2d(st + kc * kChunkBytes + r * kBoxRows * 128, &tm_b,
+                                             hs * 128 + 64 * kc, row0 + kBoxRows * r, &bfull[s]);
+                }
+            }
+            if (!ok) {
+                set_status(a.status, DS4G_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            s_bissued = bc;
         }
     } else if (warp < kFirstDequantWarp) {
         // ---------------- MMA issuers ----------------
-        // Gate/up kernel: issuer X owns A buffer X and accumulator X and
-        // issues the W_gate (X = 0) or W_up (X = 1) fill of every K step.  One
-        // thread cannot issue tcgen05.mma faster than about one per 55 cycles,
-        // slower than the tensor pipe at the token counts of a segment; two
-        // issuers keep it fed.  Down kernel (one fill per K step, bound by its
-        // dequantizers): issuer 0 alone, with two accumulators that alternate
-        // per item, so the epilogue warps drain one while the next item
-        // accumulates.  The whole warp runs the loop; lane 0 issues.
-        const int X = warp - 1;
+        // Gate/up kernel: issuer X issues the W_gate (X = 0) or W_up (X = 1)
+        // fills, A buffers X and 2 + X (halves 0 and 1), into accumulator X.
+        // One thread issues tcgen05.mma far slower than the tensor pipe runs
+        // them at a segment's token counts; two issuers keep it fed.  Down
+        // kernel (one fill per half step, bound by its dequantizers): issuer
+        // 0 alone, every A buffer in turn, with two accumulators that
+        // alternate per item, so the epilogue warps drain one while the next
+        // item accumulates.  The whole warp runs the loop; lane 0 issues.
+        const int X = warp - kFirstIssuerWarp;
         if (MODE == 1 && X == 1) {
             // no second issuer in the down kernel
         } else {
-        const uint64_t desc0 = ptx::sw128_desc(ptx::smem_addr(smem));
-        int sc = 0, nx = 0, ic = 0;                  // stages, fills of this issuer, items
-        bool ok = true;
-        for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
-            const int tile = it / a.m_tiles;
-            const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
-            const uint32_t idesc = ptx::idesc_f16(kBM, nb * kBoxRows);
-            const int ab = MODE == 1 ? (ic & 1) : 0;
-            const int uses = MODE == 1 ? (ic >> 1) : ic;
-            if (uses > 0) {
-                ok = wait_bar(&accempty[ab], (uses - 1) & 1, a.wait_ns, abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-            }
-            ptx::tc_fence_after();
-            const uint32_t acc = tmem + kAccCol + 128u * (uint32_t)(MODE == 1 ? ab : X);
-            bool first = true;
-            for (int kb = 0; ok && kb < KB; ++kb, ++sc) {
-                const int s = sc % kStages;
-                // gate/up: this issuer's fill of the stage; down: the stage's fill
-                const int b = MODE == 1 ? (sc & 1) : X;
-                ok = wait_bar(&full[s], (sc / kStages) & 1, a.wait_ns, abort_flag);
-                ok = ok && wait_bar(&afull[b], (MODE == 1 ? (sc >> 1) : nx) & 1, a.wait_ns,
-                                    abort_flag);
-                ok = __all_sync(0xffffffffu, ok);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                const uint64_t dst = desc0 + (uint64_t)((s * kStageBytes) >> 4);
-                const uint32_t a_buf = tmem + (uint32_t)b * 128u;
-                if (lane == 0) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int kk = 16 * i;
-                        const uint64_t bd =
-                            dst + (uint64_t)(((kk >> 6) * kChunkBytes + (kk & 63) * 2) >> 4);
-                        ptx::mma_f16_ts(acc, a_buf + 8 * i, bd, idesc, !(first && i == 0));
-                    }
-                    ptx::mma_commit(&aempty[b]);
-                    ptx::mma_commit(&empty[s]);
+            const uint64_t bdesc0 = ptx::sw128_desc(ptx::smem_addr(bring));
+            int hc = 0, ic = 0;                      // half steps, items
+            bool ok = true;
+            for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x, ++ic) {
+                const int tile = it / a.m_tiles;
+                const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
+                const uint32_t idesc = ptx::idesc_f16(kBM, nb * kBoxRows);
+                const int ab = MODE == 1 ? (ic & 1) : 0;
+                const int uses = MODE == 1 ? (ic >> 1) : ic;
+                if (uses > 0) {
+                    ok = wait_bar(&accempty[ab], (uses - 1) & 1, a.wait_ns, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
                 }
+                ptx::tc_fence_after();
+                const uint32_t acc = tmem + kAccCol + 128u * (uint32_t)(MODE == 1 ? ab : X);
+                for (int hs = 0; ok && hs < 2 * KB; ++hs, ++hc) {
+                    const int s = hc % R::kB;
+                    // the fill's A buffer (half hh of K step kc) and how often
+                    // it was filled before
+                    const int kc = hc >> 1, hh = hc & 1;
+                    const int buf = 2 * hh + (MODE == 0 ? X : (kc & 1));
+                    const int uses = MODE == 0 ? kc : (kc >> 1);
+                    ok = wait_bar(&bfull[s], (hc / R::kB) & 1, a.wait_ns, abort_flag);
+                    ok = ok && wait_bar(&afull[buf], uses & 1, a.wait_ns, abort_flag);
+                    ok = __all_sync(0xffffffffu, ok);
+                    if (!ok) break;
+                    ptx::tc_fence_after();
+                    const uint64_t bd0 = bdesc0 + (uint64_t)((s * kHalfBytes) >> 4);
+                    const uint32_t a_buf = tmem + (uint32_t)buf * 64u;
+                    if (lane == 0) {
+#pragma unroll
+                        for (int i = 0; i < kHalfMmas; ++i) {
+                            const int kk = 16 * i;
+                            const uint64_t bd =
+                                bd0 + (uint64_t)(((kk >> 6) * kChunkBytes + (kk & 63) * 2) >> 4);
+                            ptx::mma_f16_ts(acc, a_buf + 8 * i, bd, idesc, hs > 0 || i > 0);
+                        }
+                        ptx::mma_commit(&aempty[buf]);
+                        ptx::mma_commit(&bempty[s]);
+                    }
+                    __syncwarp();
+                }
+                if (!ok) break;
+                if (lane == 0) ptx::mma_commit(&accfull[ab]);
                 __syncwarp();
-                first = false;
-                ++nx;
             }
-            if (!ok) break;
-            if (lane == 0) ptx::mma_commit(&accfull[ab]);
+            if (!ok && lane == 0) {
+                set_status(a.status, DS4G_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every MMA issued by this thread is complete before the CTA frees
+            // its tensor memory
+            if (lane == 0) {
+                ptx::mma_commit(&drain[X]);
+                ptx::mbar_wait(&drain[X], 0, a.wait_ns);
+            }
             __syncwarp();
-        }
-        if (!ok && lane == 0) {
-            set_status(a.status, DS4G_ERR_TIMEOUT);
-            *abort_flag = 1;
-        }
-        // every MMA issued by this thread is complete before the CTA frees
-        // its tensor memory
-        if (lane == 0) {
-            ptx::mma_commit(&drain[X]);
-            ptx::mbar_wait(&drain[X], 0, a.wait_ns);
-        }
-        __syncwarp();
         }
     } else if (warp >= kFirstDequantWarp + kDequantWarps) {
         // ---------------- down epilogue warps (MODE 1) ----------------
@@ -656,7 +733,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         }
     } else {
         // ---------------- dequantizers / gate-up epilogue ----------------
-        const TcCta cta{smem, full, empty, afull, aempty, accfull, accempty, tmem,
+        const TcCta cta{wring, wfull, wempty, afull, aempty, accfull, accempty, tmem,
                         ptx::smem_addr(cbrep), abort_flag, n_items, KB};
         DequantRole<MODE, FMT>(a, cta, warp, lane, (warp - kFirstDequantWarp) >> 2).run();
     }
@@ -664,11 +741,8 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
     __syncthreads();
     // after an abort: the copies this CTA issued land before it exits
     if (threadIdx.x == 0 && *abort_flag) {
-        const int issued = s_issued;
-        for (int q = issued - kStages; q < issued; ++q) {
-            if (q < 0) continue;
-            if (!ptx::mbar_wait(&full[q % kStages], (q / kStages) & 1, a.wait_ns)) break;
-        }
+        drain_ring(wfull, R::kW, s_wissued, a.wait_ns);
+        drain_ring(bfull, R::kB, s_bissued, a.wait_ns);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -823,9 +897,7 @@ template <int MODE, int FMT>
 cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                       const TcArgs &args, int grid, cudaStream_t s)
 {
-    constexpr int NMAT = MODE == 0 ? 2 : 1;
-    const size_t smem = (size_t)kStages * (kBBytes + NMAT * kAqBytes) + 1024 +
-                        (FMT == DS4G_FMT_CB2 ? kCbRepBytes : 0);
+    const size_t smem = Ring<MODE, FMT>::kBytes + 1024;
     cudaError_t e = cudaFuncSetAttribute(tc_kernel<MODE, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
