@@ -629,7 +629,8 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         // kernel (one fill per half step, bound by its dequantizers): issuer
         // 0 alone, every A buffer in turn, with two accumulators that
         // alternate per item, so the epilogue warps drain one while the next
-        // item accumulates.  The whole warp runs the loop; lane 0 issues.
+        // item accumulates.  The whole warp runs the loop, converged; one lane chosen by
+        // elect.sync issues.
         const int X = warp - kFirstIssuerWarp;
         if (MODE == 1 && X == 1) {
             // no second issuer in the down kernel
@@ -664,21 +665,19 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                     ptx::tc_fence_after();
                     const uint64_t bd0 = bdesc0 + (uint64_t)((s * kHalfBytes) >> 4);
                     const uint32_t a_buf = tmem + (uint32_t)buf * 64u;
-                    if (lane == 0) {
 #pragma unroll
-                        for (int i = 0; i < kHalfMmas; ++i) {
-                            const int kk = 16 * i;
-                            const uint64_t bd =
-                                bd0 + (uint64_t)(((kk >> 6) * kChunkBytes + (kk & 63) * 2) >> 4);
-                            ptx::mma_f16_ts(acc, a_buf + 8 * i, bd, idesc, hs > 0 || i > 0);
-                        }
-                        ptx::mma_commit(&aempty[buf]);
-                        ptx::mma_commit(&bempty[s]);
+                    for (int i = 0; i < kHalfMmas; ++i) {
+                        const int kk = 16 * i;
+                        const uint64_t bd =
+                            bd0 + (uint64_t)(((kk >> 6) * kChunkBytes + (kk & 63) * 2) >> 4);
+                        ptx::mma_f16_ts_elect(acc, a_buf + 8 * i, bd, idesc, hs > 0 || i > 0);
                     }
+                    ptx::mma_commit_elect(&aempty[buf]);
+                    ptx::mma_commit_elect(&bempty[s]);
                     __syncwarp();
                 }
                 if (!ok) break;
-                if (lane == 0) ptx::mma_commit(&accfull[ab]);
+                ptx::mma_commit_elect(&accfull[ab]);
                 __syncwarp();
             }
             if (!ok && lane == 0) {
@@ -687,10 +686,8 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
             }
             // every MMA issued by this thread is complete before the CTA frees
             // its tensor memory
-            if (lane == 0) {
-                ptx::mma_commit(&drain[X]);
-                ptx::mbar_wait(&drain[X], 0, a.wait_ns);
-            }
+            ptx::mma_commit_elect(&drain[X]);
+            ptx::mbar_wait(&drain[X], 0, a.wait_ns);
             __syncwarp();
         }
     } else if (warp >= kFirstDequantWarp + kDequantWarps) {
