@@ -18,10 +18,14 @@ decode_32tok   7168   2048  256  8   32    Q2_K      sigmoid  2
 prefill_2048   7168   2048  256  8   2048  Q2_K      sigmoid  3
 codebook_512   7168   2048  256  8   512   codebook  sigmoid  4
 mixed_2048     7168   2048  256  8   2048  mixed     sigmoid  5
+kquant_32tok   7168   2048  256  8   32    Q4_K/Q6K  sigmoid  6
 =============  =====  ====  ===  ==  ====  ========  =======  ====
 
 mixed_2048 is the shipping mix of the ds4 weights (codebook-2-bit gate/up,
 Q2_K down) on the prefill layer with the prefill routing recipe.
+kquant_32tok is a higher-bit routed layer (Q4_K gate/up, Q6_K down; the
+ds4f-q2-q4 / ds4f-q4 downloads and the routed K-quant formats the ds4
+README names) at the 32-token decode batch.
 
 Rows are stored packed (ceil(K/256) blocks back to back) for Q2_K; the
 codebook rows (70-byte blocks) are padded to a multiple of 16 bytes so that
@@ -42,7 +46,8 @@ SOURCE = os.path.join(HERE, "synth.c")
 LIBRARY = os.path.join(HERE, "libds4g_synth.so")
 
 QK = 256
-FMT_Q2K, FMT_CB2 = 0, 1
+FMT_Q2K, FMT_CB2, FMT_Q4K, FMT_Q5K, FMT_Q6K = 0, 1, 2, 3, 4
+BLOCK_BYTES = {FMT_Q2K: 84, FMT_CB2: 70, FMT_Q4K: 144, FMT_Q5K: 176, FMT_Q6K: 210}
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 LOGITS_NORMAL, LOGITS_UNIFORM, LOGITS_BIASED, LOGITS_ZIPF = 0, 1, 2, 3
 TENSOR_GATE, TENSOR_UP, TENSOR_DOWN = 3, 4, 5
@@ -73,11 +78,11 @@ class Config:
     @property
     def block_bytes(self) -> int:
         """Bytes of one W_gate / W_up super-block."""
-        return 84 if self.format == FMT_Q2K else 70
+        return BLOCK_BYTES[self.format]
 
     @property
     def down_block_bytes(self) -> int:
-        return 84 if self.dn_format == FMT_Q2K else 70
+        return BLOCK_BYTES[self.dn_format]
 
     def row_bytes(self, K: int, align: Optional[int] = None, fmt: Optional[int] = None) -> int:
         """Row stride: ceil(K/256) blocks of `fmt` (default: the gate/up
@@ -85,7 +90,7 @@ class Config:
         own row alignment)."""
         align = self.row_align if align is None else align
         fmt = self.format if fmt is None else fmt
-        logical = -(-K // QK) * (84 if fmt == FMT_Q2K else 70)
+        logical = -(-K // QK) * BLOCK_BYTES[fmt]
         return -(-logical // align) * align
 
 
@@ -99,6 +104,8 @@ CONFIGS: Dict[str, Config] = {
                row_align=16),
         Config("mixed_2048", 7168, 2048, 256, 8, 2048, FMT_CB2, SCORE_SIGMOID, LOGITS_BIASED, 5,
                row_align=16, down_format=FMT_Q2K),
+        Config("kquant_32tok", 7168, 2048, 256, 8, 32, FMT_Q4K, SCORE_SIGMOID, LOGITS_UNIFORM, 6,
+               down_format=FMT_Q6K),
     ]
 }
 
@@ -137,6 +144,9 @@ def lib():
         L.syn_q2k_encode_block.restype = None
         L.syn_cb2_encode_block.argtypes = [vp, vp, vp]
         L.syn_cb2_encode_block.restype = None
+        for fn in ("syn_q4k_encode_block", "syn_q5k_encode_block", "syn_q6k_encode_block"):
+            getattr(L, fn).argtypes = [vp, vp]
+            getattr(L, fn).restype = None
         L.syn_make_codebook.argtypes = [u64, vp]
         L.syn_make_codebook.restype = None
         L.syn_make_experts.argtypes = [u64, i32, i32, i32, i32, i32, i64, dbl, vp, vp, i32]
@@ -179,6 +189,18 @@ def q2k_encode(w: np.ndarray) -> np.ndarray:
     out = np.zeros((w.shape[0], 84), dtype=np.uint8)
     for b in range(w.shape[0]):
         lib().syn_q2k_encode_block(_p(w[b]), _p(out[b]))
+    return out
+
+
+def kquant_encode(w: np.ndarray, fmt: int) -> np.ndarray:
+    """Encodes fp32 weights (multiple of 256) into Q4_K / Q5_K / Q6_K blocks."""
+    fn = {FMT_Q4K: "syn_q4k_encode_block", FMT_Q5K: "syn_q5k_encode_block",
+          FMT_Q6K: "syn_q6k_encode_block"}[fmt]
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1, QK)
+    out = np.zeros((w.shape[0], BLOCK_BYTES[fmt]), dtype=np.uint8)
+    f = getattr(lib(), fn)
+    for b in range(w.shape[0]):
+        f(_p(w[b]), _p(out[b]))
     return out
 
 

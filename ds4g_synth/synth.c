@@ -177,6 +177,134 @@ void syn_q2k_encode_block(const float *w, uint8_t *blk)
     blk[83] = (uint8_t)(mh >> 8);
 }
 
+/* Q4_K (levels 15) / Q5_K (levels 31) quantization of one 256-weight block.
+ * Per 32-weight sub-block s: lo = min(0, min w), hi = max w,
+ * a_s = (hi - lo) / levels, m_s = -lo; d = fp16(max a_s / 63),
+ * dmin = fp16(max m_s / 63); sc_s = clamp(rne(a_s / d), 0, 63),
+ * mn_s = clamp(rne(m_s / dmin), 0, 63);
+ * q = clamp(rne((w + dmin mn_s) / (d sc_s)), 0, levels) (0 when sc_s = 0). */
+static void k45_quantize(const float *w, int levels, int *sc, int *mn, int *q, uint16_t *dh,
+                         uint16_t *mh)
+{
+    double a[8], m[8], amax = 0, mmax = 0;
+    for (int s = 0; s < 8; ++s) {
+        double lo = 0, hi = -INFINITY;
+        for (int j = 0; j < 32; ++j) {
+            double v = w[32 * s + j];
+            if (v < lo) lo = v;
+            if (v > hi) hi = v;
+        }
+        a[s] = (hi - lo) / levels;
+        m[s] = -lo;
+        if (a[s] > amax) amax = a[s];
+        if (m[s] > mmax) mmax = m[s];
+    }
+    *dh = syn_double_to_half(amax / 63.0);
+    *mh = syn_double_to_half(mmax / 63.0);
+    double d = half_value(*dh), dmin = half_value(*mh);
+    for (int s = 0; s < 8; ++s) {
+        sc[s] = d > 0 ? clamp_int(rne(a[s] / d), 0, 63) : 0;
+        mn[s] = dmin > 0 ? clamp_int(rne(m[s] / dmin), 0, 63) : 0;
+    }
+    for (int j = 0; j < QK; ++j) {
+        int s = j / 32;
+        q[j] = sc[s] > 0 ? clamp_int(rne(((double)w[j] + dmin * mn[s]) / (d * sc[s])), 0, levels) : 0;
+    }
+}
+
+/* The 12 packed bytes of eight 6-bit scales and mins (low six bits of bytes
+ * 0..3 / 4..7 for sub-blocks 0..3, low / high nibbles of bytes 8..11 for
+ * sub-blocks 4..7, whose top two bits ride in the top bits of bytes 0..7). */
+static void k45_pack_scales(const int *sc, const int *mn, uint8_t *p)
+{
+    for (int s = 0; s < 4; ++s) {
+        p[s] = (uint8_t)(sc[s] | ((sc[s + 4] >> 4) << 6));
+        p[s + 4] = (uint8_t)(mn[s] | ((mn[s + 4] >> 4) << 6));
+        p[s + 8] = (uint8_t)((sc[s + 4] & 15) | ((mn[s + 4] & 15) << 4));
+    }
+}
+
+/* Q4_K block (144 bytes): d, dmin, packed scales, qs (weight 64c + l in the
+ * low nibble of qs[32c + l], weight 64c + 32 + l in its high nibble). */
+void syn_q4k_encode_block(const float *w, uint8_t *blk)
+{
+    int sc[8], mn[8], q[QK];
+    uint16_t dh, mh;
+    k45_quantize(w, 15, sc, mn, q, &dh, &mh);
+    memset(blk, 0, 144);
+    blk[0] = (uint8_t)(dh & 0xFF); blk[1] = (uint8_t)(dh >> 8);
+    blk[2] = (uint8_t)(mh & 0xFF); blk[3] = (uint8_t)(mh >> 8);
+    k45_pack_scales(sc, mn, blk + 4);
+    for (int j = 0; j < QK; ++j) {
+        int c = j / 64, r = j % 64;
+        blk[16 + 32 * c + r % 32] |= (uint8_t)(q[j] << (r < 32 ? 0 : 4));
+    }
+}
+
+/* Q5_K block (176 bytes): as Q4_K, with bit 4 of weight 32s + l in bit s of
+ * qh[l] (bytes 16..47) and the low nibbles at bytes 48..175. */
+void syn_q5k_encode_block(const float *w, uint8_t *blk)
+{
+    int sc[8], mn[8], q[QK];
+    uint16_t dh, mh;
+    k45_quantize(w, 31, sc, mn, q, &dh, &mh);
+    memset(blk, 0, 176);
+    blk[0] = (uint8_t)(dh & 0xFF); blk[1] = (uint8_t)(dh >> 8);
+    blk[2] = (uint8_t)(mh & 0xFF); blk[3] = (uint8_t)(mh >> 8);
+    k45_pack_scales(sc, mn, blk + 4);
+    for (int j = 0; j < QK; ++j) {
+        int c = j / 64, r = j % 64, l = r % 32;
+        blk[48 + 32 * c + l] |= (uint8_t)((q[j] & 15) << (r < 32 ? 0 : 4));
+        blk[16 + l] |= (uint8_t)(((q[j] >> 4) & 1) << (j / 32));
+    }
+}
+
+/* Q6_K block (210 bytes).  Per 16-weight sub-block t: a_t = max |w| / 31;
+ * d = fp16(max a_t / 127); sc_t = clamp(rne(a_t / d), -128, 127);
+ * q = clamp(rne(w / (d sc_t)), -32, 31) (0 when sc_t = 0), stored as
+ * v = q + 32: low nibble of v in nibble (u >> 1) of ql[64h + 32(u&1) + l],
+ * its top two bits in bits 2u..2u+1 of qh[32h + l] (h = j/128, u = (j%128)/32,
+ * l = j%32); scales at 192..207, d at 208..209. */
+void syn_q6k_encode_block(const float *w, uint8_t *blk)
+{
+    double a[16], amax = 0;
+    for (int t = 0; t < 16; ++t) {
+        double mx = 0;
+        for (int j = 0; j < 16; ++j) {
+            double v = fabs((double)w[16 * t + j]);
+            if (v > mx) mx = v;
+        }
+        a[t] = mx / 31.0;
+        if (a[t] > amax) amax = a[t];
+    }
+    uint16_t dh = syn_double_to_half(amax / 127.0);
+    double d = half_value(dh);
+    int sc[16];
+    memset(blk, 0, 210);
+    for (int t = 0; t < 16; ++t) {
+        sc[t] = d > 0 ? clamp_int(rne(a[t] / d), -128, 127) : 0;
+        blk[192 + t] = (uint8_t)(int8_t)sc[t];
+    }
+    for (int j = 0; j < QK; ++j) {
+        int t = j / 16;
+        int q = sc[t] != 0 ? clamp_int(rne((double)w[j] / (d * sc[t])), -32, 31) : 0;
+        int v = q + 32;
+        int h = j / 128, r = j % 128, u = r / 32, l = r % 32;
+        blk[64 * h + 32 * (u & 1) + l] |= (uint8_t)((v & 15) << (4 * (u >> 1)));
+        blk[128 + 32 * h + l] |= (uint8_t)((v >> 4) << (2 * u));
+    }
+    blk[208] = (uint8_t)(dh & 0xFF);
+    blk[209] = (uint8_t)(dh >> 8);
+}
+
+/* Super-block bytes of each weight format (0 Q2_K, 1 codebook, 2 Q4_K,
+ * 3 Q5_K, 4 Q6_K); 0 for an unknown format. */
+static int block_bytes(int format)
+{
+    static const int bb[5] = {84, 70, 144, 176, 210};
+    return format >= 0 && format < 5 ? bb[format] : 0;
+}
+
 /* score[i] = D * n2[i] - sum_b (2 |w_b|) * |c_ib|, accumulated over b in
  * order; each i is independent, so the vector clones round exactly like the
  * scalar one (no contraction: built with -ffp-contract=off). */
@@ -295,7 +423,7 @@ static void *expert_worker(void *arg)
 {
     expert_job *J = (expert_job *)arg;
     int nblk = (J->K + QK - 1) / QK;
-    int bb = J->format == 0 ? 84 : 70;
+    int bb = block_bytes(J->format);
     float *w = (float *)malloc(sizeof(float) * nblk * QK);
     if (!w) return (void *)1;
     for (int64_t r = J->row_begin; r < J->row_end; ++r) {
@@ -319,10 +447,14 @@ static void *expert_worker(void *arg)
         uint8_t *row = J->out + r * J->row_bytes;
         memset(row, 0, (size_t)J->row_bytes);
         for (int b = 0; b < nblk; ++b) {
-            if (J->format == 0)
-                syn_q2k_encode_block(w + b * QK, row + (int64_t)b * bb);
-            else
-                cb2_encode_block(w + b * QK, J->mag_t, J->n2, J->codebook, row + (int64_t)b * bb);
+            uint8_t *blk = row + (int64_t)b * bb;
+            switch (J->format) {
+            case 0: syn_q2k_encode_block(w + b * QK, blk); break;
+            case 1: cb2_encode_block(w + b * QK, J->mag_t, J->n2, J->codebook, blk); break;
+            case 2: syn_q4k_encode_block(w + b * QK, blk); break;
+            case 3: syn_q5k_encode_block(w + b * QK, blk); break;
+            default: syn_q6k_encode_block(w + b * QK, blk); break;
+            }
         }
     }
     free(w);
@@ -334,8 +466,8 @@ int syn_make_experts(uint64_t seed, int tensor, int E, int N, int K, int format,
                      uint8_t *out, int n_threads)
 {
     int nblk = (K + QK - 1) / QK;
-    int bb = format == 0 ? 84 : 70;
-    if (E < 1 || N < 1 || K < 1 || row_bytes < (int64_t)nblk * bb) return 1;
+    int bb = block_bytes(format);
+    if (bb == 0 || E < 1 || N < 1 || K < 1 || row_bytes < (int64_t)nblk * bb) return 1;
     if (format == 1 && !codebook) return 1;
     float mag_t[8 * 256], n2[256];
     if (format == 1) codebook_tables(codebook, mag_t, n2);

@@ -30,6 +30,7 @@ FMT_CB2 = 1
 QK = 256
 Q2K_BYTES = 84
 CB2_BYTES = 70
+Q4K_BYTES, Q5K_BYTES, Q6K_BYTES = 144, 176, 210
 
 CFLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared"]
 
@@ -80,6 +81,9 @@ class Oracle:
         lib.orc_q2k_dequant.restype = None
         lib.orc_cb2_dequant.argtypes = [vp, i64, vp, vp]
         lib.orc_cb2_dequant.restype = None
+        for name in ("orc_q4k_dequant", "orc_q5k_dequant", "orc_q6k_dequant"):
+            getattr(lib, name).argtypes = [vp, i64, vp]
+            getattr(lib, name).restype = None
         lib.orc_route.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
         lib.orc_route.restype = ctypes.c_int
         lib.orc_moe_forward.argtypes = [ctypes.POINTER(_Layer), vp, vp, i32, vp, i32,
@@ -105,6 +109,26 @@ class Oracle:
         out = np.empty(n * QK, dtype=np.float32)
         self.lib.orc_q2k_dequant(_ptr(b), n, _ptr(out))
         return out
+
+    def _kquant(self, fn, bb: int, blocks: np.ndarray) -> np.ndarray:
+        b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)
+        assert b.size % bb == 0
+        n = b.size // bb
+        out = np.empty(n * QK, dtype=np.float32)
+        fn(_ptr(b), n, _ptr(out))
+        return out
+
+    def q4k_dequant(self, blocks: np.ndarray) -> np.ndarray:
+        """blocks: uint8 [..., 144*n] -> float32 [n*256]."""
+        return self._kquant(self.lib.orc_q4k_dequant, Q4K_BYTES, blocks)
+
+    def q5k_dequant(self, blocks: np.ndarray) -> np.ndarray:
+        """blocks: uint8 [..., 176*n] -> float32 [n*256]."""
+        return self._kquant(self.lib.orc_q5k_dequant, Q5K_BYTES, blocks)
+
+    def q6k_dequant(self, blocks: np.ndarray) -> np.ndarray:
+        """blocks: uint8 [..., 210*n] -> float32 [n*256]."""
+        return self._kquant(self.lib.orc_q6k_dequant, Q6K_BYTES, blocks)
 
     def cb2_dequant(self, blocks: np.ndarray, codebook: np.ndarray) -> np.ndarray:
         b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)

@@ -36,10 +36,13 @@
 #define ORC_QK 256          /* weights per super-block                      */
 #define ORC_Q2K_BYTES 84    /* Q2_K super-block bytes                       */
 #define ORC_CB2_BYTES 70    /* codebook-2-bit super-block bytes             */
+#define ORC_Q4K_BYTES 144   /* Q4_K super-block bytes                       */
+#define ORC_Q5K_BYTES 176   /* Q5_K super-block bytes                       */
+#define ORC_Q6K_BYTES 210   /* Q6_K super-block bytes                       */
 
 enum { ORC_OK = 0, ORC_ERR_INVALID = 1, ORC_ERR_NOMEM = 2 };
 enum { ORC_SCORE_SOFTMAX = 0, ORC_SCORE_SIGMOID = 1 };
-enum { ORC_FMT_Q2K = 0, ORC_FMT_CB2 = 1 };
+enum { ORC_FMT_Q2K = 0, ORC_FMT_CB2 = 1, ORC_FMT_Q4K = 2, ORC_FMT_Q5K = 3, ORC_FMT_Q6K = 4 };
 
 /* ------------------------------------------------------------------------
  * Scalar formats.
@@ -135,6 +138,133 @@ void orc_cb2_dequant_block(const uint8_t *blk, const int8_t *codebook, float *w)
         value = value * (float)entry;
         w[j] = negate ? -value : value;
     }
+}
+
+/* ------------------------------------------------------------------------
+ * The higher-bit routed-expert formats (ds4 README mirror, "Model Weights":
+ * routed gate/up in Q2_K, Q4_K or Q5_K, routed down in Q2_K, Q4_K, Q5_K or
+ * Q6_K), GGUF K-quant layouts (ds4 README mirror, "Acknowledgements to
+ * llama.cpp and GGML").  256 weights per super-block in every case.
+ *
+ * Q4_K and Q5_K share the packed 6-bit scales: eight 32-weight sub-blocks,
+ * each with a 6-bit scale sc_s and a 6-bit min m_s in 12 bytes p[0..11]:
+ *   s < 4:  sc_s = p[s] & 63,                        m_s = p[s+4] & 63
+ *   s >= 4: sc_s = (p[s+4] & 15) | (p[s-4] >> 6) << 4,
+ *           m_s  = (p[s+4] >> 4) | (p[s]   >> 6) << 4
+ * (the top two bits of sub-blocks 4..7 ride in the top bits of bytes 0..7).
+ * --------------------------------------------------------------------- */
+static void k4_scale_min(const uint8_t *p, int s, int *sc, int *m)
+{
+    if (s < 4) {
+        *sc = p[s] & 63;
+        *m = p[s + 4] & 63;
+    } else {
+        *sc = (p[s + 4] & 15) | ((p[s - 4] >> 6) << 4);
+        *m = (p[s + 4] >> 4) | ((p[s] >> 6) << 4);
+    }
+}
+
+/* Q4_K super-block (144 bytes):
+ *   bytes  0..1   d    (fp16)        bytes 2..3  dmin (fp16)
+ *   bytes  4..15  the packed 6-bit scales and mins above
+ *   bytes 16..143 qs[128]: 4-bit quants
+ * Weight j: chunk c = j/64 (two sub-blocks), r = j%64, l = r%32; the quant is
+ * the low nibble of qs[32c + l] for r < 32 and its high nibble otherwise;
+ * sub-block s = j/32;
+ *   w_j = d * sc_s * q_j - dmin * m_s      (fp32).
+ * Both products are exact in fp32 (at most 11 + 6 + 4 significant bits), so
+ * the only rounding is the subtraction. */
+void orc_q4k_dequant_block(const uint8_t *blk, float *w)
+{
+    float d = (float)orc_half_to_double(rd16(blk));
+    float dmin = (float)orc_half_to_double(rd16(blk + 2));
+    const uint8_t *scales = blk + 4;
+    const uint8_t *qs = blk + 16;
+    for (int j = 0; j < ORC_QK; ++j) {
+        int c = j / 64, r = j % 64, l = r % 32, s = j / 32;
+        int byte = qs[32 * c + l];
+        int q = r < 32 ? (byte & 15) : (byte >> 4);
+        int sc, m;
+        k4_scale_min(scales, s, &sc, &m);
+        float scale_part = d * (float)sc;
+        float value = scale_part * (float)q;
+        float min_part = dmin * (float)m;
+        w[j] = value - min_part;
+    }
+}
+
+/* Q5_K super-block (176 bytes): as Q4_K with a fifth bit per weight:
+ *   bytes  0..1 d, 2..3 dmin, 4..15 packed scales and mins,
+ *   bytes 16..47  qh[32]: bit s of qh[l] is the high bit of weight 32s + l,
+ *   bytes 48..175 qs[128]: the low four bits, placed as in Q4_K.
+ *   q_j = low_j + 16 * ((qh[j%32] >> (j/32)) & 1),
+ *   w_j = d * sc_s * q_j - dmin * m_s      (fp32; products exact, at most
+ * 11 + 6 + 5 significant bits). */
+void orc_q5k_dequant_block(const uint8_t *blk, float *w)
+{
+    float d = (float)orc_half_to_double(rd16(blk));
+    float dmin = (float)orc_half_to_double(rd16(blk + 2));
+    const uint8_t *scales = blk + 4;
+    const uint8_t *qh = blk + 16;
+    const uint8_t *qs = blk + 48;
+    for (int j = 0; j < ORC_QK; ++j) {
+        int c = j / 64, r = j % 64, l = r % 32, s = j / 32;
+        int byte = qs[32 * c + l];
+        int low = r < 32 ? (byte & 15) : (byte >> 4);
+        int q = low + 16 * ((qh[l] >> s) & 1);
+        int sc, m;
+        k4_scale_min(scales, s, &sc, &m);
+        float scale_part = d * (float)sc;
+        float value = scale_part * (float)q;
+        float min_part = dmin * (float)m;
+        w[j] = value - min_part;
+    }
+}
+
+/* Q6_K super-block (210 bytes), symmetric, sixteen 16-weight sub-blocks:
+ *   bytes   0..127 ql[128]: low four bits
+ *   bytes 128..191 qh[64]:  high two bits
+ *   bytes 192..207 scales[16]: int8 scale of sub-block j/16
+ *   bytes 208..209 d (fp16)
+ * Weight j: half h = j/128, r = j%128, quarter u = r/32, l = r%32;
+ *   low  = nibble (u >> 1) of ql[64h + 32(u & 1) + l]   (0 = low nibble),
+ *   high = (qh[32h + l] >> 2u) & 3,
+ *   q_j  = low + 16 * high - 32                          (-32 .. 31),
+ *   w_j  = d * scales[j/16] * q_j      (fp32, exact: the significands of d,
+ * the scale and q multiply to less than 2^24). */
+void orc_q6k_dequant_block(const uint8_t *blk, float *w)
+{
+    const uint8_t *ql = blk;
+    const uint8_t *qh = blk + 128;
+    const int8_t *scales = (const int8_t *)(blk + 192);
+    float d = (float)orc_half_to_double(rd16(blk + 208));
+    for (int j = 0; j < ORC_QK; ++j) {
+        int h = j / 128, r = j % 128, u = r / 32, l = r % 32;
+        int byte = ql[64 * h + 32 * (u & 1) + l];
+        int low = (u >> 1) ? (byte >> 4) : (byte & 15);
+        int high = (qh[32 * h + l] >> (2 * u)) & 3;
+        int q = low + 16 * high - 32;
+        float scale_part = d * (float)scales[j / 16];
+        w[j] = scale_part * (float)q;
+    }
+}
+
+void orc_q4k_dequant(const uint8_t *blocks, int64_t n_blocks, float *out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b)
+        orc_q4k_dequant_block(blocks + b * ORC_Q4K_BYTES, out + b * ORC_QK);
+}
+
+void orc_q5k_dequant(const uint8_t *blocks, int64_t n_blocks, float *out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b)
+        orc_q5k_dequant_block(blocks + b * ORC_Q5K_BYTES, out + b * ORC_QK);
+}
+
+void orc_q6k_dequant(const uint8_t *blocks, int64_t n_blocks, float *out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b)
+        orc_q6k_dequant_block(blocks + b * ORC_Q6K_BYTES, out + b * ORC_QK);
 }
 
 void orc_q2k_dequant(const uint8_t *blocks, int64_t n_blocks, float *out)
@@ -265,11 +395,18 @@ typedef struct {
     const int8_t *codebook;
 } orc_layer;
 
-/* Both formats known; a codebook present when either matrix uses it. */
+/* Supported formats per matrix (ds4 README mirror, "Model Weights": routed
+ * gate/up in Q2_K, Q4_K or Q5_K, routed down also in Q6_K; the codebook
+ * format for either); a codebook present when either matrix uses it. */
 static int orc_formats_ok(const orc_layer *L)
 {
-    if (L->format != ORC_FMT_Q2K && L->format != ORC_FMT_CB2) return 0;
-    if (L->down_format != ORC_FMT_Q2K && L->down_format != ORC_FMT_CB2) return 0;
+    if (L->format != ORC_FMT_Q2K && L->format != ORC_FMT_CB2 && L->format != ORC_FMT_Q4K &&
+        L->format != ORC_FMT_Q5K)
+        return 0;
+    if (L->down_format != ORC_FMT_Q2K && L->down_format != ORC_FMT_CB2 &&
+        L->down_format != ORC_FMT_Q4K && L->down_format != ORC_FMT_Q5K &&
+        L->down_format != ORC_FMT_Q6K)
+        return 0;
     if ((L->format == ORC_FMT_CB2 || L->down_format == ORC_FMT_CB2) && !L->codebook) return 0;
     return 1;
 }
@@ -282,9 +419,15 @@ static void dequant_row(const orc_layer *L, int fmt, const uint8_t *row, int K, 
     for (int b = 0; b < nblk; ++b) {
         if (fmt == ORC_FMT_Q2K)
             orc_q2k_dequant_block(row + (int64_t)b * ORC_Q2K_BYTES, out + b * ORC_QK);
-        else
+        else if (fmt == ORC_FMT_CB2)
             orc_cb2_dequant_block(row + (int64_t)b * ORC_CB2_BYTES, L->codebook,
                                   out + b * ORC_QK);
+        else if (fmt == ORC_FMT_Q4K)
+            orc_q4k_dequant_block(row + (int64_t)b * ORC_Q4K_BYTES, out + b * ORC_QK);
+        else if (fmt == ORC_FMT_Q5K)
+            orc_q5k_dequant_block(row + (int64_t)b * ORC_Q5K_BYTES, out + b * ORC_QK);
+        else
+            orc_q6k_dequant_block(row + (int64_t)b * ORC_Q6K_BYTES, out + b * ORC_QK);
     }
 }
 

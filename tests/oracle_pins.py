@@ -61,19 +61,77 @@ def np_cb2_dequant(blocks: np.ndarray, codebook: np.ndarray) -> np.ndarray:
     return np.where(bits == 1, -v, v).reshape(-1)
 
 
+def _np_k4_scales(p: np.ndarray):
+    """[n, 12] packed bytes -> ([n, 8] scales, [n, 8] mins) as integers."""
+    p = p.astype(np.int64)
+    sc = np.concatenate([p[:, 0:4] & 63, (p[:, 8:12] & 15) | ((p[:, 0:4] >> 6) << 4)], axis=1)
+    mn = np.concatenate([p[:, 4:8] & 63, (p[:, 8:12] >> 4) | ((p[:, 4:8] >> 6) << 4)], axis=1)
+    return sc, mn
+
+
+def _np_half(b: np.ndarray) -> np.ndarray:
+    return b.copy().view(np.float16).astype(np.float32)
+
+
+def np_q4k_dequant(blocks: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1, 144)
+    n = b.shape[0]
+    d, dmin = _np_half(b[:, 0:2]), _np_half(b[:, 2:4])
+    sc, mn = _np_k4_scales(b[:, 4:16])
+    qs = b[:, 16:144].reshape(n, 4, 1, 32)
+    q = np.concatenate([qs & 15, qs >> 4], axis=2).reshape(n, 256).astype(np.float32)
+    scf = np.repeat(sc.astype(np.float32), 32, axis=1)
+    mnf = np.repeat(mn.astype(np.float32), 32, axis=1)
+    return ((d * scf) * q - dmin * mnf).reshape(-1)
+
+
+def np_q5k_dequant(blocks: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1, 176)
+    n = b.shape[0]
+    d, dmin = _np_half(b[:, 0:2]), _np_half(b[:, 2:4])
+    sc, mn = _np_k4_scales(b[:, 4:16])
+    qh = b[:, 16:48]
+    high = ((qh[:, None, :] >> np.arange(8, dtype=np.uint8)[None, :, None]) & 1).reshape(n, 256)
+    qs = b[:, 48:176].reshape(n, 4, 1, 32)
+    low = np.concatenate([qs & 15, qs >> 4], axis=2).reshape(n, 256)
+    q = (low.astype(np.int64) + 16 * high.astype(np.int64)).astype(np.float32)
+    scf = np.repeat(sc.astype(np.float32), 32, axis=1)
+    mnf = np.repeat(mn.astype(np.float32), 32, axis=1)
+    return ((d * scf) * q - dmin * mnf).reshape(-1)
+
+
+def np_q6k_dequant(blocks: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1, 210)
+    n = b.shape[0]
+    ql = b[:, 0:128].reshape(n, 2, 1, 2, 32)                     # [n, half, nibble, v, lane]
+    low = np.concatenate([ql & 15, ql >> 4], axis=2).reshape(n, 2, 4, 32)   # u = 2 nibble + v
+    qh = b[:, 128:192].reshape(n, 2, 1, 32)
+    high = (qh >> (2 * np.arange(4, dtype=np.uint8)).reshape(1, 1, 4, 1)) & 3
+    q = (low.astype(np.int64) + 16 * high.astype(np.int64) - 32).reshape(n, 256).astype(np.float32)
+    sc = np.repeat(b[:, 192:208].copy().view(np.int8).astype(np.float32), 16, axis=1)
+    d = _np_half(b[:, 208:210])
+    return ((d * sc) * q).reshape(-1)
+
+
+_NP_BLOCK = {S.FMT_Q2K: 84, S.FMT_CB2: 70, S.FMT_Q4K: 144, S.FMT_Q5K: 176, S.FMT_Q6K: 210}
+
+
 def np_dense_weights(layer, name: str, K: int) -> np.ndarray:
     """[E, N, K] fp32 weights of one tensor, dequantized with the numpy
     routines above."""
     W = layer[name]
     E, N, rb = W.shape
     fmt = layer.get("down_format", layer["format"]) if name == "w_down" else layer["format"]
-    bb = 84 if fmt == S.FMT_Q2K else 70
+    bb = _NP_BLOCK[fmt]
     nblk = -(-K // 256)
     raw = np.ascontiguousarray(W[:, :, :nblk * bb]).reshape(-1)
     if fmt == S.FMT_Q2K:
         w = np_q2k_dequant(raw)
-    else:
+    elif fmt == S.FMT_CB2:
         w = np_cb2_dequant(raw, layer["codebook"])
+    else:
+        w = {S.FMT_Q4K: np_q4k_dequant, S.FMT_Q5K: np_q5k_dequant,
+             S.FMT_Q6K: np_q6k_dequant}[fmt](raw)
     return w.reshape(E, N, nblk * 256)[:, :, :K]
 
 
@@ -197,6 +255,98 @@ def pin_q2k_numpy(orc):
     assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
 
 
+def _put_half(blk, off, bits):
+    blk[off] = bits & 0xFF
+    blk[off + 1] = bits >> 8
+
+
+def pin_q4k_worked(orc):
+    for s, p, fill, dbits, mbits, val in _rows("q4k_worked.txt"):
+        blk = np.zeros(144, dtype=np.uint8)
+        _put_half(blk, 0, int(dbits, 16))
+        _put_half(blk, 2, int(mbits, 16))
+        blk[4:16] = np.frombuffer(bytes.fromhex(p), dtype=np.uint8)
+        blk[16:] = int(fill, 16)
+        out = orc.q4k_dequant(blk)
+        exp = np.zeros(256, dtype=np.float32)
+        exp[32 * int(s):32 * int(s) + 32] = float(val)
+        assert np.array_equal(out, exp), (s, out[32 * int(s)], np.nonzero(out)[0][:4])
+
+
+def pin_q5k_worked(orc):
+    for s, p, qsf, qhf, dbits, mbits, val in _rows("q5k_worked.txt"):
+        blk = np.zeros(176, dtype=np.uint8)
+        _put_half(blk, 0, int(dbits, 16))
+        _put_half(blk, 2, int(mbits, 16))
+        blk[4:16] = np.frombuffer(bytes.fromhex(p), dtype=np.uint8)
+        blk[16:48] = int(qhf, 16)
+        blk[48:] = int(qsf, 16)
+        out = orc.q5k_dequant(blk)
+        exp = np.zeros(256, dtype=np.float32)
+        exp[32 * int(s):32 * int(s) + 32] = float(val)
+        assert np.array_equal(out, exp), (s, out[32 * int(s)], np.nonzero(out)[0][:4])
+
+
+def pin_q6k_worked(orc):
+    for t, sc, qlf, qhf, dbits, val in _rows("q6k_worked.txt"):
+        blk = np.zeros(210, dtype=np.uint8)
+        blk[0:128] = int(qlf, 16)
+        blk[128:192] = int(qhf, 16)
+        blk[192 + int(t)] = np.int8(int(sc)).view(np.uint8)
+        _put_half(blk, 208, int(dbits, 16))
+        out = orc.q6k_dequant(blk)
+        exp = np.zeros(256, dtype=np.float32)
+        exp[16 * int(t):16 * int(t) + 16] = float(val)
+        assert np.array_equal(out, exp), (t, out[16 * int(t)], np.nonzero(out)[0][:4])
+
+
+def pin_kquant_onehot(orc):
+    for row in _rows("kquant_onehot.txt"):
+        fmt, field, idx, val = row[0], row[1], int(row[2]), int(row[3], 16)
+        listed = dict((int(a), float(b)) for a, b in (c.split(":") for c in row[4:]))
+        if fmt in ("q4k", "q5k"):
+            bb = 144 if fmt == "q4k" else 176
+            blk = np.zeros(bb, dtype=np.uint8)
+            _put_half(blk, 0, 0x3C00)
+            blk[4:16] = [1, 1, 1, 1, 0, 0, 0, 0, 1, 1, 1, 1]
+            base = {"qs": 16 if fmt == "q4k" else 48, "qh": 16}[field]
+            blk[base + idx] = val
+            out = (orc.q4k_dequant if fmt == "q4k" else orc.q5k_dequant)(blk)
+            exp = np.zeros(256, dtype=np.float32)
+        else:
+            blk = np.zeros(210, dtype=np.uint8)
+            blk[192:208] = 1
+            _put_half(blk, 208, 0x3C00)
+            blk[{"ql": 0, "qh": 128}[field] + idx] = val
+            out = orc.q6k_dequant(blk)
+            exp = np.full(256, -32.0, dtype=np.float32)
+        for j, w in listed.items():
+            exp[j] = w
+        assert np.array_equal(out, exp), (row, np.nonzero(out != exp)[0][:6])
+
+
+def _random_kquant_blocks(rng, n, bb, half_offsets):
+    blk = rng.integers(0, 256, size=(n, bb), dtype=np.uint8)
+    for off in half_offsets:                  # finite fp16 fields
+        h = rng.integers(0, 0x7C00, size=n).astype(np.uint16)
+        h |= (rng.integers(0, 2, size=n).astype(np.uint16) << 15)
+        blk[:, off:off + 2] = h.view(np.uint8).reshape(n, 2)
+    return blk
+
+
+def pin_kquant_numpy(orc):
+    """Random blocks of each K-quant format: bit-exact agreement with the
+    independent numpy decoders."""
+    rng = np.random.default_rng(21)
+    for bb, offs, fo, fn in ((144, (0, 2), orc.q4k_dequant, np_q4k_dequant),
+                             (176, (0, 2), orc.q5k_dequant, np_q5k_dequant),
+                             (210, (208,), orc.q6k_dequant, np_q6k_dequant)):
+        blk = _random_kquant_blocks(rng, 512, bb, offs)
+        got = fo(blk)
+        ref = fn(blk)
+        assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), bb
+
+
 def _worked_codebook():
     cb = np.zeros((256, 8), dtype=np.int8)
     cb[0] = [8, -8, 25, -25, 43, -43, 8, 8]
@@ -281,9 +431,10 @@ def pin_route_full_k(orc):
 
 def pin_forward_dense(orc):
     """Oracle forward against the dense numpy fp64 reference: the tiny
-    workload, a padded-I layer, a sigmoid layer, a codebook layer, and the
-    two mixed layers (codebook gate/up with Q2_K down -- the shipping mix --
-    and the reverse, so that a format read for the wrong matrix fails)."""
+    workload, a padded-I layer, a sigmoid layer, a codebook layer, the two
+    mixed layers (codebook gate/up with Q2_K down -- the shipping mix -- and
+    the reverse, so that a format read for the wrong matrix fails), and
+    layers in the K-quant formats."""
     layers = [S.make_layer(S.CONFIGS["tiny"]),
               small_layer(),
               small_layer(seed=12, I=256 + 40, score=S.SCORE_SIGMOID, logits_kind=S.LOGITS_UNIFORM),
@@ -291,7 +442,14 @@ def pin_forward_dense(orc):
               small_layer(seed=15, H=512, I=320, E=5, k=2, T=3, fmt=S.FMT_CB2, align=16,
                           down_fmt=S.FMT_Q2K),
               small_layer(seed=16, H=512, I=256, E=4, k=2, T=3, fmt=S.FMT_Q2K, align=16,
-                          down_fmt=S.FMT_CB2)]
+                          down_fmt=S.FMT_CB2),
+              # the higher-bit routed formats: Q4_K gate/up with Q6_K down,
+              # Q5_K throughout, and Q2_K gate/up with Q4_K down
+              small_layer(seed=17, H=512, I=320, E=5, k=2, T=3, fmt=S.FMT_Q4K,
+                          down_fmt=S.FMT_Q6K),
+              small_layer(seed=18, H=512, I=256, E=4, k=2, T=3, fmt=S.FMT_Q5K),
+              small_layer(seed=19, H=512, I=256, E=4, k=2, T=3, fmt=S.FMT_Q2K,
+                          down_fmt=S.FMT_Q4K)]
     for L in layers:
         y, ids, w = orc.moe_forward(L, L["x"], L["logits"])
         ref = np_forward(L, L["x"], L["logits"])
@@ -403,6 +561,7 @@ def pin_quantizer_roundtrip(orc):
 ALL_PINS = [
     pin_half_decode, pin_bf16_decode, pin_q2k_onehot, pin_q2k_scale_min,
     pin_q2k_zero_scale, pin_q2k_numpy, pin_cb2_worked, pin_cb2_numpy,
+    pin_q4k_worked, pin_q5k_worked, pin_q6k_worked, pin_kquant_onehot, pin_kquant_numpy,
     pin_route_worked, pin_route_bruteforce, pin_route_full_k,
     pin_forward_dense, pin_forward_zero_scale, pin_forward_k1_single,
     pin_forward_scale_pow2, pin_forward_relabel, pin_quantizer_roundtrip,

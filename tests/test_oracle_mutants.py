@@ -75,6 +75,36 @@ MUTANTS = {
     "cb2_index_per_4": [("int o = j / 8;\n        int b = j % 8;", "int o = j / 4;\n        int b = j % 8;")],
     "route_picks_repeat": [("        ids[i] = best;\n        used[best] = 1;", "        ids[i] = best;")],
     "combine_averages_slots": [("yt[m] += w[i] * o[m];", "yt[m] += w[i] * o[m] / k;")],
+    # K-quant formats
+    "k4_scale_low_shift": [("*sc = (p[s + 4] & 15) | ((p[s - 4] >> 6) << 4);",
+                            "*sc = (p[s + 4] & 15) | ((p[s - 4] >> 6) << 5);")],
+    "k4_min_from_scale_byte": [("*m = (p[s + 4] >> 4) | ((p[s] >> 6) << 4);",
+                                "*m = (p[s + 4] >> 4) | ((p[s - 4] >> 6) << 4);")],
+    "k4_min_mask_5bit": [("*m = p[s + 4] & 63;", "*m = p[s + 4] & 31;")],
+    "q4k_nibbles_swapped": [("int q = r < 32 ? (byte & 15) : (byte >> 4);",
+                             "int q = r < 32 ? (byte >> 4) : (byte & 15);")],
+    "q4k_chunk_stride_64": [("int byte = qs[32 * c + l];\n        int q = r < 32",
+                             "int byte = qs[64 * (c / 2) + l];\n        int q = r < 32")],
+    "q4k_drops_min": [("        w[j] = value - min_part;\n    }\n}\n\n/* Q5_K",
+                       "        w[j] = value;\n    }\n}\n\n/* Q5_K")],
+    "q5k_high_bit_by_lane": [("int q = low + 16 * ((qh[l] >> s) & 1);",
+                              "int q = low + 16 * ((qh[s] >> (l % 8)) & 1);")],
+    "q5k_high_bit_weight_32": [("int q = low + 16 * ((qh[l] >> s) & 1);",
+                                "int q = low + 32 * ((qh[l] >> s) & 1);")],
+    "q5k_qs_at_16": [("const uint8_t *qs = blk + 48;", "const uint8_t *qs = blk + 16;")],
+    "q6k_no_offset": [("int q = low + 16 * high - 32;", "int q = low + 16 * high;")],
+    "q6k_ql_half_stride_32": [("int byte = ql[64 * h + 32 * (u & 1) + l];",
+                               "int byte = ql[32 * h + 32 * (u & 1) + l];")],
+    "q6k_qh_shift_u": [("int high = (qh[32 * h + l] >> (2 * u)) & 3;",
+                        "int high = (qh[32 * h + l] >> u) & 3;")],
+    "q6k_scale_per_32": [("float scale_part = d * (float)scales[j / 16];",
+                          "float scale_part = d * (float)scales[j / 32];")],
+    "q6k_unsigned_scales": [("const int8_t *scales = (const int8_t *)(blk + 192);",
+                             "const uint8_t *scales = (const uint8_t *)(blk + 192);")],
+    "q6k_d_offset": [("float d = (float)orc_half_to_double(rd16(blk + 208));",
+                      "float d = (float)orc_half_to_double(rd16(blk + 206));")],
+    "kquant_down_reads_q5k": [("            orc_q6k_dequant_block(row + (int64_t)b * ORC_Q6K_BYTES, out + b * ORC_QK);",
+                               "            orc_q5k_dequant_block(row + (int64_t)b * ORC_Q6K_BYTES, out + b * ORC_QK);")],
 }
 
 
