@@ -88,13 +88,15 @@ def parse(argv=None):
 def default_steps(cfg: S.Config):
     # ~1-2 s of device time at the expected step times
     return {"tiny": 20000, "decode_1tok": 100000, "decode_32tok": 4000,
-            "prefill_2048": 200, "codebook_512": 1000, "mixed_2048": 200}[cfg.name]
+            "prefill_2048": 200, "codebook_512": 1000, "mixed_2048": 200,
+            "kquant_32tok": 1000}[cfg.name]
 
 
 def floor_steps(cfg: S.Config):
     # about 0.2 s of device time: the least a per-config line is timed over
     return {"tiny": 5000, "decode_1tok": 5000, "decode_32tok": 150,
-            "prefill_2048": 60, "codebook_512": 80, "mixed_2048": 60}[cfg.name]
+            "prefill_2048": 60, "codebook_512": 80, "mixed_2048": 60,
+            "kquant_32tok": 100}[cfg.name]
 
 
 # ---------------------------------------------------------------------------
@@ -209,9 +211,12 @@ def tensor_peaks():
 def layer_path(cfg: S.Config) -> str:
     """Which kernels the library runs for this workload (mirrors its choice:
     the decode kernels up to 32 tokens for Q2_K, the tensor-core prefill
-    kernels (both formats) for rows of a multiple of 16 bytes otherwise, the
-    general kernels for the rest)."""
-    tc = (cfg.row_bytes(cfg.hidden) % 16 == 0 and
+    kernels (Q2_K and codebook) for rows of a multiple of 16 bytes otherwise,
+    the general kernels for the rest, among them every layer with a Q4_K /
+    Q5_K / Q6_K matrix)."""
+    two_bit = (S.FMT_Q2K, S.FMT_CB2)
+    tc = (cfg.format in two_bit and cfg.dn_format in two_bit and
+          cfg.row_bytes(cfg.hidden) % 16 == 0 and
           cfg.row_bytes(cfg.inter, fmt=cfg.dn_format) % 16 == 0)
     if (cfg.format == S.FMT_Q2K and cfg.dn_format == S.FMT_Q2K and cfg.inter % 16 == 0 and
             cfg.tokens <= 32):
@@ -224,7 +229,7 @@ def layer_path(cfg: S.Config) -> str:
 KERNEL_SOURCES = {
     "decode": ("decode.cu", "topk.cuh", "ptx.cuh", "tmap.cuh", "ds4g_common.cuh"),
     "tc_gateup": ("tc.cu", "ptx.cuh", "tmap.cuh", "ds4g_common.cuh"),
-    "gateup": ("gemv.cu", "ptx.cuh", "ds4g_common.cuh"),
+    "gateup": ("gemv.cu", "kquant.cuh", "ptx.cuh", "ds4g_common.cuh"),
 }
 
 
@@ -372,7 +377,8 @@ def reference_arm(args, cfg, rank, world):
 
 
 def workload_config(cfg: S.Config, copies: int, l2_note: str):
-    names = {S.FMT_Q2K: "Q2_K", S.FMT_CB2: "codebook-2bit"}
+    names = {S.FMT_Q2K: "Q2_K", S.FMT_CB2: "codebook-2bit", S.FMT_Q4K: "Q4_K", S.FMT_Q5K: "Q5_K",
+             S.FMT_Q6K: "Q6_K"}
     fmt = (names[cfg.format] if cfg.format == cfg.dn_format
            else f"{names[cfg.format]} gate/up + {names[cfg.dn_format]} down")
     return {"workload": f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.n_experts} "

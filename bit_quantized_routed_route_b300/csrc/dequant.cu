@@ -1,14 +1,16 @@
-// dequant.cu -- standalone dequantization of Q2_K and codebook-2-bit
-// super-blocks (the block layouts are GGUF's Q2_K and an IQ2_XXS-style
-// codebook format; ds4 README mirror, "Model Weights" and "Acknowledgements
-// to llama.cpp and GGML").
+// dequant.cu -- standalone dequantization of Q2_K, codebook-2-bit and the
+// Q4_K / Q5_K / Q6_K super-blocks (the block layouts are GGUF's K-quants and
+// an IQ2_XXS-style codebook format; ds4 README mirror, "Model Weights" and
+// "Acknowledgements to llama.cpp and GGML").
 //
-// Pure HBM streams: 84 (70) bytes in, 1 KB (fp32) or 512 B (fp16/bf16) out per
-// block.  One thread per 16 weights (Q2_K sub-block) or per 8 weights (codebook
-// group); the fp32 value is formed exactly as the definition states
-// (d * sc * q exact, one rounding in the subtraction), so fp32 output is
-// bit-exact and fp16/bf16 output is its round-to-nearest-even.
+// Pure HBM streams: one super-block in (84, 70, 144, 176 or 210 bytes), 1 KB
+// (fp32) or 512 B (fp16/bf16) out.  One thread per 16 weights (Q2_K and the
+// K-quants) or per 8 weights (codebook group); the fp32 value is formed
+// exactly as the definition states (exact products, at most one rounding, in
+// the subtraction), so fp32 output is bit-exact and fp16/bf16 output is its
+// round-to-nearest-even.
 #include "ds4g_common.cuh"
+#include "kquant.cuh"
 
 namespace ds4g {
 namespace {
@@ -128,6 +130,35 @@ __global__ void __launch_bounds__(256) cb2_dequant_kernel(const uint8_t *__restr
     }
 }
 
+// One thread = weights 16u .. 16u+15 of block b (a K-quant format).
+template <int FMT, int DT>
+__global__ void __launch_bounds__(256) kquant_dequant_kernel(const uint8_t *__restrict__ blocks,
+                                                             int64_t n_blocks,
+                                                             void *__restrict__ out)
+{
+    const int64_t total = n_blocks * 16;
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t b = i >> 4;
+        const int u = (int)(i & 15);
+        float w[16];
+        kquant_unit16<FMT>(blocks + b * block_bytes_of(FMT), u, w);
+        store16<DT>(out, (size_t)b * kQK + 16 * u, w);
+    }
+}
+
+template <int FMT>
+void launch_kquant_fmt(const uint8_t *blocks, int64_t n_blocks, void *out, int dtype, int grid,
+                       cudaStream_t s)
+{
+    if (dtype == DS4G_F32)
+        kquant_dequant_kernel<FMT, DS4G_F32><<<grid, 256, 0, s>>>(blocks, n_blocks, out);
+    else if (dtype == DS4G_F16)
+        kquant_dequant_kernel<FMT, DS4G_F16><<<grid, 256, 0, s>>>(blocks, n_blocks, out);
+    else
+        kquant_dequant_kernel<FMT, DS4G_BF16><<<grid, 256, 0, s>>>(blocks, n_blocks, out);
+}
+
 int grid_for(int64_t threads_needed)
 {
     DeviceInfo dev;
@@ -162,6 +193,19 @@ cudaError_t launch_cb2_dequant(const uint8_t *blocks, int64_t n_blocks, const in
         cb2_dequant_kernel<DS4G_F16><<<grid, 256, 0, s>>>(blocks, n_blocks, cb, out);
     else
         cb2_dequant_kernel<DS4G_BF16><<<grid, 256, 0, s>>>(blocks, n_blocks, cb, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_kquant_dequant(int fmt, const uint8_t *blocks, int64_t n_blocks, void *out,
+                                  int dtype, cudaStream_t s)
+{
+    const int grid = grid_for(n_blocks * 16);
+    if (fmt == DS4G_FMT_Q4K)
+        launch_kquant_fmt<DS4G_FMT_Q4K>(blocks, n_blocks, out, dtype, grid, s);
+    else if (fmt == DS4G_FMT_Q5K)
+        launch_kquant_fmt<DS4G_FMT_Q5K>(blocks, n_blocks, out, dtype, grid, s);
+    else
+        launch_kquant_fmt<DS4G_FMT_Q6K>(blocks, n_blocks, out, dtype, grid, s);
     return cudaGetLastError();
 }
 

@@ -58,8 +58,11 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     if (d->top_k < 1 || d->top_k > DS4G_MAX_TOPK || d->top_k > d->n_experts)
         return DS4G_ERR_INVALID;
     if (d->score != DS4G_SCORE_SOFTMAX && d->score != DS4G_SCORE_SIGMOID) return DS4G_ERR_INVALID;
-    if (d->format != DS4G_FMT_Q2K && d->format != DS4G_FMT_CB2) return DS4G_ERR_INVALID;
-    if (d->down_format != DS4G_FMT_Q2K && d->down_format != DS4G_FMT_CB2) return DS4G_ERR_INVALID;
+    // routed gate/up: Q2_K, codebook, Q4_K, Q5_K; routed down: also Q6_K
+    if (d->format != DS4G_FMT_Q2K && d->format != DS4G_FMT_CB2 && d->format != DS4G_FMT_Q4K &&
+        d->format != DS4G_FMT_Q5K)
+        return DS4G_ERR_INVALID;
+    if (block_bytes_of(d->down_format) == 0) return DS4G_ERR_INVALID;
     if (d->reserved != 0) return DS4G_ERR_INVALID;
     if ((d->flags & ~(DS4G_FORCE_GEMV | DS4G_FORCE_TC | DS4G_DEBUG_STALL)) != 0)
         return DS4G_ERR_INVALID;
@@ -83,14 +86,15 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     q.I_pad = (d->inter + kQK - 1) / kQK * kQK;
     q.H_blocks = d->hidden / kQK;
     q.I_blocks = q.I_pad / kQK;
-    q.gu_block_bytes = d->format == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
-    q.dn_block_bytes = d->down_format == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+    q.gu_block_bytes = block_bytes_of(d->format);
+    q.dn_block_bytes = block_bytes_of(d->down_format);
 
     const int64_t gu_logical = (int64_t)q.H_blocks * q.gu_block_bytes;
     const int64_t dn_logical = (int64_t)q.I_blocks * q.dn_block_bytes;
-    // Q2_K rows hold 4-byte aligned blocks, codebook rows 2-byte aligned ones
-    const int64_t gu_mult = d->format == DS4G_FMT_Q2K ? 4 : 2;
-    const int64_t dn_mult = d->down_format == DS4G_FMT_Q2K ? 4 : 2;
+    // Q2_K, Q4_K and Q5_K rows hold 4-byte aligned blocks, codebook and Q6_K
+    // rows 2-byte aligned ones
+    const int64_t gu_mult = q.gu_block_bytes % 4 == 0 ? 4 : 2;
+    const int64_t dn_mult = q.dn_block_bytes % 4 == 0 ? 4 : 2;
     if (d->gate_up_row_bytes < gu_logical || d->down_row_bytes < dn_logical)
         return DS4G_ERR_LAYOUT;
     if (d->gate_up_row_bytes % gu_mult || d->down_row_bytes % dn_mult) return DS4G_ERR_LAYOUT;
@@ -148,8 +152,9 @@ enum class Path { kDecode, kTensorCore, kGeneral };
 
 // Decode kernels up to kDecodeMaxT tokens (mma.sync up to kDecodePreferT,
 // tcgen05 above), the tensor-core prefill kernels for larger token counts,
-// the general kernels where neither applies (codebook format, or prefill
-// rows that are not a multiple of 16 bytes).
+// the general kernels where neither applies (codebook format in decode, the
+// Q4_K / Q5_K / Q6_K formats, or prefill rows that are not a multiple of 16
+// bytes).
 Path choose_path(const ds4g_moe_desc *d, const Plan &p)
 {
     if (d->flags & DS4G_FORCE_TC) return Path::kTensorCore;
@@ -304,6 +309,41 @@ ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out, in
                                         out_dtype, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+ds4g_status kquant_dequant(int fmt, const void *blocks, int64_t n_blocks, void *out,
+                           int32_t out_dtype, void *stream)
+{
+    if (n_blocks < 0) return DS4G_ERR_INVALID;
+    if (out_dtype != DS4G_F32 && out_dtype != DS4G_F16 && out_dtype != DS4G_BF16)
+        return DS4G_ERR_INVALID;
+    if (n_blocks == 0) return DS4G_OK;
+    if (!blocks || !out) return DS4G_ERR_INVALID;
+    // every block of a 4-byte aligned Q4_K / Q5_K array is 4-byte aligned;
+    // Q6_K blocks (210 bytes) only 2-byte aligned
+    if (!aligned(blocks, fmt == DS4G_FMT_Q6K ? 2 : 4) || !aligned(out, 16)) return DS4G_ERR_LAYOUT;
+    return from_cuda(launch_kquant_dequant(fmt, static_cast<const uint8_t *>(blocks), n_blocks, out,
+                                           out_dtype, static_cast<cudaStream_t>(stream)));
+}
+}  // namespace
+
+ds4g_status ds4g_q4k_dequant(const void *blocks, int64_t n_blocks, void *out, int32_t out_dtype,
+                             void *stream)
+{
+    return kquant_dequant(DS4G_FMT_Q4K, blocks, n_blocks, out, out_dtype, stream);
+}
+
+ds4g_status ds4g_q5k_dequant(const void *blocks, int64_t n_blocks, void *out, int32_t out_dtype,
+                             void *stream)
+{
+    return kquant_dequant(DS4G_FMT_Q5K, blocks, n_blocks, out, out_dtype, stream);
+}
+
+ds4g_status ds4g_q6k_dequant(const void *blocks, int64_t n_blocks, void *out, int32_t out_dtype,
+                             void *stream)
+{
+    return kquant_dequant(DS4G_FMT_Q6K, blocks, n_blocks, out, out_dtype, stream);
+}
+
 ds4g_status ds4g_cb2_dequant(const void *blocks, int64_t n_blocks, const int8_t *codebook,
                              void *out, int32_t out_dtype, void *stream)
 {
@@ -361,6 +401,7 @@ int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T)
     if (T <= 0 || make_plan(desc, T, &p) != DS4G_OK) return 0;
     const Path path = choose_path(desc, p);
     if (path == Path::kDecode) return 2;     // reset/convert, fused layer kernel
+    if (path == Path::kTensorCore && !tc_path_supported(p, desc)) return 0;   // refused
     return route_launches(T) +
            (path == Path::kDecode       ? 0
             : path == Path::kTensorCore ? kTcPathLaunches + (desc->tc_min_tokens > 0 ? kSplitLaunches : 0)

@@ -16,6 +16,20 @@ namespace ds4g {
 constexpr int kQK = 256;         // weights per super-block
 constexpr int kQ2KBytes = 84;    // Q2_K super-block
 constexpr int kCB2Bytes = 70;    // codebook-2-bit super-block
+constexpr int kQ4KBytes = 144;   // Q4_K super-block
+constexpr int kQ5KBytes = 176;   // Q5_K super-block
+constexpr int kQ6KBytes = 210;   // Q6_K super-block
+
+// Super-block bytes of a ds4g_format (0 for an unknown one).
+__host__ __device__ constexpr int block_bytes_of(int fmt)
+{
+    return fmt == DS4G_FMT_Q2K ? kQ2KBytes
+         : fmt == DS4G_FMT_CB2 ? kCB2Bytes
+         : fmt == DS4G_FMT_Q4K ? kQ4KBytes
+         : fmt == DS4G_FMT_Q5K ? kQ5KBytes
+         : fmt == DS4G_FMT_Q6K ? kQ6KBytes
+         : 0;
+}
 
 // ---------------------------------------------------------------------------
 // Workspace plan: byte offsets of every scratch array inside the caller's
@@ -26,8 +40,8 @@ struct Plan {
     int32_t I_pad;          // inter rounded up to a multiple of 256 (down K)
     int32_t H_blocks;       // hidden / 256
     int32_t I_blocks;       // I_pad / 256
-    int32_t gu_block_bytes; // 84 or 70 (W_gate, W_up)
-    int32_t dn_block_bytes; // 84 or 70 (W_down)
+    int32_t gu_block_bytes; // super-block bytes of W_gate, W_up
+    int32_t dn_block_bytes; // super-block bytes of W_down
     size_t ids, wts, counts, offsets, perm, slot_pos, active, meta;
     size_t status;          // int32 device status word (DS4G_OK or DS4G_ERR_TIMEOUT)
     size_t sync;            // [decode_sync_words] int32 counters of the decode kernels
@@ -77,6 +91,9 @@ cudaError_t launch_q2k_dequant(const uint8_t *blocks, int64_t n_blocks, void *ou
                                cudaStream_t s);
 cudaError_t launch_cb2_dequant(const uint8_t *blocks, int64_t n_blocks, const int8_t *cb,
                                void *out, int dtype, cudaStream_t s);
+// Q4_K / Q5_K / Q6_K (fmt) super-blocks to fp32 / fp16 / bf16.
+cudaError_t launch_kquant_dequant(int fmt, const uint8_t *blocks, int64_t n_blocks, void *out,
+                                  int dtype, cudaStream_t s);
 
 struct LayerArgs {
     int H, I, I_pad, E, k, A, T;

@@ -1,5 +1,6 @@
 // gemv.cu -- the general expert path: grouped dequant-and-dot on CUDA cores,
-// correct for every segment size and both formats.
+// correct for every segment size and every weight format (Q2_K, codebook,
+// and the Q4_K / Q5_K / Q6_K routed formats, which only this path runs).
 //
 // Per active expert e with segment tokens t_0..t_{n-1} (the assignments
 // perm[offsets[e] .. offsets[e+1]-1]):
@@ -17,6 +18,7 @@
 // (active expert, 8-row tile) are claimed by a persistent grid from the device
 // list written by the routing kernels, so the host never reads the routing.
 #include "ds4g_common.cuh"
+#include "kquant.cuh"
 
 namespace ds4g {
 namespace {
@@ -46,6 +48,8 @@ __device__ __forceinline__ void dequant16(const uint8_t *__restrict__ blk, int u
                 w[4 * v + by] = scale_part * (float)q - min_part;
             }
         }
+    } else if constexpr (FMT != DS4G_FMT_CB2) {
+        kquant_unit16<FMT>(blk, u, w);
     } else {
         uint32_t dbits = (uint32_t)__ldg(blk + 68) | ((uint32_t)__ldg(blk + 69) << 8);
         int G = u >> 1;
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_kernel(LayerArgs a)
         __syncthreads();
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int bb = FMT == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+    const int bb = block_bytes_of(FMT);
     const int tiles = a.I_pad / kWarps;
     const int n_items = *a.n_active * tiles;
     const int units = (a.H / kQK) * 16;
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(kWarps * 32) down_kernel(LayerArgs a)
         __syncthreads();
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int bb = FMT == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+    const int bb = block_bytes_of(FMT);
     const int tiles = a.H / kWarps;
     const int n_items = *a.n_active * tiles;
     const int units = (a.I_pad / kQK) * 16;
@@ -236,24 +240,32 @@ cudaError_t launch_combine(const LayerArgs &a, const DeviceInfo &dev, cudaStream
 }
 
 // Gate/up in the W_gate / W_up format, down in the W_down format (they may
-// differ: the shipping mix has codebook gate/up and Q2_K down).
+// differ: the shipping mix has codebook gate/up and Q2_K down; Q6_K is a
+// down-only format).
 cudaError_t launch_gemv_gateup(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s)
 {
     const int grid = min(min(a.E, a.A) * (a.I_pad / kWarps), dev.sm_count * 8);
-    if (a.gu_format == DS4G_FMT_Q2K)
-        gateup_kernel<DS4G_FMT_Q2K><<<grid, kWarps * 32, 0, s>>>(a);
-    else
-        gateup_kernel<DS4G_FMT_CB2><<<grid, kWarps * 32, 0, s>>>(a);
+    switch (a.gu_format) {
+    case DS4G_FMT_Q2K: gateup_kernel<DS4G_FMT_Q2K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_CB2: gateup_kernel<DS4G_FMT_CB2><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_Q4K: gateup_kernel<DS4G_FMT_Q4K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_Q5K: gateup_kernel<DS4G_FMT_Q5K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 
 cudaError_t launch_gemv_down(const LayerArgs &a, const DeviceInfo &dev, cudaStream_t s)
 {
     const int grid = min(min(a.E, a.A) * (a.H / kWarps), dev.sm_count * 8);
-    if (a.dn_format == DS4G_FMT_Q2K)
-        down_kernel<DS4G_FMT_Q2K><<<grid, kWarps * 32, 0, s>>>(a);
-    else
-        down_kernel<DS4G_FMT_CB2><<<grid, kWarps * 32, 0, s>>>(a);
+    switch (a.dn_format) {
+    case DS4G_FMT_Q2K: down_kernel<DS4G_FMT_Q2K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_CB2: down_kernel<DS4G_FMT_CB2><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_Q4K: down_kernel<DS4G_FMT_Q4K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_Q5K: down_kernel<DS4G_FMT_Q5K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_Q6K: down_kernel<DS4G_FMT_Q6K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

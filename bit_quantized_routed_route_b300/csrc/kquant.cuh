@@ -1,0 +1,111 @@
+// kquant.cuh -- device decoders of the higher-bit routed-expert formats:
+// Q4_K and Q5_K (routed gate/up and down) and Q6_K (routed down), the GGUF
+// K-quant super-blocks of 256 weights (ds4 README mirror, "Model Weights",
+// which lists the routed expert formats, and "Acknowledgements to llama.cpp
+// and GGML" for the GGUF layouts).
+//
+//   Q4_K (144 B): d fp16 @0, dmin fp16 @2, 12 packed scale bytes @4, qs @16
+//   Q5_K (176 B): d @0, dmin @2, packed scales @4, qh[32] @16, qs @48
+//   Q6_K (210 B): ql[128] @0, qh[64] @128, int8 scales[16] @192, d fp16 @208
+//
+// Q4_K / Q5_K: eight 32-weight sub-blocks with 6-bit scale sc_s and min m_s
+// (sub-blocks 0..3 in the low six bits of bytes 0..3 / 4..7, sub-blocks 4..7
+// in the nibbles of bytes 8..11 with their top two bits in the top bits of
+// bytes 0..7); weight 64c + l / 64c + 32 + l in the low / high nibble of
+// qs[32c + l]; Q5_K's fifth bit of weight 32s + l is bit s of qh[l];
+//   w = d * sc_s * q - dmin * m_s.
+// Q6_K: weight j (h = j/128, u = (j%128)/32, l = j%32) has its low nibble in
+// nibble u>>1 of ql[64h + 32(u&1) + l], its top two bits in bits 2u, 2u+1 of
+// qh[32h + l]; q = that 6-bit value - 32;  w = d * scales[j/16] * q.
+// Every product is exact in fp32 (at most 24 significant bits), so the
+// values below are exactly the definitions' (one rounding, in the
+// subtraction, for Q4_K / Q5_K; none for Q6_K).
+#pragma once
+
+#include "ds4g_common.cuh"
+
+namespace ds4g {
+
+// 6-bit scale and min of sub-block s of a Q4_K / Q5_K block (p = byte 4).
+__device__ __forceinline__ void k4_scale_min(const uint8_t *__restrict__ p, int s, int &sc, int &m)
+{
+    if (s < 4) {
+        sc = __ldg(p + s) & 63;
+        m = __ldg(p + s + 4) & 63;
+    } else {
+        const int b = __ldg(p + s + 4);
+        sc = (b & 15) | ((__ldg(p + s - 4) >> 6) << 4);
+        m = (b >> 4) | ((__ldg(p + s) >> 6) << 4);
+    }
+}
+
+// 16 consecutive bytes starting at a 16-byte offset of a block that is at
+// least 2-byte aligned (Q6_K) or 4-byte aligned (Q4_K, Q5_K).
+template <int ALIGN4>
+__device__ __forceinline__ void load16(const uint8_t *__restrict__ p, uint32_t (&v)[4])
+{
+    if (ALIGN4) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __ldg(reinterpret_cast<const uint32_t *>(p) + i);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = __ldg(reinterpret_cast<const uint16_t *>(p) + 2 * i);
+            const uint32_t hi = __ldg(reinterpret_cast<const uint16_t *>(p) + 2 * i + 1);
+            v[i] = lo | (hi << 16);
+        }
+    }
+}
+
+__device__ __forceinline__ int byte_of(const uint32_t (&v)[4], int i)
+{
+    return (v[i >> 2] >> (8 * (i & 3))) & 0xFF;
+}
+
+// fp32 weights 16u .. 16u+15 of one K-quant super-block (FMT = DS4G_FMT_Q4K,
+// DS4G_FMT_Q5K or DS4G_FMT_Q6K).
+template <int FMT>
+__device__ __forceinline__ void kquant_unit16(const uint8_t *__restrict__ blk, int u, float (&w)[16])
+{
+    if constexpr (FMT == DS4G_FMT_Q4K || FMT == DS4G_FMT_Q5K) {
+        const int s = u >> 1;                       // 32-weight sub-block
+        const int c = u >> 2;                       // 64-weight chunk
+        const int l0 = 16 * (u & 1);                // first lane
+        const int hi = (u >> 1) & 1;                // high nibble for odd sub-blocks
+        const uint32_t dd = (uint32_t)__ldg(reinterpret_cast<const uint16_t *>(blk)) |
+                            ((uint32_t)__ldg(reinterpret_cast<const uint16_t *>(blk) + 1) << 16);
+        const float d = half_bits(dd & 0xFFFFu), dmin = half_bits(dd >> 16);
+        int sc, m;
+        k4_scale_min(blk + 4, s, sc, m);
+        const float scale_part = d * (float)sc;
+        const float min_part = dmin * (float)m;
+        uint32_t qs[4];
+        load16<1>(blk + (FMT == DS4G_FMT_Q4K ? 16 : 48) + 32 * c + l0, qs);
+        uint32_t qh[4] = {0, 0, 0, 0};
+        if constexpr (FMT == DS4G_FMT_Q5K) load16<1>(blk + 16 + l0, qh);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            int q = (byte_of(qs, i) >> (4 * hi)) & 15;
+            if constexpr (FMT == DS4G_FMT_Q5K) q += 16 * ((byte_of(qh, i) >> s) & 1);
+            w[i] = scale_part * (float)q - min_part;
+        }
+    } else {
+        static_assert(FMT == DS4G_FMT_Q6K, "K-quant format");
+        const int h = u >> 3;                       // 128-weight half
+        const int uq = (u & 7) >> 1;                // 32-weight quarter of the half
+        const int l0 = 16 * (u & 1);
+        const float d = half_bits(__ldg(reinterpret_cast<const uint16_t *>(blk + 208)));
+        const float scale_part = d * (float)(int8_t)__ldg(blk + 192 + u);
+        uint32_t ql[4], qh[4];
+        load16<0>(blk + 64 * h + 32 * (uq & 1) + l0, ql);
+        load16<0>(blk + 128 + 32 * h + l0, qh);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int low = (byte_of(ql, i) >> (4 * (uq >> 1))) & 15;
+            const int high = (byte_of(qh, i) >> (2 * uq)) & 3;
+            w[i] = scale_part * (float)(low + 16 * high - 32);
+        }
+    }
+}
+
+}  // namespace ds4g

@@ -946,8 +946,9 @@ cudaError_t weight_map(CUtensorMap *m, const void *base, int64_t row_bytes, int6
 
 bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d)
 {
-    return p.A > 0 && d->gate_up_row_bytes % 16 == 0 && d->down_row_bytes % 16 == 0 &&
-           p.H % kBM == 0;
+    const auto fmt_ok = [](int f) { return f == DS4G_FMT_Q2K || f == DS4G_FMT_CB2; };
+    return p.A > 0 && fmt_ok(d->format) && fmt_ok(d->down_format) &&
+           d->gate_up_row_bytes % 16 == 0 && d->down_row_bytes % 16 == 0 && p.H % kBM == 0;
 }
 
 int32_t tc_max_tiles(int32_t E, int32_t A) { return E + A / kNT + 1; }

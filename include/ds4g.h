@@ -87,7 +87,10 @@ typedef enum ds4g_score {
 
 typedef enum ds4g_format {
     DS4G_FMT_Q2K = 0,          /* 84-byte Q2_K super-blocks                         */
-    DS4G_FMT_CB2 = 1           /* 70-byte codebook-2-bit super-blocks               */
+    DS4G_FMT_CB2 = 1,          /* 70-byte codebook-2-bit super-blocks               */
+    DS4G_FMT_Q4K = 2,          /* 144-byte Q4_K super-blocks (gate/up or down)      */
+    DS4G_FMT_Q5K = 3,          /* 176-byte Q5_K super-blocks (gate/up or down)      */
+    DS4G_FMT_Q6K = 4           /* 210-byte Q6_K super-blocks (down only)            */
 } ds4g_format;
 
 typedef enum ds4g_dtype {
@@ -125,7 +128,8 @@ enum {
  *   hidden % 256 == 0, 256 <= hidden <= DS4G_MAX_HIDDEN;
  *   1 <= inter <= DS4G_MAX_INTER; 1 <= n_experts <= 256;
  *   1 <= top_k <= min(8, n_experts);
- *   row_bytes >= ceil(K/256) * block_bytes and a multiple of 2;
+ *   row_bytes >= ceil(K/256) * block_bytes and a multiple of 4 (Q2_K,
+ *   Q4_K, Q5_K) or 2 (codebook, Q6_K);
  *   expert strides >= rows * row_bytes and multiples of 16;
  *   w_gate, w_up, w_down 16-byte aligned;
  *   DS4G_FORCE_TC additionally needs row_bytes % 16 == 0.
@@ -139,7 +143,14 @@ enum {
  * format / down_format: the block format of W_gate and W_up / of W_down.
  * The shipping mix of the ds4 weights is DS4G_FMT_CB2 / DS4G_FMT_Q2K
  * (IQ2_XXS up/gate, Q2_K down: ds4 README mirror, "Model Weights").  Set
- * both; the codebook is required when either is DS4G_FMT_CB2.
+ * both; the codebook is required when either is DS4G_FMT_CB2.  The routed
+ * higher-bit formats of the same page ("Model Weights": gate/up in Q2_K,
+ * Q4_K or Q5_K, down in Q2_K, Q4_K, Q5_K or Q6_K) are accepted with those
+ * roles: format in {Q2K, CB2, Q4K, Q5K}, down_format in {Q2K, CB2, Q4K,
+ * Q5K, Q6K} (else DS4G_ERR_INVALID).  Layers with a K-quant matrix run on
+ * the general (GEMV) kernels; DS4G_FORCE_TC then returns
+ * DS4G_ERR_UNSUPPORTED.  Row alignment: rows of Q2_K, Q4_K and Q5_K blocks
+ * a multiple of 4 bytes, of codebook and Q6_K blocks a multiple of 2.
  * reserved: must be 0.
  */
 typedef struct ds4g_moe_desc {
@@ -200,6 +211,33 @@ DS4G_API ds4g_status ds4g_route_topk(const float *logits, int32_t T, int32_t E, 
  * DS4G_ERR_LAYOUT (alignment); DS4G_ERR_CUDA.  n_blocks == 0 is a no-op.
  */
 DS4G_API ds4g_status ds4g_q2k_dequant(const void *blocks, int64_t n_blocks, void *out,
+                             int32_t out_dtype, void *stream);
+
+/*
+ * ds4g_q4k_dequant / ds4g_q5k_dequant / ds4g_q6k_dequant -- passage: the
+ * routed expert formats Q4_K, Q5_K (gate/up and down) and Q6_K (down) (ds4
+ * README mirror, "Model Weights") in the GGUF K-quant layouts kept from
+ * llama.cpp (same page, "Acknowledgements to llama.cpp and GGML"):
+ *   Q4_K, 144 bytes: d, dmin (fp16), 12 bytes of packed 6-bit scales and
+ *         mins of eight 32-weight sub-blocks, 128 bytes of 4-bit quants;
+ *         w = d * sc_s * q - dmin * m_s;
+ *   Q5_K, 176 bytes: as Q4_K plus 32 bytes of fifth bits (bit s of byte l
+ *         for weight 32s + l) before the low nibbles;
+ *   Q6_K, 210 bytes: 128 bytes of low nibbles, 64 bytes of top two bits,
+ *         16 int8 scales of 16-weight sub-blocks, d (fp16);
+ *         w = d * scale * (q6 - 32).
+ * n_blocks consecutive super-blocks (`blocks` 4-byte aligned for Q4_K /
+ * Q5_K, 2-byte aligned for Q6_K) to n_blocks * 256 values of out_dtype in
+ * `out` (16-byte aligned).  fp32 output is exactly the definition (every
+ * product is exact in fp32; Q4_K / Q5_K round once, in the subtraction);
+ * fp16 / bf16 output is that value rounded to nearest even.
+ * Errors as ds4g_q2k_dequant.
+ */
+DS4G_API ds4g_status ds4g_q4k_dequant(const void *blocks, int64_t n_blocks, void *out,
+                             int32_t out_dtype, void *stream);
+DS4G_API ds4g_status ds4g_q5k_dequant(const void *blocks, int64_t n_blocks, void *out,
+                             int32_t out_dtype, void *stream);
+DS4G_API ds4g_status ds4g_q6k_dequant(const void *blocks, int64_t n_blocks, void *out,
                              int32_t out_dtype, void *stream);
 
 /*

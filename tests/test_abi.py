@@ -91,6 +91,9 @@ def test_noalloc_scratch_covers_a_32_token_decode_of_the_7168_layer():
     (dict(score=2), D.ERR_INVALID),
     (dict(format=5), D.ERR_INVALID),
     (dict(down_format=5), D.ERR_INVALID),
+    (dict(format=D.FMT_Q6K, gate_up_row_bytes=210, gate_up_expert_stride=128 * 224),
+     D.ERR_INVALID),                                                       # Q6_K is down-only
+    (dict(down_format=D.FMT_Q4K, down_row_bytes=146), D.ERR_LAYOUT),       # Q4_K rows % 4
     (dict(reserved=1), D.ERR_INVALID),
     (dict(down_format=D.FMT_CB2, down_row_bytes=70), D.ERR_INVALID),      # no codebook
     (dict(flags=D.FORCE_GEMV | D.FORCE_TC), D.ERR_INVALID),
@@ -156,6 +159,13 @@ def test_dequant_validation():
     assert L.ds4g_q2k_dequant(FAKE, 4, FAKE + 4, D.F16, None) == D.ERR_LAYOUT
     assert L.ds4g_cb2_dequant(FAKE, 4, None, FAKE, D.F32, None) == D.ERR_INVALID
     assert L.ds4g_cb2_dequant(FAKE + 1, 4, FAKE, FAKE, D.F32, None) == D.ERR_LAYOUT
+    for fn, balign in ((L.ds4g_q4k_dequant, 4), (L.ds4g_q5k_dequant, 4), (L.ds4g_q6k_dequant, 2)):
+        assert fn(FAKE, 0, FAKE, D.F32, None) == D.OK
+        assert fn(FAKE, -1, FAKE, D.F32, None) == D.ERR_INVALID
+        assert fn(FAKE, 4, FAKE, 3, None) == D.ERR_INVALID
+        assert fn(None, 4, FAKE, D.F32, None) == D.ERR_INVALID
+        assert fn(FAKE + balign // 2, 4, FAKE, D.F32, None) == D.ERR_LAYOUT
+        assert fn(FAKE, 4, FAKE + 8, D.BF16, None) == D.ERR_LAYOUT
 
 
 def test_routing_view_points_inside_the_workspace():
@@ -174,8 +184,8 @@ def layer_desc(H, I, E, k, fmt=None, flags=0, align=1, down_fmt=None, tc_min_tok
     W_down in `down_fmt` (default: fmt)."""
     fmt = D.FMT_Q2K if fmt is None else fmt
     down_fmt = fmt if down_fmt is None else down_fmt
-    bb = 84 if fmt == D.FMT_Q2K else 70
-    dbb = 84 if down_fmt == D.FMT_Q2K else 70
+    sizes = {D.FMT_Q2K: 84, D.FMT_CB2: 70, D.FMT_Q4K: 144, D.FMT_Q5K: 176, D.FMT_Q6K: 210}
+    bb, dbb = sizes[fmt], sizes[down_fmt]
     gr, dr = H // 256 * bb, -(-I // 256) * dbb
     gr, dr = -(-gr // align) * align, -(-dr // align) * align
     return desc(hidden=H, inter=I, n_experts=E, top_k=k, format=fmt, down_format=down_fmt,
@@ -225,6 +235,12 @@ def test_mixed_format_descriptor_is_accepted():
     # per-segment split on the tensor-core path: + GEMV gate/up and down
     ((7168, 2048, 256, 8), 2048, dict(tc_min_tokens=16), 2 + 5 + 2),
     ((7168, 2048, 256, 8), 16, dict(tc_min_tokens=16), 2),        # decode kernels: no split
+    # the Q4_K / Q5_K / Q6_K formats run on the GEMV kernels at every T; the
+    # tensor-core kernels refuse them
+    ((7168, 2048, 256, 8), 32, dict(fmt=D.FMT_Q4K, down_fmt=D.FMT_Q6K), 1 + 3),
+    ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_Q5K), 2 + 3),
+    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_Q2K, down_fmt=D.FMT_Q4K), 1 + 3),
+    ((7168, 2048, 256, 8), 64, dict(fmt=D.FMT_Q4K, flags=D.FORCE_TC), 0),
 ])
 def test_path_choice_by_launch_count(shape, T, kw, launches):
     """The per-call path choice documented under ds4g_moe_forward ("Path"),

@@ -98,3 +98,66 @@ def test_dequant_worked_blocks(orc):
         exp = np.zeros(256, dtype=np.float32)
         exp[16 * int(s):16 * int(s) + 16] = float(val)
         assert np.array_equal(got, exp)
+
+
+# ---------------------------------------------------------------------------
+# Q4_K / Q5_K / Q6_K (the routed higher-bit formats)
+# ---------------------------------------------------------------------------
+
+KQ = {  # format: (block bytes, fp16 field offsets, library entry, oracle method)
+    S.FMT_Q4K: (144, (0, 2), D.q4k_dequant, "q4k_dequant"),
+    S.FMT_Q5K: (176, (0, 2), D.q5k_dequant, "q5k_dequant"),
+    S.FMT_Q6K: (210, (208,), D.q6k_dequant, "q6k_dequant"),
+}
+
+
+def _random_kquant(fmt, n, seed):
+    bb, offs, _, _ = KQ[fmt]
+    rng = np.random.default_rng(seed)
+    blk = rng.integers(0, 256, size=(n, bb), dtype=np.uint8)
+    for off in offs:
+        h = rng.integers(0, 0x7C00, size=n).astype(np.uint16)
+        h |= rng.integers(0, 2, size=n).astype(np.uint16) << 15
+        blk[:, off:off + 2] = h.view(np.uint8).reshape(n, 2)
+    return blk
+
+
+@pytest.mark.parametrize("fmt", [S.FMT_Q4K, S.FMT_Q5K, S.FMT_Q6K], ids=["q4k", "q5k", "q6k"])
+@pytest.mark.parametrize("n", [1, 3, 37, 4096 + 5, 200_000])
+def test_kquant_dequant_bit_exact(orc, fmt, n):
+    _, _, fn, ref_name = KQ[fmt]
+    blk = _random_kquant(fmt, n, 1000 * fmt + n)
+    ref = getattr(orc, ref_name)(blk)
+    got = _run(fn, blk, n, D.F32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    assert np.array_equal(_run(fn, blk, n, D.F16), _rne_f16(ref))
+    assert np.array_equal(_run(fn, blk, n, D.BF16), S.f32_to_bf16(ref))
+
+
+@pytest.mark.parametrize("fmt", [S.FMT_Q4K, S.FMT_Q5K, S.FMT_Q6K], ids=["q4k", "q5k", "q6k"])
+def test_kquant_dequant_generated_rows(orc, fmt):
+    bb, _, fn, ref_name = KQ[fmt]
+    W = S.make_experts(9, S.TENSOR_DOWN, 2, 64, 2048, fmt, 8 * bb)
+    ref = getattr(orc, ref_name)(W)
+    got = _run(fn, W, W.size // bb, D.F32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+class _GpuDecoders:
+    """The library's K-quant kernels behind the oracle's method names, so
+    the hand-derived worked and one-hot pins run against the GPU as well."""
+
+    def q4k_dequant(self, blk):
+        return _run(D.q4k_dequant, blk, blk.size // 144, D.F32)
+
+    def q5k_dequant(self, blk):
+        return _run(D.q5k_dequant, blk, blk.size // 176, D.F32)
+
+    def q6k_dequant(self, blk):
+        return _run(D.q6k_dequant, blk, blk.size // 210, D.F32)
+
+
+@pytest.mark.parametrize("pin", [P.pin_q4k_worked, P.pin_q5k_worked, P.pin_q6k_worked,
+                                 P.pin_kquant_onehot], ids=lambda p: p.__name__)
+def test_kquant_worked_blocks(pin):
+    pin(_GpuDecoders())

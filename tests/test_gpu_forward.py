@@ -1,10 +1,11 @@
-"""ds4g_moe_forward against the oracle on the five synthetic workloads and on
-small edge-case layers: routing bit-exact, per-token relative L2 <= 1e-3 and
+"""ds4g_moe_forward against the oracle on the synthetic workloads and on small
+edge-case layers: routing bit-exact, per-token relative L2 <= 1e-3 and
 max-abs <= 5e-3 * max|ref| on the output.
 
 Full-size workloads run at their full token counts (the launch configuration
-the benchmark times).  The oracle checks every token of the three decode
-workloads; for prefill_2048 and codebook_512 it checks at least 64 tokens
+the benchmark times).  The oracle checks every token of the decode-sized
+workloads (up to 32 tokens, the K-quant layer among them); for prefill_2048,
+codebook_512 and mixed_2048 it checks at least 64 tokens
 chosen to reach every code path (first and last token of the heaviest
 segments, both sides of each 128-token tile boundary in them, tokens routed
 to one-token segments, then seeded random ones).  Its result for a token does
@@ -22,7 +23,7 @@ from gpu_helpers import (boundary_tokens, cached_layer, check_output, check_rout
 pytestmark = pytest.mark.gpu
 
 SAMPLE = {"tiny": None, "decode_1tok": None, "decode_32tok": None, "prefill_2048": 64,
-          "codebook_512": 64, "mixed_2048": 64}
+          "codebook_512": 64, "mixed_2048": 64, "kquant_32tok": None}
 
 
 @pytest.mark.parametrize("name", list(S.CONFIGS))
@@ -51,6 +52,12 @@ def test_forward_workloads(orc, name):
     dict(H=1024, I=384, E=16, k=2, T=1, score=S.SCORE_SIGMOID, logits_kind=S.LOGITS_UNIFORM),
     dict(H=512, I=256, E=5, k=2, T=9, fmt=S.FMT_CB2, align=16),
     dict(H=512, I=200, E=7, k=3, T=17, fmt=S.FMT_CB2, align=2),
+    # the routed higher-bit formats (general kernels)
+    dict(H=512, I=320, E=5, k=2, T=9, fmt=S.FMT_Q4K, down_fmt=S.FMT_Q6K),
+    dict(H=768, I=256, E=6, k=3, T=40, fmt=S.FMT_Q5K),
+    dict(H=512, I=200, E=4, k=2, T=3, fmt=S.FMT_Q2K, down_fmt=S.FMT_Q5K),
+    dict(H=256, I=512, E=3, k=3, T=2, fmt=S.FMT_Q4K, score=S.SCORE_SIGMOID,
+         logits_kind=S.LOGITS_UNIFORM),
 ])
 def test_forward_edge_layers(orc, kw):
     layer = P.small_layer(seed=sum(kw.get(x, 0) for x in ("H", "I", "E", "T")), **kw)
@@ -88,3 +95,21 @@ def test_host_entry_point_matches_device_entry_point():
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
     D.check(D.moe_forward_host(L.desc, x_h, l_h, T, y_h, ws, ws_bytes))
     assert np.array_equal(y_h.numpy().view(np.uint32), y_dev.view(np.uint32))
+
+
+def test_forced_tensor_core_refuses_kquant_layers():
+    """The tensor-core kernels take the 2-bit formats only: forcing them on a
+    Q4_K layer returns DS4G_ERR_UNSUPPORTED without touching y."""
+    # Q4_K rows of 2 and 1 blocks are multiples of 16 bytes, so the layout
+    # checks pass and the refusal comes from the format
+    layer = P.small_layer(seed=5, H=512, I=256, E=4, k=2, T=40, fmt=S.FMT_Q4K)
+    L = to_device(layer, flags=D.FORCE_TC)
+    dev = torch.device("cuda")
+    T, H = layer["x"].shape
+    x = torch.from_numpy(layer["x"].view(np.int16)).to(dev)
+    lg = torch.from_numpy(layer["logits"]).to(dev)
+    y = torch.full((T, H), 7.0, dtype=torch.float32, device=dev)
+    ws = torch.empty(L.workspace_bytes(T), dtype=torch.uint8, device=dev)
+    assert D.moe_forward(L.desc, x, lg, T, y, ws) == D.ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bool((y == 7.0).all())
