@@ -35,7 +35,8 @@ EXPORTED = (
     "ds4g_moe_forward", "ds4g_moe_forward_host", "ds4g_moe_routing_view",
     "ds4g_moe_forward_phased", "ds4g_moe_forward_launches", "ds4g_moe_device_status",
     "ds4g_status_string", "ds4g_abi_version", "ds4g_last_cuda_error",
-    "ds4g_moe_forward_noalloc",
+    "ds4g_moe_forward_noalloc", "ds4g_expert_cache_create", "ds4g_expert_cache_workspace_bytes",
+    "ds4g_expert_cache_forward", "ds4g_expert_cache_stats", "ds4g_expert_cache_destroy",
 )
 
 
@@ -55,11 +56,11 @@ class MoeDesc(ctypes.Structure):
         ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
         ("score", ctypes.c_int32), ("format", ctypes.c_int32),
         ("flags", ctypes.c_int32), ("tc_min_tokens", ctypes.c_int32),
-        ("down_format", ctypes.c_int32), ("reserved", ctypes.c_int32),
+        ("down_format", ctypes.c_int32), ("n_slots", ctypes.c_int32),
         ("w_gate", ctypes.c_void_p), ("w_up", ctypes.c_void_p), ("w_down", ctypes.c_void_p),
         ("gate_up_row_bytes", ctypes.c_int64), ("down_row_bytes", ctypes.c_int64),
         ("gate_up_expert_stride", ctypes.c_int64), ("down_expert_stride", ctypes.c_int64),
-        ("codebook", ctypes.c_void_p),
+        ("codebook", ctypes.c_void_p), ("expert_slot", ctypes.c_void_p),
     ]
 
 
@@ -78,6 +79,12 @@ def _load() -> ctypes.CDLL:
         "ds4g_q4k_dequant": (i32, [vp, i64, vp, i32, vp]),
         "ds4g_q5k_dequant": (i32, [vp, i64, vp, i32, vp]),
         "ds4g_q6k_dequant": (i32, [vp, i64, vp, i32, vp]),
+        "ds4g_expert_cache_create": (i32, [ctypes.POINTER(MoeDesc), i32, ctypes.POINTER(vp)]),
+        "ds4g_expert_cache_workspace_bytes": (ctypes.c_size_t, [vp, i32]),
+        "ds4g_expert_cache_forward": (i32, [vp, vp, vp, i32, vp, vp, ctypes.c_size_t, vp]),
+        "ds4g_expert_cache_stats": (i32, [vp, ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                          ctypes.POINTER(i64)]),
+        "ds4g_expert_cache_destroy": (None, [vp]),
         "ds4g_moe_workspace_bytes": (sz, [pdesc, i32]),
         "ds4g_moe_forward": (i32, [pdesc, vp, vp, i32, vp, vp, sz, vp]),
         "ds4g_moe_forward_host": (i32, [pdesc, vp, vp, i32, vp, vp, sz, vp]),
@@ -248,7 +255,7 @@ class Layer:
         d.hidden, d.inter, d.n_experts, d.top_k = hidden, inter, n_experts, top_k
         d.score, d.format, d.flags, d.tc_min_tokens = score, fmt, flags, tc_min_tokens
         d.down_format = fmt if down_fmt is None else down_fmt
-        d.reserved = 0
+        d.n_slots = 0
         d.w_gate, d.w_up, d.w_down = _ptr(w_gate), _ptr(w_up), _ptr(w_down)
         d.gate_up_row_bytes = w_gate.shape[-1]
         d.down_row_bytes = w_down.shape[-1]
@@ -272,3 +279,45 @@ class Layer:
 
     def forward(self, x, logits, y, workspace, stream=None) -> None:
         check(moe_forward(self.desc, x, logits, x.shape[0], y, workspace, stream=stream))
+
+
+class ExpertCache:
+    """ds4g_expert_cache: a layer whose expert weights live in host memory
+    (page-locked uint8 tensors [E x N x row_bytes]), ``n_slots`` experts of
+    it resident on the current device and uploaded on misses.  ``forward``
+    returns the raw status (DS4G_ERR_UNSUPPORTED when a call routes to more
+    experts than there are slots)."""
+
+    def __init__(self, hidden, inter, n_experts, top_k, score, fmt, w_gate, w_up, w_down,
+                 n_slots, codebook=None, flags=0, down_fmt=None):
+        self.host = Layer(hidden, inter, n_experts, top_k, score, fmt, w_gate, w_up, w_down,
+                          codebook, flags=flags, down_fmt=down_fmt)
+        h = ctypes.c_void_p()
+        check(_lib.ds4g_expert_cache_create(ctypes.byref(self.host.desc), n_slots, ctypes.byref(h)))
+        self.handle = h
+
+    def workspace_bytes(self, T: int) -> int:
+        return _lib.ds4g_expert_cache_workspace_bytes(self.handle, T)
+
+    def forward(self, x, logits, y, workspace, ws_bytes=None, stream=None) -> int:
+        if ws_bytes is None:
+            ws_bytes = workspace.numel() * workspace.element_size()
+        return _lib.ds4g_expert_cache_forward(self.handle, _ptr(x), _ptr(logits), x.shape[0],
+                                              _ptr(y), _ptr(workspace), ws_bytes, _stream(stream))
+
+    def stats(self):
+        """(hits, misses, bytes uploaded) since creation."""
+        v = [ctypes.c_int64() for _ in range(3)]
+        check(_lib.ds4g_expert_cache_stats(self.handle, *[ctypes.byref(o) for o in v]))
+        return tuple(o.value for o in v)
+
+    def close(self) -> None:
+        if getattr(self, "handle", None) is not None and self.handle.value:
+            _lib.ds4g_expert_cache_destroy(self.handle)
+        self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # pragma: no cover - interpreter shutdown
+            pass

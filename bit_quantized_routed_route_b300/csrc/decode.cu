@@ -166,6 +166,8 @@ struct DecArgs {
     int H_blocks, I_blocks;
     const uint8_t *w_gate, *w_up, *w_down;
     int64_t gu_row, dn_row, gu_stride, dn_stride;
+    const int32_t *wslot;  // [E] weight slot of each expert, or null (slot = expert)
+    int n_wslots;
     int gu_pitch, dn_pitch;   // row pitch of the tiles in shared memory (padded against bank conflicts)
     const float *logits;   // [T][E]
     const uint16_t *x;     // [T][H] bf16
@@ -760,8 +762,9 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                 tg[0] = kTagGateUp;
                 tg[1] = it;
                 uint8_t *st = ring + (size_t)s * a.stage_bytes;
-                const uint8_t *g = a.w_gate + (size_t)e * a.gu_stride + (size_t)mt * gu_tile;
-                const uint8_t *u = a.w_up + (size_t)e * a.gu_stride + (size_t)mt * gu_tile;
+                const int we = weight_slot(a.wslot, a.n_wslots, e, a.status);
+                const uint8_t *g = a.w_gate + (size_t)we * a.gu_stride + (size_t)mt * gu_tile;
+                const uint8_t *u = a.w_up + (size_t)we * a.gu_stride + (size_t)mt * gu_tile;
                 ptx::mbar_arrive_expect_tx(&full[s], 2 * gu_tile);
                 if (a.gu_pitch == a.gu_row) {
                     ptx::bulk_g2s(st, g, gu_tile, &full[s]);
@@ -823,7 +826,7 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                         bytes += dn_tile + (tg[5 + 2 * i] >= 0 ? (uint32_t)rs.cnt[rs.act[j0 + i]] * (h_row + hs_row) : 0u);
                     ptx::mbar_arrive_expect_tx(&full[s], bytes);
                     for (int i = 0; i < cnt; ++i) {
-                        const int e = rs.act[j0 + i];
+                        const int e = weight_slot(a.wslot, a.n_wslots, rs.act[j0 + i], a.status);
                         const uint8_t *src = a.w_down + (size_t)e * a.dn_stride + (size_t)it * dn_tile;
                         if (a.dn_pitch == a.dn_row)
                             ptx::bulk_g2s(st + tg[4 + 2 * i], src, dn_tile, &full[s]);
@@ -1135,6 +1138,8 @@ struct Args {
     int H_blocks, I_blocks;
     int P_gu, P_dn;                 // row phases of the weight windows
     int64_t gu_row, dn_row;
+    const int32_t *wslot;   // [E] weight slot of each expert, or null
+    int n_wslots;
     int ks;                         // K split of gate/up tiles (1 or 2)
     const float *logits;
     const uint16_t *x;
@@ -1404,6 +1409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int64_t row = phase == 0 ? a.gu_row : a.dn_row;
                     const int nkb = phase == 0 ? kb_gu : kb_dn;
                     const int nmat = phase == 0 ? 2 : 1;
+                    const int we = weight_slot(a.wslot, a.n_wslots, c.e, a.status);
                     const uint32_t bytes = (uint32_t)(nmat * kAq + c.nt * (512 + 64));
                     for (int j = 0; ok && j < nkb; ++j, ++sc) {
                         const int kb = kh * nkb + j;
@@ -1417,10 +1423,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const int xw = (int)(((p * row + kQ2KBytes * kb) & ~15ll) / 4);
                             uint8_t *dst = st + p * (kBM / P) * kWinBytes;
                             if (phase == 0) {
-                                ptx::tma_load_3d(dst, &tm_gate, xw, mt * (kBM / P), c.e, &full[s]);
-                                ptx::tma_load_3d(dst + kAq, &tm_up, xw, mt * (kBM / P), c.e, &full[s]);
+                                ptx::tma_load_3d(dst, &tm_gate, xw, mt * (kBM / P), we, &full[s]);
+                                ptx::tma_load_3d(dst + kAq, &tm_up, xw, mt * (kBM / P), we, &full[s]);
                             } else {
-                                ptx::tma_load_3d(dst, &tm_down, xw, mt * (kBM / P), c.e, &full[s]);
+                                ptx::tma_load_3d(dst, &tm_down, xw, mt * (kBM / P), we, &full[s]);
                             }
                         }
                         for (int t = 0; t < c.nt; ++t) {
@@ -1847,12 +1853,14 @@ cudaError_t launch_decode_tc(const LayerArgs &la, const DecodeBufs &db, const De
     a.sync = db.sync;
     a.wait_ns = wait_ns;
     a.stall = stall ? 1 : 0;
+    a.wslot = la.wslot;
+    a.n_wslots = la.n_wslots;
 
     CUtensorMap m_gate, m_up, m_down;
     cudaError_t e;
-    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, la.E, a.P_gu)) != cudaSuccess ||
-        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, la.E, a.P_gu)) != cudaSuccess ||
-        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, la.E, a.P_dn)) != cudaSuccess)
+    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, la.n_wslots, a.P_gu)) != cudaSuccess ||
+        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, la.n_wslots, a.P_gu)) != cudaSuccess ||
+        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, la.n_wslots, a.P_dn)) != cudaSuccess)
         return e;
 
     // counters and status reset, activations to fp16 (the kernel copies them
@@ -1927,6 +1935,8 @@ cudaError_t launch_decode_path(const LayerArgs &la, const DecodeBufs &db, const 
     a.dn_row = la.dn_row;
     a.gu_stride = la.gu_stride;
     a.dn_stride = la.dn_stride;
+    a.wslot = la.wslot;
+    a.n_wslots = la.n_wslots;
     a.gu_pitch = (int)smem_pitch(la.gu_row);
     a.dn_pitch = (int)smem_pitch(la.dn_row);
     a.logits = db.logits;

@@ -1,7 +1,8 @@
 // ds4g_api.cu -- the C ABI of libds4g: argument validation, the workspace
 // plan and the launch sequence of one routed-MoE layer call.  Every entry
 // point validates on the host before launching anything and returns a
-// ds4g_status; no entry point allocates device memory.
+// ds4g_status; no entry point allocates device memory except the expert
+// cache's create (cache.cu).
 #include <mutex>
 
 #include "ds4g_common.cuh"
@@ -30,6 +31,8 @@ DeviceInfo g_dev[64];
 bool g_dev_ok[64];
 
 }  // namespace
+
+ds4g_status status_from_cuda(cudaError_t e) { return from_cuda(e); }
 
 ds4g_status device_info(DeviceInfo *out)
 {
@@ -63,7 +66,8 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
         d->format != DS4G_FMT_Q5K)
         return DS4G_ERR_INVALID;
     if (block_bytes_of(d->down_format) == 0) return DS4G_ERR_INVALID;
-    if (d->reserved != 0) return DS4G_ERR_INVALID;
+    if (d->n_slots < 0 || (d->n_slots == 0) != (d->expert_slot == nullptr))
+        return DS4G_ERR_INVALID;
     if ((d->flags & ~(DS4G_FORCE_GEMV | DS4G_FORCE_TC | DS4G_DEBUG_STALL)) != 0)
         return DS4G_ERR_INVALID;
     if ((d->flags & DS4G_FORCE_GEMV) && (d->flags & DS4G_FORCE_TC)) return DS4G_ERR_INVALID;
@@ -104,6 +108,7 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     if (d->gate_up_expert_stride % 16 || d->down_expert_stride % 16) return DS4G_ERR_LAYOUT;
     if (!aligned(d->w_gate, 16) || !aligned(d->w_up, 16) || !aligned(d->w_down, 16))
         return DS4G_ERR_LAYOUT;
+    if (d->expert_slot && !aligned(d->expert_slot, 4)) return DS4G_ERR_LAYOUT;
     if ((d->flags & DS4G_FORCE_TC) &&
         (d->gate_up_row_bytes % 16 != 0 || d->down_row_bytes % 16 != 0))
         return DS4G_ERR_LAYOUT;
@@ -221,6 +226,9 @@ ds4g_status forward_impl(const ds4g_moe_desc *d, const Plan &p, const uint16_t *
     a.dn_row = d->down_row_bytes;
     a.gu_stride = d->gate_up_expert_stride;
     a.dn_stride = d->down_expert_stride;
+    a.wslot = d->n_slots > 0 ? d->expert_slot : nullptr;
+    a.n_wslots = d->n_slots > 0 ? d->n_slots : p.E;
+    a.status = status;
     a.codebook = d->codebook;
     a.x = x;
     a.wts = wts;

@@ -20,6 +20,20 @@ constexpr int kQ4KBytes = 144;   // Q4_K super-block
 constexpr int kQ5KBytes = 176;   // Q5_K super-block
 constexpr int kQ6KBytes = 210;   // Q6_K super-block
 
+// The weight slot of expert e: e itself, or wslot[e] when the weight
+// tensors hold a set of resident slots (an expert cache).  An entry outside
+// 0 .. n_slots-1 is recorded as DS4G_ERR_INVALID in the status word and
+// replaced by slot 0, so no weight access leaves the tensors.
+__device__ __forceinline__ int weight_slot(const int32_t *wslot, int n_slots, int e,
+                                           int32_t *status)
+{
+    if (!wslot) return e;
+    const int s = __ldg(wslot + e);
+    if (s >= 0 && s < n_slots) return s;
+    if (status) atomicCAS(status, 0, (int32_t)DS4G_ERR_INVALID);
+    return 0;
+}
+
 // Super-block bytes of a ds4g_format (0 for an unknown one).
 __host__ __device__ constexpr int block_bytes_of(int fmt)
 {
@@ -74,6 +88,9 @@ struct DeviceInfo {
     int max_smem_optin;
 };
 ds4g_status device_info(DeviceInfo *out);
+// DS4G_OK for cudaSuccess, else DS4G_ERR_CUDA (remembering the CUDA error for
+// ds4g_last_cuda_error).
+ds4g_status status_from_cuda(cudaError_t e);
 
 // ---------------------------------------------------------------------------
 // Kernel launchers (all asynchronous on `s`; return cudaGetLastError()).
@@ -100,6 +117,9 @@ struct LayerArgs {
     int gu_format, dn_format;  // block formats of W_gate / W_up and of W_down
     const uint8_t *w_gate, *w_up, *w_down;
     int64_t gu_row, dn_row, gu_stride, dn_stride;
+    const int32_t *wslot;      // [E] weight slot of each expert, or null (slot = expert)
+    int n_wslots;              // slots the weight tensors hold (E when wslot is null)
+    int32_t *status;           // device status word
     const int8_t *codebook;
     const uint16_t *x;         // [T x H] bf16
     const float *wts;          // [A] routing weights (assignment order)

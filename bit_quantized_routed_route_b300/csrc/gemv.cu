@@ -109,8 +109,9 @@ __global__ void __launch_bounds__(kWarps * 32) gateup_kernel(LayerArgs a)
             for (int i = lane; i < seg_n; i += 32) a.hbuf[(size_t)(seg0 + i) * a.I_pad + n] = 0.0f;
             continue;
         }
-        const uint8_t *rg = a.w_gate + (size_t)e * a.gu_stride + (size_t)n * a.gu_row;
-        const uint8_t *ru = a.w_up + (size_t)e * a.gu_stride + (size_t)n * a.gu_row;
+        const int we = weight_slot(a.wslot, a.n_wslots, e, a.status);
+        const uint8_t *rg = a.w_gate + (size_t)we * a.gu_stride + (size_t)n * a.gu_row;
+        const uint8_t *ru = a.w_up + (size_t)we * a.gu_stride + (size_t)n * a.gu_row;
         for (int c0 = 0; c0 < seg_n; c0 += kTokChunk) {
             const int nt = min(kTokChunk, seg_n - c0);
             const uint16_t *xr[kTokChunk];
@@ -170,7 +171,8 @@ __global__ void __launch_bounds__(kWarps * 32) down_kernel(LayerArgs a)
         const int e = a.active[item / tiles];
         const int m = (item % tiles) * kWarps + warp;
         const int seg0 = a.offsets[e], seg_n = a.offsets[e + 1] - seg0;
-        const uint8_t *rd = a.w_down + (size_t)e * a.dn_stride + (size_t)m * a.dn_row;
+        const int we = weight_slot(a.wslot, a.n_wslots, e, a.status);
+        const uint8_t *rd = a.w_down + (size_t)we * a.dn_stride + (size_t)m * a.dn_row;
         for (int c0 = 0; c0 < seg_n; c0 += kTokChunk) {
             const int nt = min(kTokChunk, seg_n - c0);
             float acc[kTokChunk];

@@ -132,6 +132,8 @@ struct TcArgs {
     int h_perm32;               // h in the perm32 order of a Q2_K W_down (else natural)
     float *yslot;               // down output [A][H]
     const int8_t *codebook;     // [256 x 8] int8 (codebook format)
+    const int32_t *wslot;       // [E] weight slot of each expert, or null
+    int n_wslots;
     int32_t *status;
     uint64_t wait_ns;
     int stall;                  // debug: the producers issue nothing (tests the bounded waits)
@@ -552,7 +554,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
             auto prefetch_next = [&]() {
                 if (pf_it >= n_items) return;
                 const int tile = pf_it / a.m_tiles, mt = pf_it % a.m_tiles;
-                const int e = a.tiles[4 * tile];
+                const int e = weight_slot(a.wslot, a.n_wslots, a.tiles[4 * tile], a.status);
                 const int x = ((kBlockBytes * pf_kb) & ~15) / 4;
                 ptx::tma_prefetch_3d(&tm_a0, x, mt * kBM, e);
                 if (NMAT == 2) ptx::tma_prefetch_3d(&tm_a1, x, mt * kBM, e);
@@ -566,7 +568,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
             bool ok = true;
             for (int it = blockIdx.x; ok && it < n_items; it += gridDim.x) {
                 const int tile = it / a.m_tiles, mt = it % a.m_tiles;
-                const int e = a.tiles[4 * tile];
+                const int e = weight_slot(a.wslot, a.n_wslots, a.tiles[4 * tile], a.status);
                 for (int kb = 0; kb < KB; ++kb, ++wc) {
                     const int s = wc % R::kW;
                     if (wc >= R::kW &&
@@ -978,9 +980,10 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
 {
     CUtensorMap m_gate, m_up, m_down, m_x, m_h;
     cudaError_t e;
-    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, la.E, 1)) != cudaSuccess ||
-        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, la.E, 1)) != cudaSuccess ||
-        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, la.E, 1)) != cudaSuccess ||
+    const int nw = la.n_wslots;             // experts (or slots) the weight tensors hold
+    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, nw, 1)) != cudaSuccess ||
+        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, nw, 1)) != cudaSuccess ||
+        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, nw, 1)) != cudaSuccess ||
         (e = act_map(&m_x, tb.xseg, la.H, la.A)) != cudaSuccess ||
         (e = act_map(&m_h, tb.hp, la.I_pad, la.A)) != cudaSuccess)
         return e;
@@ -995,6 +998,8 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     a.hp = tb.hp;
     a.yslot = la.yslot;
     a.status = tb.status;
+    a.wslot = la.wslot;
+    a.n_wslots = la.n_wslots;
     a.wait_ns = wait_ns;
     a.stall = stall ? 1 : 0;
 

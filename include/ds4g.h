@@ -60,7 +60,7 @@
 extern "C" {
 #endif
 
-#define DS4G_ABI_VERSION 2
+#define DS4G_ABI_VERSION 3
 
 /* Symbols of the shared library (built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -151,7 +151,16 @@ enum {
  * the general (GEMV) kernels; DS4G_FORCE_TC then returns
  * DS4G_ERR_UNSUPPORTED.  Row alignment: rows of Q2_K, Q4_K and Q5_K blocks
  * a multiple of 4 bytes, of codebook and Q6_K blocks a multiple of 2.
- * reserved: must be 0.
+ * n_slots / expert_slot: where each expert's weights are.  n_slots == 0
+ * (expert_slot NULL): expert e's matrices are slot e of the weight tensors.
+ * n_slots > 0: the weight tensors hold n_slots expert slots (same row bytes
+ * and expert strides) and expert_slot [n_experts] int32 (device, 4-byte
+ * aligned) gives the slot of each expert; only the experts a call routes to
+ * need a valid slot (0 .. n_slots-1).  A routed expert whose entry is out of
+ * range has its weights read from slot 0 instead and the workspace status
+ * word reads DS4G_ERR_INVALID (see ds4g_moe_device_status); y is then not
+ * valid.  This is how ds4g_expert_cache below runs layers whose experts
+ * live in host memory.
  */
 typedef struct ds4g_moe_desc {
     int32_t hidden;
@@ -163,7 +172,7 @@ typedef struct ds4g_moe_desc {
     int32_t flags;
     int32_t tc_min_tokens;
     int32_t down_format;       /* ds4g_format of W_down                          */
-    int32_t reserved;          /* 0                                              */
+    int32_t n_slots;           /* 0, or the expert slots the weight tensors hold */
     const void *w_gate;
     const void *w_up;
     const void *w_down;
@@ -172,6 +181,7 @@ typedef struct ds4g_moe_desc {
     int64_t gate_up_expert_stride;
     int64_t down_expert_stride;
     const int8_t *codebook;    /* [256 x 8] int8, device; when a matrix is CB2  */
+    const int32_t *expert_slot;/* [n_experts] int32, device; when n_slots > 0    */
 } ds4g_moe_desc;
 
 /*
@@ -383,6 +393,54 @@ DS4G_API ds4g_status ds4g_moe_forward_noalloc(const ds4g_moe_desc *desc, const u
 
 /* Static text for a status code ("ok", "invalid argument", ...). */
 DS4G_API const char *ds4g_status_string(ds4g_status status);
+
+/*
+ * ds4g_expert_cache -- a device-resident cache of routed experts whose
+ * weights live in host memory.  Passage: routed MoE experts streamed from an
+ * in-memory cache on cache misses, with configurable expert-cache budgets
+ * (opensourcealternatives.to, FAQ; DwarfStar 4 on aiany.app, "What Sets It
+ * Apart"; SSD streaming of the routed experts in the ds4 README mirror).
+ * Here the backing store is host memory and a miss is an asynchronous
+ * host-to-device copy of the expert's three matrices.
+ *
+ * ds4g_expert_cache_create: `host_desc` describes the layer with w_gate,
+ * w_up and w_down in host memory (page-locked, e.g. cudaHostAlloc, so that
+ * the copies are asynchronous; 16-byte aligned) and n_slots = 0; codebook,
+ * when used, is a device pointer as usual.  The cache allocates, on the
+ * current device, n_slots expert slots (n_slots * (2 * gate_up_expert_stride
+ * + down_expert_stride) bytes) and the expert-to-slot map; this entry point
+ * and ds4g_expert_cache_destroy are the library's only device allocations.
+ * Errors: DS4G_ERR_INVALID (descriptor, null out, n_slots < top_k or
+ * n_slots > n_experts, host_desc->n_slots != 0); the descriptor errors of
+ * ds4g_moe_forward; DS4G_ERR_CUDA (allocation).
+ * ds4g_expert_cache_workspace_bytes: device workspace of a forward of T
+ * tokens (0 when T is invalid).
+ * ds4g_expert_cache_forward: one layer call, arguments as ds4g_moe_forward
+ * (device x, logits, y and workspace).  It routes on the device, reads back
+ * which experts the call uses (synchronizing `stream`), uploads the missing
+ * ones into the least recently used slots that this call does not use
+ * (three cudaMemcpyAsync per expert on `stream`), uploads the map, then runs
+ * the layer on the slots: y is bit-identical to ds4g_moe_forward on a
+ * device-resident copy of the weights.  The uploads precede the layer on
+ * `stream` (the fused layer needs every routed expert resident before it
+ * starts).  Calls on one cache must not overlap (one stream, or
+ * synchronized).  Errors: those of ds4g_moe_forward, plus
+ * DS4G_ERR_UNSUPPORTED when the call routes to more distinct experts than
+ * the cache has slots (nothing runs after the routing).
+ * ds4g_expert_cache_stats: expert hits, misses (uploads) and bytes uploaded
+ * since creation (any out pointer may be NULL).
+ * ds4g_expert_cache_destroy: frees the slots (synchronizes the device).
+ */
+typedef struct ds4g_expert_cache ds4g_expert_cache;
+DS4G_API ds4g_status ds4g_expert_cache_create(const ds4g_moe_desc *host_desc, int32_t n_slots,
+                                              ds4g_expert_cache **out);
+DS4G_API size_t ds4g_expert_cache_workspace_bytes(const ds4g_expert_cache *cache, int32_t T);
+DS4G_API ds4g_status ds4g_expert_cache_forward(ds4g_expert_cache *cache, const uint16_t *x,
+                                               const float *logits, int32_t T, float *y,
+                                               void *workspace, size_t ws_bytes, void *stream);
+DS4G_API ds4g_status ds4g_expert_cache_stats(const ds4g_expert_cache *cache, int64_t *hits,
+                                             int64_t *misses, int64_t *bytes_uploaded);
+DS4G_API void ds4g_expert_cache_destroy(ds4g_expert_cache *cache);
 
 /* DS4G_ABI_VERSION of the loaded library. */
 DS4G_API int32_t ds4g_abi_version(void);

@@ -30,7 +30,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_abi_version_and_status_strings():
-    assert D.abi_version() == 2
+    assert D.abi_version() == 3
     assert D.status_string(D.OK) == "ok"
     for s in range(1, 8):
         assert D.status_string(s) not in ("ok", "unknown status")
@@ -44,7 +44,7 @@ def desc(**kw):
     d = D.MoeDesc()
     d.hidden, d.inter, d.n_experts, d.top_k = 256, 128, 8, 2
     d.score, d.format, d.flags, d.tc_min_tokens = D.SCORE_SOFTMAX, D.FMT_Q2K, 0, 0
-    d.down_format, d.reserved = D.FMT_Q2K, 0
+    d.down_format, d.n_slots = D.FMT_Q2K, 0
     d.w_gate = d.w_up = d.w_down = FAKE
     d.gate_up_row_bytes, d.down_row_bytes = 84, 84
     d.gate_up_expert_stride, d.down_expert_stride = 128 * 84, 256 * 84
@@ -94,7 +94,10 @@ def test_noalloc_scratch_covers_a_32_token_decode_of_the_7168_layer():
     (dict(format=D.FMT_Q6K, gate_up_row_bytes=210, gate_up_expert_stride=128 * 224),
      D.ERR_INVALID),                                                       # Q6_K is down-only
     (dict(down_format=D.FMT_Q4K, down_row_bytes=146), D.ERR_LAYOUT),       # Q4_K rows % 4
-    (dict(reserved=1), D.ERR_INVALID),
+    (dict(n_slots=1), D.ERR_INVALID),                       # slots without a map
+    (dict(n_slots=-1), D.ERR_INVALID),
+    (dict(expert_slot=FAKE), D.ERR_INVALID),                # a map without slots
+    (dict(n_slots=4, expert_slot=FAKE + 2), D.ERR_LAYOUT),
     (dict(down_format=D.FMT_CB2, down_row_bytes=70), D.ERR_INVALID),      # no codebook
     (dict(flags=D.FORCE_GEMV | D.FORCE_TC), D.ERR_INVALID),
     (dict(flags=64), D.ERR_INVALID),
@@ -246,3 +249,22 @@ def test_path_choice_by_launch_count(shape, T, kw, launches):
     """The per-call path choice documented under ds4g_moe_forward ("Path"),
     read through ds4g_moe_forward_launches (pure host arithmetic)."""
     assert D.moe_forward_launches(layer_desc(*shape, **kw), T) == launches
+
+
+def test_expert_cache_create_validates_first():
+    """The cache's create checks its descriptor and slot count on the host
+    before it allocates anything."""
+    L = D.lib()
+    h = ctypes.c_void_p()
+    assert L.ds4g_expert_cache_create(None, 4, ctypes.byref(h)) == D.ERR_INVALID
+    assert L.ds4g_expert_cache_create(ctypes.byref(desc()), 4, None) == D.ERR_INVALID
+    assert L.ds4g_expert_cache_create(ctypes.byref(desc()), 1, ctypes.byref(h)) == D.ERR_INVALID  # < top_k
+    assert L.ds4g_expert_cache_create(ctypes.byref(desc()), 9, ctypes.byref(h)) == D.ERR_INVALID  # > E
+    assert L.ds4g_expert_cache_create(ctypes.byref(desc(n_slots=4, expert_slot=FAKE)), 4,
+                                      ctypes.byref(h)) == D.ERR_INVALID
+    assert L.ds4g_expert_cache_create(ctypes.byref(desc(hidden=300)), 4, ctypes.byref(h)) == D.ERR_SHAPE
+    assert h.value is None
+    assert L.ds4g_expert_cache_workspace_bytes(None, 4) == 0
+    assert L.ds4g_expert_cache_forward(None, FAKE, FAKE, 4, FAKE, FAKE, 1 << 20, None) == D.ERR_INVALID
+    assert L.ds4g_expert_cache_stats(None, None, None, None) == D.ERR_INVALID
+    L.ds4g_expert_cache_destroy(None)          # no-op
