@@ -826,8 +826,9 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                         bytes += dn_tile + (tg[5 + 2 * i] >= 0 ? (uint32_t)rs.cnt[rs.act[j0 + i]] * (h_row + hs_row) : 0u);
                     ptx::mbar_arrive_expect_tx(&full[s], bytes);
                     for (int i = 0; i < cnt; ++i) {
-                        const int e = weight_slot(a.wslot, a.n_wslots, rs.act[j0 + i], a.status);
-                        const uint8_t *src = a.w_down + (size_t)e * a.dn_stride + (size_t)it * dn_tile;
+                        const int e = rs.act[j0 + i];
+                        const int we = weight_slot(a.wslot, a.n_wslots, e, a.status);
+                        const uint8_t *src = a.w_down + (size_t)we * a.dn_stride + (size_t)it * dn_tile;
                         if (a.dn_pitch == a.dn_row)
                             ptx::bulk_g2s(st + tg[4 + 2 * i], src, dn_tile, &full[s]);
                         else

@@ -103,7 +103,7 @@ def test_cache_matches_device_forward(orc, kw, flags):
     L = to_device(layer, flags=flags)
     rng = np.random.default_rng(5)
     calls = [_budget_logits(rng, T, E, n_slots) for _ in range(8)]
-    routed = [set(orc.route(lg, k, layer["score"])[0].ravel().tolist()) for lg in calls]
+    routed = [set(orc.route(lg, k, layer["score"])["ids"].ravel().tolist()) for lg in calls]
     for i, (lg, expect) in enumerate(zip(calls, lru_model(routed, n_slots))):
         st, y = _cache_forward(c, layer["x"], lg)
         assert st == D.OK, D.status_string(st)
