@@ -79,6 +79,8 @@ def parse(argv=None):
                     help="time only --config (no per_config object)")
     ap.add_argument("--force", default="auto", choices=["auto", "decode", "tc"],
                     help="run the layer on one path (default: the library's choice)")
+    ap.add_argument("--no-cache-workload", action="store_true",
+                    help="skip the expert-cache workload in per_config")
     ap.add_argument("--tc-min-tokens", type=int, default=0,
                     help="per-segment split: segments below this many tokens take the GEMV "
                          "kernels (tensor-core path only; 0 = off)")
@@ -608,6 +610,53 @@ def cpu_baseline(cfg: S.Config, layer: dict):
                       f"in {dt:.1f} s"}
 
 
+CACHE_SLOTS = 128
+CACHE_POOL = 64
+
+
+def measure_cache(K: int, W: int, dev, base: "S.Config"):
+    """The expert-cache workload: the decode_32tok layer (Q2_K, 256 experts,
+    top-8, 32 tokens) with every expert in page-locked host memory and 128
+    device slots; successive batches routed by the Zipf-skewed recipe (81-106
+    distinct experts per batch), so each call uploads the experts it misses.
+    Wall-clock timed (each call reads its routing back to the host); reports
+    tokens/s, the hit rate and the host-to-device bytes per call."""
+    import bit_quantized_routed_route_b300 as D
+    layer = S.make_layer(base)
+    host = {n: torch.from_numpy(layer[n]).pin_memory() for n in ("w_gate", "w_up", "w_down")}
+    del layer
+    T, E, k, H = base.tokens, base.n_experts, base.top_k, base.hidden
+    cache = D.ExpertCache(H, base.inter, E, k, base.score, base.format, host["w_gate"],
+                          host["w_up"], host["w_down"], CACHE_SLOTS)
+    xs = [torch.from_numpy(S.make_x(100 + i, T, H).view(np.int16)).to(dev) for i in range(CACHE_POOL)]
+    lgs = [torch.from_numpy(S.make_logits(100 + i, S.LOGITS_ZIPF, T, E, k)).to(dev)
+           for i in range(CACHE_POOL)]
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    ws = torch.empty(cache.workspace_bytes(T), dtype=torch.uint8, device=dev)
+    for i in range(W):
+        D.check(cache.forward(xs[i % CACHE_POOL], lgs[i % CACHE_POOL], y, ws))
+    torch.cuda.synchronize()
+    h0, m0, b0 = cache.stats()
+    t0 = time.perf_counter()
+    for i in range(K):
+        j = (W + i) % CACHE_POOL
+        D.check(cache.forward(xs[j], lgs[j], y, ws))
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    h1, m1, b1 = cache.stats()
+    cache.close()
+    del host
+    hits, misses, up = h1 - h0, m1 - m0, b1 - b0
+    return {"value": K * T / dt, "unit": "tokens/s", "ms_per_step": 1000.0 * dt / K, "steps": K,
+            "workload": f"cache_32tok: {base.name} layer, experts in pinned host memory, "
+                        f"{CACHE_SLOTS} of {E} resident, Zipf-routed batches",
+            "timing": "wall clock (each call reads its routing back to the host)",
+            "hit_rate": hits / max(1, hits + misses),
+            "misses_per_step": misses / K,
+            "h2d_bytes_per_step": up / K,
+            "h2d_gbs": up / dt / 1e9}
+
+
 def main(argv=None):
     args = parse(argv)
     cfg = S.CONFIGS[args.config]
@@ -637,6 +686,8 @@ def main(argv=None):
                                          gpu_index=local)
             w.free()
             del w
+        if not args.no_cache_workload:
+            per_config["cache_32tok"] = measure_cache(200, W, dev, S.CONFIGS["decode_32tok"])
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
