@@ -79,6 +79,10 @@ def parse(argv=None):
                     help="time only --config (no per_config object)")
     ap.add_argument("--force", default="auto", choices=["auto", "decode", "tc"],
                     help="run the layer on one path (default: the library's choice)")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="profiling only: --config with this many experts (0 = as configured)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="profiling only: --config with this many tokens (0 = as configured)")
     ap.add_argument("--no-cache-workload", action="store_true",
                     help="skip the expert-cache workload in per_config")
     ap.add_argument("--tc-min-tokens", type=int, default=0,
@@ -660,6 +664,11 @@ def measure_cache(K: int, W: int, dev, base: "S.Config"):
 def main(argv=None):
     args = parse(argv)
     cfg = S.CONFIGS[args.config]
+    if args.experts or args.tokens:
+        # a smaller layer of the same kind, for ncu captures under the size rule
+        import dataclasses
+        cfg = dataclasses.replace(cfg, n_experts=args.experts or cfg.n_experts,
+                                  tokens=args.tokens or cfg.tokens)
     rank, world, local = dist_setup(args)
     if args.impl == "reference":
         return reference_arm(args, cfg, rank, world)
