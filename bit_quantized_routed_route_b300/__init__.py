@@ -35,7 +35,7 @@ EXPORTED = (
     "ds4g_moe_forward", "ds4g_moe_forward_host", "ds4g_moe_routing_view",
     "ds4g_moe_forward_phased", "ds4g_moe_forward_launches", "ds4g_moe_device_status",
     "ds4g_status_string", "ds4g_abi_version", "ds4g_last_cuda_error",
-    "ds4g_moe_forward_noalloc", "ds4g_expert_cache_create", "ds4g_expert_cache_workspace_bytes",
+    "ds4g_moe_forward_noalloc", "ds4g_moe_noalloc_status", "ds4g_expert_cache_create", "ds4g_expert_cache_workspace_bytes",
     "ds4g_expert_cache_forward", "ds4g_expert_cache_stats", "ds4g_expert_cache_destroy",
 )
 
@@ -79,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "ds4g_q4k_dequant": (i32, [vp, i64, vp, i32, vp]),
         "ds4g_q5k_dequant": (i32, [vp, i64, vp, i32, vp]),
         "ds4g_q6k_dequant": (i32, [vp, i64, vp, i32, vp]),
+        "ds4g_moe_noalloc_status": (i32, [ctypes.POINTER(MoeDesc), i32, ctypes.POINTER(i32), vp]),
         "ds4g_expert_cache_create": (i32, [ctypes.POINTER(MoeDesc), i32, ctypes.POINTER(vp)]),
         "ds4g_expert_cache_workspace_bytes": (ctypes.c_size_t, [vp, i32]),
         "ds4g_expert_cache_forward": (i32, [vp, vp, vp, i32, vp, vp, ctypes.c_size_t, vp]),
@@ -239,6 +240,13 @@ def moe_routing_view(desc: MoeDesc, T: int, workspace, ws_bytes=None):
                                     *[ctypes.byref(o) for o in out])
     names = ("ids", "weights", "counts", "offsets", "perm")
     return st, {n: (o.value or 0) for n, o in zip(names, out)}
+
+
+def moe_noalloc_status(desc: MoeDesc, T: int, stream=None):
+    """(status, device status word of the last ds4g_moe_forward_noalloc)."""
+    v = ctypes.c_int32(-1)
+    st = _lib.ds4g_moe_noalloc_status(ctypes.byref(desc), T, ctypes.byref(v), _stream(stream))
+    return st, v.value
 
 
 class Layer:

@@ -549,3 +549,22 @@ extern "C" ds4g_status ds4g_moe_forward_noalloc(const ds4g_moe_desc *desc, const
     return forward_impl(desc, p, x, logits, y, static_cast<uint8_t *>(scratch),
                         static_cast<cudaStream_t>(stream), PhaseEvents{{}, false});
 }
+
+extern "C" ds4g_status ds4g_moe_noalloc_status(const ds4g_moe_desc *desc, int32_t T,
+                                               int32_t *status_out, void *stream)
+{
+    using namespace ds4g;
+    if (!status_out) return DS4G_ERR_INVALID;
+    Plan p;
+    ds4g_status st = make_plan(desc, T, &p);
+    if (st != DS4G_OK) return st;
+    if (p.total > DS4G_NOALLOC_SCRATCH_BYTES) return DS4G_ERR_WORKSPACE;
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != DS4G_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(status_out, static_cast<uint8_t *>(scratch) + p.status,
+                                    sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return from_cuda(e);
+}

@@ -383,7 +383,10 @@ DS4G_API ds4g_status ds4g_moe_device_status(const ds4g_moe_desc *desc, int32_t T
  * kernel of each call), so nothing needs clearing between calls.  Calls that
  * overlap on the same GPU (other streams, other host threads) race on the
  * array: serialize them.  ds4g_moe_routing_view and ds4g_moe_device_status do
- * not apply to this entry point.
+ * not apply to this entry point; ds4g_moe_noalloc_status reads its status
+ * word.  The array's address is looked up once per device and kept for the
+ * life of the process: after a cudaDeviceReset it is stale, so a process
+ * that resets a device must not call this entry point on it again.
  * Errors: as ds4g_moe_forward.
  */
 #define DS4G_NOALLOC_SCRATCH_BYTES (32u << 20)
@@ -441,6 +444,19 @@ DS4G_API ds4g_status ds4g_expert_cache_forward(ds4g_expert_cache *cache, const u
 DS4G_API ds4g_status ds4g_expert_cache_stats(const ds4g_expert_cache *cache, int64_t *hits,
                                              int64_t *misses, int64_t *bytes_uploaded);
 DS4G_API void ds4g_expert_cache_destroy(ds4g_expert_cache *cache);
+
+/*
+ * ds4g_moe_noalloc_status -- no counterpart on the pages (failure detection of
+ * this library).  The device status word of the last
+ * ds4g_moe_forward_noalloc of this layer and T on the current device:
+ * DS4G_OK, DS4G_ERR_TIMEOUT (a bounded wait expired) or DS4G_ERR_INVALID (a
+ * routed expert's slot was out of range).  Synchronizes `stream`.  Errors:
+ * DS4G_ERR_INVALID, the descriptor errors of ds4g_moe_forward,
+ * DS4G_ERR_WORKSPACE (the layer does not fit the static scratch),
+ * DS4G_ERR_CUDA.
+ */
+DS4G_API ds4g_status ds4g_moe_noalloc_status(const ds4g_moe_desc *desc, int32_t T,
+                                             int32_t *status_out, void *stream);
 
 /* DS4G_ABI_VERSION of the loaded library. */
 DS4G_API int32_t ds4g_abi_version(void);

@@ -66,3 +66,24 @@ def test_noalloc_rejects_plans_beyond_the_static_scratch():
     lg = torch.zeros((T, E), dtype=torch.float32, device="cuda")
     y = torch.zeros((T, H), dtype=torch.float32, device="cuda")
     assert D.moe_forward_noalloc(L.desc, x, lg, T, y) == D.ERR_WORKSPACE
+
+
+def test_noalloc_status_reports_a_timeout_then_ok():
+    """ds4g_moe_noalloc_status reads the static scratch's status word: a
+    call whose producers issue nothing (DS4G_DEBUG_STALL, 2 ms waits) reads
+    DS4G_ERR_TIMEOUT; the next normal call reads DS4G_OK and is exact."""
+    layer, _ = _small("small")
+    L = to_device(layer)
+    y_ws, _ = run_forward(L, layer["x"], layer["logits"])
+    x, lg = _dev_inputs(layer)
+    T, H = layer["x"].shape
+    stalled = L.with_flags(D.DEBUG_STALL)
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    D.check(D.moe_forward_noalloc(stalled.desc, x, lg, T, y))
+    st, v = D.moe_noalloc_status(stalled.desc, T)
+    assert st == D.OK and v == D.ERR_TIMEOUT
+    D.check(D.moe_forward_noalloc(L.desc, x, lg, T, y))
+    st, v = D.moe_noalloc_status(L.desc, T)
+    assert st == D.OK and v == D.OK
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy().view(np.uint32), y_ws.view(np.uint32))
