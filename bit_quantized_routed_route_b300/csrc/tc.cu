@@ -307,15 +307,72 @@ struct TcCta {
     int n_items, KB;
 };
 
-// The dequantizing role of one warp (both kernels).  Team hh (warpgroups
-// 2hh, 2hh+1) fills half hh of every block: per K step the W_gate and W_up
-// halves into A buffers 2hh and 2hh+1 (gate/up kernel), or the W_down half
-// into A buffer 2hh + (K step & 1) (down kernel).  The two teams run
-// independently, so one team's hand-off latencies overlap the other's
-// arithmetic.  The block's offset inside its 16-byte aligned window
-// (repeating every 4 K steps for Q2_K) is dispatched once per fill to a
-// body where it is a compile-time constant, so all warps share the same few
-// bodies.
+// One thread's quarter of a block from its row window `win` of K step kb:
+// half hh, field pair k.gh (Q2_K; the block's offset inside the 16-byte
+// aligned window repeats every 4 K steps and is dispatched once per fill to
+// a body where it is a compile-time constant, so all warps share the same
+// few bodies) or weights 64*gh .. +63 of the half (codebook, `cb_lane` =
+// this lane's copy of the replicated codebook).
+template <int SH>
+__device__ __forceinline__ void q2k_window_quarter(const uint8_t *win, int hh, const QuarterConst &k,
+                                                   uint32_t (&out)[32])
+{
+    // 16-byte units 1 + 2hh .. 3 + 2hh hold the half's qs words (from word SH)
+    uint32_t qw[12];
+    const uint4 *u = reinterpret_cast<const uint4 *>(win) + 1 + 2 * hh;
+#pragma unroll
+    for (int v = 0; v < 3; ++v) {
+        const uint4 q = u[v];
+        qw[4 * v] = q.x;
+        qw[4 * v + 1] = q.y;
+        qw[4 * v + 2] = q.z;
+        qw[4 * v + 3] = q.w;
+    }
+    const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win);
+    const uint32_t sw = w32[SH + 2 * hh + k.gh];
+    const uint32_t dd = w32[SH + 20];
+    q2k_quarter<SH>(qw, sw, dd, k, out);
+}
+
+__device__ __forceinline__ void cb2_window_quarter(const uint8_t *win, int boff, int hh, int gh,
+                                                   uint32_t cb_lane, uint32_t (&out)[32])
+{
+    const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win) + (boff >> 2);
+    const int o = 4 * hh + 2 * gh;
+    uint32_t iw[3], gw[3], tw[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        iw[j] = w32[o + j];
+        gw[j] = w32[8 + o + j];
+        tw[j] = w32[16 + j];
+    }
+    cb2_quarter(iw, gw, tw, (uint32_t)(boff & 3) * 8, hh, gh, cb_lane, out);
+}
+
+template <int FMT>
+__device__ __forceinline__ void quarter_values(const uint8_t *win, int kb, int hh,
+                                               const QuarterConst &k, uint32_t cb_lane,
+                                               uint32_t (&out)[32])
+{
+    if (FMT == DS4G_FMT_Q2K) {
+        switch (kb & 3) {           // (84 * kb) mod 16, in words
+        case 0: q2k_window_quarter<0>(win, hh, k, out); break;
+        case 1: q2k_window_quarter<1>(win, hh, k, out); break;
+        case 2: q2k_window_quarter<2>(win, hh, k, out); break;
+        default: q2k_window_quarter<3>(win, hh, k, out); break;
+        }
+    } else {
+        cb2_window_quarter(win, (kCB2Bytes * kb) & 15, hh, k.gh, cb_lane, out);
+    }
+}
+
+// The dequantizing role of one warp (both kernels of tc_kernel).  Gate/up:
+// team hh (warpgroups 2hh, 2hh+1) fills half hh of every block, the W_gate
+// and W_up halves into A buffers 2hh and 2hh+1.  Down (Q2_K): team t owns the
+// K steps of parity t and fills both halves of each into its buffers 2t, 2t+1,
+// so while the issuer runs one team's K step the other team already
+// dequantizes its next one.  The two teams run independently, so one team's
+// hand-off latencies overlap the other's arithmetic.
 template <int MODE, int FMT>
 struct DequantRole {
     using R = Ring<MODE, FMT>;
@@ -339,45 +396,13 @@ struct DequantRole {
         lane_base = (uint32_t)(32 * quarter) << 16;
     }
 
-    template <int SH>
-    __device__ __forceinline__ void q2k_fill(const uint8_t *win, uint32_t (&out)[32])
+    // One fill: half hh of matrix `mat`, K step kb, window stage ws.  Gate/up
+    // kernel: hh is this team's half, the buffer 2hh + mat.  Down kernel: the
+    // team owns the K steps of its parity and fills both halves into its
+    // buffers 2*team + hh.
+    __device__ __forceinline__ void fill(int ws, int mat, int kb, int hh)
     {
-        // 16-byte units 1 + 2hh .. 3 + 2hh hold the half's qs words (from word SH)
-        uint32_t qw[12];
-        const uint4 *u = reinterpret_cast<const uint4 *>(win) + 1 + 2 * k.hh;
-#pragma unroll
-        for (int v = 0; v < 3; ++v) {
-            const uint4 q = u[v];
-            qw[4 * v] = q.x;
-            qw[4 * v + 1] = q.y;
-            qw[4 * v + 2] = q.z;
-            qw[4 * v + 3] = q.w;
-        }
-        const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win);
-        const uint32_t sw = w32[SH + 2 * k.hh + k.gh];
-        const uint32_t dd = w32[SH + 20];
-        q2k_quarter<SH>(qw, sw, dd, k, out);
-    }
-
-    __device__ __forceinline__ void cb2_fill(const uint8_t *win, int boff, uint32_t (&out)[32])
-    {
-        const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win) + (boff >> 2);
-        const int o = 4 * k.hh + 2 * k.gh;
-        uint32_t iw[3], gw[3], tw[3];
-#pragma unroll
-        for (int j = 0; j < 3; ++j) {
-            iw[j] = w32[o + j];
-            gw[j] = w32[8 + o + j];
-            tw[j] = w32[16 + j];
-        }
-        cb2_quarter(iw, gw, tw, (uint32_t)(boff & 3) * 8, k.hh, k.gh,
-                    c.cbrep + (uint32_t)(lane & 15) * 8, out);
-    }
-
-    // One fill: this team's half of matrix `mat`, K step kb, window stage ws.
-    __device__ __forceinline__ void fill(int ws, int mat, int kb)
-    {
-        const int buf = 2 * k.hh + (MODE == 0 ? mat : (kc & 1));
+        const int buf = 2 * k.hh + (MODE == 0 ? mat : hh);
         const int uses = MODE == 0 ? kc : (kc >> 1);      // earlier fills of the buffer
         if (uses > 0) {
             ok = wait_bar(&c.aempty[buf], (uses - 1) & 1, a.wait_ns, c.abort_flag);
@@ -388,16 +413,7 @@ struct DequantRole {
         const uint8_t *win = c.wring + (size_t)ws * R::kWStageBytes + mat * kAqBytes +
                              row * (kWinWords * 4);
         uint32_t out[32];
-        if (FMT == DS4G_FMT_Q2K) {
-            switch (kb & 3) {           // (84 * kb) mod 16, in words
-            case 0: q2k_fill<0>(win, out); break;
-            case 1: q2k_fill<1>(win, out); break;
-            case 2: q2k_fill<2>(win, out); break;
-            default: q2k_fill<3>(win, out); break;
-            }
-        } else {
-            cb2_fill(win, (kCB2Bytes * kb) & 15, out);
-        }
+        quarter_values<FMT>(win, kb, hh, k, c.cbrep + (uint32_t)(lane & 15) * 8, out);
         ptx::tmem_st32(c.tmem + lane_base + (uint32_t)buf * 64u + 32u * k.gh, out);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -412,11 +428,15 @@ struct DequantRole {
             const int tile = it / a.m_tiles, mt = it % a.m_tiles;
             const int row0 = a.tiles[4 * tile + 1], nlen = a.tiles[4 * tile + 2];
             for (int kb = 0; ok && kb < c.KB; ++kb, ++kc) {
+                if (MODE == 1 && (kc & 1) != k.hh) continue;     // the other team's K step
                 const int ws = kc % R::kW;
                 ok = wait_bar(&c.wfull[ws], (kc / R::kW) & 1, a.wait_ns, c.abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                for (int mat = 0; ok && mat < NMAT; ++mat) fill(ws, mat, kb);
+                if (MODE == 0)
+                    for (int mat = 0; ok && mat < NMAT; ++mat) fill(ws, mat, kb, k.hh);
+                else
+                    for (int hh = 0; ok && hh < 2; ++hh) fill(ws, 0, kb, hh);
                 if (!ok) break;
                 // this warp has read the stage's windows
                 __syncwarp();
@@ -500,7 +520,8 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < R::kW; ++s) {
             ptx::mbar_init(&wfull[s], 1);
-            ptx::mbar_init(&wempty[s], kDequantWarps);
+            // gate/up: every dequantizing warp reads every stage; down: one team
+            ptx::mbar_init(&wempty[s], MODE == 0 ? kDequantWarps : kTeamWarps);
         }
         for (int s = 0; s < R::kB; ++s) {
             ptx::mbar_init(&bfull[s], 1);
@@ -658,7 +679,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                     // the fill's A buffer (half hh of K step kc) and how often
                     // it was filled before
                     const int kc = hc >> 1, hh = hc & 1;
-                    const int buf = 2 * hh + (MODE == 0 ? X : (kc & 1));
+                    const int buf = MODE == 0 ? 2 * hh + X : 2 * (kc & 1) + hh;
                     const int uses = MODE == 0 ? kc : (kc >> 1);
                     ok = wait_bar(&bfull[s], (hc / R::kB) & 1, a.wait_ns, abort_flag);
                     ok = ok && wait_bar(&afull[buf], uses & 1, a.wait_ns, abort_flag);
@@ -742,6 +763,317 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
     if (threadIdx.x == 0 && *abort_flag) {
         drain_ring(wfull, R::kW, s_wissued, a.wait_ns);
         drain_ring(bfull, R::kB, s_bissued, a.wait_ns);
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    if (warp == 1) ptx::tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// The down kernel of codebook W_down: one item per dequantizing team.  yslot = w * (W_down . h)
+// needs one accumulator per item, so each team takes every other item of the
+// CTA with its own producer, window and activation rings, MMA issuer, two A
+// buffers (half 0 and half 1 of each K step) and accumulator; the teams never
+// wait for each other, and the four epilogue warps drain both accumulators
+// in the CTA's item order.  Two teams' rings leave each team two activation
+// half stages: enough behind the codebook dequant, too few behind the faster
+// Q2_K one, whose down kernel keeps the shared issuer of tc_kernel<1, Q2_K>
+// (measured 1.06 against 1.15 ms for codebook_512's down phase, 1.25 against
+// 1.17 ms for prefill_2048's).
+//   warps 0, 1    producer of team 0, 1: per K step of the team's item the
+//                 window stage, then the two activation half stages (h tile)
+//   warps 2, 3    MMA issuer of team 0, 1 (elected lane, converged warp)
+//   warps 4-19    dequantizers: team t = warps 4 + 8t .. 11 + 8t, thread =
+//                 weight row, quarter (half, field pair gh) of each fill
+//   warps 20-23   epilogue: routing weight, token exponent, fp32 y_slot
+// Tensor memory: A buffers 2t, 2t+1 of team t (64 columns each), accumulator
+// of team t at column 256 + 128t.
+// ---------------------------------------------------------------------------
+template <int FMT>
+struct DownRing {
+    static constexpr int kW = FMT == DS4G_FMT_Q2K ? 3 : 2;     // window stages per team
+    static constexpr int kB = 2;                               // activation half stages per team
+    static constexpr size_t kTeamBytes = (size_t)kW * kAqBytes + (size_t)kB * kHalfBytes;
+    // per team: [B half stages][window stages]; the codebook copy last
+    static constexpr size_t kBOff(int t) { return (size_t)t * kTeamBytes; }
+    static constexpr size_t kWOff(int t) { return (size_t)t * kTeamBytes + (size_t)kB * kHalfBytes; }
+    static constexpr size_t kCbOff = 2 * kTeamBytes;
+    static constexpr size_t kBytes = kCbOff + (FMT == DS4G_FMT_CB2 ? kCbRepBytes : 0);
+    static_assert(kTeamBytes % 1024 == 0, "team rings keep the 1024-byte swizzle alignment");
+    static_assert(kBytes + 1024 <= 225 * 1024, "shared-memory rings exceed the per-CTA limit");
+};
+
+constexpr int kDownThreads = (kFirstDequantWarp + kDequantWarps + kEpilogueWarps) * 32;
+
+template <int FMT>
+__global__ void __launch_bounds__(kDownThreads, 1)
+    tc_down_kernel(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_h,
+                   const TcArgs a)
+{
+    using R = DownRing<FMT>;
+    constexpr int kBlockBytes = FMT == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *cbrep = smem + R::kCbOff;
+    __shared__ __align__(8) uint64_t wfull[2][R::kW], wempty[2][R::kW], bfull[2][R::kB],
+        bempty[2][R::kB];
+    __shared__ __align__(8) uint64_t afull[kABufs], aempty[kABufs], accfull[2], accempty[2],
+        drain[2];
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort, s_wissued[2], s_bissued[2];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            for (int s = 0; s < R::kW; ++s) {
+                ptx::mbar_init(&wfull[t][s], 1);
+                ptx::mbar_init(&wempty[t][s], kTeamWarps);
+            }
+            for (int s = 0; s < R::kB; ++s) {
+                ptx::mbar_init(&bfull[t][s], 1);
+                ptx::mbar_init(&bempty[t][s], 1);
+            }
+            ptx::mbar_init(&accfull[t], 1);
+            ptx::mbar_init(&accempty[t], kEpilogueWarps);
+            ptx::mbar_init(&drain[t], 1);
+            s_wissued[t] = 0;
+            s_bissued[t] = 0;
+        }
+        for (int b = 0; b < kABufs; ++b) {
+            ptx::mbar_init(&afull[b], kTeamWarps);
+            ptx::mbar_init(&aempty[b], 1);
+        }
+        ptx::fence_mbar_init();
+        s_abort = 0;
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(&s_tmem, kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    if (FMT == DS4G_FMT_CB2) {
+        for (int i = threadIdx.x; i < 256 * kCbCopies; i += blockDim.x) {
+            const int r = i / kCbCopies, cpy = i % kCbCopies;
+            uint8_t *dst = cbrep + r * (kCbCopies * 8) + cpy * 8;
+#pragma unroll
+            for (int b = 0; b < 8; ++b) dst[b] = (uint8_t)a.codebook[8 * r + b];
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    volatile int *abort_flag = &s_abort;
+
+    const int n_items = *a.n_tiles * a.m_tiles;
+    const int KB = a.K / kQK;
+    // the CTA's items: it_j = blockIdx.x + j * gridDim.x; team t takes j = t, t + 2, ...
+    const int my_items = n_items > (int)blockIdx.x ? (n_items - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+    auto team_items = [&](int t) { return my_items > t ? (my_items - 1 - t) / 2 + 1 : 0; };
+    auto item_of = [&](int t, int q) { return (int)blockIdx.x + (2 * q + t) * (int)gridDim.x; };
+
+    if (warp < 2) {
+        // ---------------- producer of team t ----------------
+        const int t = warp;
+        if (lane == 0 && !a.stall) {
+            ptx::prefetch_tmap(&tm_w);
+            ptx::prefetch_tmap(&tm_h);
+            const int nk = team_items(t) * KB;           // K steps of the team
+            uint8_t *bring = smem + R::kBOff(t);
+            uint8_t *wring = smem + R::kWOff(t);
+            int wc = 0, bc = 0;
+            bool ok = true;
+            // the windows of K step w (weight producer part), L2 prefetch ahead
+            auto issue_w = [&](int w) -> bool {
+                const int s = w % R::kW;
+                if (w >= R::kW &&
+                    !wait_bar(&wempty[t][s], ((w / R::kW) - 1) & 1, a.wait_ns, abort_flag))
+                    return false;
+                const int it = item_of(t, w / KB), kb = w % KB;
+                const int tile = it / a.m_tiles, mt = it % a.m_tiles;
+                const int e = weight_slot(a.wslot, a.n_wslots, a.tiles[4 * tile], a.status);
+                ptx::mbar_arrive_expect_tx(&wfull[t][s], (uint32_t)kAqBytes);
+                ptx::tma_load_3d(wring + (size_t)s * kAqBytes, &tm_w, ((kBlockBytes * kb) & ~15) / 4,
+                                 mt * kBM, e, &wfull[t][s]);
+                const int pw = w + kPrefetchSteps;
+                if (pw < nk) {
+                    const int pit = item_of(t, pw / KB), pkb = pw % KB;
+                    const int pe = weight_slot(a.wslot, a.n_wslots, a.tiles[4 * (pit / a.m_tiles)], a.status);
+                    ptx::tma_prefetch_3d(&tm_w, ((kBlockBytes * pkb) & ~15) / 4,
+                                         (pit % a.m_tiles) * kBM, pe);
+                }
+                return true;
+            };
+            for (; ok && wc < nk && wc < R::kW - 1; ++wc) ok = issue_w(wc);
+            for (int kc = 0; ok && kc < nk; ++kc) {
+                const int it = item_of(t, kc / KB), kb = kc % KB;
+                const int tile = it / a.m_tiles;
+                const int row0 = a.tiles[4 * tile + 1];
+                const int nb = (a.tiles[4 * tile + 2] + kBoxRows - 1) / kBoxRows;
+                const uint32_t bytes = 2u * nb * kBoxRows * 128u;
+                for (int hh = 0; ok && hh < 2; ++hh, ++bc) {
+                    const int s = bc % R::kB;
+                    if (bc >= R::kB &&
+                        !wait_bar(&bempty[t][s], ((bc / R::kB) - 1) & 1, a.wait_ns, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *st = bring + (size_t)s * kHalfBytes;
+                    ptx::mbar_arrive_expect_tx(&bfull[t][s], bytes);
+                    for (int c2 = 0; c2 < 2; ++c2)
+                        for (int r = 0; r < nb; ++r)
+                            ptx::tma_load_2d(st + c2 * kChunkBytes + r * kBoxRows * 128, &tm_h,
+                                             (2 * kb + hh) * 128 + 64 * c2, row0 + kBoxRows * r,
+                                             &bfull[t][s]);
+                }
+                if (ok && wc < nk) ok = issue_w(wc++);
+            }
+            if (!ok) {
+                set_status(a.status, DS4G_ERR_TIMEOUT);
+                *abort_flag = 1;
+            }
+            s_wissued[t] = wc;
+            s_bissued[t] = bc;
+        }
+    } else if (warp < kFirstDequantWarp) {
+        // ---------------- MMA issuer of team t ----------------
+        const int t = warp - kFirstIssuerWarp;
+        const uint64_t bdesc0 = ptx::sw128_desc(ptx::smem_addr(smem + R::kBOff(t)));
+        const uint32_t acc = tmem + kAccCol + 128u * (uint32_t)t;
+        int hc = 0;                                     // half steps (fills) of the team
+        bool ok = true;
+        for (int q = 0; ok && q < team_items(t); ++q) {
+            const int it = item_of(t, q);
+            const int nb = (a.tiles[4 * (it / a.m_tiles) + 2] + kBoxRows - 1) / kBoxRows;
+            const uint32_t idesc = ptx::idesc_f16(kBM, nb * kBoxRows);
+            if (q > 0) {
+                ok = wait_bar(&accempty[t], (q - 1) & 1, a.wait_ns, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+            }
+            ptx::tc_fence_after();
+            for (int hs = 0; ok && hs < 2 * KB; ++hs, ++hc) {
+                const int s = hc % R::kB;
+                const int buf = 2 * t + (hc & 1);
+                ok = wait_bar(&bfull[t][s], (hc / R::kB) & 1, a.wait_ns, abort_flag);
+                ok = ok && wait_bar(&afull[buf], (hc >> 1) & 1, a.wait_ns, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const uint64_t bd0 = bdesc0 + (uint64_t)((s * kHalfBytes) >> 4);
+                const uint32_t a_buf = tmem + (uint32_t)buf * 64u;
+#pragma unroll
+                for (int i = 0; i < kHalfMmas; ++i) {
+                    const int kk = 16 * i;
+                    const uint64_t bd = bd0 + (uint64_t)(((kk >> 6) * kChunkBytes + (kk & 63) * 2) >> 4);
+                    ptx::mma_f16_ts_elect(acc, a_buf + 8 * i, bd, idesc, hs > 0 || i > 0);
+                }
+                ptx::mma_commit_elect(&aempty[buf]);
+                ptx::mma_commit_elect(&bempty[t][s]);
+                __syncwarp();
+            }
+            if (!ok) break;
+            ptx::mma_commit_elect(&accfull[t]);
+            __syncwarp();
+        }
+        if (!ok && lane == 0) {
+            set_status(a.status, DS4G_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+        ptx::mma_commit_elect(&drain[t]);
+        ptx::mbar_wait(&drain[t], 0, a.wait_ns);
+        __syncwarp();
+    } else if (warp >= kFirstDequantWarp + kDequantWarps) {
+        // ---------------- epilogue: both teams' items in the CTA's order ----------------
+        const int row = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        bool ok = true;
+        for (int j = 0; ok && j < my_items; ++j) {
+            const int t = j & 1, q = j >> 1;
+            const int it = item_of(t, q);
+            const int tile = it / a.m_tiles, mt = it % a.m_tiles;
+            const int row0 = a.tiles[4 * tile + 1], nlen = a.tiles[4 * tile + 2];
+            ok = wait_bar(&accfull[t], q & 1, a.wait_ns, abort_flag);
+            ok = __all_sync(0xffffffffu, ok);
+            if (!ok) break;
+            ptx::tc_fence_after();
+            const int m = mt * kBM + row;
+            const uint32_t acc = tmem + lane_base + kAccCol + 128u * (uint32_t)t;
+            for (int c = 0; 8 * c < nlen; ++c) {
+                float o[8];
+                ptx::tmem_ld8(acc + 8 * c, o);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int tk = 8 * c + i;
+                    if (tk < nlen) {
+                        const int pos = row0 + tk;
+                        const float sh = exp2i(2 * __ldg(a.eseg + pos) + kHExpOffset);
+                        a.yslot[(size_t)pos * a.H + m] = __ldg(a.wseg + pos) * (o[i] * sh);
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&accempty[t]);
+        }
+        if (!ok) {
+            if (lane == 0) set_status(a.status, DS4G_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+    } else {
+        // ---------------- dequantizers of team t ----------------
+        const int wg = (warp - kFirstDequantWarp) >> 2;
+        const int t = wg >> 1, gh = wg & 1;
+        const QuarterConst k = quarter_const(0, gh);
+        const int row = 32 * (warp & 3) + lane;
+        const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+        const uint32_t cb_lane = ptx::smem_addr(cbrep) + (uint32_t)(lane & 15) * 8;
+        const uint8_t *wring = smem + R::kWOff(t);
+        int kc = 0, tf = 0;
+        bool ok = true;
+        for (int q = 0; ok && q < team_items(t); ++q) {
+            for (int kb = 0; ok && kb < KB; ++kb, ++kc) {
+                const int ws = kc % R::kW;
+                ok = wait_bar(&wfull[t][ws], (kc / R::kW) & 1, a.wait_ns, abort_flag);
+                ok = __all_sync(0xffffffffu, ok);
+                if (!ok) break;
+                const uint8_t *win = wring + (size_t)ws * kAqBytes + row * (kWinWords * 4);
+                for (int hh = 0; ok && hh < 2; ++hh, ++tf) {
+                    const int buf = 2 * t + (tf & 1);
+                    if (tf >= 2) {
+                        ok = wait_bar(&aempty[buf], ((tf >> 1) - 1) & 1, a.wait_ns, abort_flag);
+                        ok = __all_sync(0xffffffffu, ok);
+                        if (!ok) break;
+                        ptx::tc_fence_after();
+                    }
+                    uint32_t out[32];
+                    quarter_values<FMT>(win, kb, hh, k, cb_lane, out);
+                    ptx::tmem_st32(tmem + lane_base + (uint32_t)buf * 64u + 32u * gh, out);
+                    ptx::tmem_st_wait();
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&afull[buf]);
+                }
+                if (!ok) break;
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&wempty[t][ws]);
+            }
+        }
+        if (!ok) {
+            if (lane == 0) set_status(a.status, DS4G_ERR_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+
+    __syncthreads();
+    // after an abort: the copies this CTA issued land before it exits
+    if (threadIdx.x == 0 && *abort_flag) {
+        for (int t = 0; t < 2; ++t) {
+            drain_ring(wfull[t], R::kW, s_wissued[t], a.wait_ns);
+            drain_ring(bfull[t], R::kB, s_bissued[t], a.wait_ns);
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -892,6 +1224,18 @@ cudaError_t act_map(CUtensorMap *m, const void *base, int64_t K, int64_t rows)
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+template <int FMT>
+cudaError_t launch_tc_down(const CUtensorMap &w, const CUtensorMap &h, const TcArgs &args, int grid,
+                           cudaStream_t s)
+{
+    const size_t smem = DownRing<FMT>::kBytes + 1024;
+    cudaError_t e = cudaFuncSetAttribute(tc_down_kernel<FMT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    tc_down_kernel<FMT><<<grid, kDownThreads, smem, s>>>(w, h, args);
+    return cudaGetLastError();
+}
+
 template <int MODE, int FMT>
 cudaError_t launch_tc(const CUtensorMap &a0, const CUtensorMap &a1, const CUtensorMap &b,
                       const TcArgs &args, int grid, cudaStream_t s)
@@ -1022,7 +1366,7 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     a.K = la.I_pad;
     a.m_tiles = la.H / kBM;
     if ((e = la.dn_format == DS4G_FMT_CB2
-                 ? launch_tc<1, DS4G_FMT_CB2>(m_down, m_down, m_h, a, dev.sm_count, s)
+                 ? launch_tc_down<DS4G_FMT_CB2>(m_down, m_h, a, dev.sm_count, s)
                  : launch_tc<1, DS4G_FMT_Q2K>(m_down, m_down, m_h, a, dev.sm_count, s)) != cudaSuccess)
         return e;
     if (split && (e = launch_gemv_down(lg, dev, s)) != cudaSuccess) return e;
