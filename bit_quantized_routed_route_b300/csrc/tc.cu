@@ -15,14 +15,15 @@
 //
 // The pipeline unit is the half block: 128 weights of every row of the item
 // (one half of a 256-weight super-block), one fill of a 64-column A buffer in
-// tensor memory, eight K = 16 MMAs.  Each half has its own team of
-// dequantizing warps and its own two A buffers, so a buffer is dequantized
-// again only after the team's other fill: the time one thread needs to issue
-// a fill's MMAs (about 100-150 cycles per tcgen05.mma while the dequantizing
-// warps run, whatever the token count) and their completion overlap the
-// dequantization of the next fill, and the two teams' hand-off latencies
-// (tensor-memory stores, barrier arrivals and waits) overlap each other's
-// arithmetic.
+// tensor memory, eight K = 16 MMAs.  Each team of dequantizing warps has its
+// own two A buffers, so a buffer is dequantized again only after the team's
+// other fill: the time one thread needs to issue a fill's MMAs (about 100-150
+// cycles per tcgen05.mma while the dequantizing warps run, whatever the token
+// count) and their completion overlap the dequantization of the next fill,
+// and the two teams' hand-off latencies (tensor-memory stores, barrier
+// arrivals and waits) overlap each other's arithmetic.  In the gate/up kernel
+// each team feeds its own issuer (one per matrix), so the teams never wait for
+// each other's fills.
 //
 // Roles inside a CTA (one CTA per SM, persistent over the items):
 //   warp 0     weight producer: per 256-wide K step, the 16-byte aligned
@@ -38,12 +39,13 @@
 //              accumulators in tensor memory.  Gate/up kernel: warp 2 issues
 //              every W_gate fill, warp 3 every W_up fill.  Down kernel: warp
 //              2 alone;
-//   warps 4-19 dequantizers, two teams (halves 0 and 1) of two warpgroups:
-//              each thread owns one weight row and, per fill, one quarter of
-//              the block, the field pair 2*gh, 2*gh+1 (Q2_K) or weights 64*gh
-//              .. +63 (codebook) of its team's half: 64 weights, 32 fp16
-//              pairs formed in registers and stored to tensor memory
-//              (tcgen05.st).  In the gate/up kernel the sixteen warps are
+//   warps 4-19 dequantizers, two teams of two warpgroups (gate/up kernel:
+//              team t dequantizes matrix t; Q2_K down kernel: team t the K
+//              steps of parity t): each thread owns one weight row and, per
+//              fill (one half of the block), the field pair 2*gh, 2*gh+1
+//              (Q2_K) or weights 64*gh .. +63 (codebook) of the half: 64
+//              weights, 32 fp16 pairs formed in registers and stored to
+//              tensor memory (tcgen05.st).  In the gate/up kernel the sixteen warps are
 //              also the epilogue after each item (tcgen05.ld of the
 //              accumulators, SiLU*up, fp16 stores of h);
 //   warps 20-23  down kernel only: the epilogue (tcgen05.ld, routing weight,
@@ -63,7 +65,7 @@
 // rounding is the multiply by d.
 //
 // Tensor memory (512 columns): columns 0..255 are the four A buffers of 64
-// columns (K = 128 fp16), 2hh and 2hh+1 for half hh; columns 256..383 and 384..511 are the fp32
+// columns (K = 128 fp16), 2t and 2t+1 for team t; columns 256..383 and 384..511 are the fp32
 // accumulators (gate and up, or the down kernel's two alternating
 // accumulators).  Every mbarrier wait is bounded; on expiry the kernel
 // records DS4G_ERR_TIMEOUT in the status word, lets every role leave its
@@ -366,13 +368,13 @@ __device__ __forceinline__ void quarter_values(const uint8_t *win, int kb, int h
     }
 }
 
-// The dequantizing role of one warp (both kernels of tc_kernel).  Gate/up:
-// team hh (warpgroups 2hh, 2hh+1) fills half hh of every block, the W_gate
-// and W_up halves into A buffers 2hh and 2hh+1.  Down (Q2_K): team t owns the
-// K steps of parity t and fills both halves of each into its buffers 2t, 2t+1,
-// so while the issuer runs one team's K step the other team already
-// dequantizes its next one.  The two teams run independently, so one team's
-// hand-off latencies overlap the other's arithmetic.
+// The dequantizing role of one warp (both kernels of tc_kernel).  Two teams
+// of two warpgroups, each with its own two A buffers (2*team, 2*team + 1 for
+// halves 0 and 1).  Gate/up: team t dequantizes matrix t (W_gate, W_up) of
+// every K step, and issuer t issues its fills alone, so each matrix is a
+// private pipeline of dequantizers and issuer.  Down (Q2_K): team t owns the
+// K steps of parity t, so while the issuer runs one team's K step the other
+// team already dequantizes its next one.
 template <int MODE, int FMT>
 struct DequantRole {
     using R = Ring<MODE, FMT>;
@@ -396,13 +398,11 @@ struct DequantRole {
         lane_base = (uint32_t)(32 * quarter) << 16;
     }
 
-    // One fill: half hh of matrix `mat`, K step kb, window stage ws.  Gate/up
-    // kernel: hh is this team's half, the buffer 2hh + mat.  Down kernel: the
-    // team owns the K steps of its parity and fills both halves into its
-    // buffers 2*team + hh.
+    // One fill: half hh of matrix `mat`, K step kb, window stage ws, into this
+    // team's buffer 2*team + hh (team = k.hh).
     __device__ __forceinline__ void fill(int ws, int mat, int kb, int hh)
     {
-        const int buf = 2 * k.hh + (MODE == 0 ? mat : hh);
+        const int buf = 2 * k.hh + hh;
         const int uses = MODE == 0 ? kc : (kc >> 1);      // earlier fills of the buffer
         if (uses > 0) {
             ok = wait_bar(&c.aempty[buf], (uses - 1) & 1, a.wait_ns, c.abort_flag);
@@ -433,10 +433,8 @@ struct DequantRole {
                 ok = wait_bar(&c.wfull[ws], (kc / R::kW) & 1, a.wait_ns, c.abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                if (MODE == 0)
-                    for (int mat = 0; ok && mat < NMAT; ++mat) fill(ws, mat, kb, k.hh);
-                else
-                    for (int hh = 0; ok && hh < 2; ++hh) fill(ws, 0, kb, hh);
+                // gate/up: team = matrix; down: the stage's only matrix
+                for (int hh = 0; ok && hh < 2; ++hh) fill(ws, MODE == 0 ? k.hh : 0, kb, hh);
                 if (!ok) break;
                 // this warp has read the stage's windows
                 __syncwarp();
@@ -645,8 +643,9 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
         }
     } else if (warp < kFirstDequantWarp) {
         // ---------------- MMA issuers ----------------
-        // Gate/up kernel: issuer X issues the W_gate (X = 0) or W_up (X = 1)
-        // fills, A buffers X and 2 + X (halves 0 and 1), into accumulator X.
+        // Gate/up kernel: issuer X issues team X's fills (W_gate for X = 0,
+        // W_up for X = 1), A buffers 2X and 2X + 1 (halves 0 and 1), into
+        // accumulator X.
         // One thread issues tcgen05.mma far slower than the tensor pipe runs
         // them at a segment's token counts; two issuers keep it fed.  Down
         // kernel (one fill per half step, bound by its dequantizers): issuer
@@ -679,7 +678,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                     // the fill's A buffer (half hh of K step kc) and how often
                     // it was filled before
                     const int kc = hc >> 1, hh = hc & 1;
-                    const int buf = MODE == 0 ? 2 * hh + X : 2 * (kc & 1) + hh;
+                    const int buf = MODE == 0 ? 2 * X + hh : 2 * (kc & 1) + hh;
                     const int uses = MODE == 0 ? kc : (kc >> 1);
                     ok = wait_bar(&bfull[s], (hc / R::kB) & 1, a.wait_ns, abort_flag);
                     ok = ok && wait_bar(&afull[buf], uses & 1, a.wait_ns, abort_flag);
