@@ -19,13 +19,15 @@ prefill_2048   7168   2048  256  8   2048  Q2_K      sigmoid  3
 codebook_512   7168   2048  256  8   512   codebook  sigmoid  4
 mixed_2048     7168   2048  256  8   2048  mixed     sigmoid  5
 kquant_32tok   7168   2048  256  8   32    Q4_K/Q6K  sigmoid  6
+mxfp4_32tok    7168   2048  256  8   32    MXFP4     sigmoid  7
 =============  =====  ====  ===  ==  ====  ========  =======  ====
 
 mixed_2048 is the shipping mix of the ds4 weights (codebook-2-bit gate/up,
 Q2_K down) on the prefill layer with the prefill routing recipe.
 kquant_32tok is a higher-bit routed layer (Q4_K gate/up, Q6_K down; the
 ds4f-q2-q4 / ds4f-q4 downloads and the routed K-quant formats the ds4
-README names) at the 32-token decode batch.
+README names) at the 32-token decode batch; mxfp4_32tok the same layer with
+MXFP4 routed experts (the ds4f-mxfp4 download).
 
 Rows are stored packed (ceil(K/256) blocks back to back) for Q2_K; the
 codebook rows (70-byte blocks) are padded to a multiple of 16 bytes so that
@@ -46,8 +48,10 @@ SOURCE = os.path.join(HERE, "synth.c")
 LIBRARY = os.path.join(HERE, "libds4g_synth.so")
 
 QK = 256
-FMT_Q2K, FMT_CB2, FMT_Q4K, FMT_Q5K, FMT_Q6K = 0, 1, 2, 3, 4
-BLOCK_BYTES = {FMT_Q2K: 84, FMT_CB2: 70, FMT_Q4K: 144, FMT_Q5K: 176, FMT_Q6K: 210}
+FMT_Q2K, FMT_CB2, FMT_Q4K, FMT_Q5K, FMT_Q6K, FMT_MXFP4 = 0, 1, 2, 3, 4, 5
+# bytes per 256 weights (MXFP4: eight 17-byte blocks of 32)
+BLOCK_BYTES = {FMT_Q2K: 84, FMT_CB2: 70, FMT_Q4K: 144, FMT_Q5K: 176, FMT_Q6K: 210,
+               FMT_MXFP4: 136}
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 LOGITS_NORMAL, LOGITS_UNIFORM, LOGITS_BIASED, LOGITS_ZIPF = 0, 1, 2, 3
 TENSOR_GATE, TENSOR_UP, TENSOR_DOWN = 3, 4, 5
@@ -106,6 +110,7 @@ CONFIGS: Dict[str, Config] = {
                row_align=16, down_format=FMT_Q2K),
         Config("kquant_32tok", 7168, 2048, 256, 8, 32, FMT_Q4K, SCORE_SIGMOID, LOGITS_UNIFORM, 6,
                down_format=FMT_Q6K),
+        Config("mxfp4_32tok", 7168, 2048, 256, 8, 32, FMT_MXFP4, SCORE_SIGMOID, LOGITS_UNIFORM, 7),
     ]
 }
 
@@ -144,7 +149,8 @@ def lib():
         L.syn_q2k_encode_block.restype = None
         L.syn_cb2_encode_block.argtypes = [vp, vp, vp]
         L.syn_cb2_encode_block.restype = None
-        for fn in ("syn_q4k_encode_block", "syn_q5k_encode_block", "syn_q6k_encode_block"):
+        for fn in ("syn_q4k_encode_block", "syn_q5k_encode_block", "syn_q6k_encode_block",
+                   "syn_mxfp4_encode_block"):
             getattr(L, fn).argtypes = [vp, vp]
             getattr(L, fn).restype = None
         L.syn_make_codebook.argtypes = [u64, vp]
@@ -195,7 +201,7 @@ def q2k_encode(w: np.ndarray) -> np.ndarray:
 def kquant_encode(w: np.ndarray, fmt: int) -> np.ndarray:
     """Encodes fp32 weights (multiple of 256) into Q4_K / Q5_K / Q6_K blocks."""
     fn = {FMT_Q4K: "syn_q4k_encode_block", FMT_Q5K: "syn_q5k_encode_block",
-          FMT_Q6K: "syn_q6k_encode_block"}[fmt]
+          FMT_Q6K: "syn_q6k_encode_block", FMT_MXFP4: "syn_mxfp4_encode_block"}[fmt]
     w = np.ascontiguousarray(w, dtype=np.float32).reshape(-1, QK)
     out = np.zeros((w.shape[0], BLOCK_BYTES[fmt]), dtype=np.uint8)
     f = getattr(lib(), fn)

@@ -297,12 +297,47 @@ void syn_q6k_encode_block(const float *w, uint8_t *blk)
     blk[209] = (uint8_t)(dh >> 8);
 }
 
+/* MXFP4 unit (eight 17-byte blocks, 256 weights).  Per 32 weights:
+ * amax = max |w|; e = clamp(ceil(log2(amax / 6)) + 127, 0, 254) (127 when
+ * amax = 0), so |w| / 2^(e-127) <= 6; each weight takes the E2M1 magnitude
+ * nearest to |w| / 2^(e-127) (0, 0.5, 1, 1.5, 2, 3, 4, 6; the lower one on a
+ * tie) and its sign (bit 3; +0 for zero); weight i of the block goes to the
+ * low nibble of byte 1 + i, weight 16 + i to the high nibble. */
+void syn_mxfp4_encode_block(const float *w, uint8_t *blk)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    memset(blk, 0, 136);
+    for (int b = 0; b < 8; ++b) {
+        const float *v = w + 32 * b;
+        uint8_t *o = blk + 17 * b;
+        double amax = 0;
+        for (int j = 0; j < 32; ++j)
+            if (fabs((double)v[j]) > amax) amax = fabs((double)v[j]);
+        int e = 127;
+        if (amax > 0) {
+            e = (int)ceil(log2(amax / 6.0)) + 127;
+            if (e < 0) e = 0;
+            if (e > 254) e = 254;
+        }
+        o[0] = (uint8_t)e;
+        double scale = ldexp(1.0, e - 127);
+        for (int j = 0; j < 32; ++j) {
+            double x = fabs((double)v[j]) / scale;
+            int best = 0;
+            for (int c = 1; c < 8; ++c)
+                if (fabs(x - mag[c]) < fabs(x - mag[best])) best = c;
+            int code = best | ((v[j] < 0 && best != 0) ? 8 : 0);
+            o[1 + j % 16] |= (uint8_t)(code << (j < 16 ? 0 : 4));
+        }
+    }
+}
+
 /* Super-block bytes of each weight format (0 Q2_K, 1 codebook, 2 Q4_K,
- * 3 Q5_K, 4 Q6_K); 0 for an unknown format. */
+ * 3 Q5_K, 4 Q6_K, 5 MXFP4 (eight blocks)); 0 for an unknown format. */
 static int block_bytes(int format)
 {
-    static const int bb[5] = {84, 70, 144, 176, 210};
-    return format >= 0 && format < 5 ? bb[format] : 0;
+    static const int bb[6] = {84, 70, 144, 176, 210, 136};
+    return format >= 0 && format < 6 ? bb[format] : 0;
 }
 
 /* score[i] = D * n2[i] - sum_b (2 |w_b|) * |c_ib|, accumulated over b in
@@ -453,7 +488,8 @@ static void *expert_worker(void *arg)
             case 1: cb2_encode_block(w + b * QK, J->mag_t, J->n2, J->codebook, blk); break;
             case 2: syn_q4k_encode_block(w + b * QK, blk); break;
             case 3: syn_q5k_encode_block(w + b * QK, blk); break;
-            default: syn_q6k_encode_block(w + b * QK, blk); break;
+            case 4: syn_q6k_encode_block(w + b * QK, blk); break;
+            default: syn_mxfp4_encode_block(w + b * QK, blk); break;
             }
         }
     }

@@ -30,7 +30,7 @@ FMT_CB2 = 1
 QK = 256
 Q2K_BYTES = 84
 CB2_BYTES = 70
-Q4K_BYTES, Q5K_BYTES, Q6K_BYTES = 144, 176, 210
+Q4K_BYTES, Q5K_BYTES, Q6K_BYTES, MXFP4_BYTES = 144, 176, 210, 136
 
 CFLAGS = ["-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared"]
 
@@ -81,7 +81,7 @@ class Oracle:
         lib.orc_q2k_dequant.restype = None
         lib.orc_cb2_dequant.argtypes = [vp, i64, vp, vp]
         lib.orc_cb2_dequant.restype = None
-        for name in ("orc_q4k_dequant", "orc_q5k_dequant", "orc_q6k_dequant"):
+        for name in ("orc_q4k_dequant", "orc_q5k_dequant", "orc_q6k_dequant", "orc_mxfp4_dequant"):
             getattr(lib, name).argtypes = [vp, i64, vp]
             getattr(lib, name).restype = None
         lib.orc_route.argtypes = [vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
@@ -129,6 +129,10 @@ class Oracle:
     def q6k_dequant(self, blocks: np.ndarray) -> np.ndarray:
         """blocks: uint8 [..., 210*n] -> float32 [n*256]."""
         return self._kquant(self.lib.orc_q6k_dequant, Q6K_BYTES, blocks)
+
+    def mxfp4_dequant(self, blocks: np.ndarray) -> np.ndarray:
+        """blocks: uint8 [..., 136*n] (eight 17-byte MXFP4 blocks per 256 weights)."""
+        return self._kquant(self.lib.orc_mxfp4_dequant, MXFP4_BYTES, blocks)
 
     def cb2_dequant(self, blocks: np.ndarray, codebook: np.ndarray) -> np.ndarray:
         b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1)

@@ -39,10 +39,13 @@
 #define ORC_Q4K_BYTES 144   /* Q4_K super-block bytes                       */
 #define ORC_Q5K_BYTES 176   /* Q5_K super-block bytes                       */
 #define ORC_Q6K_BYTES 210   /* Q6_K super-block bytes                       */
+#define ORC_MX_BYTES 17     /* MXFP4 block bytes (32 weights)               */
+#define ORC_MXFP4_BYTES 136 /* eight MXFP4 blocks = 256 weights             */
 
 enum { ORC_OK = 0, ORC_ERR_INVALID = 1, ORC_ERR_NOMEM = 2 };
 enum { ORC_SCORE_SOFTMAX = 0, ORC_SCORE_SIGMOID = 1 };
-enum { ORC_FMT_Q2K = 0, ORC_FMT_CB2 = 1, ORC_FMT_Q4K = 2, ORC_FMT_Q5K = 3, ORC_FMT_Q6K = 4 };
+enum { ORC_FMT_Q2K = 0, ORC_FMT_CB2 = 1, ORC_FMT_Q4K = 2, ORC_FMT_Q5K = 3, ORC_FMT_Q6K = 4,
+       ORC_FMT_MXFP4 = 5 };
 
 /* ------------------------------------------------------------------------
  * Scalar formats.
@@ -249,6 +252,44 @@ void orc_q6k_dequant_block(const uint8_t *blk, float *w)
     }
 }
 
+/* ------------------------------------------------------------------------
+ * MXFP4 routed experts (README "Model Weights": the ds4f-mxfp4 download keeps
+ * DeepSeek's released MXFP4 routed-expert weights), read as the OCP
+ * microscaling format in its GGUF block: 32 weights share one E8M0 scale.
+ *   byte 0       e: scale 2^(e - 127) (e = 255 is NaN)
+ *   bytes 1..16  qs: weight j (0..15) in the low nibble of qs[j], weight
+ *                j + 16 in its high nibble; each nibble an E2M1 code: bit 3
+ *                the sign, bits 0..2 the magnitude 0, 0.5, 1, 1.5, 2, 3, 4, 6
+ *   w_j = 2^(e - 127) * value(code_j)       (fp32: a power of two times a
+ *   value of at most 3 significant bits, exact unless it leaves fp32's range)
+ * Eight blocks (136 bytes) make the 256-weight unit that rows are counted in.
+ * --------------------------------------------------------------------- */
+static double e2m1_value(int code)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    double v = mag[code & 7];
+    return (code & 8) ? -v : v;
+}
+
+void orc_mxfp4_dequant_block(const uint8_t *blk, float *w)
+{
+    for (int j = 0; j < ORC_QK; ++j) {
+        const uint8_t *b = blk + (j / 32) * ORC_MX_BYTES;
+        int r = j % 32;
+        int byte = b[1 + r % 16];
+        int code = r < 16 ? (byte & 15) : (byte >> 4);
+        int e = b[0];
+        double scale = e == 255 ? NAN : ldexp(1.0, e - 127);
+        w[j] = (float)(scale * e2m1_value(code));
+    }
+}
+
+void orc_mxfp4_dequant(const uint8_t *blocks, int64_t n_blocks, float *out)
+{
+    for (int64_t b = 0; b < n_blocks; ++b)
+        orc_mxfp4_dequant_block(blocks + b * ORC_MXFP4_BYTES, out + b * ORC_QK);
+}
+
 void orc_q4k_dequant(const uint8_t *blocks, int64_t n_blocks, float *out)
 {
     for (int64_t b = 0; b < n_blocks; ++b)
@@ -401,11 +442,11 @@ typedef struct {
 static int orc_formats_ok(const orc_layer *L)
 {
     if (L->format != ORC_FMT_Q2K && L->format != ORC_FMT_CB2 && L->format != ORC_FMT_Q4K &&
-        L->format != ORC_FMT_Q5K)
+        L->format != ORC_FMT_Q5K && L->format != ORC_FMT_MXFP4)
         return 0;
     if (L->down_format != ORC_FMT_Q2K && L->down_format != ORC_FMT_CB2 &&
         L->down_format != ORC_FMT_Q4K && L->down_format != ORC_FMT_Q5K &&
-        L->down_format != ORC_FMT_Q6K)
+        L->down_format != ORC_FMT_Q6K && L->down_format != ORC_FMT_MXFP4)
         return 0;
     if ((L->format == ORC_FMT_CB2 || L->down_format == ORC_FMT_CB2) && !L->codebook) return 0;
     return 1;
@@ -426,6 +467,8 @@ static void dequant_row(const orc_layer *L, int fmt, const uint8_t *row, int K, 
             orc_q4k_dequant_block(row + (int64_t)b * ORC_Q4K_BYTES, out + b * ORC_QK);
         else if (fmt == ORC_FMT_Q5K)
             orc_q5k_dequant_block(row + (int64_t)b * ORC_Q5K_BYTES, out + b * ORC_QK);
+        else if (fmt == ORC_FMT_MXFP4)
+            orc_mxfp4_dequant_block(row + (int64_t)b * ORC_MXFP4_BYTES, out + b * ORC_QK);
         else
             orc_q6k_dequant_block(row + (int64_t)b * ORC_Q6K_BYTES, out + b * ORC_QK);
     }

@@ -113,7 +113,20 @@ def np_q6k_dequant(blocks: np.ndarray) -> np.ndarray:
     return ((d * sc) * q).reshape(-1)
 
 
-_NP_BLOCK = {S.FMT_Q2K: 84, S.FMT_CB2: 70, S.FMT_Q4K: 144, S.FMT_Q5K: 176, S.FMT_Q6K: 210}
+def np_mxfp4_dequant(blocks: np.ndarray) -> np.ndarray:
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(-1, 8, 17)
+    e = b[:, :, 0].astype(np.int64)
+    qs = b[:, :, 1:17]
+    codes = np.concatenate([qs & 15, qs >> 4], axis=2).astype(np.int64)     # [n, 8, 32]
+    mag = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])[codes & 7]
+    val = np.where(codes & 8, -mag, mag)
+    with np.errstate(over="ignore", invalid="ignore"):
+        scale = np.where(e == 255, np.nan, np.ldexp(1.0, e - 127))
+        return (scale[:, :, None] * val).astype(np.float32).reshape(-1)
+
+
+_NP_BLOCK = {S.FMT_Q2K: 84, S.FMT_CB2: 70, S.FMT_Q4K: 144, S.FMT_Q5K: 176, S.FMT_Q6K: 210,
+             S.FMT_MXFP4: 136}
 
 
 def np_dense_weights(layer, name: str, K: int) -> np.ndarray:
@@ -131,7 +144,7 @@ def np_dense_weights(layer, name: str, K: int) -> np.ndarray:
         w = np_cb2_dequant(raw, layer["codebook"])
     else:
         w = {S.FMT_Q4K: np_q4k_dequant, S.FMT_Q5K: np_q5k_dequant,
-             S.FMT_Q6K: np_q6k_dequant}[fmt](raw)
+             S.FMT_Q6K: np_q6k_dequant, S.FMT_MXFP4: np_mxfp4_dequant}[fmt](raw)
     return w.reshape(E, N, nblk * 256)[:, :, :K]
 
 
@@ -347,6 +360,32 @@ def pin_kquant_numpy(orc):
         assert np.array_equal(got.view(np.uint32), ref.view(np.uint32)), bb
 
 
+def pin_mxfp4_worked(orc):
+    for sb, e, i, byte, wl, wh in _rows("mxfp4_worked.txt"):
+        sb, i = int(sb), int(i)
+        blk = np.zeros(136, dtype=np.uint8)
+        blk[0::17] = 127
+        blk[17 * sb] = int(e)
+        blk[17 * sb + 1 + i] = int(byte, 16)
+        out = orc.mxfp4_dequant(blk)
+        exp = np.zeros(256, dtype=np.float32)
+        exp[32 * sb + i] = float(wl)
+        exp[32 * sb + 16 + i] = float(wh)
+        assert np.array_equal(out, exp), (sb, i, out[32 * sb + i], out[32 * sb + 16 + i])
+        assert np.array_equal(np.signbit(out), np.signbit(exp)), (sb, i, "sign of zero")
+
+
+def pin_mxfp4_numpy(orc):
+    """Random MXFP4 units (scale bytes below 255): bit-exact agreement with
+    the independent numpy decoder."""
+    rng = np.random.default_rng(23)
+    blk = rng.integers(0, 256, size=(512, 136), dtype=np.uint8)
+    blk[:, 0::17] = rng.integers(0, 255, size=(512, 8), dtype=np.uint8)
+    got = orc.mxfp4_dequant(blk)
+    ref = np_mxfp4_dequant(blk)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
 def _worked_codebook():
     cb = np.zeros((256, 8), dtype=np.int8)
     cb[0] = [8, -8, 25, -25, 43, -43, 8, 8]
@@ -449,7 +488,8 @@ def pin_forward_dense(orc):
                           down_fmt=S.FMT_Q6K),
               small_layer(seed=18, H=512, I=256, E=4, k=2, T=3, fmt=S.FMT_Q5K),
               small_layer(seed=19, H=512, I=256, E=4, k=2, T=3, fmt=S.FMT_Q2K,
-                          down_fmt=S.FMT_Q4K)]
+                          down_fmt=S.FMT_Q4K),
+              small_layer(seed=20, H=512, I=320, E=4, k=2, T=3, fmt=S.FMT_MXFP4)]
     for L in layers:
         y, ids, w = orc.moe_forward(L, L["x"], L["logits"])
         ref = np_forward(L, L["x"], L["logits"])
@@ -562,6 +602,7 @@ ALL_PINS = [
     pin_half_decode, pin_bf16_decode, pin_q2k_onehot, pin_q2k_scale_min,
     pin_q2k_zero_scale, pin_q2k_numpy, pin_cb2_worked, pin_cb2_numpy,
     pin_q4k_worked, pin_q5k_worked, pin_q6k_worked, pin_kquant_onehot, pin_kquant_numpy,
+    pin_mxfp4_worked, pin_mxfp4_numpy,
     pin_route_worked, pin_route_bruteforce, pin_route_full_k,
     pin_forward_dense, pin_forward_zero_scale, pin_forward_k1_single,
     pin_forward_scale_pow2, pin_forward_relabel, pin_quantizer_roundtrip,

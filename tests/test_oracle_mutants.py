@@ -103,6 +103,16 @@ MUTANTS = {
                              "const uint8_t *scales = (const uint8_t *)(blk + 192);")],
     "q6k_d_offset": [("float d = (float)orc_half_to_double(rd16(blk + 208));",
                       "float d = (float)orc_half_to_double(rd16(blk + 206));")],
+    "mxfp4_nibbles_swapped": [("int code = r < 16 ? (byte & 15) : (byte >> 4);",
+                               "int code = r < 16 ? (byte >> 4) : (byte & 15);")],
+    "mxfp4_scale_bias_126": [("double scale = e == 255 ? NAN : ldexp(1.0, e - 127);",
+                              "double scale = e == 255 ? NAN : ldexp(1.0, e - 126);")],
+    "mxfp4_e2m1_six_is_five": [("{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0}",
+                                "{0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 5.0}")],
+    "mxfp4_sign_bit_2": [("return (code & 8) ? -v : v;", "return (code & 4) ? -v : v;")],
+    "mxfp4_qs_offset_0": [("int byte = b[1 + r % 16];", "int byte = b[r % 16];")],
+    "mxfp4_block_stride_16": [("const uint8_t *b = blk + (j / 32) * ORC_MX_BYTES;",
+                               "const uint8_t *b = blk + (j / 32) * 16;")],
     "kquant_down_reads_q5k": [("            orc_q6k_dequant_block(row + (int64_t)b * ORC_Q6K_BYTES, out + b * ORC_QK);",
                                "            orc_q5k_dequant_block(row + (int64_t)b * ORC_Q6K_BYTES, out + b * ORC_QK);")],
 }
