@@ -95,14 +95,14 @@ def default_steps(cfg: S.Config):
     # ~1-2 s of device time at the expected step times
     return {"tiny": 20000, "decode_1tok": 100000, "decode_32tok": 4000,
             "prefill_2048": 200, "codebook_512": 1000, "mixed_2048": 200,
-            "kquant_32tok": 1000}[cfg.name]
+            "kquant_32tok": 1000, "mxfp4_32tok": 1000}[cfg.name]
 
 
 def floor_steps(cfg: S.Config):
     # about 0.2 s of device time: the least a per-config line is timed over
     return {"tiny": 5000, "decode_1tok": 5000, "decode_32tok": 150,
             "prefill_2048": 60, "codebook_512": 80, "mixed_2048": 60,
-            "kquant_32tok": 100}[cfg.name]
+            "kquant_32tok": 100, "mxfp4_32tok": 100}[cfg.name]
 
 
 # ---------------------------------------------------------------------------
@@ -384,7 +384,7 @@ def reference_arm(args, cfg, rank, world):
 
 def workload_config(cfg: S.Config, copies: int, l2_note: str):
     names = {S.FMT_Q2K: "Q2_K", S.FMT_CB2: "codebook-2bit", S.FMT_Q4K: "Q4_K", S.FMT_Q5K: "Q5_K",
-             S.FMT_Q6K: "Q6_K"}
+             S.FMT_Q6K: "Q6_K", S.FMT_MXFP4: "MXFP4"}
     fmt = (names[cfg.format] if cfg.format == cfg.dn_format
            else f"{names[cfg.format]} gate/up + {names[cfg.dn_format]} down")
     return {"workload": f"{cfg.name}: H={cfg.hidden} I={cfg.inter} E={cfg.n_experts} "

@@ -7,7 +7,7 @@ used for device memory and streams.  Importing this package on a machine
 where the library is missing raises immediately; there is no fallback.
 
 Entry points (same names as the C ABI, without the ``ds4g_`` prefix):
-  route_topk, q2k_dequant, cb2_dequant, q4k_dequant, q5k_dequant, q6k_dequant,
+  route_topk, q2k_dequant, cb2_dequant, q4k_dequant, q5k_dequant, q6k_dequant, mxfp4_dequant,
   moe_workspace_bytes, moe_forward,
   moe_forward_host, moe_routing_view, status_string, abi_version.
 Each returns the raw status code; ``check(status)`` turns a non-zero status
@@ -25,13 +25,13 @@ LIBRARY = os.path.join(HERE, "libds4g.so")
 
 OK, ERR_INVALID, ERR_SHAPE, ERR_LAYOUT, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(8)
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
-FMT_Q2K, FMT_CB2, FMT_Q4K, FMT_Q5K, FMT_Q6K = 0, 1, 2, 3, 4
+FMT_Q2K, FMT_CB2, FMT_Q4K, FMT_Q5K, FMT_Q6K, FMT_MXFP4 = 0, 1, 2, 3, 4, 5
 F32, F16, BF16 = 0, 1, 2
 FORCE_GEMV, FORCE_TC, DEBUG_STALL = 1, 2, 256
 
 EXPORTED = (
     "ds4g_route_topk", "ds4g_q2k_dequant", "ds4g_cb2_dequant", "ds4g_q4k_dequant",
-    "ds4g_q5k_dequant", "ds4g_q6k_dequant", "ds4g_moe_workspace_bytes",
+    "ds4g_q5k_dequant", "ds4g_q6k_dequant", "ds4g_mxfp4_dequant", "ds4g_moe_workspace_bytes",
     "ds4g_moe_forward", "ds4g_moe_forward_host", "ds4g_moe_routing_view",
     "ds4g_moe_forward_phased", "ds4g_moe_forward_launches", "ds4g_moe_device_status",
     "ds4g_status_string", "ds4g_abi_version", "ds4g_last_cuda_error",
@@ -79,6 +79,7 @@ def _load() -> ctypes.CDLL:
         "ds4g_q4k_dequant": (i32, [vp, i64, vp, i32, vp]),
         "ds4g_q5k_dequant": (i32, [vp, i64, vp, i32, vp]),
         "ds4g_q6k_dequant": (i32, [vp, i64, vp, i32, vp]),
+        "ds4g_mxfp4_dequant": (i32, [vp, i64, vp, i32, vp]),
         "ds4g_moe_noalloc_status": (i32, [ctypes.POINTER(MoeDesc), i32, ctypes.POINTER(i32), vp]),
         "ds4g_expert_cache_create": (i32, [ctypes.POINTER(MoeDesc), i32, ctypes.POINTER(vp)]),
         "ds4g_expert_cache_workspace_bytes": (ctypes.c_size_t, [vp, i32]),
@@ -168,6 +169,10 @@ def q5k_dequant(blocks, n_blocks, out, out_dtype, stream=None) -> int:
 
 def q6k_dequant(blocks, n_blocks, out, out_dtype, stream=None) -> int:
     return _lib.ds4g_q6k_dequant(_ptr(blocks), n_blocks, _ptr(out), out_dtype, _stream(stream))
+
+
+def mxfp4_dequant(blocks, n_blocks, out, out_dtype, stream=None) -> int:
+    return _lib.ds4g_mxfp4_dequant(_ptr(blocks), n_blocks, _ptr(out), out_dtype, _stream(stream))
 
 
 def cb2_dequant(blocks, n_blocks, codebook, out, out_dtype, stream=None) -> int:

@@ -204,6 +204,8 @@ cudaError_t launch_kquant_dequant(int fmt, const uint8_t *blocks, int64_t n_bloc
         launch_kquant_fmt<DS4G_FMT_Q4K>(blocks, n_blocks, out, dtype, grid, s);
     else if (fmt == DS4G_FMT_Q5K)
         launch_kquant_fmt<DS4G_FMT_Q5K>(blocks, n_blocks, out, dtype, grid, s);
+    else if (fmt == DS4G_FMT_MXFP4)
+        launch_kquant_fmt<DS4G_FMT_MXFP4>(blocks, n_blocks, out, dtype, grid, s);
     else
         launch_kquant_fmt<DS4G_FMT_Q6K>(blocks, n_blocks, out, dtype, grid, s);
     return cudaGetLastError();

@@ -61,9 +61,9 @@ ds4g_status make_plan(const ds4g_moe_desc *d, int32_t T, Plan *p)
     if (d->top_k < 1 || d->top_k > DS4G_MAX_TOPK || d->top_k > d->n_experts)
         return DS4G_ERR_INVALID;
     if (d->score != DS4G_SCORE_SOFTMAX && d->score != DS4G_SCORE_SIGMOID) return DS4G_ERR_INVALID;
-    // routed gate/up: Q2_K, codebook, Q4_K, Q5_K; routed down: also Q6_K
+    // routed gate/up: Q2_K, codebook, Q4_K, Q5_K, MXFP4; routed down: also Q6_K
     if (d->format != DS4G_FMT_Q2K && d->format != DS4G_FMT_CB2 && d->format != DS4G_FMT_Q4K &&
-        d->format != DS4G_FMT_Q5K)
+        d->format != DS4G_FMT_Q5K && d->format != DS4G_FMT_MXFP4)
         return DS4G_ERR_INVALID;
     if (block_bytes_of(d->down_format) == 0) return DS4G_ERR_INVALID;
     if (d->n_slots < 0 || (d->n_slots == 0) != (d->expert_slot == nullptr))
@@ -327,8 +327,9 @@ ds4g_status kquant_dequant(int fmt, const void *blocks, int64_t n_blocks, void *
     if (n_blocks == 0) return DS4G_OK;
     if (!blocks || !out) return DS4G_ERR_INVALID;
     // every block of a 4-byte aligned Q4_K / Q5_K array is 4-byte aligned;
-    // Q6_K blocks (210 bytes) only 2-byte aligned
-    if (!aligned(blocks, fmt == DS4G_FMT_Q6K ? 2 : 4) || !aligned(out, 16)) return DS4G_ERR_LAYOUT;
+    // Q6_K blocks (210 bytes) only 2-byte aligned; MXFP4 is read bytewise
+    const size_t balign = fmt == DS4G_FMT_Q6K ? 2 : fmt == DS4G_FMT_MXFP4 ? 1 : 4;
+    if (!aligned(blocks, balign) || !aligned(out, 16)) return DS4G_ERR_LAYOUT;
     return from_cuda(launch_kquant_dequant(fmt, static_cast<const uint8_t *>(blocks), n_blocks, out,
                                            out_dtype, static_cast<cudaStream_t>(stream)));
 }
@@ -350,6 +351,12 @@ ds4g_status ds4g_q6k_dequant(const void *blocks, int64_t n_blocks, void *out, in
                              void *stream)
 {
     return kquant_dequant(DS4G_FMT_Q6K, blocks, n_blocks, out, out_dtype, stream);
+}
+
+ds4g_status ds4g_mxfp4_dequant(const void *blocks, int64_t n_blocks, void *out, int32_t out_dtype,
+                               void *stream)
+{
+    return kquant_dequant(DS4G_FMT_MXFP4, blocks, n_blocks, out, out_dtype, stream);
 }
 
 ds4g_status ds4g_cb2_dequant(const void *blocks, int64_t n_blocks, const int8_t *codebook,

@@ -19,6 +19,7 @@ constexpr int kCB2Bytes = 70;    // codebook-2-bit super-block
 constexpr int kQ4KBytes = 144;   // Q4_K super-block
 constexpr int kQ5KBytes = 176;   // Q5_K super-block
 constexpr int kQ6KBytes = 210;   // Q6_K super-block
+constexpr int kMXFP4Bytes = 136; // eight 17-byte MXFP4 blocks (256 weights)
 
 // The weight slot of expert e: e itself, or wslot[e] when the weight
 // tensors hold a set of resident slots (an expert cache).  An entry outside
@@ -42,6 +43,7 @@ __host__ __device__ constexpr int block_bytes_of(int fmt)
          : fmt == DS4G_FMT_Q4K ? kQ4KBytes
          : fmt == DS4G_FMT_Q5K ? kQ5KBytes
          : fmt == DS4G_FMT_Q6K ? kQ6KBytes
+         : fmt == DS4G_FMT_MXFP4 ? kMXFP4Bytes
          : 0;
 }
 
@@ -108,7 +110,7 @@ cudaError_t launch_q2k_dequant(const uint8_t *blocks, int64_t n_blocks, void *ou
                                cudaStream_t s);
 cudaError_t launch_cb2_dequant(const uint8_t *blocks, int64_t n_blocks, const int8_t *cb,
                                void *out, int dtype, cudaStream_t s);
-// Q4_K / Q5_K / Q6_K (fmt) super-blocks to fp32 / fp16 / bf16.
+// Q4_K / Q5_K / Q6_K / MXFP4 (fmt) super-blocks to fp32 / fp16 / bf16.
 cudaError_t launch_kquant_dequant(int fmt, const uint8_t *blocks, int64_t n_blocks, void *out,
                                   int dtype, cudaStream_t s);
 

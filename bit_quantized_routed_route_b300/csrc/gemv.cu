@@ -1,6 +1,7 @@
 // gemv.cu -- the general expert path: grouped dequant-and-dot on CUDA cores,
 // correct for every segment size and every weight format (Q2_K, codebook,
-// and the Q4_K / Q5_K / Q6_K routed formats, which only this path runs).
+// and the Q4_K / Q5_K / Q6_K and MXFP4 routed formats, which only this path
+// runs).
 //
 // Per active expert e with segment tokens t_0..t_{n-1} (the assignments
 // perm[offsets[e] .. offsets[e+1]-1]):
@@ -252,6 +253,7 @@ cudaError_t launch_gemv_gateup(const LayerArgs &a, const DeviceInfo &dev, cudaSt
     case DS4G_FMT_CB2: gateup_kernel<DS4G_FMT_CB2><<<grid, kWarps * 32, 0, s>>>(a); break;
     case DS4G_FMT_Q4K: gateup_kernel<DS4G_FMT_Q4K><<<grid, kWarps * 32, 0, s>>>(a); break;
     case DS4G_FMT_Q5K: gateup_kernel<DS4G_FMT_Q5K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_MXFP4: gateup_kernel<DS4G_FMT_MXFP4><<<grid, kWarps * 32, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -266,6 +268,7 @@ cudaError_t launch_gemv_down(const LayerArgs &a, const DeviceInfo &dev, cudaStre
     case DS4G_FMT_Q4K: down_kernel<DS4G_FMT_Q4K><<<grid, kWarps * 32, 0, s>>>(a); break;
     case DS4G_FMT_Q5K: down_kernel<DS4G_FMT_Q5K><<<grid, kWarps * 32, 0, s>>>(a); break;
     case DS4G_FMT_Q6K: down_kernel<DS4G_FMT_Q6K><<<grid, kWarps * 32, 0, s>>>(a); break;
+    case DS4G_FMT_MXFP4: down_kernel<DS4G_FMT_MXFP4><<<grid, kWarps * 32, 0, s>>>(a); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();

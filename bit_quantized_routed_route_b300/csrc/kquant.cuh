@@ -1,8 +1,11 @@
-// kquant.cuh -- device decoders of the higher-bit routed-expert formats:
-// Q4_K and Q5_K (routed gate/up and down) and Q6_K (routed down), the GGUF
-// K-quant super-blocks of 256 weights (ds4 README mirror, "Model Weights",
-// which lists the routed expert formats, and "Acknowledgements to llama.cpp
-// and GGML" for the GGUF layouts).
+// kquant.cuh -- device decoders of the routed-expert formats beyond the
+// 2-bit ones: Q4_K and Q5_K (routed gate/up and down) and Q6_K (routed down),
+// the GGUF K-quant super-blocks of 256 weights, and MXFP4 (ds4 README mirror,
+// "Model Weights", which lists the routed expert formats and the ds4f-mxfp4
+// download, and "Acknowledgements to llama.cpp and GGML" for the GGUF
+// layouts).  MXFP4 (OCP microscaling FP4): 17-byte blocks of 32 weights, an
+// E8M0 scale byte then 16 bytes of E2M1 codes (weight i low nibble of byte
+// 1 + i, weight i + 16 high nibble); w = 2^(e-127) * value.
 //
 //   Q4_K (144 B): d fp16 @0, dmin fp16 @2, 12 packed scale bytes @4, qs @16
 //   Q5_K (176 B): d @0, dmin @2, packed scales @4, qh[32] @16, qs @48
@@ -62,12 +65,34 @@ __device__ __forceinline__ int byte_of(const uint32_t (&v)[4], int i)
     return (v[i >> 2] >> (8 * (i & 3))) & 0xFF;
 }
 
+// E2M1 value of a 4-bit code: bit 3 the sign, bits 0..2 the magnitude
+// 0, 0.5, 1, 1.5, 2, 3, 4, 6: exponent field m >> 1, mantissa bit m & 1;
+// exponent 0 is the subnormal 0 / 0.5, exponent x >= 1 gives
+// (2 + mantissa) * 2^(x-1) / 2 (integer arithmetic, then an exact halving).
+__device__ __forceinline__ float e2m1_value(int code)
+{
+    const int m = code & 7;
+    const float mag = m < 2 ? 0.5f * (float)m : 0.5f * (float)((2 + (m & 1)) << ((m >> 1) - 1));
+    return (code & 8) ? -mag : mag;
+}
+
 // fp32 weights 16u .. 16u+15 of one K-quant super-block (FMT = DS4G_FMT_Q4K,
-// DS4G_FMT_Q5K or DS4G_FMT_Q6K).
+// DS4G_FMT_Q5K or DS4G_FMT_Q6K) or MXFP4 unit of eight blocks (the low (u
+// even) or high (u odd) nibbles of block u/2: weights 16 (u&1) .. +15 of it).
 template <int FMT>
 __device__ __forceinline__ void kquant_unit16(const uint8_t *__restrict__ blk, int u, float (&w)[16])
 {
-    if constexpr (FMT == DS4G_FMT_Q4K || FMT == DS4G_FMT_Q5K) {
+    if constexpr (FMT == DS4G_FMT_MXFP4) {
+        const uint8_t *b = blk + 17 * (u >> 1);
+        const uint32_t e = __ldg(b);
+        // 2^(e-127): e = 0 is the subnormal 2^-127, e = 255 NaN
+        const float scale = e == 0 ? __uint_as_float(0x00400000u)
+                          : e == 255 ? __uint_as_float(0x7FC00000u)
+                                     : __uint_as_float(e << 23);
+        const int sh = 4 * (u & 1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = scale * e2m1_value((__ldg(b + 1 + i) >> sh) & 15);
+    } else if constexpr (FMT == DS4G_FMT_Q4K || FMT == DS4G_FMT_Q5K) {
         const int s = u >> 1;                       // 32-weight sub-block
         const int c = u >> 2;                       // 64-weight chunk
         const int l0 = 16 * (u & 1);                // first lane

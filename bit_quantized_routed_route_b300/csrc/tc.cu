@@ -378,7 +378,6 @@ __device__ __forceinline__ void quarter_values(const uint8_t *win, int kb, int h
 template <int MODE, int FMT>
 struct DequantRole {
     using R = Ring<MODE, FMT>;
-    static constexpr int NMAT = R::NMAT;
 
     const TcArgs &a;
     const TcCta &c;

@@ -90,7 +90,9 @@ typedef enum ds4g_format {
     DS4G_FMT_CB2 = 1,          /* 70-byte codebook-2-bit super-blocks               */
     DS4G_FMT_Q4K = 2,          /* 144-byte Q4_K super-blocks (gate/up or down)      */
     DS4G_FMT_Q5K = 3,          /* 176-byte Q5_K super-blocks (gate/up or down)      */
-    DS4G_FMT_Q6K = 4           /* 210-byte Q6_K super-blocks (down only)            */
+    DS4G_FMT_Q6K = 4,          /* 210-byte Q6_K super-blocks (down only)            */
+    DS4G_FMT_MXFP4 = 5         /* MXFP4: 17-byte blocks of 32 weights (gate/up, down),
+                                  counted in 136-byte units of 256 weights          */
 } ds4g_format;
 
 typedef enum ds4g_dtype {
@@ -129,7 +131,7 @@ enum {
  *   1 <= inter <= DS4G_MAX_INTER; 1 <= n_experts <= 256;
  *   1 <= top_k <= min(8, n_experts);
  *   row_bytes >= ceil(K/256) * block_bytes and a multiple of 4 (Q2_K,
- *   Q4_K, Q5_K) or 2 (codebook, Q6_K);
+ *   Q4_K, Q5_K, MXFP4) or 2 (codebook, Q6_K);
  *   expert strides >= rows * row_bytes and multiples of 16;
  *   w_gate, w_up, w_down 16-byte aligned;
  *   DS4G_FORCE_TC additionally needs row_bytes % 16 == 0.
@@ -146,11 +148,13 @@ enum {
  * both; the codebook is required when either is DS4G_FMT_CB2.  The routed
  * higher-bit formats of the same page ("Model Weights": gate/up in Q2_K,
  * Q4_K or Q5_K, down in Q2_K, Q4_K, Q5_K or Q6_K) are accepted with those
- * roles: format in {Q2K, CB2, Q4K, Q5K}, down_format in {Q2K, CB2, Q4K,
- * Q5K, Q6K} (else DS4G_ERR_INVALID).  Layers with a K-quant matrix run on
- * the general (GEMV) kernels; DS4G_FORCE_TC then returns
- * DS4G_ERR_UNSUPPORTED.  Row alignment: rows of Q2_K, Q4_K and Q5_K blocks
- * a multiple of 4 bytes, of codebook and Q6_K blocks a multiple of 2.
+ * roles: format in {Q2K, CB2, Q4K, Q5K, MXFP4}, down_format in {Q2K, CB2,
+ * Q4K, Q5K, Q6K, MXFP4} (else DS4G_ERR_INVALID).  MXFP4 is the ds4f-mxfp4
+ * routed-expert format of the same page.  Layers with a K-quant or MXFP4
+ * matrix run on the general (GEMV) kernels; DS4G_FORCE_TC then returns
+ * DS4G_ERR_UNSUPPORTED.  Row alignment: rows of Q2_K, Q4_K, Q5_K and MXFP4
+ * a multiple of 4 bytes, of codebook and Q6_K blocks a multiple of 2; rows
+ * count ceil(K/256) units of the format's bytes per 256 weights.
  * n_slots / expert_slot: where each expert's weights are.  n_slots == 0
  * (expert_slot NULL): expert e's matrices are slot e of the weight tensors.
  * n_slots > 0: the weight tensors hold n_slots expert slots (same row bytes
@@ -249,6 +253,23 @@ DS4G_API ds4g_status ds4g_q5k_dequant(const void *blocks, int64_t n_blocks, void
                              int32_t out_dtype, void *stream);
 DS4G_API ds4g_status ds4g_q6k_dequant(const void *blocks, int64_t n_blocks, void *out,
                              int32_t out_dtype, void *stream);
+
+/*
+ * ds4g_mxfp4_dequant -- passage: MXFP4 routed experts (ds4 README mirror,
+ * "Model Weights": the ds4f-mxfp4 download keeps DeepSeek's released MXFP4
+ * routed-expert weights), read as OCP microscaling FP4 in its GGUF block:
+ * 17 bytes per 32 weights, byte 0 an E8M0 scale e (2^(e-127); 255 is NaN),
+ * bytes 1..16 the E2M1 codes (weight i in the low nibble of byte 1 + i,
+ * weight i + 16 in its high nibble; bit 3 the sign, bits 0..2 the
+ * magnitude 0, 0.5, 1, 1.5, 2, 3, 4, 6); w = 2^(e-127) * value.
+ * n_blocks counts units of eight blocks (136 bytes, 256 weights); `blocks`
+ * has no alignment requirement, `out` is 16-byte aligned.  fp32 output is
+ * exactly the definition (a power of two times a 3-bit value: exact unless
+ * outside fp32's range); fp16 / bf16 output is it rounded to nearest even.
+ * Errors as ds4g_q2k_dequant.
+ */
+DS4G_API ds4g_status ds4g_mxfp4_dequant(const void *blocks, int64_t n_blocks, void *out,
+                               int32_t out_dtype, void *stream);
 
 /*
  * ds4g_cb2_dequant -- passage: the IQ2_XXS half of the IQ2_XXS / Q2_K expert

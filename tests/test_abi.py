@@ -89,8 +89,8 @@ def test_noalloc_scratch_covers_a_32_token_decode_of_the_7168_layer():
     (dict(top_k=9, n_experts=16), D.ERR_INVALID),
     (dict(top_k=3, n_experts=2), D.ERR_INVALID),
     (dict(score=2), D.ERR_INVALID),
-    (dict(format=5), D.ERR_INVALID),
-    (dict(down_format=5), D.ERR_INVALID),
+    (dict(format=6), D.ERR_INVALID),
+    (dict(down_format=6), D.ERR_INVALID),
     (dict(format=D.FMT_Q6K, gate_up_row_bytes=210, gate_up_expert_stride=128 * 224),
      D.ERR_INVALID),                                                       # Q6_K is down-only
     (dict(down_format=D.FMT_Q4K, down_row_bytes=146), D.ERR_LAYOUT),       # Q4_K rows % 4
@@ -162,12 +162,14 @@ def test_dequant_validation():
     assert L.ds4g_q2k_dequant(FAKE, 4, FAKE + 4, D.F16, None) == D.ERR_LAYOUT
     assert L.ds4g_cb2_dequant(FAKE, 4, None, FAKE, D.F32, None) == D.ERR_INVALID
     assert L.ds4g_cb2_dequant(FAKE + 1, 4, FAKE, FAKE, D.F32, None) == D.ERR_LAYOUT
-    for fn, balign in ((L.ds4g_q4k_dequant, 4), (L.ds4g_q5k_dequant, 4), (L.ds4g_q6k_dequant, 2)):
+    for fn, balign in ((L.ds4g_q4k_dequant, 4), (L.ds4g_q5k_dequant, 4), (L.ds4g_q6k_dequant, 2),
+                       (L.ds4g_mxfp4_dequant, 1)):
         assert fn(FAKE, 0, FAKE, D.F32, None) == D.OK
         assert fn(FAKE, -1, FAKE, D.F32, None) == D.ERR_INVALID
         assert fn(FAKE, 4, FAKE, 3, None) == D.ERR_INVALID
         assert fn(None, 4, FAKE, D.F32, None) == D.ERR_INVALID
-        assert fn(FAKE + balign // 2, 4, FAKE, D.F32, None) == D.ERR_LAYOUT
+        if balign > 1:
+            assert fn(FAKE + balign // 2, 4, FAKE, D.F32, None) == D.ERR_LAYOUT
         assert fn(FAKE, 4, FAKE + 8, D.BF16, None) == D.ERR_LAYOUT
 
 
@@ -187,7 +189,8 @@ def layer_desc(H, I, E, k, fmt=None, flags=0, align=1, down_fmt=None, tc_min_tok
     W_down in `down_fmt` (default: fmt)."""
     fmt = D.FMT_Q2K if fmt is None else fmt
     down_fmt = fmt if down_fmt is None else down_fmt
-    sizes = {D.FMT_Q2K: 84, D.FMT_CB2: 70, D.FMT_Q4K: 144, D.FMT_Q5K: 176, D.FMT_Q6K: 210}
+    sizes = {D.FMT_Q2K: 84, D.FMT_CB2: 70, D.FMT_Q4K: 144, D.FMT_Q5K: 176, D.FMT_Q6K: 210,
+             D.FMT_MXFP4: 136}
     bb, dbb = sizes[fmt], sizes[down_fmt]
     gr, dr = H // 256 * bb, -(-I // 256) * dbb
     gr, dr = -(-gr // align) * align, -(-dr // align) * align
@@ -244,6 +247,9 @@ def test_mixed_format_descriptor_is_accepted():
     ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_Q5K), 2 + 3),
     ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_Q2K, down_fmt=D.FMT_Q4K), 1 + 3),
     ((7168, 2048, 256, 8), 64, dict(fmt=D.FMT_Q4K, flags=D.FORCE_TC), 0),
+    # MXFP4 likewise
+    ((7168, 2048, 256, 8), 32, dict(fmt=D.FMT_MXFP4), 1 + 3),
+    ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_MXFP4, down_fmt=D.FMT_Q6K), 2 + 3),
 ])
 def test_path_choice_by_launch_count(shape, T, kw, launches):
     """The per-call path choice documented under ds4g_moe_forward ("Path"),

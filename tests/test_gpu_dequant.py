@@ -108,6 +108,7 @@ KQ = {  # format: (block bytes, fp16 field offsets, library entry, oracle method
     S.FMT_Q4K: (144, (0, 2), D.q4k_dequant, "q4k_dequant"),
     S.FMT_Q5K: (176, (0, 2), D.q5k_dequant, "q5k_dequant"),
     S.FMT_Q6K: (210, (208,), D.q6k_dequant, "q6k_dequant"),
+    S.FMT_MXFP4: (136, (), D.mxfp4_dequant, "mxfp4_dequant"),
 }
 
 
@@ -119,10 +120,13 @@ def _random_kquant(fmt, n, seed):
         h = rng.integers(0, 0x7C00, size=n).astype(np.uint16)
         h |= rng.integers(0, 2, size=n).astype(np.uint16) << 15
         blk[:, off:off + 2] = h.view(np.uint8).reshape(n, 2)
+    if fmt == S.FMT_MXFP4:                       # scale bytes below 255 (255 is NaN)
+        blk[:, 0::17] = rng.integers(0, 255, size=(n, 8), dtype=np.uint8)
     return blk
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_Q4K, S.FMT_Q5K, S.FMT_Q6K], ids=["q4k", "q5k", "q6k"])
+@pytest.mark.parametrize("fmt", [S.FMT_Q4K, S.FMT_Q5K, S.FMT_Q6K, S.FMT_MXFP4],
+                         ids=["q4k", "q5k", "q6k", "mxfp4"])
 @pytest.mark.parametrize("n", [1, 3, 37, 4096 + 5, 200_000])
 def test_kquant_dequant_bit_exact(orc, fmt, n):
     _, _, fn, ref_name = KQ[fmt]
@@ -134,7 +138,8 @@ def test_kquant_dequant_bit_exact(orc, fmt, n):
     assert np.array_equal(_run(fn, blk, n, D.BF16), S.f32_to_bf16(ref))
 
 
-@pytest.mark.parametrize("fmt", [S.FMT_Q4K, S.FMT_Q5K, S.FMT_Q6K], ids=["q4k", "q5k", "q6k"])
+@pytest.mark.parametrize("fmt", [S.FMT_Q4K, S.FMT_Q5K, S.FMT_Q6K, S.FMT_MXFP4],
+                         ids=["q4k", "q5k", "q6k", "mxfp4"])
 def test_kquant_dequant_generated_rows(orc, fmt):
     bb, _, fn, ref_name = KQ[fmt]
     W = S.make_experts(9, S.TENSOR_DOWN, 2, 64, 2048, fmt, 8 * bb)
@@ -156,8 +161,12 @@ class _GpuDecoders:
     def q6k_dequant(self, blk):
         return _run(D.q6k_dequant, blk, blk.size // 210, D.F32)
 
+    def mxfp4_dequant(self, blk):
+        return _run(D.mxfp4_dequant, blk, blk.size // 136, D.F32)
+
 
 @pytest.mark.parametrize("pin", [P.pin_q4k_worked, P.pin_q5k_worked, P.pin_q6k_worked,
-                                 P.pin_kquant_onehot], ids=lambda p: p.__name__)
+                                 P.pin_kquant_onehot, P.pin_mxfp4_worked],
+                         ids=lambda p: p.__name__)
 def test_kquant_worked_blocks(pin):
     pin(_GpuDecoders())

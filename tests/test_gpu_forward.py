@@ -23,7 +23,7 @@ from gpu_helpers import (boundary_tokens, cached_layer, check_output, check_rout
 pytestmark = pytest.mark.gpu
 
 SAMPLE = {"tiny": None, "decode_1tok": None, "decode_32tok": None, "prefill_2048": 64,
-          "codebook_512": 64, "mixed_2048": 64, "kquant_32tok": None}
+          "codebook_512": 64, "mixed_2048": 64, "kquant_32tok": None, "mxfp4_32tok": None}
 
 
 @pytest.mark.parametrize("name", list(S.CONFIGS))
@@ -58,6 +58,8 @@ def test_forward_workloads(orc, name):
     dict(H=512, I=200, E=4, k=2, T=3, fmt=S.FMT_Q2K, down_fmt=S.FMT_Q5K),
     dict(H=256, I=512, E=3, k=3, T=2, fmt=S.FMT_Q4K, score=S.SCORE_SIGMOID,
          logits_kind=S.LOGITS_UNIFORM),
+    dict(H=512, I=320, E=5, k=2, T=9, fmt=S.FMT_MXFP4),
+    dict(H=768, I=256, E=4, k=2, T=6, fmt=S.FMT_MXFP4, down_fmt=S.FMT_Q6K),
 ])
 def test_forward_edge_layers(orc, kw):
     layer = P.small_layer(seed=sum(kw.get(x, 0) for x in ("H", "I", "E", "T")), **kw)
