@@ -95,14 +95,14 @@ def default_steps(cfg: S.Config):
     # ~1-2 s of device time at the expected step times
     return {"tiny": 20000, "decode_1tok": 100000, "decode_32tok": 4000,
             "prefill_2048": 200, "codebook_512": 1000, "mixed_2048": 200,
-            "kquant_32tok": 1000, "mxfp4_32tok": 1000}[cfg.name]
+            "kquant_32tok": 1000, "mxfp4_32tok": 1000, "mxfp4_2048": 200}[cfg.name]
 
 
 def floor_steps(cfg: S.Config):
     # about 0.2 s of device time: the least a per-config line is timed over
     return {"tiny": 5000, "decode_1tok": 5000, "decode_32tok": 150,
             "prefill_2048": 60, "codebook_512": 80, "mixed_2048": 60,
-            "kquant_32tok": 100, "mxfp4_32tok": 100}[cfg.name]
+            "kquant_32tok": 100, "mxfp4_32tok": 100, "mxfp4_2048": 60}[cfg.name]
 
 
 # ---------------------------------------------------------------------------
@@ -216,12 +216,12 @@ def tensor_peaks():
 
 def layer_path(cfg: S.Config) -> str:
     """Which kernels the library runs for this workload (mirrors its choice:
-    the decode kernels up to 32 tokens for Q2_K, the tensor-core prefill
-    kernels (Q2_K and codebook) for rows of a multiple of 16 bytes otherwise,
+    the decode kernels up to 32 tokens for Q2_K, the tensor-core kernels
+    (Q2_K, codebook and MXFP4) for rows of a multiple of 16 bytes otherwise,
     the general kernels for the rest, among them every layer with a Q4_K /
     Q5_K / Q6_K matrix)."""
-    two_bit = (S.FMT_Q2K, S.FMT_CB2)
-    tc = (cfg.format in two_bit and cfg.dn_format in two_bit and
+    tc_fmts = (S.FMT_Q2K, S.FMT_CB2, S.FMT_MXFP4)
+    tc = (cfg.format in tc_fmts and cfg.dn_format in tc_fmts and
           cfg.row_bytes(cfg.hidden) % 16 == 0 and
           cfg.row_bytes(cfg.inter, fmt=cfg.dn_format) % 16 == 0)
     if (cfg.format == S.FMT_Q2K and cfg.dn_format == S.FMT_Q2K and cfg.inter % 16 == 0 and
@@ -288,9 +288,10 @@ def host_info():
 def roofline_for(cfg: S.Config, path: str, ph_ms, active, steps_b, T, k):
     """Roofline of the dominant kernel over the phased replay: its algorithmic
     bytes or flops per launch (averaged over the graph's steps) / its mean
-    duration.  Decode: the fused layer kernel against HBM.  Tensor-core path:
-    the gate/up kernel; prefill against the tensor peak, the codebook layer
-    (HBM-bound by its bytes) against HBM with its tensor fraction beside it."""
+    duration.  Decode: the fused layer kernel against HBM.  Tensor-core and
+    general paths: the gate/up kernel, against the tensor peak where its
+    flops take longer at that peak than its bytes at the HBM peak (the
+    2048-token layers), else against HBM with its tensor fraction beside it."""
     gu_b, dn_b = layer_bytes(cfg)
     H, I = cfg.hidden, cfg.inter
     x_b, y_b = T * H * 2, T * H * 4
@@ -311,7 +312,7 @@ def roofline_for(cfg: S.Config, path: str, ph_ms, active, steps_b, T, k):
     flops = 2.0 * T * k * 2 * H * I
     tflops = flops / (ph_ms[1] / 1000.0) / 1e12
     gbs = gate_up_bytes / (ph_ms[1] / 1000.0) / 1e9
-    if path == "tc" and cfg.format == S.FMT_Q2K and cfg.dn_format == S.FMT_Q2K:
+    if path == "tc" and flops / (sustained * 1e12) > gate_up_bytes / (hbm_peak * 1e9):
         return {"bound": "tensor", "kernel": "tc_kernel<0> (gate/up)", "achieved": tflops,
                 "peak": sustained, "peak_kind": f"{tkind} bf16 sustained (fp16 same rate)",
                 "unit": "TFLOP/s", "frac": tflops / sustained, "frac_of_burst": tflops / burst,

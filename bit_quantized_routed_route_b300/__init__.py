@@ -23,7 +23,8 @@ from typing import Optional
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIBRARY = os.path.join(HERE, "libds4g.so")
 
-OK, ERR_INVALID, ERR_SHAPE, ERR_LAYOUT, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT = range(8)
+(OK, ERR_INVALID, ERR_SHAPE, ERR_LAYOUT, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA, ERR_TIMEOUT,
+ ERR_RANGE) = range(9)
 SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
 FMT_Q2K, FMT_CB2, FMT_Q4K, FMT_Q5K, FMT_Q6K, FMT_MXFP4 = 0, 1, 2, 3, 4, 5
 F32, F16, BF16 = 0, 1, 2

@@ -326,9 +326,9 @@ ds4g_status kquant_dequant(int fmt, const void *blocks, int64_t n_blocks, void *
         return DS4G_ERR_INVALID;
     if (n_blocks == 0) return DS4G_OK;
     if (!blocks || !out) return DS4G_ERR_INVALID;
-    // every block of a 4-byte aligned Q4_K / Q5_K array is 4-byte aligned;
-    // Q6_K blocks (210 bytes) only 2-byte aligned; MXFP4 is read bytewise
-    const size_t balign = fmt == DS4G_FMT_Q6K ? 2 : fmt == DS4G_FMT_MXFP4 ? 1 : 4;
+    // every block of a 4-byte aligned Q4_K / Q5_K array is 4-byte aligned, and
+    // so is every 136-byte MXFP4 unit; Q6_K blocks (210 bytes) only 2-byte
+    const size_t balign = fmt == DS4G_FMT_Q6K ? 2 : 4;
     if (!aligned(blocks, balign) || !aligned(out, 16)) return DS4G_ERR_LAYOUT;
     return from_cuda(launch_kquant_dequant(fmt, static_cast<const uint8_t *>(blocks), n_blocks, out,
                                            out_dtype, static_cast<cudaStream_t>(stream)));
@@ -495,6 +495,7 @@ const char *ds4g_status_string(ds4g_status status)
     case DS4G_ERR_UNSUPPORTED: return "forced path not possible for these inputs";
     case DS4G_ERR_CUDA: return "CUDA error";
     case DS4G_ERR_TIMEOUT: return "device-side wait timed out";
+    case DS4G_ERR_RANGE: return "MXFP4 block scale outside the tensor-core kernels' exact fp16 range";
     }
     return "unknown status";
 }

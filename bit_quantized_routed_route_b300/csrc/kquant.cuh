@@ -83,15 +83,27 @@ template <int FMT>
 __device__ __forceinline__ void kquant_unit16(const uint8_t *__restrict__ blk, int u, float (&w)[16])
 {
     if constexpr (FMT == DS4G_FMT_MXFP4) {
-        const uint8_t *b = blk + 17 * (u >> 1);
-        const uint32_t e = __ldg(b);
+        // the unit (eight 17-byte blocks) is 4-byte aligned: block b's codes
+        // start at byte 17b + 1, (b + 1) & 3 bytes into an aligned word, and
+        // the aligned words that hold them end inside the unit
+        const int b = u >> 1;
+        const uint32_t e = __ldg(blk + 17 * b);
         // 2^(e-127): e = 0 is the subnormal 2^-127, e = 255 NaN
         const float scale = e == 0 ? __uint_as_float(0x00400000u)
                           : e == 255 ? __uint_as_float(0x7FC00000u)
                                      : __uint_as_float(e << 23);
+        const int mis = (b + 1) & 3;
+        const uint32_t *w4 = reinterpret_cast<const uint32_t *>(blk + ((17 * b + 1) & ~3));
+        uint32_t v[5];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = __ldg(w4 + i);
+        v[4] = mis ? __ldg(w4 + 4) : 0u;
+        uint32_t q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = __funnelshift_r(v[i], v[i + 1], 8 * mis);
         const int sh = 4 * (u & 1);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) w[i] = scale * e2m1_value((__ldg(b + 1 + i) >> sh) & 15);
+        for (int i = 0; i < 16; ++i) w[i] = scale * e2m1_value((byte_of(q, i) >> sh) & 15);
     } else if constexpr (FMT == DS4G_FMT_Q4K || FMT == DS4G_FMT_Q5K) {
         const int s = u >> 1;                       // 32-weight sub-block
         const int c = u >> 2;                       // 64-weight chunk

@@ -422,5 +422,20 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi)
     return r;
 }
 
+// The four bytes of w, each a pair of E2M1 (FP4) codes, as four fp16 pairs:
+// h[i] = (value of the low nibble of byte i, value of its high nibble), low
+// half first.  Every E2M1 value is exact in fp16.
+__device__ __forceinline__ void e2m1x8_to_half2(uint32_t w, uint32_t (&h)[4])
+{
+    asm("{\n.reg .b8 b0, b1, b2, b3;\n"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(w));
+}
+
 }  // namespace ptx
 }  // namespace ds4g

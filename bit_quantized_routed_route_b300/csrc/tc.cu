@@ -85,8 +85,11 @@ namespace {
 constexpr int kBM = 128;                  // weight rows per item (MMA M)
 constexpr int kNT = kTcTileTokens;        // tokens per item at most (MMA N)
 constexpr int kBoxRows = 16;              // token rows per activation TMA box
-constexpr int kWinWords = 28;             // 112-byte window per weight row
-constexpr int kAqBytes = kWinWords * 4 * kBM;
+// The window of one weight row per K step: the 16-byte aligned bytes that
+// hold its 256-weight unit (Q2_K 84 and codebook 70 bytes: 112; MXFP4 136
+// bytes: 144).  win_bytes: the windows of all kBM rows of an item.
+__host__ __device__ constexpr int win_words(int fmt) { return fmt == DS4G_FMT_MXFP4 ? 36 : 28; }
+__host__ __device__ constexpr int win_bytes(int fmt) { return 4 * win_words(fmt) * kBM; }
 constexpr int kChunkBytes = kNT * 128;    // one 64-wide K chunk of the activation tile
 constexpr int kHalfBytes = 2 * kChunkBytes;   // activation half stage: K = 128
 constexpr int kHalfMmas = 8;              // K = 16 MMAs per half block
@@ -115,7 +118,7 @@ struct Ring {
     static constexpr int NMAT = MODE == 0 ? 2 : 1;
     static constexpr int kW = MODE == 0 ? (FMT == DS4G_FMT_Q2K ? 3 : 2) : 4;
     static constexpr int kB = MODE == 1 && FMT == DS4G_FMT_Q2K ? 5 : 4;
-    static constexpr uint32_t kWStageBytes = NMAT * kAqBytes;
+    static constexpr uint32_t kWStageBytes = NMAT * win_bytes(FMT);
     static constexpr size_t kWOff = (size_t)kB * kHalfBytes;
     static constexpr size_t kCbOff = kWOff + (size_t)kW * kWStageBytes;
     static constexpr size_t kBytes = kCbOff + (FMT == DS4G_FMT_CB2 ? kCbRepBytes : 0);
@@ -146,6 +149,13 @@ struct TcArgs {
 __host__ __device__ __forceinline__ int perm32(int n)
 {
     return (n & ~31) | ((n & 15) << 1) | ((n >> 4) & 1);
+}
+
+// The formats whose dequantized pairs follow perm32 (Q2_K, MXFP4); the
+// codebook keeps the natural order.
+__host__ __device__ constexpr bool perm32_format(int fmt)
+{
+    return fmt == DS4G_FMT_Q2K || fmt == DS4G_FMT_MXFP4;
 }
 
 __device__ __forceinline__ void set_status(int32_t *status, int code)
@@ -351,11 +361,71 @@ __device__ __forceinline__ void cb2_window_quarter(const uint8_t *win, int boff,
     cb2_quarter(iw, gw, tw, (uint32_t)(boff & 3) * 8, hh, gh, cb_lane, out);
 }
 
+// ---------------------------------------------------------------------------
+// MXFP4 units (eight 17-byte blocks of 32 weights: an E8M0 scale byte e, then
+// 16 bytes of E2M1 codes, weight i in the low nibble of byte 1 + i and weight
+// i + 16 in the high one; w = 2^(e-127) * value).  One quarter of a fill:
+// blocks b0 = 4hh + 2gh and b0 + 1, weights 64gh .. +63 of half hh.  A code
+// byte is the weight pair (i, i + 16) of its block, stored at K positions
+// 2i, 2i + 1 of the block's 32: the perm32 order of the Q2_K operands, which
+// the activations and h follow.  cvt.rn.f16x2.e2m1x2 gives both values
+// exactly in fp16; the multiply by the block scale, an fp16 power of two, is
+// exact while e - 127 lies in [-23, 13] (every product then stays between
+// 2^-24 and 49152).  `boff`: the unit's byte offset in its 16-byte aligned
+// window (0 or 8).  Returns false when a scale outside that range (other than
+// e = 255, NaN, which propagates as the definition says) made a weight inexact.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t mx_scale2(uint32_t e, bool &exact)
+{
+    const int s = (int)e - 127;
+    const uint32_t bits = e == 255 ? 0x7E00u
+                        : s > 15   ? 0x7C00u
+                        : s >= -14 ? (uint32_t)(s + 15) << 10
+                        : s >= -24 ? 1u << (s + 24)
+                                   : 0u;
+    exact = exact && (e == 255 || (s >= -23 && s <= 13));
+    return bits | (bits << 16);
+}
+
+__device__ __forceinline__ bool mx_window_quarter(const uint8_t *win, int boff, int hh, int gh,
+                                                  uint32_t (&out)[32])
+{
+    // scale byte of block b0: an even offset (17 * b0 and boff are even), so
+    // the 34 bytes of the two blocks lie in nine aligned words, the last of
+    // them inside the 144-byte window
+    const int a0 = boff + 17 * (4 * hh + 2 * gh);
+    const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win) + (a0 >> 2);
+    const uint32_t sh = (uint32_t)(a0 & 3) * 8;             // 0 or 16
+    uint32_t W[9];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) W[i] = w32[i];
+    bool exact = true;
+    const uint32_t s2[2] = {mx_scale2((W[0] >> sh) & 0xFFu, exact),
+                            mx_scale2((W[4] >> (sh + 8)) & 0xFFu, exact)};
+#pragma unroll
+    for (int bi = 0; bi < 2; ++bi) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            // code bytes 4j .. 4j+3 of block b0 + bi (stream bytes 1 + 4j and 18 + 4j)
+            const uint32_t cw = bi == 0 ? __funnelshift_r(W[j], W[j + 1], sh + 8)
+                                        : __funnelshift_rc(W[4 + j], W[5 + j], sh + 16);
+            uint32_t h[4];
+            ptx::e2m1x8_to_half2(cw, h);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) out[16 * bi + 4 * j + u] = ptx::hmul2_u(h[u], s2[bi]);
+        }
+    }
+    return exact;
+}
+
+// One quarter's 32 fp16 pairs of any tensor-core format; false when an MXFP4
+// block scale made a weight inexact in fp16.
 template <int FMT>
-__device__ __forceinline__ void quarter_values(const uint8_t *win, int kb, int hh,
+__device__ __forceinline__ bool quarter_values(const uint8_t *win, int kb, int hh,
                                                const QuarterConst &k, uint32_t cb_lane,
                                                uint32_t (&out)[32])
 {
+    if (FMT == DS4G_FMT_MXFP4) return mx_window_quarter(win, (kMXFP4Bytes * kb) & 15, hh, k.gh, out);
     if (FMT == DS4G_FMT_Q2K) {
         switch (kb & 3) {           // (84 * kb) mod 16, in words
         case 0: q2k_window_quarter<0>(win, hh, k, out); break;
@@ -366,6 +436,7 @@ __device__ __forceinline__ void quarter_values(const uint8_t *win, int kb, int h
     } else {
         cb2_window_quarter(win, (kCB2Bytes * kb) & 15, hh, k.gh, cb_lane, out);
     }
+    return true;
 }
 
 // The dequantizing role of one warp (both kernels of tc_kernel).  Two teams
@@ -409,10 +480,11 @@ struct DequantRole {
             if (!ok) return;
             ptx::tc_fence_after();
         }
-        const uint8_t *win = c.wring + (size_t)ws * R::kWStageBytes + mat * kAqBytes +
-                             row * (kWinWords * 4);
+        const uint8_t *win = c.wring + (size_t)ws * R::kWStageBytes + mat * win_bytes(FMT) +
+                             row * (4 * win_words(FMT));
         uint32_t out[32];
-        quarter_values<FMT>(win, kb, hh, k, c.cbrep + (uint32_t)(lane & 15) * 8, out);
+        if (!quarter_values<FMT>(win, kb, hh, k, c.cbrep + (uint32_t)(lane & 15) * 8, out))
+            set_status(a.status, DS4G_ERR_RANGE);
         ptx::tmem_st32(c.tmem + lane_base + (uint32_t)buf * 64u + 32u * k.gh, out);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
@@ -500,7 +572,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
 {
     using R = Ring<MODE, FMT>;
     constexpr int NMAT = R::NMAT;
-    constexpr int kBlockBytes = FMT == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+    constexpr int kBlockBytes = block_bytes_of(FMT);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -598,7 +670,7 @@ __global__ void __launch_bounds__(tc_threads(MODE), 1)
                     ptx::mbar_arrive_expect_tx(&wfull[s], R::kWStageBytes);
                     const int x = ((kBlockBytes * kb) & ~15) / 4;
                     ptx::tma_load_3d(st, &tm_a0, x, mt * kBM, e, &wfull[s]);
-                    if (NMAT == 2) ptx::tma_load_3d(st + kAqBytes, &tm_a1, x, mt * kBM, e, &wfull[s]);
+                    if (NMAT == 2) ptx::tma_load_3d(st + win_bytes(FMT), &tm_a1, x, mt * kBM, e, &wfull[s]);
                     prefetch_next();
                 }
             }
@@ -792,7 +864,7 @@ template <int FMT>
 struct DownRing {
     static constexpr int kW = FMT == DS4G_FMT_Q2K ? 3 : 2;     // window stages per team
     static constexpr int kB = 2;                               // activation half stages per team
-    static constexpr size_t kTeamBytes = (size_t)kW * kAqBytes + (size_t)kB * kHalfBytes;
+    static constexpr size_t kTeamBytes = (size_t)kW * win_bytes(FMT) + (size_t)kB * kHalfBytes;
     // per team: [B half stages][window stages]; the codebook copy last
     static constexpr size_t kBOff(int t) { return (size_t)t * kTeamBytes; }
     static constexpr size_t kWOff(int t) { return (size_t)t * kTeamBytes + (size_t)kB * kHalfBytes; }
@@ -810,7 +882,7 @@ __global__ void __launch_bounds__(kDownThreads, 1)
                    const TcArgs a)
 {
     using R = DownRing<FMT>;
-    constexpr int kBlockBytes = FMT == DS4G_FMT_Q2K ? kQ2KBytes : kCB2Bytes;
+    constexpr int kBlockBytes = block_bytes_of(FMT);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -891,8 +963,8 @@ __global__ void __launch_bounds__(kDownThreads, 1)
                 const int it = item_of(t, w / KB), kb = w % KB;
                 const int tile = it / a.m_tiles, mt = it % a.m_tiles;
                 const int e = weight_slot(a.wslot, a.n_wslots, a.tiles[4 * tile], a.status);
-                ptx::mbar_arrive_expect_tx(&wfull[t][s], (uint32_t)kAqBytes);
-                ptx::tma_load_3d(wring + (size_t)s * kAqBytes, &tm_w, ((kBlockBytes * kb) & ~15) / 4,
+                ptx::mbar_arrive_expect_tx(&wfull[t][s], (uint32_t)win_bytes(FMT));
+                ptx::tma_load_3d(wring + (size_t)s * win_bytes(FMT), &tm_w, ((kBlockBytes * kb) & ~15) / 4,
                                  mt * kBM, e, &wfull[t][s]);
                 const int pw = w + kPrefetchSteps;
                 if (pw < nk) {
@@ -1037,7 +1109,7 @@ __global__ void __launch_bounds__(kDownThreads, 1)
                 ok = wait_bar(&wfull[t][ws], (kc / R::kW) & 1, a.wait_ns, abort_flag);
                 ok = __all_sync(0xffffffffu, ok);
                 if (!ok) break;
-                const uint8_t *win = wring + (size_t)ws * kAqBytes + row * (kWinWords * 4);
+                const uint8_t *win = wring + (size_t)ws * win_bytes(FMT) + row * (4 * win_words(FMT));
                 for (int hh = 0; ok && hh < 2; ++hh, ++tf) {
                     const int buf = 2 * t + (tf & 1);
                     if (tf >= 2) {
@@ -1047,7 +1119,8 @@ __global__ void __launch_bounds__(kDownThreads, 1)
                         ptx::tc_fence_after();
                     }
                     uint32_t out[32];
-                    quarter_values<FMT>(win, kb, hh, k, cb_lane, out);
+                    if (!quarter_values<FMT>(win, kb, hh, k, cb_lane, out))
+                        set_status(a.status, DS4G_ERR_RANGE);
                     ptx::tmem_st32(tmem + lane_base + (uint32_t)buf * 64u + 32u * gh, out);
                     ptx::tmem_st_wait();
                     ptx::tc_fence_before();
@@ -1268,9 +1341,9 @@ cudaError_t get_encode(PFN_cuTensorMapEncodeTiled_v12000 *out)
 }
 
 // 3-D map over [experts][rows][row words] of one quantized weight tensor:
-// box = 28 words (112 bytes) x 128 rows x 1 expert, no swizzle, zero fill.
+// box = box_words x 128 rows x 1 expert, no swizzle, zero fill.
 cudaError_t weight_map(CUtensorMap *m, const void *base, int64_t row_bytes, int64_t rows,
-                       int64_t expert_stride, int64_t experts, int phases)
+                       int64_t expert_stride, int64_t experts, int phases, int box_words)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     cudaError_t e = get_encode(&enc);
@@ -1280,7 +1353,7 @@ cudaError_t weight_map(CUtensorMap *m, const void *base, int64_t row_bytes, int6
     cuuint64_t dims[3] = {(cuuint64_t)(phases * row_bytes / 4), (cuuint64_t)(rows / phases),
                           (cuuint64_t)experts};
     cuuint64_t strides[2] = {(cuuint64_t)(phases * row_bytes), (cuuint64_t)expert_stride};
-    cuuint32_t box[3] = {(cuuint32_t)kWinWords, (cuuint32_t)(kBM / phases), 1};
+    cuuint32_t box[3] = {(cuuint32_t)box_words, (cuuint32_t)(kBM / phases), 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void *>(base), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -1290,7 +1363,9 @@ cudaError_t weight_map(CUtensorMap *m, const void *base, int64_t row_bytes, int6
 
 bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d)
 {
-    const auto fmt_ok = [](int f) { return f == DS4G_FMT_Q2K || f == DS4G_FMT_CB2; };
+    const auto fmt_ok = [](int f) {
+        return f == DS4G_FMT_Q2K || f == DS4G_FMT_CB2 || f == DS4G_FMT_MXFP4;
+    };
     return p.A > 0 && fmt_ok(d->format) && fmt_ok(d->down_format) &&
            d->gate_up_row_bytes % 16 == 0 && d->down_row_bytes % 16 == 0 && p.H % kBM == 0;
 }
@@ -1311,7 +1386,7 @@ cudaError_t launch_tc_prep(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     const int prep_grid = dev.sm_count * 4;
     tc_prep_kernel<<<prep_grid, 256, 0, s>>>(la.x, la.H, la.k, la.A, la.perm, la.counts,
                                              la.offsets, la.E, tb.xseg, tb.tiles, tb.n_tiles,
-                                             la.gu_format == DS4G_FMT_Q2K ? 1 : 0, la.wts, tb.wseg,
+                                             perm32_format(la.gu_format) ? 1 : 0, la.wts, tb.wseg,
                                              tb.texp, tb.eseg, tb.min_tokens, tb.light, tb.n_light);
     return cudaGetLastError();
 }
@@ -1323,9 +1398,10 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     CUtensorMap m_gate, m_up, m_down, m_x, m_h;
     cudaError_t e;
     const int nw = la.n_wslots;             // experts (or slots) the weight tensors hold
-    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, nw, 1)) != cudaSuccess ||
-        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, nw, 1)) != cudaSuccess ||
-        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, nw, 1)) != cudaSuccess ||
+    const int gw = win_words(la.gu_format), dw = win_words(la.dn_format);
+    if ((e = weight_map(&m_gate, la.w_gate, la.gu_row, la.I, la.gu_stride, nw, 1, gw)) != cudaSuccess ||
+        (e = weight_map(&m_up, la.w_up, la.gu_row, la.I, la.gu_stride, nw, 1, gw)) != cudaSuccess ||
+        (e = weight_map(&m_down, la.w_down, la.dn_row, la.H, la.dn_stride, nw, 1, dw)) != cudaSuccess ||
         (e = act_map(&m_x, tb.xseg, la.H, la.A)) != cudaSuccess ||
         (e = act_map(&m_h, tb.hp, la.I_pad, la.A)) != cudaSuccess)
         return e;
@@ -1348,24 +1424,26 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     a.K = la.H;
     a.m_tiles = la.I_pad / kBM;
     a.codebook = la.codebook;
-    a.h_perm32 = la.dn_format == DS4G_FMT_Q2K ? 1 : 0;
+    a.h_perm32 = perm32_format(la.dn_format) ? 1 : 0;
     // per-segment split: the light segments' experts on the GEMV kernels
     LayerArgs lg = la;
     lg.active = tb.light;
     lg.n_active = tb.n_light;
     const bool split = tb.min_tokens > 0;
-    if ((e = la.gu_format == DS4G_FMT_CB2
-                 ? launch_tc<0, DS4G_FMT_CB2>(m_gate, m_up, m_x, a, dev.sm_count, s)
-                 : launch_tc<0, DS4G_FMT_Q2K>(m_gate, m_up, m_x, a, dev.sm_count, s)) != cudaSuccess)
+    if ((e = la.gu_format == DS4G_FMT_CB2     ? launch_tc<0, DS4G_FMT_CB2>(m_gate, m_up, m_x, a, dev.sm_count, s)
+             : la.gu_format == DS4G_FMT_MXFP4 ? launch_tc<0, DS4G_FMT_MXFP4>(m_gate, m_up, m_x, a, dev.sm_count, s)
+                                              : launch_tc<0, DS4G_FMT_Q2K>(m_gate, m_up, m_x, a, dev.sm_count, s)) !=
+        cudaSuccess)
         return e;
     if (split && (e = launch_gemv_gateup(lg, dev, s)) != cudaSuccess) return e;
     if (ev && (e = record_phase(ev[2], s)) != cudaSuccess) return e;
 
     a.K = la.I_pad;
     a.m_tiles = la.H / kBM;
-    if ((e = la.dn_format == DS4G_FMT_CB2
-                 ? launch_tc_down<DS4G_FMT_CB2>(m_down, m_h, a, dev.sm_count, s)
-                 : launch_tc<1, DS4G_FMT_Q2K>(m_down, m_down, m_h, a, dev.sm_count, s)) != cudaSuccess)
+    if ((e = la.dn_format == DS4G_FMT_CB2     ? launch_tc_down<DS4G_FMT_CB2>(m_down, m_h, a, dev.sm_count, s)
+             : la.dn_format == DS4G_FMT_MXFP4 ? launch_tc<1, DS4G_FMT_MXFP4>(m_down, m_down, m_h, a, dev.sm_count, s)
+                                              : launch_tc<1, DS4G_FMT_Q2K>(m_down, m_down, m_h, a, dev.sm_count, s)) !=
+        cudaSuccess)
         return e;
     if (split && (e = launch_gemv_down(lg, dev, s)) != cudaSuccess) return e;
     if (ev && (e = record_phase(ev[3], s)) != cudaSuccess) return e;

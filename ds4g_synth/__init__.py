@@ -20,6 +20,7 @@ codebook_512   7168   2048  256  8   512   codebook  sigmoid  4
 mixed_2048     7168   2048  256  8   2048  mixed     sigmoid  5
 kquant_32tok   7168   2048  256  8   32    Q4_K/Q6K  sigmoid  6
 mxfp4_32tok    7168   2048  256  8   32    MXFP4     sigmoid  7
+mxfp4_2048     7168   2048  256  8   2048  MXFP4     sigmoid  8
 =============  =====  ====  ===  ==  ====  ========  =======  ====
 
 mixed_2048 is the shipping mix of the ds4 weights (codebook-2-bit gate/up,
@@ -27,7 +28,8 @@ Q2_K down) on the prefill layer with the prefill routing recipe.
 kquant_32tok is a higher-bit routed layer (Q4_K gate/up, Q6_K down; the
 ds4f-q2-q4 / ds4f-q4 downloads and the routed K-quant formats the ds4
 README names) at the 32-token decode batch; mxfp4_32tok the same layer with
-MXFP4 routed experts (the ds4f-mxfp4 download).
+MXFP4 routed experts (the ds4f-mxfp4 download), and mxfp4_2048 those experts
+on the prefill layer with the prefill routing recipe.
 
 Rows are stored packed (ceil(K/256) blocks back to back) for Q2_K; the
 codebook rows (70-byte blocks) are padded to a multiple of 16 bytes so that
@@ -111,6 +113,7 @@ CONFIGS: Dict[str, Config] = {
         Config("kquant_32tok", 7168, 2048, 256, 8, 32, FMT_Q4K, SCORE_SIGMOID, LOGITS_UNIFORM, 6,
                down_format=FMT_Q6K),
         Config("mxfp4_32tok", 7168, 2048, 256, 8, 32, FMT_MXFP4, SCORE_SIGMOID, LOGITS_UNIFORM, 7),
+        Config("mxfp4_2048", 7168, 2048, 256, 8, 2048, FMT_MXFP4, SCORE_SIGMOID, LOGITS_BIASED, 8),
     ]
 }
 

@@ -77,7 +77,10 @@ typedef enum ds4g_status {
     DS4G_ERR_WORKSPACE = 4,    /* workspace pointer misaligned or too small        */
     DS4G_ERR_UNSUPPORTED = 5,  /* a forced path that cannot run on these inputs    */
     DS4G_ERR_CUDA = 6,         /* a CUDA runtime call or kernel launch failed      */
-    DS4G_ERR_TIMEOUT = 7       /* a bounded device-side wait expired (device status) */
+    DS4G_ERR_TIMEOUT = 7,      /* a bounded device-side wait expired (device status) */
+    DS4G_ERR_RANGE = 8         /* device status: an MXFP4 block scale outside
+                                  2^-23 .. 2^13 met on the tensor-core kernels,
+                                  whose fp16 operands then rounded weights     */
 } ds4g_status;
 
 typedef enum ds4g_score {
@@ -150,9 +153,15 @@ enum {
  * Q4_K or Q5_K, down in Q2_K, Q4_K, Q5_K or Q6_K) are accepted with those
  * roles: format in {Q2K, CB2, Q4K, Q5K, MXFP4}, down_format in {Q2K, CB2,
  * Q4K, Q5K, Q6K, MXFP4} (else DS4G_ERR_INVALID).  MXFP4 is the ds4f-mxfp4
- * routed-expert format of the same page.  Layers with a K-quant or MXFP4
- * matrix run on the general (GEMV) kernels; DS4G_FORCE_TC then returns
- * DS4G_ERR_UNSUPPORTED.  Row alignment: rows of Q2_K, Q4_K, Q5_K and MXFP4
+ * routed-expert format of the same page.  Layers with a K-quant matrix run
+ * on the general (GEMV) kernels; DS4G_FORCE_TC then returns
+ * DS4G_ERR_UNSUPPORTED.  MXFP4 matrices also run on the tensor-core kernels,
+ * with weights converted exactly to fp16 operands while every block scale
+ * 2^(e-127) of the call's experts lies in 2^-23 .. 2^13 (any trained weight:
+ * |w| from 2^-24 to 49152); a scale outside it (bar e = 255, NaN) rounds
+ * those weights and sets the workspace status word to DS4G_ERR_RANGE (the
+ * GEMV kernels, DS4G_FORCE_GEMV, compute such layers in fp32).  Row
+ * alignment: rows of Q2_K, Q4_K, Q5_K and MXFP4
  * a multiple of 4 bytes, of codebook and Q6_K blocks a multiple of 2; rows
  * count ceil(K/256) units of the format's bytes per 256 weights.
  * n_slots / expert_slot: where each expert's weights are.  n_slots == 0
@@ -263,7 +272,7 @@ DS4G_API ds4g_status ds4g_q6k_dequant(const void *blocks, int64_t n_blocks, void
  * weight i + 16 in its high nibble; bit 3 the sign, bits 0..2 the
  * magnitude 0, 0.5, 1, 1.5, 2, 3, 4, 6); w = 2^(e-127) * value.
  * n_blocks counts units of eight blocks (136 bytes, 256 weights); `blocks`
- * has no alignment requirement, `out` is 16-byte aligned.  fp32 output is
+ * is 4-byte aligned, `out` 16-byte aligned.  fp32 output is
  * exactly the definition (a power of two times a 3-bit value: exact unless
  * outside fp32's range); fp16 / bf16 output is it rounded to nearest even.
  * Errors as ds4g_q2k_dequant.
@@ -305,9 +314,9 @@ DS4G_API size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
  *           ds4g_moe_routing_view).
  * Path (one per call): Q2_K layers with inter % 16 == 0 and T <= 32 run
  * the decode kernels (mma.sync up to 8 vectors, tcgen05 from 9 to 32, the
- * latter with hidden % 128 == 0); otherwise layers whose row_bytes are
- * multiples of 16 and hidden % 128 == 0 run the tensor-core kernels; all
- * others run the GEMV kernels.  DS4G_FORCE_TC forces the tensor-core kernels
+ * latter with hidden % 128 == 0); otherwise layers of Q2_K, codebook and
+ * MXFP4 matrices whose row_bytes are multiples of 16 and hidden % 128 == 0
+ * run the tensor-core kernels; all others run the GEMV kernels.  DS4G_FORCE_TC forces the tensor-core kernels
  * and DS4G_FORCE_GEMV rules them out.
  * Errors: DS4G_ERR_INVALID, DS4G_ERR_SHAPE, DS4G_ERR_LAYOUT,
  * DS4G_ERR_WORKSPACE, DS4G_ERR_UNSUPPORTED (a forced path that cannot run),

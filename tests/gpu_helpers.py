@@ -42,9 +42,10 @@ def to_device(layer: dict, flags: int = 0, tc_min_tokens: int = 0) -> D.Layer:
                    down_fmt=layer.get("down_format"))
 
 
-def run_forward(L: D.Layer, x: np.ndarray, logits: np.ndarray):
+def run_forward(L: D.Layer, x: np.ndarray, logits: np.ndarray, with_status: bool = False):
     """Runs ds4g_moe_forward; returns (y fp32 numpy, routing dict of numpy
-    arrays read back through ds4g_moe_routing_view)."""
+    arrays read back through ds4g_moe_routing_view), and with `with_status`
+    the workspace status word (ds4g_moe_device_status) third."""
     dev = torch.device("cuda")
     T = x.shape[0]
     xd = torch.from_numpy(np.ascontiguousarray(x).view(np.int16)).to(dev)
@@ -73,6 +74,10 @@ def run_forward(L: D.Layer, x: np.ndarray, logits: np.ndarray):
                    counts=grab(v["counts"], E, torch.int32),
                    offsets=grab(v["offsets"], E + 1, torch.int32),
                    perm=grab(v["perm"], A, torch.int32))
+    if with_status:
+        st, dev_status = D.moe_device_status(L.desc, T, ws, ws_bytes)
+        D.check(st)
+        return y.cpu().numpy(), routing, dev_status
     return y.cpu().numpy(), routing
 
 

@@ -32,7 +32,7 @@ def test_library_exports_every_declared_symbol():
 def test_abi_version_and_status_strings():
     assert D.abi_version() == 3
     assert D.status_string(D.OK) == "ok"
-    for s in range(1, 8):
+    for s in range(1, 9):
         assert D.status_string(s) not in ("ok", "unknown status")
     assert D.status_string(99) == "unknown status"
 
@@ -163,13 +163,12 @@ def test_dequant_validation():
     assert L.ds4g_cb2_dequant(FAKE, 4, None, FAKE, D.F32, None) == D.ERR_INVALID
     assert L.ds4g_cb2_dequant(FAKE + 1, 4, FAKE, FAKE, D.F32, None) == D.ERR_LAYOUT
     for fn, balign in ((L.ds4g_q4k_dequant, 4), (L.ds4g_q5k_dequant, 4), (L.ds4g_q6k_dequant, 2),
-                       (L.ds4g_mxfp4_dequant, 1)):
+                       (L.ds4g_mxfp4_dequant, 4)):
         assert fn(FAKE, 0, FAKE, D.F32, None) == D.OK
         assert fn(FAKE, -1, FAKE, D.F32, None) == D.ERR_INVALID
         assert fn(FAKE, 4, FAKE, 3, None) == D.ERR_INVALID
         assert fn(None, 4, FAKE, D.F32, None) == D.ERR_INVALID
-        if balign > 1:
-            assert fn(FAKE + balign // 2, 4, FAKE, D.F32, None) == D.ERR_LAYOUT
+        assert fn(FAKE + balign // 2, 4, FAKE, D.F32, None) == D.ERR_LAYOUT
         assert fn(FAKE, 4, FAKE + 8, D.BF16, None) == D.ERR_LAYOUT
 
 
@@ -247,9 +246,14 @@ def test_mixed_format_descriptor_is_accepted():
     ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_Q5K), 2 + 3),
     ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_Q2K, down_fmt=D.FMT_Q4K), 1 + 3),
     ((7168, 2048, 256, 8), 64, dict(fmt=D.FMT_Q4K, flags=D.FORCE_TC), 0),
-    # MXFP4 likewise
-    ((7168, 2048, 256, 8), 32, dict(fmt=D.FMT_MXFP4), 1 + 3),
+    # MXFP4 takes the tensor-core kernels at every T (16-byte rows: an even
+    # number of 136-byte units), alone or with the 2-bit formats; with a
+    # K-quant matrix, or 408-byte rows, the GEMV kernels
+    ((7168, 2048, 256, 8), 32, dict(fmt=D.FMT_MXFP4), 1 + 5),
+    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_MXFP4, down_fmt=D.FMT_Q2K), 1 + 5),
     ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_MXFP4, down_fmt=D.FMT_Q6K), 2 + 3),
+    ((768, 512, 8, 2), 100, dict(fmt=D.FMT_MXFP4), 2 + 3),
+    ((768, 512, 8, 2), 100, dict(fmt=D.FMT_MXFP4, flags=D.FORCE_TC), 0),
 ])
 def test_path_choice_by_launch_count(shape, T, kw, launches):
     """The per-call path choice documented under ds4g_moe_forward ("Path"),

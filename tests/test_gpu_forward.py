@@ -4,8 +4,9 @@ max-abs <= 5e-3 * max|ref| on the output.
 
 Full-size workloads run at their full token counts (the launch configuration
 the benchmark times).  The oracle checks every token of the decode-sized
-workloads (up to 32 tokens, the K-quant layer among them); for prefill_2048,
-codebook_512 and mixed_2048 it checks at least 64 tokens
+workloads (up to 32 tokens, the K-quant and MXFP4 layers among them); for
+prefill_2048, codebook_512, mixed_2048 and mxfp4_2048 it checks at least 64
+tokens
 chosen to reach every code path (first and last token of the heaviest
 segments, both sides of each 128-token tile boundary in them, tokens routed
 to one-token segments, then seeded random ones).  Its result for a token does
@@ -23,7 +24,8 @@ from gpu_helpers import (boundary_tokens, cached_layer, check_output, check_rout
 pytestmark = pytest.mark.gpu
 
 SAMPLE = {"tiny": None, "decode_1tok": None, "decode_32tok": None, "prefill_2048": 64,
-          "codebook_512": 64, "mixed_2048": 64, "kquant_32tok": None, "mxfp4_32tok": None}
+          "codebook_512": 64, "mixed_2048": 64, "kquant_32tok": None, "mxfp4_32tok": None,
+          "mxfp4_2048": 64}
 
 
 @pytest.mark.parametrize("name", list(S.CONFIGS))

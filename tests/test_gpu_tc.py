@@ -110,6 +110,50 @@ def test_mixed_format_layers(orc, kw):
     check_output(y, yref)
 
 
+@pytest.mark.parametrize("kw", [
+    dict(H=512, I=512, E=8, k=2, T=12),                       # units at window offsets 0 and 8
+    dict(H=1024, I=320, E=6, k=3, T=150),                     # ragged inter; segments over 128 tokens
+    dict(H=2048, I=1024, E=33, k=5, T=70),                    # E not a multiple of 32
+    dict(H=1024, I=512, E=1, k=1, T=300),                     # one expert, three token tiles
+    dict(H=1024, I=512, E=5, k=2, T=40, down_fmt=S.FMT_Q2K),  # MXFP4 gate/up, Q2_K down
+    dict(H=1024, I=512, E=5, k=2, T=40, down_fmt=S.FMT_CB2, align=16),   # h in natural order
+    dict(H=1024, I=512, E=5, k=2, T=40, fmt=S.FMT_CB2, down_fmt=S.FMT_MXFP4, align=16),
+], ids=["offsets", "ragged_I", "E33", "one_expert", "mx_q2k", "mx_cb2", "cb2_mx"])
+def test_tc_forward_mxfp4_layers(orc, kw):
+    """MXFP4 matrices on the tensor-core kernels: each code byte becomes an
+    fp16 pair of E2M1 values, times the block's power-of-two scale (exact for
+    these weights, so the status word stays clear), alone or mixed with the
+    2-bit formats in one layer."""
+    kw = dict(dict(fmt=S.FMT_MXFP4), **kw)
+    layer = P.small_layer(seed=5000 + kw["H"] + kw["T"], score=S.SCORE_SIGMOID, **kw)
+    L = to_device(layer, flags=D.FORCE_TC)
+    y, routing, st = run_forward(L, layer["x"], layer["logits"], with_status=True)
+    assert st == D.OK
+    check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    check_output(y, yref)
+
+
+def test_tc_mxfp4_scale_outside_fp16_range_is_reported(orc):
+    """A block scale of 2^-30 (exact in the fp32 definition; its weights fall
+    below fp16's smallest subnormal): the tensor-core kernels round those
+    weights and the status word reads DS4G_ERR_RANGE, while the GEMV kernels
+    compute the layer in fp32 with the status word clear.  Both stay within
+    the tolerance here, the rounded weights being that small."""
+    layer = P.small_layer(seed=77, H=512, I=512, E=4, k=2, T=16, fmt=S.FMT_MXFP4,
+                          score=S.SCORE_SIGMOID)
+    layer["w_up"][:, 0, 17] = 97          # scale byte of block 1, row 0, every expert
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    L = to_device(layer)
+    y_tc, _, st_tc = run_forward(L, layer["x"], layer["logits"], with_status=True)
+    assert st_tc == D.ERR_RANGE
+    check_output(y_tc, yref)
+    y_gv, _, st_gv = run_forward(L.with_flags(D.FORCE_GEMV), layer["x"], layer["logits"],
+                                 with_status=True)
+    assert st_gv == D.OK
+    check_output(y_gv, yref)
+
+
 @pytest.mark.parametrize("theta,fmt", [(8, S.FMT_Q2K), (8, S.FMT_CB2), (1000, S.FMT_Q2K),
                                         (1, S.FMT_CB2)],
                          ids=["q2k_theta8", "cb2_theta8", "all_light", "all_heavy"])
