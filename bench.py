@@ -217,12 +217,9 @@ def tensor_peaks():
 def layer_path(cfg: S.Config) -> str:
     """Which kernels the library runs for this workload (mirrors its choice:
     the decode kernels up to 32 tokens for Q2_K, the tensor-core kernels
-    (Q2_K, codebook and MXFP4) for rows of a multiple of 16 bytes otherwise,
-    the general kernels for the rest, among them every layer with a Q4_K /
-    Q5_K / Q6_K matrix)."""
-    tc_fmts = (S.FMT_Q2K, S.FMT_CB2, S.FMT_MXFP4)
-    tc = (cfg.format in tc_fmts and cfg.dn_format in tc_fmts and
-          cfg.row_bytes(cfg.hidden) % 16 == 0 and
+    (every format) for rows of a multiple of 16 bytes otherwise, the general
+    kernels for the rest)."""
+    tc = (cfg.row_bytes(cfg.hidden) % 16 == 0 and
           cfg.row_bytes(cfg.inter, fmt=cfg.dn_format) % 16 == 0)
     if (cfg.format == S.FMT_Q2K and cfg.dn_format == S.FMT_Q2K and cfg.inter % 16 == 0 and
             cfg.tokens <= 32):

@@ -87,8 +87,15 @@ constexpr int kNT = kTcTileTokens;        // tokens per item at most (MMA N)
 constexpr int kBoxRows = 16;              // token rows per activation TMA box
 // The window of one weight row per K step: the 16-byte aligned bytes that
 // hold its 256-weight unit (Q2_K 84 and codebook 70 bytes: 112; MXFP4 136
-// bytes: 144).  win_bytes: the windows of all kBM rows of an item.
-__host__ __device__ constexpr int win_words(int fmt) { return fmt == DS4G_FMT_MXFP4 ? 36 : 28; }
+// and Q4_K 144 bytes: 144; Q5_K 176; Q6_K 210 bytes at an even offset: 224).
+// win_bytes: the windows of all kBM rows of an item.
+__host__ __device__ constexpr int win_words(int fmt)
+{
+    return fmt == DS4G_FMT_MXFP4 || fmt == DS4G_FMT_Q4K ? 36
+         : fmt == DS4G_FMT_Q5K                          ? 44
+         : fmt == DS4G_FMT_Q6K                          ? 56
+                                                        : 28;
+}
 __host__ __device__ constexpr int win_bytes(int fmt) { return 4 * win_words(fmt) * kBM; }
 constexpr int kChunkBytes = kNT * 128;    // one 64-wide K chunk of the activation tile
 constexpr int kHalfBytes = 2 * kChunkBytes;   // activation half stage: K = 128
@@ -116,7 +123,7 @@ constexpr int kCbRepBytes = 256 * kCbCopies * 8;
 template <int MODE, int FMT>
 struct Ring {
     static constexpr int NMAT = MODE == 0 ? 2 : 1;
-    static constexpr int kW = MODE == 0 ? (FMT == DS4G_FMT_Q2K ? 3 : 2) : 4;
+    static constexpr int kW = MODE == 0 ? (FMT == DS4G_FMT_Q2K ? 3 : 2) : (FMT == DS4G_FMT_Q6K ? 3 : 4);
     static constexpr int kB = MODE == 1 && FMT == DS4G_FMT_Q2K ? 5 : 4;
     static constexpr uint32_t kWStageBytes = NMAT * win_bytes(FMT);
     static constexpr size_t kWOff = (size_t)kB * kHalfBytes;
@@ -373,9 +380,11 @@ __device__ __forceinline__ void cb2_window_quarter(const uint8_t *win, int boff,
 // exact while e - 127 lies in [-23, 13] (every product then stays between
 // 2^-24 and 49152).  `boff`: the unit's byte offset in its 16-byte aligned
 // window (0 or 8).  Returns false when a scale outside that range (other than
-// e = 255, NaN, which propagates as the definition says) made a weight inexact.
+// e = 255, NaN, which propagates as the definition says) met a nonzero code,
+// so that a weight came out inexact (all-zero blocks, such as the zero-filled
+// rows past `inter`, stay exact whatever their scale byte).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t mx_scale2(uint32_t e, bool &exact)
+__device__ __forceinline__ uint32_t mx_scale2(uint32_t e, bool &in_range)
 {
     const int s = (int)e - 127;
     const uint32_t bits = e == 255 ? 0x7E00u
@@ -383,7 +392,7 @@ __device__ __forceinline__ uint32_t mx_scale2(uint32_t e, bool &exact)
                         : s >= -14 ? (uint32_t)(s + 15) << 10
                         : s >= -24 ? 1u << (s + 24)
                                    : 0u;
-    exact = exact && (e == 255 || (s >= -23 && s <= 13));
+    in_range = e == 255 || (s >= -23 && s <= 13);
     return bits | (bits << 16);
 }
 
@@ -400,22 +409,164 @@ __device__ __forceinline__ bool mx_window_quarter(const uint8_t *win, int boff, 
 #pragma unroll
     for (int i = 0; i < 9; ++i) W[i] = w32[i];
     bool exact = true;
-    const uint32_t s2[2] = {mx_scale2((W[0] >> sh) & 0xFFu, exact),
-                            mx_scale2((W[4] >> (sh + 8)) & 0xFFu, exact)};
 #pragma unroll
     for (int bi = 0; bi < 2; ++bi) {
+        bool in_range;
+        const uint32_t s2 = mx_scale2(bi == 0 ? (W[0] >> sh) & 0xFFu : (W[4] >> (sh + 8)) & 0xFFu,
+                                      in_range);
+        // code bytes 4j .. 4j+3 of block b0 + bi (stream bytes 1 + 4j and 18 + 4j)
+        uint32_t cw[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            cw[j] = bi == 0 ? __funnelshift_r(W[j], W[j + 1], sh + 8)
+                            : __funnelshift_rc(W[4 + j], W[5 + j], sh + 16);
+        if (!in_range && ((cw[0] | cw[1] | cw[2] | cw[3]) & 0x77777777u) != 0) exact = false;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            // code bytes 4j .. 4j+3 of block b0 + bi (stream bytes 1 + 4j and 18 + 4j)
-            const uint32_t cw = bi == 0 ? __funnelshift_r(W[j], W[j + 1], sh + 8)
-                                        : __funnelshift_rc(W[4 + j], W[5 + j], sh + 16);
             uint32_t h[4];
-            ptx::e2m1x8_to_half2(cw, h);
+            ptx::e2m1x8_to_half2(cw[j], h);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) out[16 * bi + 4 * j + u] = ptx::hmul2_u(h[u], s2[bi]);
+            for (int u = 0; u < 4; ++u) out[16 * bi + 4 * j + u] = ptx::hmul2_u(h[u], s2);
         }
     }
     return exact;
+}
+
+// ---------------------------------------------------------------------------
+// Q4_K / Q5_K super-blocks (144 / 176 bytes: d, dmin, 12 bytes of packed
+// 6-bit scales and mins of eight 32-weight sub-blocks, Q5_K's qh[32] of
+// fifth bits, qs[128] of nibbles; weight 64c + l / 64c + 32 + l in the low /
+// high nibble of qs[32c + l], the fifth bit of weight 32s + l bit s of
+// qh[l]).  Both sizes are multiples of 16, so a block starts its window.
+// One quarter: chunk c = 2hh + gh, weights 64c .. +63 in natural order;
+// pairs 0..15 come from the low nibbles of qs[32c + 2j], qs[32c + 2j + 1]
+// (sub-block 2c), pairs 16..31 from their high nibbles (sub-block 2c + 1),
+// read in place.  Per pair, with exact fp16 operands:
+//   v = 1024 + q  (low nibble)  or  1024 + 16 q  (high nibble, fifth bit at 256)
+//   n = v * S + C = q * sc         S = sc or sc / 16, C = -1024 * S; exact (<= 1953)
+//   w = fp16(fp16(n * d + HI) + LO)   HI + LO = -dmin * m exactly (as Q2_K)
+// ---------------------------------------------------------------------------
+struct SubConst {
+    uint32_t S2, C2, HI2, LO2;
+};
+
+__device__ __forceinline__ SubConst k45_sub_const(int sc, int m, float inv, uint32_t ndmin2)
+{
+    SubConst k;
+    const float s = (float)sc * inv;
+    k.S2 = ptx::pack_half2(s, s);
+    k.C2 = ptx::pack_half2(-1024.0f * s, -1024.0f * s);
+    const uint32_t m2 = ptx::pack_half2((float)m, (float)m);
+    k.HI2 = ptx::hmul2_u(m2, ndmin2);
+    k.LO2 = ptx::hfma2_u(m2, ndmin2, k.HI2 ^ 0x80008000u);
+    return k;
+}
+
+__device__ __forceinline__ uint32_t k45_weight(uint32_t v, const SubConst &k, uint32_t d2)
+{
+    return ptx::hadd2_u(ptx::hfma2_u(ptx::hfma2_u(v, k.S2, k.C2), d2, k.HI2), k.LO2);
+}
+
+template <int Q5>
+__device__ __forceinline__ void k45_window_quarter(const uint8_t *win, int hh, int gh,
+                                                   uint32_t (&out)[32])
+{
+    const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win);
+    const int c = 2 * hh + gh;
+    const uint32_t dd = w32[0];
+    const uint32_t d2 = __byte_perm(dd, 0, 0x1010);
+    const uint32_t ndmin2 = __byte_perm(dd, 0, 0x3232) ^ 0x80008000u;
+    // scale bytes q[0..11] in w32[1..3]; sub-block s = 2c + t.  s < 4 (hh 0):
+    // sc = q[s] & 63, m = q[s+4] & 63; s >= 4 (hh 1): sc = (q[s+4] & 15) |
+    // (q[s-4] >> 6) << 4, m = (q[s+4] >> 4) | (q[s] >> 6) << 4.  Either way the
+    // three bytes sit at position 2gh + t of words 1, 2, 3.
+    SubConst k[2];
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        const int sh = 8 * (2 * gh + t);
+        const int b0 = (w32[1] >> sh) & 0xFF, b1 = (w32[2] >> sh) & 0xFF, b2 = (w32[3] >> sh) & 0xFF;
+        const int sc = hh ? (b2 & 15) | ((b0 >> 6) << 4) : b0 & 63;
+        const int m = hh ? (b2 >> 4) | ((b1 >> 6) << 4) : b1 & 63;
+        k[t] = k45_sub_const(sc, m, t ? 0.0625f : 1.0f, ndmin2);
+    }
+    const uint32_t k1024 = 0x64006400u;
+    const int qs0 = (Q5 ? 48 : 16) / 4 + 8 * c;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t W = w32[qs0 + i];                   // qs bytes 32c + 4i .. +3
+        const uint32_t x[2] = {__byte_perm(W, 0, 0x4140), __byte_perm(W, 0, 0x4342)};
+        uint32_t y[2] = {0, 0};
+        if (Q5) {
+            const uint32_t Y = w32[4 + i];                 // qh bytes 4i .. 4i+3
+            y[0] = __byte_perm(Y, 0, 0x4140);
+            y[1] = __byte_perm(Y, 0, 0x4342);
+        }
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            uint32_t vlo = ptx::lop3_and_or(x[p], 0x000F000Fu, k1024);
+            uint32_t vhi = ptx::lop3_and_or(x[p], 0x00F000F0u, k1024);
+            if (Q5) {
+                // bit 2c (value 16) and bit 2c + 1 (value 256, high nibble in place)
+                vlo = ptx::lop3_and_or((y[p] << 4) >> (2 * c), 0x00100010u, vlo);
+                vhi = ptx::lop3_and_or((y[p] << 8) >> (2 * c + 1), 0x01000100u, vhi);
+            }
+            out[2 * i + p] = k45_weight(vlo, k[0], d2);
+            out[16 + 2 * i + p] = k45_weight(vhi, k[1], d2);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Q6_K super-blocks (210 bytes: ql[128], qh[64], int8 scales[16], d; weight
+// j = 128h + 32u + l has its low nibble in nibble u >> 1 of ql[64h + 32(u&1)
+// + l], its top two bits in bits 2u, 2u + 1 of qh[32h + l];
+// w = d * scales[j / 16] * (q - 32)).  A block sits at an even offset `boff`
+// of its 224-byte window.  One quarter: half hh, weights 64gh .. +63 of it in
+// natural order: pairs 0..15 (u = 2gh) from nibble gh of ql[64hh + 2j, +1]
+// and bits 4gh, 4gh+1 of qh[32hh + 2j, +1]; pairs 16..31 (u = 2gh + 1) from
+// ql[64hh + 32 + ..] and bits 4gh+2, 4gh+3.  Per pair:
+//   v = 1024 + q exactly;  v - 1056 = q - 32 exactly;
+//   w = fp16((q - 32) * fp16(d * sc))   two roundings, each relative to w.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void q6k_window_quarter(const uint8_t *win, int boff, int hh, int gh,
+                                                   uint32_t (&out)[32])
+{
+    const uint32_t *w32 = reinterpret_cast<const uint32_t *>(win) + (boff >> 2);
+    const uint32_t fs = (uint32_t)(boff & 3) * 8;          // 0 or 16
+    // d (bytes 208, 209) and the four scales of the quarter (bytes 192 + 8hh + 4gh ..)
+    // d lies inside one aligned word (boff is even); no word past the window is read
+    const float d = __half2float(__ushort_as_half((unsigned short)((w32[52] >> fs) & 0xFFFFu)));
+    const int so = 48 + 2 * hh + gh;                       // word of the scale bytes
+    const uint32_t sw = __funnelshift_r(w32[so], w32[so + 1], fs);
+    uint32_t SD2[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float sd = d * (float)(int8_t)((sw >> (8 * q)) & 0xFF);
+        SD2[q] = ptx::pack_half2(sd, sd);
+    }
+    // qh bytes 32hh .. +31 (word 32 + 8hh on): the bits of both parts
+    uint32_t QH[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) QH[i] = __funnelshift_r(w32[32 + 8 * hh + i], w32[33 + 8 * hh + i], fs);
+    const uint32_t k1024 = 0x64006400u, k1056 = 0x64206420u;
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {
+        const int qw = 16 * hh + 8 * part;                 // word of ql[64hh + 32 part]
+        const int hs = 4 * gh + 2 * part;                  // qh bit pair
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t L = __funnelshift_r(w32[qw + i], w32[qw + i + 1], fs) >> (4 * gh);
+            const uint32_t x[2] = {__byte_perm(L, 0, 0x4140), __byte_perm(L, 0, 0x4342)};
+            const uint32_t y[2] = {__byte_perm(QH[i], 0, 0x4140), __byte_perm(QH[i], 0, 0x4342)};
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                uint32_t v = ptx::lop3_and_or(x[p], 0x000F000Fu, k1024);
+                v = ptx::lop3_and_or((y[p] >> hs) << 4, 0x00300030u, v);
+                const int j = 16 * part + 2 * i + p;       // pair index of the quarter
+                out[j] = ptx::hmul2_u(ptx::hsub2_u(v, k1056), SD2[j >> 3]);
+            }
+        }
+    }
 }
 
 // One quarter's 32 fp16 pairs of any tensor-core format; false when an MXFP4
@@ -426,6 +577,14 @@ __device__ __forceinline__ bool quarter_values(const uint8_t *win, int kb, int h
                                                uint32_t (&out)[32])
 {
     if (FMT == DS4G_FMT_MXFP4) return mx_window_quarter(win, (kMXFP4Bytes * kb) & 15, hh, k.gh, out);
+    if (FMT == DS4G_FMT_Q4K || FMT == DS4G_FMT_Q5K) {
+        k45_window_quarter<FMT == DS4G_FMT_Q5K>(win, hh, k.gh, out);
+        return true;
+    }
+    if (FMT == DS4G_FMT_Q6K) {
+        q6k_window_quarter(win, (kQ6KBytes * kb) & 15, hh, k.gh, out);
+        return true;
+    }
     if (FMT == DS4G_FMT_Q2K) {
         switch (kb & 3) {           // (84 * kb) mod 16, in words
         case 0: q2k_window_quarter<0>(win, hh, k, out); break;
@@ -1363,10 +1522,12 @@ cudaError_t weight_map(CUtensorMap *m, const void *base, int64_t row_bytes, int6
 
 bool tc_path_supported(const Plan &p, const ds4g_moe_desc *d)
 {
+    // every format has a tensor-core dequantizer (Q6_K only for W_down)
     const auto fmt_ok = [](int f) {
-        return f == DS4G_FMT_Q2K || f == DS4G_FMT_CB2 || f == DS4G_FMT_MXFP4;
+        return f == DS4G_FMT_Q2K || f == DS4G_FMT_CB2 || f == DS4G_FMT_MXFP4 ||
+               f == DS4G_FMT_Q4K || f == DS4G_FMT_Q5K;
     };
-    return p.A > 0 && fmt_ok(d->format) && fmt_ok(d->down_format) &&
+    return p.A > 0 && fmt_ok(d->format) && (fmt_ok(d->down_format) || d->down_format == DS4G_FMT_Q6K) &&
            d->gate_up_row_bytes % 16 == 0 && d->down_row_bytes % 16 == 0 && p.H % kBM == 0;
 }
 
@@ -1430,21 +1591,28 @@ cudaError_t launch_tc_path(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     lg.active = tb.light;
     lg.n_active = tb.n_light;
     const bool split = tb.min_tokens > 0;
-    if ((e = la.gu_format == DS4G_FMT_CB2     ? launch_tc<0, DS4G_FMT_CB2>(m_gate, m_up, m_x, a, dev.sm_count, s)
-             : la.gu_format == DS4G_FMT_MXFP4 ? launch_tc<0, DS4G_FMT_MXFP4>(m_gate, m_up, m_x, a, dev.sm_count, s)
-                                              : launch_tc<0, DS4G_FMT_Q2K>(m_gate, m_up, m_x, a, dev.sm_count, s)) !=
-        cudaSuccess)
-        return e;
+    switch (la.gu_format) {
+    case DS4G_FMT_CB2: e = launch_tc<0, DS4G_FMT_CB2>(m_gate, m_up, m_x, a, dev.sm_count, s); break;
+    case DS4G_FMT_MXFP4: e = launch_tc<0, DS4G_FMT_MXFP4>(m_gate, m_up, m_x, a, dev.sm_count, s); break;
+    case DS4G_FMT_Q4K: e = launch_tc<0, DS4G_FMT_Q4K>(m_gate, m_up, m_x, a, dev.sm_count, s); break;
+    case DS4G_FMT_Q5K: e = launch_tc<0, DS4G_FMT_Q5K>(m_gate, m_up, m_x, a, dev.sm_count, s); break;
+    default: e = launch_tc<0, DS4G_FMT_Q2K>(m_gate, m_up, m_x, a, dev.sm_count, s); break;
+    }
+    if (e != cudaSuccess) return e;
     if (split && (e = launch_gemv_gateup(lg, dev, s)) != cudaSuccess) return e;
     if (ev && (e = record_phase(ev[2], s)) != cudaSuccess) return e;
 
     a.K = la.I_pad;
     a.m_tiles = la.H / kBM;
-    if ((e = la.dn_format == DS4G_FMT_CB2     ? launch_tc_down<DS4G_FMT_CB2>(m_down, m_h, a, dev.sm_count, s)
-             : la.dn_format == DS4G_FMT_MXFP4 ? launch_tc<1, DS4G_FMT_MXFP4>(m_down, m_down, m_h, a, dev.sm_count, s)
-                                              : launch_tc<1, DS4G_FMT_Q2K>(m_down, m_down, m_h, a, dev.sm_count, s)) !=
-        cudaSuccess)
-        return e;
+    switch (la.dn_format) {
+    case DS4G_FMT_CB2: e = launch_tc_down<DS4G_FMT_CB2>(m_down, m_h, a, dev.sm_count, s); break;
+    case DS4G_FMT_MXFP4: e = launch_tc<1, DS4G_FMT_MXFP4>(m_down, m_down, m_h, a, dev.sm_count, s); break;
+    case DS4G_FMT_Q4K: e = launch_tc<1, DS4G_FMT_Q4K>(m_down, m_down, m_h, a, dev.sm_count, s); break;
+    case DS4G_FMT_Q5K: e = launch_tc<1, DS4G_FMT_Q5K>(m_down, m_down, m_h, a, dev.sm_count, s); break;
+    case DS4G_FMT_Q6K: e = launch_tc<1, DS4G_FMT_Q6K>(m_down, m_down, m_h, a, dev.sm_count, s); break;
+    default: e = launch_tc<1, DS4G_FMT_Q2K>(m_down, m_down, m_h, a, dev.sm_count, s); break;
+    }
+    if (e != cudaSuccess) return e;
     if (split && (e = launch_gemv_down(lg, dev, s)) != cudaSuccess) return e;
     if (ev && (e = record_phase(ev[3], s)) != cudaSuccess) return e;
 

@@ -153,13 +153,13 @@ enum {
  * Q4_K or Q5_K, down in Q2_K, Q4_K, Q5_K or Q6_K) are accepted with those
  * roles: format in {Q2K, CB2, Q4K, Q5K, MXFP4}, down_format in {Q2K, CB2,
  * Q4K, Q5K, Q6K, MXFP4} (else DS4G_ERR_INVALID).  MXFP4 is the ds4f-mxfp4
- * routed-expert format of the same page.  Layers with a K-quant matrix run
- * on the general (GEMV) kernels; DS4G_FORCE_TC then returns
- * DS4G_ERR_UNSUPPORTED.  MXFP4 matrices also run on the tensor-core kernels,
- * with weights converted exactly to fp16 operands while every block scale
+ * routed-expert format of the same page.  Every format has a tensor-core
+ * dequantizer (see "Path" under ds4g_moe_forward).  MXFP4 weights become
+ * exact fp16 operands there while every block scale
  * 2^(e-127) of the call's experts lies in 2^-23 .. 2^13 (any trained weight:
- * |w| from 2^-24 to 49152); a scale outside it (bar e = 255, NaN) rounds
- * those weights and sets the workspace status word to DS4G_ERR_RANGE (the
+ * |w| from 2^-24 to 49152); a scale outside it (bar e = 255, NaN) on a
+ * block with a nonzero code rounds those weights and sets the workspace
+ * status word to DS4G_ERR_RANGE (the
  * GEMV kernels, DS4G_FORCE_GEMV, compute such layers in fp32).  Row
  * alignment: rows of Q2_K, Q4_K, Q5_K and MXFP4
  * a multiple of 4 bytes, of codebook and Q6_K blocks a multiple of 2; rows
@@ -314,9 +314,10 @@ DS4G_API size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
  *           ds4g_moe_routing_view).
  * Path (one per call): Q2_K layers with inter % 16 == 0 and T <= 32 run
  * the decode kernels (mma.sync up to 8 vectors, tcgen05 from 9 to 32, the
- * latter with hidden % 128 == 0); otherwise layers of Q2_K, codebook and
- * MXFP4 matrices whose row_bytes are multiples of 16 and hidden % 128 == 0
- * run the tensor-core kernels; all others run the GEMV kernels.  DS4G_FORCE_TC forces the tensor-core kernels
+ * latter with hidden % 128 == 0); otherwise layers whose row_bytes are
+ * multiples of 16 (any formats; Q6_K W_down rows: inter padded to a
+ * multiple of 2048; MXFP4: an even number of 136-byte units) run the
+ * tensor-core kernels; all others run the GEMV kernels.  DS4G_FORCE_TC forces the tensor-core kernels
  * and DS4G_FORCE_GEMV rules them out.
  * Errors: DS4G_ERR_INVALID, DS4G_ERR_SHAPE, DS4G_ERR_LAYOUT,
  * DS4G_ERR_WORKSPACE, DS4G_ERR_UNSUPPORTED (a forced path that cannot run),

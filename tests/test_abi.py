@@ -240,20 +240,20 @@ def test_mixed_format_descriptor_is_accepted():
     # per-segment split on the tensor-core path: + GEMV gate/up and down
     ((7168, 2048, 256, 8), 2048, dict(tc_min_tokens=16), 2 + 5 + 2),
     ((7168, 2048, 256, 8), 16, dict(tc_min_tokens=16), 2),        # decode kernels: no split
-    # the Q4_K / Q5_K / Q6_K formats run on the GEMV kernels at every T; the
-    # tensor-core kernels refuse them
-    ((7168, 2048, 256, 8), 32, dict(fmt=D.FMT_Q4K, down_fmt=D.FMT_Q6K), 1 + 3),
-    ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_Q5K), 2 + 3),
-    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_Q2K, down_fmt=D.FMT_Q4K), 1 + 3),
-    ((7168, 2048, 256, 8), 64, dict(fmt=D.FMT_Q4K, flags=D.FORCE_TC), 0),
-    # MXFP4 takes the tensor-core kernels at every T (16-byte rows: an even
-    # number of 136-byte units), alone or with the 2-bit formats; with a
-    # K-quant matrix, or 408-byte rows, the GEMV kernels
+    # the Q4_K / Q5_K / Q6_K and MXFP4 formats take the tensor-core kernels at
+    # every T when their rows are multiples of 16 bytes (Q6_K: I_pad a multiple
+    # of 2048; MXFP4: an even number of 136-byte units), alone or mixed
+    ((7168, 2048, 256, 8), 32, dict(fmt=D.FMT_Q4K, down_fmt=D.FMT_Q6K), 1 + 5),
+    ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_Q5K), 2 + 5),
+    ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_Q2K, down_fmt=D.FMT_Q4K), 1 + 5),
+    ((7168, 2048, 256, 8), 64, dict(fmt=D.FMT_Q4K, flags=D.FORCE_TC), 1 + 5),
     ((7168, 2048, 256, 8), 32, dict(fmt=D.FMT_MXFP4), 1 + 5),
     ((7168, 2048, 256, 8), 1, dict(fmt=D.FMT_MXFP4, down_fmt=D.FMT_Q2K), 1 + 5),
-    ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_MXFP4, down_fmt=D.FMT_Q6K), 2 + 3),
+    ((7168, 2048, 256, 8), 2048, dict(fmt=D.FMT_MXFP4, down_fmt=D.FMT_Q6K), 2 + 5),
+    # otherwise the GEMV kernels: 408-byte MXFP4 rows, 420-byte Q6_K rows
     ((768, 512, 8, 2), 100, dict(fmt=D.FMT_MXFP4), 2 + 3),
     ((768, 512, 8, 2), 100, dict(fmt=D.FMT_MXFP4, flags=D.FORCE_TC), 0),
+    ((7168, 512, 256, 8), 32, dict(fmt=D.FMT_Q4K, down_fmt=D.FMT_Q6K), 1 + 3),
 ])
 def test_path_choice_by_launch_count(shape, T, kw, launches):
     """The per-call path choice documented under ds4g_moe_forward ("Path"),

@@ -101,12 +101,12 @@ def test_host_entry_point_matches_device_entry_point():
     assert np.array_equal(y_h.numpy().view(np.uint32), y_dev.view(np.uint32))
 
 
-def test_forced_tensor_core_refuses_kquant_layers():
-    """The tensor-core kernels take the 2-bit formats only: forcing them on a
-    Q4_K layer returns DS4G_ERR_UNSUPPORTED without touching y."""
-    # Q4_K rows of 2 and 1 blocks are multiples of 16 bytes, so the layout
-    # checks pass and the refusal comes from the format
-    layer = P.small_layer(seed=5, H=512, I=256, E=4, k=2, T=40, fmt=S.FMT_Q4K)
+def test_forced_tensor_core_refuses_unaligned_kquant_rows():
+    """The tensor-core kernels stage whole 16-byte windows: forcing them on a
+    layer whose Q6_K W_down rows (two 210-byte blocks) are not a multiple of
+    16 bytes returns DS4G_ERR_LAYOUT without touching y."""
+    layer = P.small_layer(seed=5, H=512, I=256, E=4, k=2, T=40, fmt=S.FMT_Q4K,
+                          down_fmt=S.FMT_Q6K)
     L = to_device(layer, flags=D.FORCE_TC)
     dev = torch.device("cuda")
     T, H = layer["x"].shape
@@ -114,6 +114,6 @@ def test_forced_tensor_core_refuses_kquant_layers():
     lg = torch.from_numpy(layer["logits"]).to(dev)
     y = torch.full((T, H), 7.0, dtype=torch.float32, device=dev)
     ws = torch.empty(L.workspace_bytes(T), dtype=torch.uint8, device=dev)
-    assert D.moe_forward(L.desc, x, lg, T, y, ws) == D.ERR_UNSUPPORTED
+    assert D.moe_forward(L.desc, x, lg, T, y, ws) == D.ERR_LAYOUT
     torch.cuda.synchronize()
     assert bool((y == 7.0).all())

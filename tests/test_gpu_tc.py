@@ -115,7 +115,7 @@ def test_mixed_format_layers(orc, kw):
     dict(H=1024, I=320, E=6, k=3, T=150),                     # ragged inter; segments over 128 tokens
     dict(H=2048, I=1024, E=33, k=5, T=70),                    # E not a multiple of 32
     dict(H=1024, I=512, E=1, k=1, T=300),                     # one expert, three token tiles
-    dict(H=1024, I=512, E=5, k=2, T=40, down_fmt=S.FMT_Q2K),  # MXFP4 gate/up, Q2_K down
+    dict(H=1024, I=512, E=5, k=2, T=40, down_fmt=S.FMT_Q2K, align=16),   # MXFP4 gate/up, Q2_K down
     dict(H=1024, I=512, E=5, k=2, T=40, down_fmt=S.FMT_CB2, align=16),   # h in natural order
     dict(H=1024, I=512, E=5, k=2, T=40, fmt=S.FMT_CB2, down_fmt=S.FMT_MXFP4, align=16),
 ], ids=["offsets", "ragged_I", "E33", "one_expert", "mx_q2k", "mx_cb2", "cb2_mx"])
@@ -126,6 +126,31 @@ def test_tc_forward_mxfp4_layers(orc, kw):
     2-bit formats in one layer."""
     kw = dict(dict(fmt=S.FMT_MXFP4), **kw)
     layer = P.small_layer(seed=5000 + kw["H"] + kw["T"], score=S.SCORE_SIGMOID, **kw)
+    L = to_device(layer, flags=D.FORCE_TC)
+    y, routing, st = run_forward(L, layer["x"], layer["logits"], with_status=True)
+    assert st == D.OK
+    check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    check_output(y, yref)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(H=512, I=512, E=8, k=2, T=12, fmt=S.FMT_Q4K),
+    dict(H=1024, I=320, E=6, k=3, T=150, fmt=S.FMT_Q5K),                  # ragged inter; > 128 tokens
+    dict(H=1024, I=1800, E=5, k=2, T=40, fmt=S.FMT_Q4K, down_fmt=S.FMT_Q6K),   # Q6_K at every even offset
+    dict(H=2048, I=512, E=33, k=5, T=70, fmt=S.FMT_Q5K, down_fmt=S.FMT_Q4K),
+    dict(H=1024, I=512, E=1, k=1, T=300, fmt=S.FMT_Q4K, down_fmt=S.FMT_Q5K),   # one expert, three tiles
+    dict(H=1024, I=2048, E=4, k=2, T=24, fmt=S.FMT_Q5K, down_fmt=S.FMT_Q6K),
+    dict(H=1024, I=512, E=5, k=2, T=40, fmt=S.FMT_CB2, down_fmt=S.FMT_Q4K, align=16),
+    dict(H=1024, I=512, E=5, k=2, T=40, fmt=S.FMT_Q4K, down_fmt=S.FMT_Q2K, align=16),
+    dict(H=1024, I=512, E=5, k=2, T=40, fmt=S.FMT_MXFP4, down_fmt=S.FMT_Q5K),
+], ids=["q4k", "q5k_ragged_I", "q4k_q6k", "q5k_q4k_E33", "q4k_q5k_one_expert", "q5k_q6k",
+        "cb2_q4k", "q4k_q2k", "mx_q5k"])
+def test_tc_forward_kquant_layers(orc, kw):
+    """The Q4_K / Q5_K super-blocks (gate/up or down) and Q6_K (down) on the
+    tensor-core kernels, in natural order (h too), alone or mixed with the
+    other formats in one layer."""
+    layer = P.small_layer(seed=6000 + kw["H"] + kw["T"], score=S.SCORE_SIGMOID, **kw)
     L = to_device(layer, flags=D.FORCE_TC)
     y, routing, st = run_forward(L, layer["x"], layer["logits"], with_status=True)
     assert st == D.OK
