@@ -800,6 +800,11 @@ __global__ void __launch_bounds__(kLaunchBound, 1) decode_q2k_kernel(DecArgs a)
                         const int n_e = rs.cnt[e];
                         const uint32_t hb = (uint32_t)n_e * (h_row + hs_row);
                         const bool h_in = used + dn_smem + hb <= a.stage_bytes;
+                        // the one-vector kernel reads h from shared memory
+                        // only: an expert whose h rows no longer fit starts
+                        // the next stage (the launcher checked that a W_down
+                        // tile and its h rows fit one stage)
+                        if (kSmemOnly && !h_in && cnt > 0) break;
                         const uint32_t need = dn_smem + (h_in ? hb : 0);
                         if (cnt > 0 && used + need > a.stage_bytes) break;
                         if (!wait_counter(done + e, a.I * n_e, a.wait_ns)) {

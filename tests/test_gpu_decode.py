@@ -8,7 +8,7 @@ import torch
 import bit_quantized_routed_route_b300 as D
 import ds4g_synth as S
 import oracle_pins as P
-from gpu_helpers import check_output, check_routing, run_forward, to_device
+from gpu_helpers import cached_layer, check_output, check_routing, run_forward, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -34,6 +34,25 @@ def test_decode_path(orc, kw):
     y, routing = run_forward(L, layer["x"], layer["logits"])
     check_routing(routing, orc.route(layer["logits"], layer["top_k"], layer["score"]))
     yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    check_output(y, yref)
+
+
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_decode_full_width_layer(orc, T):
+    """The 7168/2048/256/top-8 layer at 1..8 tokens on the mma.sync decode
+    kernel (the first T tokens of the 32-token workload): 2352-byte gate/up
+    rows copied whole, 672-byte W_down rows padded to 688 bytes in shared
+    memory, and down stages that fit two experts' tiles and h rows plus a
+    third tile without its h rows (the one-vector kernel must start a new
+    stage there, as it reads h from shared memory only)."""
+    layer = cached_layer("decode_32tok")
+    x, lg = layer["x"][:T], layer["logits"][:T]
+    L = to_device(layer)
+    assert D.moe_forward_launches(L.desc, T) == 2
+    y, routing, st = run_forward(L, x, lg, with_status=True)
+    assert st == D.OK
+    check_routing(routing, orc.route(lg, layer["top_k"], layer["score"]))
+    yref, _, _ = orc.moe_forward(layer, x, lg)
     check_output(y, yref)
 
 
