@@ -216,13 +216,14 @@ def tensor_peaks():
 
 def layer_path(cfg: S.Config) -> str:
     """Which kernels the library runs for this workload (mirrors its choice:
-    the decode kernels up to 32 tokens for Q2_K, the tensor-core kernels
-    (every format) for rows of a multiple of 16 bytes otherwise, the general
-    kernels for the rest)."""
+    the tensor-core kernels (every format) for rows of a multiple of 16
+    bytes, except Q2_K at up to 3 tokens; the Q2_K decode kernels up to 3
+    tokens, or up to 32 where the tensor-core kernels cannot take the rows;
+    the general kernels for the rest)."""
     tc = (cfg.row_bytes(cfg.hidden) % 16 == 0 and
           cfg.row_bytes(cfg.inter, fmt=cfg.dn_format) % 16 == 0)
     if (cfg.format == S.FMT_Q2K and cfg.dn_format == S.FMT_Q2K and cfg.inter % 16 == 0 and
-            cfg.tokens <= 32):
+            (cfg.tokens <= 3 or (cfg.tokens <= 32 and not tc))):
         return "decode"
     return "tc" if tc else "general"
 

@@ -155,18 +155,24 @@ namespace {
 
 enum class Path { kDecode, kTensorCore, kGeneral };
 
-// Decode kernels up to kDecodeMaxT tokens (mma.sync up to kDecodePreferT,
-// tcgen05 above), the tensor-core prefill kernels for larger token counts,
-// the general kernels where neither applies (codebook format in decode, the
-// Q4_K / Q5_K / Q6_K formats, or prefill rows that are not a multiple of 16
-// bytes).
+// Up to kDecodeOverTcT tokens the Q2_K decode kernels beat the tensor-core
+// kernels; from four tokens on the tensor-core kernels win where they apply
+// (7168/2048/256/top-8, measured: 0.088 against 0.127 ms at one token, 0.17
+// against 0.20 at two, 0.35 against 0.38 at four, 1.48 against 1.86 at 32).
+constexpr int kDecodeOverTcT = 3;
+
+// The Q2_K decode kernels up to kDecodeOverTcT tokens, and up to kDecodeMaxT
+// where the tensor-core kernels do not apply (mma.sync up to kDecodePreferT,
+// tcgen05 above); otherwise the tensor-core kernels for rows of a multiple of
+// 16 bytes, in every format; the general kernels where neither applies.
 Path choose_path(const ds4g_moe_desc *d, const Plan &p)
 {
     if (d->flags & DS4G_FORCE_TC) return Path::kTensorCore;
     const bool decode = decode_path_supported(p, d);
     if (d->flags & DS4G_FORCE_GEMV) return decode ? Path::kDecode : Path::kGeneral;
-    if (decode) return Path::kDecode;
-    if (tc_path_supported(p, d)) return Path::kTensorCore;
+    const bool tc = tc_path_supported(p, d);
+    if (decode && (p.T <= kDecodeOverTcT || !tc)) return Path::kDecode;
+    if (tc) return Path::kTensorCore;
     return Path::kGeneral;
 }
 

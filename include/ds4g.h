@@ -312,12 +312,13 @@ DS4G_API size_t ds4g_moe_workspace_bytes(const ds4g_moe_desc *desc, int32_t T);
  *           ds4g_moe_workspace_bytes(desc, T) bytes, 256-byte aligned.  After
  *           the call it holds the routing of this call (see
  *           ds4g_moe_routing_view).
- * Path (one per call): Q2_K layers with inter % 16 == 0 and T <= 32 run
- * the decode kernels (mma.sync up to 8 vectors, tcgen05 from 9 to 32, the
- * latter with hidden % 128 == 0); otherwise layers whose row_bytes are
- * multiples of 16 (any formats; Q6_K W_down rows: inter padded to a
- * multiple of 2048; MXFP4: an even number of 136-byte units) run the
- * tensor-core kernels; all others run the GEMV kernels.  DS4G_FORCE_TC forces the tensor-core kernels
+ * Path (one per call): layers whose row_bytes are multiples of 16 (any
+ * formats; Q6_K W_down rows: inter padded to a multiple of 2048; MXFP4: an
+ * even number of 136-byte units) run the tensor-core kernels, except Q2_K
+ * layers with inter % 16 == 0 at T <= 3, which run the decode kernels.  Q2_K
+ * layers that the tensor-core kernels cannot take run the decode kernels up
+ * to T = 32 (mma.sync up to 8 vectors, tcgen05 from 9 to 32, the latter with
+ * hidden % 128 == 0).  All others run the GEMV kernels.  DS4G_FORCE_TC forces the tensor-core kernels
  * and DS4G_FORCE_GEMV rules them out.
  * Errors: DS4G_ERR_INVALID, DS4G_ERR_SHAPE, DS4G_ERR_LAYOUT,
  * DS4G_ERR_WORKSPACE, DS4G_ERR_UNSUPPORTED (a forced path that cannot run),

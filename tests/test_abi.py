@@ -216,11 +216,16 @@ def test_mixed_format_descriptor_is_accepted():
 
 
 @pytest.mark.parametrize("shape,T,kw,launches", [
-    # decode kernels (reset + fused layer): Q2_K, inter % 16 == 0, up to 32 vectors
+    # decode kernels (reset + fused layer): Q2_K, inter % 16 == 0, up to 3
+    # vectors, or up to 32 where the tensor-core kernels cannot stage the rows
+    # (504-byte W_down rows here)
     ((4096, 1536, 64, 6), 1, {}, 2),
-    ((7168, 2048, 256, 8), 32, {}, 2),
-    # tensor-core path above 32 vectors: routing (1 launch up to 64 tokens, else 2) +
-    # token exponents, prep/gather, gate/up, down, combine
+    ((4096, 1536, 64, 6), 32, {}, 2),
+    ((7168, 2048, 256, 8), 3, {}, 2),
+    # tensor-core path from 4 vectors: routing (1 launch up to 64 tokens, else
+    # 2) + token exponents, prep/gather, gate/up, down, combine
+    ((7168, 2048, 256, 8), 4, {}, 1 + 5),
+    ((7168, 2048, 256, 8), 32, {}, 1 + 5),
     ((7168, 2048, 256, 8), 33, {}, 1 + 5),
     ((7168, 2048, 256, 8), 65, {}, 2 + 5),
     # rows that are not multiples of 16 bytes: GEMV kernels (routing + 3)
@@ -236,10 +241,11 @@ def test_mixed_format_descriptor_is_accepted():
     # tensor-core kernels elsewhere; FORCE_TC needs 16-byte rows (504-byte down rows here)
     ((4096, 1536, 64, 6), 1, dict(flags=D.FORCE_GEMV), 2),
     ((7168, 2048, 256, 8), 100, dict(flags=D.FORCE_GEMV), 2 + 3),
+    ((7168, 2048, 256, 8), 32, dict(flags=D.FORCE_GEMV), 2),
     ((4096, 1536, 64, 6), 1, dict(flags=D.FORCE_TC), 0),
     # per-segment split on the tensor-core path: + GEMV gate/up and down
     ((7168, 2048, 256, 8), 2048, dict(tc_min_tokens=16), 2 + 5 + 2),
-    ((7168, 2048, 256, 8), 16, dict(tc_min_tokens=16), 2),        # decode kernels: no split
+    ((7168, 2048, 256, 8), 3, dict(tc_min_tokens=16), 2),         # decode kernels: no split
     # the Q4_K / Q5_K / Q6_K and MXFP4 formats take the tensor-core kernels at
     # every T when their rows are multiples of 16 bytes (Q6_K: I_pad a multiple
     # of 2048; MXFP4: an even number of 136-byte units), alone or mixed

@@ -37,17 +37,19 @@ def test_decode_path(orc, kw):
     check_output(y, yref)
 
 
-@pytest.mark.parametrize("T", [1, 2, 5, 8])
+@pytest.mark.parametrize("T", [1, 2, 5, 8, 12, 32])
 def test_decode_full_width_layer(orc, T):
-    """The 7168/2048/256/top-8 layer at 1..8 tokens on the mma.sync decode
-    kernel (the first T tokens of the 32-token workload): 2352-byte gate/up
-    rows copied whole, 672-byte W_down rows padded to 688 bytes in shared
-    memory, and down stages that fit two experts' tiles and h rows plus a
-    third tile without its h rows (the one-vector kernel must start a new
-    stage there, as it reads h from shared memory only)."""
+    """The 7168/2048/256/top-8 layer on the decode kernels (the first T tokens
+    of the 32-token workload; from 4 tokens on the call would take the
+    tensor-core kernels unless forced): 2352-byte gate/up rows copied whole,
+    672-byte W_down rows padded to 688 bytes in shared memory, and down
+    stages that fit two experts' tiles and h rows plus a third tile without
+    its h rows (the one-vector kernel must start a new stage there, as it
+    reads h from shared memory only); 12 and 32 tokens on the tcgen05 decode
+    kernel."""
     layer = cached_layer("decode_32tok")
     x, lg = layer["x"][:T], layer["logits"][:T]
-    L = to_device(layer)
+    L = to_device(layer, flags=D.FORCE_GEMV)
     assert D.moe_forward_launches(L.desc, T) == 2
     y, routing, st = run_forward(L, x, lg, with_status=True)
     assert st == D.OK

@@ -17,7 +17,7 @@ from gpu_helpers import check_output, to_device
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("T,flags", [(3, 0), (12, 0), (3, D.FORCE_TC)],
+@pytest.mark.parametrize("T,flags", [(3, 0), (12, D.FORCE_GEMV), (3, D.FORCE_TC)],
                          ids=["decode_mma_sync", "decode_tcgen05", "tensor_core"])
 def test_bounded_wait_expires_and_reports_timeout(orc, T, flags):
     layer = P.small_layer(seed=31, H=1024, I=512, E=8, k=2, T=T, align=16)
