@@ -12,9 +12,11 @@
 //                 registers; k rounds of two warp reductions (largest
 //                 order key, then lowest expert id holding it).
 //   scan_kernel   one CTA: histogram, exclusive scan, then a stable counting
-//                 sort of the assignments a = t*k + i by expert (warp
-//                 match-any ranks + per-warp bases), ascending t inside each
-//                 segment.  Integer atomics only; no float atomics.
+//                 sort of the assignments a = t*k + i by expert: each warp
+//                 counts, then places, one contiguous chunk (warp match-any
+//                 ranks + per-warp, per-expert bases), so the order inside
+//                 each segment is ascending a.  Integer atomics only; no
+//                 float atomics.
 //   route_small   both phases in one CTA for small T (decode), one launch.
 //
 // With an activation pointer the kernels also write the decode path's
@@ -77,7 +79,6 @@ template <int NW>
 struct ScanSmem {
     int count[DS4G_MAX_EXPERTS];
     int offset[DS4G_MAX_EXPERTS + 1];
-    int running[DS4G_MAX_EXPERTS];
     int warp_base[NW][DS4G_MAX_EXPERTS];
     int warp_sum[8];
     int act_sum[8];
@@ -92,7 +93,7 @@ __device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
                           int32_t *active, int32_t *n_active)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid < DS4G_MAX_EXPERTS) { sm.count[tid] = 0; sm.running[tid] = 0; }
+    if (tid < DS4G_MAX_EXPERTS) sm.count[tid] = 0;
     __syncthreads();
     for (int a = tid; a < A; a += blockDim.x) {
         int e = ids[a];
@@ -142,34 +143,47 @@ __device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
     }
     if (tid == 0 && offsets) offsets[E] = sm.offset[E];
     __syncthreads();
-    // stable placement, 1024 assignments per round
-    for (int base = 0; base < A; base += blockDim.x) {
-        for (int i = tid; i < NW * DS4G_MAX_EXPERTS; i += blockDim.x)
-            (&sm.warp_base[0][0])[i] = 0;
-        __syncthreads();
-        int a = base + tid;
-        int e = (a < A) ? ids[a] : -1;
+    // stable placement: warp w takes the contiguous chunk [w*C, (w+1)*C) of
+    // the assignments; pass 1 counts its chunk per expert, a prefix over the
+    // warps (in chunk order) turns the counts into each warp's first position
+    // per expert, and pass 2 places the chunk in order (32 at a time, lanes
+    // of equal expert ranked by lane)
+    for (int i = tid; i < NW * DS4G_MAX_EXPERTS; i += blockDim.x) (&sm.warp_base[0][0])[i] = 0;
+    __syncthreads();
+    const int C = ((A + NW - 1) / NW + 31) / 32 * 32;
+    const int a_end = min(A, (warp + 1) * C);
+    for (int a0 = warp * C; a0 < a_end; a0 += 32) {
+        const int a = a0 + lane;
+        int e = a < a_end ? ids[a] : -1;
         if (e < 0 || e >= E) e = -1;
-        unsigned same = __match_any_sync(0xffffffffu, e);
-        int rank = __popc(same & ((1u << lane) - 1u));
-        if (e >= 0 && rank == 0) sm.warp_base[warp][e] = __popc(same);
-        __syncthreads();
-        if (tid < E) {
-            int run = sm.running[tid];
-            for (int w = 0; w < NW; ++w) {
-                int cnt = sm.warp_base[w][tid];
-                sm.warp_base[w][tid] = run;
-                run += cnt;
-            }
-            sm.running[tid] = run;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        if (e >= 0 && __popc(same & ((1u << lane) - 1u)) == 0) sm.warp_base[warp][e] += __popc(same);
+        __syncwarp();
+    }
+    __syncthreads();
+    if (tid < E) {
+        int run = sm.offset[tid];
+        for (int w = 0; w < NW; ++w) {
+            const int cnt = sm.warp_base[w][tid];
+            sm.warp_base[w][tid] = run;
+            run += cnt;
         }
-        __syncthreads();
+    }
+    __syncthreads();
+    for (int a0 = warp * C; a0 < a_end; a0 += 32) {
+        const int a = a0 + lane;
+        int e = a < a_end ? ids[a] : -1;
+        if (e < 0 || e >= E) e = -1;
+        const unsigned same = __match_any_sync(0xffffffffu, e);
+        const int rank = __popc(same & ((1u << lane) - 1u));
         if (e >= 0) {
-            int pos = sm.offset[e] + sm.warp_base[warp][e] + rank;
+            const int pos = sm.warp_base[warp][e] + rank;
             if (perm) perm[pos] = a;
             if (slot_pos) slot_pos[a] = pos;
         }
-        __syncthreads();
+        __syncwarp();
+        if (e >= 0 && rank == 0) sm.warp_base[warp][e] += __popc(same);
+        __syncwarp();
     }
 }
 
