@@ -11,12 +11,12 @@
 //   topk_kernel   one warp per token; each lane holds E/32 logits in
 //                 registers; k rounds of two warp reductions (largest
 //                 order key, then lowest expert id holding it).
-//   scan_kernel   one CTA: histogram, exclusive scan, then a stable counting
-//                 sort of the assignments a = t*k + i by expert: each warp
-//                 counts, then places, one contiguous chunk (warp match-any
-//                 ranks + per-warp, per-expert bases), so the order inside
-//                 each segment is ascending a.  Integer atomics only; no
-//                 float atomics.
+//   scan_kernel   one CTA: a stable counting sort of the assignments
+//                 a = t*k + i by expert: each warp counts, then places, one
+//                 contiguous chunk (warp match-any ranks + per-warp,
+//                 per-expert bases), with the counts, the exclusive scan over
+//                 the experts and the active list in between, so the order
+//                 inside each segment is ascending a.  No atomics.
 //   route_small   both phases in one CTA for small T (decode), one launch.
 //
 // With an activation pointer the kernels also write the decode path's
@@ -77,7 +77,6 @@ __global__ void __launch_bounds__(256) topk_kernel(const float *__restrict__ log
 // Shared state of the counting sort (one CTA of NW >= 8 warps).
 template <int NW>
 struct ScanSmem {
-    int count[DS4G_MAX_EXPERTS];
     int offset[DS4G_MAX_EXPERTS + 1];
     int warp_base[NW][DS4G_MAX_EXPERTS];
     int warp_sum[8];
@@ -87,21 +86,54 @@ struct ScanSmem {
 // counts / offsets / perm / slot_pos / active from ids[A].  Called by all
 // NW * 32 threads of the CTA.  `ids` may have been written earlier in the same
 // kernel, so it is read through the coherent path (no __restrict__).
+//
+// Warp w takes the contiguous chunk [w*C, (w+1)*C) of the assignments.  Pass 1
+// counts its chunk per expert (warp match-any, warp-private table); the
+// counts per expert are the sums over the warps; an exclusive scan over the
+// experts gives the offsets; a prefix over the warps (in chunk order) turns
+// each warp's counts into its first position per expert; pass 2 places the
+// chunk in order (lanes of equal expert ranked by lane), so each segment is
+// in ascending a.  The ids of a chunk are read eight loads at a time.
+constexpr int kScanBatch = 8;
+
+template <int NW>
+__device__ __forceinline__ void load_ids(const int32_t *ids, int a0, int a_end, int E, int lane,
+                                         int (&eb)[kScanBatch])
+{
+#pragma unroll
+    for (int u = 0; u < kScanBatch; ++u) {
+        const int a = a0 + 32 * u + lane;
+        const int e = a < a_end ? ids[a] : -1;
+        eb[u] = e >= 0 && e < E ? e : -1;
+    }
+}
+
 template <int NW>
 __device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
                           int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *slot_pos,
                           int32_t *active, int32_t *n_active)
 {
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid < DS4G_MAX_EXPERTS) sm.count[tid] = 0;
+    const unsigned below = (1u << lane) - 1u;
+    for (int i = tid; i < NW * DS4G_MAX_EXPERTS; i += blockDim.x) (&sm.warp_base[0][0])[i] = 0;
     __syncthreads();
-    for (int a = tid; a < A; a += blockDim.x) {
-        int e = ids[a];
-        if (e >= 0 && e < E) atomicAdd(&sm.count[e], 1);
+    const int C = ((A + NW - 1) / NW + 31) / 32 * 32;
+    const int a_beg = warp * C, a_end = min(A, (warp + 1) * C);
+    for (int a0 = a_beg; a0 < a_end; a0 += 32 * kScanBatch) {
+        int eb[kScanBatch];
+        load_ids<NW>(ids, a0, a_end, E, lane, eb);
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) {
+            const unsigned same = __match_any_sync(0xffffffffu, eb[u]);
+            if (eb[u] >= 0 && (same & below) == 0) sm.warp_base[warp][eb[u]] += __popc(same);
+            __syncwarp();
+        }
     }
     __syncthreads();
     // exclusive scan over E <= 256 experts: 8 warps x 32
-    int c = (tid < E) ? sm.count[tid] : 0;
+    int c = 0;
+    if (tid < E)
+        for (int w = 0; w < NW; ++w) c += sm.warp_base[w][tid];
     int incl = c;
     if (warp < 8) {
 #pragma unroll
@@ -130,7 +162,7 @@ __device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
         unsigned b = __ballot_sync(0xffffffffu, act);
         int base = 0;
         for (int w = 0; w < warp; ++w) base += sm.act_sum[w];
-        if (act && active) active[base + __popc(b & ((1u << lane) - 1u))] = tid;
+        if (act && active) active[base + __popc(b & below)] = tid;
         if (tid == 255 && n_active) {
             int tot = 0;
             for (int w = 0; w < 8; ++w) tot += sm.act_sum[w];
@@ -140,28 +172,7 @@ __device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
     if (tid < E) {
         if (counts) counts[tid] = c;
         if (offsets) offsets[tid] = sm.offset[tid];
-    }
-    if (tid == 0 && offsets) offsets[E] = sm.offset[E];
-    __syncthreads();
-    // stable placement: warp w takes the contiguous chunk [w*C, (w+1)*C) of
-    // the assignments; pass 1 counts its chunk per expert, a prefix over the
-    // warps (in chunk order) turns the counts into each warp's first position
-    // per expert, and pass 2 places the chunk in order (32 at a time, lanes
-    // of equal expert ranked by lane)
-    for (int i = tid; i < NW * DS4G_MAX_EXPERTS; i += blockDim.x) (&sm.warp_base[0][0])[i] = 0;
-    __syncthreads();
-    const int C = ((A + NW - 1) / NW + 31) / 32 * 32;
-    const int a_end = min(A, (warp + 1) * C);
-    for (int a0 = warp * C; a0 < a_end; a0 += 32) {
-        const int a = a0 + lane;
-        int e = a < a_end ? ids[a] : -1;
-        if (e < 0 || e >= E) e = -1;
-        const unsigned same = __match_any_sync(0xffffffffu, e);
-        if (e >= 0 && __popc(same & ((1u << lane) - 1u)) == 0) sm.warp_base[warp][e] += __popc(same);
-        __syncwarp();
-    }
-    __syncthreads();
-    if (tid < E) {
+        // each warp's first position per expert
         int run = sm.offset[tid];
         for (int w = 0; w < NW; ++w) {
             const int cnt = sm.warp_base[w][tid];
@@ -169,21 +180,26 @@ __device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
             run += cnt;
         }
     }
+    if (tid == 0 && offsets) offsets[E] = sm.offset[E];
     __syncthreads();
-    for (int a0 = warp * C; a0 < a_end; a0 += 32) {
-        const int a = a0 + lane;
-        int e = a < a_end ? ids[a] : -1;
-        if (e < 0 || e >= E) e = -1;
-        const unsigned same = __match_any_sync(0xffffffffu, e);
-        const int rank = __popc(same & ((1u << lane) - 1u));
-        if (e >= 0) {
-            const int pos = sm.warp_base[warp][e] + rank;
-            if (perm) perm[pos] = a;
-            if (slot_pos) slot_pos[a] = pos;
+    for (int a0 = a_beg; a0 < a_end; a0 += 32 * kScanBatch) {
+        int eb[kScanBatch];
+        load_ids<NW>(ids, a0, a_end, E, lane, eb);
+#pragma unroll
+        for (int u = 0; u < kScanBatch; ++u) {
+            const int e = eb[u];
+            const unsigned same = __match_any_sync(0xffffffffu, e);
+            const int rank = __popc(same & below);
+            if (e >= 0) {
+                const int a = a0 + 32 * u + lane;
+                const int pos = sm.warp_base[warp][e] + rank;
+                if (perm) perm[pos] = a;
+                if (slot_pos) slot_pos[a] = pos;
+            }
+            __syncwarp();
+            if (e >= 0 && rank == 0) sm.warp_base[warp][e] += __popc(same);
+            __syncwarp();
         }
-        __syncwarp();
-        if (e >= 0 && rank == 0) sm.warp_base[warp][e] += __popc(same);
-        __syncwarp();
     }
 }
 
