@@ -1,5 +1,5 @@
 #!/usr/bin/env python3
-"""Benchmark of the routed-MoE expert layer over 2-bit quantized experts.
+"""Benchmark of the routed-MoE expert layer over low-bit quantized experts.
 
 One step = one call of the whole layer (routing, counts/offsets/permutation,
 fused dequant gate/up + SiLU, down projection, weighted combine) over one
@@ -8,7 +8,8 @@ expert intermediate 2048, 256 Q2_K experts, top-8, 2048 tokens per step
 (the largest single-GPU workload; the tcgen05 tensor-core kernels).  The
 same JSON line carries a `per_config` object with the other workloads
 (single-token decode, 32-token decode, 512-token codebook layer, the tiny
-layer), each timed in the same run the same way.
+layer, the shipping mix, the K-quant and MXFP4 layers, the expert cache),
+each timed in the same run the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
   python bench.py --impl reference ...     # the CPU oracle, timed as it stands
@@ -708,9 +709,9 @@ def main(argv=None):
         "steps": K, "warmup": W, "ms_per_step": head["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
-        "arithmetic": ("fp16 tensor-core operands (decode: exact 2-bit fields and fp16 "
-                       "activations; prefill: weights dequantized to fp16), fp32 accumulation "
-                       "and fp32 output"),
+        "arithmetic": ("fp16 tensor-core operands (Q2_K decode kernels: exact 2-bit fields and "
+                       "fp16 activations; tensor-core kernels: weights dequantized to fp16), "
+                       "fp32 accumulation and fp32 output"),
         "config": head["config"],
         "roofline": head["roofline"],
         "path": head["path"],

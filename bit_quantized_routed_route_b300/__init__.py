@@ -1,5 +1,5 @@
 """Python binding of libds4g, the B300 (sm_103a) routed-MoE expert layer over
-2-bit quantized experts.
+low-bit quantized experts.
 
 Argument marshalling only: every step of the layer runs in the CUDA kernels of
 ``libds4g.so`` behind the C ABI declared in ``include/ds4g.h``.  PyTorch is

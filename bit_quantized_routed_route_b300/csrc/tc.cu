@@ -1,7 +1,9 @@
-// tc.cu -- the tensor-core path for Q2_K and codebook-2-bit experts: expert
-// segments long enough that the layer is a dense contraction (prefill; ds4
-// README mirror, "So, what can I do with this software?" names micro-batched
-// prefill on CUDA).
+// tc.cu -- the tensor-core path for every routed-expert format (Q2_K,
+// codebook-2-bit, Q4_K, Q5_K, Q6_K for W_down, MXFP4; any mix per matrix):
+// the weights are dequantized to fp16 into tensor memory and contracted with
+// tcgen05 MMAs, for every call above three tokens whose rows can be staged
+// (ds4 README mirror, "So, what can I do with this software?" names
+// micro-batched decode and prefill on CUDA; "Model Weights" the formats).
 //
 // Per active expert e with segment rows P = offsets[e] .. offsets[e+1]-1
 // (assignments in segment order):
@@ -59,10 +61,12 @@
 // the group, so one half2 of scales serves both lanes without replication.
 // Inside every aligned group of 32, weight 16b + l is stored at K position
 // 2l + b (the activation operand and h use the same order, so the
-// contraction is unchanged).  Codebook-2-bit weights keep the natural order:
-// each 8-weight codebook row comes from a 16-way replicated copy of the
-// codebook in shared memory, c*s is formed exactly in fp16 and the single
-// rounding is the multiply by d.
+// contraction is unchanged).  MXFP4 follows the same order (a code byte is
+// the pair i, i + 16 of its block).  Codebook-2-bit weights keep the natural
+// order: each 8-weight codebook row comes from a 16-way replicated copy of
+// the codebook in shared memory, c*s is formed exactly in fp16 and the single
+// rounding is the multiply by d.  So do the K-quant formats (the quarter
+// decoders below state their arithmetic).
 //
 // Tensor memory (512 columns): columns 0..255 are the four A buffers of 64
 // columns (K = 128 fp16), 2t and 2t+1 for team t; columns 256..383 and 384..511 are the fp32

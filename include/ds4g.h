@@ -1,7 +1,8 @@
 /*
  * ds4g.h -- C ABI of libds4g: the routed mixture-of-experts expert layer over
- * 2-bit quantized expert weights, as hand-written CUDA kernels for the
- * NVIDIA B300 (sm_103a).
+ * low-bit quantized expert weights (2-bit in the shipping mix; also the
+ * routed Q4_K / Q5_K / Q6_K and MXFP4 formats), as hand-written CUDA kernels
+ * for the NVIDIA B300 (sm_103a).
  *
  * What the layer is.  The ds4 README (codehub.bot mirror, section "Model
  * Weights") states that only the routed MoE experts are quantized -- up/gate

@@ -2,9 +2,8 @@
 routing bit-exact, per-token relative L2 <= 1e-3 and max-abs <= 5e-3 *
 max|ref| on the output.
 
-The path runs by itself for layers above the decode token counts whose rows
-are multiples of 16 bytes (both formats); DS4G_FORCE_TC sends smaller layers
-to it.
+The path runs by itself for layers whose rows are multiples of 16 bytes (every
+format; Q2_K from 4 tokens on); DS4G_FORCE_TC sends the others to it.
 Cases span several 128-row weight tiles and several 128-token tiles, with
 ragged tails on both (inter not a multiple of 128, segments longer than one
 token tile), a single expert, k = E, and the full-size decode layer."""
