@@ -1346,7 +1346,9 @@ __global__ void __launch_bounds__(256) token_exp_kernel(const uint16_t *__restri
 //   16b + l of every aligned group of 32 at position 2l + b (perm32), in
 //   natural order for the codebook format.  One thread writes 16 consecutive
 //   positions.
-__global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict__ x, int H, int k,
+constexpr int kPrepWarps = DS4G_MAX_EXPERTS / 32;   // tc_prep_kernel: one thread per expert
+
+__global__ void __launch_bounds__(kPrepWarps * 32) tc_prep_kernel(const uint16_t *__restrict__ x, int H, int k,
                                                       int A, const int32_t *__restrict__ perm,
                                                       const int32_t *counts,
                                                       const int32_t *offsets, int E,
@@ -1364,33 +1366,41 @@ __global__ void __launch_bounds__(256) tc_prep_kernel(const uint16_t *__restrict
         eseg[p] = texp[perm[p] / k];
     }
     if (blockIdx.x == 0) {
-        __shared__ int s_nt[DS4G_MAX_EXPERTS];
-        __shared__ int s_base[DS4G_MAX_EXPERTS + 1];
-        const int e = threadIdx.x;
-        if (e < DS4G_MAX_EXPERTS)
-            s_nt[e] = e < E && counts[e] >= min_tokens ? (counts[e] + kNT - 1) / kNT : 0;
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            int run = 0, nl = 0;
-            for (int i = 0; i < E; ++i) {
-                s_base[i] = run;
-                run += s_nt[i];
-                if (counts[i] > 0 && counts[i] < min_tokens) light[nl++] = i;
-            }
-            s_base[E] = run;
-            *n_tiles = run;
-            *n_light = nl;
+        // thread e (256 threads, one per expert): its tile count, an exclusive
+        // scan over the experts (warp shuffles, then the warp totals) for its
+        // first tile, and a ballot compaction of the light experts in id order
+        __shared__ int s_wtiles[kPrepWarps], s_wlight[kPrepWarps];
+        const int e = threadIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+        const int c = e < E ? counts[e] : 0;
+        const int nt = c > 0 && c >= min_tokens ? (c + kNT - 1) / kNT : 0;
+        const bool is_light = c > 0 && c < min_tokens;
+        int incl = nt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
         }
+        const unsigned lb = __ballot_sync(0xffffffffu, is_light);
+        if (lane == 31) s_wtiles[warp] = incl;
+        if (lane == 0) s_wlight[warp] = __popc(lb);
         __syncthreads();
-        if (e < E) {
-            const int c = counts[e], o = offsets[e];
-            for (int j = 0; j < s_nt[e]; ++j) {
-                int32_t *t = tiles + 4 * (s_base[e] + j);
-                t[0] = e;
-                t[1] = o + j * kNT;
-                t[2] = min(kNT, c - j * kNT);
-                t[3] = 0;
-            }
+        int tbase = 0, lbase = 0;
+        for (int w = 0; w < warp; ++w) {
+            tbase += s_wtiles[w];
+            lbase += s_wlight[w];
+        }
+        if (is_light) light[lbase + __popc(lb & ((1u << lane) - 1u))] = e;
+        if (e == kPrepWarps * 32 - 1) {
+            *n_tiles = tbase + incl;
+            *n_light = lbase + __popc(lb);
+        }
+        const int o = e < E ? offsets[e] : 0;
+        for (int j = 0; j < nt; ++j) {
+            int32_t *t = tiles + 4 * (tbase + incl - nt + j);
+            t[0] = e;
+            t[1] = o + j * kNT;
+            t[2] = min(kNT, c - j * kNT);
+            t[3] = 0;
         }
     }
     const int per_row = H / 16;
@@ -1549,7 +1559,7 @@ cudaError_t launch_tc_prep(const LayerArgs &la, const TcBufs &tb, const DeviceIn
     cudaError_t e = launch_token_exponents(la.x, la.T, la.H, tb.texp, s);
     if (e != cudaSuccess) return e;
     const int prep_grid = dev.sm_count * 4;
-    tc_prep_kernel<<<prep_grid, 256, 0, s>>>(la.x, la.H, la.k, la.A, la.perm, la.counts,
+    tc_prep_kernel<<<prep_grid, kPrepWarps * 32, 0, s>>>(la.x, la.H, la.k, la.A, la.perm, la.counts,
                                              la.offsets, la.E, tb.xseg, tb.tiles, tb.n_tiles,
                                              perm32_format(la.gu_format) ? 1 : 0, la.wts, tb.wseg,
                                              tb.texp, tb.eseg, tb.min_tokens, tb.light, tb.n_light);
