@@ -17,6 +17,10 @@ import ds4g_synth as S
     ("decode_32tok", 2048 * 28 * 84, 7168 * 8 * 84),  # 4,816,896 and 4,816,896 bytes
     # codebook format: 70 bytes per 256 weights
     ("codebook_512", 2048 * 28 * 70, 7168 * 8 * 70),  # 4,014,080 and 4,014,080 bytes
+    # each matrix in its own format
+    ("mixed_2048", 2048 * 28 * 70, 7168 * 8 * 84),    # codebook gate/up, Q2_K down
+    ("kquant_32tok", 2048 * 28 * 144, 7168 * 8 * 210),  # Q4_K gate/up, Q6_K down
+    ("mxfp4_32tok", 2048 * 28 * 136, 7168 * 8 * 136),   # eight 17-byte blocks per 256 weights
 ])
 def test_layer_bytes_per_expert(name, gate_bytes, down_bytes):
     assert bench.layer_bytes(S.CONFIGS[name]) == (gate_bytes, down_bytes)
@@ -52,3 +56,20 @@ def test_source_hash_ignores_comments_and_blank_lines(tmp_path, monkeypatch):
     assert bench.kernel_source_hash("probe") == h0
     (csrc / "k.cu").write_text("int a = 2;\n")
     assert bench.kernel_source_hash("probe") != h0
+
+
+@pytest.mark.parametrize("name", list(S.CONFIGS))
+def test_layer_path_mirrors_the_library(name):
+    """The benchmark's own statement of which kernels run (`layer_path`, used
+    for the roofline) agrees with the library's choice, read through
+    ds4g_moe_forward_launches on the workload's descriptor (host arithmetic
+    only): decode = 2 launches, tensor core = routing + 5, general = routing + 3."""
+    import bit_quantized_routed_route_b300 as D
+    from test_abi import layer_desc
+    cfg = S.CONFIGS[name]
+    d = layer_desc(cfg.hidden, cfg.inter, cfg.n_experts, cfg.top_k, fmt=cfg.format,
+                   align=cfg.row_align, down_fmt=cfg.dn_format)
+    route = 1 if cfg.tokens <= 64 else 2
+    expect = {"decode": 2, "tc": route + 5, "general": route + 3}[bench.layer_path(cfg)]
+    assert D.moe_forward_launches(d, cfg.tokens) == expect
+

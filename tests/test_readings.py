@@ -1,0 +1,60 @@
+"""Number-format facts that the tensor-core kernels' exactness claims rest
+on, checked on the CPU with numpy's IEEE fp16 (no kernel or oracle code):
+
+* MXFP4 (ds4 README mirror, "Model Weights": the ds4f-mxfp4 routed experts,
+  read as OCP microscaling FP4): every E2M1 value times the block scale
+  2^s is exact in fp16 for s in [-23, 13], and not for s = -24 or 14, which
+  is the range outside which the kernels report DS4G_ERR_RANGE;
+* Q4_K / Q5_K (same page, the routed K-quant formats): the integer q * sc
+  (q < 32, sc < 64) and the constants -1024 * sc and -64 * sc used to form
+  it are exact fp16 values, so n = v * S + C is exact;
+* Q6_K: (q - 32) * sc reaches past fp16's exact integers, which is why its
+  weights take the form fp16((q - 32) * fp16(d * sc)) with two roundings."""
+import numpy as np
+
+E2M1 = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def exact_in_fp16(v):
+    v = np.asarray(v, dtype=np.float64)
+    with np.errstate(over="ignore"):          # values past 65504 become inf: not exact
+        return np.all(v.astype(np.float16).astype(np.float64) == v)
+
+
+def test_e2m1_times_power_of_two_is_exact_in_fp16_from_2_pow_m23_to_2_pow_13():
+    for s in range(-23, 14):
+        vals = np.concatenate([E2M1, -E2M1]) * 2.0 ** s
+        assert exact_in_fp16(vals), s
+        # the scale itself is an fp16 value too (a subnormal below 2^-14)
+        assert exact_in_fp16([2.0 ** s])
+    # one step outside: 0.5 * 2^-24 underflows, 4 * 2^14 overflows
+    assert not exact_in_fp16(E2M1 * 2.0 ** -24)
+    assert not exact_in_fp16(E2M1 * 2.0 ** 14)
+
+
+def test_e2m1_code_to_value_through_fp16_bits():
+    # the low three bits placed at fp16 bits 9..11 give value * 2^-14 for every
+    # code, subnormal 0.5 included (the magnitude grid of E2M1)
+    for m in range(8):
+        bits = np.array([m << 9], dtype=np.uint16)
+        assert bits.view(np.float16)[0].astype(np.float64) == E2M1[m] * 2.0 ** -14
+
+
+def test_k45_integer_products_are_exact_in_fp16():
+    q = np.arange(32, dtype=np.float64)[:, None]
+    sc = np.arange(64, dtype=np.float64)[None, :]
+    assert (q * sc).max() == 1953
+    assert exact_in_fp16(q * sc)
+    assert exact_in_fp16(-1024.0 * sc) and exact_in_fp16(sc / 16.0) and exact_in_fp16(-64.0 * sc)
+    # 1024 + q and 1024 + 16 q (+ 256 for the fifth bit) are exact too
+    assert exact_in_fp16(1024.0 + np.arange(32)) and exact_in_fp16(1024.0 + 16.0 * np.arange(16) + 256.0)
+
+
+def test_q6k_products_exceed_fp16_exact_integers():
+    q = np.arange(64, dtype=np.float64)[:, None] - 32.0
+    sc = np.arange(-128, 128, dtype=np.float64)[None, :]
+    prod = q * sc
+    assert np.abs(prod).max() == 4096
+    assert not exact_in_fp16(prod)
+    # while q - 32 itself, from v = 1024 + q, is exact
+    assert exact_in_fp16((1024.0 + np.arange(64)) - 1056.0)
