@@ -96,7 +96,6 @@ struct ScanSmem {
 // in ascending a.  The ids of a chunk are read eight loads at a time.
 constexpr int kScanBatch = 8;
 
-template <int NW>
 __device__ __forceinline__ void load_ids(const int32_t *ids, int a0, int a_end, int E, int lane,
                                          int (&eb)[kScanBatch])
 {
@@ -121,7 +120,7 @@ __device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
     const int a_beg = warp * C, a_end = min(A, (warp + 1) * C);
     for (int a0 = a_beg; a0 < a_end; a0 += 32 * kScanBatch) {
         int eb[kScanBatch];
-        load_ids<NW>(ids, a0, a_end, E, lane, eb);
+        load_ids(ids, a0, a_end, E, lane, eb);
 #pragma unroll
         for (int u = 0; u < kScanBatch; ++u) {
             const unsigned same = __match_any_sync(0xffffffffu, eb[u]);
@@ -184,7 +183,7 @@ __device__ void scan_body(ScanSmem<NW> &sm, const int32_t *ids, int A, int E,
     __syncthreads();
     for (int a0 = a_beg; a0 < a_end; a0 += 32 * kScanBatch) {
         int eb[kScanBatch];
-        load_ids<NW>(ids, a0, a_end, E, lane, eb);
+        load_ids(ids, a0, a_end, E, lane, eb);
 #pragma unroll
         for (int u = 0; u < kScanBatch; ++u) {
             const int e = eb[u];
