@@ -383,10 +383,13 @@ DS4G_API int32_t ds4g_moe_forward_launches(const ds4g_moe_desc *desc, int32_t T)
 /*
  * ds4g_moe_device_status -- no counterpart on the pages (failure detection
  * of this library).  The device status word of the last
- * ds4g_moe_forward on this workspace: DS4G_OK, or DS4G_ERR_TIMEOUT when a
- * bounded wait inside a kernel expired (the kernel then returned early and y
- * is not valid).  Synchronizes `stream`.  Errors: DS4G_ERR_INVALID,
- * DS4G_ERR_WORKSPACE, DS4G_ERR_CUDA.
+ * ds4g_moe_forward on this workspace (the first problem a kernel recorded):
+ * DS4G_OK; DS4G_ERR_TIMEOUT when a bounded wait inside a kernel expired (the
+ * kernel then returned early and y is not valid); DS4G_ERR_INVALID when a
+ * routed expert's slot map entry was out of range (y not valid);
+ * DS4G_ERR_RANGE when an MXFP4 block scale beyond fp16 was rounded on the
+ * tensor-core kernels (y computed, those weights inexact).  Synchronizes
+ * `stream`.  Errors: DS4G_ERR_INVALID, DS4G_ERR_WORKSPACE, DS4G_ERR_CUDA.
  */
 DS4G_API ds4g_status ds4g_moe_device_status(const ds4g_moe_desc *desc, int32_t T,
                                             const void *workspace, size_t ws_bytes,
