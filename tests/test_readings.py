@@ -58,3 +58,59 @@ def test_q6k_products_exceed_fp16_exact_integers():
     assert not exact_in_fp16(prod)
     # while q - 32 itself, from v = 1024 + q, is exact
     assert exact_in_fp16((1024.0 + np.arange(64)) - 1056.0)
+
+
+# ---------------------------------------------------------------------------
+# Why the MXFP4 layers keep fp16 activations: the block-scaled tensor-core
+# MMAs multiply MX-quantized activations (FP8 E4M3 or FP4 E2M1 elements, one
+# power-of-two scale per 32 along K, scale exponent floor(log2 amax) minus
+# the element format's largest exponent, per the OCP microscaling layout).
+# Quantizing x that way alone, with everything else computed by the oracle,
+# already costs far more than the 1e-3 per-token tolerance.
+# ---------------------------------------------------------------------------
+
+def _round_to_grid(v, mant_bits, emin, vmax):
+    """Round-to-nearest-even onto a minifloat grid with `mant_bits` mantissa
+    bits, smallest normal exponent `emin` (subnormals below) and largest
+    finite value `vmax` (saturating)."""
+    a = np.abs(v)
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, emin)
+    quantum = 2.0 ** (e - mant_bits)
+    q = np.round(a / quantum) * quantum
+    return np.sign(v) * np.minimum(q, vmax)
+
+
+def _mx_quantize(x, mant_bits, emin, emax, vmax):
+    """x [T x H] -> MX values: per 32 consecutive elements along H a scale
+    2^(floor(log2 amax) - emax), elements rounded onto the element grid."""
+    T, H = x.shape
+    b = x.reshape(T, H // 32, 32)
+    amax = np.abs(b).max(axis=2, keepdims=True)
+    sexp = np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - emax
+    scale = 2.0 ** sexp
+    return (_round_to_grid(b / scale, mant_bits, emin, vmax) * scale).reshape(T, H)
+
+
+def _per_token_rel_l2(y, ref):
+    return np.linalg.norm(y - ref, axis=1) / np.linalg.norm(ref, axis=1)
+
+
+def test_mx_quantized_activations_break_the_tolerance(orc):
+    import ds4g_synth as S
+    import oracle_pins as P
+    layer = P.small_layer(seed=91, H=1024, I=512, E=8, k=2, T=16, fmt=S.FMT_MXFP4,
+                          score=S.SCORE_SIGMOID)
+    x = S.bf16_to_f32(layer["x"]).astype(np.float64)
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    errs = {}
+    for name, (mant, emin, emax, vmax) in {"e4m3": (3, -6, 8, 448.0),
+                                           "e2m1": (1, 0, 2, 6.0)}.items():
+        xq = _mx_quantize(x, mant, emin, emax, vmax)
+        # every MX value (at most 4 significant bits) is exact in bf16
+        xb = S.f32_to_bf16(xq.astype(np.float32))
+        assert np.array_equal(S.bf16_to_f32(xb).astype(np.float64), xq)
+        y, _, _ = orc.moe_forward(layer, xb, layer["logits"])
+        errs[name] = _per_token_rel_l2(y, yref).max()
+    assert errs["e4m3"] > 5e-3, errs            # FP8 activations: several times the 1e-3 bar
+    assert errs["e2m1"] > 5e-2, errs            # FP4 activations: far beyond it
