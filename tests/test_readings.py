@@ -114,3 +114,26 @@ def test_mx_quantized_activations_break_the_tolerance(orc):
         errs[name] = _per_token_rel_l2(y, yref).max()
     assert errs["e4m3"] > 5e-3, errs            # FP8 activations: several times the 1e-3 bar
     assert errs["e2m1"] > 5e-2, errs            # FP4 activations: far beyond it
+
+
+def test_fp8_activation_terms_needed_for_the_tolerance(orc):
+    """Splitting x into MX-FP8 terms, each quantizing the previous residual:
+    two terms still leave more than 1e-3, three reproduce the bf16
+    activations exactly (8 significant bits within three 4-bit terms), so a
+    native FP8-activation MMA would need three MMAs per K step."""
+    import ds4g_synth as S
+    import oracle_pins as P
+    layer = P.small_layer(seed=91, H=1024, I=512, E=8, k=2, T=16, fmt=S.FMT_MXFP4,
+                          score=S.SCORE_SIGMOID)
+    x = S.bf16_to_f32(layer["x"]).astype(np.float64)
+    yref, _, _ = orc.moe_forward(layer, layer["x"], layer["logits"])
+    q = lambda v: _mx_quantize(v, 3, -6, 8, 448.0)
+    t1 = q(x)
+    t2 = q(x - t1)
+    t3 = q(x - t1 - t2)
+    errs = []
+    for xs in (t1 + t2, t1 + t2 + t3):
+        y, _, _ = orc.moe_forward(layer, S.f32_to_bf16(xs.astype(np.float32)), layer["logits"])
+        errs.append(_per_token_rel_l2(y, yref).max())
+    assert errs[0] > 1e-3, errs
+    assert np.array_equal(t1 + t2 + t3, x) and errs[1] == 0.0, errs
