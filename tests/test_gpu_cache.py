@@ -94,7 +94,9 @@ def _budget_logits(rng, T, E, n_slots):
     (dict(H=512, I=256, E=12, k=3, T=40, align=16), D.FORCE_TC),            # tensor-core kernels
     (dict(H=512, I=320, E=10, k=2, T=9, fmt=S.FMT_Q4K, down_fmt=S.FMT_Q6K), 0),   # general
     (dict(H=512, I=256, E=10, k=2, T=7, fmt=S.FMT_CB2, align=16), 0),       # codebook
-], ids=["decode", "tensor_core", "kquant", "codebook"])
+    (dict(H=512, I=2048, E=10, k=2, T=9, fmt=S.FMT_Q4K, down_fmt=S.FMT_Q6K), 0),  # K-quant, tensor core
+    (dict(H=512, I=512, E=10, k=2, T=9, fmt=S.FMT_MXFP4), 0),              # MXFP4, tensor core
+], ids=["decode", "tensor_core", "kquant", "codebook", "kquant_tc", "mxfp4_tc"])
 def test_cache_matches_device_forward(orc, kw, flags):
     layer = P.small_layer(seed=61 + kw["T"], **kw)
     E, k, T = layer["n_experts"], layer["top_k"], layer["x"].shape[0]
