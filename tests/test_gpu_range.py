@@ -40,7 +40,10 @@ def ranged_x(T: int, H: int, seed: int) -> np.ndarray:
     (dict(H=1024, I=512, E=8, k=2, T=40, align=16), D.FORCE_TC),           # tensor-core kernels
     (dict(H=512, I=256, E=5, k=2, T=9, fmt=S.FMT_CB2, align=16), 0),       # codebook, tensor core
     (dict(H=512, I=200, E=7, k=3, T=17, fmt=S.FMT_CB2, align=2), 0),       # general kernels
-], ids=["decode_mma_sync", "decode_mma_sync_xp", "decode_tcgen05", "tensor_core", "codebook_tc", "general"])
+    (dict(H=1024, I=512, E=8, k=2, T=12, fmt=S.FMT_Q5K, down_fmt=S.FMT_Q4K), 0),   # K-quant, tensor core
+    (dict(H=1024, I=512, E=8, k=2, T=12, fmt=S.FMT_MXFP4), 0),            # MXFP4, tensor core
+], ids=["decode_mma_sync", "decode_mma_sync_xp", "decode_tcgen05", "tensor_core", "codebook_tc", "general",
+        "kquant_tc", "mxfp4_tc"])
 def test_large_and_small_activations(orc, kw, flags):
     layer = P.small_layer(seed=41 + kw["T"], **kw)
     T, H = layer["x"].shape
